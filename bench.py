@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Throughput of the sharded mixed-precision AdamW step on GB300.
+
+One step = one pass of the whole hot path over one step's synthetic gradients: for every
+reduce-scatter bucket (stages 1/2) or FSDP unit (stage 3: all-gather of the unit first) the
+fused reduce + unscale + inf/nan flag + AdamW + 16-bit cast kernel, then the commit/skip
+decision.  Default workload: ZeRO-2 over a ragged 10,000-tensor model, N_d = 7 emulated ranks.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO step params updated/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "params/s"
+DEFAULT_CONFIG = 1
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-elems", type=int, default=4_194_304)
+    ap.add_argument("--mem-budget-gb", type=float, default=160.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Bench:
+    """A workload bound to the product API with pre-generated contribution sets."""
+
+    def __init__(self, w, mem_budget_gb: float, n_sets_wanted: int):
+        import torch
+        import synth
+        from zero_sharded_mixed_03_gb300.emulate import EmulatedGroup
+        import zero_sharded_mixed_03_gb300 as Z
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        import gpu_harness as H
+
+        self.torch, self.Z, self.H, self.synth = torch, Z, H, synth
+        self.w = w
+        self.run = H.Run(w)            # plan, state, 16-bit buffers, initial parameters
+        self.g = self.run.g
+        self.units = self.run.units
+        self.info = self.run.info
+        self.bound = self.run.bound
+        self.all_bound = len(self.bound) == w.n_d
+        self.calls = self.run.ranges()
+        # Contribution layout of one step: for each call the slices the bound ranks read.
+        # All ranks bound: the call's whole range.  Otherwise: each bound rank's shard slice.
+        self.read_spans = []          # per call: list of (flat lo, flat hi, compact offset)
+        off = 0
+        for which, lo, hi in self.calls:
+            spans = []
+            if self.all_bound:
+                spans.append((lo, hi, off, 0))
+                off += hi - lo
+            else:
+                for r in sorted(self.bound):
+                    if w.stage == 3:
+                        U = self.units[which]
+                        a, e = U[5] + r * U[4], U[5] + (r + 1) * U[4]
+                    else:
+                        S = self.units[0][4]
+                        a, e = max(lo, r * S), min(hi, (r + 1) * S)
+                    if a < e:
+                        spans.append((a, e, off, a - lo))
+                        off += e - a
+                # one base pointer per contribution: a compact layout serves one bound rank
+                assert len(spans) <= 1, "compact contributions need a single bound rank"
+            self.read_spans.append(spans)
+        self.set_elems = off
+        set_bytes = off * 2 * w.n_d
+        self.n_sets = int(max(1, min(n_sets_wanted, (mem_budget_gb * 1e9) // max(1, set_bytes))))
+        self.sets = []
+        for s in range(self.n_sets):
+            bufs = [torch.empty(max(8, off), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+            for r in range(w.n_d):
+                st = synth.grad_stream(w, s + 1, r)
+                for spans in self.read_spans:
+                    for (a, e, o, _rel) in spans:
+                        H.fill_device(bufs[r][o:o + (e - a)], st, self.units, a, e)
+            self.sets.append(bufs)
+        torch.cuda.synchronize()
+        self.elems_per_step = int(self.info.shard) * len(self.bound)
+        self.bytes_per_elem = 2 * w.n_d + 26
+        self.hyper = self.run.hyper
+        self.scaler = self.run.scaler
+
+    def call_ptrs(self, bufs, ci):
+        """Per-rank contribution pointers of call ci: base such that base + c_off hits the slice."""
+        spans = self.read_spans[ci]
+        if not spans:
+            return [bufs[r].data_ptr() for r in range(self.w.n_d)]
+        a, e, o, rel = spans[0]
+        # compact slice o holds flat [a, e), which the kernel addresses as call offset `rel`
+        return [bufs[r].data_ptr() + 2 * (o - rel) for r in range(self.w.n_d)]
+
+    def step(self, bufs, events=None, gather_events=None):
+        launches = 0
+        for ci, (which, lo, hi) in enumerate(self.calls):
+            if self.w.stage == 3:
+                if gather_events is not None:
+                    gather_events[0].append(self._event())
+                self.g.gather(which, self.run.gather_buf)
+                if gather_events is not None:
+                    gather_events[1].append(self._event())
+                self.g.release(which)
+                launches += 1
+            if events is not None:
+                events[0].append(self._event())
+            self.g.step(self.call_ptrs(bufs, ci), which, self.hyper, self.scaler)
+            if events is not None:
+                events[1].append(self._event())
+            launches += 1
+        res = self.g.finish(self.scaler)
+        if res.skipped:
+            launches += 1
+        return res, launches
+
+    def _event(self):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+
+def gpu_arm(args, world, rank, local):
+    import torch
+    from synth import workloads as W
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = W.workload(args.config)
+    b = Bench(w, args.mem_budget_gb, args.warmup + args.steps)
+    peak, peak_kind = peaks()
+
+    for k in range(args.warmup):
+        b.step(b.sets[k % b.n_sets])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev_fused = ([], [])
+    ev_gather = ([], [])
+    launches = 0
+    skipped = 0
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(args.steps):
+        res, n = b.step(b.sets[(args.warmup + k) % b.n_sets], ev_fused, ev_gather)
+        launches += n
+        skipped += res.skipped
+    t1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    fused_ms = [a.elapsed_time(c) for a, c in zip(*ev_fused)]
+    gather_ms = [a.elapsed_time(c) for a, c in zip(*ev_gather)]
+
+    applied = args.steps - skipped
+    elems = b.elems_per_step
+    value = world * elems * applied / (ms / 1e3)
+    step_bytes = elems * b.bytes_per_elem
+    gather_bytes = 4 * int(b.info.phi_pad) if w.stage == 3 else 0
+    hbm_gbs = (step_bytes + gather_bytes) * args.steps / (ms / 1e3) / 1e9
+    # dominant kernel: the fused step; algorithmic bytes per launch = elements x (2 N_d + 26)
+    per_launch_elems = elems / max(1, len(b.calls))
+    launch_bytes = per_launch_elems * b.bytes_per_elem
+    avg_fused_s = statistics.mean(fused_ms) / 1e3 if fused_ms else float("nan")
+    achieved = launch_bytes / avg_fused_s / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": peak_kind, "kernel": "fused_step_kernel",
+                "launch_bytes": int(launch_bytes), "avg_launch_us": round(avg_fused_s * 1e6, 2),
+                "launches_timed": len(fused_ms)}
+    if gather_ms:
+        g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
+        roofline["gather_achieved_gbs"] = round(g_bytes / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
+
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype":
+           "fp16" if w.dtype == W.FP16 else "bf16", "data": "synthetic",
+           "config": {"workload": w.name, "config_index": args.config, "n_d": w.n_d,
+                      "stage": w.stage, "phi": w.phi, "bucket_elems": w.bucket_elems,
+                      "units": len(b.units), "bound_ranks": len(b.bound),
+                      "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
+                      "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
+                      "contribution_sets": b.n_sets},
+           "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
+           "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,
+           "clocks": clk}
+
+    if not args.no_e2e:
+        out["e2e"] = e2e_leg(b, min(args.steps, 10), world, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_elems)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def e2e_leg(b: Bench, steps: int, world: int, dist):
+    """Same metric through the public API with the gradients in pinned host memory: every step
+    copies its contributions host->device, runs the step, and reads the step result back."""
+    torch = b.torch
+    host = [torch.empty(b.set_elems, dtype=torch.int16, pin_memory=True) for _ in range(b.w.n_d)]
+    for r in range(b.w.n_d):
+        host[r].copy_(b.sets[0][r][:b.set_elems])
+    dev = b.sets[0]
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t = time.perf_counter()
+    applied = 0
+    for k in range(steps):
+        for r in range(b.w.n_d):
+            dev[r][:b.set_elems].copy_(host[r], non_blocking=True)
+        res, _ = b.step(dev)          # finish() reads the step result (flag) back to the host
+        applied += 1 - res.skipped
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t
+    if dist:
+        tt = torch.tensor([el], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el = float(tt.item())
+    return {"value": world * b.elems_per_step * applied / el, "unit": UNIT,
+            "h2d_bytes_per_step": 2 * b.set_elems * b.w.n_d, "d2h_bytes_per_step": 4,
+            "steps": steps}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_run(w, sample_elems: int, steps: int, warmup: int = 0):
+    """Time the CPU oracle (single thread) on the first `sample_elems` flat elements."""
+    import numpy as np
+    import oracle
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import gpu_harness as H
+    L = oracle.Layout(w.sizes, w.n_d, w.unit_first or None)
+    units = [tuple(int(x) for x in u) for u in L.units]
+    n = min(sample_elems, L.total_pad)
+    p = oracle.widen16(H.fill_host(synth.param_stream(w), units, 0, n), w.dtype).astype(np.float32)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    out16 = np.zeros(n, np.uint16)
+    sc = oracle.ScalerState(w.scaler)
+    times = []
+    for k in range(1, warmup + steps + 1):
+        c = [H.fill_host(synth.grad_stream(w, k, r), units, 0, n) for r in range(w.n_d)]
+        t = time.perf_counter()
+        k9 = oracle.consts(w.hyper, sc.t + 1, sc.scale, w.n_d)
+        g, flag = oracle.reduce(c, w.dtype, float(k9[8]))
+        if flag:
+            oracle.recast(p, w.dtype, out16)
+        else:
+            oracle.adamw(g, p, m, v, k9, w.dtype, out16)
+        sc.update(flag)
+        if k > warmup:
+            times.append(time.perf_counter() - t)
+    return n, times
+
+
+def cpu_baseline(w, sample_elems: int):
+    n, times = oracle_sample_run(w, sample_elems, 2)
+    return {"value": n * len(times) / sum(times), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {n} flat elements of {w.name}, {len(times)} steps, single-threaded "
+                      f"oracle (reduce over {w.n_d} ranks + AdamW + cast), input generation excluded",
+            "host_cpus": os.cpu_count()}
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    from synth import workloads as W
+    w = W.workload(args.config)
+    n, times = oracle_sample_run(w, args.cpu_sample_elems, max(1, args.steps), args.warmup)
+    total = sum(times)
+    value = n * len(times) / total
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic",
+           "config": {"workload": w.name, "config_index": args.config, "n_d": w.n_d,
+                      "stage": w.stage, "phi": w.phi, "sample_elems": n},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": f"first {n} flat elements per step, single-threaded"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+    gpu_arm(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,227 @@
+/*
+ * zero.h -- C ABI of the GB300 (sm_103a) sharded mixed-precision AdamW step.
+ *
+ * The data-parallel hot path of ZeRO as described on the page "Zero Redundancy
+ * Optimizer (ZeRO) and Fully Sharded Data Parallelism (FSDP): Mathematical
+ * Foundations of Memory Partitioning, Communication Complexity, and Overlapped
+ * Execution" (llms.blog), sections "ZeRO-Stage 1/2/3", "Execution Flow for
+ * ZeRO-1", "ZeRO-3 / FSDP Layer Execution Lifecycle" and "FSDP-1: FlatParameter
+ * and Module-Level Wrapping".
+ *
+ * The N_d data-parallel ranks are emulated inside one GPU: every rank's 16-bit
+ * gradient contribution is a separate device buffer.  For each shard a bound
+ * rank owns, one fused kernel
+ *   (1) reduces the N_d contributions in fp32, r ascending, and multiplies by
+ *       inv = fp32(1 / (N_d * loss_scale))   [the reduce-scatter's reduction],
+ *   (2) ORs a global non-finite flag           [dynamic loss-scale skip],
+ *   (3) applies AdamW to the fp32 master/m/v of the shard,
+ *   (4) casts the new weight to bf16/fp16 into the all-gather destination.
+ *
+ * Conventions
+ *  - Every call returns a zero_status_t; no exception or abort crosses the ABI.
+ *    On an error, zero_last_error() (thread-local) describes it.
+ *  - The plan owns host tables and a few scalars only.  ALL device memory
+ *    (state, contributions, 16-bit buffers, workspace) is owned by the caller
+ *    and is never freed by the library.  The library allocates no device memory.
+ *  - Calls that take a `stream` (a cudaStream_t passed as void*) are
+ *    asynchronous on it, except zero_step_finish, which synchronises it.
+ *  - Device pointers must be aligned to their element size (2 B for 16-bit
+ *    data, 4 B for fp32, 8 B for the workspace); otherwise ZERO_EALIGN.  The
+ *    128-bit vector path is used when every base pointer is 16-byte aligned and
+ *    every stream of a launch has the same element phase modulo 8 (always true
+ *    for the state layout below when bucket_elems is a multiple of 8); other
+ *    launches use the scalar path of the same kernel.
+ *  - Kernels never trap or assert; they contain no waits.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = 1,  /* invalid argument (null pointer, bad stage, size, rank ...) */
+    ZERO_EALIGN = 2,  /* a pointer is not aligned to its element size */
+    ZERO_ECUDA = 3,   /* a CUDA runtime call failed */
+    ZERO_ESTATE = 4,  /* call out of order (e.g. finish before every bucket was stepped) */
+    ZERO_ERANGE = 5   /* a size beyond a documented limit */
+} zero_status_t;
+
+enum { ZERO_BF16 = 0, ZERO_FP16 = 1 };
+
+/* Largest supported N_d (contribution pointers travel in the kernel parameters). */
+#define ZERO_MAX_RANKS 128
+
+typedef struct zero_plan zero_plan_t;
+
+/* AdamW hyperparameters (decoupled weight decay, bias-corrected moments). */
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+} zero_hyper_t;
+
+/* Dynamic loss scale.  On a step whose reduced gradient holds inf/nan the step
+ * is skipped and scale = max(scale * backoff_factor, min_scale); after
+ * growth_interval consecutive applied steps scale *= growth_factor. */
+typedef struct {
+    double scale;
+    double growth_factor;
+    double backoff_factor;
+    double min_scale;
+    int64_t growth_interval;
+    int64_t good_steps;      /* applied steps since the last change of scale */
+} zero_scaler_t;
+
+typedef struct {
+    int64_t n_tensors;
+    int64_t n_units;         /* FSDP units (stage 3); 1 for stages 1/2 */
+    int64_t n_buckets;       /* reduce-scatter buckets (stages 1/2); n_units for stage 3 */
+    int64_t phi;             /* sum of tensor sizes */
+    int64_t phi_pad;         /* sum of padded unit sizes = length of the global flat index space */
+    int64_t shard;           /* elements each rank owns: sum over units of phi_pad_u / N_d */
+    int64_t max_contrib_elems; /* elements every contribution buffer must hold for the largest
+                                  bucket (stages 1/2) or unit (stage 3) */
+    int64_t max_unit_pad;    /* largest padded unit (stage 3 gather destination length) */
+    int64_t workspace_bytes; /* device workspace the caller provides (zero_bind) */
+    int32_t n_d;
+    int32_t stage;
+    int32_t dtype16;
+    int32_t reserved;
+} zero_plan_info_t;
+
+/* Table selectors for zero_plan_tables (all entries int64, row-major). */
+enum {
+    ZERO_TABLE_TENSOR_OFFSET = 0,  /* 1 col: global flat offset of each tensor */
+    ZERO_TABLE_UNITS = 1,          /* 7 cols: first tensor, tensor count, numel, numel_pad,
+                                      shard size S_u, global base, rank-local shard base */
+    ZERO_TABLE_SHARD_SEGMENTS = 2, /* 6 cols: rank, unit, tensor (-1 = padding), offset in the
+                                      tensor (or the padding), rank-local shard offset, length;
+                                      ordered by rank, unit, flat position */
+    ZERO_TABLE_BUCKET_SEGMENTS = 3,/* 5 cols: bucket, rank, flat start, rank-local shard offset,
+                                      length; ordered by bucket, rank (stages 1/2) */
+    ZERO_TABLE_STATE_LAYOUT = 4    /* 4 cols: rank, unit, element offset of the unit's shard in the
+                                      rank's state buffers, length (physical layout, see zero_bind) */
+};
+
+typedef struct {
+    int32_t skipped;         /* 1: a non-finite gradient was seen, the step was not applied */
+    int32_t reserved;
+    int64_t t;               /* applied steps so far (after this step) */
+    double scale;            /* loss scale to use for the next step */
+} zero_step_result_t;
+
+/* Per-rank bytes.  logical[s][c]: stage s in (DDP, ZeRO-1, ZeRO-2, ZeRO-3), component c in
+ * (16-bit params, 16-bit grads, fp32 optimizer state) at phi_pad -- the closed forms of
+ * section "Static Memory Allocation" and the stage equations M(ZeRO-1/2/3). */
+typedef struct {
+    int64_t logical[4][3];
+    int64_t logical_total[4];
+    int64_t logical_ddp_fp32_grads;  /* the 18-Phi variant with fp32 gradient buffers */
+    int64_t physical_state_bytes;    /* per bound rank: master/m/v, both ping-pong copies */
+    int64_t physical_param16_bytes;  /* stages 1/2: flat buffer; stage 3: one rank's shard */
+    int64_t physical_contrib_bytes;  /* N_d contribution buffers of the largest bucket/unit */
+    int64_t physical_gather_bytes;   /* stage 3: largest full-unit buffer */
+    int64_t workspace_bytes;
+} zero_mem_report_t;
+
+/* Elements sent (= received) per rank per step, sections "Standard Ring-AllReduce
+ * Communication Analysis", "ZeRO-1 and ZeRO-2 Communication Volume", "ZeRO-3 and FSDP
+ * Communication Volume".  One ring collective over phi_pad moves (N_d-1)/N_d * phi_pad. */
+typedef struct {
+    int64_t per_collective;   /* (N_d - 1) * shard */
+    int64_t ddp;              /* all-reduce = scatter-reduce + all-gather */
+    int64_t zero1;            /* reduce-scatter + all-gather */
+    int64_t zero2;
+    int64_t zero3;            /* forward all-gather + backward all-gather + reduce-scatter */
+    int64_t this_stage;       /* the entry for the plan's stage */
+    int64_t bytes_per_elem;   /* 2 (16-bit) */
+    int64_t collectives_per_step; /* reduce-scatters + all-gathers issued per step by this plan */
+} zero_comm_report_t;
+
+/* Build the flat-buffer partition ("FSDP-1: FlatParameter": tensors flattened in the given
+ * order, each unit padded at its tail to a multiple of N_d and sliced into N_d equal shards).
+ *   tensor_sizes[n_tensors]  element counts (>= 0)
+ *   stage                    1, 2 or 3
+ *   bucket_elems             stages 1/2: reduce-scatter bucket size in elements (0 = one
+ *                            bucket); stage 3: must be 0
+ *   unit_first[n_units]      stage 3: first tensor of each unit, strictly increasing, starting
+ *                            at 0 (NULL / 0 = one unit); stages 1/2: must be NULL / 0
+ *   dtype16                  ZERO_BF16 or ZERO_FP16
+ * On success *out owns host memory only; release it with zero_plan_destroy. */
+zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, int n_d, int stage,
+                               int64_t bucket_elems, const int64_t* unit_first, int64_t n_units,
+                               int dtype16, zero_plan_t** out);
+
+zero_status_t zero_plan_info(const zero_plan_t* plan, zero_plan_info_t* out);
+
+/* Element count of rank `rank`'s state buffers (master, m, v; and stage 3's 16-bit shard).
+ * The layout places each unit's shard at an offset congruent, modulo 8, to the unit-local
+ * start of that shard, so the fp32 state, the 16-bit contributions and the 16-bit output
+ * share one 128-bit vector phase.  Unused gap elements are never read or written. */
+zero_status_t zero_rank_state_elems(const zero_plan_t* plan, int rank, int64_t* elems);
+
+/* Copy table `which` into dst (capacity `cap` int64 values).  *n_rows receives the row
+ * count; if the table does not fit, nothing is written and ZERO_ERANGE is returned. */
+zero_status_t zero_plan_tables(const zero_plan_t* plan, int which, int64_t* dst, int64_t cap,
+                               int64_t* n_rows);
+
+/* Bind rank `rank`'s device buffers (caller-owned, each of zero_rank_state_elems elements):
+ *   master[2], m[2], v[2]  fp32 ping-pong pairs; index 0 holds the current state at bind time
+ *   shard16                stage 3: the rank's 16-bit parameter shard; else NULL
+ *   full16                 stages 1/2: the flat 16-bit parameter buffer (phi_pad elements),
+ *                          shared by every rank (all replicas are identical); else NULL
+ *   workspace              device memory of info.workspace_bytes (the non-finite flag);
+ *                          plan-wide: every bind must pass the same pointer
+ * Synchronously clears the workspace.  Only bound ranks are updated by zero_step. */
+zero_status_t zero_bind(zero_plan_t* plan, int rank, float* const master[2], float* const m[2],
+                        float* const v[2], void* shard16, void* full16, void* workspace);
+
+/* Stage 3: register the 16-bit shard of a rank whose optimizer runs elsewhere, so that
+ * zero_gather_layer can reconstruct full units.  The buffer follows that rank's layout. */
+zero_status_t zero_bind_peer(zero_plan_t* plan, int rank, const void* shard16);
+
+/* One fused reduce + AdamW + cast over every bound rank's part of bucket / unit `which`.
+ *   grad_contribs[n_contribs]  n_contribs == N_d device pointers; contribution r holds rank r's
+ *                              16-bit gradient for the whole range of the bucket (stages 1/2:
+ *                              [b*B, min((b+1)*B, phi_pad)); which = -1: all of [0, phi_pad))
+ *                              or of the unit (stage 3: phi_pad_u elements, padding zero)
+ *   hyper                      AdamW hyperparameters (identical for every call of one step)
+ *   scaler                     loss scale to unscale with (NULL: 1); read, not modified
+ * A step is the sequence of calls that covers every bucket (or unit) exactly once, ended by
+ * zero_step_finish.  New state is written to the non-current half of each ping-pong pair. */
+zero_status_t zero_step(zero_plan_t* plan, const void* const* grad_contribs, int64_t n_contribs,
+                        int64_t which, const zero_hyper_t* hyper, const zero_scaler_t* scaler,
+                        void* stream);
+
+/* End the step: read the non-finite flag (synchronises `stream`).  Flag clear: the new state
+ * becomes current, t += 1.  Flag set: the state is left unchanged and the 16-bit parameters are
+ * re-cast from the unchanged master (one extra kernel).  Updates *scaler (if not NULL), clears
+ * the flag, and fills *out (may be NULL). */
+zero_status_t zero_step_finish(zero_plan_t* plan, zero_scaler_t* scaler, void* stream,
+                               zero_step_result_t* out);
+
+/* Stage 3 all-gather of unit `unit` ("ZeRO-3 / FSDP Layer Execution Lifecycle"): copies the
+ * N_d 16-bit shards (bound or peer ranks) into full_unit16 (phi_pad_u elements, padding
+ * included).  The unit stays "gathered" until zero_release_layer. */
+zero_status_t zero_gather_layer(zero_plan_t* plan, int64_t unit, void* full_unit16, void* stream);
+
+/* Mark unit `unit`'s gathered buffer free; the caller may reuse its memory. */
+zero_status_t zero_release_layer(zero_plan_t* plan, int64_t unit);
+
+zero_status_t zero_memory_report(const zero_plan_t* plan, zero_mem_report_t* out);
+zero_status_t zero_comm_report(const zero_plan_t* plan, zero_comm_report_t* out);
+
+/* Applied steps so far and the index (0/1) of the current half of each ping-pong pair. */
+zero_status_t zero_state_cursor(const zero_plan_t* plan, int64_t* t, int* current);
+
+const char* zero_last_error(void);
+void zero_plan_destroy(zero_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_H */

@@ -59,6 +59,10 @@ def lib():
         L.orc_sharded_step.restype = ctypes.c_int
         L.orc_sharded_step.argtypes = [vp, i64, vp, i64, ctypes.c_int, ctypes.c_int, i64,
                                        ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_scaler_update.restype = i64
+        L.orc_scaler_update.argtypes = [ctypes.c_int, i64, ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(i64), ctypes.c_double, ctypes.c_double, i64,
+                                        ctypes.c_double]
         L.orc_ddp_step.restype = ctypes.c_int
         L.orc_ddp_step.argtypes = [i64, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp, vp, vp]
         L.orc_gather_unit.restype = ctypes.c_int
@@ -181,6 +185,27 @@ def sharded_step(layout: Layout, stage: int, bucket_elems: int, is_fp16: int, co
         _p(layout.sizes), layout.sizes.size, _p(layout.unit_first), layout.n_units_arg, n_d,
         stage, bucket_elems, is_fp16, _ptrs(contribs), _p(bound), _ptrs(p), _ptrs(m), _ptrs(v),
         _ptrs(shard16 if shard16 is not None else [None] * n_d), _p(full16), _p(k9))
+
+
+class ScalerState:
+    """Oracle-side loss-scale trajectory (scale, clean-step counter, applied steps t)."""
+
+    def __init__(self, scaler_cfg, t: int = 0):
+        self.cfg = scaler_cfg
+        self.scale = scaler_cfg.init_scale if scaler_cfg is not None else 1.0
+        self.good = 0
+        self.t = t
+
+    def update(self, flag: int) -> None:
+        if self.cfg is None:
+            self.t = self.t if flag else self.t + 1
+            return
+        sc = ctypes.c_double(self.scale)
+        gd = ctypes.c_int64(self.good)
+        self.t = int(lib().orc_scaler_update(int(flag), self.t, ctypes.byref(sc), ctypes.byref(gd),
+                                             self.cfg.growth_factor, self.cfg.backoff_factor,
+                                             self.cfg.growth_interval, self.cfg.min_scale))
+        self.scale, self.good = sc.value, gd.value
 
 
 def ddp_step(contribs, is_fp16, p, m, v, out16, k9) -> int:

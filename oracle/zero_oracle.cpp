@@ -479,6 +479,27 @@ int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* uni
     return flag;
 }
 
+// ---- A8 commit/skip of the dynamic loss scale (R5): on a flagged step the
+// scale backs off (not below min_scale) and the clean-step counter restarts;
+// after `interval` consecutive applied steps the scale grows.  Returns the
+// number of applied steps after this one (t unchanged on a skip). ----
+int64_t orc_scaler_update(int flag, int64_t t, double* scale, int64_t* good, double growth,
+                          double backoff, int64_t interval, double min_scale)
+{
+    if (flag) {
+        double s = *scale * backoff;
+        *scale = (s < min_scale) ? min_scale : s;
+        *good = 0;
+        return t;
+    }
+    *good += 1;
+    if (interval > 0 && *good >= interval) {
+        *scale = *scale * growth;
+        *good = 0;
+    }
+    return t + 1;
+}
+
 // ---- Unsharded data parallelism, brute force: all-reduce (sum over ranks,
 // r ascending, times inv) of the full buffers, then one AdamW over all n
 // elements.  Returns the non-finite flag. ----

@@ -1,0 +1,283 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs.
+
+Tolerances (fp32 master/m/v): |gpu - oracle| <= 1e-6 |oracle| + 1e-8; 16-bit params: <= 1 ulp;
+tables, skip decisions, step counts and loss scales: exact.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+import synth
+import zero_sharded_mixed_03_gb300 as Z
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    Z.lib()   # the product library must load; no fallback exists
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _mk(wid, sizes, n_d, stage, steps=3, bucket=0, units=(), dtype=W.BF16, scaler=None,
+        outliers=False, inject=None, bound=None):
+    return W.Workload(wid=wid, name=f"case{wid}", sizes=tuple(sizes), n_d=n_d, stage=stage,
+                      bucket_elems=bucket, unit_first=tuple(units), dtype=dtype, steps=steps,
+                      hyper=W.Hyper(), scaler=scaler, outliers=outliers, inject=inject,
+                      bound_ranks=bound)
+
+
+def _ragged(seed, n, hi):
+    rng = np.random.default_rng(seed)
+    return [int(x) for x in rng.integers(1, hi, size=n)]
+
+
+SMALL_CASES = {
+    "z1_nd4_tiles_ragged_tail": _mk(101, [3 * 65536 + 13], 4, 1),
+    "z2_nd7_ragged_tensors": _mk(102, _ragged(1, 60, 5000), 7, 2, steps=4),
+    "z2_nd8_fp16_buckets_inf": _mk(103, _ragged(2, 40, 9000), 8, 2, steps=4, bucket=10_000,
+                                   dtype=W.FP16, scaler=W.Scaler(), outliers=True,
+                                   inject=(2, 3, 77_777)),
+    "z2_nd5_odd_bucket_scalar_path": _mk(104, _ragged(3, 30, 7000), 5, 2, bucket=12_345),
+    "z3_nd16_units": _mk(105, _ragged(4, 24, 6000), 16, 3, units=(0, 5, 11, 17, 23)),
+    "z3_nd3_fp16_peers_skip_first": _mk(106, _ragged(5, 12, 3000), 3, 3, units=(0, 4, 9),
+                                        dtype=W.FP16, scaler=W.Scaler(init_scale=1024.0),
+                                        inject=(1, 2, 1234), bound=(0, 2)),
+    "z1_nd1": _mk(107, [1000, 1], 1, 1),
+    "z2_nd40_many_segments": _mk(108, _ragged(6, 50, 9000), 40, 2, bucket=4096),
+    "z2_nd20_rank_batches": _mk(109, _ragged(7, 20, 20000), 20, 2),
+    "z2_tiny_shard_below_vector": _mk(110, [5], 3, 2),
+    "z3_nd16_fp16": _mk(111, _ragged(8, 16, 12000), 16, 3, units=(0, 3, 8), dtype=W.FP16),
+    "z2_nd8_subset_bound": _mk(112, _ragged(9, 25, 8000), 8, 2, bucket=8000, bound=(1, 6)),
+    "z3_nd16_empty_unit_tensors": _mk(113, [0, 40, 0, 0, 33, 1, 0], 16, 3, units=(0, 2, 4)),
+}
+
+
+def _compare_full(run: H.Run, o: H.OracleFull, label: str):
+    mism = 0
+    for r in run.bound:
+        got = run.read_logical(r)
+        for k, want in (("master", o.p[r]), ("m", o.m[r]), ("v", o.v[r])):
+            mism += H.assert_state_close(got[k], want, f"{label} rank {r} {k}")
+        if run.w.stage == 3:
+            g16 = run.g.logical(r, run.g.shard16[r]).cpu().numpy().view(np.uint16)
+            mism += H.assert_16_close(g16, o.sh16[r], f"{label} rank {r} shard16")
+    if run.w.stage != 3:
+        g16 = run.g.full16.cpu().numpy().view(np.uint16)
+        mism += H.assert_16_close(g16, o.full16, f"{label} full16")
+    return mism
+
+
+def _run_full(w: W.Workload):
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    mism = 0
+    try:
+        for k in range(1, w.steps + 1):
+            expect_g = [o.gathered(u) for u in range(len(o.units))] if w.stage == 3 else None
+
+            def check(u, lo, hi, buf):
+                got = buf[:hi - lo].cpu().numpy().view(np.uint16)
+                assert np.array_equal(got, expect_g[u]), f"gather of unit {u} at step {k}"
+
+            res = run.step(k, check if w.stage == 3 else None)
+            flag = o.step(k)
+            assert res.skipped == flag, f"step {k}"
+            assert res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
+            mism += _compare_full(run, o, f"{w.name} step {k}")
+    finally:
+        run.close()
+    return mism
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_small_case_full_parity(name):
+    _run_full(SMALL_CASES[name])
+
+
+def test_config0_full_parity():
+    w = W.workload(0)
+    mism = _run_full(w)
+    print(f"configs[0]: {mism} bit mismatches (within tolerance)")
+
+
+def _run_sampled(w: W.Workload, bound=None, n_random=20000):
+    run = H.Run(w, bound=bound)
+    try:
+        idx = H.sample_indices(run, n_random)
+        o = H.OracleSampled(w, idx)
+        peer_idx, peer16 = None, None
+        if w.stage == 3:
+            # elements of ranks without local state: the gather must return their initial values
+            allr = H.sample_indices(run, 4000, seed=1, bound_only=False)
+            rank, _ = run.locate(allr)
+            peer_idx = allr[rank < 0]
+            peer16 = H.values_at(synth.param_stream(w), o.units, peer_idx)
+        mism = 0
+        for k in range(1, w.steps + 1):
+            if w.stage == 3:
+                exp_idx = np.concatenate([idx, peer_idx])
+                exp16 = np.concatenate([o.out16, peer16])
+
+            def check(u, lo, hi, buf):
+                sel = (exp_idx >= lo) & (exp_idx < hi)
+                if sel.any():
+                    got = buf[torch.from_numpy(exp_idx[sel] - lo).cuda()].cpu().numpy().view(np.uint16)
+                    assert np.array_equal(got, exp16[sel]), f"gather unit {u} step {k}"
+
+            res = run.step(k, check if w.stage == 3 else None)
+            flag = o.step(k)
+            assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
+            st, g16 = run.read_sampled(idx)
+            for key, want in (("master", o.p), ("m", o.m), ("v", o.v)):
+                mism += H.assert_state_close(st[key], want, f"{w.name} step {k} {key}")
+            mism += H.assert_16_close(g16, o.out16, f"{w.name} step {k} 16-bit")
+        return idx.size, mism
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("i", [1, 2, 3])
+def test_config_sampled_parity(i):
+    n, mism = _run_sampled(W.workload(i))
+    print(f"configs[{i}]: {n} sampled elements, {mism} bit mismatches (within tolerance)")
+
+
+def test_config4_rank0_and_last_rank_sampled():
+    w = W.workload(4)
+    n, mism = _run_sampled(w, bound=(0, w.n_d - 1))
+    print(f"configs[4] ranks 0 and {w.n_d - 1}: {n} sampled elements, {mism} bit mismatches")
+
+
+# ---------------------------------------------------------------------- guards and errors
+
+def test_guard_bands_and_layout_gaps_untouched():
+    """Buffers embedded in larger ones filled with a canary: nothing outside the plan's
+    elements (and nothing in the layout's phase gaps) may change."""
+    sizes = _ragged(11, 30, 5000)
+    n_d, G = 7, 256
+    plan = Z.zero_plan_create(sizes, n_d, 3, 0, [0, 9, 19], Z.ZERO_BF16)
+    try:
+        rows = Z.zero_plan_tables(plan, Z.ZERO_TABLE_STATE_LAYOUT)
+        units = Z.zero_plan_tables(plan, Z.ZERO_TABLE_UNITS)
+        canary_f = np.float32(np.frombuffer(np.uint32(0x7FBADBAD).tobytes(), np.float32)[0])
+        big, views, sh = {}, {}, {}
+        for r in range(n_d):
+            n = Z.zero_rank_state_elems(plan, r)
+            b = torch.full((6, n + 2 * G), 0, dtype=torch.float32, device="cuda")
+            b.view(torch.int32).fill_(0x7FBADBAD)
+            s16 = torch.full((n + 2 * G,), 0x5A5A, dtype=torch.int16, device="cuda")
+            big[r], sh[r] = b, s16
+            for (rr, u, off, cnt) in rows:
+                if rr == r:
+                    b[:, G + off:G + off + cnt] = 0.0
+                    b[0, G + off:G + off + cnt] = 0.01
+                    s16[G + off:G + off + cnt] = 0
+            views[r] = [b[j, G:G + n] for j in range(6)]
+        ws = torch.zeros(64, dtype=torch.int32, device="cuda")
+        for r in range(n_d):
+            v = views[r]
+            Z.zero_bind(plan, r, [v[0].data_ptr(), v[1].data_ptr()], [v[2].data_ptr(), v[3].data_ptr()],
+                        [v[4].data_ptr(), v[5].data_ptr()], sh[r][G:].data_ptr(), None, ws.data_ptr())
+        maxc = Z.zero_plan_info(plan).max_contrib_elems
+        contribs = [torch.full((maxc,), 0x3C00, dtype=torch.int16, device="cuda") for _ in range(n_d)]
+        gbuf = torch.full((maxc + 2 * G,), 0x1234, dtype=torch.int16, device="cuda")
+        for u, U in enumerate(units):
+            Z.zero_gather_layer(plan, u, gbuf[G:].data_ptr())
+            Z.zero_release_layer(plan, u)
+            assert (gbuf[:G] == 0x1234).all() and (gbuf[G + U[3]:] == 0x1234).all()
+            Z.zero_step(plan, [c.data_ptr() for c in contribs], u, Z.hyper(), None)
+        res = Z.zero_step_finish(plan, None)
+        assert res.skipped == 0 and res.t == 1
+        torch.cuda.synchronize()
+        for r in range(n_d):
+            b = big[r].view(torch.int32).cpu().numpy()
+            s16 = sh[r].cpu().numpy()
+            mask = np.ones(b.shape[1], dtype=bool)
+            for (rr, u, off, cnt) in rows:
+                if rr == r:
+                    mask[G + off:G + off + cnt] = False
+            assert (b[:, mask] == 0x7FBADBAD).all(), f"rank {r} state guard/gap overwritten"
+            assert (s16[mask] == 0x5A5A).all(), f"rank {r} shard16 guard/gap overwritten"
+            assert not (b[0, ~mask] == 0x7FBADBAD).any()
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
+def test_misaligned_contributions_take_the_scalar_path():
+    """Contribution views starting one element past a 16-byte boundary: same results."""
+    w = _mk(120, _ragged(12, 20, 4000), 4, 2, steps=2)
+    ref = H.Run(w)
+    alt = H.Run(w)
+    try:
+        for k in (1, 2):
+            ref.step(k)
+            for which, lo, hi in alt.ranges():
+                for r in range(w.n_d):
+                    H.fill_device(alt.contribs[r], synth.grad_stream(w, k, r),
+                                  alt.units, lo, hi)
+                shifted = []
+                for c in alt.contribs:
+                    s = torch.empty(c.numel() + 1, dtype=torch.int16, device="cuda")
+                    s[1:] = c
+                    shifted.append(s)
+                alt.g.step([s[1:].data_ptr() for s in shifted], which, alt.hyper, None)
+                torch.cuda.synchronize()
+            alt.g.finish(None)
+        for r in ref.bound:
+            a, b = ref.read_logical(r), alt.read_logical(r)
+            for key in a:
+                assert np.array_equal(a[key].view(np.uint32), b[key].view(np.uint32))
+        assert torch.equal(ref.g.full16, alt.g.full16)
+    finally:
+        ref.close()
+        alt.close()
+
+
+def test_step_lifecycle_errors():
+    w = _mk(121, [1000, 2000], 2, 2, bucket=1000)
+    run = H.Run(w)
+    try:
+        ptrs = [c.data_ptr() for c in run.contribs]
+        run.g.step(ptrs, 0, run.hyper)
+        with pytest.raises(Z.ZeroError) as e:
+            run.g.step(ptrs, 0, run.hyper)            # bucket twice in one step
+        assert e.value.status == Z.ZERO_ESTATE
+        with pytest.raises(Z.ZeroError) as e:
+            run.g.finish()                              # buckets 1, 2 missing
+        assert e.value.status == Z.ZERO_ESTATE
+        with pytest.raises(Z.ZeroError) as e:
+            run.g.step(ptrs, 1, Z.hyper(lr=2e-3))       # hyperparameters changed mid-step
+        assert e.value.status == Z.ZERO_EINVAL
+        run.g.step(ptrs, 1, run.hyper)
+        run.g.step(ptrs, 2, run.hyper)
+        assert run.g.finish().t == 1
+        with pytest.raises(Z.ZeroError) as e:
+            run.g.step(ptrs, -2, run.hyper)
+        assert e.value.status == Z.ZERO_EINVAL
+    finally:
+        run.close()
+
+
+def test_empty_model_step():
+    plan = Z.zero_plan_create([], 3, 2, 0, None, Z.ZERO_BF16)
+    try:
+        ws = torch.zeros(64, dtype=torch.int32, device="cuda")
+        dummy = torch.zeros(8, dtype=torch.float32, device="cuda")
+        d2 = torch.zeros(8, dtype=torch.float32, device="cuda")
+        f16 = torch.zeros(8, dtype=torch.int16, device="cuda")
+        Z.zero_bind(plan, 0, [dummy.data_ptr(), d2.data_ptr()], [dummy.data_ptr() + 4, d2.data_ptr() + 4],
+                    [dummy.data_ptr() + 8, d2.data_ptr() + 8], None, f16.data_ptr(), ws.data_ptr())
+        Z.zero_step(plan, [f16.data_ptr()] * 3, -1, Z.hyper(), None)
+        res = Z.zero_step_finish(plan, None)
+        assert res.skipped == 0 and res.t == 1
+    finally:
+        Z.zero_plan_destroy(plan)

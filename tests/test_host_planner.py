@@ -1,0 +1,175 @@
+"""Host-side checks of libzero (no GPU): exports, tables vs the oracle, accounting, errors."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import zero_sharded_mixed_03_gb300 as Z
+from synth import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_library_exports_every_declared_symbol():
+    with open(os.path.join(ROOT, "include", "zero.h")) as f:
+        text = f.read()
+    declared = set(re.findall(r"^\s*(?:zero_status_t|const char\*|void)\s+(zero_\w+)\s*\(", text, re.M))
+    assert len(declared) >= 15
+    L = Z.lib()
+    for name in sorted(declared):
+        assert hasattr(L, name), name
+    assert declared <= set(Z.EXPORTED)
+
+
+def _plan_for(sizes, n_d, stage, bucket=0, units=None, dtype=Z.ZERO_BF16):
+    return Z.zero_plan_create(list(sizes), n_d, stage, bucket, list(units) if units else None, dtype)
+
+
+def _compare_tables(sizes, n_d, stage, bucket, units):
+    plan = _plan_for(sizes, n_d, stage, bucket, units)
+    try:
+        L = oracle.Layout(sizes, n_d, units)
+        assert [r[0] for r in Z.zero_plan_tables(plan, Z.ZERO_TABLE_TENSOR_OFFSET)] == \
+            [int(x) for x in L.tensor_offset]
+        assert Z.zero_plan_tables(plan, Z.ZERO_TABLE_UNITS) == [tuple(int(x) for x in u) for u in L.units]
+        assert Z.zero_plan_tables(plan, Z.ZERO_TABLE_SHARD_SEGMENTS) == \
+            [tuple(int(x) for x in r) for r in L.shard_segments()]
+        if stage != 3:
+            assert Z.zero_plan_tables(plan, Z.ZERO_TABLE_BUCKET_SEGMENTS) == \
+                [tuple(int(x) for x in r) for r in L.bucket_segments(bucket)]
+        info = Z.zero_plan_info(plan)
+        assert info.phi == sum(sizes) and info.phi_pad == L.total_pad and info.shard == L.shard_total
+        # accounting == oracle closed forms
+        mem = Z.zero_memory_report(plan)
+        om = oracle.memory(L.total_pad, n_d)
+        assert [mem.logical[s][c] for s in range(4) for c in range(3)] == [int(x) for x in om[:12]]
+        assert mem.logical_ddp_fp32_grads == int(om[12])
+        com = Z.zero_comm_report(plan)
+        oc = oracle.comm(L.total_pad, n_d)
+        assert [com.ddp, com.zero1, com.zero2, com.zero3] == [int(x) for x in oc]
+        assert com.this_stage == int(oc[stage])
+        _check_state_layout(plan, L, n_d)
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
+def _check_state_layout(plan, L, n_d):
+    rows = Z.zero_plan_tables(plan, Z.ZERO_TABLE_STATE_LAYOUT)
+    assert len(rows) == n_d * len(L.units)
+    for r in range(n_d):
+        elems = Z.zero_rank_state_elems(plan, r)
+        mine = [row for row in rows if row[0] == r]
+        end = 0
+        for (rr, u, off, n), U in zip(mine, L.units):
+            assert n == U[4]
+            assert off >= end                           # no overlap, unit order kept
+            assert (off - r * n) % 8 == 0               # phase of the 16-bit shard start
+            assert off - end < 8                        # gap below one vector
+            end = off + n
+        assert end <= elems and elems % 8 == 0 and elems - end < 8
+
+
+def test_tables_match_oracle_random():
+    rng = np.random.default_rng(20)
+    for _ in range(300):
+        nt = int(rng.integers(0, 14))
+        sizes = [int(x) for x in rng.integers(0, 40, size=nt)]
+        n_d = int(rng.integers(1, 17))
+        stage = int(rng.integers(1, 4))
+        units, bucket = None, 0
+        if stage == 3 and nt > 1 and rng.random() < 0.7:
+            cuts = sorted(set(int(x) for x in rng.integers(1, nt, size=int(rng.integers(1, 4)))))
+            units = [0] + cuts
+        if stage != 3:
+            bucket = int(rng.integers(0, 50))
+        _compare_tables(sizes, n_d, stage, bucket, units)
+
+
+@pytest.mark.parametrize("i", range(W.N_WORKLOADS))
+def test_tables_match_oracle_workloads(i):
+    w = W.workload(i)
+    _compare_tables(w.sizes, w.n_d, w.stage, w.bucket_elems, w.unit_first or None)
+
+
+def test_workload_shapes_in_planner():
+    # configs 2-4: all shards a multiple of 8 elements (vector phase 0 everywhere)
+    for i in (2, 3, 4):
+        w = W.workload(i)
+        plan = _plan_for(w.sizes, w.n_d, w.stage, w.bucket_elems, w.unit_first or None)
+        rows = Z.zero_plan_tables(plan, Z.ZERO_TABLE_UNITS)
+        assert all(u[4] % 8 == 0 for u in rows)
+        Z.zero_plan_destroy(plan)
+    w = W.workload(2)
+    plan = _plan_for(w.sizes, w.n_d, w.stage, w.bucket_elems)
+    info = Z.zero_plan_info(plan)
+    assert info.n_buckets == 5 and info.shard == 15_554_976 and info.phi_pad == 124_439_808
+    Z.zero_plan_destroy(plan)
+    w = W.workload(4)
+    plan = _plan_for(w.sizes, w.n_d, w.stage, 0, w.unit_first)
+    assert Z.zero_plan_info(plan).shard == 842_301_952
+    Z.zero_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("args,code", [
+    (([4, 4], 0, 1), Z.ZERO_EINVAL),
+    (([4, 4], 4, 4), Z.ZERO_EINVAL),
+    (([4, -1], 2, 1), Z.ZERO_EINVAL),
+    (([4, 4], Z.ZERO_MAX_RANKS + 1, 1), Z.ZERO_ERANGE),
+])
+def test_plan_create_errors(args, code):
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_plan_create(*args)
+    assert e.value.status == code
+
+
+def test_plan_create_argument_errors():
+    for kw, code in [(dict(stage=3, bucket_elems=8), Z.ZERO_EINVAL),
+                     (dict(stage=1, unit_first=[0, 1]), Z.ZERO_EINVAL),
+                     (dict(stage=3, unit_first=[1]), Z.ZERO_EINVAL),
+                     (dict(stage=3, unit_first=[0, 2, 2]), Z.ZERO_EINVAL),
+                     (dict(stage=2, dtype16=7), Z.ZERO_EINVAL),
+                     (dict(stage=2, bucket_elems=-1), Z.ZERO_EINVAL)]:
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_plan_create([3, 5, 7], 2, **kw)
+        assert e.value.status == code, kw
+        assert Z.zero_last_error()
+
+
+def test_calls_out_of_order_fail_without_touching_the_gpu():
+    plan = _plan_for([10, 20], 3, 2, 8)
+    try:
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_step_finish(plan, None)
+        assert e.value.status == Z.ZERO_ESTATE
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_gather_layer(plan, 0, 0x1000)
+        assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:     # nothing bound yet
+            Z.zero_step(plan, [0x1000] * 3, 0, Z.hyper(), None)
+        assert e.value.status == Z.ZERO_ESTATE
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_step(plan, [0x1000] * 2, 0, Z.hyper(), None)
+        assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_bind_peer(plan, 0, 0x1000)
+        assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_plan_tables(plan, 99)
+        assert e.value.status == Z.ZERO_EINVAL
+        buf = (ctypes.c_int64 * 1)()
+        n = ctypes.c_int64()
+        assert Z.lib().zero_plan_tables(plan, Z.ZERO_TABLE_SHARD_SEGMENTS, buf, 1, ctypes.byref(n)) \
+            == Z.ZERO_ERANGE
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
+def test_empty_model_plan():
+    plan = _plan_for([], 4, 2, 0)
+    info = Z.zero_plan_info(plan)
+    assert info.phi == info.phi_pad == info.shard == info.n_buckets == 0
+    assert Z.zero_plan_tables(plan, Z.ZERO_TABLE_SHARD_SEGMENTS) == []
+    Z.zero_plan_destroy(plan)

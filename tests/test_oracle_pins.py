@@ -545,3 +545,20 @@ def test_workload_shapes():
     w1 = W.workload(1)
     assert len(w1.sizes) == 10000 and min(w1.sizes) >= 1 and max(w1.sizes) <= 65536
     assert 50e6 < w1.phi < 70e6
+
+
+def test_scaler_trajectory():
+    """Skip + halve on a flagged step (t unchanged); grow x2 after `interval` clean steps;
+    never below the minimum scale."""
+    cfg = W.Scaler(init_scale=8.0, growth_interval=3, min_scale=2.0)
+    s = oracle.ScalerState(cfg)
+    trace = []
+    for flag in [0, 1, 0, 0, 0, 1, 1, 1, 0]:
+        s.update(flag)
+        trace.append((s.t, s.scale, s.good))
+    assert trace == [(1, 8.0, 1), (1, 4.0, 0), (2, 4.0, 1), (3, 4.0, 2), (4, 8.0, 0),
+                     (4, 4.0, 0), (4, 2.0, 0), (4, 2.0, 0), (5, 2.0, 1)]
+    s = oracle.ScalerState(None)
+    for flag in [0, 1, 0]:
+        s.update(flag)
+    assert (s.t, s.scale) == (2, 1.0)

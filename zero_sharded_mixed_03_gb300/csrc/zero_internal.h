@@ -1,0 +1,103 @@
+// zero_internal.h -- plan representation shared by the host planner
+// (zero_plan.cpp) and the device side (zero_step.cu).  Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/zero.h"
+
+namespace zero {
+
+// One FSDP unit's FlatParameter ("FSDP-1: FlatParameter and Module-Level
+// Wrapping"): its tensors are contiguous in the global flat index space,
+// followed by tail padding up to a multiple of N_d.
+struct Unit {
+    int64_t first;       // first tensor
+    int64_t count;       // tensors in the unit
+    int64_t numel;       // sum of its tensor sizes
+    int64_t numel_pad;   // numel rounded up to a multiple of N_d
+    int64_t shard;       // numel_pad / N_d
+    int64_t base;        // global flat offset of the unit
+    int64_t shard_base;  // logical offset of the unit's shard inside a rank's shard
+};
+
+// A rank's device buffers (all caller-owned).
+struct Rank {
+    bool bound = false;          // optimizer state bound: updated by zero_step
+    bool peer = false;           // stage 3: 16-bit shard only (optimizer elsewhere)
+    float* master[2] = {nullptr, nullptr};
+    float* m[2] = {nullptr, nullptr};
+    float* v[2] = {nullptr, nullptr};
+    uint16_t* shard16 = nullptr; // stage 3
+};
+
+// Elementwise work item of one launch: n elements of one rank's shard.
+//   contributions: element c_off of every contribution buffer
+//   state:         element s_off of the rank's master/m/v (both halves)
+//   16-bit output: element o_off of `out16`
+struct Segment {
+    int64_t n;
+    int64_t c_off;
+    int64_t s_off;
+    int64_t o_off;
+    int rank;
+    uint16_t* out16;
+};
+
+}  // namespace zero
+
+struct zero_plan {
+    int n_d = 0;
+    int stage = 0;
+    int dtype16 = 0;
+    int64_t bucket_elems = 0;           // 0 = whole buffer
+    std::vector<int64_t> sizes;
+    std::vector<int64_t> tensor_offset;
+    std::vector<zero::Unit> units;
+    int64_t phi = 0;
+    int64_t phi_pad = 0;
+    int64_t shard_total = 0;
+    int64_t n_buckets = 0;
+    // Physical state layout: phys_off[r][u] = element offset of unit u's shard in rank r's
+    // state buffers; state_elems[r] = their length.
+    std::vector<std::vector<int64_t>> phys_off;
+    std::vector<int64_t> state_elems;
+
+    // Bindings (device pointers, caller-owned).
+    std::vector<zero::Rank> ranks;
+    uint16_t* full16 = nullptr;
+    uint32_t* workspace = nullptr;
+    int device = -1;
+
+    // Step state.
+    int64_t t = 0;                      // applied steps
+    int cur = 0;                        // current half of the ping-pong pairs
+    bool in_step = false;
+    std::vector<char> covered;          // per bucket / unit in the open step
+    float consts[9] = {0};              // fp32 step constants of the open step
+    double step_scale = 1.0;
+    zero_hyper_t step_hyper = {0, 0, 0, 0, 0};
+    std::vector<char> gathered;         // stage 3: per unit
+};
+
+namespace zero {
+
+// Thread-local last-error text (zero_last_error).
+zero_status_t fail(zero_status_t code, const std::string& msg);
+
+// Bucket b's global flat range [lo, hi) (stages 1/2); b = -1: the whole buffer.
+void bucket_range(const zero_plan* p, int64_t b, int64_t* lo, int64_t* hi);
+
+// Work items of one zero_step call over the bound ranks.
+std::vector<Segment> step_segments(const zero_plan* p, int64_t which, int cur_out);
+
+// Work items covering every bound rank's whole shard (re-cast of a skipped step).
+std::vector<Segment> shard_segments_all(const zero_plan* p);
+
+// fp32 step constants, computed in double and rounded once:
+// b1, 1-b1, b2, 1-b2, eps, lr*wd, lr/(1-b1^t), sqrt(1-b2^t), 1/(N_d*scale).
+void step_constants(const zero_hyper_t& h, int64_t t, double scale, int n_d, float out[9]);
+
+}  // namespace zero

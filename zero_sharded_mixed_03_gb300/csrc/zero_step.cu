@@ -1,0 +1,716 @@
+// zero_step.cu -- device side of the sharded mixed-precision AdamW step for
+// GB300 (sm_103a): bind, the fused reduce + AdamW + cast kernel, commit/skip,
+// the skip re-cast and the stage-3 gather.
+//
+// Page: "Zero Redundancy Optimizer (ZeRO) and Fully Sharded Data Parallelism
+// (FSDP): Mathematical Foundations ..." (llms.blog):
+//   "Execution Flow for ZeRO-1" steps 2-4 (reduce-scatter of the averaged
+//   gradient, shard update, all-gather of the 16-bit shards), "ZeRO-Stage 2"
+//   (gradients reduced as produced, here per bucket), "ZeRO-3 / FSDP Layer
+//   Execution Lifecycle" (per-unit all-gather and reduce-scatter).
+//
+// The path is elementwise plus a reduction over N_d ranks: about 15 flops per
+// parameter against 2*N_d + 26 bytes, far below any tensor-core ridge, so it
+// is written for HBM bandwidth: 128-bit loads/stores, one pass, fp32 state
+// double-buffered so the global skip decision needs no second pass.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "zero_internal.h"
+
+namespace zero {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxSegs = 32;      // work items per launch (more are split across launches)
+constexpr int kScalarSlots = 16;  // per segment: up to 7 head + 7 tail elements
+constexpr int kWorkspaceBytes = 256;
+
+// ------------------------------------------------------------------ launch parameters
+
+struct KSeg {
+    const float* p_in;
+    const float* m_in;
+    const float* v_in;
+    float* p_out;
+    float* m_out;
+    float* v_out;
+    uint16_t* out16;
+    int64_t c_off;   // element offset into every contribution buffer
+    int64_t n;       // elements
+    int64_t nvec;    // aligned vectors in the body
+    int64_t vbeg;    // index of the first body vector in the launch
+    int32_t head;    // scalar elements before the body
+    int32_t tail;    // scalar elements after the body
+};
+
+struct StepParams {
+    const uint16_t* c[ZERO_MAX_RANKS];
+    KSeg seg[kMaxSegs];
+    float k[9];       // b1, 1-b1, b2, 1-b2, eps, lr*wd, lr/bc1, sqrt(bc2), inv
+    int n_d;
+    int n_seg;
+    int64_t total_vec;
+    uint32_t* flag;
+};
+
+struct CopySeg {
+    const uint16_t* src;
+    uint16_t* dst;
+    int64_t n, nvec, vbeg;
+    int32_t head, tail;
+};
+
+struct CopyParams {
+    CopySeg seg[kMaxSegs];
+    int n_seg;
+    int64_t total_vec;
+};
+
+// ------------------------------------------------------------------ element helpers
+
+// 16-bit -> fp32 widening (exact).  bf16 is the upper half of an IEEE binary32.
+template <int DT>
+__device__ __forceinline__ float widen1(uint16_t h)
+{
+    if constexpr (DT == ZERO_BF16) return __uint_as_float((uint32_t)h << 16);
+    else return __half2float(__ushort_as_half(h));
+}
+
+template <int DT>
+__device__ __forceinline__ void widen2(uint32_t w, float& lo, float& hi)
+{
+    if constexpr (DT == ZERO_BF16) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xFFFF0000u);
+    } else {
+        __half2 h = *reinterpret_cast<const __half2*>(&w);
+        float2 f = __half22float2(h);
+        lo = f.x;
+        hi = f.y;
+    }
+}
+
+// fp32 -> 16-bit, round to nearest even.
+template <int DT>
+__device__ __forceinline__ uint16_t narrow1(float f)
+{
+    if constexpr (DT == ZERO_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    else return __half_as_ushort(__float2half_rn(f));
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t narrow2(float lo, float hi)
+{
+    if constexpr (DT == ZERO_BF16) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&b);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+__device__ __forceinline__ bool nonfinite(float g)
+{
+    return (__float_as_uint(g) & 0x7F800000u) == 0x7F800000u;
+}
+
+// AdamW on one element with separately rounded IEEE operations (no contraction):
+//   m = b1 m + (1-b1) g ; v = b2 v + (1-b2) g^2 ; d = sqrt(v)/sqrt(bc2) + eps
+//   p = p - (lr wd) p   ; p = p - (lr/bc1) (m / d)
+__device__ __forceinline__ void adamw1(float g, float& p, float& m, float& v, const float* k)
+{
+    m = __fadd_rn(__fmul_rn(k[0], m), __fmul_rn(k[1], g));
+    v = __fadd_rn(__fmul_rn(k[2], v), __fmul_rn(k[3], __fmul_rn(g, g)));
+    const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), k[7]), k[4]);
+    p = __fsub_rn(p, __fmul_rn(k[5], p));
+    p = __fsub_rn(p, __fmul_rn(k[6], __fdiv_rn(m, d)));
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* p)
+{
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+// ------------------------------------------------------------------ fused step kernel
+
+template <int DT>
+__device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, int64_t e)
+{
+    float sum = 0.0f;
+    for (int r = 0; r < P.n_d; ++r) sum = __fadd_rn(sum, widen1<DT>(P.c[r][S.c_off + e]));
+    const float g = __fmul_rn(sum, P.k[8]);
+    float p = S.p_in[e], m = S.m_in[e], v = S.v_in[e];
+    adamw1(g, p, m, v, P.k);
+    S.p_out[e] = p;
+    S.m_out[e] = m;
+    S.v_out[e] = v;
+    S.out16[e] = narrow1<DT>(p);
+    return nonfinite(g);
+}
+
+// Eight consecutive elements starting at e: 128-bit loads of the N_d contribution slices
+// (batches of NB ranks in flight), 2 x 128-bit per fp32 state array, 128-bit 16-bit store.
+template <int DT, int NB>
+__device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, int64_t e)
+{
+    const float4 p0 = __ldg(reinterpret_cast<const float4*>(S.p_in + e));
+    const float4 p1 = __ldg(reinterpret_cast<const float4*>(S.p_in + e) + 1);
+    const float4 m0 = __ldg(reinterpret_cast<const float4*>(S.m_in + e));
+    const float4 m1 = __ldg(reinterpret_cast<const float4*>(S.m_in + e) + 1);
+    const float4 v0 = __ldg(reinterpret_cast<const float4*>(S.v_in + e));
+    const float4 v1 = __ldg(reinterpret_cast<const float4*>(S.v_in + e) + 1);
+
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int r0 = 0; r0 < P.n_d; r0 += NB) {
+        uint4 c[NB];
+#pragma unroll
+        for (int q = 0; q < NB; ++q)
+            if (r0 + q < P.n_d) c[q] = ld_stream(P.c[r0 + q] + S.c_off + e);
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            if (r0 + q < P.n_d) {
+                const uint32_t w[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float lo, hi;
+                    widen2<DT>(w[j], lo, hi);
+                    acc[2 * j] = __fadd_rn(acc[2 * j], lo);
+                    acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], hi);
+                }
+            }
+        }
+    }
+
+    float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float g = __fmul_rn(acc[j], P.k[8]);
+        bad |= nonfinite(g);
+        adamw1(g, p[j], m[j], v[j], P.k);
+    }
+    __stcs(reinterpret_cast<float4*>(S.p_out + e), make_float4(p[0], p[1], p[2], p[3]));
+    __stcs(reinterpret_cast<float4*>(S.p_out + e) + 1, make_float4(p[4], p[5], p[6], p[7]));
+    __stcs(reinterpret_cast<float4*>(S.m_out + e), make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(reinterpret_cast<float4*>(S.m_out + e) + 1, make_float4(m[4], m[5], m[6], m[7]));
+    __stcs(reinterpret_cast<float4*>(S.v_out + e), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<float4*>(S.v_out + e) + 1, make_float4(v[4], v[5], v[6], v[7]));
+    uint4 o;
+    o.x = narrow2<DT>(p[0], p[1]);
+    o.y = narrow2<DT>(p[2], p[3]);
+    o.z = narrow2<DT>(p[4], p[5]);
+    o.w = narrow2<DT>(p[6], p[7]);
+    __stcs(reinterpret_cast<uint4*>(S.out16 + e), o);
+    return bad;
+}
+
+// Persistent grid-stride kernel over the concatenated body vectors of all segments, plus
+// kScalarSlots scalar slots per segment for the unaligned head and tail.  VEC = 8: 128-bit
+// body; VEC = 1: every element is a body vector of one (streams of different phases).
+template <int DT, int NB, int VEC>
+__global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_constant__ StepParams P)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    bool bad = false;
+
+    if constexpr (VEC == 8) {
+        for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
+            const KSeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) bad |= step_scalar<DT>(P, S, e);
+        }
+    }
+
+    int s = 0;
+    for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
+        while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
+        const KSeg& S = P.seg[s];
+        if constexpr (VEC == 8) bad |= step_vec8<DT, NB>(P, S, S.head + 8 * (vi - S.vbeg));
+        else bad |= step_scalar<DT>(P, S, vi - S.vbeg);
+    }
+
+    // Global non-finite flag: one OR across the block, one atomic per block that saw one.
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(P.flag, 1u);
+}
+
+// ------------------------------------------------------------------ re-cast kernel (skip)
+
+template <int DT, int VEC>
+__global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant__ StepParams P)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if constexpr (VEC == 8) {
+        for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
+            const KSeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) S.out16[e] = narrow1<DT>(S.p_in[e]);
+        }
+    }
+    int s = 0;
+    for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
+        while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
+        const KSeg& S = P.seg[s];
+        if constexpr (VEC == 8) {
+            const int64_t e = S.head + 8 * (vi - S.vbeg);
+            const float4 a = __ldcs(reinterpret_cast<const float4*>(S.p_in + e));
+            const float4 b = __ldcs(reinterpret_cast<const float4*>(S.p_in + e) + 1);
+            uint4 o;
+            o.x = narrow2<DT>(a.x, a.y);
+            o.y = narrow2<DT>(a.z, a.w);
+            o.z = narrow2<DT>(b.x, b.y);
+            o.w = narrow2<DT>(b.z, b.w);
+            __stcs(reinterpret_cast<uint4*>(S.out16 + e), o);
+        } else {
+            const int64_t e = vi - S.vbeg;
+            S.out16[e] = narrow1<DT>(S.p_in[e]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ gather kernel (stage 3)
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ CopyParams P)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if constexpr (VEC == 8) {
+        for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
+            const CopySeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) S.dst[e] = S.src[e];
+        }
+    }
+    int s = 0;
+    for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
+        while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
+        const CopySeg& S = P.seg[s];
+        if constexpr (VEC == 8) {
+            const int64_t e = S.head + 8 * (vi - S.vbeg);
+            __stcs(reinterpret_cast<uint4*>(S.dst + e), __ldcs(reinterpret_cast<const uint4*>(S.src + e)));
+        } else {
+            const int64_t e = vi - S.vbeg;
+            S.dst[e] = S.src[e];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host helpers
+
+inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Elements before the first 16-byte boundary of a 16-bit stream starting at p.
+inline int head16(const void* p) { return (int)(((16 - ((uintptr_t)p % 16)) % 16) / 2); }
+
+struct DeviceProps {
+    int sms = 0;
+    int blocks_per_sm = 0;
+};
+
+int device_sms(int dev)
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = sms;
+    }
+    return cache[dev];
+}
+
+template <typename K>
+int grid_for(K kernel, int dev, int64_t work)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
+        per_sm = 1;
+    per_sm = std::max(per_sm, 1);
+    const int64_t cap = (int64_t)device_sms(dev) * per_sm;
+    const int64_t need = std::max<int64_t>(1, (work + kThreads - 1) / kThreads);
+    return (int)std::max<int64_t>(1, std::min(cap, need));
+}
+
+zero_status_t cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(ZERO_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Fill one launch's KSeg list from plan segments [b, e), deciding the vector path.
+// Returns true when every stream of every segment shares one 16-byte phase.
+bool build_step_params(const zero_plan* p, const std::vector<Segment>& segs, size_t b, size_t e,
+                       const void* const* contribs, int in_half, StepParams& P)
+{
+    bool vec_ok = true;
+    P.n_seg = (int)(e - b);
+    for (size_t i = b; i < e; ++i) {
+        const Segment& sg = segs[i];
+        const Rank& R = p->ranks[(size_t)sg.rank];
+        KSeg& K = P.seg[i - b];
+        K.p_in = R.master[in_half] + sg.s_off;
+        K.m_in = R.m[in_half] + sg.s_off;
+        K.v_in = R.v[in_half] + sg.s_off;
+        K.p_out = R.master[in_half ^ 1] + sg.s_off;
+        K.m_out = R.m[in_half ^ 1] + sg.s_off;
+        K.v_out = R.v[in_half ^ 1] + sg.s_off;
+        K.out16 = sg.out16 + sg.o_off;
+        K.c_off = sg.c_off;
+        K.n = sg.n;
+        const int h = head16(K.out16);
+        if (contribs)
+            for (int r = 0; r < p->n_d; ++r)
+                vec_ok &= head16((const uint16_t*)contribs[r] + sg.c_off) == h;
+        const int64_t hh = std::min<int64_t>(h, sg.n);
+        const float* fp[6] = {K.p_in, K.m_in, K.v_in, K.p_out, K.m_out, K.v_out};
+        for (const float* f : fp) vec_ok &= aligned(f + hh, 16);
+        K.head = (int32_t)hh;
+        K.nvec = (sg.n - hh) / 8;
+        K.tail = (int32_t)(sg.n - hh - 8 * K.nvec);
+    }
+    return vec_ok;
+}
+
+void finalize_vectors(StepParams& P, bool vec)
+{
+    int64_t acc = 0;
+    for (int i = 0; i < P.n_seg; ++i) {
+        KSeg& K = P.seg[i];
+        if (!vec) {
+            K.head = 0;
+            K.tail = 0;
+            K.nvec = K.n;
+        }
+        K.vbeg = acc;
+        acc += K.nvec;
+    }
+    P.total_vec = acc;
+}
+
+template <int DT>
+zero_status_t launch_fused(const zero_plan* p, StepParams& P, bool vec, cudaStream_t st)
+{
+    finalize_vectors(P, vec);
+    const int nd = P.n_d;
+    const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
+    auto go = [&](auto kernel) {
+        const int grid = grid_for(kernel, p->device, work);
+        kernel<<<grid, kThreads, 0, st>>>(P);
+    };
+    if (!vec) go(fused_step_kernel<DT, 1, 1>);
+    else if (nd <= 4) go(fused_step_kernel<DT, 4, 8>);
+    else if (nd <= 8) go(fused_step_kernel<DT, 8, 8>);
+    else go(fused_step_kernel<DT, 16, 8>);
+    const cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? ZERO_OK : cuda_fail(err, "fused step launch");
+}
+
+template <int DT>
+zero_status_t launch_recast(const zero_plan* p, StepParams& P, bool vec, cudaStream_t st)
+{
+    finalize_vectors(P, vec);
+    const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
+    if (vec) {
+        recast_kernel<DT, 8><<<grid_for(recast_kernel<DT, 8>, p->device, work), kThreads, 0, st>>>(P);
+    } else {
+        recast_kernel<DT, 1><<<grid_for(recast_kernel<DT, 1>, p->device, work), kThreads, 0, st>>>(P);
+    }
+    const cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? ZERO_OK : cuda_fail(err, "re-cast launch");
+}
+
+zero_status_t set_device(const zero_plan* p)
+{
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (p->device >= 0 && cur != p->device) {
+        e = cudaSetDevice(p->device);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    }
+    return ZERO_OK;
+}
+
+}  // namespace
+}  // namespace zero
+
+using namespace zero;
+
+extern "C" {
+
+zero_status_t zero_bind(zero_plan_t* p, int rank, float* const master[2], float* const m[2],
+                        float* const v[2], void* shard16, void* full16, void* workspace)
+{
+    if (!p || !master || !m || !v) return fail(ZERO_EINVAL, "zero_bind: NULL argument");
+    if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind: bad rank");
+    if (p->in_step) return fail(ZERO_ESTATE, "zero_bind: a step is open");
+    float* bufs[6] = {master[0], master[1], m[0], m[1], v[0], v[1]};
+    const int64_t elems = p->state_elems[(size_t)rank];
+    if (elems > 0 && (master[0] == master[1] || m[0] == m[1] || v[0] == v[1]))
+        return fail(ZERO_EINVAL, "zero_bind: the two halves of a ping-pong pair must differ");
+    for (float* b : bufs) {
+        if (elems > 0 && !b) return fail(ZERO_EINVAL, "zero_bind: NULL state buffer");
+        if (!aligned(b, 4)) return fail(ZERO_EALIGN, "zero_bind: fp32 state not 4-byte aligned");
+    }
+    if (p->stage == 3) {
+        if (elems > 0 && !shard16) return fail(ZERO_EINVAL, "zero_bind: stage 3 needs shard16");
+        if (!aligned(shard16, 2)) return fail(ZERO_EALIGN, "zero_bind: shard16 not 2-byte aligned");
+    } else {
+        if (!full16 && !p->full16 && p->phi_pad > 0)
+            return fail(ZERO_EINVAL, "zero_bind: stages 1/2 need the flat 16-bit buffer");
+        if (full16 && p->full16 && full16 != p->full16)
+            return fail(ZERO_EINVAL, "zero_bind: full16 differs from an earlier bind");
+        if (!aligned(full16, 2)) return fail(ZERO_EALIGN, "zero_bind: full16 not 2-byte aligned");
+    }
+    if (!workspace && !p->workspace) return fail(ZERO_EINVAL, "zero_bind: workspace is NULL");
+    if (workspace && p->workspace && workspace != p->workspace)
+        return fail(ZERO_EINVAL, "zero_bind: workspace differs from an earlier bind");
+    if (!aligned(workspace, 8)) return fail(ZERO_EALIGN, "zero_bind: workspace not 8-byte aligned");
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_bind: cudaGetDevice");
+    if (p->device >= 0 && p->device != dev)
+        return fail(ZERO_EINVAL, "zero_bind: buffers of one plan must live on one device");
+    if (workspace && !p->workspace) {
+        e = cudaMemset(workspace, 0, kWorkspaceBytes);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "zero_bind: clearing the workspace");
+        p->workspace = (uint32_t*)workspace;
+    }
+    p->device = dev;
+    if (full16) p->full16 = (uint16_t*)full16;
+    Rank& R = p->ranks[(size_t)rank];
+    R.bound = true;
+    R.peer = false;
+    for (int h = 0; h < 2; ++h) {
+        R.master[h] = master[h];
+        R.m[h] = m[h];
+        R.v[h] = v[h];
+    }
+    R.shard16 = (uint16_t*)shard16;
+    return ZERO_OK;
+}
+
+zero_status_t zero_bind_peer(zero_plan_t* p, int rank, const void* shard16)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_bind_peer: NULL plan");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_bind_peer: stage 3 only");
+    if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind_peer: bad rank");
+    if (!shard16 && p->state_elems[(size_t)rank] > 0)
+        return fail(ZERO_EINVAL, "zero_bind_peer: NULL shard16");
+    if (!aligned(shard16, 2)) return fail(ZERO_EALIGN, "zero_bind_peer: shard16 not 2-byte aligned");
+    Rank& R = p->ranks[(size_t)rank];
+    if (R.bound) return fail(ZERO_ESTATE, "zero_bind_peer: rank already bound with state");
+    R.peer = true;
+    R.shard16 = (uint16_t*)shard16;
+    return ZERO_OK;
+}
+
+zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
+                        int64_t which, const zero_hyper_t* hyper, const zero_scaler_t* scaler,
+                        void* stream)
+{
+    if (!p || !grad_contribs || !hyper) return fail(ZERO_EINVAL, "zero_step: NULL argument");
+    if (n_contribs != p->n_d) return fail(ZERO_EINVAL, "zero_step: need one contribution per rank");
+    if (!p->workspace) return fail(ZERO_ESTATE, "zero_step: no rank bound");
+    bool any = false;
+    for (const Rank& R : p->ranks) any |= R.bound;
+    if (!any) return fail(ZERO_ESTATE, "zero_step: no rank bound");
+    for (int64_t r = 0; r < n_contribs; ++r) {
+        if (!grad_contribs[r]) return fail(ZERO_EINVAL, "zero_step: NULL contribution");
+        if (!aligned(grad_contribs[r], 2))
+            return fail(ZERO_EALIGN, "zero_step: contribution not 2-byte aligned");
+    }
+    const double scale = scaler ? scaler->scale : 1.0;
+    if (!(scale > 0.0) || !std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_step: bad loss scale");
+    if (p->stage == 3) {
+        if (which < 0 || which >= (int64_t)p->units.size())
+            return fail(ZERO_EINVAL, "zero_step: unit out of range");
+    } else if (which < -1 || which >= p->n_buckets) {
+        return fail(ZERO_EINVAL, "zero_step: bucket out of range");
+    }
+
+    if (!p->in_step) {
+        step_constants(*hyper, p->t + 1, scale, p->n_d, p->consts);
+        p->step_hyper = *hyper;
+        p->step_scale = scale;
+    } else if (std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0 || p->step_scale != scale) {
+        return fail(ZERO_EINVAL, "zero_step: hyperparameters / scale changed inside a step");
+    }
+    if (which == -1) {
+        if (p->in_step) return fail(ZERO_ESTATE, "zero_step: bucket -1 must be the only call of a step");
+    } else if (p->covered[(size_t)which]) {
+        return fail(ZERO_ESTATE, "zero_step: bucket/unit already stepped in this step");
+    }
+
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    const std::vector<Segment> segs = step_segments(p, which, p->cur ^ 1);
+    cudaStream_t s = (cudaStream_t)stream;
+    for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
+        const size_t e = std::min(segs.size(), b + kMaxSegs);
+        StepParams P;
+        std::memset(&P, 0, sizeof(P));
+        for (int r = 0; r < p->n_d; ++r) P.c[r] = (const uint16_t*)grad_contribs[r];
+        std::memcpy(P.k, p->consts, sizeof(P.k));
+        P.n_d = p->n_d;
+        P.flag = p->workspace;
+        const bool vec = build_step_params(p, segs, b, e, grad_contribs, p->cur, P);
+        st = p->dtype16 == ZERO_BF16 ? launch_fused<ZERO_BF16>(p, P, vec, s)
+                                     : launch_fused<ZERO_FP16>(p, P, vec, s);
+        if (st != ZERO_OK) return st;
+    }
+    p->in_step = true;
+    if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
+    else p->covered[(size_t)which] = 1;
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_finish(zero_plan_t* p, zero_scaler_t* scaler, void* stream,
+                               zero_step_result_t* out)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_step_finish: NULL plan");
+    if (!p->in_step) return fail(ZERO_ESTATE, "zero_step_finish: no open step");
+    for (int64_t b = 0; b < p->n_buckets; ++b)
+        if (!p->covered[(size_t)b])
+            return fail(ZERO_ESTATE, "zero_step_finish: a bucket/unit was not stepped");
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t flag = 0;
+    cudaError_t e = cudaMemcpyAsync(&flag, p->workspace, sizeof(flag), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_finish: reading the flag");
+
+    const bool skipped = flag != 0;
+    if (!skipped) {
+        p->cur ^= 1;
+        p->t += 1;
+        if (scaler) {
+            scaler->good_steps += 1;
+            if (scaler->growth_interval > 0 && scaler->good_steps >= scaler->growth_interval) {
+                scaler->scale *= scaler->growth_factor;
+                scaler->good_steps = 0;
+            }
+        }
+    } else {
+        const std::vector<Segment> segs = shard_segments_all(p);
+        for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
+            const size_t en = std::min(segs.size(), b + kMaxSegs);
+            StepParams P;
+            std::memset(&P, 0, sizeof(P));
+            P.n_d = p->n_d;
+            const bool vec = build_step_params(p, segs, b, en, nullptr, p->cur, P);
+            st = p->dtype16 == ZERO_BF16 ? launch_recast<ZERO_BF16>(p, P, vec, s)
+                                         : launch_recast<ZERO_FP16>(p, P, vec, s);
+            if (st != ZERO_OK) return st;
+        }
+        if (scaler) {
+            scaler->scale = std::max(scaler->scale * scaler->backoff_factor, scaler->min_scale);
+            scaler->good_steps = 0;
+        }
+        e = cudaMemsetAsync(p->workspace, 0, sizeof(uint32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_step_finish: clearing the flag");
+    }
+    p->in_step = false;
+    std::fill(p->covered.begin(), p->covered.end(), 0);
+    if (out) {
+        out->skipped = skipped ? 1 : 0;
+        out->reserved = 0;
+        out->t = p->t;
+        out->scale = scaler ? scaler->scale : 1.0;
+    }
+    return ZERO_OK;
+}
+
+zero_status_t zero_gather_layer(zero_plan_t* p, int64_t unit, void* full_unit16, void* stream)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_gather_layer: NULL plan");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_gather_layer: stage 3 only");
+    if (unit < 0 || unit >= (int64_t)p->units.size())
+        return fail(ZERO_EINVAL, "zero_gather_layer: unit out of range");
+    if (p->gathered[(size_t)unit]) return fail(ZERO_ESTATE, "zero_gather_layer: unit not released");
+    const Unit& U = p->units[(size_t)unit];
+    if (U.numel_pad > 0 && !full_unit16) return fail(ZERO_EINVAL, "zero_gather_layer: NULL destination");
+    if (!aligned(full_unit16, 2)) return fail(ZERO_EALIGN, "zero_gather_layer: destination not 2-byte aligned");
+    for (const Rank& R : p->ranks)
+        if (!R.shard16 && U.shard > 0)
+            return fail(ZERO_ESTATE, "zero_gather_layer: a rank has no 16-bit shard bound");
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    for (int r0 = 0; r0 < p->n_d && U.shard > 0; r0 += kMaxSegs) {
+        CopyParams P;
+        std::memset(&P, 0, sizeof(P));
+        bool vec = true;
+        const int r1 = std::min(p->n_d, r0 + kMaxSegs);
+        P.n_seg = r1 - r0;
+        for (int r = r0; r < r1; ++r) {
+            CopySeg& K = P.seg[r - r0];
+            K.src = p->ranks[(size_t)r].shard16 + p->phys_off[(size_t)r][(size_t)unit];
+            K.dst = (uint16_t*)full_unit16 + r * U.shard;
+            K.n = U.shard;
+            const int h = head16(K.dst);
+            vec &= head16(K.src) == h;
+            K.head = (int32_t)std::min<int64_t>(h, K.n);
+            K.nvec = (K.n - K.head) / 8;
+            K.tail = (int32_t)(K.n - K.head - 8 * K.nvec);
+        }
+        int64_t acc = 0;
+        for (int i = 0; i < P.n_seg; ++i) {
+            CopySeg& K = P.seg[i];
+            if (!vec) {
+                K.head = K.tail = 0;
+                K.nvec = K.n;
+            }
+            K.vbeg = acc;
+            acc += K.nvec;
+        }
+        P.total_vec = acc;
+        const int64_t work = std::max<int64_t>(acc, (int64_t)P.n_seg * kScalarSlots);
+        if (vec) gather_kernel<8><<<grid_for(gather_kernel<8>, p->device, work), kThreads, 0, s>>>(P);
+        else gather_kernel<1><<<grid_for(gather_kernel<1>, p->device, work), kThreads, 0, s>>>(P);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    }
+    p->gathered[(size_t)unit] = 1;
+    return ZERO_OK;
+}
+
+zero_status_t zero_release_layer(zero_plan_t* p, int64_t unit)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_release_layer: NULL plan");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_release_layer: stage 3 only");
+    if (unit < 0 || unit >= (int64_t)p->units.size())
+        return fail(ZERO_EINVAL, "zero_release_layer: unit out of range");
+    if (!p->gathered[(size_t)unit]) return fail(ZERO_ESTATE, "zero_release_layer: unit not gathered");
+    p->gathered[(size_t)unit] = 0;
+    return ZERO_OK;
+}
+
+}  // extern "C"

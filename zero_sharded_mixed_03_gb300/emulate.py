@@ -1,0 +1,117 @@
+"""An emulated data-parallel group on one GPU.
+
+The N_d ranks of the group live in one GPU's HBM: each bound rank owns its fp32
+master/m/v shard (a ping-pong pair each), stage 3 ranks own a 16-bit parameter
+shard, and stages 1/2 share one flat 16-bit parameter buffer (every replica is
+identical).  This module only allocates those buffers with torch and forwards
+them to the C ABI; every step of the optimizer runs in libzero's kernels.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from . import (ZERO_BF16, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS, zero_bind, zero_bind_peer,
+               zero_gather_layer, zero_plan_create, zero_plan_destroy, zero_plan_info,
+               zero_plan_tables, zero_rank_state_elems, zero_release_layer, zero_state_cursor,
+               zero_step, zero_step_finish)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+class EmulatedGroup:
+    """Plan + device buffers of N_d emulated ranks (only `bound_ranks` carry optimizer state)."""
+
+    def __init__(self, sizes: Sequence[int], n_d: int, stage: int, bucket_elems: int = 0,
+                 unit_first: Optional[Sequence[int]] = None, dtype16: int = ZERO_BF16,
+                 bound_ranks: Optional[Sequence[int]] = None, device: str = "cuda"):
+        self.device = torch.device(device)
+        self.n_d, self.stage, self.dtype16 = n_d, stage, dtype16
+        self.plan = zero_plan_create(list(sizes), n_d, stage, bucket_elems,
+                                     list(unit_first) if unit_first else None, dtype16)
+        self.info = zero_plan_info(self.plan)
+        self.units = zero_plan_tables(self.plan, ZERO_TABLE_UNITS)
+        layout = zero_plan_tables(self.plan, ZERO_TABLE_STATE_LAYOUT)
+        self.phys_off: Dict[int, List[int]] = {}
+        for r, u, off, _n in layout:
+            self.phys_off.setdefault(r, []).append(off)
+        self.bound = list(bound_ranks) if bound_ranks is not None else list(range(n_d))
+        self.state: Dict[int, Dict[str, List[torch.Tensor]]] = {}
+        self.shard16: Dict[int, torch.Tensor] = {}
+        self.workspace = torch.zeros(int(self.info.workspace_bytes) // 4, dtype=torch.int32,
+                                     device=self.device)
+        self.full16 = None
+        if stage != 3:
+            self.full16 = torch.zeros(int(self.info.phi_pad), dtype=torch.int16, device=self.device)
+        for r in self.bound:
+            n = zero_rank_state_elems(self.plan, r)
+            st = {k: [torch.zeros(n, dtype=torch.float32, device=self.device) for _ in range(2)]
+                  for k in ("master", "m", "v")}
+            self.state[r] = st
+            sh = None
+            if stage == 3:
+                sh = torch.zeros(n, dtype=torch.int16, device=self.device)
+                self.shard16[r] = sh
+            zero_bind(self.plan, r, [t.data_ptr() for t in st["master"]],
+                      [t.data_ptr() for t in st["m"]], [t.data_ptr() for t in st["v"]],
+                      sh.data_ptr() if sh is not None else None,
+                      self.full16.data_ptr() if self.full16 is not None else None,
+                      self.workspace.data_ptr())
+
+    # ------------------------------------------------------------------ layout helpers
+    def shard_slices(self, rank: int):
+        """(unit, physical offset, length, unit base, unit shard size) of the rank's shard."""
+        out = []
+        for u, (first, count, numel, numel_pad, shard, base, shard_base) in enumerate(self.units):
+            out.append((u, self.phys_off[rank][u], shard, base, shard))
+        return out
+
+    def bind_peer_shard(self, rank: int) -> torch.Tensor:
+        """Stage 3: allocate and register the 16-bit shard of a rank without local state."""
+        n = zero_rank_state_elems(self.plan, rank)
+        sh = torch.zeros(n, dtype=torch.int16, device=self.device)
+        zero_bind_peer(self.plan, rank, sh.data_ptr())
+        self.shard16[rank] = sh
+        return sh
+
+    def current(self) -> int:
+        return zero_state_cursor(self.plan)[1]
+
+    def t(self) -> int:
+        return zero_state_cursor(self.plan)[0]
+
+    def state_tensor(self, rank: int, name: str) -> torch.Tensor:
+        return self.state[rank][name][self.current()]
+
+    def logical(self, rank: int, phys: torch.Tensor) -> torch.Tensor:
+        """Gather a rank's buffer from the physical layout into logical shard order."""
+        parts = [phys[off:off + n] for (_u, off, n, _b, _s) in self.shard_slices(rank)]
+        return torch.cat(parts) if parts else phys[:0]
+
+    # ------------------------------------------------------------------ the step
+    def step(self, contribs: Sequence[int], which: int, hyper, scaler=None, stream=None) -> None:
+        zero_step(self.plan, list(contribs), which, hyper, scaler, _stream_handle(stream))
+
+    def finish(self, scaler=None, stream=None):
+        return zero_step_finish(self.plan, scaler, _stream_handle(stream))
+
+    def gather(self, unit: int, dst: torch.Tensor, stream=None) -> None:
+        zero_gather_layer(self.plan, unit, dst.data_ptr(), _stream_handle(stream))
+
+    def release(self, unit: int) -> None:
+        zero_release_layer(self.plan, unit)
+
+    def close(self) -> None:
+        if self.plan:
+            zero_plan_destroy(self.plan)
+            self.plan = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
