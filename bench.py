@@ -123,7 +123,7 @@ class Bench:
 
         self.torch, self.Z, self.H, self.synth = torch, Z, H, synth
         self.w = w
-        self.run = H.Run(w)            # plan, state, 16-bit buffers, initial parameters
+        self.run = H.Run(w, alloc_contribs=False)   # plan, state, 16-bit buffers, initial params
         self.g = self.run.g
         self.units = self.run.units
         self.info = self.run.info

@@ -60,7 +60,7 @@ def values_at(stream: synth.Stream, units, idx: np.ndarray) -> np.ndarray:
 class Run:
     """One workload on the GPU through the product API."""
 
-    def __init__(self, w: W.Workload, bound=None, peers: bool = True):
+    def __init__(self, w: W.Workload, bound=None, peers: bool = True, alloc_contribs: bool = True):
         self.w = w
         b = bound if bound is not None else w.ranks()
         self.g = EmulatedGroup(w.sizes, w.n_d, w.stage, w.bucket_elems, w.unit_first or None,
@@ -95,7 +95,7 @@ class Run:
                                    c.growth_interval)
         self.hyper = Z.hyper(w.hyper.lr, w.hyper.beta1, w.hyper.beta2, w.hyper.eps,
                              w.hyper.weight_decay)
-        n_c = int(self.info.max_contrib_elems)
+        n_c = int(self.info.max_contrib_elems) if alloc_contribs else 0
         self.contribs = [torch.empty(max(8, n_c), dtype=torch.int16, device="cuda")
                          for _ in range(w.n_d)]
         self.gather_buf = None
