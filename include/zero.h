@@ -217,6 +217,43 @@ zero_status_t zero_comm_report(const zero_plan_t* plan, zero_comm_report_t* out)
 /* Applied steps so far and the index (0/1) of the current half of each ping-pong pair. */
 zero_status_t zero_state_cursor(const zero_plan_t* plan, int64_t* t, int* current);
 
+/* ---------------------------------------------------------------------------------------
+ * No-allocation variant of the fused step (the pages have no counterpart of this call).
+ *
+ * For callers that cannot allocate device memory themselves: code that runs inside a host
+ * framework which has reserved the GPU's memory for its own pool, or latency-critical loops
+ * that cannot afford cudaMalloc/cudaFree (which may synchronise the whole device).  Such a
+ * caller cannot provide the workspace zero_bind needs.  This call needs no plan and no
+ * workspace: it runs the same fused reduce + AdamW + cast kernel over ONE flat range and keeps
+ * the kernel's scratch (the 4-byte non-finite flag) in a library-owned static device array of
+ * ZERO_NOALLOC_SCRATCH_BYTES bytes.  Every GPU that loads the library holds that array until
+ * the process exits.  The library allocates nothing here: no cudaMalloc, no cudaFree.
+ *
+ *   grad_contribs[n_d]   device pointers, n elements of 16-bit gradient each
+ *   master_in/m_in/v_in  fp32 state read (n elements); not modified
+ *   master_out/m_out/v_out  fp32 state written (n elements); must not alias the inputs
+ *   out16                16-bit parameters written (n elements), even when the flag is set
+ *   t                    1-based index of the step being applied (bias correction)
+ *   loss_scale           gradients are multiplied by 1 / (n_d * loss_scale)
+ *   *nonfinite           receives 1 if any reduced gradient element is inf/nan, else 0
+ * The call is enqueued on `stream` and then synchronises it to read the flag.
+ *
+ * Set-up: the first call on each device looks up the array's device address (with that device
+ * current) and caches it; make that first call before any stream capture.  All calls share
+ * the one array: the flag is cleared at the start of every call, and calls that overlap on
+ * the GPU (different streams, threads or processes sharing the library) race on it.
+ * Limits: n_d <= ZERO_MAX_RANKS (else ZERO_ERANGE); the call uses 4 of the
+ * ZERO_NOALLOC_SCRATCH_BYTES bytes whatever n and n_d are.
+ * --------------------------------------------------------------------------------------- */
+#define ZERO_NOALLOC_SCRATCH_BYTES 256
+
+zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d, int64_t n,
+                                      int dtype16, const float* master_in, const float* m_in,
+                                      const float* v_in, float* master_out, float* m_out,
+                                      float* v_out, void* out16, const zero_hyper_t* hyper,
+                                      int64_t t, double loss_scale, void* stream,
+                                      int32_t* nonfinite);
+
 const char* zero_last_error(void);
 void zero_plan_destroy(zero_plan_t* plan);
 

@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_EALIGN", 3: "ZERO_ECUDA
 EXPORTED = ["zero_plan_create", "zero_plan_info", "zero_rank_state_elems", "zero_plan_tables",
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",
             "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_state_cursor",
-            "zero_last_error", "zero_plan_destroy"]
+            "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
+ZERO_NOALLOC_SCRATCH_BYTES = 256
 
 
 class ZeroError(RuntimeError):
@@ -123,6 +124,10 @@ def lib() -> ctypes.CDLL:
         L.zero_state_cursor.argtypes = [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_int)]
         L.zero_last_error.restype = ctypes.c_char_p
         L.zero_last_error.argtypes = []
+        L.zero_step_range_noalloc.restype = st
+        L.zero_step_range_noalloc.argtypes = [_vp, _int, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              _vp, ctypes.POINTER(zero_hyper_t), _i64,
+                                              ctypes.c_double, _vp, ctypes.POINTER(ctypes.c_int32)]
         L.zero_plan_destroy.restype = None
         L.zero_plan_destroy.argtypes = [_vp]
         _lib = L
@@ -242,6 +247,20 @@ def zero_last_error() -> str:
 def zero_plan_destroy(plan: int) -> None:
     if plan:
         lib().zero_plan_destroy(plan)
+
+
+def zero_step_range_noalloc(grad_contribs: Sequence[int], n: int, dtype16: int, master_in: int,
+                            m_in: int, v_in: int, master_out: int, m_out: int, v_out: int,
+                            out16: int, hyper: zero_hyper_t, t: int, loss_scale: float = 1.0,
+                            stream: int = 0) -> int:
+    """Fused step over one flat range without any workspace; returns the non-finite flag."""
+    flag = ctypes.c_int32(0)
+    _check(lib().zero_step_range_noalloc(_ptr_array(grad_contribs), len(grad_contribs), n, dtype16,
+                                         master_in or None, m_in or None, v_in or None,
+                                         master_out or None, m_out or None, v_out or None,
+                                         out16 or None, ctypes.byref(hyper), t, loss_scale,
+                                         stream or None, ctypes.byref(flag)))
+    return int(flag.value)
 
 
 def hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01) -> zero_hyper_t:

@@ -713,4 +713,160 @@ zero_status_t zero_release_layer(zero_plan_t* p, int64_t unit)
     return ZERO_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// No-allocation variant: the fused step over one flat range with its scratch (the non-finite
+// flag) in a library-owned static device array instead of a caller workspace.
+// ---------------------------------------------------------------------------------------
+
+}  // extern "C"
+
+static __device__ __align__(256) uint32_t g_noalloc_scratch[ZERO_NOALLOC_SCRATCH_BYTES / 4];
+
+namespace zero {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once per device).
+// In host code the array's name is only a host-side handle, never a device address.
+zero_status_t noalloc_scratch(void** out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(ZERO_ERANGE, "zero_step_range_noalloc: device index beyond the supported range");
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return cuda_fail(e, "zero_step_range_noalloc: cudaGetSymbolAddress of the scratch");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return ZERO_OK;
+}
+
+template <int DT>
+cudaError_t noalloc_launch(StepParams& P, bool vec, int dev, cudaStream_t st)
+{
+    int64_t acc = 0;
+    KSeg& K = P.seg[0];
+    if (!vec) {
+        K.head = 0;
+        K.tail = 0;
+        K.nvec = K.n;
+    }
+    K.vbeg = 0;
+    acc = K.nvec;
+    P.total_vec = acc;
+    const int64_t work = std::max<int64_t>(acc, (int64_t)kScalarSlots);
+    auto go = [&](auto kernel) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
+            per_sm = 1;
+        const int64_t cap = (int64_t)device_sms(dev) * std::max(per_sm, 1);
+        const int64_t need = std::max<int64_t>(1, (work + kThreads - 1) / kThreads);
+        kernel<<<(int)std::max<int64_t>(1, std::min(cap, need)), kThreads, 0, st>>>(P);
+    };
+    if (!vec) go(fused_step_kernel<DT, 1, 1>);
+    else if (P.n_d <= 4) go(fused_step_kernel<DT, 4, 8>);
+    else if (P.n_d <= 8) go(fused_step_kernel<DT, 8, 8>);
+    else go(fused_step_kernel<DT, 16, 8>);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace zero
+
+extern "C" {
+
+zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d, int64_t n,
+                                      int dtype16, const float* master_in, const float* m_in,
+                                      const float* v_in, float* master_out, float* m_out,
+                                      float* v_out, void* out16, const zero_hyper_t* hyper,
+                                      int64_t t, double loss_scale, void* stream,
+                                      int32_t* nonfinite)
+{
+    static_assert(sizeof(uint32_t) <= ZERO_NOALLOC_SCRATCH_BYTES, "flag must fit the scratch");
+    if (!grad_contribs || !hyper || !nonfinite)
+        return fail(ZERO_EINVAL, "zero_step_range_noalloc: NULL argument");
+    if (n_d < 1) return fail(ZERO_EINVAL, "zero_step_range_noalloc: n_d must be >= 1");
+    if (n_d > ZERO_MAX_RANKS)
+        return fail(ZERO_ERANGE, "zero_step_range_noalloc: n_d exceeds ZERO_MAX_RANKS");
+    if (n < 0) return fail(ZERO_EINVAL, "zero_step_range_noalloc: n < 0");
+    if (dtype16 != ZERO_BF16 && dtype16 != ZERO_FP16)
+        return fail(ZERO_EINVAL, "zero_step_range_noalloc: bad dtype16");
+    if (t < 1) return fail(ZERO_EINVAL, "zero_step_range_noalloc: t must be >= 1");
+    if (!(loss_scale > 0.0) || !std::isfinite(loss_scale))
+        return fail(ZERO_EINVAL, "zero_step_range_noalloc: bad loss scale");
+    const float* fin[3] = {master_in, m_in, v_in};
+    float* fout[3] = {master_out, m_out, v_out};
+    if (n > 0) {
+        for (int i = 0; i < 3; ++i) {
+            if (!fin[i] || !fout[i]) return fail(ZERO_EINVAL, "zero_step_range_noalloc: NULL state");
+            if (fin[i] == fout[i])
+                return fail(ZERO_EINVAL, "zero_step_range_noalloc: output state aliases its input");
+            if (!aligned(fin[i], 4) || !aligned(fout[i], 4))
+                return fail(ZERO_EALIGN, "zero_step_range_noalloc: fp32 state not 4-byte aligned");
+        }
+        if (!out16) return fail(ZERO_EINVAL, "zero_step_range_noalloc: NULL out16");
+        if (!aligned(out16, 2)) return fail(ZERO_EALIGN, "zero_step_range_noalloc: out16 not 2-byte aligned");
+        for (int r = 0; r < n_d; ++r) {
+            if (!grad_contribs[r]) return fail(ZERO_EINVAL, "zero_step_range_noalloc: NULL contribution");
+            if (!aligned(grad_contribs[r], 2))
+                return fail(ZERO_EALIGN, "zero_step_range_noalloc: contribution not 2-byte aligned");
+        }
+    }
+    void* scratch = nullptr;
+    zero_status_t st = noalloc_scratch(&scratch);
+    if (st != ZERO_OK) return st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: cudaGetDevice");
+    cudaStream_t s = (cudaStream_t)stream;
+    e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);   // the flag must start at zero
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: clearing the flag");
+    if (n > 0) {
+        StepParams P;
+        std::memset(&P, 0, sizeof(P));
+        for (int r = 0; r < n_d; ++r) P.c[r] = (const uint16_t*)grad_contribs[r];
+        step_constants(*hyper, t, loss_scale, n_d, P.k);
+        P.n_d = n_d;
+        P.n_seg = 1;
+        P.flag = (uint32_t*)scratch;
+        KSeg& K = P.seg[0];
+        K.p_in = master_in;
+        K.m_in = m_in;
+        K.v_in = v_in;
+        K.p_out = master_out;
+        K.m_out = m_out;
+        K.v_out = v_out;
+        K.out16 = (uint16_t*)out16;
+        K.c_off = 0;
+        K.n = n;
+        const int h = head16(K.out16);
+        bool vec = true;
+        for (int r = 0; r < n_d; ++r) vec &= head16(P.c[r]) == h;
+        const int64_t hh = std::min<int64_t>(h, n);
+        const float* fp[6] = {K.p_in, K.m_in, K.v_in, K.p_out, K.m_out, K.v_out};
+        for (const float* f : fp) vec &= aligned(f + hh, 16);
+        K.head = (int32_t)hh;
+        K.nvec = (n - hh) / 8;
+        K.tail = (int32_t)(n - hh - 8 * K.nvec);
+        e = dtype16 == ZERO_BF16 ? noalloc_launch<ZERO_BF16>(P, vec, dev, s)
+                                 : noalloc_launch<ZERO_FP16>(P, vec, dev, s);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: launch");
+    }
+    uint32_t flag = 0;
+    e = cudaMemcpyAsync(&flag, scratch, sizeof(flag), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: reading the flag");
+    *nonfinite = flag ? 1 : 0;
+    return ZERO_OK;
+}
+
 }  // extern "C"
