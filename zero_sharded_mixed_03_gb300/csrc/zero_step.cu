@@ -27,9 +27,12 @@
 namespace zero {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;  // 128-thread blocks: more registers per thread, more loads in flight
 constexpr int kMaxSegs = 32;      // work items per launch (more are split across launches)
-constexpr int kScalarSlots = 16;  // per segment: up to 7 head + 7 tail elements
+constexpr int kScalarSlots = 16;
+// Contribution slices loaded per batch (128-bit each) before they are summed; four keep the
+// register count at 96 so five 128-thread blocks stay resident per SM for every N_d.
+constexpr int kRankBatch = 4;  // per segment: up to 7 head + 7 tail elements
 constexpr int kWorkspaceBytes = 256;
 
 // ------------------------------------------------------------------ launch parameters
@@ -161,12 +164,12 @@ __device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, 
 template <int DT, int NB>
 __device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, int64_t e)
 {
-    const float4 p0 = __ldg(reinterpret_cast<const float4*>(S.p_in + e));
-    const float4 p1 = __ldg(reinterpret_cast<const float4*>(S.p_in + e) + 1);
-    const float4 m0 = __ldg(reinterpret_cast<const float4*>(S.m_in + e));
-    const float4 m1 = __ldg(reinterpret_cast<const float4*>(S.m_in + e) + 1);
-    const float4 v0 = __ldg(reinterpret_cast<const float4*>(S.v_in + e));
-    const float4 v1 = __ldg(reinterpret_cast<const float4*>(S.v_in + e) + 1);
+    const float4 p0 = __ldcs(reinterpret_cast<const float4*>(S.p_in + e));
+    const float4 p1 = __ldcs(reinterpret_cast<const float4*>(S.p_in + e) + 1);
+    const float4 m0 = __ldcs(reinterpret_cast<const float4*>(S.m_in + e));
+    const float4 m1 = __ldcs(reinterpret_cast<const float4*>(S.m_in + e) + 1);
+    const float4 v0 = __ldcs(reinterpret_cast<const float4*>(S.v_in + e));
+    const float4 v1 = __ldcs(reinterpret_cast<const float4*>(S.v_in + e) + 1);
 
     float acc[8];
 #pragma unroll
@@ -415,16 +418,13 @@ template <int DT>
 zero_status_t launch_fused(const zero_plan* p, StepParams& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
-    const int nd = P.n_d;
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     auto go = [&](auto kernel) {
         const int grid = grid_for(kernel, p->device, work);
         kernel<<<grid, kThreads, 0, st>>>(P);
     };
     if (!vec) go(fused_step_kernel<DT, 1, 1>);
-    else if (nd <= 4) go(fused_step_kernel<DT, 4, 8>);
-    else if (nd <= 8) go(fused_step_kernel<DT, 8, 8>);
-    else go(fused_step_kernel<DT, 16, 8>);
+    else go(fused_step_kernel<DT, kRankBatch, 8>);
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? ZERO_OK : cuda_fail(err, "fused step launch");
 }
@@ -773,9 +773,7 @@ cudaError_t noalloc_launch(StepParams& P, bool vec, int dev, cudaStream_t st)
         kernel<<<(int)std::max<int64_t>(1, std::min(cap, need)), kThreads, 0, st>>>(P);
     };
     if (!vec) go(fused_step_kernel<DT, 1, 1>);
-    else if (P.n_d <= 4) go(fused_step_kernel<DT, 4, 8>);
-    else if (P.n_d <= 8) go(fused_step_kernel<DT, 8, 8>);
-    else go(fused_step_kernel<DT, 16, 8>);
+    else go(fused_step_kernel<DT, kRankBatch, 8>);
     return cudaGetLastError();
 }
 
