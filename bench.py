@@ -26,6 +26,11 @@ METRIC = "ZeRO step params updated/s and achieved HBM GB/s vs GB300 peak (1 GPU)
 UNIT = "params/s"
 DEFAULT_CONFIG = 1
 FALLBACK_HBM_GBS = 6800.0
+# Gradient sets rotated through the timed steps.  A backward pass rewrites the same gradient
+# buffers every step, so a few persistent sets model training; each step still reads inputs
+# it did not read the step before, and every set is far larger than the 129 MB L2.  (Cycling
+# through tens of GB of distinct sets instead measures GPU TLB reach, not the step.)
+ROTATE_SETS = 4
 
 
 def parse_args():
@@ -160,7 +165,7 @@ class Bench:
         for s in range(self.n_sets):
             bufs = [torch.empty(max(8, off), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
             for r in range(w.n_d):
-                st = synth.grad_stream(w, s + 1, r)
+                st = synth.grad_stream(w, s + 1, r, planted=False)   # no skip in the rotation
                 for spans in self.read_spans:
                     for (a, e, o, _rel) in spans:
                         H.fill_device(bufs[r][o:o + (e - a)], st, self.units, a, e)
@@ -169,7 +174,6 @@ class Bench:
         self.elems_per_step = int(self.info.shard) * len(self.bound)
         self.bytes_per_elem = 2 * w.n_d + 26
         self.hyper = self.run.hyper
-        self.scaler = self.run.scaler
 
     def call_ptrs(self, bufs, ci):
         """Per-rank contribution pointers of call ci: base such that base + c_off hits the slice."""
@@ -180,32 +184,35 @@ class Bench:
         # compact slice o holds flat [a, e), which the kernel addresses as call offset `rel`
         return [bufs[r].data_ptr() + 2 * (o - rel) for r in range(self.w.n_d)]
 
-    def step(self, bufs, events=None, gather_events=None):
+    def step(self, bufs, events=None, gather_events=None, wait=False):
+        """Enqueue one step; with wait=True also read the step result back (synchronises).
+
+        events / gather_events: iterators of pre-created (start, end) CUDA event pairs recorded
+        around each fused launch / gather launch.  Returns (result or None, kernel launches).
+        """
         launches = 0
         for ci, (which, lo, hi) in enumerate(self.calls):
             if self.w.stage == 3:
                 if gather_events is not None:
-                    gather_events[0].append(self._event())
+                    a, c = next(gather_events)
+                    a.record()
                 self.g.gather(which, self.run.gather_buf)
                 if gather_events is not None:
-                    gather_events[1].append(self._event())
+                    c.record()
                 self.g.release(which)
                 launches += 1
             if events is not None:
-                events[0].append(self._event())
-            self.g.step(self.call_ptrs(bufs, ci), which, self.hyper, self.scaler)
+                a, c = next(events)
+                a.record()
+            self.g.step(self.call_ptrs(bufs, ci), which, self.hyper)
             if events is not None:
-                events[1].append(self._event())
+                c.record()
             launches += 1
-        res = self.g.finish(self.scaler)
-        if res.skipped:
-            launches += 1
+        res = self.g.finish(wait=wait)
+        # the re-cast kernel(s) (which return at once unless the step was skipped) + the commit
+        n_segs = len(self.bound) * len(self.units)
+        launches += (n_segs + 31) // 32 + 1
         return res, launches
-
-    def _event(self):
-        e = self.torch.cuda.Event(enable_timing=True)
-        e.record()
-        return e
 
 
 def gpu_arm(args, world, rank, local):
@@ -217,7 +224,7 @@ def gpu_arm(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     w = W.workload(args.config)
-    b = Bench(w, args.mem_budget_gb, args.warmup + args.steps)
+    b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps))
     peak, peak_kind = peaks()
 
     for k in range(args.warmup):
@@ -229,10 +236,14 @@ def gpu_arm(args, world, rank, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    ev_fused = ([], [])
-    ev_gather = ([], [])
+    def pairs(n):
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n)]
+    fused_pairs = pairs(args.steps * len(b.calls))
+    gather_pairs = pairs(args.steps * len(b.calls)) if w.stage == 3 else []
+    ev_fused, ev_gather = iter(fused_pairs), iter(gather_pairs)
     launches = 0
-    skipped = 0
+    skipped_before = b.g.step_state().skipped_total
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -240,9 +251,9 @@ def gpu_arm(args, world, rank, local):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record()
     for k in range(args.steps):
-        res, n = b.step(b.sets[(args.warmup + k) % b.n_sets], ev_fused, ev_gather)
+        _, n = b.step(b.sets[(args.warmup + k) % b.n_sets], ev_fused,
+                      ev_gather if w.stage == 3 else None)
         launches += n
-        skipped += res.skipped
     t1.record()
     torch.cuda.synchronize()
     if dist:
@@ -253,8 +264,9 @@ def gpu_arm(args, world, rank, local):
         tt = torch.tensor([ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-    fused_ms = [a.elapsed_time(c) for a, c in zip(*ev_fused)]
-    gather_ms = [a.elapsed_time(c) for a, c in zip(*ev_gather)]
+    skipped = b.g.step_state().skipped_total - skipped_before
+    fused_ms = [a.elapsed_time(c) for a, c in fused_pairs]
+    gather_ms = [a.elapsed_time(c) for a, c in gather_pairs]
 
     applied = args.steps - skipped
     elems = b.elems_per_step
@@ -316,7 +328,7 @@ def e2e_leg(b: Bench, steps: int, world: int, dist):
     for k in range(steps):
         for r in range(b.w.n_d):
             dev[r][:b.set_elems].copy_(host[r], non_blocking=True)
-        res, _ = b.step(dev)          # finish() reads the step result (flag) back to the host
+        res, _ = b.step(dev, wait=True)   # reads the step result back to the host
         applied += 1 - res.skipped
     torch.cuda.synchronize()
     el = time.perf_counter() - t
@@ -325,7 +337,7 @@ def e2e_leg(b: Bench, steps: int, world: int, dist):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         el = float(tt.item())
     return {"value": world * b.elems_per_step * applied / el, "unit": UNIT,
-            "h2d_bytes_per_step": 2 * b.set_elems * b.w.n_d, "d2h_bytes_per_step": 4,
+            "h2d_bytes_per_step": 2 * b.set_elems * b.w.n_d, "d2h_bytes_per_step": 64,
             "steps": steps}
 
 

@@ -24,9 +24,14 @@
  *    (state, contributions, 16-bit buffers, workspace) is owned by the caller
  *    and is never freed by the library.  The library allocates no device memory.
  *  - Calls that take a `stream` (a cudaStream_t passed as void*) are
- *    asynchronous on it, except zero_step_finish, which synchronises it.
+ *    asynchronous on it, except zero_set_scaler, zero_read_state and
+ *    zero_step_finish with a result pointer, which synchronise it.  The skip
+ *    decision, the applied-step count t, the current ping-pong half and the
+ *    loss scale live on the device (in the workspace), so a training loop
+ *    enqueues step after step without waiting for the host.  Issue every call
+ *    of one plan on one stream (or order the streams yourself).
  *  - Device pointers must be aligned to their element size (2 B for 16-bit
- *    data, 4 B for fp32, 8 B for the workspace); otherwise ZERO_EALIGN.  The
+ *    data, 4 B for fp32, 16 B for the workspace); otherwise ZERO_EALIGN.  The
  *    128-bit vector path is used when every base pointer is 16-byte aligned and
  *    every stream of a launch has the same element phase modulo 8 (always true
  *    for the state layout below when bucket_elems is a multiple of 8); other
@@ -63,16 +68,16 @@ typedef struct {
     double lr, beta1, beta2, eps, weight_decay;
 } zero_hyper_t;
 
-/* Dynamic loss scale.  On a step whose reduced gradient holds inf/nan the step
- * is skipped and scale = max(scale * backoff_factor, min_scale); after
- * growth_interval consecutive applied steps scale *= growth_factor. */
+/* Dynamic loss scale (kept on the device once set with zero_set_scaler).  On a step whose
+ * reduced gradient holds inf/nan the step is skipped and scale = max(scale * backoff_factor,
+ * min_scale); after growth_interval consecutive applied steps scale *= growth_factor. */
 typedef struct {
     double scale;
     double growth_factor;
     double backoff_factor;
     double min_scale;
     int64_t growth_interval;
-    int64_t good_steps;      /* applied steps since the last change of scale */
+    int64_t good_steps;      /* applied steps since the last change of scale (initial value) */
 } zero_scaler_t;
 
 typedef struct {
@@ -85,7 +90,8 @@ typedef struct {
     int64_t max_contrib_elems; /* elements every contribution buffer must hold for the largest
                                   bucket (stages 1/2) or unit (stage 3) */
     int64_t max_unit_pad;    /* largest padded unit (stage 3 gather destination length) */
-    int64_t workspace_bytes; /* device workspace the caller provides (zero_bind) */
+    int64_t workspace_bytes; /* device workspace the caller provides (zero_bind): 256 bytes of
+                                step state and a table of Adam bias corrections */
     int32_t n_d;
     int32_t stage;
     int32_t dtype16;
@@ -106,11 +112,15 @@ enum {
                                       rank's state buffers, length (physical layout, see zero_bind) */
 };
 
+/* Device-resident step state, read back by zero_read_state / zero_step_finish. */
 typedef struct {
-    int32_t skipped;         /* 1: a non-finite gradient was seen, the step was not applied */
-    int32_t reserved;
-    int64_t t;               /* applied steps so far (after this step) */
-    double scale;            /* loss scale to use for the next step */
+    int32_t skipped;         /* 1: the last finished step saw inf/nan and was not applied */
+    int32_t current;         /* current half (0/1) of every ping-pong pair */
+    int64_t t;               /* applied steps so far */
+    double scale;            /* loss scale of the next step */
+    int64_t good_steps;      /* applied steps since the last change of scale */
+    int64_t skipped_total;   /* skipped steps so far */
+    int64_t finished;        /* finished steps (applied + skipped) */
 } zero_step_result_t;
 
 /* Per-rank bytes.  logical[s][c]: stage s in (DDP, ZeRO-1, ZeRO-2, ZeRO-3), component c in
@@ -173,9 +183,11 @@ zero_status_t zero_plan_tables(const zero_plan_t* plan, int which, int64_t* dst,
  *   shard16                stage 3: the rank's 16-bit parameter shard; else NULL
  *   full16                 stages 1/2: the flat 16-bit parameter buffer (phi_pad elements),
  *                          shared by every rank (all replicas are identical); else NULL
- *   workspace              device memory of info.workspace_bytes (the non-finite flag);
- *                          plan-wide: every bind must pass the same pointer
- * Synchronously clears the workspace.  Only bound ranks are updated by zero_step. */
+ *   workspace              device memory of info.workspace_bytes, 16-byte aligned: the step
+ *                          state (non-finite flag, current half, t, loss scale) and the bias
+ *                          corrections; plan-wide: every bind must pass the same pointer
+ * The first bind synchronously initialises the workspace (t = 0, half 0 current, scale 1).
+ * Bind every rank before the first step.  Only bound ranks are updated by zero_step. */
 zero_status_t zero_bind(zero_plan_t* plan, int rank, float* const master[2], float* const m[2],
                         float* const v[2], void* shard16, void* full16, void* workspace);
 
@@ -183,25 +195,40 @@ zero_status_t zero_bind(zero_plan_t* plan, int rank, float* const master[2], flo
  * zero_gather_layer can reconstruct full units.  The buffer follows that rank's layout. */
 zero_status_t zero_bind_peer(zero_plan_t* plan, int rank, const void* shard16);
 
+/* Set (cfg != NULL) or disable (cfg == NULL: scale fixed at 1) the dynamic loss scale: writes
+ * cfg->scale and cfg->good_steps into the device state and keeps the growth/back-off settings.
+ * Not inside an open step.  Synchronises `stream`. */
+zero_status_t zero_set_scaler(zero_plan_t* plan, const zero_scaler_t* cfg, void* stream);
+
 /* One fused reduce + AdamW + cast over every bound rank's part of bucket / unit `which`.
  *   grad_contribs[n_contribs]  n_contribs == N_d device pointers; contribution r holds rank r's
  *                              16-bit gradient for the whole range of the bucket (stages 1/2:
  *                              [b*B, min((b+1)*B, phi_pad)); which = -1: all of [0, phi_pad))
- *                              or of the unit (stage 3: phi_pad_u elements, padding zero)
- *   hyper                      AdamW hyperparameters (identical for every call of one step)
- *   scaler                     loss scale to unscale with (NULL: 1); read, not modified
- * A step is the sequence of calls that covers every bucket (or unit) exactly once, ended by
- * zero_step_finish.  New state is written to the non-current half of each ping-pong pair. */
+ *                              or of the unit (stage 3: phi_pad_u elements, padding zero).
+ *                              Only the bound ranks' shard slices are read.
+ *   hyper                      AdamW hyperparameters (identical for every call of one step);
+ *                              betas in [0, 1)
+ * The step index t + 1, the loss scale and the current half are read on the device.  A step
+ * is the sequence of calls that covers every bucket (or unit) exactly once, ended by
+ * zero_step_finish.  New state is written to the non-current half of each ping-pong pair.
+ * The first call with new betas copies a bias-correction table into the workspace. */
 zero_status_t zero_step(zero_plan_t* plan, const void* const* grad_contribs, int64_t n_contribs,
-                        int64_t which, const zero_hyper_t* hyper, const zero_scaler_t* scaler,
-                        void* stream);
+                        int64_t which, const zero_hyper_t* hyper, void* stream);
 
-/* End the step: read the non-finite flag (synchronises `stream`).  Flag clear: the new state
- * becomes current, t += 1.  Flag set: the state is left unchanged and the 16-bit parameters are
- * re-cast from the unchanged master (one extra kernel).  Updates *scaler (if not NULL), clears
- * the flag, and fills *out (may be NULL). */
-zero_status_t zero_step_finish(zero_plan_t* plan, zero_scaler_t* scaler, void* stream,
-                               zero_step_result_t* out);
+/* End the step on the device: a re-cast kernel (which does nothing unless the flag is set)
+ * rewrites the 16-bit parameters of a skipped step from the unchanged master, then a
+ * one-thread commit either makes the new state current (t += 1, loss-scale growth) or keeps
+ * the old one (loss-scale back-off), and clears the flag.  With out == NULL the call only
+ * enqueues this work; with out != NULL it also synchronises `stream` and reads the state. */
+zero_status_t zero_step_finish(zero_plan_t* plan, void* stream, zero_step_result_t* out);
+
+/* Read the device-resident step state (synchronises `stream`). */
+zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_t* out);
+
+/* Overwrite the device-resident step state, e.g. when resuming from a checkpoint whose fp32
+ * master/m/v were saved from the half `in->current` after `in->t` applied steps.  Clears the
+ * non-finite flag.  Not inside an open step.  Synchronises `stream`. */
+zero_status_t zero_restore_state(zero_plan_t* plan, const zero_step_result_t* in, void* stream);
 
 /* Stage 3 all-gather of unit `unit` ("ZeRO-3 / FSDP Layer Execution Lifecycle"): copies the
  * N_d 16-bit shards (bound or peer ranks) into full_unit16 (phi_pad_u elements, padding
@@ -213,9 +240,6 @@ zero_status_t zero_release_layer(zero_plan_t* plan, int64_t unit);
 
 zero_status_t zero_memory_report(const zero_plan_t* plan, zero_mem_report_t* out);
 zero_status_t zero_comm_report(const zero_plan_t* plan, zero_comm_report_t* out);
-
-/* Applied steps so far and the index (0/1) of the current half of each ping-pong pair. */
-zero_status_t zero_state_cursor(const zero_plan_t* plan, int64_t* t, int* current);
 
 /* ---------------------------------------------------------------------------------------
  * No-allocation variant of the fused step (the pages have no counterpart of this call).

@@ -140,11 +140,14 @@ def param_stream(w) -> Stream:
     return Stream(w.wid, KIND_PARAM, 0, 0, w.param_sigma, w.dtype)
 
 
-def grad_stream(w, step: int, rank: int) -> Stream:
-    """Gradient contribution of `rank` at 1-based `step`, over the global flat index space."""
+def grad_stream(w, step: int, rank: int, planted: bool = True) -> Stream:
+    """Gradient contribution of `rank` at 1-based `step`, over the global flat index space.
+
+    planted=False leaves out the workload's planted inf (the values are otherwise identical).
+    """
     from .workloads import KIND_GRAD, INF16
     inj_idx, inj_bits = -1, 0
-    if w.inject is not None and w.inject[0] == step and w.inject[1] == rank:
+    if planted and w.inject is not None and w.inject[0] == step and w.inject[1] == rank:
         inj_idx, inj_bits = w.inject[2], INF16[w.dtype]
     return Stream(w.wid, KIND_GRAD, step, rank, w.grad_sigma, w.dtype, w.outliers, inj_idx,
                   inj_bits)

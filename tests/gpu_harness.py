@@ -93,6 +93,7 @@ class Run:
             c = w.scaler
             self.scaler = Z.scaler(c.init_scale, c.growth_factor, c.backoff_factor, c.min_scale,
                                    c.growth_interval)
+            self.g.set_scaler(self.scaler)
         self.hyper = Z.hyper(w.hyper.lr, w.hyper.beta1, w.hyper.beta2, w.hyper.eps,
                              w.hyper.weight_decay)
         n_c = int(self.info.max_contrib_elems) if alloc_contribs else 0
@@ -121,8 +122,8 @@ class Run:
                 self.g.release(which)
             for r in range(self.w.n_d):
                 fill_device(self.contribs[r], synth.grad_stream(self.w, k, r), self.units, lo, hi)
-            self.g.step([c.data_ptr() for c in self.contribs], which, self.hyper, self.scaler)
-        return self.g.finish(self.scaler)
+            self.g.step([c.data_ptr() for c in self.contribs], which, self.hyper)
+        return self.g.finish()
 
     # ------------------------------------------------------------------ readback
     def locate(self, idx: np.ndarray):

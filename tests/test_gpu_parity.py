@@ -182,7 +182,7 @@ def test_guard_bands_and_layout_gaps_untouched():
                     b[0, G + off:G + off + cnt] = 0.01
                     s16[G + off:G + off + cnt] = 0
             views[r] = [b[j, G:G + n] for j in range(6)]
-        ws = torch.zeros(64, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(Z.zero_plan_info(plan).workspace_bytes // 4, dtype=torch.int32, device="cuda")
         for r in range(n_d):
             v = views[r]
             Z.zero_bind(plan, r, [v[0].data_ptr(), v[1].data_ptr()], [v[2].data_ptr(), v[3].data_ptr()],
@@ -194,8 +194,8 @@ def test_guard_bands_and_layout_gaps_untouched():
             Z.zero_gather_layer(plan, u, gbuf[G:].data_ptr())
             Z.zero_release_layer(plan, u)
             assert (gbuf[:G] == 0x1234).all() and (gbuf[G + U[3]:] == 0x1234).all()
-            Z.zero_step(plan, [c.data_ptr() for c in contribs], u, Z.hyper(), None)
-        res = Z.zero_step_finish(plan, None)
+            Z.zero_step(plan, [c.data_ptr() for c in contribs], u, Z.hyper())
+        res = Z.zero_step_finish(plan)
         assert res.skipped == 0 and res.t == 1
         torch.cuda.synchronize()
         for r in range(n_d):
@@ -229,9 +229,9 @@ def test_misaligned_contributions_take_the_scalar_path():
                     s = torch.empty(c.numel() + 1, dtype=torch.int16, device="cuda")
                     s[1:] = c
                     shifted.append(s)
-                alt.g.step([s[1:].data_ptr() for s in shifted], which, alt.hyper, None)
+                alt.g.step([s[1:].data_ptr() for s in shifted], which, alt.hyper)
                 torch.cuda.synchronize()
-            alt.g.finish(None)
+            alt.g.finish()
         for r in ref.bound:
             a, b = ref.read_logical(r), alt.read_logical(r)
             for key in a:
@@ -270,14 +270,80 @@ def test_step_lifecycle_errors():
 def test_empty_model_step():
     plan = Z.zero_plan_create([], 3, 2, 0, None, Z.ZERO_BF16)
     try:
-        ws = torch.zeros(64, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(Z.zero_plan_info(plan).workspace_bytes // 4, dtype=torch.int32, device="cuda")
         dummy = torch.zeros(8, dtype=torch.float32, device="cuda")
         d2 = torch.zeros(8, dtype=torch.float32, device="cuda")
         f16 = torch.zeros(8, dtype=torch.int16, device="cuda")
         Z.zero_bind(plan, 0, [dummy.data_ptr(), d2.data_ptr()], [dummy.data_ptr() + 4, d2.data_ptr() + 4],
                     [dummy.data_ptr() + 8, d2.data_ptr() + 8], None, f16.data_ptr(), ws.data_ptr())
-        Z.zero_step(plan, [f16.data_ptr()] * 3, -1, Z.hyper(), None)
-        res = Z.zero_step_finish(plan, None)
+        Z.zero_step(plan, [f16.data_ptr()] * 3, -1, Z.hyper())
+        res = Z.zero_step_finish(plan)
         assert res.skipped == 0 and res.t == 1
     finally:
         Z.zero_plan_destroy(plan)
+
+
+# ---------------------------------------------------------------------- device-resident step state
+
+def test_steps_enqueued_without_host_waits():
+    """Five steps (one with a planted inf) enqueued back to back, the commit left on the device:
+    one read-back at the end must match the oracle's state, t, loss scale and skip count."""
+    w = _mk(130, _ragged(13, 30, 6000), 6, 2, steps=5, bucket=9_000, dtype=W.FP16,
+            scaler=W.Scaler(init_scale=4096.0, growth_interval=2), inject=(3, 4, 5_000))
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    try:
+        for k in range(1, w.steps + 1):
+            for which, lo, hi in run.ranges():
+                for r in range(w.n_d):
+                    H.fill_device(run.contribs[r], synth.grad_stream(w, k, r), run.units, lo, hi)
+                run.g.step([c.data_ptr() for c in run.contribs], which, run.hyper)
+            assert run.g.finish(wait=False) is None
+            o.step(k)
+        st = run.g.step_state()
+        assert (st.t, st.scale, st.skipped_total, st.finished) == (o.sc.t, o.sc.scale, 1, 5)
+        assert st.good_steps == o.sc.good
+        _compare_full(run, o, "enqueued")
+    finally:
+        run.close()
+
+
+def test_bias_table_saturates():
+    """beta1 = 0.5, beta2 = 0.6: 1 - beta^t rounds to 1 after ~72 steps; 90 steps cross the
+    end of the table and keep matching the oracle."""
+    w = W.Workload(wid=131, name="sat", sizes=tuple(_ragged(14, 8, 3000)), n_d=3, stage=1,
+                   bucket_elems=0, unit_first=(), dtype=W.BF16, steps=90,
+                   hyper=W.Hyper(beta1=0.5, beta2=0.6), scaler=None)
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    try:
+        for k in range(1, w.steps + 1):
+            res = run.step(k)
+            o.step(k)
+            assert res.t == k
+            if k in (1, 2, 70, 73, 90):
+                _compare_full(run, o, f"saturating table, step {k}")
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("beta2,t0", [(0.999, 40_000), (0.99999, 70_000)])
+def test_restored_state_far_into_training(beta2, t0):
+    """Resume at t0 applied steps with a non-default loss scale.  With beta2 = 0.99999 the
+    bias corrections of t0 + 1 lie beyond the table and are formed on the GPU in double."""
+    w = W.Workload(wid=132, name="resume", sizes=tuple(_ragged(15, 10, 5000)), n_d=4, stage=2,
+                   bucket_elems=6_000, unit_first=(), dtype=W.FP16, steps=2,
+                   hyper=W.Hyper(beta2=beta2), scaler=W.Scaler(init_scale=256.0))
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    try:
+        state = Z.zero_step_result_t(0, 0, t0, 256.0, 5, 0, t0)
+        Z.zero_restore_state(run.g.plan, state)
+        o.sc.t, o.sc.good = t0, 5
+        for k in (1, 2):
+            res = run.step(k)
+            o.step(k)
+            assert (res.t, res.scale) == (o.sc.t, o.sc.scale)
+            _compare_full(run, o, f"restored at t={t0}, step {k}")
+    finally:
+        run.close()

@@ -142,16 +142,16 @@ def test_calls_out_of_order_fail_without_touching_the_gpu():
     plan = _plan_for([10, 20], 3, 2, 8)
     try:
         with pytest.raises(Z.ZeroError) as e:
-            Z.zero_step_finish(plan, None)
+            Z.zero_step_finish(plan)
         assert e.value.status == Z.ZERO_ESTATE
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_gather_layer(plan, 0, 0x1000)
         assert e.value.status == Z.ZERO_EINVAL
         with pytest.raises(Z.ZeroError) as e:     # nothing bound yet
-            Z.zero_step(plan, [0x1000] * 3, 0, Z.hyper(), None)
+            Z.zero_step(plan, [0x1000] * 3, 0, Z.hyper())
         assert e.value.status == Z.ZERO_ESTATE
         with pytest.raises(Z.ZeroError) as e:
-            Z.zero_step(plan, [0x1000] * 2, 0, Z.hyper(), None)
+            Z.zero_step(plan, [0x1000] * 2, 0, Z.hyper())
         assert e.value.status == Z.ZERO_EINVAL
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_bind_peer(plan, 0, 0x1000)

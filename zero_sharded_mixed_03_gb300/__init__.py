@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_EALIGN", 3: "ZERO_ECUDA
 
 EXPORTED = ["zero_plan_create", "zero_plan_info", "zero_rank_state_elems", "zero_plan_tables",
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",
-            "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_state_cursor",
+            "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_set_scaler",
+            "zero_read_state", "zero_restore_state",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
@@ -59,8 +60,10 @@ class zero_plan_info_t(ctypes.Structure):
 
 
 class zero_step_result_t(ctypes.Structure):
-    _fields_ = [("skipped", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("t", ctypes.c_int64), ("scale", ctypes.c_double)]
+    _fields_ = [("skipped", ctypes.c_int32), ("current", ctypes.c_int32),
+                ("t", ctypes.c_int64), ("scale", ctypes.c_double),
+                ("good_steps", ctypes.c_int64), ("skipped_total", ctypes.c_int64),
+                ("finished", ctypes.c_int64)]
 
 
 class zero_mem_report_t(ctypes.Structure):
@@ -107,11 +110,15 @@ def lib() -> ctypes.CDLL:
         L.zero_bind_peer.restype = st
         L.zero_bind_peer.argtypes = [_vp, _int, _vp]
         L.zero_step.restype = st
-        L.zero_step.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t),
-                                ctypes.POINTER(zero_scaler_t), _vp]
+        L.zero_step.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t), _vp]
         L.zero_step_finish.restype = st
-        L.zero_step_finish.argtypes = [_vp, ctypes.POINTER(zero_scaler_t), _vp,
-                                       ctypes.POINTER(zero_step_result_t)]
+        L.zero_step_finish.argtypes = [_vp, _vp, ctypes.POINTER(zero_step_result_t)]
+        L.zero_set_scaler.restype = st
+        L.zero_set_scaler.argtypes = [_vp, ctypes.POINTER(zero_scaler_t), _vp]
+        L.zero_read_state.restype = st
+        L.zero_read_state.argtypes = [_vp, _vp, ctypes.POINTER(zero_step_result_t)]
+        L.zero_restore_state.restype = st
+        L.zero_restore_state.argtypes = [_vp, ctypes.POINTER(zero_step_result_t), _vp]
         L.zero_gather_layer.restype = st
         L.zero_gather_layer.argtypes = [_vp, _i64, _vp, _vp]
         L.zero_release_layer.restype = st
@@ -120,8 +127,6 @@ def lib() -> ctypes.CDLL:
         L.zero_memory_report.argtypes = [_vp, ctypes.POINTER(zero_mem_report_t)]
         L.zero_comm_report.restype = st
         L.zero_comm_report.argtypes = [_vp, ctypes.POINTER(zero_comm_report_t)]
-        L.zero_state_cursor.restype = st
-        L.zero_state_cursor.argtypes = [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_int)]
         L.zero_last_error.restype = ctypes.c_char_p
         L.zero_last_error.argtypes = []
         L.zero_step_range_noalloc.restype = st
@@ -199,17 +204,32 @@ def zero_bind_peer(plan: int, rank: int, shard16: int) -> None:
     _check(lib().zero_bind_peer(plan, rank, shard16 or None))
 
 
+def zero_set_scaler(plan: int, scaler: Optional[zero_scaler_t], stream: int = 0) -> None:
+    _check(lib().zero_set_scaler(plan, ctypes.byref(scaler) if scaler is not None else None,
+                                 stream or None))
+
+
 def zero_step(plan: int, grad_contribs: Sequence[int], which: int, hyper: zero_hyper_t,
-              scaler: Optional[zero_scaler_t], stream: int = 0) -> None:
+              stream: int = 0) -> None:
     _check(lib().zero_step(plan, _ptr_array(grad_contribs), len(grad_contribs), which,
-                           ctypes.byref(hyper), ctypes.byref(scaler) if scaler is not None else None,
-                           stream or None))
+                           ctypes.byref(hyper), stream or None))
 
 
-def zero_step_finish(plan: int, scaler: Optional[zero_scaler_t], stream: int = 0) -> zero_step_result_t:
+def zero_step_finish(plan: int, stream: int = 0, wait: bool = True) -> Optional[zero_step_result_t]:
+    """Enqueue the commit; with wait=True also read back the step state (synchronises)."""
+    res = zero_step_result_t() if wait else None
+    _check(lib().zero_step_finish(plan, stream or None,
+                                  ctypes.byref(res) if res is not None else None))
+    return res
+
+
+def zero_restore_state(plan: int, state: zero_step_result_t, stream: int = 0) -> None:
+    _check(lib().zero_restore_state(plan, ctypes.byref(state), stream or None))
+
+
+def zero_read_state(plan: int, stream: int = 0) -> zero_step_result_t:
     res = zero_step_result_t()
-    _check(lib().zero_step_finish(plan, ctypes.byref(scaler) if scaler is not None else None,
-                                  stream or None, ctypes.byref(res)))
+    _check(lib().zero_read_state(plan, stream or None, ctypes.byref(res)))
     return res
 
 
@@ -231,12 +251,6 @@ def zero_comm_report(plan: int) -> zero_comm_report_t:
     rep = zero_comm_report_t()
     _check(lib().zero_comm_report(plan, ctypes.byref(rep)))
     return rep
-
-
-def zero_state_cursor(plan: int):
-    t, cur = _i64(), _int()
-    _check(lib().zero_state_cursor(plan, ctypes.byref(t), ctypes.byref(cur)))
-    return int(t.value), int(cur.value)
 
 
 def zero_last_error() -> str:

@@ -46,6 +46,12 @@ struct Segment {
     uint16_t* out16;
 };
 
+// Workspace layout: 256 bytes of device-resident step state, then the bias-correction
+// table, entry t (t >= 1) = (1 - beta1^t, sqrt(1 - beta2^t)) in double.
+constexpr int64_t kStateBytes = 256;
+constexpr int64_t kBiasCap = 1 << 16;
+constexpr int64_t kWorkspaceBytes = kStateBytes + 16 * (kBiasCap + 1);
+
 }  // namespace zero
 
 struct zero_plan {
@@ -71,14 +77,19 @@ struct zero_plan {
     uint32_t* workspace = nullptr;
     int device = -1;
 
-    // Step state.
-    int64_t t = 0;                      // applied steps
-    int cur = 0;                        // current half of the ping-pong pairs
+    // Host side of the step lifecycle (the applied-step count, the current ping-pong half
+    // and the loss scale live on the device, in the workspace).
     bool in_step = false;
+    bool stepped = false;               // a step has been enqueued since the plan was bound
     std::vector<char> covered;          // per bucket / unit in the open step
-    float consts[9] = {0};              // fp32 step constants of the open step
-    double step_scale = 1.0;
+    float consts[9] = {0};              // fp32 constants that do not depend on t or the scale
     zero_hyper_t step_hyper = {0, 0, 0, 0, 0};
+    zero_scaler_t scaler = {1.0, 1.0, 1.0, 1.0, 0, 0};
+    int scaler_dynamic = 0;
+    std::vector<double> bias_host;      // the table last copied into the workspace
+    int64_t bias_len = 0;
+    int bias_saturates = 0;
+    double bias_beta1 = -1.0, bias_beta2 = -1.0;
     std::vector<char> gathered;         // stage 3: per unit
 };
 

@@ -222,7 +222,7 @@ zero_status_t zero_plan_info(const zero_plan_t* p, zero_plan_info_t* out)
     }
     out->max_contrib_elems = maxc;
     out->max_unit_pad = maxu;
-    out->workspace_bytes = 256;
+    out->workspace_bytes = kWorkspaceBytes;
     out->n_d = p->n_d;
     out->stage = p->stage;
     out->dtype16 = p->dtype16;
@@ -365,14 +365,6 @@ zero_status_t zero_comm_report(const zero_plan_t* p, zero_comm_report_t* out)
     out->bytes_per_elem = 2;
     out->collectives_per_step =
         p->stage == 3 ? 3 * (int64_t)p->units.size() : 2 * p->n_buckets;
-    return ZERO_OK;
-}
-
-zero_status_t zero_state_cursor(const zero_plan_t* p, int64_t* t, int* current)
-{
-    if (!p) return fail(ZERO_EINVAL, "zero_state_cursor: NULL plan");
-    if (t) *t = p->t;
-    if (current) *current = p->cur;
     return ZERO_OK;
 }
 

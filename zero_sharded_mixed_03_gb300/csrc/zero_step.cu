@@ -1,6 +1,6 @@
 // zero_step.cu -- device side of the sharded mixed-precision AdamW step for
-// GB300 (sm_103a): bind, the fused reduce + AdamW + cast kernel, commit/skip,
-// the skip re-cast and the stage-3 gather.
+// GB300 (sm_103a): bind, the fused reduce + AdamW + cast kernel, the device-side
+// commit/skip, the skip re-cast and the stage-3 gather.
 //
 // Page: "Zero Redundancy Optimizer (ZeRO) and Fully Sharded Data Parallelism
 // (FSDP): Mathematical Foundations ..." (llms.blog):
@@ -12,7 +12,10 @@
 // The path is elementwise plus a reduction over N_d ranks: about 15 flops per
 // parameter against 2*N_d + 26 bytes, far below any tensor-core ridge, so it
 // is written for HBM bandwidth: 128-bit loads/stores, one pass, fp32 state
-// double-buffered so the global skip decision needs no second pass.
+// double-buffered so the global skip decision needs no second pass.  The
+// decision itself stays on the GPU: the current half of every ping-pong pair,
+// the applied-step count t and the loss scale live in the caller's workspace,
+// so consecutive steps are enqueued back to back with no host round trip.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -27,40 +30,69 @@
 namespace zero {
 namespace {
 
-constexpr int kThreads = 128;  // 128-thread blocks: more registers per thread, more loads in flight
+constexpr int kThreads = 128;     // 128-thread blocks: 70 registers, 7 blocks resident per SM
 constexpr int kMaxSegs = 32;      // work items per launch (more are split across launches)
-constexpr int kScalarSlots = 16;
-// Contribution slices loaded per batch (128-bit each) before they are summed; four keep the
-// register count at 96 so five 128-thread blocks stay resident per SM for every N_d.
-constexpr int kRankBatch = 4;  // per segment: up to 7 head + 7 tail elements
-constexpr int kWorkspaceBytes = 256;
+constexpr int kScalarSlots = 16;  // per segment: up to 7 head + 7 tail elements
+// Contribution slices loaded (128-bit each) per batch before they are summed.
+constexpr int kRankBatch = 4;
+
+// ------------------------------------------------------------------ device-resident step state
+
+// First 64 bytes of the workspace.  Written only by commit_kernel (and by the host before
+// the first step); read by the step and re-cast kernels of the following step.
+struct DevState {
+    uint32_t flag;          // OR of the non-finite flags of the open step
+    uint32_t cur;           // current half of every ping-pong pair
+    uint32_t last_skipped;  // 1 if the last finished step was skipped
+    uint32_t pad0;
+    int64_t t;              // applied steps
+    int64_t skipped;        // skipped steps, total
+    int64_t good;           // applied steps since the last change of the loss scale
+    int64_t finished;       // finished steps (applied + skipped)
+    double scale;           // loss scale of the next step
+    int64_t pad1;
+};
+static_assert(sizeof(DevState) == 64, "DevState layout");
+
+static_assert(sizeof(DevState) <= kStateBytes, "DevState fits its workspace slot");
 
 // ------------------------------------------------------------------ launch parameters
 
 struct KSeg {
-    const float* p_in;
-    const float* m_in;
-    const float* v_in;
-    float* p_out;
-    float* m_out;
-    float* v_out;
+    float* p[2];       // master, both halves, at the segment start
+    float* m[2];
+    float* v[2];
     uint16_t* out16;
-    int64_t c_off;   // element offset into every contribution buffer
-    int64_t n;       // elements
-    int64_t nvec;    // aligned vectors in the body
-    int64_t vbeg;    // index of the first body vector in the launch
-    int32_t head;    // scalar elements before the body
-    int32_t tail;    // scalar elements after the body
+    int64_t c_off;     // element offset into every contribution buffer
+    int64_t n;         // elements
+    int64_t nvec;      // aligned vectors in the body
+    int64_t vbeg;      // index of the first body vector in the launch
+    int32_t head;      // scalar elements before the body
+    int32_t tail;      // scalar elements after the body
 };
 
 struct StepParams {
     const uint16_t* c[ZERO_MAX_RANKS];
     KSeg seg[kMaxSegs];
-    float k[9];       // b1, 1-b1, b2, 1-b2, eps, lr*wd, lr/bc1, sqrt(bc2), inv
-    int n_d;
-    int n_seg;
+    float k[9];        // b1, 1-b1, b2, 1-b2, eps, lr*wd, lr/bc1, sqrt(bc2), inv
+    double lr;         // device mode: lr/bc1 is formed on the GPU from the table
+    double beta1, beta2;
+    const double* bias;        // device mode: bias-correction table (pairs)
+    int64_t bias_len;          // entries 1..bias_len are valid
+    int32_t bias_saturates;    // entries beyond bias_len equal entry bias_len
+    int32_t n_d;
+    int32_t n_seg;
+    int32_t pad;
     int64_t total_vec;
     uint32_t* flag;
+    const DevState* st;        // nullptr: host mode (constants in k, current half 0)
+};
+
+struct CommitParams {
+    DevState* st;
+    double growth, backoff, min_scale;
+    int64_t interval;
+    int32_t dynamic;           // 0: fixed loss scale (no back-off, no growth)
 };
 
 struct CopySeg {
@@ -125,16 +157,25 @@ __device__ __forceinline__ bool nonfinite(float g)
     return (__float_as_uint(g) & 0x7F800000u) == 0x7F800000u;
 }
 
+// The three constants that depend on t and the loss scale, formed per block.
+struct StepK {
+    float step;   // lr / (1 - beta1^t)
+    float bc2s;   // sqrt(1 - beta2^t)
+    float inv;    // 1 / (N_d * loss_scale)
+};
+
 // AdamW on one element with separately rounded IEEE operations (no contraction):
 //   m = b1 m + (1-b1) g ; v = b2 v + (1-b2) g^2 ; d = sqrt(v)/sqrt(bc2) + eps
 //   p = p - (lr wd) p   ; p = p - (lr/bc1) (m / d)
-__device__ __forceinline__ void adamw1(float g, float& p, float& m, float& v, const float* k)
+// k[0..5] (b1, 1-b1, b2, 1-b2, eps, lr*wd) stay in the kernel parameters.
+__device__ __forceinline__ void adamw1(float g, float& p, float& m, float& v, const float* k,
+                                       const StepK& sk)
 {
     m = __fadd_rn(__fmul_rn(k[0], m), __fmul_rn(k[1], g));
     v = __fadd_rn(__fmul_rn(k[2], v), __fmul_rn(k[3], __fmul_rn(g, g)));
-    const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), k[7]), k[4]);
+    const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), sk.bc2s), k[4]);
     p = __fsub_rn(p, __fmul_rn(k[5], p));
-    p = __fsub_rn(p, __fmul_rn(k[6], __fdiv_rn(m, d)));
+    p = __fsub_rn(p, __fmul_rn(sk.step, __fdiv_rn(m, d)));
 }
 
 __device__ __forceinline__ uint4 ld_stream(const void* p)
@@ -142,19 +183,52 @@ __device__ __forceinline__ uint4 ld_stream(const void* p)
     return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
+// The step's fp32 constants and the current half, formed once per block by thread 0.
+// Device mode: t and the loss scale come from the workspace; the fp32 roundings of
+// lr/bc1, sqrt(bc2) and 1/(N_d*scale) are the same IEEE double operations the host uses.
+__device__ __forceinline__ void block_constants(const StepParams& P, float* sk, int* scur)
+{
+    if (threadIdx.x == 0) {
+        sk[0] = P.k[6];
+        sk[1] = P.k[7];
+        sk[2] = P.k[8];
+        int cur = 0;
+        if (P.st) {
+            const volatile DevState* st = P.st;
+            const int64_t t = st->t + 1;   // the step being applied
+            double bc1, bc2s;
+            if (t <= P.bias_len || P.bias_saturates) {
+                const int64_t i = t <= P.bias_len ? t : P.bias_len;
+                bc1 = P.bias[2 * i];
+                bc2s = P.bias[2 * i + 1];
+            } else {
+                bc1 = __dsub_rn(1.0, pow(P.beta1, (double)t));
+                bc2s = __dsqrt_rn(__dsub_rn(1.0, pow(P.beta2, (double)t)));
+            }
+            sk[0] = __double2float_rn(__ddiv_rn(P.lr, bc1));
+            sk[1] = __double2float_rn(bc2s);
+            sk[2] = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)P.n_d, st->scale)));
+            cur = (int)st->cur;
+        }
+        *scur = cur;
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------------ fused step kernel
 
 template <int DT>
-__device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, int64_t e)
+__device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, int64_t e,
+                                            const StepK& sk, int cur)
 {
     float sum = 0.0f;
     for (int r = 0; r < P.n_d; ++r) sum = __fadd_rn(sum, widen1<DT>(P.c[r][S.c_off + e]));
-    const float g = __fmul_rn(sum, P.k[8]);
-    float p = S.p_in[e], m = S.m_in[e], v = S.v_in[e];
-    adamw1(g, p, m, v, P.k);
-    S.p_out[e] = p;
-    S.m_out[e] = m;
-    S.v_out[e] = v;
+    const float g = __fmul_rn(sum, sk.inv);
+    float p = S.p[cur][e], m = S.m[cur][e], v = S.v[cur][e];
+    adamw1(g, p, m, v, P.k, sk);
+    S.p[cur ^ 1][e] = p;
+    S.m[cur ^ 1][e] = m;
+    S.v[cur ^ 1][e] = v;
     S.out16[e] = narrow1<DT>(p);
     return nonfinite(g);
 }
@@ -162,14 +236,18 @@ __device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, 
 // Eight consecutive elements starting at e: 128-bit loads of the N_d contribution slices
 // (batches of NB ranks in flight), 2 x 128-bit per fp32 state array, 128-bit 16-bit store.
 template <int DT, int NB>
-__device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, int64_t e)
+__device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, int64_t e,
+                                          const StepK& sk, int cur)
 {
-    const float4 p0 = __ldcs(reinterpret_cast<const float4*>(S.p_in + e));
-    const float4 p1 = __ldcs(reinterpret_cast<const float4*>(S.p_in + e) + 1);
-    const float4 m0 = __ldcs(reinterpret_cast<const float4*>(S.m_in + e));
-    const float4 m1 = __ldcs(reinterpret_cast<const float4*>(S.m_in + e) + 1);
-    const float4 v0 = __ldcs(reinterpret_cast<const float4*>(S.v_in + e));
-    const float4 v1 = __ldcs(reinterpret_cast<const float4*>(S.v_in + e) + 1);
+    const float* pin = S.p[cur] + e;
+    const float* min_ = S.m[cur] + e;
+    const float* vin = S.v[cur] + e;
+    const float4 p0 = __ldcs(reinterpret_cast<const float4*>(pin));
+    const float4 p1 = __ldcs(reinterpret_cast<const float4*>(pin) + 1);
+    const float4 m0 = __ldcs(reinterpret_cast<const float4*>(min_));
+    const float4 m1 = __ldcs(reinterpret_cast<const float4*>(min_) + 1);
+    const float4 v0 = __ldcs(reinterpret_cast<const float4*>(vin));
+    const float4 v1 = __ldcs(reinterpret_cast<const float4*>(vin) + 1);
 
     float acc[8];
 #pragma unroll
@@ -200,16 +278,19 @@ __device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, in
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float g = __fmul_rn(acc[j], P.k[8]);
+        const float g = __fmul_rn(acc[j], sk.inv);
         bad |= nonfinite(g);
-        adamw1(g, p[j], m[j], v[j], P.k);
+        adamw1(g, p[j], m[j], v[j], P.k, sk);
     }
-    __stcs(reinterpret_cast<float4*>(S.p_out + e), make_float4(p[0], p[1], p[2], p[3]));
-    __stcs(reinterpret_cast<float4*>(S.p_out + e) + 1, make_float4(p[4], p[5], p[6], p[7]));
-    __stcs(reinterpret_cast<float4*>(S.m_out + e), make_float4(m[0], m[1], m[2], m[3]));
-    __stcs(reinterpret_cast<float4*>(S.m_out + e) + 1, make_float4(m[4], m[5], m[6], m[7]));
-    __stcs(reinterpret_cast<float4*>(S.v_out + e), make_float4(v[0], v[1], v[2], v[3]));
-    __stcs(reinterpret_cast<float4*>(S.v_out + e) + 1, make_float4(v[4], v[5], v[6], v[7]));
+    float4* pout = reinterpret_cast<float4*>(S.p[cur ^ 1] + e);
+    float4* mout = reinterpret_cast<float4*>(S.m[cur ^ 1] + e);
+    float4* vout = reinterpret_cast<float4*>(S.v[cur ^ 1] + e);
+    __stcs(pout, make_float4(p[0], p[1], p[2], p[3]));
+    __stcs(pout + 1, make_float4(p[4], p[5], p[6], p[7]));
+    __stcs(mout, make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(mout + 1, make_float4(m[4], m[5], m[6], m[7]));
+    __stcs(vout, make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(vout + 1, make_float4(v[4], v[5], v[6], v[7]));
     uint4 o;
     o.x = narrow2<DT>(p[0], p[1]);
     o.y = narrow2<DT>(p[2], p[3]);
@@ -222,9 +303,15 @@ __device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, in
 // Persistent grid-stride kernel over the concatenated body vectors of all segments, plus
 // kScalarSlots scalar slots per segment for the unaligned head and tail.  VEC = 8: 128-bit
 // body; VEC = 1: every element is a body vector of one (streams of different phases).
+// Reads the current half of each pair and writes the other.
 template <int DT, int NB, int VEC>
 __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_constant__ StepParams P)
 {
+    __shared__ float sk3[3];
+    __shared__ int scur;
+    block_constants(P, sk3, &scur);
+    const StepK sk = {sk3[0], sk3[1], sk3[2]};
+    const int cur = scur;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     bool bad = false;
@@ -236,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
             int64_t e = -1;
             if (k < S.head) e = k;
             else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
-            if (e >= 0) bad |= step_scalar<DT>(P, S, e);
+            if (e >= 0) bad |= step_scalar<DT>(P, S, e, sk, cur);
         }
     }
 
@@ -244,19 +331,31 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
     for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
         while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
         const KSeg& S = P.seg[s];
-        if constexpr (VEC == 8) bad |= step_vec8<DT, NB>(P, S, S.head + 8 * (vi - S.vbeg));
-        else bad |= step_scalar<DT>(P, S, vi - S.vbeg);
+        if constexpr (VEC == 8) bad |= step_vec8<DT, NB>(P, S, S.head + 8 * (vi - S.vbeg), sk, cur);
+        else bad |= step_scalar<DT>(P, S, vi - S.vbeg, sk, cur);
     }
 
     // Global non-finite flag: one OR across the block, one atomic per block that saw one.
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(P.flag, 1u);
 }
 
-// ------------------------------------------------------------------ re-cast kernel (skip)
+// ------------------------------------------------------------------ skip: re-cast + commit
 
+// On a flagged step the fused kernels have already written 16-bit values of the rejected
+// update; rewrite them from the unchanged current master.  Every block returns at once when
+// the flag is clear (the usual case), so the launch costs a few microseconds.
 template <int DT, int VEC>
 __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant__ StepParams P)
 {
+    __shared__ int go, scur;
+    if (threadIdx.x == 0) {
+        const volatile DevState* st = P.st;
+        go = st->flag != 0;
+        scur = (int)st->cur;
+    }
+    __syncthreads();
+    if (!go) return;
+    const int cur = scur;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     if constexpr (VEC == 8) {
@@ -266,7 +365,7 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
             int64_t e = -1;
             if (k < S.head) e = k;
             else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
-            if (e >= 0) S.out16[e] = narrow1<DT>(S.p_in[e]);
+            if (e >= 0) S.out16[e] = narrow1<DT>(S.p[cur][e]);
         }
     }
     int s = 0;
@@ -275,8 +374,8 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
         const KSeg& S = P.seg[s];
         if constexpr (VEC == 8) {
             const int64_t e = S.head + 8 * (vi - S.vbeg);
-            const float4 a = __ldcs(reinterpret_cast<const float4*>(S.p_in + e));
-            const float4 b = __ldcs(reinterpret_cast<const float4*>(S.p_in + e) + 1);
+            const float4 a = __ldcs(reinterpret_cast<const float4*>(S.p[cur] + e));
+            const float4 b = __ldcs(reinterpret_cast<const float4*>(S.p[cur] + e) + 1);
             uint4 o;
             o.x = narrow2<DT>(a.x, a.y);
             o.y = narrow2<DT>(a.z, a.w);
@@ -285,9 +384,38 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
             __stcs(reinterpret_cast<uint4*>(S.out16 + e), o);
         } else {
             const int64_t e = vi - S.vbeg;
-            S.out16[e] = narrow1<DT>(S.p_in[e]);
+            S.out16[e] = narrow1<DT>(S.p[cur][e]);
         }
     }
+}
+
+// Close the step on the device: flag clear -> flip the current half, t += 1, count a clean
+// step and grow the scale after `interval` of them; flag set -> keep the state, back the
+// scale off (not below min_scale).  Then clear the flag for the next step.
+__global__ void commit_kernel(const CommitParams C)
+{
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    volatile DevState* st = C.st;
+    if (st->flag) {
+        st->last_skipped = 1;
+        st->skipped = st->skipped + 1;
+        if (C.dynamic) {
+            const double s = st->scale * C.backoff;
+            st->scale = s < C.min_scale ? C.min_scale : s;
+        }
+        st->good = 0;
+    } else {
+        st->last_skipped = 0;
+        st->cur = st->cur ^ 1u;
+        st->t = st->t + 1;
+        st->good = st->good + 1;
+        if (C.dynamic && C.interval > 0 && st->good >= C.interval) {
+            st->scale = st->scale * C.growth;
+            st->good = 0;
+        }
+    }
+    st->finished = st->finished + 1;
+    st->flag = 0;
 }
 
 // ------------------------------------------------------------------ gather kernel (stage 3)
@@ -328,11 +456,6 @@ inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0
 // Elements before the first 16-byte boundary of a 16-bit stream starting at p.
 inline int head16(const void* p) { return (int)(((16 - ((uintptr_t)p % 16)) % 16) / 2); }
 
-struct DeviceProps {
-    int sms = 0;
-    int blocks_per_sm = 0;
-};
-
 int device_sms(int dev)
 {
     static std::mutex mu;
@@ -347,14 +470,24 @@ int device_sms(int dev)
     return cache[dev];
 }
 
+// Resident blocks per SM of one kernel (queried once per kernel).
+template <typename K>
+int blocks_per_sm(K kernel)
+{
+    static int cached = 0;
+    if (cached == 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
+            per_sm = 1;
+        cached = std::max(per_sm, 1);
+    }
+    return cached;
+}
+
 template <typename K>
 int grid_for(K kernel, int dev, int64_t work)
 {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
-        per_sm = 1;
-    per_sm = std::max(per_sm, 1);
-    const int64_t cap = (int64_t)device_sms(dev) * per_sm;
+    const int64_t cap = (int64_t)device_sms(dev) * blocks_per_sm(kernel);
     const int64_t need = std::max<int64_t>(1, (work + kThreads - 1) / kThreads);
     return (int)std::max<int64_t>(1, std::min(cap, need));
 }
@@ -364,10 +497,16 @@ zero_status_t cuda_fail(cudaError_t e, const char* what)
     return fail(ZERO_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+DevState* dev_state(const zero_plan* p) { return reinterpret_cast<DevState*>(p->workspace); }
+const double* bias_table(const zero_plan* p)
+{
+    return reinterpret_cast<const double*>(reinterpret_cast<const char*>(p->workspace) + kStateBytes);
+}
+
 // Fill one launch's KSeg list from plan segments [b, e), deciding the vector path.
 // Returns true when every stream of every segment shares one 16-byte phase.
 bool build_step_params(const zero_plan* p, const std::vector<Segment>& segs, size_t b, size_t e,
-                       const void* const* contribs, int in_half, StepParams& P)
+                       const void* const* contribs, StepParams& P)
 {
     bool vec_ok = true;
     P.n_seg = (int)(e - b);
@@ -375,22 +514,21 @@ bool build_step_params(const zero_plan* p, const std::vector<Segment>& segs, siz
         const Segment& sg = segs[i];
         const Rank& R = p->ranks[(size_t)sg.rank];
         KSeg& K = P.seg[i - b];
-        K.p_in = R.master[in_half] + sg.s_off;
-        K.m_in = R.m[in_half] + sg.s_off;
-        K.v_in = R.v[in_half] + sg.s_off;
-        K.p_out = R.master[in_half ^ 1] + sg.s_off;
-        K.m_out = R.m[in_half ^ 1] + sg.s_off;
-        K.v_out = R.v[in_half ^ 1] + sg.s_off;
+        for (int h = 0; h < 2; ++h) {
+            K.p[h] = R.master[h] + sg.s_off;
+            K.m[h] = R.m[h] + sg.s_off;
+            K.v[h] = R.v[h] + sg.s_off;
+        }
         K.out16 = sg.out16 + sg.o_off;
         K.c_off = sg.c_off;
         K.n = sg.n;
-        const int h = head16(K.out16);
+        const int hd = head16(K.out16);
         if (contribs)
             for (int r = 0; r < p->n_d; ++r)
-                vec_ok &= head16((const uint16_t*)contribs[r] + sg.c_off) == h;
-        const int64_t hh = std::min<int64_t>(h, sg.n);
-        const float* fp[6] = {K.p_in, K.m_in, K.v_in, K.p_out, K.m_out, K.v_out};
-        for (const float* f : fp) vec_ok &= aligned(f + hh, 16);
+                vec_ok &= head16((const uint16_t*)contribs[r] + sg.c_off) == hd;
+        const int64_t hh = std::min<int64_t>(hd, sg.n);
+        for (int h = 0; h < 2; ++h)
+            vec_ok &= aligned(K.p[h] + hh, 16) && aligned(K.m[h] + hh, 16) && aligned(K.v[h] + hh, 16);
         K.head = (int32_t)hh;
         K.nvec = (sg.n - hh) / 8;
         K.tail = (int32_t)(sg.n - hh - 8 * K.nvec);
@@ -415,32 +553,26 @@ void finalize_vectors(StepParams& P, bool vec)
 }
 
 template <int DT>
-zero_status_t launch_fused(const zero_plan* p, StepParams& P, bool vec, cudaStream_t st)
+cudaError_t launch_fused(int dev, StepParams& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
-    auto go = [&](auto kernel) {
-        const int grid = grid_for(kernel, p->device, work);
-        kernel<<<grid, kThreads, 0, st>>>(P);
-    };
-    if (!vec) go(fused_step_kernel<DT, 1, 1>);
-    else go(fused_step_kernel<DT, kRankBatch, 8>);
-    const cudaError_t err = cudaGetLastError();
-    return err == cudaSuccess ? ZERO_OK : cuda_fail(err, "fused step launch");
+    if (!vec)
+        fused_step_kernel<DT, 1, 1><<<grid_for(fused_step_kernel<DT, 1, 1>, dev, work), kThreads, 0, st>>>(P);
+    else
+        fused_step_kernel<DT, kRankBatch, 8>
+            <<<grid_for(fused_step_kernel<DT, kRankBatch, 8>, dev, work), kThreads, 0, st>>>(P);
+    return cudaGetLastError();
 }
 
 template <int DT>
-zero_status_t launch_recast(const zero_plan* p, StepParams& P, bool vec, cudaStream_t st)
+cudaError_t launch_recast(int dev, StepParams& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
-    if (vec) {
-        recast_kernel<DT, 8><<<grid_for(recast_kernel<DT, 8>, p->device, work), kThreads, 0, st>>>(P);
-    } else {
-        recast_kernel<DT, 1><<<grid_for(recast_kernel<DT, 1>, p->device, work), kThreads, 0, st>>>(P);
-    }
-    const cudaError_t err = cudaGetLastError();
-    return err == cudaSuccess ? ZERO_OK : cuda_fail(err, "re-cast launch");
+    if (vec) recast_kernel<DT, 8><<<grid_for(recast_kernel<DT, 8>, dev, work), kThreads, 0, st>>>(P);
+    else recast_kernel<DT, 1><<<grid_for(recast_kernel<DT, 1>, dev, work), kThreads, 0, st>>>(P);
+    return cudaGetLastError();
 }
 
 zero_status_t set_device(const zero_plan* p)
@@ -452,6 +584,54 @@ zero_status_t set_device(const zero_plan* p)
         e = cudaSetDevice(p->device);
         if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
     }
+    return ZERO_OK;
+}
+
+// (Re)build the bias-correction table for (beta1, beta2) and copy it into the workspace.
+// Entries run until 1 - beta^t rounds to 1 for both betas (then the table saturates) or
+// until kBiasCap entries; beyond a non-saturated table the kernel computes the powers itself.
+zero_status_t upload_bias_table(zero_plan* p, double beta1, double beta2, cudaStream_t s)
+{
+    std::vector<double>& tab = p->bias_host;
+    tab.assign(2, 0.0);
+    int64_t len = 0;
+    bool sat = false;
+    for (int64_t t = 1; t <= kBiasCap; ++t) {
+        const double bc1 = 1.0 - std::pow(beta1, (double)t);
+        const double bc2 = 1.0 - std::pow(beta2, (double)t);
+        tab.push_back(bc1);
+        tab.push_back(std::sqrt(bc2));
+        len = t;
+        if (bc1 == 1.0 && bc2 == 1.0) {
+            sat = true;
+            break;
+        }
+    }
+    const cudaError_t e = cudaMemcpyAsync(reinterpret_cast<char*>(p->workspace) + kStateBytes,
+                                          tab.data(), tab.size() * sizeof(double),
+                                          cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "uploading the bias-correction table");
+    p->bias_len = len;
+    p->bias_saturates = sat ? 1 : 0;
+    p->bias_beta1 = beta1;
+    p->bias_beta2 = beta2;
+    return ZERO_OK;
+}
+
+zero_status_t read_state(zero_plan* p, cudaStream_t s, zero_step_result_t* out)
+{
+    DevState host;
+    cudaError_t e = cudaMemcpyAsync(&host, p->workspace, sizeof(host), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the step state");
+    std::memset(out, 0, sizeof(*out));
+    out->skipped = (int32_t)host.last_skipped;
+    out->current = (int32_t)host.cur;
+    out->t = host.t;
+    out->scale = host.scale;
+    out->good_steps = host.good;
+    out->skipped_total = host.skipped;
+    out->finished = host.finished;
     return ZERO_OK;
 }
 
@@ -467,7 +647,7 @@ zero_status_t zero_bind(zero_plan_t* p, int rank, float* const master[2], float*
 {
     if (!p || !master || !m || !v) return fail(ZERO_EINVAL, "zero_bind: NULL argument");
     if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind: bad rank");
-    if (p->in_step) return fail(ZERO_ESTATE, "zero_bind: a step is open");
+    if (p->in_step || p->stepped) return fail(ZERO_ESTATE, "zero_bind: bind every rank before the first step");
     float* bufs[6] = {master[0], master[1], m[0], m[1], v[0], v[1]};
     const int64_t elems = p->state_elems[(size_t)rank];
     if (elems > 0 && (master[0] == master[1] || m[0] == m[1] || v[0] == v[1]))
@@ -489,7 +669,7 @@ zero_status_t zero_bind(zero_plan_t* p, int rank, float* const master[2], float*
     if (!workspace && !p->workspace) return fail(ZERO_EINVAL, "zero_bind: workspace is NULL");
     if (workspace && p->workspace && workspace != p->workspace)
         return fail(ZERO_EINVAL, "zero_bind: workspace differs from an earlier bind");
-    if (!aligned(workspace, 8)) return fail(ZERO_EALIGN, "zero_bind: workspace not 8-byte aligned");
+    if (!aligned(workspace, 16)) return fail(ZERO_EALIGN, "zero_bind: workspace not 16-byte aligned");
 
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -497,9 +677,12 @@ zero_status_t zero_bind(zero_plan_t* p, int rank, float* const master[2], float*
     if (p->device >= 0 && p->device != dev)
         return fail(ZERO_EINVAL, "zero_bind: buffers of one plan must live on one device");
     if (workspace && !p->workspace) {
-        e = cudaMemset(workspace, 0, kWorkspaceBytes);
+        DevState init;
+        std::memset(&init, 0, sizeof(init));
+        init.scale = 1.0;
+        e = cudaMemcpy(workspace, &init, sizeof(init), cudaMemcpyHostToDevice);
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
-        if (e != cudaSuccess) return cuda_fail(e, "zero_bind: clearing the workspace");
+        if (e != cudaSuccess) return cuda_fail(e, "zero_bind: initialising the workspace");
         p->workspace = (uint32_t*)workspace;
     }
     p->device = dev;
@@ -531,9 +714,35 @@ zero_status_t zero_bind_peer(zero_plan_t* p, int rank, const void* shard16)
     return ZERO_OK;
 }
 
+zero_status_t zero_set_scaler(zero_plan_t* p, const zero_scaler_t* cfg, void* stream)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_set_scaler: NULL plan");
+    if (!p->workspace) return fail(ZERO_ESTATE, "zero_set_scaler: bind a rank first");
+    if (p->in_step) return fail(ZERO_ESTATE, "zero_set_scaler: a step is open");
+    double scale = 1.0;
+    int64_t good = 0;
+    if (cfg) {
+        if (!(cfg->scale > 0.0) || !std::isfinite(cfg->scale) || !(cfg->backoff_factor > 0.0) ||
+            !(cfg->growth_factor > 0.0) || !(cfg->min_scale > 0.0) || cfg->good_steps < 0)
+            return fail(ZERO_EINVAL, "zero_set_scaler: bad scaler settings");
+        scale = cfg->scale;
+        good = cfg->good_steps;
+        p->scaler = *cfg;
+    }
+    p->scaler_dynamic = cfg ? 1 : 0;
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    DevState* d = dev_state(p);
+    cudaError_t e = cudaMemcpyAsync(&d->scale, &scale, sizeof(scale), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&d->good, &good, sizeof(good), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_set_scaler: writing the loss scale");
+    return ZERO_OK;
+}
+
 zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
-                        int64_t which, const zero_hyper_t* hyper, const zero_scaler_t* scaler,
-                        void* stream)
+                        int64_t which, const zero_hyper_t* hyper, void* stream)
 {
     if (!p || !grad_contribs || !hyper) return fail(ZERO_EINVAL, "zero_step: NULL argument");
     if (n_contribs != p->n_d) return fail(ZERO_EINVAL, "zero_step: need one contribution per rank");
@@ -546,22 +755,17 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
         if (!aligned(grad_contribs[r], 2))
             return fail(ZERO_EALIGN, "zero_step: contribution not 2-byte aligned");
     }
-    const double scale = scaler ? scaler->scale : 1.0;
-    if (!(scale > 0.0) || !std::isfinite(scale)) return fail(ZERO_EINVAL, "zero_step: bad loss scale");
+    if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
+        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay))
+        return fail(ZERO_EINVAL, "zero_step: betas must lie in [0, 1) and lr, eps, wd be finite");
     if (p->stage == 3) {
         if (which < 0 || which >= (int64_t)p->units.size())
             return fail(ZERO_EINVAL, "zero_step: unit out of range");
     } else if (which < -1 || which >= p->n_buckets) {
         return fail(ZERO_EINVAL, "zero_step: bucket out of range");
     }
-
-    if (!p->in_step) {
-        step_constants(*hyper, p->t + 1, scale, p->n_d, p->consts);
-        p->step_hyper = *hyper;
-        p->step_scale = scale;
-    } else if (std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0 || p->step_scale != scale) {
-        return fail(ZERO_EINVAL, "zero_step: hyperparameters / scale changed inside a step");
-    }
+    if (p->in_step && std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0)
+        return fail(ZERO_EINVAL, "zero_step: hyperparameters changed inside a step");
     if (which == -1) {
         if (p->in_step) return fail(ZERO_ESTATE, "zero_step: bucket -1 must be the only call of a step");
     } else if (p->covered[(size_t)which]) {
@@ -570,20 +774,37 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
 
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
-    const std::vector<Segment> segs = step_segments(p, which, p->cur ^ 1);
     cudaStream_t s = (cudaStream_t)stream;
+    if (!p->in_step) {
+        if (p->bias_len == 0 || p->bias_beta1 != hyper->beta1 || p->bias_beta2 != hyper->beta2) {
+            st = upload_bias_table(p, hyper->beta1, hyper->beta2, s);
+            if (st != ZERO_OK) return st;
+        }
+        // t, the loss scale and the current half are read on the device; the constants that
+        // do not depend on them are rounded here once.
+        step_constants(*hyper, 1, 1.0, p->n_d, p->consts);
+        p->step_hyper = *hyper;
+    }
+    const std::vector<Segment> segs = step_segments(p, which, 0);
     for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
         const size_t e = std::min(segs.size(), b + kMaxSegs);
         StepParams P;
         std::memset(&P, 0, sizeof(P));
         for (int r = 0; r < p->n_d; ++r) P.c[r] = (const uint16_t*)grad_contribs[r];
         std::memcpy(P.k, p->consts, sizeof(P.k));
+        P.lr = hyper->lr;
+        P.beta1 = hyper->beta1;
+        P.beta2 = hyper->beta2;
+        P.bias = bias_table(p);
+        P.bias_len = p->bias_len;
+        P.bias_saturates = p->bias_saturates;
         P.n_d = p->n_d;
-        P.flag = p->workspace;
-        const bool vec = build_step_params(p, segs, b, e, grad_contribs, p->cur, P);
-        st = p->dtype16 == ZERO_BF16 ? launch_fused<ZERO_BF16>(p, P, vec, s)
-                                     : launch_fused<ZERO_FP16>(p, P, vec, s);
-        if (st != ZERO_OK) return st;
+        P.st = dev_state(p);
+        P.flag = &dev_state(p)->flag;
+        const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
+        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_fused<ZERO_BF16>(p->device, P, vec, s)
+                                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s);
+        if (err != cudaSuccess) return cuda_fail(err, "fused step launch");
     }
     p->in_step = true;
     if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
@@ -591,8 +812,7 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
     return ZERO_OK;
 }
 
-zero_status_t zero_step_finish(zero_plan_t* p, zero_scaler_t* scaler, void* stream,
-                               zero_step_result_t* out)
+zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t* out)
 {
     if (!p) return fail(ZERO_EINVAL, "zero_step_finish: NULL plan");
     if (!p->in_step) return fail(ZERO_ESTATE, "zero_step_finish: no open step");
@@ -602,49 +822,69 @@ zero_status_t zero_step_finish(zero_plan_t* p, zero_scaler_t* scaler, void* stre
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    uint32_t flag = 0;
-    cudaError_t e = cudaMemcpyAsync(&flag, p->workspace, sizeof(flag), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_fail(e, "zero_step_finish: reading the flag");
 
-    const bool skipped = flag != 0;
-    if (!skipped) {
-        p->cur ^= 1;
-        p->t += 1;
-        if (scaler) {
-            scaler->good_steps += 1;
-            if (scaler->growth_interval > 0 && scaler->good_steps >= scaler->growth_interval) {
-                scaler->scale *= scaler->growth_factor;
-                scaler->good_steps = 0;
-            }
-        }
-    } else {
-        const std::vector<Segment> segs = shard_segments_all(p);
-        for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
-            const size_t en = std::min(segs.size(), b + kMaxSegs);
-            StepParams P;
-            std::memset(&P, 0, sizeof(P));
-            P.n_d = p->n_d;
-            const bool vec = build_step_params(p, segs, b, en, nullptr, p->cur, P);
-            st = p->dtype16 == ZERO_BF16 ? launch_recast<ZERO_BF16>(p, P, vec, s)
-                                         : launch_recast<ZERO_FP16>(p, P, vec, s);
-            if (st != ZERO_OK) return st;
-        }
-        if (scaler) {
-            scaler->scale = std::max(scaler->scale * scaler->backoff_factor, scaler->min_scale);
-            scaler->good_steps = 0;
-        }
-        e = cudaMemsetAsync(p->workspace, 0, sizeof(uint32_t), s);
-        if (e != cudaSuccess) return cuda_fail(e, "zero_step_finish: clearing the flag");
+    // Re-cast (no-op unless the flag is set), then the one-thread commit.
+    const std::vector<Segment> segs = shard_segments_all(p);
+    for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
+        const size_t en = std::min(segs.size(), b + kMaxSegs);
+        StepParams P;
+        std::memset(&P, 0, sizeof(P));
+        P.n_d = p->n_d;
+        P.st = dev_state(p);
+        const bool vec = build_step_params(p, segs, b, en, nullptr, P);
+        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_recast<ZERO_BF16>(p->device, P, vec, s)
+                                                        : launch_recast<ZERO_FP16>(p->device, P, vec, s);
+        if (err != cudaSuccess) return cuda_fail(err, "re-cast launch");
     }
+    CommitParams C;
+    C.st = dev_state(p);
+    C.growth = p->scaler.growth_factor;
+    C.backoff = p->scaler.backoff_factor;
+    C.min_scale = p->scaler.min_scale;
+    C.interval = p->scaler.growth_interval;
+    C.dynamic = p->scaler_dynamic;
+    commit_kernel<<<1, 32, 0, s>>>(C);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
     p->in_step = false;
+    p->stepped = true;
     std::fill(p->covered.begin(), p->covered.end(), 0);
-    if (out) {
-        out->skipped = skipped ? 1 : 0;
-        out->reserved = 0;
-        out->t = p->t;
-        out->scale = scaler ? scaler->scale : 1.0;
-    }
+    if (out) return read_state(p, s, out);
+    return ZERO_OK;
+}
+
+zero_status_t zero_read_state(zero_plan_t* p, void* stream, zero_step_result_t* out)
+{
+    if (!p || !out) return fail(ZERO_EINVAL, "zero_read_state: NULL argument");
+    if (!p->workspace) return fail(ZERO_ESTATE, "zero_read_state: no rank bound");
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    return read_state(p, (cudaStream_t)stream, out);
+}
+
+zero_status_t zero_restore_state(zero_plan_t* p, const zero_step_result_t* in, void* stream)
+{
+    if (!p || !in) return fail(ZERO_EINVAL, "zero_restore_state: NULL argument");
+    if (!p->workspace) return fail(ZERO_ESTATE, "zero_restore_state: no rank bound");
+    if (p->in_step) return fail(ZERO_ESTATE, "zero_restore_state: a step is open");
+    if (in->t < 0 || in->good_steps < 0 || in->skipped_total < 0 || in->finished < 0 ||
+        (in->current != 0 && in->current != 1) || !(in->scale > 0.0) || !std::isfinite(in->scale))
+        return fail(ZERO_EINVAL, "zero_restore_state: bad state");
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    DevState d;
+    std::memset(&d, 0, sizeof(d));
+    d.cur = (uint32_t)in->current;
+    d.last_skipped = in->skipped ? 1u : 0u;
+    d.t = in->t;
+    d.skipped = in->skipped_total;
+    d.good = in->good_steps;
+    d.finished = in->finished;
+    d.scale = in->scale;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(dev_state(p), &d, sizeof(d), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_restore_state: writing the state");
     return ZERO_OK;
 }
 
@@ -750,33 +990,6 @@ zero_status_t noalloc_scratch(void** out)
     return ZERO_OK;
 }
 
-template <int DT>
-cudaError_t noalloc_launch(StepParams& P, bool vec, int dev, cudaStream_t st)
-{
-    int64_t acc = 0;
-    KSeg& K = P.seg[0];
-    if (!vec) {
-        K.head = 0;
-        K.tail = 0;
-        K.nvec = K.n;
-    }
-    K.vbeg = 0;
-    acc = K.nvec;
-    P.total_vec = acc;
-    const int64_t work = std::max<int64_t>(acc, (int64_t)kScalarSlots);
-    auto go = [&](auto kernel) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
-            per_sm = 1;
-        const int64_t cap = (int64_t)device_sms(dev) * std::max(per_sm, 1);
-        const int64_t need = std::max<int64_t>(1, (work + kThreads - 1) / kThreads);
-        kernel<<<(int)std::max<int64_t>(1, std::min(cap, need)), kThreads, 0, st>>>(P);
-    };
-    if (!vec) go(fused_step_kernel<DT, 1, 1>);
-    else go(fused_step_kernel<DT, kRankBatch, 8>);
-    return cudaGetLastError();
-}
-
 }  // namespace
 }  // namespace zero
 
@@ -829,6 +1042,7 @@ zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d,
     e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);   // the flag must start at zero
     if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: clearing the flag");
     if (n > 0) {
+        // Host mode of the fused kernel: all constants from the host, half 0 read, half 1 written.
         StepParams P;
         std::memset(&P, 0, sizeof(P));
         for (int r = 0; r < n_d; ++r) P.c[r] = (const uint16_t*)grad_contribs[r];
@@ -836,13 +1050,14 @@ zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d,
         P.n_d = n_d;
         P.n_seg = 1;
         P.flag = (uint32_t*)scratch;
+        P.st = nullptr;
         KSeg& K = P.seg[0];
-        K.p_in = master_in;
-        K.m_in = m_in;
-        K.v_in = v_in;
-        K.p_out = master_out;
-        K.m_out = m_out;
-        K.v_out = v_out;
+        K.p[0] = const_cast<float*>(master_in);
+        K.m[0] = const_cast<float*>(m_in);
+        K.v[0] = const_cast<float*>(v_in);
+        K.p[1] = master_out;
+        K.m[1] = m_out;
+        K.v[1] = v_out;
         K.out16 = (uint16_t*)out16;
         K.c_off = 0;
         K.n = n;
@@ -850,13 +1065,13 @@ zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d,
         bool vec = true;
         for (int r = 0; r < n_d; ++r) vec &= head16(P.c[r]) == h;
         const int64_t hh = std::min<int64_t>(h, n);
-        const float* fp[6] = {K.p_in, K.m_in, K.v_in, K.p_out, K.m_out, K.v_out};
-        for (const float* f : fp) vec &= aligned(f + hh, 16);
+        for (int i = 0; i < 2; ++i)
+            vec &= aligned(K.p[i] + hh, 16) && aligned(K.m[i] + hh, 16) && aligned(K.v[i] + hh, 16);
         K.head = (int32_t)hh;
         K.nvec = (n - hh) / 8;
         K.tail = (int32_t)(n - hh - 8 * K.nvec);
-        e = dtype16 == ZERO_BF16 ? noalloc_launch<ZERO_BF16>(P, vec, dev, s)
-                                 : noalloc_launch<ZERO_FP16>(P, vec, dev, s);
+        e = dtype16 == ZERO_BF16 ? launch_fused<ZERO_BF16>(dev, P, vec, s)
+                                 : launch_fused<ZERO_FP16>(dev, P, vec, s);
         if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: launch");
     }
     uint32_t flag = 0;

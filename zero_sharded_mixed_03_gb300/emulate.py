@@ -14,8 +14,8 @@ import torch
 
 from . import (ZERO_BF16, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS, zero_bind, zero_bind_peer,
                zero_gather_layer, zero_plan_create, zero_plan_destroy, zero_plan_info,
-               zero_plan_tables, zero_rank_state_elems, zero_release_layer, zero_state_cursor,
-               zero_step, zero_step_finish)
+               zero_plan_tables, zero_rank_state_elems, zero_read_state, zero_release_layer,
+               zero_set_scaler, zero_step, zero_step_finish)
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
@@ -78,11 +78,18 @@ class EmulatedGroup:
         self.shard16[rank] = sh
         return sh
 
+    def step_state(self, stream=None):
+        """Device-resident step state (synchronises the stream)."""
+        return zero_read_state(self.plan, _stream_handle(stream))
+
     def current(self) -> int:
-        return zero_state_cursor(self.plan)[1]
+        return self.step_state().current
 
     def t(self) -> int:
-        return zero_state_cursor(self.plan)[0]
+        return self.step_state().t
+
+    def set_scaler(self, scaler, stream=None) -> None:
+        zero_set_scaler(self.plan, scaler, _stream_handle(stream))
 
     def state_tensor(self, rank: int, name: str) -> torch.Tensor:
         return self.state[rank][name][self.current()]
@@ -93,11 +100,12 @@ class EmulatedGroup:
         return torch.cat(parts) if parts else phys[:0]
 
     # ------------------------------------------------------------------ the step
-    def step(self, contribs: Sequence[int], which: int, hyper, scaler=None, stream=None) -> None:
-        zero_step(self.plan, list(contribs), which, hyper, scaler, _stream_handle(stream))
+    def step(self, contribs: Sequence[int], which: int, hyper, stream=None) -> None:
+        zero_step(self.plan, list(contribs), which, hyper, _stream_handle(stream))
 
-    def finish(self, scaler=None, stream=None):
-        return zero_step_finish(self.plan, scaler, _stream_handle(stream))
+    def finish(self, stream=None, wait: bool = True):
+        """Commit the step on the device; wait=True also returns the read-back state."""
+        return zero_step_finish(self.plan, _stream_handle(stream), wait)
 
     def gather(self, unit: int, dst: torch.Tensor, stream=None) -> None:
         zero_gather_layer(self.plan, unit, dst.data_ptr(), _stream_handle(stream))
