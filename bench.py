@@ -71,6 +71,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, dist=None) -> float:
+    """Largest value over the ranks of the (optional) process group: the job's wall time is
+    the slowest replica's.  NCCL reduces a CUDA tensor, gloo a CPU one."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(elems_per_step: int, applied_steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput of N independent replicas: every rank updates elems_per_step
+    parameters per applied step; the job takes the slowest rank's time."""
+    return world * elems_per_step * applied_steps / seconds
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -278,16 +296,14 @@ def gpu_arm(args, world, rank, local):
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     if dist:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, dist)
     skipped = b.g.step_state().skipped_total - skipped_before
     fused_ms = [a.elapsed_time(c) for a, c in fused_pairs]
     gather_ms = [a.elapsed_time(c) for a, c in gather_pairs]
 
     applied = args.steps - skipped
     elems = b.elems_per_step
-    value = world * elems * applied / (ms / 1e3)
+    value = job_value(elems, applied, world, ms / 1e3)
     step_bytes = elems * b.bytes_per_elem
     gather_bytes = 4 * int(b.info.phi_pad) if w.stage == 3 else 0
     hbm_gbs = (step_bytes + gather_bytes) * args.steps / (ms / 1e3) / 1e9
@@ -350,10 +366,8 @@ def e2e_leg(b: Bench, steps: int, world: int, dist):
     torch.cuda.synchronize()
     el = time.perf_counter() - t
     if dist:
-        tt = torch.tensor([el], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        el = float(tt.item())
-    return {"value": world * b.elems_per_step * applied / el, "unit": UNIT,
+        el = max_over_ranks(el, dist)
+    return {"value": job_value(b.elems_per_step, applied, world, el), "unit": UNIT,
             "h2d_bytes_per_step": 2 * b.set_elems * b.w.n_d, "d2h_bytes_per_step": 64,
             "steps": steps}
 
