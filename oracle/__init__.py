@@ -59,6 +59,12 @@ def lib():
         L.orc_sharded_step.restype = ctypes.c_int
         L.orc_sharded_step.argtypes = [vp, i64, vp, i64, ctypes.c_int, ctypes.c_int, i64,
                                        ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_sharded_step_ex.restype = ctypes.c_int
+        L.orc_sharded_step_ex.argtypes = [vp, i64, vp, i64, ctypes.c_int, ctypes.c_int, i64,
+                                          ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
+        L.orc_clip_coef.restype = ctypes.c_float
+        L.orc_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
         L.orc_scaler_update.restype = i64
         L.orc_scaler_update.argtypes = [ctypes.c_int, i64, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(i64), ctypes.c_double, ctypes.c_double, i64,
@@ -206,6 +212,24 @@ class ScalerState:
                                              self.cfg.growth_factor, self.cfg.backoff_factor,
                                              self.cfg.growth_interval, self.cfg.min_scale))
         self.scale, self.good = sc.value, gd.value
+
+
+def sharded_step_ex(layout: Layout, stage: int, bucket_elems: int, is_fp16: int, contribs,
+                    bound, p, m, v, shard16, full16, k9, max_norm: float = 0.0):
+    """Sharded step with the optional norm / clipping; returns (flag, norm^2)."""
+    bound = np.ascontiguousarray(np.asarray(bound, dtype=np.int32))
+    n_d = layout.n_d
+    norm2 = ctypes.c_double(0.0)
+    flag = lib().orc_sharded_step_ex(
+        _p(layout.sizes), layout.sizes.size, _p(layout.unit_first), layout.n_units_arg, n_d,
+        stage, bucket_elems, is_fp16, _ptrs(contribs), _p(bound), _ptrs(p), _ptrs(m), _ptrs(v),
+        _ptrs(shard16 if shard16 is not None else [None] * n_d), _p(full16), _p(k9),
+        float(max_norm), ctypes.byref(norm2))
+    return flag, norm2.value
+
+
+def clip_coef(norm2: float, max_norm: float) -> float:
+    return float(lib().orc_clip_coef(norm2, max_norm))
 
 
 def ddp_step(contribs, is_fp16, p, m, v, out16, k9) -> int:

@@ -27,6 +27,11 @@
 //   R6 16-bit casts round to nearest, ties to even.
 //   R7 All fp32 arithmetic uses separately rounded operations in the order
 //      written below (built with -ffp-contract=off, no fast-math).
+//   R8 Optional global gradient norm and clipping: norm^2 = sum over the
+//      updated elements of fp32(g*g), summed in double, g the averaged,
+//      unscaled, unclipped gradient; clipping multiplies g by
+//      fp32(min(1, max_norm / (sqrt(norm^2) + 1e-6))) before AdamW (the rule
+//      of torch.nn.utils.clip_grad_norm_).  The skip flag is taken on g.
 //
 // Parity pins (tests/test_oracle_pins.py): closed-form memory and
 // communication figures of [ZF]; brute-force tables on tiny inputs; DDP
@@ -162,6 +167,14 @@ inline float reduce_one(int n_d, const uint16_t* const* c, int64_t idx, int is_f
 }
 
 inline int nonfinite(float g) { return std::isfinite(g) ? 0 : 1; }
+
+// Clip coefficient of R8 (NaN stays NaN; only a skipped step can see one).
+float clip_coef(double norm2, double max_norm)
+{
+    double c = max_norm / (std::sqrt(norm2) + 1e-6);
+    if (c > 1.0) c = 1.0;
+    return (float)c;
+}
 
 // AdamW on one element, fp32, in this order (R1, R7).
 inline void adamw_one(float g, float& p, float& m, float& v, const Consts& k)
@@ -418,11 +431,13 @@ void orc_comm(int64_t phi_pad, int n_d, int64_t* out)
 // full16:     stages 1/2: the flat 16-bit parameter buffer (phi_pad).
 // k9:         orc_consts(...) for this step.
 // Returns the global non-finite flag (1 = step skipped, state untouched).
-int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* unit_first,
-                     int64_t n_units, int n_d, int stage, int64_t bucket_elems, int is_fp16,
-                     const uint16_t* const* contrib, const int32_t* bound, float* const* p,
-                     float* const* m, float* const* v, uint16_t* const* shard16,
-                     uint16_t* full16, const float* k9)
+// Same as orc_sharded_step, with the optional global gradient norm and clipping (R8):
+// max_norm > 0 clips; *norm2_out (if not NULL) receives norm^2.
+int orc_sharded_step_ex(const int64_t* sizes, int64_t n_tensors, const int64_t* unit_first,
+                        int64_t n_units, int n_d, int stage, int64_t bucket_elems, int is_fp16,
+                        const uint16_t* const* contrib, const int32_t* bound, float* const* p,
+                        float* const* m, float* const* v, uint16_t* const* shard16,
+                        uint16_t* full16, const float* k9, double max_norm, double* norm2_out)
 {
     Layout L;
     if (!make_layout(sizes, n_tensors, unit_first, n_units, n_d, L)) return -1;
@@ -435,6 +450,7 @@ int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* uni
     for (int r = 0; r < n_d; ++r)
         if (bound[r]) g[(size_t)r].assign((size_t)L.shard_total, 0.0f);
     int flag = 0;
+    double norm2 = 0.0;
     if (stage != 3) {
         const Unit& U = L.units[0];
         const int64_t nrows = orc_bucket_segments(U.numel_pad, n_d, bucket_elems, nullptr, 0);
@@ -448,6 +464,7 @@ int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* uni
                 const float gi = reduce_one(n_d, contrib, a + i, is_fp16, k.inv);
                 g[(size_t)r][(size_t)(off + i)] = gi;
                 flag |= nonfinite(gi);
+                norm2 += (double)(gi * gi);
             }
         }
     } else {
@@ -459,9 +476,13 @@ int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* uni
                                                 k.inv);
                     g[(size_t)r][(size_t)(U.shard_base + i)] = gi;
                     flag |= nonfinite(gi);
+                    norm2 += (double)(gi * gi);
                 }
             }
     }
+
+    if (norm2_out) *norm2_out = norm2;
+    const float coef = max_norm > 0.0 ? clip_coef(norm2, max_norm) : 1.0f;
 
     // Phase 2: update each bound rank's shard and cast it into the all-gather
     // destination, or, on a skipped step, re-cast the unchanged master.
@@ -470,7 +491,8 @@ int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* uni
         for (const Unit& U : L.units)
             for (int64_t i = 0; i < U.shard; ++i) {
                 const size_t j = (size_t)(U.shard_base + i);
-                if (!flag) adamw_one(g[(size_t)r][j], p[r][j], m[r][j], v[r][j], k);
+                const float gj = max_norm > 0.0 ? g[(size_t)r][j] * coef : g[(size_t)r][j];
+                if (!flag) adamw_one(gj, p[r][j], m[r][j], v[r][j], k);
                 const uint16_t h = round16(p[r][j], is_fp16);
                 if (stage != 3) full16[U.base + r * U.shard + i] = h;
                 else shard16[r][j] = h;
@@ -478,6 +500,19 @@ int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* uni
     }
     return flag;
 }
+
+int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* unit_first,
+                     int64_t n_units, int n_d, int stage, int64_t bucket_elems, int is_fp16,
+                     const uint16_t* const* contrib, const int32_t* bound, float* const* p,
+                     float* const* m, float* const* v, uint16_t* const* shard16,
+                     uint16_t* full16, const float* k9)
+{
+    return orc_sharded_step_ex(sizes, n_tensors, unit_first, n_units, n_d, stage, bucket_elems,
+                               is_fp16, contrib, bound, p, m, v, shard16, full16, k9, 0.0,
+                               nullptr);
+}
+
+float orc_clip_coef(double norm2, double max_norm) { return clip_coef(norm2, max_norm); }
 
 // ---- A8 commit/skip of the dynamic loss scale (R5): on a flagged step the
 // scale backs off (not below min_scale) and the clean-step counter restarts;

@@ -562,3 +562,73 @@ def test_scaler_trajectory():
     for flag in [0, 1, 0]:
         s.update(flag)
     assert (s.t, s.scale) == (2, 1.0)
+
+
+# ----------------------------------------------------------------- gradient norm and clipping
+
+def _oracle_run_1rank(gs16, p16, hyper, max_norm, is_fp16=0):
+    """Run the sharded oracle with N_d = 1 over a sequence of 16-bit gradients."""
+    n = p16.size
+    L = oracle.Layout([n], 1)
+    P = [oracle.widen16(p16, is_fp16).astype(np.float32)]
+    M, V = [np.zeros(n, np.float32)], [np.zeros(n, np.float32)]
+    full = p16.copy()
+    norms = []
+    for t, c in enumerate(gs16, start=1):
+        k9 = oracle.consts(hyper, t, 1.0, 1)
+        flag, n2 = oracle.sharded_step_ex(L, 1, 0, is_fp16, [c], [1], P, M, V, None, full, k9,
+                                          max_norm)
+        assert flag == 0
+        norms.append(n2)
+    return P[0], M[0], V[0], norms
+
+
+def test_clipping_matches_torch():
+    """Clip-by-global-norm then AdamW against torch.nn.utils.clip_grad_norm_ + torch AdamW
+    (library cross-check of reading R8), with the clip active on every step."""
+    hyper = W.Hyper()
+    rng = np.random.default_rng(30)
+    n = 5000
+    p16 = _rand16(rng, n, 0, 0.02)
+    gs = [_rand16(rng, n, 0, 0.01) for _ in range(4)]
+    max_norm = 0.05                       # norm of ~N(0, 1e-2) over 5000 elements is ~0.7
+    P, M, V, norms = _oracle_run_1rank(gs, p16, hyper, max_norm)
+    tp = torch.nn.Parameter(torch.from_numpy(oracle.widen16(p16, 0).astype(np.float32)))
+    opt = torch.optim.AdamW([tp], lr=hyper.lr, betas=(hyper.beta1, hyper.beta2), eps=hyper.eps,
+                            weight_decay=hyper.weight_decay, foreach=False)
+    for c, n2 in zip(gs, norms):
+        tp.grad = torch.from_numpy(oracle.widen16(c, 0).astype(np.float32))
+        tn = torch.nn.utils.clip_grad_norm_([tp], max_norm)
+        assert abs(float(tn) - math.sqrt(n2)) <= 1e-6 * math.sqrt(n2)
+        opt.step()
+    st = opt.state[tp]
+    for mine, ref in [(P, tp.detach().numpy()), (M, st["exp_avg"].numpy()), (V, st["exp_avg_sq"].numpy())]:
+        assert np.all(np.abs(mine - ref) <= 1e-6 * np.abs(ref) + 1e-8)
+
+
+def test_norm_and_coefficient_closed_forms():
+    """Constant gradient c = 2^-7 over n = 4096 elements: norm^2 = n c^2 exactly, norm = 64 c;
+    max_norm = 16 c gives coef = fp32(16c / (64c + 1e-6)) and m = fp32(0.1) * fp32(c * coef)."""
+    hyper = W.Hyper()
+    n, c = 4096, 2.0 ** -7
+    g16 = oracle.round16(np.full(n, c, np.float32), 0)
+    p16 = oracle.round16(np.zeros(n, np.float32), 0)
+    P, M, V, norms = _oracle_run_1rank([g16], p16, hyper, 16 * c)
+    assert fractions.Fraction(norms[0]) == n * fractions.Fraction(c) ** 2
+    coef = np.float32(16 * c / (64 * c + 1e-6))
+    assert oracle.clip_coef(norms[0], 16 * c) == coef
+    assert np.all(M == np.float32(1 - hyper.beta1) * (np.float32(c) * coef))
+    # a bound above the norm leaves the step bit-identical to the unclipped one
+    P2, M2, V2, _ = _oracle_run_1rank([g16], p16, hyper, 1.0)
+    P3, M3, V3, _ = _oracle_run_1rank([g16], p16, hyper, 0.0)
+    assert np.array_equal(P2, P3) and np.array_equal(M2, M3) and np.array_equal(V2, V3)
+
+
+def test_norm_is_exact_sum_of_squares():
+    """Gradients that are small multiples of 2^-8: fp32(g*g) and their double sum are exact."""
+    rng = np.random.default_rng(31)
+    ints = rng.integers(-64, 65, size=777)
+    g16 = oracle.round16((ints / 256.0).astype(np.float32), 0)
+    _, _, _, norms = _oracle_run_1rank([g16], oracle.round16(np.zeros(777, np.float32), 0),
+                                       W.Hyper(), 0.0)
+    assert fractions.Fraction(norms[0]) == sum(fractions.Fraction(int(i), 256) ** 2 for i in ints)
