@@ -26,8 +26,12 @@ vp = ctypes.c_void_p
 
 
 def build() -> str:
-    cmd = ["g++", *CFLAGS, "-shared", "-fPIC", SRC, "-o", LIB]
+    # compile to a private file, then rename: a process loading the library never sees a
+    # half-written file even when several processes build at once
+    tmp = f"{LIB}.{os.getpid()}.tmp"
+    cmd = ["g++", *CFLAGS, "-shared", "-fPIC", SRC, "-o", tmp]
     subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
     return LIB
 
 

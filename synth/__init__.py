@@ -30,17 +30,21 @@ i64 = ctypes.c_int64
 
 def build_host() -> str:
     src = os.path.join(_HERE, "synth_host.cpp")
+    tmp = f"{HOST_LIB}.{os.getpid()}.tmp"        # renamed into place: never half-written
     cmd = ["g++", "-O2", "-ffp-contract=off", "-std=c++17", "-shared", "-fPIC", src, "-o",
-           HOST_LIB, "-lpthread"]
+           tmp, "-lpthread"]
     subprocess.run(cmd, check=True)
+    os.replace(tmp, HOST_LIB)
     return HOST_LIB
 
 
 def build_device() -> str:
     src = os.path.join(_HERE, "synth_dev.cu")
+    tmp = f"{DEV_LIB}.{os.getpid()}.tmp"
     cmd = [NVCC, "-gencode", GENCODE, "-O3", "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
-           src, "-o", DEV_LIB]
+           src, "-o", tmp]
     subprocess.run(cmd, check=True)
+    os.replace(tmp, DEV_LIB)
     return DEV_LIB
 
 

@@ -27,7 +27,9 @@ def build(verbose: bool = False) -> str:
     for cmd, pr in procs:
         if pr.wait() != 0:
             raise RuntimeError("compile failed: " + " ".join(cmd))
-    subprocess.run([NVCC, *GENCODE, "-shared", *objs, "-o", LIB], check=True)
+    tmp = f"{LIB}.{os.getpid()}.tmp"             # renamed into place: never half-written
+    subprocess.run([NVCC, *GENCODE, "-shared", *objs, "-o", tmp], check=True)
+    os.replace(tmp, LIB)
     return LIB
 
 
