@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=4_194_304)
     ap.add_argument("--mem-budget-gb", type=float, default=160.0)
+    ap.add_argument("--grad-norm", choices=["off", "report", "clip"], default="off",
+                    help="report: global gradient norm inside the fused pass; clip: norm pre-pass "
+                         "over every bucket/unit, then the update clipped at max norm 1.0")
     return ap.parse_args()
 
 
@@ -153,7 +156,7 @@ class ClockSampler:
 class Bench:
     """A workload bound to the product API with pre-generated contribution sets."""
 
-    def __init__(self, w, mem_budget_gb: float, n_sets_wanted: int):
+    def __init__(self, w, mem_budget_gb: float, n_sets_wanted: int, grad_norm: str = "off"):
         import torch
         import synth
         from zero_sharded_mixed_03_gb300.emulate import EmulatedGroup
@@ -209,6 +212,11 @@ class Bench:
         self.elems_per_step = int(self.info.shard) * len(self.bound)
         self.bytes_per_elem = 2 * w.n_d + 26
         self.hyper = self.run.hyper
+        self.clip = grad_norm == "clip"
+        if grad_norm != "off":
+            h = self.hyper
+            self.hyper = Z.hyper(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay,
+                                 1.0 if self.clip else 0.0, grad_norm == "report")
 
     def call_ptrs(self, bufs, ci):
         """Per-rank contribution pointers of call ci: base such that base + c_off hits the slice."""
@@ -226,6 +234,10 @@ class Bench:
         around each fused launch / gather launch.  Returns (result or None, kernel launches).
         """
         launches = 0
+        if self.clip:
+            for ci, (which, lo, hi) in enumerate(self.calls):
+                self.g.grad_norm(self.call_ptrs(bufs, ci), which)
+                launches += 1
         for ci, (which, lo, hi) in enumerate(self.calls):
             if self.w.stage == 3:
                 if gather_events is not None:
@@ -259,7 +271,7 @@ def gpu_arm(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     w = W.workload(args.config)
-    b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps))
+    b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm)
     peak, peak_kind = peaks()
 
     for k in range(args.warmup):
@@ -305,6 +317,8 @@ def gpu_arm(args, world, rank, local):
     elems = b.elems_per_step
     value = job_value(elems, applied, world, ms / 1e3)
     step_bytes = elems * b.bytes_per_elem
+    if args.grad_norm == "clip":                    # the norm pre-pass reads the gradients again
+        step_bytes += elems * 2 * w.n_d
     gather_bytes = 4 * int(b.info.phi_pad) if w.stage == 3 else 0
     hbm_gbs = (step_bytes + gather_bytes) * args.steps / (ms / 1e3) / 1e9
     # dominant kernel: the fused step; algorithmic bytes per launch = elements x (2 N_d + 26)
@@ -330,7 +344,7 @@ def gpu_arm(args, world, rank, local):
                       "units": len(b.units), "bound_ranks": len(b.bound),
                       "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
-                      "contribution_sets": b.n_sets},
+                      "contribution_sets": b.n_sets, "grad_norm": args.grad_norm},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,
            "clocks": clk}

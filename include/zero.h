@@ -63,10 +63,18 @@ enum { ZERO_BF16 = 0, ZERO_FP16 = 1 };
 
 typedef struct zero_plan zero_plan_t;
 
-/* AdamW hyperparameters (decoupled weight decay, bias-corrected moments). */
+/* AdamW hyperparameters (decoupled weight decay, bias-corrected moments), plus the optional
+ * global gradient norm: max_grad_norm > 0 clips the averaged, unscaled gradient g by
+ * fp32(min(1, max_grad_norm / (norm + 1e-6))), norm = sqrt(sum of fp32(g*g) in double), which
+ * needs zero_grad_norm over every bucket/unit of the step first; flags & ZERO_REPORT_GRAD_NORM
+ * computes the norm inside the fused pass for reporting (no clipping, no extra pass). */
 typedef struct {
     double lr, beta1, beta2, eps, weight_decay;
+    double max_grad_norm;    /* 0: no clipping */
+    int64_t flags;           /* ZERO_REPORT_GRAD_NORM */
 } zero_hyper_t;
+
+#define ZERO_REPORT_GRAD_NORM 1
 
 /* Dynamic loss scale (kept on the device once set with zero_set_scaler).  On a step whose
  * reduced gradient holds inf/nan the step is skipped and scale = max(scale * backoff_factor,
@@ -121,6 +129,7 @@ typedef struct {
     int64_t good_steps;      /* applied steps since the last change of scale */
     int64_t skipped_total;   /* skipped steps so far */
     int64_t finished;        /* finished steps (applied + skipped) */
+    double grad_norm;        /* global gradient norm of the last finished step, -1 if not computed */
 } zero_step_result_t;
 
 /* Per-rank bytes.  logical[s][c]: stage s in (DDP, ZeRO-1, ZeRO-2, ZeRO-3), component c in
@@ -215,6 +224,13 @@ zero_status_t zero_set_scaler(zero_plan_t* plan, const zero_scaler_t* cfg, void*
 zero_status_t zero_step(zero_plan_t* plan, const void* const* grad_contribs, int64_t n_contribs,
                         int64_t which, const zero_hyper_t* hyper, void* stream);
 
+/* Gradient-norm pre-pass of bucket / unit `which` (same contributions as zero_step): adds the
+ * bound ranks' sum of fp32(g*g) to the step's norm on the device, reading only the 16-bit
+ * contributions (2 N_d bytes per element).  Needed before the first zero_step of a step that
+ * clips (hyper->max_grad_norm > 0); call it for every bucket/unit, before any zero_step. */
+zero_status_t zero_grad_norm(zero_plan_t* plan, const void* const* grad_contribs,
+                             int64_t n_contribs, int64_t which, void* stream);
+
 /* End the step on the device: a re-cast kernel (which does nothing unless the flag is set)
  * rewrites the 16-bit parameters of a skipped step from the unchanged master, then a
  * one-thread commit either makes the new state current (t += 1, loss-scale growth) or keeps
@@ -257,6 +273,7 @@ zero_status_t zero_comm_report(const zero_plan_t* plan, zero_comm_report_t* out)
  *   master_in/m_in/v_in  fp32 state read (n elements); not modified
  *   master_out/m_out/v_out  fp32 state written (n elements); must not alias the inputs
  *   out16                16-bit parameters written (n elements), even when the flag is set
+ *   hyper                AdamW hyperparameters; max_grad_norm and flags must be 0 here
  *   t                    1-based index of the step being applied (bias correction)
  *   loss_scale           gradients are multiplied by 1 / (n_d * loss_scale)
  *   *nonfinite           receives 1 if any reduced gradient element is inf/nan, else 0

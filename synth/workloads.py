@@ -36,6 +36,8 @@ class Hyper:
     beta2: float = 0.999
     eps: float = 1e-8
     weight_decay: float = 0.01
+    max_grad_norm: float = 0.0       # > 0: clip by the global gradient norm
+    report_norm: bool = False        # compute the global gradient norm in the fused pass
 
 
 @dataclasses.dataclass(frozen=True)

@@ -95,7 +95,7 @@ class Run:
                                    c.growth_interval)
             self.g.set_scaler(self.scaler)
         self.hyper = Z.hyper(w.hyper.lr, w.hyper.beta1, w.hyper.beta2, w.hyper.eps,
-                             w.hyper.weight_decay)
+                             w.hyper.weight_decay, w.hyper.max_grad_norm, w.hyper.report_norm)
         n_c = int(self.info.max_contrib_elems) if alloc_contribs else 0
         self.contribs = [torch.empty(max(8, n_c), dtype=torch.int16, device="cuda")
                          for _ in range(w.n_d)]
@@ -113,7 +113,13 @@ class Run:
                 for b in range(int(self.info.n_buckets))]
 
     def step(self, k: int, gather_check=None):
-        """Run 1-based step k: (stage 3: gather, then) reduce + update per bucket / unit."""
+        """Run 1-based step k: (stage 3: gather, then) reduce + update per bucket / unit.
+        With clipping, a gradient-norm pass over every bucket / unit comes first."""
+        if self.w.hyper.max_grad_norm > 0:
+            for which, lo, hi in self.ranges():
+                for r in range(self.w.n_d):
+                    fill_device(self.contribs[r], synth.grad_stream(self.w, k, r), self.units, lo, hi)
+                self.g.grad_norm([c.data_ptr() for c in self.contribs], which)
         for which, lo, hi in self.ranges():
             if self.w.stage == 3:
                 self.g.gather(which, self.gather_buf)
@@ -236,9 +242,10 @@ class OracleFull:
         n = self.L.total_pad
         c = [fill_host(synth.grad_stream(w, k, r), self.units, 0, n) for r in range(w.n_d)]
         k9 = oracle.consts(w.hyper, self.sc.t + 1, self.sc.scale, w.n_d)
-        flag = oracle.sharded_step(self.L, w.stage, w.bucket_elems, w.dtype, c, self.bound, self.p,
-                                   self.m, self.v, self.sh16 if w.stage == 3 else None,
-                                   self.full16 if w.stage != 3 else None, k9)
+        flag, self.norm2 = oracle.sharded_step_ex(
+            self.L, w.stage, w.bucket_elems, w.dtype, c, self.bound, self.p, self.m, self.v,
+            self.sh16 if w.stage == 3 else None, self.full16 if w.stage != 3 else None, k9,
+            w.hyper.max_grad_norm)
         self.sc.update(flag)
         return flag
 

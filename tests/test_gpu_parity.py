@@ -347,3 +347,91 @@ def test_restored_state_far_into_training(beta2, t0):
             _compare_full(run, o, f"restored at t={t0}, step {k}")
     finally:
         run.close()
+
+
+# ---------------------------------------------------------------------- gradient norm and clipping
+
+def _hyper(max_norm=0.0, report=False):
+    return W.Hyper(max_grad_norm=max_norm, report_norm=report)
+
+
+CLIP_CASES = {
+    "z1_nd4_clip": W.Workload(wid=140, name="clip1", sizes=(70_001, 333), n_d=4, stage=1,
+                              bucket_elems=0, unit_first=(), dtype=W.BF16, steps=3,
+                              hyper=_hyper(0.05), scaler=None),
+    "z2_nd8_fp16_buckets_clip_skip": W.Workload(
+        wid=141, name="clip2", sizes=tuple(_ragged(16, 40, 9000)), n_d=8, stage=2,
+        bucket_elems=10_000, unit_first=(), dtype=W.FP16, steps=4, hyper=_hyper(1e-6),
+        scaler=W.Scaler(), outliers=True, inject=(2, 5, 33_333)),
+    "z3_nd16_units_clip": W.Workload(
+        wid=142, name="clip3", sizes=tuple(_ragged(17, 24, 6000)), n_d=16, stage=3,
+        bucket_elems=0, unit_first=(0, 5, 11, 17, 23), dtype=W.BF16, steps=3,
+        hyper=_hyper(0.02), scaler=None),
+    "z2_nd7_report_only": W.Workload(
+        wid=143, name="report", sizes=tuple(_ragged(18, 60, 5000)), n_d=7, stage=2,
+        bucket_elems=20_000, unit_first=(), dtype=W.BF16, steps=3, hyper=_hyper(0.0, True),
+        scaler=None),
+}
+
+
+@pytest.mark.parametrize("name", list(CLIP_CASES))
+def test_norm_and_clipping_full_parity(name):
+    w = CLIP_CASES[name]
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    try:
+        for k in range(1, w.steps + 1):
+            res = run.step(k)
+            flag = o.step(k)
+            assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale
+            want = np.sqrt(o.norm2)
+            if np.isfinite(want):
+                assert abs(res.grad_norm - want) <= 1e-12 * want, (res.grad_norm, want)
+            else:
+                assert not np.isfinite(res.grad_norm)
+            _compare_full(run, o, f"{name} step {k}")
+    finally:
+        run.close()
+
+
+def test_report_only_leaves_the_update_unchanged():
+    w = CLIP_CASES["z2_nd7_report_only"]
+    plain = dataclasses.replace(w, hyper=_hyper(0.0, False))
+    a, b = H.Run(w), H.Run(plain)
+    try:
+        for k in (1, 2):
+            ra, rb = a.step(k), b.step(k)
+            assert ra.grad_norm > 0 and rb.grad_norm == -1.0
+            for r in a.bound:
+                x, y = a.read_logical(r), b.read_logical(r)
+                for key in x:
+                    assert np.array_equal(x[key].view(np.uint32), y[key].view(np.uint32))
+    finally:
+        a.close()
+        b.close()
+
+
+def test_norm_is_deterministic_and_pass_order_is_checked():
+    w = CLIP_CASES["z1_nd4_clip"]
+    norms = []
+    for _ in range(2):
+        run = H.Run(w)
+        try:
+            norms.append(run.step(1).grad_norm)
+        finally:
+            run.close()
+    assert norms[0] == norms[1]
+    run = H.Run(w)
+    try:
+        ptrs = [c.data_ptr() for c in run.contribs]
+        with pytest.raises(Z.ZeroError) as e:            # clipping without the norm pass
+            run.g.step(ptrs, -1, run.hyper)
+        assert e.value.status == Z.ZERO_ESTATE
+        plain = Z.hyper()
+        run.g.step(ptrs, -1, plain)
+        with pytest.raises(Z.ZeroError) as e:            # the norm must precede the update
+            run.g.grad_norm(ptrs, -1)
+        assert e.value.status == Z.ZERO_ESTATE
+        run.g.finish()
+    finally:
+        run.close()

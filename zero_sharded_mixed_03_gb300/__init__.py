@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(HERE, "libzero.so")
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ESTATE, ZERO_ERANGE = range(6)
 ZERO_BF16, ZERO_FP16 = 0, 1
 ZERO_MAX_RANKS = 128
+ZERO_REPORT_GRAD_NORM = 1
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT) = range(5)
 TABLE_COLS = {0: 1, 1: 7, 2: 6, 3: 5, 4: 4}
@@ -27,7 +28,7 @@ STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_EALIGN", 3: "ZERO_ECUDA
 EXPORTED = ["zero_plan_create", "zero_plan_info", "zero_rank_state_elems", "zero_plan_tables",
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",
             "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_set_scaler",
-            "zero_read_state", "zero_restore_state",
+            "zero_read_state", "zero_restore_state", "zero_grad_norm",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
@@ -40,7 +41,8 @@ class ZeroError(RuntimeError):
 
 class zero_hyper_t(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
-                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double),
+                ("max_grad_norm", ctypes.c_double), ("flags", ctypes.c_int64)]
 
 
 class zero_scaler_t(ctypes.Structure):
@@ -63,7 +65,7 @@ class zero_step_result_t(ctypes.Structure):
     _fields_ = [("skipped", ctypes.c_int32), ("current", ctypes.c_int32),
                 ("t", ctypes.c_int64), ("scale", ctypes.c_double),
                 ("good_steps", ctypes.c_int64), ("skipped_total", ctypes.c_int64),
-                ("finished", ctypes.c_int64)]
+                ("finished", ctypes.c_int64), ("grad_norm", ctypes.c_double)]
 
 
 class zero_mem_report_t(ctypes.Structure):
@@ -117,6 +119,8 @@ def lib() -> ctypes.CDLL:
         L.zero_set_scaler.argtypes = [_vp, ctypes.POINTER(zero_scaler_t), _vp]
         L.zero_read_state.restype = st
         L.zero_read_state.argtypes = [_vp, _vp, ctypes.POINTER(zero_step_result_t)]
+        L.zero_grad_norm.restype = st
+        L.zero_grad_norm.argtypes = [_vp, _vp, _i64, _i64, _vp]
         L.zero_restore_state.restype = st
         L.zero_restore_state.argtypes = [_vp, ctypes.POINTER(zero_step_result_t), _vp]
         L.zero_gather_layer.restype = st
@@ -215,6 +219,11 @@ def zero_step(plan: int, grad_contribs: Sequence[int], which: int, hyper: zero_h
                            ctypes.byref(hyper), stream or None))
 
 
+def zero_grad_norm(plan: int, grad_contribs: Sequence[int], which: int, stream: int = 0) -> None:
+    _check(lib().zero_grad_norm(plan, _ptr_array(grad_contribs), len(grad_contribs), which,
+                                stream or None))
+
+
 def zero_step_finish(plan: int, stream: int = 0, wait: bool = True) -> Optional[zero_step_result_t]:
     """Enqueue the commit; with wait=True also read back the step state (synchronises)."""
     res = zero_step_result_t() if wait else None
@@ -277,8 +286,10 @@ def zero_step_range_noalloc(grad_contribs: Sequence[int], n: int, dtype16: int, 
     return int(flag.value)
 
 
-def hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01) -> zero_hyper_t:
-    return zero_hyper_t(lr, beta1, beta2, eps, weight_decay)
+def hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, max_grad_norm=0.0,
+          report_grad_norm=False) -> zero_hyper_t:
+    return zero_hyper_t(lr, beta1, beta2, eps, weight_decay, max_grad_norm,
+                        ZERO_REPORT_GRAD_NORM if report_grad_norm else 0)
 
 
 def scaler(scale=65536.0, growth_factor=2.0, backoff_factor=0.5, min_scale=1.0,

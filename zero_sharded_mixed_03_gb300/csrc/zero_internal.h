@@ -50,7 +50,9 @@ struct Segment {
 // table, entry t (t >= 1) = (1 - beta1^t, sqrt(1 - beta2^t)) in double.
 constexpr int64_t kStateBytes = 256;
 constexpr int64_t kBiasCap = 1 << 16;
-constexpr int64_t kWorkspaceBytes = kStateBytes + 16 * (kBiasCap + 1);
+// then one double per block of a launch: partial sums of the gradient norm
+constexpr int64_t kNormSlots = 4096;
+constexpr int64_t kWorkspaceBytes = kStateBytes + 16 * (kBiasCap + 1) + 8 * kNormSlots;
 
 }  // namespace zero
 
@@ -82,6 +84,8 @@ struct zero_plan {
     bool in_step = false;
     bool stepped = false;               // a step has been enqueued since the plan was bound
     std::vector<char> covered;          // per bucket / unit in the open step
+    std::vector<char> norm_covered;     // per bucket / unit: gradient-norm pre-pass done
+    bool norm_open = false;             // a norm pre-pass of the next step has been issued
     float consts[9] = {0};              // fp32 constants that do not depend on t or the scale
     zero_hyper_t step_hyper = {0, 0, 0, 0, 0};
     zero_scaler_t scaler = {1.0, 1.0, 1.0, 1.0, 0, 0};

@@ -196,6 +196,7 @@ zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, i
     }
     p->ranks.assign((size_t)n_d, Rank());
     p->covered.assign((size_t)std::max<int64_t>(p->n_buckets, 1), 0);
+    p->norm_covered.assign((size_t)std::max<int64_t>(p->n_buckets, 1), 0);
     p->gathered.assign(p->units.size(), 0);
     *out = p;
     return ZERO_OK;

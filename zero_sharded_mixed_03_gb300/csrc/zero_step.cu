@@ -44,15 +44,19 @@ struct DevState {
     uint32_t flag;          // OR of the non-finite flags of the open step
     uint32_t cur;           // current half of every ping-pong pair
     uint32_t last_skipped;  // 1 if the last finished step was skipped
-    uint32_t pad0;
+    uint32_t blocks_done;   // blocks of the running norm launch that have stored their partial
     int64_t t;              // applied steps
     int64_t skipped;        // skipped steps, total
     int64_t good;           // applied steps since the last change of the loss scale
     int64_t finished;       // finished steps (applied + skipped)
     double scale;           // loss scale of the next step
-    int64_t pad1;
+    double norm2;           // open step: sum of fp32(g*g) so far
+    double last_norm2;      // last finished step's sum
+    uint32_t norm_valid;    // open step computed a norm
+    uint32_t last_norm_valid;
+    int64_t pad[2];
 };
-static_assert(sizeof(DevState) == 64, "DevState layout");
+static_assert(sizeof(DevState) == 96, "DevState layout");
 
 static_assert(sizeof(DevState) <= kStateBytes, "DevState fits its workspace slot");
 
@@ -85,7 +89,9 @@ struct StepParams {
     int32_t pad;
     int64_t total_vec;
     uint32_t* flag;
-    const DevState* st;        // nullptr: host mode (constants in k, current half 0)
+    DevState* st;              // nullptr: host mode (constants in k, current half 0)
+    double max_norm;           // clip mode: the bound on the global gradient norm
+    double* partials;          // norm modes: one slot per block
 };
 
 struct CommitParams {
@@ -157,11 +163,32 @@ __device__ __forceinline__ bool nonfinite(float g)
     return (__float_as_uint(g) & 0x7F800000u) == 0x7F800000u;
 }
 
-// The three constants that depend on t and the loss scale, formed per block.
+// The constants that depend on t, the loss scale and the gradient norm, formed per block.
 struct StepK {
     float step;   // lr / (1 - beta1^t)
     float bc2s;   // sqrt(1 - beta2^t)
     float inv;    // 1 / (N_d * loss_scale)
+    float coef;   // clip mode: min(1, max_norm / (norm + 1e-6)); else 1
+};
+
+// What the fused kernel does with the gradient norm.
+enum { kPlain = 0, kNormAcc = 1, kClip = 2 };
+
+// Per-thread sum of the fp32 squares as an unevaluated pair hi + lo of floats, extended by an
+// error-free TwoSum (Knuth) per term: ~48 significant bits from fp32 operations only (GB300's
+// fp64 rate is far below its fp32 rate).  Converted to double once, at the end of the thread.
+struct NormAcc {
+    float hi = 0.0f, lo = 0.0f;
+    __device__ __forceinline__ void add(float p)
+    {
+        const float s = __fadd_rn(hi, p);
+        const float bp = __fsub_rn(s, hi);
+        const float ap = __fsub_rn(s, bp);
+        const float e = __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(p, bp));
+        hi = s;
+        lo = __fadd_rn(lo, e);
+    }
+    __device__ __forceinline__ double value() const { return (double)hi + (double)lo; }
 };
 
 // AdamW on one element with separately rounded IEEE operations (no contraction):
@@ -192,6 +219,7 @@ __device__ __forceinline__ void block_constants(const StepParams& P, float* sk, 
         sk[0] = P.k[6];
         sk[1] = P.k[7];
         sk[2] = P.k[8];
+        sk[3] = 1.0f;
         int cur = 0;
         if (P.st) {
             const volatile DevState* st = P.st;
@@ -208,6 +236,11 @@ __device__ __forceinline__ void block_constants(const StepParams& P, float* sk, 
             sk[0] = __double2float_rn(__ddiv_rn(P.lr, bc1));
             sk[1] = __double2float_rn(bc2s);
             sk[2] = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)P.n_d, st->scale)));
+            if (P.max_norm > 0.0) {
+                double c = __ddiv_rn(P.max_norm, __dadd_rn(__dsqrt_rn(st->norm2), 1e-6));
+                if (c > 1.0) c = 1.0;
+                sk[3] = __double2float_rn(c);
+            }
             cur = (int)st->cur;
         }
         *scur = cur;
@@ -217,15 +250,17 @@ __device__ __forceinline__ void block_constants(const StepParams& P, float* sk, 
 
 // ------------------------------------------------------------------ fused step kernel
 
-template <int DT>
+template <int DT, int MODE>
 __device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, int64_t e,
-                                            const StepK& sk, int cur)
+                                            const StepK& sk, int cur, NormAcc& norm2)
 {
     float sum = 0.0f;
     for (int r = 0; r < P.n_d; ++r) sum = __fadd_rn(sum, widen1<DT>(P.c[r][S.c_off + e]));
     const float g = __fmul_rn(sum, sk.inv);
+    if constexpr (MODE == kNormAcc) norm2.add(__fmul_rn(g, g));
+    const float gu = MODE == kClip ? __fmul_rn(g, sk.coef) : g;
     float p = S.p[cur][e], m = S.m[cur][e], v = S.v[cur][e];
-    adamw1(g, p, m, v, P.k, sk);
+    adamw1(gu, p, m, v, P.k, sk);
     S.p[cur ^ 1][e] = p;
     S.m[cur ^ 1][e] = m;
     S.v[cur ^ 1][e] = v;
@@ -235,9 +270,9 @@ __device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, 
 
 // Eight consecutive elements starting at e: 128-bit loads of the N_d contribution slices
 // (batches of NB ranks in flight), 2 x 128-bit per fp32 state array, 128-bit 16-bit store.
-template <int DT, int NB>
+template <int DT, int NB, int MODE>
 __device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, int64_t e,
-                                          const StepK& sk, int cur)
+                                          const StepK& sk, int cur, NormAcc& norm2)
 {
     const float* pin = S.p[cur] + e;
     const float* min_ = S.m[cur] + e;
@@ -280,7 +315,9 @@ __device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, in
     for (int j = 0; j < 8; ++j) {
         const float g = __fmul_rn(acc[j], sk.inv);
         bad |= nonfinite(g);
-        adamw1(g, p[j], m[j], v[j], P.k, sk);
+        if constexpr (MODE == kNormAcc) norm2.add(__fmul_rn(g, g));
+        const float gu = MODE == kClip ? __fmul_rn(g, sk.coef) : g;
+        adamw1(gu, p[j], m[j], v[j], P.k, sk);
     }
     float4* pout = reinterpret_cast<float4*>(S.p[cur ^ 1] + e);
     float4* mout = reinterpret_cast<float4*>(S.m[cur ^ 1] + e);
@@ -300,21 +337,68 @@ __device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, in
     return bad;
 }
 
+// Sum of one double over the block in a fixed pattern (shuffle tree per warp, warps in order);
+// the result is valid in thread 0.
+__device__ __forceinline__ double block_sum_fixed(double x, double* warp_sum)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xFFFFFFFFu, x, o);
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = x;
+    __syncthreads();
+    double b = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kThreads / 32; ++w) b += warp_sum[w];
+    __syncthreads();
+    return b;
+}
+
+// Block sum of the per-thread norm partials, stored in this block's slot; the last block of
+// the launch to store (an atomic ticket, nothing waits) adds all slots to the step's norm in a
+// fixed order (thread t takes slots t, t + 128, ...; then the fixed block pattern), so the sum
+// does not depend on which blocks finish first.
+__device__ __forceinline__ void block_norm_commit(const StepParams& P, double part)
+{
+    __shared__ double warp_sum[kThreads / 32];
+    __shared__ bool last;
+    const double b = block_sum_fixed(part, warp_sum);
+    if (threadIdx.x == 0) {
+        P.partials[blockIdx.x] = b;
+        __threadfence();
+        const unsigned ticket = atomicAdd(&P.st->blocks_done, 1u);
+        last = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const volatile double* slots = P.partials;
+    double x = 0.0;
+    for (unsigned i = threadIdx.x; i < gridDim.x; i += kThreads) x += slots[i];
+    const double sum = block_sum_fixed(x, warp_sum);
+    if (threadIdx.x == 0) {
+        volatile DevState* st = P.st;
+        st->norm2 = st->norm2 + sum;
+        st->norm_valid = 1;
+        st->blocks_done = 0;
+        __threadfence();
+    }
+}
+
 // Persistent grid-stride kernel over the concatenated body vectors of all segments, plus
 // kScalarSlots scalar slots per segment for the unaligned head and tail.  VEC = 8: 128-bit
 // body; VEC = 1: every element is a body vector of one (streams of different phases).
 // Reads the current half of each pair and writes the other.
-template <int DT, int NB, int VEC>
+template <int DT, int NB, int VEC, int MODE>
 __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_constant__ StepParams P)
 {
-    __shared__ float sk3[3];
+    __shared__ float sk4[4];
     __shared__ int scur;
-    block_constants(P, sk3, &scur);
-    const StepK sk = {sk3[0], sk3[1], sk3[2]};
+    block_constants(P, sk4, &scur);
+    const StepK sk = {sk4[0], sk4[1], sk4[2], sk4[3]};
     const int cur = scur;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     bool bad = false;
+    NormAcc norm2;
 
     if constexpr (VEC == 8) {
         for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
@@ -323,7 +407,7 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
             int64_t e = -1;
             if (k < S.head) e = k;
             else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
-            if (e >= 0) bad |= step_scalar<DT>(P, S, e, sk, cur);
+            if (e >= 0) bad |= step_scalar<DT, MODE>(P, S, e, sk, cur, norm2);
         }
     }
 
@@ -331,12 +415,83 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
     for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
         while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
         const KSeg& S = P.seg[s];
-        if constexpr (VEC == 8) bad |= step_vec8<DT, NB>(P, S, S.head + 8 * (vi - S.vbeg), sk, cur);
-        else bad |= step_scalar<DT>(P, S, vi - S.vbeg, sk, cur);
+        if constexpr (VEC == 8)
+            bad |= step_vec8<DT, NB, MODE>(P, S, S.head + 8 * (vi - S.vbeg), sk, cur, norm2);
+        else
+            bad |= step_scalar<DT, MODE>(P, S, vi - S.vbeg, sk, cur, norm2);
     }
 
     // Global non-finite flag: one OR across the block, one atomic per block that saw one.
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(P.flag, 1u);
+    if constexpr (MODE == kNormAcc) block_norm_commit(P, norm2.value());
+}
+
+// Gradient-norm pre-pass: the reduction of the fused kernel without the update; reads only
+// the contributions.
+template <int DT, int NB, int VEC>
+__global__ void __launch_bounds__(kThreads) grad_norm_kernel(const __grid_constant__ StepParams P)
+{
+    __shared__ float sk4[4];
+    __shared__ int scur;
+    block_constants(P, sk4, &scur);
+    const float inv = sk4[2];
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    NormAcc norm2;
+    auto one = [&](const KSeg& S, int64_t e) {
+        float sum = 0.0f;
+        for (int r = 0; r < P.n_d; ++r) sum = __fadd_rn(sum, widen1<DT>(P.c[r][S.c_off + e]));
+        const float g = __fmul_rn(sum, inv);
+        norm2.add(__fmul_rn(g, g));
+    };
+    if constexpr (VEC == 8) {
+        for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
+            const KSeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) one(S, e);
+        }
+    }
+    int s = 0;
+    for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
+        while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
+        const KSeg& S = P.seg[s];
+        if constexpr (VEC == 8) {
+            const int64_t e = S.head + 8 * (vi - S.vbeg);
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+            for (int r0 = 0; r0 < P.n_d; r0 += NB) {
+                uint4 c[NB];
+#pragma unroll
+                for (int q = 0; q < NB; ++q)
+                    if (r0 + q < P.n_d) c[q] = ld_stream(P.c[r0 + q] + S.c_off + e);
+#pragma unroll
+                for (int q = 0; q < NB; ++q) {
+                    if (r0 + q < P.n_d) {
+                        const uint32_t w[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float lo, hi;
+                            widen2<DT>(w[j], lo, hi);
+                            acc[2 * j] = __fadd_rn(acc[2 * j], lo);
+                            acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], hi);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float g = __fmul_rn(acc[j], inv);
+                norm2.add(__fmul_rn(g, g));
+            }
+        } else {
+            one(S, vi - S.vbeg);
+        }
+    }
+    block_norm_commit(P, norm2.value());
 }
 
 // ------------------------------------------------------------------ skip: re-cast + commit
@@ -416,6 +571,10 @@ __global__ void commit_kernel(const CommitParams C)
     }
     st->finished = st->finished + 1;
     st->flag = 0;
+    st->last_norm2 = st->norm2;
+    st->last_norm_valid = st->norm_valid;
+    st->norm2 = 0.0;
+    st->norm_valid = 0;
 }
 
 // ------------------------------------------------------------------ gather kernel (stage 3)
@@ -498,6 +657,11 @@ zero_status_t cuda_fail(cudaError_t e, const char* what)
 }
 
 DevState* dev_state(const zero_plan* p) { return reinterpret_cast<DevState*>(p->workspace); }
+double* norm_slots(const zero_plan* p)
+{
+    return reinterpret_cast<double*>(reinterpret_cast<char*>(p->workspace) + kStateBytes +
+                                      16 * (kBiasCap + 1));
+}
 const double* bias_table(const zero_plan* p)
 {
     return reinterpret_cast<const double*>(reinterpret_cast<const char*>(p->workspace) + kStateBytes);
@@ -552,16 +716,39 @@ void finalize_vectors(StepParams& P, bool vec)
     P.total_vec = acc;
 }
 
+template <typename K>
+void launch_grid(K kernel, int dev, int64_t work, const StepParams& P, cudaStream_t st)
+{
+    int grid = grid_for(kernel, dev, work);
+    if (P.partials) grid = (int)std::min<int64_t>(grid, kNormSlots);
+    kernel<<<grid, kThreads, 0, st>>>(P);
+}
+
+template <int DT, int MODE>
+void launch_fused_mode(int dev, const StepParams& P, bool vec, int64_t work, cudaStream_t st)
+{
+    if (!vec) launch_grid(fused_step_kernel<DT, 1, 1, MODE>, dev, work, P, st);
+    else launch_grid(fused_step_kernel<DT, kRankBatch, 8, MODE>, dev, work, P, st);
+}
+
 template <int DT>
-cudaError_t launch_fused(int dev, StepParams& P, bool vec, cudaStream_t st)
+cudaError_t launch_fused(int dev, StepParams& P, bool vec, cudaStream_t st, int mode = kPlain)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
-    if (!vec)
-        fused_step_kernel<DT, 1, 1><<<grid_for(fused_step_kernel<DT, 1, 1>, dev, work), kThreads, 0, st>>>(P);
-    else
-        fused_step_kernel<DT, kRankBatch, 8>
-            <<<grid_for(fused_step_kernel<DT, kRankBatch, 8>, dev, work), kThreads, 0, st>>>(P);
+    if (mode == kNormAcc) launch_fused_mode<DT, kNormAcc>(dev, P, vec, work, st);
+    else if (mode == kClip) launch_fused_mode<DT, kClip>(dev, P, vec, work, st);
+    else launch_fused_mode<DT, kPlain>(dev, P, vec, work, st);
+    return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_norm(int dev, StepParams& P, bool vec, cudaStream_t st)
+{
+    finalize_vectors(P, vec);
+    const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
+    if (!vec) launch_grid(grad_norm_kernel<DT, 1, 1>, dev, work, P, st);
+    else launch_grid(grad_norm_kernel<DT, kRankBatch, 8>, dev, work, P, st);
     return cudaGetLastError();
 }
 
@@ -632,7 +819,52 @@ zero_status_t read_state(zero_plan* p, cudaStream_t s, zero_step_result_t* out)
     out->good_steps = host.good;
     out->skipped_total = host.skipped;
     out->finished = host.finished;
+    out->grad_norm = host.last_norm_valid ? std::sqrt(host.last_norm2) : -1.0;
     return ZERO_OK;
+}
+
+// Arguments shared by zero_step and zero_grad_norm.
+zero_status_t check_call(const zero_plan_t* p, const void* const* grad_contribs,
+                         int64_t n_contribs, int64_t which, const char* fn)
+{
+    const std::string f(fn);
+    if (!p || !grad_contribs) return fail(ZERO_EINVAL, f + ": NULL argument");
+    if (n_contribs != p->n_d) return fail(ZERO_EINVAL, f + ": need one contribution per rank");
+    if (!p->workspace) return fail(ZERO_ESTATE, f + ": no rank bound");
+    bool any = false;
+    for (const Rank& R : p->ranks) any |= R.bound;
+    if (!any) return fail(ZERO_ESTATE, f + ": no rank bound");
+    for (int64_t r = 0; r < n_contribs; ++r) {
+        if (!grad_contribs[r]) return fail(ZERO_EINVAL, f + ": NULL contribution");
+        if (!aligned(grad_contribs[r], 2))
+            return fail(ZERO_EALIGN, f + ": contribution not 2-byte aligned");
+    }
+    if (p->stage == 3) {
+        if (which < 0 || which >= (int64_t)p->units.size())
+            return fail(ZERO_EINVAL, f + ": unit out of range");
+    } else if (which < -1 || which >= p->n_buckets) {
+        return fail(ZERO_EINVAL, f + ": bucket out of range");
+    }
+    return ZERO_OK;
+}
+
+// Fill and launch one chunk of segments [b, e) of a zero_step / zero_grad_norm call.
+void fill_call_params(const zero_plan* p, const void* const* grad_contribs, StepParams& P)
+{
+    std::memset(&P, 0, sizeof(P));
+    for (int r = 0; r < p->n_d; ++r) P.c[r] = (const uint16_t*)grad_contribs[r];
+    std::memcpy(P.k, p->consts, sizeof(P.k));
+    P.lr = p->step_hyper.lr;
+    P.beta1 = p->step_hyper.beta1;
+    P.beta2 = p->step_hyper.beta2;
+    P.bias = bias_table(p);
+    P.bias_len = p->bias_len;
+    P.bias_saturates = p->bias_saturates;
+    P.n_d = p->n_d;
+    P.st = dev_state(p);
+    P.flag = &dev_state(p)->flag;
+    P.partials = norm_slots(p);
+    P.max_norm = 0.0;
 }
 
 }  // namespace
@@ -741,29 +973,51 @@ zero_status_t zero_set_scaler(zero_plan_t* p, const zero_scaler_t* cfg, void* st
     return ZERO_OK;
 }
 
+zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
+                             int64_t which, void* stream)
+{
+    zero_status_t st = check_call(p, grad_contribs, n_contribs, which, "zero_grad_norm");
+    if (st != ZERO_OK) return st;
+    if (p->in_step)
+        return fail(ZERO_ESTATE, "zero_grad_norm: the norm must precede every zero_step of a step");
+    if (which == -1) {
+        if (p->norm_open) return fail(ZERO_ESTATE, "zero_grad_norm: bucket -1 must be the only call");
+    } else if (p->norm_covered[(size_t)which]) {
+        return fail(ZERO_ESTATE, "zero_grad_norm: bucket/unit already included");
+    }
+    st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const std::vector<Segment> segs = step_segments(p, which, 0);
+    for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
+        const size_t e = std::min(segs.size(), b + kMaxSegs);
+        StepParams P;
+        fill_call_params(p, grad_contribs, P);
+        const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
+        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_norm<ZERO_BF16>(p->device, P, vec, s)
+                                                        : launch_norm<ZERO_FP16>(p->device, P, vec, s);
+        if (err != cudaSuccess) return cuda_fail(err, "gradient-norm launch");
+    }
+    p->norm_open = true;
+    if (which == -1) std::fill(p->norm_covered.begin(), p->norm_covered.end(), 1);
+    else p->norm_covered[(size_t)which] = 1;
+    return ZERO_OK;
+}
+
 zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
                         int64_t which, const zero_hyper_t* hyper, void* stream)
 {
-    if (!p || !grad_contribs || !hyper) return fail(ZERO_EINVAL, "zero_step: NULL argument");
-    if (n_contribs != p->n_d) return fail(ZERO_EINVAL, "zero_step: need one contribution per rank");
-    if (!p->workspace) return fail(ZERO_ESTATE, "zero_step: no rank bound");
-    bool any = false;
-    for (const Rank& R : p->ranks) any |= R.bound;
-    if (!any) return fail(ZERO_ESTATE, "zero_step: no rank bound");
-    for (int64_t r = 0; r < n_contribs; ++r) {
-        if (!grad_contribs[r]) return fail(ZERO_EINVAL, "zero_step: NULL contribution");
-        if (!aligned(grad_contribs[r], 2))
-            return fail(ZERO_EALIGN, "zero_step: contribution not 2-byte aligned");
-    }
+    if (!hyper) return fail(ZERO_EINVAL, "zero_step: NULL argument");
+    zero_status_t cst = check_call(p, grad_contribs, n_contribs, which, "zero_step");
+    if (cst != ZERO_OK) return cst;
     if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
-        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay))
-        return fail(ZERO_EINVAL, "zero_step: betas must lie in [0, 1) and lr, eps, wd be finite");
-    if (p->stage == 3) {
-        if (which < 0 || which >= (int64_t)p->units.size())
-            return fail(ZERO_EINVAL, "zero_step: unit out of range");
-    } else if (which < -1 || which >= p->n_buckets) {
-        return fail(ZERO_EINVAL, "zero_step: bucket out of range");
-    }
+        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay) ||
+        !(hyper->max_grad_norm >= 0.0) || !std::isfinite(hyper->max_grad_norm))
+        return fail(ZERO_EINVAL, "zero_step: betas must lie in [0, 1); lr, eps, wd, max_grad_norm finite");
+    if (hyper->max_grad_norm > 0.0)
+        for (int64_t b = 0; b < p->n_buckets; ++b)
+            if (!p->norm_covered[(size_t)b])
+                return fail(ZERO_ESTATE, "zero_step: clipping needs zero_grad_norm over every bucket/unit first");
     if (p->in_step && std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0)
         return fail(ZERO_EINVAL, "zero_step: hyperparameters changed inside a step");
     if (which == -1) {
@@ -785,25 +1039,19 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
         step_constants(*hyper, 1, 1.0, p->n_d, p->consts);
         p->step_hyper = *hyper;
     }
+    // clip: the norm is complete on the device; report: accumulate it in this pass
+    int mode = kPlain;
+    if (hyper->max_grad_norm > 0.0) mode = kClip;
+    else if ((hyper->flags & ZERO_REPORT_GRAD_NORM) && !p->norm_open) mode = kNormAcc;
     const std::vector<Segment> segs = step_segments(p, which, 0);
     for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
         const size_t e = std::min(segs.size(), b + kMaxSegs);
         StepParams P;
-        std::memset(&P, 0, sizeof(P));
-        for (int r = 0; r < p->n_d; ++r) P.c[r] = (const uint16_t*)grad_contribs[r];
-        std::memcpy(P.k, p->consts, sizeof(P.k));
-        P.lr = hyper->lr;
-        P.beta1 = hyper->beta1;
-        P.beta2 = hyper->beta2;
-        P.bias = bias_table(p);
-        P.bias_len = p->bias_len;
-        P.bias_saturates = p->bias_saturates;
-        P.n_d = p->n_d;
-        P.st = dev_state(p);
-        P.flag = &dev_state(p)->flag;
+        fill_call_params(p, grad_contribs, P);
+        P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
         const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
-        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_fused<ZERO_BF16>(p->device, P, vec, s)
-                                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s);
+        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode)
+                                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode);
         if (err != cudaSuccess) return cuda_fail(err, "fused step launch");
     }
     p->in_step = true;
@@ -848,7 +1096,9 @@ zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t*
     if (e != cudaSuccess) return cuda_fail(e, "commit launch");
     p->in_step = false;
     p->stepped = true;
+    p->norm_open = false;
     std::fill(p->covered.begin(), p->covered.end(), 0);
+    std::fill(p->norm_covered.begin(), p->norm_covered.end(), 0);
     if (out) return read_state(p, s, out);
     return ZERO_OK;
 }
@@ -1012,6 +1262,8 @@ zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d,
     if (dtype16 != ZERO_BF16 && dtype16 != ZERO_FP16)
         return fail(ZERO_EINVAL, "zero_step_range_noalloc: bad dtype16");
     if (t < 1) return fail(ZERO_EINVAL, "zero_step_range_noalloc: t must be >= 1");
+    if (hyper->max_grad_norm != 0.0 || hyper->flags != 0)
+        return fail(ZERO_EINVAL, "zero_step_range_noalloc: no gradient-norm options here");
     if (!(loss_scale > 0.0) || !std::isfinite(loss_scale))
         return fail(ZERO_EINVAL, "zero_step_range_noalloc: bad loss scale");
     const float* fin[3] = {master_in, m_in, v_in};

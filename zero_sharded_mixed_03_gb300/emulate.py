@@ -14,7 +14,8 @@ import torch
 
 from . import (ZERO_BF16, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS, zero_bind, zero_bind_peer,
                zero_gather_layer, zero_plan_create, zero_plan_destroy, zero_plan_info,
-               zero_plan_tables, zero_rank_state_elems, zero_read_state, zero_release_layer,
+               zero_grad_norm, zero_plan_tables, zero_rank_state_elems, zero_read_state,
+               zero_release_layer,
                zero_set_scaler, zero_step, zero_step_finish)
 
 
@@ -102,6 +103,10 @@ class EmulatedGroup:
     # ------------------------------------------------------------------ the step
     def step(self, contribs: Sequence[int], which: int, hyper, stream=None) -> None:
         zero_step(self.plan, list(contribs), which, hyper, _stream_handle(stream))
+
+    def grad_norm(self, contribs: Sequence[int], which: int, stream=None) -> None:
+        """Gradient-norm pre-pass of one bucket/unit (needed before a clipping step)."""
+        zero_grad_norm(self.plan, list(contribs), which, _stream_handle(stream))
 
     def finish(self, stream=None, wait: bool = True):
         """Commit the step on the device; wait=True also returns the read-back state."""
