@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=4_194_304)
     ap.add_argument("--mem-budget-gb", type=float, default=160.0)
+    ap.add_argument("--overlap", action="store_true",
+                    help="stage 3: gather unit u+1 on a second stream while unit u steps "
+                         "(zero_step_units_overlapped); no per-launch events in this mode")
     ap.add_argument("--grad-norm", choices=["off", "report", "clip"], default="off",
                     help="report: global gradient norm inside the fused pass; clip: norm pre-pass "
                          "over every bucket/unit, then the update clipped at max norm 1.0")
@@ -227,6 +230,19 @@ class Bench:
         # compact slice o holds flat [a, e), which the kernel addresses as call offset `rel`
         return [bufs[r].data_ptr() + 2 * (o - rel) for r in range(self.w.n_d)]
 
+    def step_overlapped(self, bufs, comm, wait=False):
+        """Whole stage-3 step through zero_step_units_overlapped; returns (result, launches)."""
+        if not hasattr(self, "_gbufs"):
+            n = max(8, int(self.info.max_unit_pad))
+            self._gbufs = [self.torch.empty(n, dtype=self.torch.int16, device="cuda") for _ in range(2)]
+        ptrs = [p for ci in range(len(self.calls)) for p in self.call_ptrs(bufs, ci)]
+        res = self.Z.zero_step_units_overlapped(
+            self.g.plan, ptrs, [b.data_ptr() for b in self._gbufs], self.hyper,
+            self.torch.cuda.current_stream().cuda_stream, comm.cuda_stream, wait)
+        n_segs = len(self.bound) * len(self.units)
+        launches = (2 + self.clip) * len(self.calls) + (n_segs + 31) // 32 + 1
+        return res, launches
+
     def step(self, bufs, events=None, gather_events=None, wait=False):
         """Enqueue one step; with wait=True also read the step result back (synchronises).
 
@@ -297,9 +313,14 @@ def gpu_arm(args, world, rank, local):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record()
+    overlap = args.overlap and w.stage == 3
+    comm = torch.cuda.Stream() if overlap else None
     for k in range(args.steps):
-        _, n = b.step(b.sets[(args.warmup + k) % b.n_sets], ev_fused,
-                      ev_gather if w.stage == 3 else None)
+        if overlap:
+            _, n = b.step_overlapped(b.sets[(args.warmup + k) % b.n_sets], comm)
+        else:
+            _, n = b.step(b.sets[(args.warmup + k) % b.n_sets], ev_fused,
+                          ev_gather if w.stage == 3 else None)
         launches += n
     t1.record()
     torch.cuda.synchronize()
@@ -310,8 +331,8 @@ def gpu_arm(args, world, rank, local):
     if dist:
         ms = max_over_ranks(ms, dist)
     skipped = b.g.step_state().skipped_total - skipped_before
-    fused_ms = [a.elapsed_time(c) for a, c in fused_pairs]
-    gather_ms = [a.elapsed_time(c) for a, c in gather_pairs]
+    fused_ms = [] if overlap else [a.elapsed_time(c) for a, c in fused_pairs]
+    gather_ms = [] if overlap else [a.elapsed_time(c) for a, c in gather_pairs]
 
     applied = args.steps - skipped
     elems = b.elems_per_step
@@ -331,6 +352,8 @@ def gpu_arm(args, world, rank, local):
                 "peak_source": peak_kind, "kernel": "fused_step_kernel",
                 "launch_bytes": int(launch_bytes), "avg_launch_us": round(avg_fused_s * 1e6, 2),
                 "launches_timed": len(fused_ms)}
+    if not fused_ms:                                # overlapped schedule: no per-launch events
+        roofline = None
     if gather_ms:
         g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
         roofline["gather_achieved_gbs"] = round(g_bytes / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
@@ -344,7 +367,8 @@ def gpu_arm(args, world, rank, local):
                       "units": len(b.units), "bound_ranks": len(b.bound),
                       "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
-                      "contribution_sets": b.n_sets, "grad_norm": args.grad_norm},
+                      "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
+                      "overlap": overlap},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,
            "clocks": clk}

@@ -251,6 +251,20 @@ zero_status_t zero_restore_state(zero_plan_t* plan, const zero_step_result_t* in
  * included).  The unit stays "gathered" until zero_release_layer. */
 zero_status_t zero_gather_layer(zero_plan_t* plan, int64_t unit, void* full_unit16, void* stream);
 
+/* A whole stage-3 step with the all-gather overlapped ("Overlapping Computation and
+ * Communication Streams"): for every unit u in order, `comm_stream` gathers u into
+ * gather_bufs[u % 2] (each max_unit_pad elements) while `compute_stream` runs the fused step
+ * of unit u-1; unit u's step waits only for its own gather (the point where a layer's
+ * backward would consume W_u), and a buffer is re-filled only after the step that followed
+ * its gather has been enqueued past it.  Ends with zero_step_finish on `compute_stream`
+ * (out as there).  unit_contribs: n_units * N_d pointers, unit-major (unit u's N_d
+ * contributions at [u * N_d]).  With max_grad_norm > 0 a norm pre-pass over every unit runs
+ * first on compute_stream.  Stage 3 only; the two streams must differ. */
+zero_status_t zero_step_units_overlapped(zero_plan_t* plan, const void* const* unit_contribs,
+                                         int64_t n_ptrs, void* const* gather_bufs,
+                                         const zero_hyper_t* hyper, void* compute_stream,
+                                         void* comm_stream, zero_step_result_t* out);
+
 /* Mark unit `unit`'s gathered buffer free; the caller may reuse its memory. */
 zero_status_t zero_release_layer(zero_plan_t* plan, int64_t unit);
 

@@ -435,3 +435,59 @@ def test_norm_is_deterministic_and_pass_order_is_checked():
         run.g.finish()
     finally:
         run.close()
+
+
+# ---------------------------------------------------------------------- overlapped stage-3 schedule
+
+OVERLAP_CASES = {
+    "z3_nd16_units": SMALL_CASES["z3_nd16_units"],
+    "z3_nd3_fp16_peers_skip_first": SMALL_CASES["z3_nd3_fp16_peers_skip_first"],
+    "z3_nd16_units_clip": CLIP_CASES["z3_nd16_units_clip"],
+}
+
+
+@pytest.mark.parametrize("name", list(OVERLAP_CASES))
+def test_overlapped_stage3_schedule_full_parity(name):
+    """Gathers on a second stream, double-buffered, against the oracle: states, shards and the
+    last two gathered units (left in the two buffers) must match."""
+    w = OVERLAP_CASES[name]
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    comm = torch.cuda.Stream()
+    nu = len(run.units)
+    maxu = int(run.info.max_unit_pad)
+    bufs = [torch.empty(max(8, maxu), dtype=torch.int16, device="cuda") for _ in range(2)]
+    contribs = [[torch.empty(max(8, U[3]), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+                for U in run.units]
+    try:
+        for k in range(1, w.steps + 1):
+            expect_g = [o.gathered(u) for u in range(nu)]
+            for u, (which, lo, hi) in enumerate(run.ranges()):
+                for r in range(w.n_d):
+                    H.fill_device(contribs[u][r], synth.grad_stream(w, k, r), run.units, lo, hi)
+            ptrs = [c.data_ptr() for unit in contribs for c in unit]
+            res = Z.zero_step_units_overlapped(run.g.plan, ptrs, [b.data_ptr() for b in bufs],
+                                               run.hyper, torch.cuda.current_stream().cuda_stream,
+                                               comm.cuda_stream)
+            flag = o.step(k)
+            assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale
+            torch.cuda.synchronize()
+            for u in range(max(0, nu - 2), nu):
+                got = bufs[u % 2][:run.units[u][3]].cpu().numpy().view(np.uint16)
+                assert np.array_equal(got, expect_g[u]), f"gathered unit {u} at step {k}"
+            _compare_full(run, o, f"overlapped {name} step {k}")
+    finally:
+        run.close()
+
+
+def test_overlapped_schedule_argument_errors():
+    w = SMALL_CASES["z2_nd7_ragged_tensors"]
+    run = H.Run(w)
+    try:
+        s = torch.cuda.current_stream().cuda_stream
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_step_units_overlapped(run.g.plan, [run.contribs[0].data_ptr()] * w.n_d,
+                                         [0x1000, 0x2000], run.hyper, s, torch.cuda.Stream().cuda_stream)
+        assert e.value.status == Z.ZERO_EINVAL                     # stage 3 only
+    finally:
+        run.close()

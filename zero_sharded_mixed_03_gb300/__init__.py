@@ -29,6 +29,7 @@ EXPORTED = ["zero_plan_create", "zero_plan_info", "zero_rank_state_elems", "zero
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",
             "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_set_scaler",
             "zero_read_state", "zero_restore_state", "zero_grad_norm",
+            "zero_step_units_overlapped",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
@@ -119,6 +120,9 @@ def lib() -> ctypes.CDLL:
         L.zero_set_scaler.argtypes = [_vp, ctypes.POINTER(zero_scaler_t), _vp]
         L.zero_read_state.restype = st
         L.zero_read_state.argtypes = [_vp, _vp, ctypes.POINTER(zero_step_result_t)]
+        L.zero_step_units_overlapped.restype = st
+        L.zero_step_units_overlapped.argtypes = [_vp, _vp, _i64, _vp, ctypes.POINTER(zero_hyper_t),
+                                                 _vp, _vp, ctypes.POINTER(zero_step_result_t)]
         L.zero_grad_norm.restype = st
         L.zero_grad_norm.argtypes = [_vp, _vp, _i64, _i64, _vp]
         L.zero_restore_state.restype = st
@@ -222,6 +226,17 @@ def zero_step(plan: int, grad_contribs: Sequence[int], which: int, hyper: zero_h
 def zero_grad_norm(plan: int, grad_contribs: Sequence[int], which: int, stream: int = 0) -> None:
     _check(lib().zero_grad_norm(plan, _ptr_array(grad_contribs), len(grad_contribs), which,
                                 stream or None))
+
+
+def zero_step_units_overlapped(plan: int, unit_contribs: Sequence[int], gather_bufs: Sequence[int],
+                               hyper: zero_hyper_t, compute_stream: int, comm_stream: int,
+                               wait: bool = True) -> Optional[zero_step_result_t]:
+    res = zero_step_result_t() if wait else None
+    _check(lib().zero_step_units_overlapped(plan, _ptr_array(unit_contribs), len(unit_contribs),
+                                            _ptr_array(gather_bufs), ctypes.byref(hyper),
+                                            compute_stream or None, comm_stream or None,
+                                            ctypes.byref(res) if res is not None else None))
+    return res
 
 
 def zero_step_finish(plan: int, stream: int = 0, wait: bool = True) -> Optional[zero_step_result_t]:

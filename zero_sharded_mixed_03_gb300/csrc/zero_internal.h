@@ -95,6 +95,10 @@ struct zero_plan {
     int bias_saturates = 0;
     double bias_beta1 = -1.0, bias_beta2 = -1.0;
     std::vector<char> gathered;         // stage 3: per unit
+    // Overlapped stage-3 schedule: CUDA events (created on first use, released by
+    // zero_plan_destroy through the hook the device side installs).
+    void* ov_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    void (*release_hook)(zero_plan*) = nullptr;
 };
 
 namespace zero {

@@ -202,7 +202,11 @@ zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, i
     return ZERO_OK;
 }
 
-void zero_plan_destroy(zero_plan_t* plan) { delete plan; }
+void zero_plan_destroy(zero_plan_t* plan)
+{
+    if (plan && plan->release_hook) plan->release_hook(plan);
+    delete plan;
+}
 
 zero_status_t zero_plan_info(const zero_plan_t* p, zero_plan_info_t* out)
 {

@@ -1203,6 +1203,72 @@ zero_status_t zero_release_layer(zero_plan_t* p, int64_t unit)
     return ZERO_OK;
 }
 
+zero_status_t zero_step_units_overlapped(zero_plan_t* p, const void* const* unit_contribs,
+                                         int64_t n_ptrs, void* const* gather_bufs,
+                                         const zero_hyper_t* hyper, void* compute_stream,
+                                         void* comm_stream, zero_step_result_t* out)
+{
+    if (!p || !unit_contribs || !gather_bufs || !hyper)
+        return fail(ZERO_EINVAL, "zero_step_units_overlapped: NULL argument");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_step_units_overlapped: stage 3 only");
+    const int64_t nu = (int64_t)p->units.size();
+    if (n_ptrs != nu * p->n_d)
+        return fail(ZERO_EINVAL, "zero_step_units_overlapped: need n_units * N_d contributions");
+    if (compute_stream == comm_stream)
+        return fail(ZERO_EINVAL, "zero_step_units_overlapped: the two streams must differ");
+    if (p->in_step) return fail(ZERO_ESTATE, "zero_step_units_overlapped: a step is open");
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    if (!p->ov_events[0]) {
+        for (int i = 0; i < 5; ++i) {
+            cudaEvent_t ev;
+            const cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: event");
+            p->ov_events[i] = ev;
+        }
+        p->release_hook = [](zero_plan* q) {
+            for (void*& ev : q->ov_events)
+                if (ev) {
+                    cudaEventDestroy((cudaEvent_t)ev);
+                    ev = nullptr;
+                }
+        };
+    }
+    cudaStream_t cs = (cudaStream_t)compute_stream, ms = (cudaStream_t)comm_stream;
+    cudaEvent_t start = (cudaEvent_t)p->ov_events[0];
+    cudaEvent_t gathered[2] = {(cudaEvent_t)p->ov_events[1], (cudaEvent_t)p->ov_events[2]};
+    cudaEvent_t released[2] = {(cudaEvent_t)p->ov_events[3], (cudaEvent_t)p->ov_events[4]};
+    const int64_t nd = p->n_d;
+    if (hyper->max_grad_norm > 0.0)
+        for (int64_t u = 0; u < nu; ++u) {
+            st = zero_grad_norm(p, unit_contribs + u * nd, nd, u, compute_stream);
+            if (st != ZERO_OK) return st;
+        }
+    cudaError_t e = cudaEventRecord(start, cs);           // the previous step's shards are final
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ms, start, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: ordering the streams");
+    for (int64_t u = 0; u < nu; ++u) {
+        const int b = (int)(u % 2);
+        if (u >= 2) {
+            e = cudaStreamWaitEvent(ms, released[b], 0);
+            if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: wait release");
+        }
+        st = zero_gather_layer(p, u, gather_bufs[b], comm_stream);
+        if (st != ZERO_OK) return st;
+        e = cudaEventRecord(gathered[b], ms);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, gathered[b], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: wait gather");
+        // (a layer's forward/backward would consume gather_bufs[b] here)
+        st = zero_release_layer(p, u);
+        if (st != ZERO_OK) return st;
+        e = cudaEventRecord(released[b], cs);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: record release");
+        st = zero_step(p, unit_contribs + u * nd, nd, u, hyper, compute_stream);
+        if (st != ZERO_OK) return st;
+    }
+    return zero_step_finish(p, compute_stream, out);
+}
+
 // ---------------------------------------------------------------------------------------
 // No-allocation variant: the fused step over one flat range with its scratch (the non-finite
 // flag) in a library-owned static device array instead of a caller workspace.
