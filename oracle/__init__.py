@@ -69,6 +69,14 @@ def lib():
                                           ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
         L.orc_clip_coef.restype = ctypes.c_float
         L.orc_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
+        L.orc_pp_chunks.restype = i64
+        L.orc_pp_chunks.argtypes = [vp, vp, i64, vp, i64, ctypes.c_int, vp, i64,
+                                    ctypes.POINTER(i64)]
+        L.orc_pp_step.restype = ctypes.c_int
+        L.orc_pp_step.argtypes = [vp, vp, i64, vp, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                  vp, vp, vp, vp]
+        L.orc_pp_gather.restype = ctypes.c_int
+        L.orc_pp_gather.argtypes = [vp, vp, i64, vp, i64, ctypes.c_int, i64, vp, vp]
         L.orc_scaler_update.restype = i64
         L.orc_scaler_update.argtypes = [ctypes.c_int, i64, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(i64), ctypes.c_double, ctypes.c_double, i64,
@@ -173,6 +181,45 @@ class Layout:
         rows = np.zeros((max(1, n), 5), dtype=np.int64)
         L.orc_bucket_segments(self.total_pad, self.n_d, bucket_elems, _p(rows), n)
         return rows[:n]
+
+
+class PerParam:
+    """Oracle of FSDP-2 per-parameter (dim-0) sharding."""
+
+    def __init__(self, sizes, dim0, n_d: int, unit_first=None):
+        self.sizes, self.dim0 = _i64(sizes), _i64(dim0)
+        self.unit_first = None if not unit_first else _i64(unit_first)
+        self.n_units_arg = 0 if self.unit_first is None else self.unit_first.size
+        self.n_d = n_d
+        L = lib()
+        per = i64(0)
+        n = L.orc_pp_chunks(_p(self.sizes), _p(self.dim0), self.sizes.size, _p(self.unit_first),
+                            self.n_units_arg, n_d, None, 0, ctypes.byref(per))
+        if n < 0:
+            raise ValueError("invalid per-parameter layout")
+        rows = np.zeros((max(1, n), 9), dtype=np.int64)
+        L.orc_pp_chunks(_p(self.sizes), _p(self.dim0), self.sizes.size, _p(self.unit_first),
+                        self.n_units_arg, n_d, _p(rows), n, None)
+        self.chunks = rows[:n]       # rank, unit, tensor, row0, rows, cols, c_rows, contrib_off, state_off
+        self.per_rank = per.value
+        firsts = list(self.unit_first) if self.unit_first is not None else [0]
+        ends = firsts[1:] + [self.sizes.size]
+        self.unit_numel = [int(self.sizes[f:e].sum()) for f, e in zip(firsts, ends)]
+        self.unit_base = np.concatenate([[0], np.cumsum(self.unit_numel)]).astype(np.int64)
+
+    def step(self, is_fp16, contribs, bound, p, m, v, shard16, k9) -> int:
+        bound = np.ascontiguousarray(np.asarray(bound, dtype=np.int32))
+        return lib().orc_pp_step(_p(self.sizes), _p(self.dim0), self.sizes.size, _p(self.unit_first),
+                                 self.n_units_arg, self.n_d, is_fp16, _ptrs(contribs), _p(bound),
+                                 _ptrs(p), _ptrs(m), _ptrs(v), _ptrs(shard16), _p(k9))
+
+    def gather(self, unit: int, shard16) -> np.ndarray:
+        out = np.zeros(self.unit_numel[unit], dtype=np.uint16)
+        rc = lib().orc_pp_gather(_p(self.sizes), _p(self.dim0), self.sizes.size, _p(self.unit_first),
+                                 self.n_units_arg, self.n_d, unit, _ptrs(shard16), _p(out))
+        if rc != 0:
+            raise ValueError("invalid gather arguments")
+        return out
 
 
 def memory(phi_pad: int, n_d: int) -> np.ndarray:

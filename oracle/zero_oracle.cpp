@@ -514,6 +514,146 @@ int orc_sharded_step(const int64_t* sizes, int64_t n_tensors, const int64_t* uni
 
 float orc_clip_coef(double norm2, double max_norm) { return clip_coef(norm2, max_norm); }
 
+// ---- FSDP-2 per-parameter sharding ([ZF] "FSDP-2: Per-Parameter Sharding via DTensor
+// (fully_shard)": tensors are sharded individually along their leading dimension, Shard(0),
+// without flattening).  Reading: tensor t with d0_t rows of cols_t = size_t / d0_t elements;
+// chunk c_t = ceil(d0_t / N_d) rows; rank r owns rows [r c_t, min((r+1) c_t, d0_t)); every
+// rank's local shard is c_t * cols_t elements (rows beyond d0_t are padding).  A unit's
+// gradient buffer is its tensors concatenated without padding; rank r's local shards follow
+// each other in (unit, tensor) order. ----
+
+namespace {
+struct PChunk {
+    int64_t rank, unit, tensor, row0, rows, cols, c_rows, contrib_off, state_off;
+};
+
+bool pp_chunks(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors, const int64_t* unit_first,
+               int64_t n_units, int n_d, std::vector<PChunk>& out, std::vector<int64_t>& unit_base,
+               int64_t& per_rank)
+{
+    std::vector<int64_t> firsts;
+    if (unit_first == nullptr || n_units <= 0) firsts.push_back(0);
+    else firsts.assign(unit_first, unit_first + n_units);
+    if (n_d < 1 || firsts[0] != 0) return false;
+    for (size_t u = 1; u < firsts.size(); ++u)
+        if (firsts[u] <= firsts[u - 1] || firsts[u] > n_tensors) return false;
+    for (int64_t t = 0; t < n_tensors; ++t)
+        if (sizes[t] < 0 || dim0[t] < 0 || (dim0[t] == 0 && sizes[t] != 0) ||
+            (dim0[t] > 0 && sizes[t] % dim0[t] != 0))
+            return false;
+    out.clear();
+    unit_base.assign(firsts.size() + 1, 0);
+    for (size_t u = 0; u < firsts.size(); ++u) {
+        const int64_t end = (u + 1 < firsts.size()) ? firsts[u + 1] : n_tensors;
+        int64_t numel = 0;
+        for (int64_t t = firsts[u]; t < end; ++t) numel += sizes[t];
+        unit_base[u + 1] = unit_base[u] + numel;
+    }
+    per_rank = 0;
+    for (int r = 0; r < n_d; ++r) {
+        int64_t state = 0;
+        for (size_t u = 0; u < firsts.size(); ++u) {
+            const int64_t end = (u + 1 < firsts.size()) ? firsts[u + 1] : n_tensors;
+            int64_t off = 0;  // tensor offset inside the unit's gradient buffer
+            for (int64_t t = firsts[u]; t < end; ++t) {
+                PChunk c;
+                c.rank = r;
+                c.unit = (int64_t)u;
+                c.tensor = t;
+                c.cols = dim0[t] > 0 ? sizes[t] / dim0[t] : 0;
+                c.c_rows = (dim0[t] + n_d - 1) / n_d;
+                c.row0 = r * c.c_rows;
+                int64_t last = c.row0 + c.c_rows;
+                if (last > dim0[t]) last = dim0[t];
+                c.rows = last > c.row0 ? last - c.row0 : 0;
+                c.contrib_off = off + c.row0 * c.cols;
+                c.state_off = state;
+                out.push_back(c);
+                state += c.c_rows * c.cols;
+                off += sizes[t];
+            }
+        }
+        per_rank = state;   // the same for every rank
+    }
+    return true;
+}
+}  // namespace
+
+// Rows of 9 int64: rank, unit, tensor, first row, owned rows, cols, chunk rows, offset of the
+// owned rows in the unit's gradient buffer, offset of the local shard in the rank's state.
+// Order: rank, unit, tensor.  Returns the row count (-1 on invalid input).
+int64_t orc_pp_chunks(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
+                      const int64_t* unit_first, int64_t n_units, int n_d, int64_t* rows, int64_t cap,
+                      int64_t* per_rank_out)
+{
+    std::vector<PChunk> ch;
+    std::vector<int64_t> ub;
+    int64_t per_rank = 0;
+    if (!pp_chunks(sizes, dim0, n_tensors, unit_first, n_units, n_d, ch, ub, per_rank)) return -1;
+    if (per_rank_out) *per_rank_out = per_rank;
+    for (size_t i = 0; i < ch.size() && (int64_t)i < cap; ++i) {
+        const PChunk& c = ch[i];
+        const int64_t row[9] = {c.rank, c.unit, c.tensor, c.row0, c.rows, c.cols, c.c_rows,
+                                c.contrib_off, c.state_off};
+        std::memcpy(rows + 9 * i, row, sizeof(row));
+    }
+    return (int64_t)ch.size();
+}
+
+// Whole per-parameter-sharded step.  contrib[r]: rank r's gradient over every unit's buffer
+// (units concatenated, unpadded); p/m/v/shard16[r]: rank r's local shards (padded layout).
+// Returns the global non-finite flag.
+int orc_pp_step(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
+                const int64_t* unit_first, int64_t n_units, int n_d, int is_fp16,
+                const uint16_t* const* contrib, const int32_t* bound, float* const* p,
+                float* const* m, float* const* v, uint16_t* const* shard16, const float* k9)
+{
+    std::vector<PChunk> ch;
+    std::vector<int64_t> ub;
+    int64_t per_rank = 0;
+    if (!pp_chunks(sizes, dim0, n_tensors, unit_first, n_units, n_d, ch, ub, per_rank)) return -1;
+    const Consts k = unpack(k9);
+    std::vector<std::vector<float>> g((size_t)n_d);
+    for (int r = 0; r < n_d; ++r)
+        if (bound[r]) g[(size_t)r].assign((size_t)per_rank, 0.0f);
+    int flag = 0;
+    for (const PChunk& c : ch) {
+        if (!bound[c.rank]) continue;
+        for (int64_t i = 0; i < c.rows * c.cols; ++i) {
+            const float gi = reduce_one(n_d, contrib, ub[(size_t)c.unit] + c.contrib_off + i, is_fp16,
+                                        k.inv);
+            g[(size_t)c.rank][(size_t)(c.state_off + i)] = gi;
+            flag |= nonfinite(gi);
+        }
+    }
+    for (const PChunk& c : ch) {
+        if (!bound[c.rank]) continue;
+        const int r = (int)c.rank;
+        for (int64_t i = 0; i < c.rows * c.cols; ++i) {
+            const size_t j = (size_t)(c.state_off + i);
+            if (!flag) adamw_one(g[(size_t)r][j], p[r][j], m[r][j], v[r][j], k);
+            shard16[r][j] = round16(p[r][j], is_fp16);
+        }
+    }
+    return flag;
+}
+
+// All-gather of unit `unit` into its unpadded buffer: every rank's owned rows of every tensor.
+int orc_pp_gather(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
+                  const int64_t* unit_first, int64_t n_units, int n_d, int64_t unit,
+                  const uint16_t* const* shard16, uint16_t* full_unit)
+{
+    std::vector<PChunk> ch;
+    std::vector<int64_t> ub;
+    int64_t per_rank = 0;
+    if (!pp_chunks(sizes, dim0, n_tensors, unit_first, n_units, n_d, ch, ub, per_rank)) return -1;
+    for (const PChunk& c : ch)
+        if (c.unit == unit)
+            for (int64_t i = 0; i < c.rows * c.cols; ++i)
+                full_unit[c.contrib_off + i] = shard16[c.rank][c.state_off + i];
+    return 0;
+}
+
 // ---- A8 commit/skip of the dynamic loss scale (R5): on a flagged step the
 // scale backs off (not below min_scale) and the clean-step counter restarts;
 // after `interval` consecutive applied steps the scale grows.  Returns the

@@ -632,3 +632,85 @@ def test_norm_is_exact_sum_of_squares():
     _, _, _, norms = _oracle_run_1rank([g16], oracle.round16(np.zeros(777, np.float32), 0),
                                        W.Hyper(), 0.0)
     assert fractions.Fraction(norms[0]) == sum(fractions.Fraction(int(i), 256) ** 2 for i in ints)
+
+
+# ----------------------------------------------------------------- FSDP-2 per-parameter sharding
+
+def _random_pp_case(rng, max_tensors=8):
+    nt = int(rng.integers(1, max_tensors + 1))
+    dim0 = [int(x) for x in rng.integers(0, 9, size=nt)]
+    cols = [int(x) for x in rng.integers(1, 5, size=nt)]
+    sizes = [d * c for d, c in zip(dim0, cols)]
+    units = []
+    if nt > 1 and rng.random() < 0.6:
+        cuts = sorted(set(int(x) for x in rng.integers(1, nt, size=int(rng.integers(1, 3)))))
+        units = [0] + cuts
+    return sizes, dim0, units
+
+
+def test_per_param_chunks_brute_force():
+    """Owner of element (tensor t, row i) = i // ceil(d0_t / N_d), by enumeration."""
+    rng = np.random.default_rng(40)
+    for _ in range(300):
+        sizes, dim0, units = _random_pp_case(rng)
+        n_d = int(rng.integers(1, 7))
+        pp = oracle.PerParam(sizes, dim0, n_d, units)
+        firsts = units or [0]
+        unit_of = {t: max(i for i, f in enumerate(firsts) if f <= t) for t in range(len(sizes))}
+        want, state = [], {r: 0 for r in range(n_d)}
+        for r in range(n_d):
+            for t in range(len(sizes)):
+                u = unit_of[t]
+                cols = sizes[t] // dim0[t] if dim0[t] else 0
+                c_rows = -(-dim0[t] // n_d)
+                owned = [i for i in range(dim0[t]) if i // c_rows == r] if c_rows else []
+                unit_start = sum(sizes[firsts[u]:t])
+                row0 = r * c_rows
+                want.append((r, u, t, row0, len(owned), cols, c_rows, unit_start + row0 * cols, state[r]))
+                assert not owned or owned[0] == row0
+                state[r] += c_rows * cols
+        assert [tuple(int(x) for x in row) for row in pp.chunks] == want
+        assert all(state[r] == pp.per_rank for r in range(n_d))
+
+
+def test_per_param_union_equals_ddp():
+    """[ZF] 'Mathematical Formulation of ZeRO Partitioning Stages': per-parameter sharding also
+    keeps data-parallel semantics -- the owned rows of every rank's update, placed back, equal
+    the unsharded step bit for bit, and gathering the 16-bit shards rebuilds each unit."""
+    rng = np.random.default_rng(41)
+    hyper = W.Hyper()
+    for trial in range(150):
+        sizes, dim0, units = _random_pp_case(rng)
+        n_d = int(rng.integers(1, 7))
+        is_fp16 = int(rng.integers(0, 2))
+        pp = oracle.PerParam(sizes, dim0, n_d, units)
+        n = int(sum(sizes))
+        params16 = _rand16(rng, n, is_fp16, 0.02)
+        contribs = [_rand16(rng, n, is_fp16) for _ in range(n_d)]
+        k9 = oracle.consts(hyper, int(rng.integers(1, 5)), 1.0, n_d)
+        p, m, v, sh = [], [], [], []
+        for r in range(n_d):
+            P = np.zeros(max(1, pp.per_rank), np.float32)
+            S16 = np.zeros(max(1, pp.per_rank), np.uint16)
+            for (rr, u, t, row0, rows, cols, c_rows, coff, soff) in pp.chunks:
+                if rr == r and rows:
+                    g0 = pp.unit_base[u] + coff
+                    S16[soff:soff + rows * cols] = params16[g0:g0 + rows * cols]
+                    P[soff:soff + rows * cols] = oracle.widen16(params16[g0:g0 + rows * cols], is_fp16)
+            p.append(P)
+            m.append(np.zeros_like(P))
+            v.append(np.zeros_like(P))
+            sh.append(S16)
+        assert pp.step(is_fp16, contribs, [1] * n_d, p, m, v, sh, k9) == 0
+        Pd = oracle.widen16(params16, is_fp16).astype(np.float32)
+        Md, Vd = np.zeros(n, np.float32), np.zeros(n, np.float32)
+        out = np.zeros(n, np.uint16)
+        assert oracle.ddp_step(contribs, is_fp16, Pd, Md, Vd, out, k9) == 0
+        for (r, u, t, row0, rows, cols, c_rows, coff, soff) in pp.chunks:
+            g0 = pp.unit_base[u] + coff
+            for mine, ref in ((p[r], Pd), (m[r], Md), (v[r], Vd)):
+                assert np.array_equal(mine[soff:soff + rows * cols].view(np.uint32),
+                                      ref[g0:g0 + rows * cols].view(np.uint32)), trial
+        for u in range(len(pp.unit_numel)):
+            lo = pp.unit_base[u]
+            assert np.array_equal(pp.gather(u, sh), out[lo:lo + pp.unit_numel[u]])
