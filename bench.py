@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=4_194_304)
     ap.add_argument("--mem-budget-gb", type=float, default=160.0)
+    ap.add_argument("--per-param", action="store_true",
+                    help="FSDP-2 per-parameter (dim-0) sharding of the same model")
     ap.add_argument("--overlap", action="store_true",
                     help="stage 3: gather unit u+1 on a second stream while unit u steps "
                          "(zero_step_units_overlapped); no per-launch events in this mode")
@@ -185,6 +187,11 @@ class Bench:
             if self.all_bound:
                 spans.append((lo, hi, off, 0))
                 off += hi - lo
+            elif w.per_param:
+                # a rank's rows are spread over the whole unit: every unit reuses one
+                # unit-sized buffer per contributing rank
+                spans.append((lo, hi, 0, 0))
+                off = max(off, hi - lo)
             else:
                 for r in sorted(self.bound):
                     if w.stage == 3:
@@ -215,11 +222,40 @@ class Bench:
         self.elems_per_step = int(self.info.shard) * len(self.bound)
         self.bytes_per_elem = 2 * w.n_d + 26
         self.hyper = self.run.hyper
+        self._count_launches()
         self.clip = grad_norm == "clip"
         if grad_norm != "off":
             h = self.hyper
             self.hyper = Z.hyper(h.lr, h.beta1, h.beta2, h.eps, h.weight_decay,
                                  1.0 if self.clip else 0.0, grad_norm == "report")
+
+    def _count_launches(self):
+        """Kernel launches per step, from the plan's work items: one launch per 32 items (256
+        when a call has more than 32), per call; gathers copy 32 shards per launch."""
+        def launches(items):
+            return 0 if items == 0 else (1 if items <= 32 else -(-items // 256))
+        bound = set(self.bound)
+        w = self.w
+        fused, gathers = [], []
+        all_items = 0
+        for which, lo, hi in self.calls:
+            if w.per_param:
+                items = sum(1 for c in self.g.chunks if c[1] == which and c[4] > 0 and c[0] in bound)
+                copies = sum(1 for c in self.g.chunks if c[1] == which and c[4] > 0)
+            elif w.stage == 3:
+                items = len(bound) if self.units[which][4] > 0 else 0
+                copies = w.n_d if self.units[which][4] > 0 else 0
+            else:
+                S = self.units[0][4]
+                items = sum(1 for r in bound if max(lo, r * S) < min(hi, (r + 1) * S))
+                copies = 0
+            all_items += items if w.stage == 3 else 0
+            fused.append(launches(items))
+            gathers.append(-(-copies // 32))
+        if w.stage != 3:
+            all_items = len(bound)
+        self.fused_launches, self.gather_launches = fused, gathers
+        self.recast_launches = launches(all_items)
 
     def call_ptrs(self, bufs, ci):
         """Per-rank contribution pointers of call ci: base such that base + c_off hits the slice."""
@@ -239,8 +275,8 @@ class Bench:
         res = self.Z.zero_step_units_overlapped(
             self.g.plan, ptrs, [b.data_ptr() for b in self._gbufs], self.hyper,
             self.torch.cuda.current_stream().cuda_stream, comm.cuda_stream, wait)
-        n_segs = len(self.bound) * len(self.units)
-        launches = (2 + self.clip) * len(self.calls) + (n_segs + 31) // 32 + 1
+        launches = ((1 + self.clip) * sum(self.fused_launches) + sum(self.gather_launches)
+                    + self.recast_launches + 1)
         return res, launches
 
     def step(self, bufs, events=None, gather_events=None, wait=False):
@@ -253,7 +289,7 @@ class Bench:
         if self.clip:
             for ci, (which, lo, hi) in enumerate(self.calls):
                 self.g.grad_norm(self.call_ptrs(bufs, ci), which)
-                launches += 1
+                launches += self.fused_launches[ci]
         for ci, (which, lo, hi) in enumerate(self.calls):
             if self.w.stage == 3:
                 if gather_events is not None:
@@ -263,18 +299,17 @@ class Bench:
                 if gather_events is not None:
                     c.record()
                 self.g.release(which)
-                launches += 1
+                launches += self.gather_launches[ci]
             if events is not None:
                 a, c = next(events)
                 a.record()
             self.g.step(self.call_ptrs(bufs, ci), which, self.hyper)
             if events is not None:
                 c.record()
-            launches += 1
+            launches += self.fused_launches[ci]
         res = self.g.finish(wait=wait)
         # the re-cast kernel(s) (which return at once unless the step was skipped) + the commit
-        n_segs = len(self.bound) * len(self.units)
-        launches += (n_segs + 31) // 32 + 1
+        launches += self.recast_launches + 1
         return res, launches
 
 
@@ -287,6 +322,8 @@ def gpu_arm(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     w = W.workload(args.config)
+    if args.per_param:
+        w = W.per_param_variant(w)
     b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm)
     peak, peak_kind = peaks()
 
@@ -368,7 +405,7 @@ def gpu_arm(args, world, rank, local):
                       "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
-                      "overlap": overlap},
+                      "overlap": overlap, "per_param": w.per_param},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,
            "clocks": clk}

@@ -116,8 +116,12 @@ enum {
                                       ordered by rank, unit, flat position */
     ZERO_TABLE_BUCKET_SEGMENTS = 3,/* 5 cols: bucket, rank, flat start, rank-local shard offset,
                                       length; ordered by bucket, rank (stages 1/2) */
-    ZERO_TABLE_STATE_LAYOUT = 4    /* 4 cols: rank, unit, element offset of the unit's shard in the
+    ZERO_TABLE_STATE_LAYOUT = 4,   /* 4 cols: rank, unit, element offset of the unit's shard in the
                                       rank's state buffers, length (physical layout, see zero_bind) */
+    ZERO_TABLE_PARAM_CHUNKS = 5    /* per-parameter plans, 10 cols: rank, unit, tensor, first row,
+                                      owned rows, cols, chunk rows, offset of the owned rows in the
+                                      unit's gradient buffer, logical and physical offset of the
+                                      local shard in the rank's state; ordered rank, unit, tensor */
 };
 
 /* Device-resident step state, read back by zero_read_state / zero_step_finish. */
@@ -173,6 +177,18 @@ typedef struct {
 zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, int n_d, int stage,
                                int64_t bucket_elems, const int64_t* unit_first, int64_t n_units,
                                int dtype16, zero_plan_t** out);
+
+/* FSDP-2 per-parameter sharding ("FSDP-2: Per-Parameter Sharding via DTensor (fully_shard)":
+ * each tensor sharded along its leading dimension, Shard(0), without flattening).  Tensor t has
+ * dim0[t] rows of tensor_sizes[t] / dim0[t] elements; rank r owns rows
+ * [r*c, min((r+1)*c, dim0[t])), c = ceil(dim0[t] / N_d), and holds a local shard of c rows per
+ * tensor (rows past the tensor are padding, never touched).  Stage-3 semantics otherwise: units
+ * group tensors for the gather, each unit's gradient buffer is its tensors concatenated without
+ * padding (phi_pad == phi), zero_bind takes a 16-bit shard per rank, zero_gather_layer rebuilds
+ * a unit (info.max_unit_pad elements).  Tables: ZERO_TABLE_UNITS and ZERO_TABLE_PARAM_CHUNKS. */
+zero_status_t zero_plan_create_per_param(const int64_t* tensor_sizes, const int64_t* dim0,
+                                         int64_t n_tensors, int n_d, const int64_t* unit_first,
+                                         int64_t n_units, int dtype16, zero_plan_t** out);
 
 zero_status_t zero_plan_info(const zero_plan_t* plan, zero_plan_info_t* out);
 

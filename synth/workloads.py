@@ -68,6 +68,8 @@ class Workload:
     outliers: bool = False
     inject: Optional[Tuple[int, int, int]] = None   # (step 1-based, rank, flat index) of a +inf
     bound_ranks: Optional[Tuple[int, ...]] = None   # ranks whose shard is updated; None = all
+    dim0: Optional[Tuple[int, ...]] = None          # leading dimension of every tensor
+    per_param: bool = False                         # FSDP-2 per-parameter (dim-0) sharding
 
     @property
     def phi(self) -> int:
@@ -101,6 +103,30 @@ def gpt_sizes(vocab: int, ctx: int, d: int, ffn: int, layers: int) -> Tuple[List
     unit_first.append(len(sizes))
     sizes += [d, d]
     return sizes, unit_first
+
+
+def gpt_dim0(vocab: int, ctx: int, d: int, ffn: int, layers: int) -> List[int]:
+    """Leading dimensions of gpt_sizes' tensors (Conv1D weights are stored (in, out))."""
+    dims = [vocab, ctx]
+    for _ in range(layers):
+        dims += [d, d, d, 3 * d, d, d, d, d, d, ffn, ffn, d]
+    return dims + [d, d]
+
+
+def llama_dim0(vocab: int, d: int, ffn: int, layers: int) -> List[int]:
+    """Leading dimensions of llama_sizes' tensors (Linear weights are stored (out, in))."""
+    dims = [vocab]
+    for _ in range(layers):
+        dims += [d, d, d, d, d, d, ffn, ffn, d]
+    return dims + [d, vocab]
+
+
+def per_param_variant(w: "Workload") -> "Workload":
+    """The same workload under FSDP-2 per-parameter sharding (stage-3 semantics)."""
+    assert w.dim0 is not None
+    units = w.unit_first if w.unit_first else (0,)
+    return dataclasses.replace(w, wid=w.wid + 100, name=w.name + "_per_param", stage=3,
+                               bucket_elems=0, unit_first=units, per_param=True)
 
 
 def llama_sizes(vocab: int, d: int, ffn: int, layers: int) -> Tuple[List[int], List[int]]:
@@ -138,13 +164,15 @@ def loguniform_sizes(n: int, lo_log2: int = 0, hi_log2: int = 16, wid: int = 1) 
 
 def _cfg0() -> Workload:
     return Workload(wid=0, name="zero1_flat_phi2^20_nd4_bf16", sizes=(1 << 20,), n_d=4, stage=1,
-                    bucket_elems=0, unit_first=(), dtype=BF16, steps=3, hyper=Hyper(), scaler=None)
+                    bucket_elems=0, unit_first=(), dtype=BF16, steps=3, hyper=Hyper(), scaler=None,
+                    dim0=(1 << 20,))
 
 
 def _cfg1() -> Workload:
-    return Workload(wid=1, name="zero2_ragged_10000tensors_nd7_bf16",
-                    sizes=tuple(loguniform_sizes(10000, wid=1)), n_d=7, stage=2, bucket_elems=0,
-                    unit_first=(), dtype=BF16, steps=5, hyper=Hyper(), scaler=None)
+    sizes = tuple(loguniform_sizes(10000, wid=1))
+    return Workload(wid=1, name="zero2_ragged_10000tensors_nd7_bf16", sizes=sizes, n_d=7, stage=2,
+                    bucket_elems=0, unit_first=(), dtype=BF16, steps=5, hyper=Hyper(), scaler=None,
+                    dim0=sizes)
 
 
 def _cfg2() -> Workload:
@@ -152,21 +180,23 @@ def _cfg2() -> Workload:
     phi = sum(sizes)
     return Workload(wid=2, name="zero2_bucketed_gpt2small_nd8_fp16", sizes=tuple(sizes), n_d=8,
                     stage=2, bucket_elems=25_000_000, unit_first=(), dtype=FP16, steps=10,
-                    hyper=Hyper(), scaler=Scaler(), outliers=True, inject=(3, 0, phi // 2))
+                    hyper=Hyper(), scaler=Scaler(), outliers=True, inject=(3, 0, phi // 2),
+                    dim0=tuple(gpt_dim0(50257, 1024, 768, 3072, 12)))
 
 
 def _cfg3() -> Workload:
     sizes, units = gpt_sizes(50257, 2048, 2048, 8192, 24)
     return Workload(wid=3, name="zero3_per_layer_gpt1.3b_nd16_bf16", sizes=tuple(sizes), n_d=16,
                     stage=3, bucket_elems=0, unit_first=tuple(units), dtype=BF16, steps=4,
-                    hyper=Hyper(), scaler=None)
+                    hyper=Hyper(), scaler=None, dim0=tuple(gpt_dim0(50257, 2048, 2048, 8192, 24)))
 
 
 def _cfg4() -> Workload:
     sizes, units = llama_sizes(32000, 4096, 11008, 32)
     return Workload(wid=4, name="zero3_one_rank_llama6.74b_nd8_bf16", sizes=tuple(sizes), n_d=8,
                     stage=3, bucket_elems=0, unit_first=tuple(units), dtype=BF16, steps=5,
-                    hyper=Hyper(), scaler=None, bound_ranks=(0,))
+                    hyper=Hyper(), scaler=None, bound_ranks=(0,),
+                    dim0=tuple(llama_dim0(32000, 4096, 11008, 32)))
 
 
 _BUILDERS = [_cfg0, _cfg1, _cfg2, _cfg3, _cfg4]

@@ -64,7 +64,7 @@ class Run:
         self.w = w
         b = bound if bound is not None else w.ranks()
         self.g = EmulatedGroup(w.sizes, w.n_d, w.stage, w.bucket_elems, w.unit_first or None,
-                               w.dtype, b)
+                               w.dtype, b, dim0=w.dim0 if w.per_param else None)
         self.units = self.g.units
         self.info = self.g.info
         self.bound = list(b)
@@ -77,6 +77,19 @@ class Run:
                 off = self.g.phys_off[r][0]
                 self.g.state[r]["master"][0][off:off + S] = \
                     self.g.full16[r * S:(r + 1) * S].view(t16).float()
+        elif w.per_param:
+            ranks = list(range(w.n_d)) if peers else self.bound
+            for r in ranks:
+                sh = self.g.shard16[r] if r in self.g.shard16 else self.g.bind_peer_shard(r)
+                for (_r, u, _t, _row0, rows, cols, c_rows, coff, _so, phys) in self.g.rank_chunks(r):
+                    if rows:
+                        a = self.units[u][5] + coff
+                        fill_device(sh[phys:phys + rows * cols], ps, self.units, a, a + rows * cols)
+                if r in self.g.state:
+                    m0 = self.g.state[r]["master"][0]
+                    for c in self.g.rank_chunks(r):
+                        phys, n = c[9], c[6] * c[5]
+                        m0[phys:phys + n] = sh[phys:phys + n].view(t16).float()
         else:
             ranks = list(range(w.n_d)) if peers else self.bound
             for r in ranks:
@@ -136,6 +149,19 @@ class Run:
         """(rank, physical offset) of flat indices; rank -1 when not owned by a bound rank."""
         rank = np.full(idx.size, -1, dtype=np.int64)
         phys = np.zeros(idx.size, dtype=np.int64)
+        if self.w.per_param:
+            ch = np.array([c for c in self.g.chunks if c[4] > 0], dtype=np.int64).reshape(-1, 10)
+            start = np.array([self.units[int(u)][5] for u in ch[:, 1]], dtype=np.int64) + ch[:, 7]
+            order = np.argsort(start)
+            start, ch = start[order], ch[order]
+            j = np.searchsorted(start, idx, side="right") - 1
+            ok = (j >= 0)
+            j = np.clip(j, 0, max(0, len(start) - 1))
+            ok &= idx < start[j] + ch[j, 4] * ch[j, 5]
+            rank[ok] = ch[j[ok], 0]
+            phys[ok] = ch[j[ok], 9] + idx[ok] - start[j[ok]]
+            rank[~np.isin(rank, self.bound)] = -1
+            return rank, phys
         for u, (_f, _c, _n, numel_pad, S, base, _sb) in enumerate(self.units):
             sel = (idx >= base) & (idx < base + numel_pad)
             if not sel.any() or S == 0:
@@ -185,13 +211,22 @@ def expected_flag(w: W.Workload, k: int) -> int:
     return int(w.inject is not None and w.inject[0] == k)
 
 
+def oracle_units(w: W.Workload):
+    """(first, count, numel, numel_pad, shard, base, shard_base) of every unit, from the
+    oracle's own partition (per-parameter plans: unpadded unit buffers)."""
+    if w.per_param:
+        pp = oracle.PerParam(w.sizes, w.dim0, w.n_d, w.unit_first or None)
+        return [(0, 0, n, n, 0, int(b), 0) for n, b in zip(pp.unit_numel, pp.unit_base[:-1])]
+    L = oracle.Layout(w.sizes, w.n_d, w.unit_first or None)
+    return [tuple(int(x) for x in u) for u in L.units]
+
+
 class OracleSampled:
     """Oracle trajectory of the sampled flat indices (elementwise replay of every step)."""
 
     def __init__(self, w: W.Workload, idx: np.ndarray):
         self.w, self.idx = w, idx
-        self.L = oracle.Layout(w.sizes, w.n_d, w.unit_first or None)
-        units = [tuple(int(x) for x in u) for u in self.L.units]
+        units = oracle_units(w)
         self.units = units
         p16 = values_at(synth.param_stream(w), units, idx)
         self.p = oracle.widen16(p16, w.dtype).astype(np.float32)
@@ -220,12 +255,31 @@ class OracleFull:
 
     def __init__(self, w: W.Workload, bound):
         self.w = w
-        self.L = oracle.Layout(w.sizes, w.n_d, w.unit_first or None)
-        self.units = [tuple(int(x) for x in u) for u in self.L.units]
-        n = self.L.total_pad
-        self.params16 = fill_host(synth.param_stream(w), self.units, 0, n)
+        self.units = oracle_units(w)
         self.bound = [1 if r in bound else 0 for r in range(w.n_d)]
         self.p, self.m, self.v, self.sh16 = [], [], [], []
+        self.sc = oracle.ScalerState(w.scaler)
+        if w.per_param:
+            assert w.hyper.max_grad_norm == 0
+            self.pp = oracle.PerParam(w.sizes, w.dim0, w.n_d, w.unit_first or None)
+            self.total = int(self.pp.unit_base[-1])
+            self.params16 = fill_host(synth.param_stream(w), self.units, 0, self.total)
+            for r in range(w.n_d):
+                P = np.zeros(max(1, self.pp.per_rank), np.float32)
+                S16 = np.zeros(max(1, self.pp.per_rank), np.uint16)
+                for (rr, u, t, row0, rows, cols, c_rows, coff, soff) in self.pp.chunks:
+                    if rr == r and rows:
+                        g0 = self.pp.unit_base[u] + coff
+                        S16[soff:soff + rows * cols] = self.params16[g0:g0 + rows * cols]
+                P[:] = oracle.widen16(S16, w.dtype)
+                self.p.append(P)
+                self.m.append(np.zeros_like(P))
+                self.v.append(np.zeros_like(P))
+                self.sh16.append(S16)
+            return
+        self.L = oracle.Layout(w.sizes, w.n_d, w.unit_first or None)
+        n = self.L.total_pad
+        self.params16 = fill_host(synth.param_stream(w), self.units, 0, n)
         for r in range(w.n_d):
             idx = np.concatenate([np.arange(U[5] + r * U[4], U[5] + (r + 1) * U[4]) for U in self.units]) \
                 if self.units else np.zeros(0, np.int64)
@@ -235,10 +289,16 @@ class OracleFull:
             self.v.append(np.zeros(idx.size, np.float32))
             self.sh16.append(self.params16[idx].copy())
         self.full16 = self.params16.copy()
-        self.sc = oracle.ScalerState(w.scaler)
 
     def step(self, k: int) -> int:
         w = self.w
+        if w.per_param:
+            c = [fill_host(synth.grad_stream(w, k, r), self.units, 0, self.total) for r in range(w.n_d)]
+            k9 = oracle.consts(w.hyper, self.sc.t + 1, self.sc.scale, w.n_d)
+            flag = self.pp.step(w.dtype, c, self.bound, self.p, self.m, self.v, self.sh16, k9)
+            self.norm2 = float("nan")
+            self.sc.update(flag)
+            return flag
         n = self.L.total_pad
         c = [fill_host(synth.grad_stream(w, k, r), self.units, 0, n) for r in range(w.n_d)]
         k9 = oracle.consts(w.hyper, self.sc.t + 1, self.sc.scale, w.n_d)
@@ -250,6 +310,8 @@ class OracleFull:
         return flag
 
     def gathered(self, u: int) -> np.ndarray:
+        if self.w.per_param:
+            return self.pp.gather(u, self.sh16)
         return oracle.gather_unit(self.L, u, self.sh16)
 
 
@@ -294,7 +356,12 @@ def sample_indices(run: Run, n_random: int = 20000, seed: int = 0,
         edges += [base + r * S for r in range(run.w.n_d + 1)]
     if run.w.stage != 3 and run.w.bucket_elems:
         edges += list(range(0, n, run.w.bucket_elems))
-    offs = oracle.Layout(run.w.sizes, run.w.n_d, run.w.unit_first or None).tensor_offset
+    if run.w.per_param:                               # every rank's row-chunk boundaries
+        edges += [run.units[c[1]][5] + c[7] for c in run.g.chunks]
+    if run.w.per_param:
+        offs = np.concatenate([[0], np.cumsum(run.w.sizes)[:-1]]).astype(np.int64)
+    else:
+        offs = oracle.Layout(run.w.sizes, run.w.n_d, run.w.unit_first or None).tensor_offset
     pick = offs[rng.integers(0, offs.size, size=min(400, offs.size))] if offs.size else []
     edges += [int(x) for x in pick]
     e = np.array(edges, dtype=np.int64)

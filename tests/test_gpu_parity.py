@@ -491,3 +491,45 @@ def test_overlapped_schedule_argument_errors():
         assert e.value.status == Z.ZERO_EINVAL                     # stage 3 only
     finally:
         run.close()
+
+
+# ---------------------------------------------------------------------- FSDP-2 per-parameter plans
+
+def _pp(wid, n_t, n_d, seed, dtype=W.BF16, units=(0,), steps=3, scaler=None, inject=None,
+        bound=None, max_rows=300, max_cols=64):
+    rng = np.random.default_rng(seed)
+    dim0 = [int(x) for x in rng.integers(1, max_rows, size=n_t)]
+    sizes = [d * int(c) for d, c in zip(dim0, rng.integers(1, max_cols, size=n_t))]
+    return W.Workload(wid=wid, name=f"pp{wid}", sizes=tuple(sizes), n_d=n_d, stage=3,
+                      bucket_elems=0, unit_first=tuple(units), dtype=dtype, steps=steps,
+                      hyper=W.Hyper(), scaler=scaler, inject=inject, bound_ranks=bound,
+                      dim0=tuple(dim0), per_param=True)
+
+
+PP_CASES = {
+    "pp_nd4_units": _pp(150, 20, 4, 1, units=(0, 6, 13)),
+    "pp_nd8_fp16_peers_skip": _pp(151, 16, 8, 2, dtype=W.FP16, units=(0, 5, 9),
+                                  scaler=W.Scaler(init_scale=512.0), inject=(2, 3, 4_321),
+                                  bound=(0, 3, 7)),
+    "pp_nd16_rows_below_ranks": _pp(152, 30, 16, 3, units=(0, 10, 20), max_rows=20),
+}
+
+
+@pytest.mark.parametrize("name", list(PP_CASES))
+def test_per_param_full_parity(name):
+    _run_full(PP_CASES[name])
+
+
+@pytest.mark.parametrize("i", [3, 4])
+def test_per_param_config_sampled(i):
+    w = W.per_param_variant(W.workload(i))
+    n, mism = _run_sampled(w, bound=(0, w.n_d - 1) if i == 4 else None)
+    print(f"per-parameter configs[{i}]: {n} sampled elements, {mism} bit mismatches")
+
+
+def test_per_param_overlapped_schedule():
+    OVERLAP_CASES["pp"] = PP_CASES["pp_nd4_units"]
+    try:
+        test_overlapped_stage3_schedule_full_parity("pp")
+    finally:
+        del OVERLAP_CASES["pp"]

@@ -173,3 +173,58 @@ def test_empty_model_plan():
     assert info.phi == info.phi_pad == info.shard == info.n_buckets == 0
     assert Z.zero_plan_tables(plan, Z.ZERO_TABLE_SHARD_SEGMENTS) == []
     Z.zero_plan_destroy(plan)
+
+
+# ---------------------------------------------------------------------- FSDP-2 per-parameter plans
+
+def _compare_per_param(sizes, dim0, n_d, units):
+    plan = Z.zero_plan_create_per_param(sizes, dim0, n_d, units or None)
+    try:
+        pp = oracle.PerParam(sizes, dim0, n_d, units or None)
+        rows = Z.zero_plan_tables(plan, Z.ZERO_TABLE_PARAM_CHUNKS)
+        assert [r[:9] for r in rows] == [tuple(int(x) for x in c) for c in pp.chunks]
+        info = Z.zero_plan_info(plan)
+        assert info.shard == pp.per_rank and info.phi == info.phi_pad == sum(sizes)
+        ut = Z.zero_plan_tables(plan, Z.ZERO_TABLE_UNITS)
+        assert [u[2] for u in ut] == pp.unit_numel and [u[5] for u in ut] == list(pp.unit_base[:-1])
+        for r in range(n_d):
+            elems = Z.zero_rank_state_elems(plan, r)
+            end = 0
+            for row in rows:
+                if row[0] != r:
+                    continue
+                phys, local = row[9], row[6] * row[5]
+                assert phys >= end and phys - end < 8 and (phys - row[7]) % 8 == 0
+                end = phys + local
+            assert end <= elems and elems % 8 == 0
+        with pytest.raises(Z.ZeroError):
+            Z.zero_plan_tables(plan, Z.ZERO_TABLE_SHARD_SEGMENTS)
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
+def test_per_param_tables_match_oracle_random():
+    rng = np.random.default_rng(50)
+    for _ in range(200):
+        nt = int(rng.integers(1, 10))
+        dim0 = [int(x) for x in rng.integers(0, 30, size=nt)]
+        sizes = [d * int(c) for d, c in zip(dim0, rng.integers(1, 9, size=nt))]
+        units = []
+        if nt > 1 and rng.random() < 0.6:
+            units = [0] + sorted(set(int(x) for x in rng.integers(1, nt, size=2)))
+        _compare_per_param(sizes, dim0, int(rng.integers(1, 17)), units)
+
+
+@pytest.mark.parametrize("i", [2, 3, 4])
+def test_per_param_tables_match_oracle_workloads(i):
+    w = W.per_param_variant(W.workload(i))
+    _compare_per_param(list(w.sizes), list(w.dim0), w.n_d, list(w.unit_first))
+
+
+def test_per_param_argument_errors():
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_plan_create_per_param([10, 7], [3, 7], 2)         # 10 is not a multiple of 3
+    assert e.value.status == Z.ZERO_EINVAL
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_plan_create_per_param([0, 7], [0, 7], 0)
+    assert e.value.status == Z.ZERO_EINVAL

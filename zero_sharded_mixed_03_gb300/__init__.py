@@ -20,12 +20,12 @@ ZERO_BF16, ZERO_FP16 = 0, 1
 ZERO_MAX_RANKS = 128
 ZERO_REPORT_GRAD_NORM = 1
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
- ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT) = range(5)
-TABLE_COLS = {0: 1, 1: 7, 2: 6, 3: 5, 4: 4}
+ ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)
+TABLE_COLS = {0: 1, 1: 7, 2: 6, 3: 5, 4: 4, 5: 10}
 STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_EALIGN", 3: "ZERO_ECUDA",
                 4: "ZERO_ESTATE", 5: "ZERO_ERANGE"}
 
-EXPORTED = ["zero_plan_create", "zero_plan_info", "zero_rank_state_elems", "zero_plan_tables",
+EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", "zero_rank_state_elems", "zero_plan_tables",
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",
             "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_set_scaler",
             "zero_read_state", "zero_restore_state", "zero_grad_norm",
@@ -102,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.zero_plan_create.restype = st
         L.zero_plan_create.argtypes = [_vp, _i64, _int, _int, _i64, _vp, _i64, _int,
                                        ctypes.POINTER(_vp)]
+        L.zero_plan_create_per_param.restype = st
+        L.zero_plan_create_per_param.argtypes = [_vp, _vp, _i64, _int, _vp, _i64, _int,
+                                                 ctypes.POINTER(_vp)]
         L.zero_plan_info.restype = st
         L.zero_plan_info.argtypes = [_vp, ctypes.POINTER(zero_plan_info_t)]
         L.zero_rank_state_elems.restype = st
@@ -177,6 +180,19 @@ def zero_plan_create(tensor_sizes: Sequence[int], n_d: int, stage: int, bucket_e
     _check(lib().zero_plan_create(sizes, len(tensor_sizes), n_d, stage, bucket_elems, units,
                                   len(unit_first) if unit_first else 0, dtype16,
                                   ctypes.byref(out)))
+    return int(out.value)
+
+
+def zero_plan_create_per_param(tensor_sizes: Sequence[int], dim0: Sequence[int], n_d: int,
+                               unit_first: Optional[Sequence[int]] = None,
+                               dtype16: int = ZERO_BF16) -> int:
+    sizes = _i64_array(tensor_sizes)
+    d0 = _i64_array(dim0)
+    units = _i64_array(unit_first) if unit_first else None
+    out = _vp()
+    _check(lib().zero_plan_create_per_param(sizes, d0, len(tensor_sizes), n_d, units,
+                                            len(unit_first) if unit_first else 0, dtype16,
+                                            ctypes.byref(out)))
     return int(out.value)
 
 

@@ -37,6 +37,16 @@ struct Rank {
 //   contributions: element c_off of every contribution buffer
 //   state:         element s_off of the rank's master/m/v (both halves)
 //   16-bit output: element o_off of `out16`
+// FSDP-2 per-parameter sharding: rank `rank`'s chunk of tensor `tensor` (rows
+// [row0, row0 + rows) of a tensor with `cols` elements per row; the local shard holds
+// c_rows * cols elements, rows beyond the tensor being padding).
+struct Chunk {
+    int64_t rank, unit, tensor, row0, rows, cols, c_rows;
+    int64_t contrib_off;  // offset of the owned rows in the unit's gradient buffer
+    int64_t state_off;    // logical offset of the local shard in the rank's state
+    int64_t phys_off;     // physical offset (16-byte phase of contrib_off)
+};
+
 struct Segment {
     int64_t n;
     int64_t c_off;
@@ -71,6 +81,10 @@ struct zero_plan {
     // Physical state layout: phys_off[r][u] = element offset of unit u's shard in rank r's
     // state buffers; state_elems[r] = their length.
     std::vector<std::vector<int64_t>> phys_off;
+    // FSDP-2 per-parameter plans (stage-3 semantics, one chunk per rank and tensor).
+    bool per_param = false;
+    std::vector<int64_t> dim0;
+    std::vector<zero::Chunk> chunks;    // rank-major, then unit, then tensor
     std::vector<int64_t> state_elems;
 
     // Bindings (device pointers, caller-owned).

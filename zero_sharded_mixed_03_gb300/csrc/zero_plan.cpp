@@ -42,6 +42,14 @@ std::vector<Segment> step_segments(const zero_plan* p, int64_t which, int cur_ou
 {
     (void)cur_out;
     std::vector<Segment> segs;
+    if (p->per_param) {
+        for (const Chunk& c : p->chunks) {
+            if (c.unit != which || c.rows == 0 || !p->ranks[(size_t)c.rank].bound) continue;
+            segs.push_back(Segment{c.rows * c.cols, c.contrib_off, c.phys_off, c.phys_off,
+                                   (int)c.rank, p->ranks[(size_t)c.rank].shard16});
+        }
+        return segs;
+    }
     if (p->stage == 3) {
         const Unit& U = p->units[(size_t)which];
         for (int r = 0; r < p->n_d; ++r) {
@@ -68,6 +76,14 @@ std::vector<Segment> step_segments(const zero_plan* p, int64_t which, int cur_ou
 std::vector<Segment> shard_segments_all(const zero_plan* p)
 {
     std::vector<Segment> segs;
+    if (p->per_param) {
+        for (const Chunk& c : p->chunks) {
+            if (c.rows == 0 || !p->ranks[(size_t)c.rank].bound) continue;
+            segs.push_back(Segment{c.rows * c.cols, 0, c.phys_off, c.phys_off, (int)c.rank,
+                                   p->ranks[(size_t)c.rank].shard16});
+        }
+        return segs;
+    }
     for (int r = 0; r < p->n_d; ++r) {
         if (!p->ranks[(size_t)r].bound) continue;
         for (size_t u = 0; u < p->units.size(); ++u) {
@@ -202,6 +218,78 @@ zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, i
     return ZERO_OK;
 }
 
+zero_status_t zero_plan_create_per_param(const int64_t* tensor_sizes, const int64_t* dim0,
+                                         int64_t n_tensors, int n_d, const int64_t* unit_first,
+                                         int64_t n_units, int dtype16, zero_plan_t** out)
+{
+    if (out == nullptr) return fail(ZERO_EINVAL, "zero_plan_create_per_param: out is NULL");
+    *out = nullptr;
+    if (n_tensors > 0 && dim0 == nullptr)
+        return fail(ZERO_EINVAL, "zero_plan_create_per_param: dim0 is NULL");
+    for (int64_t t = 0; t < n_tensors; ++t) {
+        if (tensor_sizes && (dim0[t] < 0 || (dim0[t] == 0 && tensor_sizes[t] != 0) ||
+                             (dim0[t] > 0 && tensor_sizes[t] % dim0[t] != 0)))
+            return fail(ZERO_EINVAL, "zero_plan_create_per_param: size is not a multiple of dim0");
+    }
+    zero_plan_t* p = nullptr;
+    zero_status_t st = zero_plan_create(tensor_sizes, n_tensors, n_d, 3, 0, unit_first, n_units,
+                                        dtype16, &p);
+    if (st != ZERO_OK) return st;
+    p->per_param = true;
+    p->dim0.assign(dim0, dim0 + n_tensors);
+    // units: unpadded gradient buffers; a rank's unit shard = its padded local chunks
+    int64_t base = 0, shard_base = 0;
+    for (Unit& U : p->units) {
+        U.numel_pad = U.numel;
+        U.base = base;
+        int64_t off = 0;
+        U.shard = 0;
+        for (int64_t t = U.first; t < U.first + U.count; ++t) {
+            p->tensor_offset[(size_t)t] = base + off;
+            off += p->sizes[(size_t)t];
+            const int64_t rows_t = p->dim0[(size_t)t];
+            const int64_t cols = rows_t > 0 ? p->sizes[(size_t)t] / rows_t : 0;
+            U.shard += ceil_div(rows_t, n_d) * cols;
+        }
+        U.shard_base = shard_base;
+        base += U.numel;
+        shard_base += U.shard;
+    }
+    p->phi_pad = base;
+    p->shard_total = shard_base;
+    p->chunks.clear();
+    for (int r = 0; r < n_d; ++r) {
+        int64_t logical = 0, cursor = 0;
+        for (size_t u = 0; u < p->units.size(); ++u) {
+            const Unit& U = p->units[u];
+            int64_t off = 0;
+            for (int64_t t = U.first; t < U.first + U.count; ++t) {
+                Chunk c;
+                c.rank = r;
+                c.unit = (int64_t)u;
+                c.tensor = t;
+                const int64_t rows_t = p->dim0[(size_t)t];
+                c.cols = rows_t > 0 ? p->sizes[(size_t)t] / rows_t : 0;
+                c.c_rows = ceil_div(rows_t, n_d);
+                c.row0 = r * c.c_rows;
+                c.rows = std::max<int64_t>(0, std::min(c.row0 + c.c_rows, rows_t) - c.row0);
+                c.contrib_off = off + c.row0 * c.cols;
+                c.state_off = logical;
+                const int64_t want = c.contrib_off % 8;
+                c.phys_off = cursor + (((want - cursor) % 8) + 8) % 8;
+                if (t == U.first) p->phys_off[(size_t)r][u] = c.phys_off;
+                cursor = c.phys_off + c.c_rows * c.cols;
+                logical += c.c_rows * c.cols;
+                off += p->sizes[(size_t)t];
+                p->chunks.push_back(c);
+            }
+        }
+        p->state_elems[(size_t)r] = ceil_div(cursor, 8) * 8;
+    }
+    *out = p;
+    return ZERO_OK;
+}
+
 void zero_plan_destroy(zero_plan_t* plan)
 {
     if (plan && plan->release_hook) plan->release_hook(plan);
@@ -259,7 +347,15 @@ zero_status_t zero_plan_tables(const zero_plan_t* p, int which, int64_t* dst, in
             rows.insert(rows.end(), {U.first, U.count, U.numel, U.numel_pad, U.shard, U.base,
                                      U.shard_base});
         break;
+    case ZERO_TABLE_PARAM_CHUNKS:
+        if (!p->per_param) return fail(ZERO_EINVAL, "zero_plan_tables: not a per-parameter plan");
+        cols = 10;
+        for (const Chunk& c : p->chunks)
+            rows.insert(rows.end(), {c.rank, c.unit, c.tensor, c.row0, c.rows, c.cols, c.c_rows,
+                                     c.contrib_off, c.state_off, c.phys_off});
+        break;
     case ZERO_TABLE_SHARD_SEGMENTS:
+        if (p->per_param) return fail(ZERO_EINVAL, "zero_plan_tables: flat-buffer table of a per-parameter plan");
         cols = 6;
         // Per (rank, unit): the shard interval cut at tensor boundaries, then the tail padding.
         for (int r = 0; r < p->n_d; ++r)
@@ -288,6 +384,7 @@ zero_status_t zero_plan_tables(const zero_plan_t* p, int which, int64_t* dst, in
             }
         break;
     case ZERO_TABLE_BUCKET_SEGMENTS:
+        if (p->per_param) return fail(ZERO_EINVAL, "zero_plan_tables: flat-buffer table of a per-parameter plan");
         cols = 5;
         if (p->stage != 3) {
             const int64_t S = p->units[0].shard;
@@ -302,6 +399,7 @@ zero_status_t zero_plan_tables(const zero_plan_t* p, int which, int64_t* dst, in
         }
         break;
     case ZERO_TABLE_STATE_LAYOUT:
+        if (p->per_param) return fail(ZERO_EINVAL, "zero_plan_tables: use ZERO_TABLE_PARAM_CHUNKS");
         cols = 4;
         for (int r = 0; r < p->n_d; ++r)
             for (size_t u = 0; u < p->units.size(); ++u)

@@ -32,6 +32,7 @@ namespace {
 
 constexpr int kThreads = 128;     // 128-thread blocks: 70 registers, 7 blocks resident per SM
 constexpr int kMaxSegs = 32;      // work items per launch (more are split across launches)
+constexpr int kWideSegs = 256;    // capacity of the wide parameter block (calls with many items)
 constexpr int kScalarSlots = 16;  // per segment: up to 7 head + 7 tail elements
 // Contribution slices loaded (128-bit each) per batch before they are summed.
 constexpr int kRankBatch = 4;
@@ -75,9 +76,10 @@ struct KSeg {
     int32_t tail;      // scalar elements after the body
 };
 
-struct StepParams {
+template <int MS>
+struct StepParamsT {
     const uint16_t* c[ZERO_MAX_RANKS];
-    KSeg seg[kMaxSegs];
+    KSeg seg[MS];
     float k[9];        // b1, 1-b1, b2, 1-b2, eps, lr*wd, lr/bc1, sqrt(bc2), inv
     double lr;         // device mode: lr/bc1 is formed on the GPU from the table
     double beta1, beta2;
@@ -93,6 +95,10 @@ struct StepParams {
     double max_norm;           // clip mode: the bound on the global gradient norm
     double* partials;          // norm modes: one slot per block
 };
+// The usual parameter block (4 KB), and a wide one (26 KB, under the 32 KB kernel-parameter
+// limit) for calls with many work items, e.g. per-parameter plans (one item per tensor chunk).
+using StepParams = StepParamsT<kMaxSegs>;
+using StepParamsWide = StepParamsT<kWideSegs>;
 
 struct CommitParams {
     DevState* st;
@@ -213,7 +219,8 @@ __device__ __forceinline__ uint4 ld_stream(const void* p)
 // The step's fp32 constants and the current half, formed once per block by thread 0.
 // Device mode: t and the loss scale come from the workspace; the fp32 roundings of
 // lr/bc1, sqrt(bc2) and 1/(N_d*scale) are the same IEEE double operations the host uses.
-__device__ __forceinline__ void block_constants(const StepParams& P, float* sk, int* scur)
+template <typename PT>
+__device__ __forceinline__ void block_constants(const PT& P, float* sk, int* scur)
 {
     if (threadIdx.x == 0) {
         sk[0] = P.k[6];
@@ -250,8 +257,8 @@ __device__ __forceinline__ void block_constants(const StepParams& P, float* sk, 
 
 // ------------------------------------------------------------------ fused step kernel
 
-template <int DT, int MODE>
-__device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, int64_t e,
+template <int DT, int MODE, typename PT>
+__device__ __forceinline__ bool step_scalar(const PT& P, const KSeg& S, int64_t e,
                                             const StepK& sk, int cur, NormAcc& norm2)
 {
     float sum = 0.0f;
@@ -270,8 +277,8 @@ __device__ __forceinline__ bool step_scalar(const StepParams& P, const KSeg& S, 
 
 // Eight consecutive elements starting at e: 128-bit loads of the N_d contribution slices
 // (batches of NB ranks in flight), 2 x 128-bit per fp32 state array, 128-bit 16-bit store.
-template <int DT, int NB, int MODE>
-__device__ __forceinline__ bool step_vec8(const StepParams& P, const KSeg& S, int64_t e,
+template <int DT, int NB, int MODE, typename PT>
+__device__ __forceinline__ bool step_vec8(const PT& P, const KSeg& S, int64_t e,
                                           const StepK& sk, int cur, NormAcc& norm2)
 {
     const float* pin = S.p[cur] + e;
@@ -356,7 +363,8 @@ __device__ __forceinline__ double block_sum_fixed(double x, double* warp_sum)
 // the launch to store (an atomic ticket, nothing waits) adds all slots to the step's norm in a
 // fixed order (thread t takes slots t, t + 128, ...; then the fixed block pattern), so the sum
 // does not depend on which blocks finish first.
-__device__ __forceinline__ void block_norm_commit(const StepParams& P, double part)
+template <typename PT>
+__device__ __forceinline__ void block_norm_commit(const PT& P, double part)
 {
     __shared__ double warp_sum[kThreads / 32];
     __shared__ bool last;
@@ -387,8 +395,8 @@ __device__ __forceinline__ void block_norm_commit(const StepParams& P, double pa
 // kScalarSlots scalar slots per segment for the unaligned head and tail.  VEC = 8: 128-bit
 // body; VEC = 1: every element is a body vector of one (streams of different phases).
 // Reads the current half of each pair and writes the other.
-template <int DT, int NB, int VEC, int MODE>
-__global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_constant__ StepParams P)
+template <int DT, int NB, int VEC, int MODE, typename PT>
+__global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_constant__ PT P)
 {
     __shared__ float sk4[4];
     __shared__ int scur;
@@ -428,8 +436,8 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
 
 // Gradient-norm pre-pass: the reduction of the fused kernel without the update; reads only
 // the contributions.
-template <int DT, int NB, int VEC>
-__global__ void __launch_bounds__(kThreads) grad_norm_kernel(const __grid_constant__ StepParams P)
+template <int DT, int NB, int VEC, typename PT>
+__global__ void __launch_bounds__(kThreads) grad_norm_kernel(const __grid_constant__ PT P)
 {
     __shared__ float sk4[4];
     __shared__ int scur;
@@ -499,8 +507,8 @@ __global__ void __launch_bounds__(kThreads) grad_norm_kernel(const __grid_consta
 // On a flagged step the fused kernels have already written 16-bit values of the rejected
 // update; rewrite them from the unchanged current master.  Every block returns at once when
 // the flag is clear (the usual case), so the launch costs a few microseconds.
-template <int DT, int VEC>
-__global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant__ StepParams P)
+template <int DT, int VEC, typename PT>
+__global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant__ PT P)
 {
     __shared__ int go, scur;
     if (threadIdx.x == 0) {
@@ -669,8 +677,9 @@ const double* bias_table(const zero_plan* p)
 
 // Fill one launch's KSeg list from plan segments [b, e), deciding the vector path.
 // Returns true when every stream of every segment shares one 16-byte phase.
+template <typename PT>
 bool build_step_params(const zero_plan* p, const std::vector<Segment>& segs, size_t b, size_t e,
-                       const void* const* contribs, StepParams& P)
+                       const void* const* contribs, PT& P)
 {
     bool vec_ok = true;
     P.n_seg = (int)(e - b);
@@ -700,7 +709,8 @@ bool build_step_params(const zero_plan* p, const std::vector<Segment>& segs, siz
     return vec_ok;
 }
 
-void finalize_vectors(StepParams& P, bool vec)
+template <typename PT>
+void finalize_vectors(PT& P, bool vec)
 {
     int64_t acc = 0;
     for (int i = 0; i < P.n_seg; ++i) {
@@ -716,23 +726,23 @@ void finalize_vectors(StepParams& P, bool vec)
     P.total_vec = acc;
 }
 
-template <typename K>
-void launch_grid(K kernel, int dev, int64_t work, const StepParams& P, cudaStream_t st)
+template <typename K, typename PT>
+void launch_grid(K kernel, int dev, int64_t work, const PT& P, cudaStream_t st)
 {
     int grid = grid_for(kernel, dev, work);
     if (P.partials) grid = (int)std::min<int64_t>(grid, kNormSlots);
     kernel<<<grid, kThreads, 0, st>>>(P);
 }
 
-template <int DT, int MODE>
-void launch_fused_mode(int dev, const StepParams& P, bool vec, int64_t work, cudaStream_t st)
+template <int DT, int MODE, typename PT>
+void launch_fused_mode(int dev, const PT& P, bool vec, int64_t work, cudaStream_t st)
 {
-    if (!vec) launch_grid(fused_step_kernel<DT, 1, 1, MODE>, dev, work, P, st);
-    else launch_grid(fused_step_kernel<DT, kRankBatch, 8, MODE>, dev, work, P, st);
+    if (!vec) launch_grid(fused_step_kernel<DT, 1, 1, MODE, PT>, dev, work, P, st);
+    else launch_grid(fused_step_kernel<DT, kRankBatch, 8, MODE, PT>, dev, work, P, st);
 }
 
-template <int DT>
-cudaError_t launch_fused(int dev, StepParams& P, bool vec, cudaStream_t st, int mode = kPlain)
+template <int DT, typename PT>
+cudaError_t launch_fused(int dev, PT& P, bool vec, cudaStream_t st, int mode = kPlain)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
@@ -742,23 +752,23 @@ cudaError_t launch_fused(int dev, StepParams& P, bool vec, cudaStream_t st, int 
     return cudaGetLastError();
 }
 
-template <int DT>
-cudaError_t launch_norm(int dev, StepParams& P, bool vec, cudaStream_t st)
+template <int DT, typename PT>
+cudaError_t launch_norm(int dev, PT& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
-    if (!vec) launch_grid(grad_norm_kernel<DT, 1, 1>, dev, work, P, st);
-    else launch_grid(grad_norm_kernel<DT, kRankBatch, 8>, dev, work, P, st);
+    if (!vec) launch_grid(grad_norm_kernel<DT, 1, 1, PT>, dev, work, P, st);
+    else launch_grid(grad_norm_kernel<DT, kRankBatch, 8, PT>, dev, work, P, st);
     return cudaGetLastError();
 }
 
-template <int DT>
-cudaError_t launch_recast(int dev, StepParams& P, bool vec, cudaStream_t st)
+template <int DT, typename PT>
+cudaError_t launch_recast(int dev, PT& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
-    if (vec) recast_kernel<DT, 8><<<grid_for(recast_kernel<DT, 8>, dev, work), kThreads, 0, st>>>(P);
-    else recast_kernel<DT, 1><<<grid_for(recast_kernel<DT, 1>, dev, work), kThreads, 0, st>>>(P);
+    if (vec) launch_grid(recast_kernel<DT, 8, PT>, dev, work, P, st);
+    else launch_grid(recast_kernel<DT, 1, PT>, dev, work, P, st);
     return cudaGetLastError();
 }
 
@@ -849,7 +859,8 @@ zero_status_t check_call(const zero_plan_t* p, const void* const* grad_contribs,
 }
 
 // Fill and launch one chunk of segments [b, e) of a zero_step / zero_grad_norm call.
-void fill_call_params(const zero_plan* p, const void* const* grad_contribs, StepParams& P)
+template <typename PT>
+void fill_call_params(const zero_plan* p, const void* const* grad_contribs, PT& P)
 {
     std::memset(&P, 0, sizeof(P));
     for (int r = 0; r < p->n_d; ++r) P.c[r] = (const uint16_t*)grad_contribs[r];
@@ -989,15 +1000,26 @@ zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, i
     if (st != ZERO_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     const std::vector<Segment> segs = step_segments(p, which, 0);
-    for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
-        const size_t e = std::min(segs.size(), b + kMaxSegs);
+    auto run = [&](auto& P, size_t cap) -> cudaError_t {
+        for (size_t b = 0; b < segs.size(); b += cap) {
+            const size_t e = std::min(segs.size(), b + cap);
+            fill_call_params(p, grad_contribs, P);
+            const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
+            const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_norm<ZERO_BF16>(p->device, P, vec, s)
+                                                            : launch_norm<ZERO_FP16>(p->device, P, vec, s);
+            if (err != cudaSuccess) return err;
+        }
+        return cudaSuccess;
+    };
+    cudaError_t err;
+    if (segs.size() > (size_t)kMaxSegs) {
+        StepParamsWide P;
+        err = run(P, kWideSegs);
+    } else {
         StepParams P;
-        fill_call_params(p, grad_contribs, P);
-        const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
-        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_norm<ZERO_BF16>(p->device, P, vec, s)
-                                                        : launch_norm<ZERO_FP16>(p->device, P, vec, s);
-        if (err != cudaSuccess) return cuda_fail(err, "gradient-norm launch");
+        err = run(P, kMaxSegs);
     }
+    if (err != cudaSuccess) return cuda_fail(err, "gradient-norm launch");
     p->norm_open = true;
     if (which == -1) std::fill(p->norm_covered.begin(), p->norm_covered.end(), 1);
     else p->norm_covered[(size_t)which] = 1;
@@ -1044,16 +1066,28 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
     if (hyper->max_grad_norm > 0.0) mode = kClip;
     else if ((hyper->flags & ZERO_REPORT_GRAD_NORM) && !p->norm_open) mode = kNormAcc;
     const std::vector<Segment> segs = step_segments(p, which, 0);
-    for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
-        const size_t e = std::min(segs.size(), b + kMaxSegs);
+    auto run = [&](auto& P, size_t cap) -> cudaError_t {
+        for (size_t b = 0; b < segs.size(); b += cap) {
+            const size_t e = std::min(segs.size(), b + cap);
+            fill_call_params(p, grad_contribs, P);
+            P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
+            const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
+            const cudaError_t err = p->dtype16 == ZERO_BF16
+                                        ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode)
+                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode);
+            if (err != cudaSuccess) return err;
+        }
+        return cudaSuccess;
+    };
+    cudaError_t lerr;
+    if (segs.size() > (size_t)kMaxSegs) {
+        StepParamsWide P;
+        lerr = run(P, kWideSegs);
+    } else {
         StepParams P;
-        fill_call_params(p, grad_contribs, P);
-        P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
-        const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
-        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode)
-                                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode);
-        if (err != cudaSuccess) return cuda_fail(err, "fused step launch");
+        lerr = run(P, kMaxSegs);
     }
+    if (lerr != cudaSuccess) return cuda_fail(lerr, "fused step launch");
     p->in_step = true;
     if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
     else p->covered[(size_t)which] = 1;
@@ -1073,17 +1107,28 @@ zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t*
 
     // Re-cast (no-op unless the flag is set), then the one-thread commit.
     const std::vector<Segment> segs = shard_segments_all(p);
-    for (size_t b = 0; b < segs.size(); b += kMaxSegs) {
-        const size_t en = std::min(segs.size(), b + kMaxSegs);
+    auto run = [&](auto& P, size_t cap) -> cudaError_t {
+        for (size_t b = 0; b < segs.size(); b += cap) {
+            const size_t en = std::min(segs.size(), b + cap);
+            std::memset(&P, 0, sizeof(P));
+            P.n_d = p->n_d;
+            P.st = dev_state(p);
+            const bool vec = build_step_params(p, segs, b, en, nullptr, P);
+            const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_recast<ZERO_BF16>(p->device, P, vec, s)
+                                                            : launch_recast<ZERO_FP16>(p->device, P, vec, s);
+            if (err != cudaSuccess) return err;
+        }
+        return cudaSuccess;
+    };
+    cudaError_t rerr;
+    if (segs.size() > (size_t)kMaxSegs) {
+        StepParamsWide P;
+        rerr = run(P, kWideSegs);
+    } else {
         StepParams P;
-        std::memset(&P, 0, sizeof(P));
-        P.n_d = p->n_d;
-        P.st = dev_state(p);
-        const bool vec = build_step_params(p, segs, b, en, nullptr, P);
-        const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_recast<ZERO_BF16>(p->device, P, vec, s)
-                                                        : launch_recast<ZERO_FP16>(p->device, P, vec, s);
-        if (err != cudaSuccess) return cuda_fail(err, "re-cast launch");
+        rerr = run(P, kMaxSegs);
     }
+    if (rerr != cudaSuccess) return cuda_fail(rerr, "re-cast launch");
     CommitParams C;
     C.st = dev_state(p);
     C.growth = p->scaler.growth_factor;
@@ -1154,17 +1199,30 @@ zero_status_t zero_gather_layer(zero_plan_t* p, int64_t unit, void* full_unit16,
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    for (int r0 = 0; r0 < p->n_d && U.shard > 0; r0 += kMaxSegs) {
+    // copy list: (source in a rank's 16-bit shard, destination in the unit, length)
+    struct Copy { const uint16_t* src; uint16_t* dst; int64_t n; };
+    std::vector<Copy> copies;
+    if (p->per_param) {
+        for (const Chunk& c : p->chunks)
+            if (c.unit == unit && c.rows > 0)
+                copies.push_back({p->ranks[(size_t)c.rank].shard16 + c.phys_off,
+                                  (uint16_t*)full_unit16 + c.contrib_off, c.rows * c.cols});
+    } else if (U.shard > 0) {
+        for (int r = 0; r < p->n_d; ++r)
+            copies.push_back({p->ranks[(size_t)r].shard16 + p->phys_off[(size_t)r][(size_t)unit],
+                              (uint16_t*)full_unit16 + r * U.shard, U.shard});
+    }
+    for (size_t c0 = 0; c0 < copies.size(); c0 += kMaxSegs) {
         CopyParams P;
         std::memset(&P, 0, sizeof(P));
         bool vec = true;
-        const int r1 = std::min(p->n_d, r0 + kMaxSegs);
-        P.n_seg = r1 - r0;
-        for (int r = r0; r < r1; ++r) {
-            CopySeg& K = P.seg[r - r0];
-            K.src = p->ranks[(size_t)r].shard16 + p->phys_off[(size_t)r][(size_t)unit];
-            K.dst = (uint16_t*)full_unit16 + r * U.shard;
-            K.n = U.shard;
+        const size_t c1 = std::min(copies.size(), c0 + kMaxSegs);
+        P.n_seg = (int)(c1 - c0);
+        for (size_t i = c0; i < c1; ++i) {
+            CopySeg& K = P.seg[i - c0];
+            K.src = copies[i].src;
+            K.dst = copies[i].dst;
+            K.n = copies[i].n;
             const int h = head16(K.dst);
             vec &= head16(K.src) == h;
             K.head = (int32_t)std::min<int64_t>(h, K.n);

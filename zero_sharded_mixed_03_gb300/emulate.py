@@ -12,7 +12,8 @@ from typing import Dict, List, Optional, Sequence
 
 import torch
 
-from . import (ZERO_BF16, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS, zero_bind, zero_bind_peer,
+from . import (ZERO_BF16, ZERO_TABLE_PARAM_CHUNKS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS,
+               zero_bind, zero_bind_peer, zero_plan_create_per_param,
                zero_gather_layer, zero_plan_create, zero_plan_destroy, zero_plan_info,
                zero_grad_norm, zero_plan_tables, zero_rank_state_elems, zero_read_state,
                zero_release_layer,
@@ -29,17 +30,30 @@ class EmulatedGroup:
 
     def __init__(self, sizes: Sequence[int], n_d: int, stage: int, bucket_elems: int = 0,
                  unit_first: Optional[Sequence[int]] = None, dtype16: int = ZERO_BF16,
-                 bound_ranks: Optional[Sequence[int]] = None, device: str = "cuda"):
+                 bound_ranks: Optional[Sequence[int]] = None, device: str = "cuda",
+                 dim0: Optional[Sequence[int]] = None):
+        """dim0 given: FSDP-2 per-parameter sharding (stage-3 semantics) instead of flat units."""
         self.device = torch.device(device)
-        self.n_d, self.stage, self.dtype16 = n_d, stage, dtype16
-        self.plan = zero_plan_create(list(sizes), n_d, stage, bucket_elems,
-                                     list(unit_first) if unit_first else None, dtype16)
+        self.n_d, self.dtype16 = n_d, dtype16
+        self.per_param = dim0 is not None
+        self.stage = 3 if self.per_param else stage
+        if self.per_param:
+            self.plan = zero_plan_create_per_param(list(sizes), list(dim0), n_d,
+                                                   list(unit_first) if unit_first else None, dtype16)
+        else:
+            self.plan = zero_plan_create(list(sizes), n_d, stage, bucket_elems,
+                                         list(unit_first) if unit_first else None, dtype16)
+        stage = self.stage
         self.info = zero_plan_info(self.plan)
         self.units = zero_plan_tables(self.plan, ZERO_TABLE_UNITS)
-        layout = zero_plan_tables(self.plan, ZERO_TABLE_STATE_LAYOUT)
         self.phys_off: Dict[int, List[int]] = {}
-        for r, u, off, _n in layout:
-            self.phys_off.setdefault(r, []).append(off)
+        self.chunks = []
+        if self.per_param:
+            # rank, unit, tensor, row0, rows, cols, c_rows, contrib_off, state_off, phys_off
+            self.chunks = zero_plan_tables(self.plan, ZERO_TABLE_PARAM_CHUNKS)
+        else:
+            for r, u, off, _n in zero_plan_tables(self.plan, ZERO_TABLE_STATE_LAYOUT):
+                self.phys_off.setdefault(r, []).append(off)
         self.bound = list(bound_ranks) if bound_ranks is not None else list(range(n_d))
         self.state: Dict[int, Dict[str, List[torch.Tensor]]] = {}
         self.shard16: Dict[int, torch.Tensor] = {}
@@ -95,8 +109,16 @@ class EmulatedGroup:
     def state_tensor(self, rank: int, name: str) -> torch.Tensor:
         return self.state[rank][name][self.current()]
 
+    def rank_chunks(self, rank: int):
+        """Per-parameter plans: the rank's chunks (rank, unit, tensor, row0, rows, cols, c_rows,
+        contrib_off, state_off, phys_off)."""
+        return [c for c in self.chunks if c[0] == rank]
+
     def logical(self, rank: int, phys: torch.Tensor) -> torch.Tensor:
         """Gather a rank's buffer from the physical layout into logical shard order."""
+        if self.per_param:
+            parts = [phys[c[9]:c[9] + c[6] * c[5]] for c in self.rank_chunks(rank)]
+            return torch.cat(parts) if parts else phys[:0]
         parts = [phys[off:off + n] for (_u, off, n, _b, _s) in self.shard_slices(rank)]
         return torch.cat(parts) if parts else phys[:0]
 
