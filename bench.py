@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=4_194_304)
     ap.add_argument("--mem-budget-gb", type=float, default=160.0)
+    ap.add_argument("--offload", action="store_true",
+                    help="ZeRO-Offload: gradients reduced on the GPU into pinned host memory, AdamW "
+                         "on the host CPU threads, 16-bit parameters copied back")
     ap.add_argument("--per-param", action="store_true",
                     help="FSDP-2 per-parameter (dim-0) sharding of the same model")
     ap.add_argument("--overlap", action="store_true",
@@ -255,7 +258,8 @@ class Bench:
         if w.stage != 3:
             all_items = len(bound)
         self.fused_launches, self.gather_launches = fused, gathers
-        self.recast_launches = launches(all_items)
+        # offloaded plans re-cast on the host: no re-cast kernel
+        self.recast_launches = 0 if w.offload else launches(all_items)
 
     def call_ptrs(self, bufs, ci):
         """Per-rank contribution pointers of call ci: base such that base + c_off hits the slice."""
@@ -324,6 +328,9 @@ def gpu_arm(args, world, rank, local):
     w = W.workload(args.config)
     if args.per_param:
         w = W.per_param_variant(w)
+    if args.offload:
+        import dataclasses
+        w = dataclasses.replace(w, offload=True)
     b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm)
     peak, peak_kind = peaks()
 
@@ -389,7 +396,7 @@ def gpu_arm(args, world, rank, local):
                 "peak_source": peak_kind, "kernel": "fused_step_kernel",
                 "launch_bytes": int(launch_bytes), "avg_launch_us": round(avg_fused_s * 1e6, 2),
                 "launches_timed": len(fused_ms)}
-    if not fused_ms:                                # overlapped schedule: no per-launch events
+    if not fused_ms or w.offload:                   # overlapped / offloaded: no fused kernel
         roofline = None
     if gather_ms:
         g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
@@ -405,7 +412,8 @@ def gpu_arm(args, world, rank, local):
                       "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
-                      "overlap": overlap, "per_param": w.per_param},
+                      "overlap": overlap, "per_param": w.per_param, "offload": w.offload,
+                      "offload_threads": b.g.offload_threads if w.offload else None},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,
            "clocks": clk}

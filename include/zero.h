@@ -281,6 +281,33 @@ zero_status_t zero_step_units_overlapped(zero_plan_t* plan, const void* const* u
                                          const zero_hyper_t* hyper, void* compute_stream,
                                          void* comm_stream, zero_step_result_t* out);
 
+/* ---- ZeRO-Offload ("ZeRO-Offload Mechanics": the optimizer step runs on the host CPU over
+ * fp32 state in host memory; gradients go to the host, updated parameters come back). ----
+ * Bind rank `rank` with host-resident state: master/m/v (host memory, zero_rank_state_elems
+ * floats each, updated in place by CPU threads), grad_host (pinned, same length: the GPU
+ * writes the averaged fp32 gradient there over NVLink-C2C), param16_host (pinned, 16-bit:
+ * the CPU writes the new parameters there before they are copied back).  shard16 / full16 /
+ * workspace as for zero_bind.  A plan's bound ranks are either all offloaded or all on the
+ * GPU; bind every rank before the first step. */
+zero_status_t zero_bind_offload(zero_plan_t* plan, int rank, float* master, float* m, float* v,
+                                float* grad_host, void* param16_host, void* shard16, void* full16,
+                                void* workspace);
+
+/* Offloaded counterpart of zero_step: reduces bucket / unit `which` on the GPU (same
+ * contributions, scaling and non-finite flag) and writes the averaged gradient into the bound
+ * ranks' grad_host.  No gradient-norm options. */
+zero_status_t zero_offload_step(zero_plan_t* plan, const void* const* grad_contribs,
+                                int64_t n_contribs, int64_t which, const zero_hyper_t* hyper,
+                                void* stream);
+
+/* End an offloaded step: synchronises `stream`, then `threads` CPU threads apply AdamW to the
+ * host state (or, if the flag is set, re-cast the unchanged master) with the same fp32
+ * operation order as the GPU kernel, the 16-bit parameters are copied to the all-gather
+ * destination on `stream`, and the commit kernel updates t / the loss scale.  out as for
+ * zero_step_finish. */
+zero_status_t zero_offload_finish(zero_plan_t* plan, int threads, void* stream,
+                                  zero_step_result_t* out);
+
 /* Mark unit `unit`'s gathered buffer free; the caller may reuse its memory. */
 zero_status_t zero_release_layer(zero_plan_t* plan, int64_t unit);
 

@@ -70,6 +70,7 @@ class Workload:
     bound_ranks: Optional[Tuple[int, ...]] = None   # ranks whose shard is updated; None = all
     dim0: Optional[Tuple[int, ...]] = None          # leading dimension of every tensor
     per_param: bool = False                         # FSDP-2 per-parameter (dim-0) sharding
+    offload: bool = False                           # ZeRO-Offload: fp32 state on the host CPU
 
     @property
     def phi(self) -> int:

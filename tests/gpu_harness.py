@@ -64,7 +64,8 @@ class Run:
         self.w = w
         b = bound if bound is not None else w.ranks()
         self.g = EmulatedGroup(w.sizes, w.n_d, w.stage, w.bucket_elems, w.unit_first or None,
-                               w.dtype, b, dim0=w.dim0 if w.per_param else None)
+                               w.dtype, b, dim0=w.dim0 if w.per_param else None,
+                               offload=w.offload)
         self.units = self.g.units
         self.info = self.g.info
         self.bound = list(b)
@@ -186,7 +187,8 @@ class Run:
             sel = np.nonzero(rank == r)[0]
             pi = torch.from_numpy(phys[sel]).cuda()
             for k in out:
-                out[k][sel] = self.g.state_tensor(int(r), k)[pi].cpu().numpy()
+                t = self.g.state_tensor(int(r), k)
+                out[k][sel] = t[pi.to(t.device)].cpu().numpy()
             if self.w.stage == 3:
                 out16[sel] = self.g.shard16[int(r)][pi].cpu().numpy().view(np.uint16)
         if self.w.stage != 3:

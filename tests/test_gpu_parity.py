@@ -533,3 +533,57 @@ def test_per_param_overlapped_schedule():
         test_overlapped_stage3_schedule_full_parity("pp")
     finally:
         del OVERLAP_CASES["pp"]
+
+
+# ---------------------------------------------------------------------- ZeRO-Offload
+
+OFFLOAD_CASES = {
+    "z1_nd4": dataclasses.replace(SMALL_CASES["z1_nd4_tiles_ragged_tail"], wid=160, offload=True),
+    "z2_nd8_fp16_buckets_inf": dataclasses.replace(SMALL_CASES["z2_nd8_fp16_buckets_inf"], wid=161,
+                                                   offload=True),
+    "z2_nd5_odd_bucket_scalar_path": dataclasses.replace(
+        SMALL_CASES["z2_nd5_odd_bucket_scalar_path"], wid=162, offload=True),
+    "z3_nd3_fp16_peers_skip_first": dataclasses.replace(
+        SMALL_CASES["z3_nd3_fp16_peers_skip_first"], wid=163, offload=True),
+    "pp_nd4_units": dataclasses.replace(PP_CASES["pp_nd4_units"], wid=164, offload=True),
+}
+
+
+@pytest.mark.parametrize("name", list(OFFLOAD_CASES))
+def test_offload_full_parity(name):
+    """Host-CPU AdamW over host-resident state (gradients reduced on the GPU and written to
+    pinned host memory) against the oracle: the same fp32 operation order, so 0 mismatches."""
+    mism = _run_full(OFFLOAD_CASES[name])
+    assert mism == 0
+
+
+def test_offload_sampled_config1():
+    w = dataclasses.replace(W.workload(1), offload=True)
+    n, mism = _run_sampled(w)
+    print(f"offloaded configs[1]: {n} sampled elements, {mism} bit mismatches")
+    assert mism == 0
+
+
+def test_offload_rejects_mixing_and_pageable_buffers():
+    plan = Z.zero_plan_create([1000], 2, 1, 0, None, Z.ZERO_BF16)
+    try:
+        n = Z.zero_rank_state_elems(plan, 0)
+        ws = torch.zeros(Z.zero_plan_info(plan).workspace_bytes // 4, dtype=torch.int32, device="cuda")
+        f16 = torch.zeros(1000, dtype=torch.int16, device="cuda")
+        host = [torch.zeros(n, dtype=torch.float32) for _ in range(4)]     # pageable
+        p16 = torch.zeros(n, dtype=torch.int16)
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_bind_offload(plan, 0, *(h.data_ptr() for h in host), p16.data_ptr(), None,
+                                f16.data_ptr(), ws.data_ptr())
+        assert e.value.status == Z.ZERO_EINVAL
+        dev = [torch.zeros(n, dtype=torch.float32, device="cuda") for _ in range(6)]
+        Z.zero_bind(plan, 1, [dev[0].data_ptr(), dev[1].data_ptr()], [dev[2].data_ptr(), dev[3].data_ptr()],
+                    [dev[4].data_ptr(), dev[5].data_ptr()], None, f16.data_ptr(), ws.data_ptr())
+        pinned = [torch.zeros(n, dtype=torch.float32, pin_memory=True) for _ in range(4)]
+        p16p = torch.zeros(n, dtype=torch.int16, pin_memory=True)
+        with pytest.raises(Z.ZeroError) as e:                      # on-GPU rank already bound
+            Z.zero_bind_offload(plan, 0, *(h.data_ptr() for h in pinned), p16p.data_ptr(), None,
+                                f16.data_ptr(), ws.data_ptr())
+        assert e.value.status == Z.ZERO_ESTATE
+    finally:
+        Z.zero_plan_destroy(plan)

@@ -29,7 +29,8 @@ EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", 
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",
             "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_set_scaler",
             "zero_read_state", "zero_restore_state", "zero_grad_norm",
-            "zero_step_units_overlapped",
+            "zero_step_units_overlapped", "zero_bind_offload", "zero_offload_step",
+            "zero_offload_finish",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
@@ -126,6 +127,12 @@ def lib() -> ctypes.CDLL:
         L.zero_step_units_overlapped.restype = st
         L.zero_step_units_overlapped.argtypes = [_vp, _vp, _i64, _vp, ctypes.POINTER(zero_hyper_t),
                                                  _vp, _vp, ctypes.POINTER(zero_step_result_t)]
+        L.zero_bind_offload.restype = st
+        L.zero_bind_offload.argtypes = [_vp, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.zero_offload_step.restype = st
+        L.zero_offload_step.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t), _vp]
+        L.zero_offload_finish.restype = st
+        L.zero_offload_finish.argtypes = [_vp, _int, _vp, ctypes.POINTER(zero_step_result_t)]
         L.zero_grad_norm.restype = st
         L.zero_grad_norm.argtypes = [_vp, _vp, _i64, _i64, _vp]
         L.zero_restore_state.restype = st
@@ -252,6 +259,28 @@ def zero_step_units_overlapped(plan: int, unit_contribs: Sequence[int], gather_b
                                             _ptr_array(gather_bufs), ctypes.byref(hyper),
                                             compute_stream or None, comm_stream or None,
                                             ctypes.byref(res) if res is not None else None))
+    return res
+
+
+def zero_bind_offload(plan: int, rank: int, master: int, m: int, v: int, grad_host: int,
+                      param16_host: int, shard16: Optional[int], full16: Optional[int],
+                      workspace: int) -> None:
+    _check(lib().zero_bind_offload(plan, rank, master or None, m or None, v or None,
+                                   grad_host or None, param16_host or None, shard16 or None,
+                                   full16 or None, workspace or None))
+
+
+def zero_offload_step(plan: int, grad_contribs: Sequence[int], which: int, hyper: zero_hyper_t,
+                      stream: int = 0) -> None:
+    _check(lib().zero_offload_step(plan, _ptr_array(grad_contribs), len(grad_contribs), which,
+                                   ctypes.byref(hyper), stream or None))
+
+
+def zero_offload_finish(plan: int, threads: int, stream: int = 0,
+                        wait: bool = True) -> Optional[zero_step_result_t]:
+    res = zero_step_result_t() if wait else None
+    _check(lib().zero_offload_finish(plan, threads, stream or None,
+                                     ctypes.byref(res) if res is not None else None))
     return res
 
 

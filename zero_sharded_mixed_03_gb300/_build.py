@@ -11,7 +11,9 @@ OBJ_DIR = os.path.join(HERE, "_build")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
-SOURCES = ["zero_plan.cpp", "zero_step.cu"]
+SOURCES = ["zero_plan.cpp", "zero_step.cu", "zero_offload.cpp"]
+# the host AdamW must round every fp32 operation separately, like the GPU kernel
+EXTRA = {"zero_offload.cpp": ["-Xcompiler", "-ffp-contract=off", "-Xcompiler", "-fno-fast-math"]}
 
 
 def build(verbose: bool = False) -> str:
@@ -20,7 +22,7 @@ def build(verbose: bool = False) -> str:
     for src in SOURCES:
         obj = os.path.join(OBJ_DIR, src + ".o")
         objs.append(obj)
-        cmd = [NVCC, *GENCODE, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [NVCC, *GENCODE, *FLAGS, *EXTRA.get(src, []), "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((cmd, subprocess.Popen(cmd)))
@@ -28,7 +30,7 @@ def build(verbose: bool = False) -> str:
         if pr.wait() != 0:
             raise RuntimeError("compile failed: " + " ".join(cmd))
     tmp = f"{LIB}.{os.getpid()}.tmp"             # renamed into place: never half-written
-    subprocess.run([NVCC, *GENCODE, "-shared", *objs, "-o", tmp], check=True)
+    subprocess.run([NVCC, *GENCODE, "-shared", *objs, "-o", tmp, "-lpthread"], check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -31,7 +31,26 @@ struct Rank {
     float* m[2] = {nullptr, nullptr};
     float* v[2] = {nullptr, nullptr};
     uint16_t* shard16 = nullptr; // stage 3
+    // ZeRO-Offload: fp32 state and the gradient / 16-bit staging live in host memory
+    bool offload = false;
+    float* grad_host = nullptr;   // averaged fp32 gradient written by the GPU (pinned)
+    uint16_t* param16_host = nullptr;   // 16-bit parameters produced by the CPU (pinned)
 };
+
+// A contiguous piece of an offloaded rank's state for the CPU update.
+struct CpuSpan {
+    float* master;
+    float* m;
+    float* v;
+    const float* grad;
+    uint16_t* out16;
+    int64_t n;
+};
+
+// CPU AdamW (or, for a skipped step, the re-cast of the unchanged master) over the spans, on
+// `threads` threads; k = the nine fp32 step constants.
+void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16, bool skipped,
+               int threads);
 
 // Elementwise work item of one launch: n elements of one rank's shard.
 //   contributions: element c_off of every contribution buffer
@@ -83,6 +102,7 @@ struct zero_plan {
     std::vector<std::vector<int64_t>> phys_off;
     // FSDP-2 per-parameter plans (stage-3 semantics, one chunk per rank and tensor).
     bool per_param = false;
+    bool offload = false;               // bound ranks keep their fp32 state in host memory
     std::vector<int64_t> dim0;
     std::vector<zero::Chunk> chunks;    // rank-major, then unit, then tensor
     std::vector<int64_t> state_elems;

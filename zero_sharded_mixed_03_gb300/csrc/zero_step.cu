@@ -502,6 +502,79 @@ __global__ void __launch_bounds__(kThreads) grad_norm_kernel(const __grid_consta
     block_norm_commit(P, norm2.value());
 }
 
+// ZeRO-Offload: the reduction of the fused kernel, its averaged gradient written into the
+// rank's pinned host buffer (S.p[0]) over NVLink-C2C instead of feeding an on-GPU update.
+template <int DT, int NB, int VEC, typename PT>
+__global__ void __launch_bounds__(kThreads) reduce_to_host_kernel(const __grid_constant__ PT P)
+{
+    __shared__ float sk4[4];
+    __shared__ int scur;
+    block_constants(P, sk4, &scur);
+    const float inv = sk4[2];
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    bool bad = false;
+    auto one = [&](const KSeg& S, int64_t e) {
+        float sum = 0.0f;
+        for (int r = 0; r < P.n_d; ++r) sum = __fadd_rn(sum, widen1<DT>(P.c[r][S.c_off + e]));
+        const float g = __fmul_rn(sum, inv);
+        bad |= nonfinite(g);
+        S.p[0][e] = g;
+    };
+    if constexpr (VEC == 8) {
+        for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
+            const KSeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) one(S, e);
+        }
+    }
+    int s = 0;
+    for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
+        while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
+        const KSeg& S = P.seg[s];
+        if constexpr (VEC == 8) {
+            const int64_t e = S.head + 8 * (vi - S.vbeg);
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+            for (int r0 = 0; r0 < P.n_d; r0 += NB) {
+                uint4 c[NB];
+#pragma unroll
+                for (int q = 0; q < NB; ++q)
+                    if (r0 + q < P.n_d) c[q] = ld_stream(P.c[r0 + q] + S.c_off + e);
+#pragma unroll
+                for (int q = 0; q < NB; ++q) {
+                    if (r0 + q < P.n_d) {
+                        const uint32_t w[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float lo, hi;
+                            widen2<DT>(w[j], lo, hi);
+                            acc[2 * j] = __fadd_rn(acc[2 * j], lo);
+                            acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], hi);
+                        }
+                    }
+                }
+            }
+            float g[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                g[j] = __fmul_rn(acc[j], inv);
+                bad |= nonfinite(g[j]);
+            }
+            float4* dst = reinterpret_cast<float4*>(S.p[0] + e);
+            dst[0] = make_float4(g[0], g[1], g[2], g[3]);
+            dst[1] = make_float4(g[4], g[5], g[6], g[7]);
+        } else {
+            one(S, vi - S.vbeg);
+        }
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(P.flag, 1u);
+}
+
 // ------------------------------------------------------------------ skip: re-cast + commit
 
 // On a flagged step the fused kernels have already written 16-bit values of the rejected
@@ -763,6 +836,16 @@ cudaError_t launch_norm(int dev, PT& P, bool vec, cudaStream_t st)
 }
 
 template <int DT, typename PT>
+cudaError_t launch_reduce_to_host(int dev, PT& P, bool vec, cudaStream_t st)
+{
+    finalize_vectors(P, vec);
+    const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
+    if (!vec) launch_grid(reduce_to_host_kernel<DT, 1, 1, PT>, dev, work, P, st);
+    else launch_grid(reduce_to_host_kernel<DT, kRankBatch, 8, PT>, dev, work, P, st);
+    return cudaGetLastError();
+}
+
+template <int DT, typename PT>
 cudaError_t launch_recast(int dev, PT& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
@@ -859,6 +942,33 @@ zero_status_t check_call(const zero_plan_t* p, const void* const* grad_contribs,
 }
 
 // Fill and launch one chunk of segments [b, e) of a zero_step / zero_grad_norm call.
+// Offload work items: the kernel writes the averaged gradient at grad_host + s_off.
+template <typename PT>
+bool build_offload_params(const zero_plan* p, const std::vector<Segment>& segs, size_t b, size_t e,
+                          const void* const* contribs, PT& P)
+{
+    bool vec_ok = true;
+    P.n_seg = (int)(e - b);
+    for (size_t i = b; i < e; ++i) {
+        const Segment& sg = segs[i];
+        const Rank& R = p->ranks[(size_t)sg.rank];
+        KSeg& K = P.seg[i - b];
+        std::memset(&K, 0, sizeof(K));
+        K.p[0] = R.grad_host + sg.s_off;
+        K.c_off = sg.c_off;
+        K.n = sg.n;
+        const int hd = head16((const uint16_t*)contribs[0] + sg.c_off);
+        for (int r = 1; r < p->n_d; ++r)
+            vec_ok &= head16((const uint16_t*)contribs[r] + sg.c_off) == hd;
+        const int64_t hh = std::min<int64_t>(hd, sg.n);
+        vec_ok &= aligned(K.p[0] + hh, 16);
+        K.head = (int32_t)hh;
+        K.nvec = (sg.n - hh) / 8;
+        K.tail = (int32_t)(sg.n - hh - 8 * K.nvec);
+    }
+    return vec_ok;
+}
+
 template <typename PT>
 void fill_call_params(const zero_plan* p, const void* const* grad_contribs, PT& P)
 {
@@ -891,6 +1001,7 @@ zero_status_t zero_bind(zero_plan_t* p, int rank, float* const master[2], float*
     if (!p || !master || !m || !v) return fail(ZERO_EINVAL, "zero_bind: NULL argument");
     if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind: bad rank");
     if (p->in_step || p->stepped) return fail(ZERO_ESTATE, "zero_bind: bind every rank before the first step");
+    if (p->offload) return fail(ZERO_ESTATE, "zero_bind: this plan offloads its ranks (zero_bind_offload)");
     float* bufs[6] = {master[0], master[1], m[0], m[1], v[0], v[1]};
     const int64_t elems = p->state_elems[(size_t)rank];
     if (elems > 0 && (master[0] == master[1] || m[0] == m[1] || v[0] == v[1]))
@@ -1030,6 +1141,7 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
                         int64_t which, const zero_hyper_t* hyper, void* stream)
 {
     if (!hyper) return fail(ZERO_EINVAL, "zero_step: NULL argument");
+    if (p && p->offload) return fail(ZERO_ESTATE, "zero_step: offloaded plan (zero_offload_step)");
     zero_status_t cst = check_call(p, grad_contribs, n_contribs, which, "zero_step");
     if (cst != ZERO_OK) return cst;
     if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
@@ -1258,6 +1370,181 @@ zero_status_t zero_release_layer(zero_plan_t* p, int64_t unit)
         return fail(ZERO_EINVAL, "zero_release_layer: unit out of range");
     if (!p->gathered[(size_t)unit]) return fail(ZERO_ESTATE, "zero_release_layer: unit not gathered");
     p->gathered[(size_t)unit] = 0;
+    return ZERO_OK;
+}
+
+zero_status_t zero_bind_offload(zero_plan_t* p, int rank, float* master, float* m, float* v,
+                                float* grad_host, void* param16_host, void* shard16, void* full16,
+                                void* workspace)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_bind_offload: NULL plan");
+    if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind_offload: bad rank");
+    if (p->in_step || p->stepped)
+        return fail(ZERO_ESTATE, "zero_bind_offload: bind every rank before the first step");
+    for (const Rank& R : p->ranks)
+        if (R.bound && !R.offload)
+            return fail(ZERO_ESTATE, "zero_bind_offload: the plan already has on-GPU ranks");
+    const int64_t elems = p->state_elems[(size_t)rank];
+    if (elems > 0 && (!master || !m || !v || !grad_host || !param16_host))
+        return fail(ZERO_EINVAL, "zero_bind_offload: NULL host buffer");
+    if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(grad_host, 4) ||
+        !aligned(param16_host, 2))
+        return fail(ZERO_EALIGN, "zero_bind_offload: host buffers not aligned to their element size");
+    if (elems > 0) {
+        // the GPU writes grad_host and the copy engines read param16_host: both must be pinned
+        const void* pinned[2] = {grad_host, param16_host};
+        for (const void* q : pinned) {
+            cudaPointerAttributes at;
+            const cudaError_t e = cudaPointerGetAttributes(&at, q);
+            if (e != cudaSuccess || at.type != cudaMemoryTypeHost)
+                return fail(ZERO_EINVAL, "zero_bind_offload: grad_host and param16_host must be "
+                                         "pinned host memory (cudaHostAlloc / cudaHostRegister)");
+        }
+    }
+    // the 16-bit destination and the workspace are device memory, as for zero_bind
+    if (p->stage == 3) {
+        if (elems > 0 && !shard16) return fail(ZERO_EINVAL, "zero_bind_offload: stage 3 needs shard16");
+    } else if (!full16 && !p->full16 && p->phi_pad > 0) {
+        return fail(ZERO_EINVAL, "zero_bind_offload: stages 1/2 need the flat 16-bit buffer");
+    }
+    if (!workspace && !p->workspace) return fail(ZERO_EINVAL, "zero_bind_offload: workspace is NULL");
+    if (workspace && p->workspace && workspace != p->workspace)
+        return fail(ZERO_EINVAL, "zero_bind_offload: workspace differs from an earlier bind");
+    if (!aligned(workspace, 16)) return fail(ZERO_EALIGN, "zero_bind_offload: workspace not 16-byte aligned");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_bind_offload: cudaGetDevice");
+    if (workspace && !p->workspace) {
+        DevState init;
+        std::memset(&init, 0, sizeof(init));
+        init.scale = 1.0;
+        e = cudaMemcpy(workspace, &init, sizeof(init), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "zero_bind_offload: initialising the workspace");
+        p->workspace = (uint32_t*)workspace;
+    }
+    p->device = dev;
+    if (full16) p->full16 = (uint16_t*)full16;
+    Rank& R = p->ranks[(size_t)rank];
+    R.bound = true;
+    R.offload = true;
+    R.master[0] = master;
+    R.m[0] = m;
+    R.v[0] = v;
+    R.master[1] = R.m[1] = R.v[1] = nullptr;
+    R.grad_host = grad_host;
+    R.param16_host = (uint16_t*)param16_host;
+    R.shard16 = (uint16_t*)shard16;
+    p->offload = true;
+    return ZERO_OK;
+}
+
+zero_status_t zero_offload_step(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
+                                int64_t which, const zero_hyper_t* hyper, void* stream)
+{
+    if (!hyper) return fail(ZERO_EINVAL, "zero_offload_step: NULL argument");
+    zero_status_t st = check_call(p, grad_contribs, n_contribs, which, "zero_offload_step");
+    if (st != ZERO_OK) return st;
+    if (!p->offload) return fail(ZERO_ESTATE, "zero_offload_step: no offloaded rank bound");
+    if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
+        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay))
+        return fail(ZERO_EINVAL, "zero_offload_step: betas must lie in [0, 1); lr, eps, wd finite");
+    if (hyper->max_grad_norm != 0.0 || hyper->flags != 0)
+        return fail(ZERO_EINVAL, "zero_offload_step: no gradient-norm options on the offload path");
+    if (p->in_step && std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0)
+        return fail(ZERO_EINVAL, "zero_offload_step: hyperparameters changed inside a step");
+    if (which == -1) {
+        if (p->in_step) return fail(ZERO_ESTATE, "zero_offload_step: bucket -1 must be the only call");
+    } else if (p->covered[(size_t)which]) {
+        return fail(ZERO_ESTATE, "zero_offload_step: bucket/unit already stepped in this step");
+    }
+    st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!p->in_step) {
+        if (p->bias_len == 0 || p->bias_beta1 != hyper->beta1 || p->bias_beta2 != hyper->beta2) {
+            st = upload_bias_table(p, hyper->beta1, hyper->beta2, s);
+            if (st != ZERO_OK) return st;
+        }
+        step_constants(*hyper, 1, 1.0, p->n_d, p->consts);
+        p->step_hyper = *hyper;
+    }
+    const std::vector<Segment> segs = step_segments(p, which, 0);
+    auto run = [&](auto& P, size_t cap) -> cudaError_t {
+        for (size_t b = 0; b < segs.size(); b += cap) {
+            const size_t e = std::min(segs.size(), b + cap);
+            fill_call_params(p, grad_contribs, P);
+            const bool vec = build_offload_params(p, segs, b, e, grad_contribs, P);
+            const cudaError_t err = p->dtype16 == ZERO_BF16
+                                        ? launch_reduce_to_host<ZERO_BF16>(p->device, P, vec, s)
+                                        : launch_reduce_to_host<ZERO_FP16>(p->device, P, vec, s);
+            if (err != cudaSuccess) return err;
+        }
+        return cudaSuccess;
+    };
+    cudaError_t err;
+    if (segs.size() > (size_t)kMaxSegs) {
+        StepParamsWide P;
+        err = run(P, kWideSegs);
+    } else {
+        StepParams P;
+        err = run(P, kMaxSegs);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "reduce-to-host launch");
+    p->in_step = true;
+    if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
+    else p->covered[(size_t)which] = 1;
+    return ZERO_OK;
+}
+
+zero_status_t zero_offload_finish(zero_plan_t* p, int threads, void* stream, zero_step_result_t* out)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_offload_finish: NULL plan");
+    if (!p->offload) return fail(ZERO_ESTATE, "zero_offload_finish: no offloaded rank bound");
+    if (!p->in_step) return fail(ZERO_ESTATE, "zero_offload_finish: no open step");
+    for (int64_t b = 0; b < p->n_buckets; ++b)
+        if (!p->covered[(size_t)b])
+            return fail(ZERO_ESTATE, "zero_offload_finish: a bucket/unit was not stepped");
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the gradients are in host memory once the stream is drained; t and the scale decide
+    // the constants, the flag decides between the update and the re-cast
+    DevState host;
+    cudaError_t e = cudaMemcpyAsync(&host, p->workspace, sizeof(host), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: reading the step state");
+    float k9[9];
+    step_constants(p->step_hyper, host.t + 1, host.scale, p->n_d, k9);
+    const std::vector<Segment> segs = shard_segments_all(p);
+    std::vector<CpuSpan> spans;
+    for (const Segment& sg : segs) {
+        const Rank& R = p->ranks[(size_t)sg.rank];
+        spans.push_back(CpuSpan{R.master[0] + sg.s_off, R.m[0] + sg.s_off, R.v[0] + sg.s_off,
+                                R.grad_host + sg.s_off, R.param16_host + sg.s_off, sg.n});
+    }
+    cpu_adamw(spans, k9, p->dtype16, host.flag != 0, threads > 0 ? threads : 1);
+    // 16-bit parameters back to the all-gather destination
+    for (const Segment& sg : segs) {
+        const Rank& R = p->ranks[(size_t)sg.rank];
+        e = cudaMemcpyAsync(sg.out16 + sg.o_off, R.param16_host + sg.s_off, 2 * (size_t)sg.n,
+                            cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: copying the parameters");
+    }
+    CommitParams C;
+    C.st = dev_state(p);
+    C.growth = p->scaler.growth_factor;
+    C.backoff = p->scaler.backoff_factor;
+    C.min_scale = p->scaler.min_scale;
+    C.interval = p->scaler.growth_interval;
+    C.dynamic = p->scaler_dynamic;
+    commit_kernel<<<1, 32, 0, s>>>(C);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    p->in_step = false;
+    p->stepped = true;
+    std::fill(p->covered.begin(), p->covered.end(), 0);
+    if (out) return read_state(p, s, out);
     return ZERO_OK;
 }
 

@@ -13,7 +13,8 @@ from typing import Dict, List, Optional, Sequence
 import torch
 
 from . import (ZERO_BF16, ZERO_TABLE_PARAM_CHUNKS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS,
-               zero_bind, zero_bind_peer, zero_plan_create_per_param,
+               zero_bind, zero_bind_offload, zero_bind_peer, zero_offload_finish,
+               zero_offload_step, zero_plan_create_per_param,
                zero_gather_layer, zero_plan_create, zero_plan_destroy, zero_plan_info,
                zero_grad_norm, zero_plan_tables, zero_rank_state_elems, zero_read_state,
                zero_release_layer,
@@ -31,9 +32,15 @@ class EmulatedGroup:
     def __init__(self, sizes: Sequence[int], n_d: int, stage: int, bucket_elems: int = 0,
                  unit_first: Optional[Sequence[int]] = None, dtype16: int = ZERO_BF16,
                  bound_ranks: Optional[Sequence[int]] = None, device: str = "cuda",
-                 dim0: Optional[Sequence[int]] = None):
-        """dim0 given: FSDP-2 per-parameter sharding (stage-3 semantics) instead of flat units."""
+                 dim0: Optional[Sequence[int]] = None, offload: bool = False,
+                 offload_threads: int = 0):
+        """dim0 given: FSDP-2 per-parameter sharding (stage-3 semantics) instead of flat units.
+        offload: ZeRO-Offload -- the bound ranks' fp32 state lives in (pinned) host memory and is
+        updated by `offload_threads` CPU threads (default: all CPUs)."""
+        import os
         self.device = torch.device(device)
+        self.offload = offload
+        self.offload_threads = offload_threads or (os.cpu_count() or 1)
         self.n_d, self.dtype16 = n_d, dtype16
         self.per_param = dim0 is not None
         self.stage = 3 if self.per_param else stage
@@ -62,8 +69,27 @@ class EmulatedGroup:
         self.full16 = None
         if stage != 3:
             self.full16 = torch.zeros(int(self.info.phi_pad), dtype=torch.int16, device=self.device)
+        self.grad_host: Dict[int, torch.Tensor] = {}
+        self.param16_host: Dict[int, torch.Tensor] = {}
         for r in self.bound:
             n = zero_rank_state_elems(self.plan, r)
+            if offload:
+                st = {k: [torch.zeros(n, dtype=torch.float32, pin_memory=True)]
+                      for k in ("master", "m", "v")}
+                self.state[r] = st
+                self.grad_host[r] = torch.zeros(n, dtype=torch.float32, pin_memory=True)
+                self.param16_host[r] = torch.zeros(n, dtype=torch.int16, pin_memory=True)
+                sh = None
+                if stage == 3:
+                    sh = torch.zeros(n, dtype=torch.int16, device=self.device)
+                    self.shard16[r] = sh
+                zero_bind_offload(self.plan, r, st["master"][0].data_ptr(), st["m"][0].data_ptr(),
+                                  st["v"][0].data_ptr(), self.grad_host[r].data_ptr(),
+                                  self.param16_host[r].data_ptr(),
+                                  sh.data_ptr() if sh is not None else None,
+                                  self.full16.data_ptr() if self.full16 is not None else None,
+                                  self.workspace.data_ptr())
+                continue
             st = {k: [torch.zeros(n, dtype=torch.float32, device=self.device) for _ in range(2)]
                   for k in ("master", "m", "v")}
             self.state[r] = st
@@ -107,6 +133,8 @@ class EmulatedGroup:
         zero_set_scaler(self.plan, scaler, _stream_handle(stream))
 
     def state_tensor(self, rank: int, name: str) -> torch.Tensor:
+        if self.offload:                       # updated in place on the host
+            return self.state[rank][name][0]
         return self.state[rank][name][self.current()]
 
     def rank_chunks(self, rank: int):
@@ -124,6 +152,9 @@ class EmulatedGroup:
 
     # ------------------------------------------------------------------ the step
     def step(self, contribs: Sequence[int], which: int, hyper, stream=None) -> None:
+        if self.offload:
+            zero_offload_step(self.plan, list(contribs), which, hyper, _stream_handle(stream))
+            return
         zero_step(self.plan, list(contribs), which, hyper, _stream_handle(stream))
 
     def grad_norm(self, contribs: Sequence[int], which: int, stream=None) -> None:
@@ -132,6 +163,8 @@ class EmulatedGroup:
 
     def finish(self, stream=None, wait: bool = True):
         """Commit the step on the device; wait=True also returns the read-back state."""
+        if self.offload:
+            return zero_offload_finish(self.plan, self.offload_threads, _stream_handle(stream), wait)
         return zero_step_finish(self.plan, _stream_handle(stream), wait)
 
     def gather(self, unit: int, dst: torch.Tensor, stream=None) -> None:
