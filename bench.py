@@ -280,7 +280,7 @@ class Bench:
             self.g.plan, ptrs, [b.data_ptr() for b in self._gbufs], self.hyper,
             self.torch.cuda.current_stream().cuda_stream, comm.cuda_stream, wait)
         launches = ((1 + self.clip) * sum(self.fused_launches) + sum(self.gather_launches)
-                    + self.recast_launches + 1)
+                    + self.recast_launches + (0 if self.recast_launches else 1))
         return res, launches
 
     def step(self, bufs, events=None, gather_events=None, wait=False):
@@ -312,8 +312,9 @@ class Bench:
                 c.record()
             launches += self.fused_launches[ci]
         res = self.g.finish(wait=wait)
-        # the re-cast kernel(s) (which return at once unless the step was skipped) + the commit
-        launches += self.recast_launches + 1
+        # the re-cast kernel(s) (which return at once unless the step was skipped); the last one
+        # also commits (a separate commit launch only when there is nothing to re-cast)
+        launches += self.recast_launches + (0 if self.recast_launches else 1)
         return res, launches
 
 

@@ -587,3 +587,51 @@ def test_offload_rejects_mixing_and_pageable_buffers():
         assert e.value.status == Z.ZERO_ESTATE
     finally:
         Z.zero_plan_destroy(plan)
+
+
+# ---------------------------------------------------------------------- tiny-case sweep
+
+def test_tiny_case_sweep():
+    """Bounds and peeling: 150 random plans with phi <= 80, N_d 1..16, stages 1/2/3, bf16 and
+    fp16, odd buckets, zero-size tensors, and half of them fed contributions that start one
+    element past a 16-byte boundary (scalar path); two steps each against the oracle."""
+    rng = np.random.default_rng(60)
+    for trial in range(150):
+        nt = int(rng.integers(1, 7))
+        sizes = [int(x) for x in rng.integers(0, 15, size=nt)]
+        if sum(sizes) == 0:
+            sizes[0] = 1
+        n_d = int(rng.integers(1, 17))
+        stage = int(rng.integers(1, 4))
+        units = ()
+        if stage == 3 and nt > 1:
+            units = tuple([0] + sorted(set(int(x) for x in rng.integers(1, nt, size=2))))
+        bucket = int(rng.integers(0, 30)) if stage == 2 else 0
+        dtype = int(rng.integers(0, 2))
+        w = W.Workload(wid=300 + trial, name=f"tiny{trial}", sizes=tuple(sizes), n_d=n_d,
+                       stage=stage, bucket_elems=bucket, unit_first=units, dtype=dtype, steps=2,
+                       hyper=W.Hyper(), scaler=None)
+        shift = bool(rng.integers(0, 2))
+        run = H.Run(w)
+        o = H.OracleFull(w, run.bound)
+        try:
+            for k in (1, 2):
+                for which, lo, hi in run.ranges():
+                    if stage == 3:
+                        run.g.gather(which, run.gather_buf)
+                        run.g.release(which)
+                    ptrs = []
+                    for r in range(n_d):
+                        H.fill_device(run.contribs[r], synth.grad_stream(w, k, r), run.units, lo, hi)
+                        if shift:
+                            sh = torch.zeros(run.contribs[r].numel() + 1, dtype=torch.int16, device="cuda")
+                            sh[1:] = run.contribs[r]
+                            run.contribs[r] = sh[1:]
+                        ptrs.append(run.contribs[r].data_ptr())
+                    run.g.step(ptrs, which, run.hyper)
+                res = run.g.finish()
+                flag = o.step(k)
+                assert res.skipped == flag == 0 and res.t == k, trial
+                _compare_full(run, o, f"tiny case {trial} step {k}")
+        finally:
+            run.close()

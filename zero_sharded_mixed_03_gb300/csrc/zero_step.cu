@@ -76,6 +76,13 @@ struct KSeg {
     int32_t tail;      // scalar elements after the body
 };
 
+struct CommitParams {
+    DevState* st;
+    double growth, backoff, min_scale;
+    int64_t interval;
+    int32_t dynamic;           // 0: fixed loss scale (no back-off, no growth)
+};
+
 template <int MS>
 struct StepParamsT {
     const uint16_t* c[ZERO_MAX_RANKS];
@@ -94,18 +101,13 @@ struct StepParamsT {
     DevState* st;              // nullptr: host mode (constants in k, current half 0)
     double max_norm;           // clip mode: the bound on the global gradient norm
     double* partials;          // norm modes: one slot per block
+    CommitParams commit;       // re-cast launch that also closes the step
+    int32_t do_commit;
 };
 // The usual parameter block (4 KB), and a wide one (26 KB, under the 32 KB kernel-parameter
 // limit) for calls with many work items, e.g. per-parameter plans (one item per tensor chunk).
 using StepParams = StepParamsT<kMaxSegs>;
 using StepParamsWide = StepParamsT<kWideSegs>;
-
-struct CommitParams {
-    DevState* st;
-    double growth, backoff, min_scale;
-    int64_t interval;
-    int32_t dynamic;           // 0: fixed loss scale (no back-off, no growth)
-};
 
 struct CopySeg {
     const uint16_t* src;
@@ -590,11 +592,10 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
         scur = (int)st->cur;
     }
     __syncthreads();
-    if (!go) return;
     const int cur = scur;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    if constexpr (VEC == 8) {
+    if (go && VEC == 8) {
         for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
             const KSeg& S = P.seg[q / kScalarSlots];
             const int k = (int)(q % kScalarSlots);
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
         }
     }
     int s = 0;
-    for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
+    for (int64_t vi = go ? tid : P.total_vec; vi < P.total_vec; vi += stride) {
         while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
         const KSeg& S = P.seg[s];
         if constexpr (VEC == 8) {
@@ -623,14 +624,31 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
             S.out16[e] = narrow1<DT>(S.p[cur][e]);
         }
     }
+    // The last launch of the re-cast also closes the step: the last block to finish (atomic
+    // ticket; every block read the flag and the current half before taking its ticket)
+    // applies the commit.
+    if (P.do_commit) {
+        __shared__ bool last;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            last = atomicAdd(&P.st->blocks_done, 1u) == gridDim.x - 1;
+        }
+        __syncthreads();
+        if (last && threadIdx.x == 0) {
+            __threadfence();
+            reinterpret_cast<volatile DevState*>(P.st)->blocks_done = 0;
+            commit_state(P.commit);
+            __threadfence();
+        }
+    }
 }
 
 // Close the step on the device: flag clear -> flip the current half, t += 1, count a clean
 // step and grow the scale after `interval` of them; flag set -> keep the state, back the
 // scale off (not below min_scale).  Then clear the flag for the next step.
-__global__ void commit_kernel(const CommitParams C)
+__device__ __forceinline__ void commit_state(const CommitParams& C)
 {
-    if (blockIdx.x != 0 || threadIdx.x != 0) return;
     volatile DevState* st = C.st;
     if (st->flag) {
         st->last_skipped = 1;
@@ -656,6 +674,12 @@ __global__ void commit_kernel(const CommitParams C)
     st->last_norm_valid = st->norm_valid;
     st->norm2 = 0.0;
     st->norm_valid = 0;
+}
+
+__global__ void commit_kernel(const CommitParams C)
+{
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    commit_state(C);
 }
 
 // ------------------------------------------------------------------ gather kernel (stage 3)
@@ -1219,12 +1243,21 @@ zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t*
 
     // Re-cast (no-op unless the flag is set), then the one-thread commit.
     const std::vector<Segment> segs = shard_segments_all(p);
+    CommitParams C;
+    C.st = dev_state(p);
+    C.growth = p->scaler.growth_factor;
+    C.backoff = p->scaler.backoff_factor;
+    C.min_scale = p->scaler.min_scale;
+    C.interval = p->scaler.growth_interval;
+    C.dynamic = p->scaler_dynamic;
     auto run = [&](auto& P, size_t cap) -> cudaError_t {
         for (size_t b = 0; b < segs.size(); b += cap) {
             const size_t en = std::min(segs.size(), b + cap);
             std::memset(&P, 0, sizeof(P));
             P.n_d = p->n_d;
             P.st = dev_state(p);
+            P.commit = C;
+            P.do_commit = en == segs.size();
             const bool vec = build_step_params(p, segs, b, en, nullptr, P);
             const cudaError_t err = p->dtype16 == ZERO_BF16 ? launch_recast<ZERO_BF16>(p->device, P, vec, s)
                                                             : launch_recast<ZERO_FP16>(p->device, P, vec, s);
@@ -1241,16 +1274,11 @@ zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t*
         rerr = run(P, kMaxSegs);
     }
     if (rerr != cudaSuccess) return cuda_fail(rerr, "re-cast launch");
-    CommitParams C;
-    C.st = dev_state(p);
-    C.growth = p->scaler.growth_factor;
-    C.backoff = p->scaler.backoff_factor;
-    C.min_scale = p->scaler.min_scale;
-    C.interval = p->scaler.growth_interval;
-    C.dynamic = p->scaler_dynamic;
-    commit_kernel<<<1, 32, 0, s>>>(C);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    if (segs.empty()) {                      // nothing to re-cast: commit on its own
+        commit_kernel<<<1, 32, 0, s>>>(C);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    }
     p->in_step = false;
     p->stepped = true;
     p->norm_open = false;
