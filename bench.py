@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=4_194_304)
     ap.add_argument("--mem-budget-gb", type=float, default=160.0)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="enqueue the timed steps one by one instead of replaying them as one "
+                         "captured CUDA graph")
     ap.add_argument("--offload", action="store_true",
                     help="ZeRO-Offload: gradients reduced on the GPU into pinned host memory, AdamW "
                          "on the host CPU threads, 16-bit parameters copied back")
@@ -344,29 +347,57 @@ def gpu_arm(args, world, rank, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    def pairs(n):
-        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    def pairs(n, external=False):
+        kw = {"external": True} if external else {}
+        return [(torch.cuda.Event(enable_timing=True, **kw), torch.cuda.Event(enable_timing=True, **kw))
                 for _ in range(n)]
-    fused_pairs = pairs(args.steps * len(b.calls))
-    gather_pairs = pairs(args.steps * len(b.calls)) if w.stage == 3 else []
+    overlap = args.overlap and w.stage == 3
+    comm = torch.cuda.Stream() if overlap else None
+    # Timed region: the K steps captured as one CUDA graph (the host does all enqueueing at
+    # capture time), with timing events captured as graph nodes around every fused / gather
+    # launch; --no-graph (or a torch without graph timing events) enqueues them step by step.
+    # (offloaded steps synchronise with the host; a graph needs the bias table built by warm-up)
+    use_graph = not args.no_graph and not w.offload and args.warmup > 0
+    if use_graph:
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            use_graph = False
+    n_calls = args.steps * len(b.calls)
+    fused_pairs = pairs(n_calls, use_graph) if not overlap else []
+    gather_pairs = pairs(n_calls, use_graph) if (w.stage == 3 and not overlap) else []
     ev_fused, ev_gather = iter(fused_pairs), iter(gather_pairs)
     launches = 0
     skipped_before = b.g.step_state().skipped_total
+
+    def timed_steps():
+        nonlocal launches
+        for k in range(args.steps):
+            bufs = b.sets[(args.warmup + k) % b.n_sets]
+            if overlap:
+                _, n = b.step_overlapped(bufs, comm)
+            else:
+                _, n = b.step(bufs, ev_fused, ev_gather if w.stage == 3 else None)
+            launches += n
+
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                timed_steps()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record()
-    overlap = args.overlap and w.stage == 3
-    comm = torch.cuda.Stream() if overlap else None
-    for k in range(args.steps):
-        if overlap:
-            _, n = b.step_overlapped(b.sets[(args.warmup + k) % b.n_sets], comm)
-        else:
-            _, n = b.step(b.sets[(args.warmup + k) % b.n_sets], ev_fused,
-                          ev_gather if w.stage == 3 else None)
-        launches += n
+    if graph is not None:
+        graph.replay()
+    else:
+        timed_steps()
     t1.record()
     torch.cuda.synchronize()
     if dist:
@@ -376,8 +407,8 @@ def gpu_arm(args, world, rank, local):
     if dist:
         ms = max_over_ranks(ms, dist)
     skipped = b.g.step_state().skipped_total - skipped_before
-    fused_ms = [] if overlap else [a.elapsed_time(c) for a, c in fused_pairs]
-    gather_ms = [] if overlap else [a.elapsed_time(c) for a, c in gather_pairs]
+    fused_ms = [a.elapsed_time(c) for a, c in fused_pairs]
+    gather_ms = [a.elapsed_time(c) for a, c in gather_pairs]
 
     applied = args.steps - skipped
     elems = b.elems_per_step
@@ -413,7 +444,8 @@ def gpu_arm(args, world, rank, local):
                       "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
-                      "overlap": overlap, "per_param": w.per_param, "offload": w.offload,
+                      "overlap": overlap, "graph": graph is not None, "per_param": w.per_param,
+                      "offload": w.offload,
                       "offload_threads": b.g.offload_threads if w.offload else None},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,

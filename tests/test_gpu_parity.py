@@ -635,3 +635,56 @@ def test_tiny_case_sweep():
                 _compare_full(run, o, f"tiny case {trial} step {k}")
         finally:
             run.close()
+
+
+# ---------------------------------------------------------------------- CUDA graph capture
+
+@pytest.mark.parametrize("name", ["z2_nd8_fp16_buckets_inf", "z3_nd16_units"])
+def test_step_captured_in_a_cuda_graph(name):
+    """The step state lives on the device, so a whole step -- every bucket / unit's fused
+    launch, the re-cast and the commit -- can be captured once and replayed: replays with new
+    gradients written in place into the same buffers must follow the oracle step by step,
+    through a skipped step and the loss-scale back-off."""
+    w = dataclasses.replace(SMALL_CASES[name], steps=5)
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    ranges = run.ranges()
+    bufs = [[torch.empty(max(8, hi - lo), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+            for (_, lo, hi) in ranges]
+
+    def fill(k):
+        for (which, lo, hi), unit in zip(ranges, bufs):
+            for r in range(w.n_d):
+                H.fill_device(unit[r], synth.grad_stream(w, k, r), run.units, lo, hi)
+
+    def enqueue():
+        for (which, lo, hi), unit in zip(ranges, bufs):
+            run.g.step([b.data_ptr() for b in unit], which, run.hyper)
+        run.g.finish(wait=False)
+
+    try:
+        fill(1)
+        enqueue()                              # step 1 uncaptured: builds the bias table
+        o.step(1)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        fill(2)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                enqueue()                      # captured, not run
+        skips = 0
+        for k in range(2, w.steps + 1):
+            if k > 2:
+                fill(k)
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            skips += o.step(k)
+            st = run.g.step_state()
+            assert (st.t, st.scale, st.skipped_total) == (o.sc.t, o.sc.scale, skips)
+            _compare_full(run, o, f"graph replay {name} step {k}")
+    finally:
+        run.close()
