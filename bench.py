@@ -11,6 +11,7 @@ Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the sam
 from __future__ import annotations
 
 import argparse
+import importlib
 import json
 import os
 import statistics
@@ -25,6 +26,7 @@ sys.path.insert(0, ROOT)
 METRIC = "ZeRO step params updated/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "params/s"
 DEFAULT_CONFIG = 1
+DEFAULT_STAGING = "ldg"
 FALLBACK_HBM_GBS = 6800.0
 # Gradient sets rotated through the timed steps.  A backward pass rewrites the same gradient
 # buffers every step, so a few persistent sets model training; each step still reads inputs
@@ -32,17 +34,17 @@ FALLBACK_HBM_GBS = 6800.0
 # through tens of GB of distinct sets instead measures GPU TLB reach, not the step.)
 ROTATE_SETS = 4
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the fused kernel from
-# one ncu capture, per workload, valid only for the kernel source it was taken on (first 16 hex
-# digits of the SHA-256 of zero_step.cu); reported as null once that source changes.
-# Capture: profiles/fused_step_zero2_ragged_nd7_ncu_full.md.
-MEASURED_TRAFFIC = {1: ("a3994173384ce9b3", 2_304_368_576)}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the step kernel from
+# one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
+# (first 16 hex digits of the SHA-256 of zero_step.cu); reported as null once that source
+# changes.  Captures: profiles/*_ncu_full.md.
+MEASURED_TRAFFIC = {}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_step.cu")
 
 
-def measured_traffic(config: int):
+def measured_traffic(config: int, kernel: str):
     import hashlib
-    rec = MEASURED_TRAFFIC.get(config)
+    rec = MEASURED_TRAFFIC.get((config, kernel))
     if rec is None:
         return None
     with open(KERNEL_SOURCE, "rb") as f:
@@ -72,6 +74,11 @@ def parse_args():
     ap.add_argument("--overlap", action="store_true",
                     help="stage 3: gather unit u+1 on a second stream while unit u steps "
                          "(zero_step_units_overlapped); no per-launch events in this mode")
+    ap.add_argument("--staging", choices=["ldg", "bulk"], default=DEFAULT_STAGING,
+                    help="ldg: 128-bit register loads; bulk: cp.async.bulk (TMA) staging of the "
+                         "contribution and state tiles into shared memory")
+    ap.add_argument("--bulk-tile", type=int, default=0, help="bulk staging: elements per tile")
+    ap.add_argument("--bulk-stages", type=int, default=0, help="bulk staging: ring depth")
     ap.add_argument("--grad-norm", choices=["off", "report", "clip"], default="off",
                     help="report: global gradient norm inside the fused pass; clip: norm pre-pass "
                          "over every bucket/unit, then the update clipped at max norm 1.0")
@@ -167,7 +174,8 @@ class ClockSampler:
 class Bench:
     """A workload bound to the product API with pre-generated contribution sets."""
 
-    def __init__(self, w, mem_budget_gb: float, n_sets_wanted: int, grad_norm: str = "off"):
+    def __init__(self, w, mem_budget_gb: float, n_sets_wanted: int, grad_norm: str = "off",
+                 options=None):
         import torch
         import synth
         from zero_sharded_mixed_03_gb300.emulate import EmulatedGroup
@@ -177,7 +185,8 @@ class Bench:
 
         self.torch, self.Z, self.H, self.synth = torch, Z, H, synth
         self.w = w
-        self.run = H.Run(w, alloc_contribs=False)   # plan, state, 16-bit buffers, initial params
+        # plan, state, 16-bit buffers, initial params
+        self.run = H.Run(w, alloc_contribs=False, options=options)
         self.g = self.run.g
         self.units = self.run.units
         self.info = self.run.info
@@ -335,7 +344,13 @@ def gpu_arm(args, world, rank, local):
     if args.offload:
         import dataclasses
         w = dataclasses.replace(w, offload=True)
-    b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm)
+    Z = importlib.import_module("zero_sharded_mixed_03_gb300")
+    options = {}
+    if args.staging == "bulk":
+        options = {Z.ZERO_OPT_STAGING: 1, Z.ZERO_OPT_BULK_TILE: args.bulk_tile,
+                   Z.ZERO_OPT_BULK_STAGES: args.bulk_stages}
+    b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm,
+              options)
     peak, peak_kind = peaks()
 
     for k in range(args.warmup):
@@ -423,9 +438,10 @@ def gpu_arm(args, world, rank, local):
     launch_bytes = per_launch_elems * b.bytes_per_elem
     avg_fused_s = statistics.mean(fused_ms) / 1e3 if fused_ms else float("nan")
     achieved = launch_bytes / avg_fused_s / 1e9
+    kernel = "bulk_step_kernel" if args.staging == "bulk" else "fused_step_kernel"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config),
-                "peak_source": peak_kind, "kernel": "fused_step_kernel",
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config, kernel),
+                "peak_source": peak_kind, "kernel": kernel,
                 "launch_bytes": int(launch_bytes), "avg_launch_us": round(avg_fused_s * 1e6, 2),
                 "launches_timed": len(fused_ms)}
     if not fused_ms or w.offload:                   # overlapped / offloaded: no fused kernel
@@ -445,7 +461,7 @@ def gpu_arm(args, world, rank, local):
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
                       "overlap": overlap, "graph": graph is not None, "per_param": w.per_param,
-                      "offload": w.offload,
+                      "offload": w.offload, "staging": args.staging,
                       "offload_threads": b.g.offload_threads if w.offload else None},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,

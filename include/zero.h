@@ -36,7 +36,9 @@
  *    every stream of a launch has the same element phase modulo 8 (always true
  *    for the state layout below when bucket_elems is a multiple of 8); other
  *    launches use the scalar path of the same kernel.
- *  - Kernels never trap or assert; they contain no waits.
+ *  - Kernels never trap or assert.  The only waits are those of the bulk-staged step kernel
+ *    (zero_set_option, ZERO_OPT_STAGING = 1) on its shared-memory barriers; each is bounded
+ *    in time (ZERO_OPT_WAIT_LIMIT_NS) and one that runs out is reported as ZERO_ETIMEOUT.
  */
 #ifndef ZERO_H
 #define ZERO_H
@@ -53,7 +55,8 @@ typedef enum {
     ZERO_EALIGN = 2,  /* a pointer is not aligned to its element size */
     ZERO_ECUDA = 3,   /* a CUDA runtime call failed */
     ZERO_ESTATE = 4,  /* call out of order (e.g. finish before every bucket was stepped) */
-    ZERO_ERANGE = 5   /* a size beyond a documented limit */
+    ZERO_ERANGE = 5,  /* a size beyond a documented limit */
+    ZERO_ETIMEOUT = 6 /* a bounded wait inside a kernel ran out; the step was discarded */
 } zero_status_t;
 
 enum { ZERO_BF16 = 0, ZERO_FP16 = 1 };
@@ -254,8 +257,37 @@ zero_status_t zero_grad_norm(zero_plan_t* plan, const void* const* grad_contribs
  * enqueues this work; with out != NULL it also synchronises `stream` and reads the state. */
 zero_status_t zero_step_finish(zero_plan_t* plan, void* stream, zero_step_result_t* out);
 
-/* Read the device-resident step state (synchronises `stream`). */
+/* Read the device-resident step state (synchronises `stream`).  zero_read_state and
+ * zero_step_finish (out != NULL) return ZERO_ETIMEOUT, with *out filled, when a wait of the
+ * bulk-staged kernel ran out since the state was last read: every step finished since then
+ * was discarded (state, t, loss scale and counters unchanged; 16-bit parameters rewritten
+ * from the current master).  Reading the state clears the condition. */
 zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_t* out);
+
+/* Execution options of a plan (not inside an open step; values are checked here):
+ *   ZERO_OPT_STAGING        0 (default): the fused step loads the contribution slices and the
+ *                           fp32 state with 128-bit register loads.  1: a producer warp stages
+ *                           them tile by tile into a ring of shared-memory buffers with 1-D
+ *                           cp.async.bulk copies (the TMA engine) completing on mbarriers, and
+ *                           four consumer warps reduce and update from shared memory.  Both
+ *                           give identical results, bit for bit.  Launches whose streams do not
+ *                           share one 16-byte phase use the scalar path either way.
+ *   ZERO_OPT_WAIT_LIMIT_NS  bound on each barrier wait of the bulk-staged kernel, in ns of
+ *                           %globaltimer (default 1e9; 0 gives up at the first wait that does
+ *                           not succeed at once).  A wait that runs out sets the plan's error
+ *                           word, its block drains its own copies in flight and returns.
+ *   ZERO_OPT_BULK_TILE      elements per staged tile, a multiple of 8 in [8, 8192]; 0 (default):
+ *                           the largest power of two up to 2048 with tile * (2 N_d + 12) bytes
+ *                           within 56 KB.
+ *   ZERO_OPT_BULK_STAGES    ring depth in [2, 16]; 0 (default): 2 (two blocks per SM).
+ * A tile/stage pair whose ring does not fit one block's shared memory gives ZERO_ERANGE. */
+enum {
+    ZERO_OPT_STAGING = 0,
+    ZERO_OPT_WAIT_LIMIT_NS = 1,
+    ZERO_OPT_BULK_TILE = 2,
+    ZERO_OPT_BULK_STAGES = 3
+};
+zero_status_t zero_set_option(zero_plan_t* plan, int option, int64_t value);
 
 /* Overwrite the device-resident step state, e.g. when resuming from a checkpoint whose fp32
  * master/m/v were saved from the half `in->current` after `in->t` applied steps.  Clears the

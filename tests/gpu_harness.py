@@ -60,12 +60,16 @@ def values_at(stream: synth.Stream, units, idx: np.ndarray) -> np.ndarray:
 class Run:
     """One workload on the GPU through the product API."""
 
-    def __init__(self, w: W.Workload, bound=None, peers: bool = True, alloc_contribs: bool = True):
+    def __init__(self, w: W.Workload, bound=None, peers: bool = True, alloc_contribs: bool = True,
+                 options=None):
+        """options: {ZERO_OPT_*: value} applied with zero_set_option (e.g. bulk staging)."""
         self.w = w
         b = bound if bound is not None else w.ranks()
         self.g = EmulatedGroup(w.sizes, w.n_d, w.stage, w.bucket_elems, w.unit_first or None,
                                w.dtype, b, dim0=w.dim0 if w.per_param else None,
                                offload=w.offload)
+        for opt, val in (options or {}).items():
+            self.g.set_option(opt, val)
         self.units = self.g.units
         self.info = self.g.info
         self.bound = list(b)

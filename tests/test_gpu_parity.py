@@ -76,8 +76,8 @@ def _compare_full(run: H.Run, o: H.OracleFull, label: str):
     return mism
 
 
-def _run_full(w: W.Workload):
-    run = H.Run(w)
+def _run_full(w: W.Workload, options=None):
+    run = H.Run(w, options=options)
     o = H.OracleFull(w, run.bound)
     mism = 0
     try:
@@ -109,8 +109,8 @@ def test_config0_full_parity():
     print(f"configs[0]: {mism} bit mismatches (within tolerance)")
 
 
-def _run_sampled(w: W.Workload, bound=None, n_random=20000):
-    run = H.Run(w, bound=bound)
+def _run_sampled(w: W.Workload, bound=None, n_random=20000, options=None):
+    run = H.Run(w, bound=bound, options=options)
     try:
         idx = H.sample_indices(run, n_random)
         o = H.OracleSampled(w, idx)
@@ -374,10 +374,9 @@ CLIP_CASES = {
 }
 
 
-@pytest.mark.parametrize("name", list(CLIP_CASES))
-def test_norm_and_clipping_full_parity(name):
+def _run_clip(name, options=None):
     w = CLIP_CASES[name]
-    run = H.Run(w)
+    run = H.Run(w, options=options)
     o = H.OracleFull(w, run.bound)
     try:
         for k in range(1, w.steps + 1):
@@ -392,6 +391,11 @@ def test_norm_and_clipping_full_parity(name):
             _compare_full(run, o, f"{name} step {k}")
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("name", list(CLIP_CASES))
+def test_norm_and_clipping_full_parity(name):
+    _run_clip(name)
 
 
 def test_report_only_leaves_the_update_unchanged():
@@ -686,5 +690,97 @@ def test_step_captured_in_a_cuda_graph(name):
             st = run.g.step_state()
             assert (st.t, st.scale, st.skipped_total) == (o.sc.t, o.sc.scale, skips)
             _compare_full(run, o, f"graph replay {name} step {k}")
+    finally:
+        run.close()
+
+
+# ---------------------------------------------------------------------- bulk (TMA) staging
+
+BULK = {Z.ZERO_OPT_STAGING: 1}
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_bulk_staging_small_case_full_parity(name):
+    _run_full(SMALL_CASES[name], options=BULK)
+
+
+def test_bulk_staging_config0_full_parity():
+    mism = _run_full(W.workload(0), options=BULK)
+    print(f"configs[0], bulk staging: {mism} bit mismatches (within tolerance)")
+
+
+@pytest.mark.parametrize("i", [1, 3])
+def test_bulk_staging_config_sampled(i):
+    n, mism = _run_sampled(W.workload(i), options=BULK)
+    print(f"configs[{i}], bulk staging: {n} sampled elements, {mism} bit mismatches")
+
+
+@pytest.mark.parametrize("name", list(CLIP_CASES))
+def test_bulk_staging_norm_and_clipping(name):
+    _run_clip(name, options=BULK)
+
+
+@pytest.mark.parametrize("name,tile,stages", [
+    ("z2_nd7_ragged_tensors", 8, 2), ("z2_nd7_ragged_tensors", 64, 16),
+    ("z2_nd8_fp16_buckets_inf", 1024, 3), ("z3_nd16_units", 512, 2),
+    ("z1_nd4_tiles_ragged_tail", 4096, 2), ("z1_nd1", 8192, 2)])
+def test_bulk_staging_geometries(name, tile, stages):
+    """Tiles from one 8-element vector to 8192 elements and rings of 2 to 16 buffers, over
+    ragged tensors, buckets and units (segments shorter than a tile, tiles cut at segment
+    ends, one tile larger than the whole model)."""
+    _run_full(SMALL_CASES[name], options={Z.ZERO_OPT_STAGING: 1, Z.ZERO_OPT_BULK_TILE: tile,
+                                          Z.ZERO_OPT_BULK_STAGES: stages})
+
+
+def test_bulk_staging_is_bit_identical_to_register_loads():
+    w = dataclasses.replace(SMALL_CASES["z2_nd8_fp16_buckets_inf"], steps=4)
+    a, b = H.Run(w), H.Run(w, options=BULK)
+    try:
+        for k in range(1, w.steps + 1):
+            ra, rb = a.step(k), b.step(k)
+            assert (ra.skipped, ra.t, ra.scale) == (rb.skipped, rb.t, rb.scale)
+            for r in a.bound:
+                x, y = a.read_logical(r), b.read_logical(r)
+                for key in x:
+                    assert np.array_equal(x[key].view(np.uint32), y[key].view(np.uint32)), (k, r, key)
+            assert torch.equal(a.g.full16, b.g.full16), k
+    finally:
+        a.close()
+        b.close()
+
+
+def test_bulk_staging_wait_limit_runs_out_and_the_step_is_discarded():
+    """A wait limit of 0 makes the first barrier wait that is not already satisfied give up:
+    the kernel records it, drains its copies and returns; zero_step_finish reports
+    ZERO_ETIMEOUT, the step is discarded (state bits, t, scale and counters unchanged, 16-bit
+    parameters rewritten from the unchanged master), and the next step runs normally."""
+    w = _mk(170, [4_000_000 + 13], 4, 1, steps=2)
+    run = H.Run(w, options=BULK)
+    o = H.OracleFull(w, run.bound)
+    try:
+        res = run.step(1)
+        o.step(1)
+        assert res.t == 1
+        _compare_full(run, o, "before the timeout")
+        before = {r: run.read_logical(r) for r in run.bound}
+        f16 = run.g.full16.clone()
+        run.g.set_option(Z.ZERO_OPT_WAIT_LIMIT_NS, 0)
+        with pytest.raises(Z.ZeroError) as e:
+            run.step(2)
+        assert e.value.status == Z.ZERO_ETIMEOUT
+        st = e.value.result
+        assert (st.t, st.finished, st.skipped_total, st.skipped) == (1, 1, 0, 1)
+        for r in run.bound:
+            now = run.read_logical(r)
+            for key in now:
+                assert np.array_equal(now[key].view(np.uint32), before[r][key].view(np.uint32)), key
+        assert torch.equal(run.g.full16, f16)
+        run.g.set_option(Z.ZERO_OPT_WAIT_LIMIT_NS, 1_000_000_000)
+        st = run.g.step_state()                 # the report cleared the condition
+        assert (st.t, st.finished) == (1, 1)
+        res = run.step(2)
+        o.step(2)
+        assert (res.t, res.finished, res.skipped) == (2, 2, 0)
+        _compare_full(run, o, "after the timeout")
     finally:
         run.close()

@@ -167,6 +167,46 @@ def test_calls_out_of_order_fail_without_touching_the_gpu():
         Z.zero_plan_destroy(plan)
 
 
+def test_execution_options_are_checked_on_the_host():
+    """zero_set_option: values outside their ranges give EINVAL; a staging ring (stages x tile x
+    (2 N_d + 12) bytes + 256 bytes of barriers) beyond one block's 227 KB of shared memory gives
+    ERANGE and leaves the earlier geometry in place."""
+    plan = _plan_for([10, 20], 7, 2, 8)
+    try:
+        for opt, val in ((Z.ZERO_OPT_STAGING, 2), (Z.ZERO_OPT_STAGING, -1),
+                         (Z.ZERO_OPT_WAIT_LIMIT_NS, -1), (Z.ZERO_OPT_BULK_TILE, 12),
+                         (Z.ZERO_OPT_BULK_TILE, 16384), (Z.ZERO_OPT_BULK_TILE, 4),
+                         (Z.ZERO_OPT_BULK_STAGES, 1), (Z.ZERO_OPT_BULK_STAGES, 17), (9, 0)):
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_set_option(plan, opt, val)
+            assert e.value.status == Z.ZERO_EINVAL, (opt, val)
+        for opt, val in ((Z.ZERO_OPT_STAGING, 1), (Z.ZERO_OPT_STAGING, 0),
+                         (Z.ZERO_OPT_WAIT_LIMIT_NS, 0), (Z.ZERO_OPT_BULK_TILE, 4096),
+                         (Z.ZERO_OPT_BULK_TILE, 1024), (Z.ZERO_OPT_BULK_STAGES, 8)):
+            Z.zero_set_option(plan, opt, val)
+        # 1024 x 26 B = 26 KB per buffer: 8 fit, 16 do not
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_set_option(plan, Z.ZERO_OPT_BULK_STAGES, 16)
+        assert e.value.status == Z.ZERO_ERANGE
+        # 8192 x 26 B = 208 KB per buffer: two do not fit
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_set_option(plan, Z.ZERO_OPT_BULK_TILE, 8192)
+        assert e.value.status == Z.ZERO_ERANGE
+        Z.zero_set_option(plan, Z.ZERO_OPT_BULK_STAGES, 0)     # automatic: 2 buffers of 104 KB
+        Z.zero_set_option(plan, Z.ZERO_OPT_BULK_TILE, 4096)
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_set_option(plan, Z.ZERO_OPT_BULK_STAGES, 3)
+        assert e.value.status == Z.ZERO_ERANGE
+    finally:
+        Z.zero_plan_destroy(plan)
+    plan = _plan_for([10], 1, 1)
+    try:                                     # N_d = 1: 8192 x 14 B x 2 + 256 B fit in 227 KB
+        Z.zero_set_option(plan, Z.ZERO_OPT_BULK_TILE, 8192)
+        Z.zero_set_option(plan, Z.ZERO_OPT_BULK_STAGES, 2)
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
 def test_empty_model_plan():
     plan = _plan_for([], 4, 2, 0)
     info = Z.zero_plan_info(plan)

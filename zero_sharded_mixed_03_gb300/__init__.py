@@ -15,30 +15,32 @@ from typing import Optional, Sequence
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libzero.so")
 
-ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ESTATE, ZERO_ERANGE = range(6)
+ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ESTATE, ZERO_ERANGE, ZERO_ETIMEOUT = range(7)
 ZERO_BF16, ZERO_FP16 = 0, 1
 ZERO_MAX_RANKS = 128
 ZERO_REPORT_GRAD_NORM = 1
+ZERO_OPT_STAGING, ZERO_OPT_WAIT_LIMIT_NS, ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES = range(4)
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)
 TABLE_COLS = {0: 1, 1: 7, 2: 6, 3: 5, 4: 4, 5: 10}
 STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_EALIGN", 3: "ZERO_ECUDA",
-                4: "ZERO_ESTATE", 5: "ZERO_ERANGE"}
+                4: "ZERO_ESTATE", 5: "ZERO_ERANGE", 6: "ZERO_ETIMEOUT"}
 
 EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", "zero_rank_state_elems", "zero_plan_tables",
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",
             "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_set_scaler",
             "zero_read_state", "zero_restore_state", "zero_grad_norm",
             "zero_step_units_overlapped", "zero_bind_offload", "zero_offload_step",
-            "zero_offload_finish",
+            "zero_offload_finish", "zero_set_option",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
 
 class ZeroError(RuntimeError):
-    def __init__(self, status: int, msg: str):
+    def __init__(self, status: int, msg: str, result=None):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
         self.status = status
+        self.result = result   # the step state read with a ZERO_ETIMEOUT report
 
 
 class zero_hyper_t(ctypes.Structure):
@@ -135,6 +137,8 @@ def lib() -> ctypes.CDLL:
         L.zero_offload_finish.argtypes = [_vp, _int, _vp, ctypes.POINTER(zero_step_result_t)]
         L.zero_grad_norm.restype = st
         L.zero_grad_norm.argtypes = [_vp, _vp, _i64, _i64, _vp]
+        L.zero_set_option.restype = st
+        L.zero_set_option.argtypes = [_vp, _int, _i64]
         L.zero_restore_state.restype = st
         L.zero_restore_state.argtypes = [_vp, ctypes.POINTER(zero_step_result_t), _vp]
         L.zero_gather_layer.restype = st
@@ -157,10 +161,10 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def _check(status: int) -> None:
+def _check(status: int, result=None) -> None:
     if status != ZERO_OK:
         msg = lib().zero_last_error()
-        raise ZeroError(status, msg.decode() if msg else "")
+        raise ZeroError(status, msg.decode() if msg else "", result)
 
 
 def _ptr_array(ptrs: Sequence[Optional[int]]):
@@ -288,7 +292,7 @@ def zero_step_finish(plan: int, stream: int = 0, wait: bool = True) -> Optional[
     """Enqueue the commit; with wait=True also read back the step state (synchronises)."""
     res = zero_step_result_t() if wait else None
     _check(lib().zero_step_finish(plan, stream or None,
-                                  ctypes.byref(res) if res is not None else None))
+                                  ctypes.byref(res) if res is not None else None), res)
     return res
 
 
@@ -298,8 +302,14 @@ def zero_restore_state(plan: int, state: zero_step_result_t, stream: int = 0) ->
 
 def zero_read_state(plan: int, stream: int = 0) -> zero_step_result_t:
     res = zero_step_result_t()
-    _check(lib().zero_read_state(plan, stream or None, ctypes.byref(res)))
+    _check(lib().zero_read_state(plan, stream or None, ctypes.byref(res)), res)
     return res
+
+
+def zero_set_option(plan: int, option: int, value: int) -> None:
+    """ZERO_OPT_STAGING (0 register loads, 1 cp.async.bulk staging), ZERO_OPT_WAIT_LIMIT_NS,
+    ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES (0 = chosen from N_d)."""
+    _check(lib().zero_set_option(plan, option, int(value)))
 
 
 def zero_gather_layer(plan: int, unit: int, full_unit16: int, stream: int = 0) -> None:

@@ -39,8 +39,9 @@ constexpr int kRankBatch = 4;
 
 // ------------------------------------------------------------------ device-resident step state
 
-// First 64 bytes of the workspace.  Written only by commit_kernel (and by the host before
-// the first step); read by the step and re-cast kernels of the following step.
+// First 96 bytes of the workspace.  Written by the commit (the last re-cast block or
+// commit_kernel), by the host before the first step, and by the kernels' atomics (flag,
+// error, norm tickets); read by the step and re-cast kernels of the following step.
 struct DevState {
     uint32_t flag;          // OR of the non-finite flags of the open step
     uint32_t cur;           // current half of every ping-pong pair
@@ -55,7 +56,10 @@ struct DevState {
     double last_norm2;      // last finished step's sum
     uint32_t norm_valid;    // open step computed a norm
     uint32_t last_norm_valid;
-    int64_t pad[2];
+    uint32_t error;         // bit 0: a barrier wait ran out; bit 1: a drain ran out (sticky
+                            // until read; every step finished meanwhile is discarded)
+    uint32_t pad32;
+    int64_t pad;
 };
 static_assert(sizeof(DevState) == 96, "DevState layout");
 
@@ -103,6 +107,11 @@ struct StepParamsT {
     double* partials;          // norm modes: one slot per block
     CommitParams commit;       // re-cast launch that also closes the step
     int32_t do_commit;
+    // bulk-staged kernel: tile geometry and the bound on each barrier wait
+    int32_t tile;              // body elements per tile (a multiple of 8)
+    int32_t stages;            // ring depth
+    int64_t n_tiles;           // tiles over all segments of the launch
+    uint64_t wait_ns;
 };
 // The usual parameter block (4 KB), and a wide one (26 KB, under the 32 KB kernel-parameter
 // limit) for calls with many work items, e.g. per-parameter plans (one item per tensor chunk).
@@ -346,8 +355,9 @@ __device__ __forceinline__ bool step_vec8(const PT& P, const KSeg& S, int64_t e,
     return bad;
 }
 
-// Sum of one double over the block in a fixed pattern (shuffle tree per warp, warps in order);
-// the result is valid in thread 0.
+// Sum of one double over a block of NT threads in a fixed pattern (shuffle tree per warp,
+// warps in order); the result is valid in thread 0.
+template <int NT>
 __device__ __forceinline__ double block_sum_fixed(double x, double* warp_sum)
 {
 #pragma unroll
@@ -356,7 +366,7 @@ __device__ __forceinline__ double block_sum_fixed(double x, double* warp_sum)
     __syncthreads();
     double b = 0.0;
     if (threadIdx.x == 0)
-        for (int w = 0; w < kThreads / 32; ++w) b += warp_sum[w];
+        for (int w = 0; w < NT / 32; ++w) b += warp_sum[w];
     __syncthreads();
     return b;
 }
@@ -365,12 +375,12 @@ __device__ __forceinline__ double block_sum_fixed(double x, double* warp_sum)
 // the launch to store (an atomic ticket, nothing waits) adds all slots to the step's norm in a
 // fixed order (thread t takes slots t, t + 128, ...; then the fixed block pattern), so the sum
 // does not depend on which blocks finish first.
-template <typename PT>
+template <int NT, typename PT>
 __device__ __forceinline__ void block_norm_commit(const PT& P, double part)
 {
-    __shared__ double warp_sum[kThreads / 32];
+    __shared__ double warp_sum[NT / 32];
     __shared__ bool last;
-    const double b = block_sum_fixed(part, warp_sum);
+    const double b = block_sum_fixed<NT>(part, warp_sum);
     if (threadIdx.x == 0) {
         P.partials[blockIdx.x] = b;
         __threadfence();
@@ -382,8 +392,8 @@ __device__ __forceinline__ void block_norm_commit(const PT& P, double part)
     __threadfence();
     const volatile double* slots = P.partials;
     double x = 0.0;
-    for (unsigned i = threadIdx.x; i < gridDim.x; i += kThreads) x += slots[i];
-    const double sum = block_sum_fixed(x, warp_sum);
+    for (unsigned i = threadIdx.x; i < gridDim.x; i += NT) x += slots[i];
+    const double sum = block_sum_fixed<NT>(x, warp_sum);
     if (threadIdx.x == 0) {
         volatile DevState* st = P.st;
         st->norm2 = st->norm2 + sum;
@@ -433,7 +443,278 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
 
     // Global non-finite flag: one OR across the block, one atomic per block that saw one.
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(P.flag, 1u);
-    if constexpr (MODE == kNormAcc) block_norm_commit(P, norm2.value());
+    if constexpr (MODE == kNormAcc) block_norm_commit<kThreads>(P, norm2.value());
+}
+
+// ------------------------------------------------------------------ bulk-staged step kernel
+
+// The same step with its HBM reads staged through shared memory by the TMA engine.  Warp
+// kBulkConsumers (one lane) is the producer: per tile it issues 1-D cp.async.bulk copies of
+// the N_d contribution slices and of the master/m/v slices into the next buffer of a ring,
+// all completing on that buffer's "full" mbarrier.  The consumer warps wait on it, reduce and
+// update from shared memory (quads of 4 elements: 64-bit and 128-bit shared loads without
+// bank conflicts), store the new state and the 16-bit cast straight to HBM, and release the
+// buffer on its "empty" mbarrier.  Every wait is bounded (P.wait_ns of %globaltimer and an
+// iteration cap); one that runs out sets DevState::error and ends that warp's loop, and the
+// producer waits (bounded again) for every copy it issued before the block returns.
+constexpr int kBulkConsumers = 8;                        // consumer warps
+constexpr int kBulkThreads = 32 * (kBulkConsumers + 1);  // + the producer warp
+constexpr int kBulkBarrierBytes = 256;                   // full[16] + empty[16] mbarriers
+constexpr int kBulkMaxStages = 16;
+constexpr int kBulkMaxTile = 8192;
+constexpr uint64_t kDrainNs = 2000000000ull;             // bound on the final drain
+constexpr uint32_t kWaitIterCap = 1u << 26;              // polls per wait, whatever the clock
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking probe of the same condition.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase of parity `parity` of barrier `bar` has completed.  False when
+// limit_ns of %globaltimer (or kWaitIterCap polls) pass first; limit 0 gives up as soon as
+// the first, non-blocking probe fails.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < kWaitIterCap; ++i) {
+        if (global_ns() - t0 >= limit_ns) return false;
+        if (mbar_try(bar, parity)) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared of `bytes` (both addresses 16-byte aligned, bytes a multiple
+// of 16), completing on barrier `bar`; every byte is read once, so L2 evicts it first.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Launch tile `tile` (tiles increase along a thread's loop): segment s, first body element
+// e0 and length (a multiple of 8).  s and base (first tile of segment s) carry the walk.
+struct TileRef {
+    int64_t e0;
+    int32_t len;
+};
+
+template <typename PT>
+__device__ __forceinline__ TileRef locate_tile(const PT& P, int64_t tile, int& s, int64_t& base)
+{
+    for (;;) {
+        const int64_t nt = (8 * P.seg[s].nvec + P.tile - 1) / P.tile;
+        if (tile < base + nt) break;
+        base += nt;
+        ++s;
+    }
+    const KSeg& S = P.seg[s];
+    const int64_t off = (tile - base) * P.tile;
+    TileRef r;
+    r.e0 = S.head + off;
+    r.len = (int32_t)min((int64_t)P.tile, 8 * S.nvec - off);
+    return r;
+}
+
+// Four consecutive elements e .. e+3 (quad q of the tile in buffer `buf`).
+template <int DT, int MODE, typename PT>
+__device__ __forceinline__ bool step_quad_staged(const PT& P, const KSeg& S, const unsigned char* buf,
+                                                 int64_t e, int q, const StepK& sk, int cur,
+                                                 NormAcc& norm2)
+{
+    const int tile = P.tile;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const unsigned char* c = buf + 8 * q;
+#pragma unroll 4
+    for (int r = 0; r < P.n_d; ++r) {
+        const uint2 w = *reinterpret_cast<const uint2*>(c + (size_t)r * tile * 2);
+        float a, b, d, f;
+        widen2<DT>(w.x, a, b);
+        widen2<DT>(w.y, d, f);
+        acc[0] = __fadd_rn(acc[0], a);
+        acc[1] = __fadd_rn(acc[1], b);
+        acc[2] = __fadd_rn(acc[2], d);
+        acc[3] = __fadd_rn(acc[3], f);
+    }
+    const unsigned char* sb = buf + (size_t)P.n_d * tile * 2 + 16 * q;
+    const float4 p4 = *reinterpret_cast<const float4*>(sb);
+    const float4 m4 = *reinterpret_cast<const float4*>(sb + (size_t)tile * 4);
+    const float4 v4 = *reinterpret_cast<const float4*>(sb + (size_t)tile * 8);
+    float p[4] = {p4.x, p4.y, p4.z, p4.w};
+    float m[4] = {m4.x, m4.y, m4.z, m4.w};
+    float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float g = __fmul_rn(acc[j], sk.inv);
+        bad |= nonfinite(g);
+        if constexpr (MODE == kNormAcc) norm2.add(__fmul_rn(g, g));
+        const float gu = MODE == kClip ? __fmul_rn(g, sk.coef) : g;
+        adamw1(gu, p[j], m[j], v[j], P.k, sk);
+    }
+    __stcs(reinterpret_cast<float4*>(S.p[cur ^ 1] + e), make_float4(p[0], p[1], p[2], p[3]));
+    __stcs(reinterpret_cast<float4*>(S.m[cur ^ 1] + e), make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(reinterpret_cast<float4*>(S.v[cur ^ 1] + e), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<uint2*>(S.out16 + e), make_uint2(narrow2<DT>(p[0], p[1]), narrow2<DT>(p[2], p[3])));
+    return bad;
+}
+
+// Persistent: block b takes tiles b, b + grid, ...; its k-th tile uses buffer k % stages.
+// Dynamic shared memory (from a 128-byte boundary): kBulkBarrierBytes of mbarriers, then
+// `stages` buffers of tile * (2 N_d + 12) bytes: N_d contribution slices (tile * 2 bytes
+// each), master, m, v.
+template <int DT, int MODE, typename PT>
+__global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_constant__ PT P)
+{
+    extern __shared__ __align__(128) unsigned char bulk_raw[];
+    __shared__ float sk4[4];
+    __shared__ int scur;
+    // 128-byte aligned start whatever the static shared memory before it (launches add 128 B)
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(bulk_raw);
+    const uint32_t full0 = (raw + 127u) & ~127u;
+    const unsigned char* bulk_smem = bulk_raw + (full0 - raw);
+    const uint32_t empty0 = full0 + 8u * kBulkMaxStages;
+    const uint32_t stage_bytes = (uint32_t)P.tile * (2u * (uint32_t)P.n_d + 12u);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P.stages; ++i) {
+            mbar_init(full0 + 8u * i, 1);
+            mbar_init(empty0 + 8u * i, kBulkConsumers);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    block_constants(P, sk4, &scur);   // ends with __syncthreads: the barriers are ready
+    const StepK sk = {sk4[0], sk4[1], sk4[2], sk4[3]};
+    const int cur = scur;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    bool bad = false;
+    uint32_t err = 0;
+    NormAcc norm2;
+
+    if (warp < kBulkConsumers) {
+        const int ct = threadIdx.x;
+        constexpr int kCT = 32 * kBulkConsumers;
+        // unaligned heads and tails: plain loads
+        for (int64_t q = (int64_t)blockIdx.x * kCT + ct; q < (int64_t)P.n_seg * kScalarSlots;
+             q += (int64_t)gridDim.x * kCT) {
+            const KSeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) bad |= step_scalar<DT, MODE>(P, S, e, sk, cur, norm2);
+        }
+        int s = 0;
+        int64_t base = 0;
+        uint32_t k = 0;
+        for (int64_t tile = blockIdx.x; tile < P.n_tiles; tile += gridDim.x, ++k) {
+            const TileRef T = locate_tile(P, tile, s, base);
+            const uint32_t st = k % (uint32_t)P.stages;
+            const bool ok = mbar_wait(full0 + 8u * st, (k / (uint32_t)P.stages) & 1u, P.wait_ns);
+            if (__any_sync(0xFFFFFFFFu, !ok)) {
+                err |= 1u;
+                break;
+            }
+            const KSeg& S = P.seg[s];
+            const unsigned char* buf = bulk_smem + kBulkBarrierBytes + (size_t)st * stage_bytes;
+            for (int q = ct; q < T.len / 4; q += kCT)
+                bad |= step_quad_staged<DT, MODE>(P, S, buf, T.e0 + 4 * q, q, sk, cur, norm2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8u * st);
+        }
+    } else if (lane == 0) {
+        const uint64_t policy = evict_first_policy();
+        const uint32_t ring0 = full0 + kBulkBarrierBytes;
+        const uint32_t cbytes = (uint32_t)P.tile * 2u, sbytes = (uint32_t)P.tile * 4u;
+        int s = 0;
+        int64_t base = 0;
+        uint32_t k = 0;   // tiles issued
+        for (int64_t tile = blockIdx.x; tile < P.n_tiles; tile += gridDim.x, ++k) {
+            const TileRef T = locate_tile(P, tile, s, base);
+            const uint32_t st = k % (uint32_t)P.stages;
+            if (k >= (uint32_t)P.stages &&
+                !mbar_wait(empty0 + 8u * st, ((k / (uint32_t)P.stages) - 1u) & 1u, P.wait_ns)) {
+                err |= 1u;
+                break;
+            }
+            const KSeg& S = P.seg[s];
+            const uint32_t full = full0 + 8u * st;
+            const uint32_t dst = ring0 + st * stage_bytes;
+            const uint32_t len = (uint32_t)T.len;
+            mbar_arrive_expect_tx(full, len * (2u * (uint32_t)P.n_d + 12u));
+            for (int r = 0; r < P.n_d; ++r)
+                bulk_load(dst + (uint32_t)r * cbytes, P.c[r] + S.c_off + T.e0, 2u * len, full, policy);
+            const uint32_t sdst = dst + (uint32_t)P.n_d * cbytes;
+            bulk_load(sdst, S.p[cur] + T.e0, 4u * len, full, policy);
+            bulk_load(sdst + sbytes, S.m[cur] + T.e0, 4u * len, full, policy);
+            bulk_load(sdst + 2u * sbytes, S.v[cur] + T.e0, 4u * len, full, policy);
+        }
+        // Drain: the last phase issued on each buffer completes before the block returns.
+        const uint32_t ns = (uint32_t)P.stages;
+        for (uint32_t j = k > ns ? k - ns : 0u; j < k; ++j)
+            if (!mbar_wait(full0 + 8u * (j % ns), (j / ns) & 1u, kDrainNs)) err |= 2u;
+    }
+    if (err) atomicOr(&P.st->error, err);
+
+    // Global non-finite flag: one OR across the block, one atomic per block that saw one.
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(P.flag, 1u);
+    if constexpr (MODE == kNormAcc) block_norm_commit<kBulkThreads>(P, norm2.value());
 }
 
 // Gradient-norm pre-pass: the reduction of the fused kernel without the update; reads only
@@ -501,7 +782,7 @@ __global__ void __launch_bounds__(kThreads) grad_norm_kernel(const __grid_consta
             one(S, vi - S.vbeg);
         }
     }
-    block_norm_commit(P, norm2.value());
+    block_norm_commit<kThreads>(P, norm2.value());
 }
 
 // ZeRO-Offload: the reduction of the fused kernel, its averaged gradient written into the
@@ -579,8 +860,8 @@ __global__ void __launch_bounds__(kThreads) reduce_to_host_kernel(const __grid_c
 
 // ------------------------------------------------------------------ skip: re-cast + commit
 
-// On a flagged step the fused kernels have already written 16-bit values of the rejected
-// update; rewrite them from the unchanged current master.  Every block returns at once when
+// On a flagged (or discarded) step the fused kernels have already written 16-bit values of
+// the rejected update; rewrite them from the unchanged current master.  Every block returns at once when
 // the flag is clear (the usual case), so the launch costs a few microseconds.
 template <int DT, int VEC, typename PT>
 __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant__ PT P)
@@ -588,7 +869,7 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
     __shared__ int go, scur;
     if (threadIdx.x == 0) {
         const volatile DevState* st = P.st;
-        go = st->flag != 0;
+        go = (st->flag | st->error) != 0;
         scur = (int)st->cur;
     }
     __syncthreads();
@@ -646,11 +927,14 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
 
 // Close the step on the device: flag clear -> flip the current half, t += 1, count a clean
 // step and grow the scale after `interval` of them; flag set -> keep the state, back the
-// scale off (not below min_scale).  Then clear the flag for the next step.
+// scale off (not below min_scale).  Then clear the flag for the next step.  While the error
+// word is set (a bounded wait ran out) the step is discarded: nothing but the flag moves.
 __device__ __forceinline__ void commit_state(const CommitParams& C)
 {
     volatile DevState* st = C.st;
-    if (st->flag) {
+    if (st->error) {
+        st->last_skipped = 1;
+    } else if (st->flag) {
         st->last_skipped = 1;
         st->skipped = st->skipped + 1;
         if (C.dynamic) {
@@ -668,7 +952,7 @@ __device__ __forceinline__ void commit_state(const CommitParams& C)
             st->good = 0;
         }
     }
-    st->finished = st->finished + 1;
+    if (!st->error) st->finished = st->finished + 1;
     st->flag = 0;
     st->last_norm2 = st->norm2;
     st->last_norm_valid = st->norm_valid;
@@ -838,10 +1122,107 @@ void launch_fused_mode(int dev, const PT& P, bool vec, int64_t work, cudaStream_
     else launch_grid(fused_step_kernel<DT, kRankBatch, 8, MODE, PT>, dev, work, P, st);
 }
 
+// Geometry of the bulk-staged kernel (tile == 0: register-load kernel).
+struct BulkCfg {
+    int tile = 0;
+    int stages = 0;
+    uint64_t wait_ns = 0;
+};
+
+// Dynamic shared memory of one block: alignment slack, barriers, the ring.
+int64_t bulk_smem_bytes(int64_t tile, int64_t stages, int64_t n_d)
+{
+    return 128 + kBulkBarrierBytes + stages * tile * (2 * n_d + 12);
+}
+
+// Default geometry: the largest power-of-two tile up to 2048 elements whose buffer stays
+// within 56 KB, two buffers, so that two blocks (16 consumer warps) share an SM.  Measured
+// on GB300 (N_d = 7 and 16): more blocks per SM beat deeper rings, and larger tiles beat
+// more blocks, up to about 50 KB per buffer.
+int auto_bulk_tile(int n_d)
+{
+    int tile = 2048;
+    while (tile > 8 && (int64_t)tile * (2 * n_d + 12) > 56 * 1024) tile /= 2;
+    return tile;
+}
+
+int auto_bulk_stages(int /*tile*/, int /*n_d*/) { return 2; }
+
+BulkCfg bulk_config(const zero_plan* p)
+{
+    BulkCfg b;
+    if (!p->staging) return b;
+    b.tile = p->bulk_tile > 0 ? (int)p->bulk_tile : auto_bulk_tile(p->n_d);
+    b.stages = p->bulk_stages > 0 ? p->bulk_stages : auto_bulk_stages(b.tile, p->n_d);
+    b.wait_ns = (uint64_t)p->wait_limit_ns;
+    return b;
+}
+
+int optin_smem(int dev)
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+// Launch the bulk-staged kernel.  The dynamic shared-memory attribute and the occupancy are
+// set / queried when the ring size changes (host calls only; none inside a graph capture
+// once a step of the same geometry has run).
+template <int DT, int MODE, typename PT>
+cudaError_t launch_bulk_mode(int dev, PT& P, const BulkCfg& B, cudaStream_t st)
+{
+    static std::mutex mu;
+    static int64_t set_bytes[64] = {0};
+    static int per_sm_at[64] = {0};
+    auto kernel = bulk_step_kernel<DT, MODE, PT>;
+    const int64_t smem = bulk_smem_bytes(B.tile, B.stages, P.n_d);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int per_sm = 1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (set_bytes[dev] != smem) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, (size_t)smem);
+            if (e != cudaSuccess) return e;
+            per_sm_at[dev] = std::max(n, 1);
+            set_bytes[dev] = smem;
+        }
+        per_sm = per_sm_at[dev];
+    }
+    P.tile = B.tile;
+    P.stages = B.stages;
+    P.wait_ns = B.wait_ns;
+    int64_t tiles = 0;
+    for (int i = 0; i < P.n_seg; ++i) tiles += (8 * P.seg[i].nvec + B.tile - 1) / B.tile;
+    P.n_tiles = tiles;
+    const int64_t scalar_blocks = ((int64_t)P.n_seg * kScalarSlots + 32 * kBulkConsumers - 1) /
+                                  (32 * kBulkConsumers);
+    int64_t grid = std::min<int64_t>((int64_t)device_sms(dev) * per_sm, std::max(tiles, scalar_blocks));
+    grid = std::max<int64_t>(1, grid);
+    if (P.partials) grid = std::min<int64_t>(grid, kNormSlots);
+    kernel<<<(int)grid, kBulkThreads, (size_t)smem, st>>>(P);
+    return cudaGetLastError();
+}
+
 template <int DT, typename PT>
-cudaError_t launch_fused(int dev, PT& P, bool vec, cudaStream_t st, int mode = kPlain)
+cudaError_t launch_fused(int dev, PT& P, bool vec, cudaStream_t st, int mode = kPlain,
+                         const BulkCfg* bulk = nullptr)
 {
     finalize_vectors(P, vec);
+    if (bulk && bulk->tile > 0 && vec && P.st) {
+        if (mode == kNormAcc) return launch_bulk_mode<DT, kNormAcc>(dev, P, *bulk, st);
+        if (mode == kClip) return launch_bulk_mode<DT, kClip>(dev, P, *bulk, st);
+        return launch_bulk_mode<DT, kPlain>(dev, P, *bulk, st);
+    }
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     if (mode == kNormAcc) launch_fused_mode<DT, kNormAcc>(dev, P, vec, work, st);
     else if (mode == kClip) launch_fused_mode<DT, kClip>(dev, P, vec, work, st);
@@ -937,6 +1318,16 @@ zero_status_t read_state(zero_plan* p, cudaStream_t s, zero_step_result_t* out)
     out->skipped_total = host.skipped;
     out->finished = host.finished;
     out->grad_norm = host.last_norm_valid ? std::sqrt(host.last_norm2) : -1.0;
+    if (host.error) {
+        e = cudaMemsetAsync(&dev_state(p)->error, 0, sizeof(host.error), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+        return fail(ZERO_ETIMEOUT, (host.error & 2u)
+                                       ? "a barrier wait and the drain of the bulk-staged step ran out; "
+                                         "the steps finished since the last read were discarded"
+                                       : "a barrier wait of the bulk-staged step ran out; the steps "
+                                         "finished since the last read were discarded");
+    }
     return ZERO_OK;
 }
 
@@ -1119,6 +1510,46 @@ zero_status_t zero_set_scaler(zero_plan_t* p, const zero_scaler_t* cfg, void* st
     return ZERO_OK;
 }
 
+zero_status_t zero_set_option(zero_plan_t* p, int option, int64_t value)
+{
+    if (!p) return fail(ZERO_EINVAL, "zero_set_option: NULL plan");
+    if (p->in_step) return fail(ZERO_ESTATE, "zero_set_option: a step is open");
+    int64_t tile = p->bulk_tile, stages = p->bulk_stages;
+    switch (option) {
+    case ZERO_OPT_STAGING:
+        if (value != 0 && value != 1) return fail(ZERO_EINVAL, "zero_set_option: staging must be 0 or 1");
+        p->staging = (int)value;
+        return ZERO_OK;
+    case ZERO_OPT_WAIT_LIMIT_NS:
+        if (value < 0) return fail(ZERO_EINVAL, "zero_set_option: negative wait limit");
+        p->wait_limit_ns = value;
+        return ZERO_OK;
+    case ZERO_OPT_BULK_TILE:
+        if (value != 0 && (value < 8 || value > kBulkMaxTile || value % 8 != 0))
+            return fail(ZERO_EINVAL, "zero_set_option: tile must be 0 or a multiple of 8 in [8, 8192]");
+        tile = value;
+        break;
+    case ZERO_OPT_BULK_STAGES:
+        if (value != 0 && (value < 2 || value > kBulkMaxStages))
+            return fail(ZERO_EINVAL, "zero_set_option: stages must be 0 or in [2, 16]");
+        stages = value;
+        break;
+    default:
+        return fail(ZERO_EINVAL, "zero_set_option: unknown option");
+    }
+    const int64_t t = tile > 0 ? tile : auto_bulk_tile(p->n_d);
+    const int64_t n = stages > 0 ? stages : auto_bulk_stages((int)t, p->n_d);
+    // 227 KB: the opt-in shared memory of one block on this architecture (the device's own
+    // figure is checked as well once a device is known)
+    int64_t cap = 227 * 1024;
+    if (p->device >= 0 && optin_smem(p->device) > 0) cap = std::min<int64_t>(cap, optin_smem(p->device));
+    if (bulk_smem_bytes(t, n, p->n_d) > cap)
+        return fail(ZERO_ERANGE, "zero_set_option: the staging ring does not fit one block's shared memory");
+    p->bulk_tile = tile;
+    p->bulk_stages = (int)stages;
+    return ZERO_OK;
+}
+
 zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
                              int64_t which, void* stream)
 {
@@ -1202,6 +1633,7 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
     if (hyper->max_grad_norm > 0.0) mode = kClip;
     else if ((hyper->flags & ZERO_REPORT_GRAD_NORM) && !p->norm_open) mode = kNormAcc;
     const std::vector<Segment> segs = step_segments(p, which, 0);
+    const BulkCfg bulk = bulk_config(p);
     auto run = [&](auto& P, size_t cap) -> cudaError_t {
         for (size_t b = 0; b < segs.size(); b += cap) {
             const size_t e = std::min(segs.size(), b + cap);
@@ -1209,8 +1641,8 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
             P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
             const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
             const cudaError_t err = p->dtype16 == ZERO_BF16
-                                        ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode)
-                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode);
+                                        ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode, &bulk)
+                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode, &bulk);
             if (err != cudaSuccess) return err;
         }
         return cudaSuccess;

@@ -12,7 +12,7 @@ from typing import Dict, List, Optional, Sequence
 
 import torch
 
-from . import (ZERO_BF16, ZERO_TABLE_PARAM_CHUNKS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS,
+from . import (ZERO_BF16, zero_set_option, ZERO_TABLE_PARAM_CHUNKS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_UNITS,
                zero_bind, zero_bind_offload, zero_bind_peer, zero_offload_finish,
                zero_offload_step, zero_plan_create_per_param,
                zero_gather_layer, zero_plan_create, zero_plan_destroy, zero_plan_info,
@@ -131,6 +131,9 @@ class EmulatedGroup:
 
     def set_scaler(self, scaler, stream=None) -> None:
         zero_set_scaler(self.plan, scaler, _stream_handle(stream))
+
+    def set_option(self, option: int, value: int) -> None:
+        zero_set_option(self.plan, option, value)
 
     def state_tensor(self, rank: int, name: str) -> torch.Tensor:
         if self.offload:                       # updated in place on the host
