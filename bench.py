@@ -38,7 +38,8 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_step.cu); reported as null once that source
 # changes.  Captures: profiles/*_ncu_full.md.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {(1, "fused_step_kernel"): ("4e99b3a813d68f4b", 2_303_957_504),
+                    (1, "bulk_step_kernel"): ("4e99b3a813d68f4b", 2_294_720_768)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_step.cu")
 
 
@@ -479,29 +480,48 @@ def gpu_arm(args, world, rank, local):
 
 def e2e_leg(b: Bench, steps: int, world: int, dist):
     """Same metric through the public API with the gradients in pinned host memory: every step
-    copies its contributions host->device, runs the step, and reads the step result back."""
+    copies its contributions host->device, runs the step, and reads the step result back.
+    With two device buffer sets the copy of step k+1 (on a copy stream) runs while step k
+    computes, as a training loop would double-buffer its inputs; the host->device link
+    (about 209 GB/s from pinned Grace memory, copy engines and SM loads alike) bounds it."""
     torch = b.torch
     host = [torch.empty(b.set_elems, dtype=torch.int16, pin_memory=True) for _ in range(b.w.n_d)]
     for r in range(b.w.n_d):
         host[r].copy_(b.sets[0][r][:b.set_elems])
-    dev = b.sets[0]
+    bufs = b.sets[:2]
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in bufs]
+
+    def fetch(k):
+        dev = bufs[k % len(bufs)]
+        copy.wait_stream(compute)          # the set's previous step has finished with it
+        with torch.cuda.stream(copy):
+            for r in range(b.w.n_d):
+                dev[r][:b.set_elems].copy_(host[r], non_blocking=True)
+            copied[k % len(bufs)].record(copy)
+
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t = time.perf_counter()
     applied = 0
+    fetch(0)
     for k in range(steps):
-        for r in range(b.w.n_d):
-            dev[r][:b.set_elems].copy_(host[r], non_blocking=True)
-        res, _ = b.step(dev, wait=True)   # reads the step result back to the host
+        compute.wait_event(copied[k % len(bufs)])
+        if len(bufs) > 1 and k + 1 < steps:
+            fetch(k + 1)
+        res, _ = b.step(bufs[k % len(bufs)], wait=True)   # reads the step result back
         applied += 1 - res.skipped
+        if len(bufs) == 1 and k + 1 < steps:
+            fetch(k + 1)
     torch.cuda.synchronize()
     el = time.perf_counter() - t
     if dist:
         el = max_over_ranks(el, dist)
     return {"value": job_value(b.elems_per_step, applied, world, el), "unit": UNIT,
             "h2d_bytes_per_step": 2 * b.set_elems * b.w.n_d, "d2h_bytes_per_step": 64,
-            "steps": steps}
+            "steps": steps, "double_buffered": len(bufs) > 1}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

@@ -1,5 +1,7 @@
 // zero_step.cu -- device side of the sharded mixed-precision AdamW step for
-// GB300 (sm_103a): bind, the fused reduce + AdamW + cast kernel, the device-side
+// GB300 (sm_103a): bind, the fused reduce + AdamW + cast kernel (128-bit register
+// loads, or a variant whose tiles are staged into shared memory by cp.async.bulk
+// copies), the gradient-norm pre-pass, the offload reduction, the device-side
 // commit/skip, the skip re-cast and the stage-3 gather.
 //
 // Page: "Zero Redundancy Optimizer (ZeRO) and Fully Sharded Data Parallelism
@@ -30,7 +32,7 @@
 namespace zero {
 namespace {
 
-constexpr int kThreads = 128;     // 128-thread blocks: 70 registers, 7 blocks resident per SM
+constexpr int kThreads = 128;     // 128-thread blocks: 72 registers, 7 blocks resident per SM
 constexpr int kMaxSegs = 32;      // work items per launch (more are split across launches)
 constexpr int kWideSegs = 256;    // capacity of the wide parameter block (calls with many items)
 constexpr int kScalarSlots = 16;  // per segment: up to 7 head + 7 tail elements
@@ -887,20 +889,42 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
         }
     }
     int s = 0;
-    for (int64_t vi = go ? tid : P.total_vec; vi < P.total_vec; vi += stride) {
-        while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
-        const KSeg& S = P.seg[s];
-        if constexpr (VEC == 8) {
-            const int64_t e = S.head + 8 * (vi - S.vbeg);
-            const float4 a = __ldcs(reinterpret_cast<const float4*>(S.p[cur] + e));
-            const float4 b = __ldcs(reinterpret_cast<const float4*>(S.p[cur] + e) + 1);
-            uint4 o;
-            o.x = narrow2<DT>(a.x, a.y);
-            o.y = narrow2<DT>(a.z, a.w);
-            o.z = narrow2<DT>(b.x, b.y);
-            o.w = narrow2<DT>(b.z, b.w);
-            __stcs(reinterpret_cast<uint4*>(S.out16 + e), o);
-        } else {
+    if constexpr (VEC == 8) {
+        // four vectors per thread and iteration, loads before stores: the launch has one block
+        // per SM, so each thread keeps several loads in flight
+        constexpr int kU = 4;
+        for (int64_t v0 = go ? tid : P.total_vec; v0 < P.total_vec; v0 += kU * stride) {
+            float4 a[kU], b[kU];
+            uint16_t* dst[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t vi = v0 + u * stride;
+                dst[u] = nullptr;
+                if (vi < P.total_vec) {
+                    while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
+                    const KSeg& S = P.seg[s];
+                    const int64_t e = S.head + 8 * (vi - S.vbeg);
+                    a[u] = __ldcs(reinterpret_cast<const float4*>(S.p[cur] + e));
+                    b[u] = __ldcs(reinterpret_cast<const float4*>(S.p[cur] + e) + 1);
+                    dst[u] = S.out16 + e;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (dst[u]) {
+                    uint4 o;
+                    o.x = narrow2<DT>(a[u].x, a[u].y);
+                    o.y = narrow2<DT>(a[u].z, a[u].w);
+                    o.z = narrow2<DT>(b[u].x, b[u].y);
+                    o.w = narrow2<DT>(b[u].z, b[u].w);
+                    __stcs(reinterpret_cast<uint4*>(dst[u]), o);
+                }
+            }
+        }
+    } else {
+        for (int64_t vi = go ? tid : P.total_vec; vi < P.total_vec; vi += stride) {
+            while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
+            const KSeg& S = P.seg[s];
             const int64_t e = vi - S.vbeg;
             S.out16[e] = narrow1<DT>(S.p[cur][e]);
         }
@@ -932,30 +956,43 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
 __device__ __forceinline__ void commit_state(const CommitParams& C)
 {
     volatile DevState* st = C.st;
-    if (st->error) {
-        st->last_skipped = 1;
-    } else if (st->flag) {
-        st->last_skipped = 1;
-        st->skipped = st->skipped + 1;
+    // All fields are loaded first (independent loads: one round trip to L2), then the new
+    // values are formed and stored.
+    const uint32_t error = st->error, flag = st->flag, cur = st->cur, norm_valid = st->norm_valid;
+    const int64_t t = st->t, skipped = st->skipped, good = st->good, finished = st->finished;
+    const double scale = st->scale, norm2 = st->norm2;
+    uint32_t n_cur = cur, n_last = 1;
+    int64_t n_t = t, n_skipped = skipped, n_good = good;
+    double n_scale = scale;
+    if (error) {
+        // discarded: nothing else moves
+    } else if (flag) {
+        n_skipped = skipped + 1;
         if (C.dynamic) {
-            const double s = st->scale * C.backoff;
-            st->scale = s < C.min_scale ? C.min_scale : s;
+            const double sc = scale * C.backoff;
+            n_scale = sc < C.min_scale ? C.min_scale : sc;
         }
-        st->good = 0;
+        n_good = 0;
     } else {
-        st->last_skipped = 0;
-        st->cur = st->cur ^ 1u;
-        st->t = st->t + 1;
-        st->good = st->good + 1;
-        if (C.dynamic && C.interval > 0 && st->good >= C.interval) {
-            st->scale = st->scale * C.growth;
-            st->good = 0;
+        n_last = 0;
+        n_cur = cur ^ 1u;
+        n_t = t + 1;
+        n_good = good + 1;
+        if (C.dynamic && C.interval > 0 && n_good >= C.interval) {
+            n_scale = scale * C.growth;
+            n_good = 0;
         }
     }
-    if (!st->error) st->finished = st->finished + 1;
+    st->last_skipped = n_last;
+    st->cur = n_cur;
+    st->t = n_t;
+    st->skipped = n_skipped;
+    st->good = n_good;
+    st->scale = n_scale;
+    st->finished = error ? finished : finished + 1;
     st->flag = 0;
-    st->last_norm2 = st->norm2;
-    st->last_norm_valid = st->norm_valid;
+    st->last_norm2 = norm2;
+    st->last_norm_valid = norm_valid;
     st->norm2 = 0.0;
     st->norm_valid = 0;
 }
@@ -1250,13 +1287,18 @@ cudaError_t launch_reduce_to_host(int dev, PT& P, bool vec, cudaStream_t st)
     return cudaGetLastError();
 }
 
+// One block per SM at most: the launch does nothing on a clean step (the usual case) except
+// read the flag and take the commit ticket, so its cost is the block count; a skipped step's
+// re-cast (6 bytes per element) still streams at a good fraction of HBM bandwidth.
 template <int DT, typename PT>
 cudaError_t launch_recast(int dev, PT& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
-    if (vec) launch_grid(recast_kernel<DT, 8, PT>, dev, work, P, st);
-    else launch_grid(recast_kernel<DT, 1, PT>, dev, work, P, st);
+    const int64_t need = std::max<int64_t>(1, (work + kThreads - 1) / kThreads);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(device_sms(dev), need));
+    if (vec) recast_kernel<DT, 8, PT><<<grid, kThreads, 0, st>>>(P);
+    else recast_kernel<DT, 1, PT><<<grid, kThreads, 0, st>>>(P);
     return cudaGetLastError();
 }
 
