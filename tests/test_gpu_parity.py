@@ -454,8 +454,11 @@ OVERLAP_CASES = {
 def test_overlapped_stage3_schedule_full_parity(name):
     """Gathers on a second stream, double-buffered, against the oracle: states, shards and the
     last two gathered units (left in the two buffers) must match."""
-    w = OVERLAP_CASES[name]
-    run = H.Run(w)
+    _run_overlap(OVERLAP_CASES[name], name)
+
+
+def _run_overlap(w, name, options=None):
+    run = H.Run(w, options=options)
     o = H.OracleFull(w, run.bound)
     comm = torch.cuda.Stream()
     nu = len(run.units)
@@ -643,14 +646,15 @@ def test_tiny_case_sweep():
 
 # ---------------------------------------------------------------------- CUDA graph capture
 
+@pytest.mark.parametrize("staging", [0, 1])
 @pytest.mark.parametrize("name", ["z2_nd8_fp16_buckets_inf", "z3_nd16_units"])
-def test_step_captured_in_a_cuda_graph(name):
+def test_step_captured_in_a_cuda_graph(name, staging):
     """The step state lives on the device, so a whole step -- every bucket / unit's fused
     launch, the re-cast and the commit -- can be captured once and replayed: replays with new
     gradients written in place into the same buffers must follow the oracle step by step,
-    through a skipped step and the loss-scale back-off."""
+    through a skipped step and the loss-scale back-off.  staging 1: the bulk-staged kernel."""
     w = dataclasses.replace(SMALL_CASES[name], steps=5)
-    run = H.Run(w)
+    run = H.Run(w, options={Z.ZERO_OPT_STAGING: staging})
     o = H.OracleFull(w, run.bound)
     ranges = run.ranges()
     bufs = [[torch.empty(max(8, hi - lo), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
@@ -718,6 +722,16 @@ def test_bulk_staging_config_sampled(i):
 @pytest.mark.parametrize("name", list(CLIP_CASES))
 def test_bulk_staging_norm_and_clipping(name):
     _run_clip(name, options=BULK)
+
+
+@pytest.mark.parametrize("name", list(PP_CASES))
+def test_bulk_staging_per_param_full_parity(name):
+    """Per-parameter plans: one work item per tensor chunk, up to 256 per launch."""
+    _run_full(PP_CASES[name], options=BULK)
+
+
+def test_bulk_staging_overlapped_schedule():
+    _run_overlap(OVERLAP_CASES["z3_nd16_units"], "bulk z3_nd16_units", options=BULK)
 
 
 @pytest.mark.parametrize("name,tile,stages", [

@@ -26,6 +26,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "zero_internal.h"
 
@@ -38,6 +39,8 @@ constexpr int kWideSegs = 256;    // capacity of the wide parameter block (calls
 constexpr int kScalarSlots = 16;  // per segment: up to 7 head + 7 tail elements
 // Contribution slices loaded (128-bit each) per batch before they are summed.
 constexpr int kRankBatch = 4;
+// The gradient-norm pre-pass reads nothing else, so it keeps more slices in flight.
+constexpr int kNormRankBatch = 8;
 
 // ------------------------------------------------------------------ device-resident step state
 
@@ -1055,18 +1058,23 @@ int device_sms(int dev)
     return cache[dev];
 }
 
-// Resident blocks per SM of one kernel (queried once per kernel).
+// Resident blocks per SM of one kernel, queried once per kernel.  Kernels of one signature
+// share this template's statics, so the cache is keyed by the kernel's address.
 template <typename K>
 int blocks_per_sm(K kernel)
 {
-    static int cached = 0;
-    if (cached == 0) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
-            per_sm = 1;
-        cached = std::max(per_sm, 1);
-    }
-    return cached;
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> cache;
+    const void* key = reinterpret_cast<const void*>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
+        per_sm = 1;
+    per_sm = std::max(per_sm, 1);
+    cache.emplace(key, per_sm);
+    return per_sm;
 }
 
 template <typename K>
@@ -1273,7 +1281,7 @@ cudaError_t launch_norm(int dev, PT& P, bool vec, cudaStream_t st)
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     if (!vec) launch_grid(grad_norm_kernel<DT, 1, 1, PT>, dev, work, P, st);
-    else launch_grid(grad_norm_kernel<DT, kRankBatch, 8, PT>, dev, work, P, st);
+    else launch_grid(grad_norm_kernel<DT, kNormRankBatch, 8, PT>, dev, work, P, st);
     return cudaGetLastError();
 }
 
