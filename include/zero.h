@@ -251,10 +251,11 @@ zero_status_t zero_grad_norm(zero_plan_t* plan, const void* const* grad_contribs
                              int64_t n_contribs, int64_t which, void* stream);
 
 /* End the step on the device: a re-cast kernel (which does nothing unless the flag is set)
- * rewrites the 16-bit parameters of a skipped step from the unchanged master, then a
- * one-thread commit either makes the new state current (t += 1, loss-scale growth) or keeps
- * the old one (loss-scale back-off), and clears the flag.  With out == NULL the call only
- * enqueues this work; with out != NULL it also synchronises `stream` and reads the state. */
+ * rewrites the 16-bit parameters of a skipped step from the unchanged master, and its last
+ * block to finish commits: it either makes the new state current (t += 1, loss-scale growth)
+ * or keeps the old one (loss-scale back-off), and clears the flag.  With out == NULL the call
+ * only enqueues this work; with out != NULL it also synchronises `stream` and reads the
+ * state. */
 zero_status_t zero_step_finish(zero_plan_t* plan, void* stream, zero_step_result_t* out);
 
 /* Read the device-resident step state (synchronises `stream`).  zero_read_state and
@@ -269,7 +270,7 @@ zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_
  *                           fp32 state with 128-bit register loads.  1: a producer warp stages
  *                           them tile by tile into a ring of shared-memory buffers with 1-D
  *                           cp.async.bulk copies (the TMA engine) completing on mbarriers, and
- *                           four consumer warps reduce and update from shared memory.  Both
+ *                           eight consumer warps reduce and update from shared memory.  Both
  *                           give identical results, bit for bit.  Launches whose streams do not
  *                           share one 16-byte phase use the scalar path either way.
  *   ZERO_OPT_WAIT_LIMIT_NS  bound on each barrier wait of the bulk-staged kernel, in ns of
