@@ -38,8 +38,8 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_step.cu); reported as null once that source
 # changes.  Captures: profiles/*_ncu_full.md.
-MEASURED_TRAFFIC = {(1, "fused_step_kernel"): ("4e99b3a813d68f4b", 2_303_957_504),
-                    (1, "bulk_step_kernel"): ("4e99b3a813d68f4b", 2_294_720_768)}
+MEASURED_TRAFFIC = {(1, "fused_step_kernel"): ("fefc07ed053e1679", 2_301_633_280),
+                    (1, "bulk_step_kernel"): ("fefc07ed053e1679", 2_294_535_936)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_step.cu")
 
 
