@@ -103,6 +103,22 @@ def test_small_case_full_parity(name):
     _run_full(SMALL_CASES[name])
 
 
+# N_d at its limit (ZERO_MAX_RANKS = 128 contribution pointers in the kernel parameters):
+# ZeRO-2 over ragged tensors with buckets, and ZeRO-3 with an fp16 skip; both kernels.
+MAX_RANK_CASES = {
+    "z2_nd128_buckets": _mk(190, _ragged(30, 12, 40000), 128, 2, steps=2, bucket=50_000),
+    "z3_nd128_fp16_skip": _mk(191, _ragged(31, 9, 30000), 128, 3, steps=3, units=(0, 4),
+                              dtype=W.FP16, scaler=W.Scaler(init_scale=2048.0),
+                              inject=(2, 77, 5), bound=(0, 64, 127)),
+}
+
+
+@pytest.mark.parametrize("staging", [0, 1])
+@pytest.mark.parametrize("name", list(MAX_RANK_CASES))
+def test_max_ranks_full_parity(name, staging):
+    _run_full(MAX_RANK_CASES[name], options={Z.ZERO_OPT_STAGING: staging})
+
+
 def test_config0_full_parity():
     w = W.workload(0)
     mism = _run_full(w)
