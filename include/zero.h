@@ -37,8 +37,9 @@
  *    for the state layout below when bucket_elems is a multiple of 8); other
  *    launches use the scalar path of the same kernel.
  *  - Kernels never trap or assert.  The only waits are those of the bulk-staged step kernel
- *    (zero_set_option, ZERO_OPT_STAGING = 1) on its shared-memory barriers; each is bounded
- *    in time (ZERO_OPT_WAIT_LIMIT_NS) and one that runs out is reported as ZERO_ETIMEOUT.
+ *    (the default; zero_set_option, ZERO_OPT_STAGING) on its shared-memory barriers; each is
+ *    bounded in time (ZERO_OPT_WAIT_LIMIT_NS) and one that runs out is reported as
+ *    ZERO_ETIMEOUT.
  */
 #ifndef ZERO_H
 #define ZERO_H
@@ -266,20 +267,22 @@ zero_status_t zero_step_finish(zero_plan_t* plan, void* stream, zero_step_result
 zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_t* out);
 
 /* Execution options of a plan (not inside an open step; values are checked here):
- *   ZERO_OPT_STAGING        0 (default): the fused step loads the contribution slices and the
- *                           fp32 state with 128-bit register loads.  1: a producer warp stages
- *                           them tile by tile into a ring of shared-memory buffers with 1-D
- *                           cp.async.bulk copies (the TMA engine) completing on mbarriers, and
- *                           eight consumer warps reduce and update from shared memory.  Both
- *                           give identical results, bit for bit.  Launches whose streams do not
- *                           share one 16-byte phase use the scalar path either way.
+ *   ZERO_OPT_STAGING        1 (default): per block a producer warp stages the contribution
+ *                           slices and the fp32 state tile by tile into a ring of shared-memory
+ *                           buffers with 1-D cp.async.bulk copies (the TMA engine) completing on
+ *                           mbarriers, and four consumer warps reduce and update from shared
+ *                           memory.  0: every thread loads them with 128-bit register loads.
+ *                           Both give identical results, bit for bit.  Launches whose streams
+ *                           do not share one 16-byte phase use the scalar register-load path
+ *                           either way, and so do steps that report the gradient norm from the
+ *                           fused pass (ZERO_REPORT_GRAD_NORM without clipping).
  *   ZERO_OPT_WAIT_LIMIT_NS  bound on each barrier wait of the bulk-staged kernel, in ns of
  *                           %globaltimer (default 1e9; 0 gives up at the first wait that does
  *                           not succeed at once).  A wait that runs out sets the plan's error
  *                           word, its block drains its own copies in flight and returns.
  *   ZERO_OPT_BULK_TILE      elements per staged tile, a multiple of 8 in [8, 8192]; 0 (default):
- *                           the largest power of two up to 2048 with tile * (2 N_d + 12) bytes
- *                           within 56 KB.
+ *                           the largest multiple of 512 up to 2048 with tile * (2 N_d + 12)
+ *                           bytes within 45 KB (a power of two below 512 for N_d >= 40).
  *   ZERO_OPT_BULK_STAGES    ring depth in [2, 16]; 0 (default): 2 (two blocks per SM).
  * A tile/stage pair whose ring does not fit one block's shared memory gives ZERO_ERANGE. */
 enum {

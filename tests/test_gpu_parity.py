@@ -617,7 +617,8 @@ def test_offload_rejects_mixing_and_pageable_buffers():
 def test_tiny_case_sweep():
     """Bounds and peeling: 150 random plans with phi <= 80, N_d 1..16, stages 1/2/3, bf16 and
     fp16, odd buckets, zero-size tensors, and half of them fed contributions that start one
-    element past a 16-byte boundary (scalar path); two steps each against the oracle."""
+    element past a 16-byte boundary (scalar path); the two step kernels alternate; two steps
+    each against the oracle."""
     rng = np.random.default_rng(60)
     for trial in range(150):
         nt = int(rng.integers(1, 7))
@@ -635,7 +636,7 @@ def test_tiny_case_sweep():
                        stage=stage, bucket_elems=bucket, unit_first=units, dtype=dtype, steps=2,
                        hyper=W.Hyper(), scaler=None)
         shift = bool(rng.integers(0, 2))
-        run = H.Run(w)
+        run = H.Run(w, options={Z.ZERO_OPT_STAGING: trial % 2})
         o = H.OracleFull(w, run.bound)
         try:
             for k in (1, 2):
@@ -714,40 +715,45 @@ def test_step_captured_in_a_cuda_graph(name, staging):
         run.close()
 
 
-# ---------------------------------------------------------------------- bulk (TMA) staging
+# ---------------------------------------------------------------------- the two step kernels
+# The cases above run the default, bulk-staged kernel (cp.async.bulk into shared memory); the
+# register-load kernel re-runs them here, and the bulk kernel's own geometry, bit identity and
+# timeout tests follow.
 
 BULK = {Z.ZERO_OPT_STAGING: 1}
+LDG = {Z.ZERO_OPT_STAGING: 0}
 
 
 @pytest.mark.parametrize("name", list(SMALL_CASES))
-def test_bulk_staging_small_case_full_parity(name):
-    _run_full(SMALL_CASES[name], options=BULK)
+def test_register_loads_small_case_full_parity(name):
+    _run_full(SMALL_CASES[name], options=LDG)
 
 
-def test_bulk_staging_config0_full_parity():
-    mism = _run_full(W.workload(0), options=BULK)
-    print(f"configs[0], bulk staging: {mism} bit mismatches (within tolerance)")
+def test_register_loads_config0_full_parity():
+    mism = _run_full(W.workload(0), options=LDG)
+    print(f"configs[0], register loads: {mism} bit mismatches (within tolerance)")
 
 
-@pytest.mark.parametrize("i", [1, 3])
-def test_bulk_staging_config_sampled(i):
-    n, mism = _run_sampled(W.workload(i), options=BULK)
-    print(f"configs[{i}], bulk staging: {n} sampled elements, {mism} bit mismatches")
+@pytest.mark.parametrize("i", [1, 2, 3, 4])
+def test_register_loads_config_sampled(i):
+    w = W.workload(i)
+    n, mism = _run_sampled(w, bound=(0, w.n_d - 1) if i == 4 else None, options=LDG)
+    print(f"configs[{i}], register loads: {n} sampled elements, {mism} bit mismatches")
 
 
 @pytest.mark.parametrize("name", list(CLIP_CASES))
-def test_bulk_staging_norm_and_clipping(name):
-    _run_clip(name, options=BULK)
+def test_register_loads_norm_and_clipping(name):
+    _run_clip(name, options=LDG)
 
 
 @pytest.mark.parametrize("name", list(PP_CASES))
-def test_bulk_staging_per_param_full_parity(name):
+def test_register_loads_per_param_full_parity(name):
     """Per-parameter plans: one work item per tensor chunk, up to 256 per launch."""
-    _run_full(PP_CASES[name], options=BULK)
+    _run_full(PP_CASES[name], options=LDG)
 
 
-def test_bulk_staging_overlapped_schedule():
-    _run_overlap(OVERLAP_CASES["z3_nd16_units"], "bulk z3_nd16_units", options=BULK)
+def test_register_loads_overlapped_schedule():
+    _run_overlap(OVERLAP_CASES["z3_nd16_units"], "register loads z3_nd16_units", options=LDG)
 
 
 @pytest.mark.parametrize("name,tile,stages", [
@@ -764,7 +770,7 @@ def test_bulk_staging_geometries(name, tile, stages):
 
 def test_bulk_staging_is_bit_identical_to_register_loads():
     w = dataclasses.replace(SMALL_CASES["z2_nd8_fp16_buckets_inf"], steps=4)
-    a, b = H.Run(w), H.Run(w, options=BULK)
+    a, b = H.Run(w, options=LDG), H.Run(w, options=BULK)
     try:
         for k in range(1, w.steps + 1):
             ra, rb = a.step(k), b.step(k)

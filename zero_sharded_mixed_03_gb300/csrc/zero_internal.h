@@ -130,7 +130,7 @@ struct zero_plan {
     double bias_beta1 = -1.0, bias_beta2 = -1.0;
     std::vector<char> gathered;         // stage 3: per unit
     // Execution options (zero_set_option).
-    int staging = 0;                    // 1: cp.async.bulk staging of the fused step
+    int staging = 1;                    // 1: cp.async.bulk staging of the fused step; 0: register loads
     int64_t wait_limit_ns = 1000000000; // bound on each barrier wait of the staged kernel
     int64_t bulk_tile = 0;              // elements per staged tile (0: chosen from N_d)
     int bulk_stages = 0;                // ring depth (0: chosen from the tile)

@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
 // buffer on its "empty" mbarrier.  Every wait is bounded (P.wait_ns of %globaltimer and an
 // iteration cap); one that runs out sets DevState::error and ends that warp's loop, and the
 // producer waits (bounded again) for every copy it issued before the block returns.
-constexpr int kBulkConsumers = 8;                        // consumer warps
+constexpr int kBulkConsumers = 4;                        // consumer warps
 constexpr int kBulkThreads = 32 * (kBulkConsumers + 1);  // + the producer warp
 constexpr int kBulkBarrierBytes = 256;                   // full[16] + empty[16] mbarriers
 constexpr int kBulkMaxStages = 16;
@@ -1180,15 +1180,19 @@ int64_t bulk_smem_bytes(int64_t tile, int64_t stages, int64_t n_d)
     return 128 + kBulkBarrierBytes + stages * tile * (2 * n_d + 12);
 }
 
-// Default geometry: the largest power-of-two tile up to 2048 elements whose buffer stays
-// within 56 KB, two buffers, so that two blocks (16 consumer warps) share an SM.  Measured
-// on GB300 (N_d = 7 and 16): more blocks per SM beat deeper rings, and larger tiles beat
-// more blocks, up to about 50 KB per buffer.
+// Default geometry: two buffers of the largest tile, a multiple of 512 elements (whole passes
+// of the consumer threads over 4-element quads) up to 2048, within 45 KB per buffer; for
+// N_d >= 40 the largest power of two within 45 KB.  Two blocks then share an SM with a
+// 80-90 KB ring each.  Measured on GB300 with N_d = 7, 8 and 16: two blocks of ~4
+// consumer warps with 40-50 KB tiles beat both deeper rings and more, smaller blocks.
 int auto_bulk_tile(int n_d)
 {
-    int tile = 2048;
-    while (tile > 8 && (int64_t)tile * (2 * n_d + 12) > 56 * 1024) tile /= 2;
-    return tile;
+    const int64_t per_elem = 2 * n_d + 12, cap = 45 * 1024;
+    int64_t tile = std::min<int64_t>(2048, cap / per_elem / 512 * 512);
+    if (tile >= 512) return (int)tile;
+    tile = 256;
+    while (tile > 8 && tile * per_elem > cap) tile /= 2;
+    return (int)tile;
 }
 
 int auto_bulk_stages(int /*tile*/, int /*n_d*/) { return 2; }
@@ -1263,8 +1267,10 @@ cudaError_t launch_fused(int dev, PT& P, bool vec, cudaStream_t st, int mode = k
                          const BulkCfg* bulk = nullptr)
 {
     finalize_vectors(P, vec);
-    if (bulk && bulk->tile > 0 && vec && P.st) {
-        if (mode == kNormAcc) return launch_bulk_mode<DT, kNormAcc>(dev, P, *bulk, st);
+    // Norm-report steps keep the register-load kernel: the per-element norm accumulation is a
+    // serial chain per thread, which the bulk kernel's few consumer warps do not hide
+    // (ragged N_d = 7 workload on GB300: 367 us against 353 us).
+    if (bulk && bulk->tile > 0 && vec && P.st && mode != kNormAcc) {
         if (mode == kClip) return launch_bulk_mode<DT, kClip>(dev, P, *bulk, st);
         return launch_bulk_mode<DT, kPlain>(dev, P, *bulk, st);
     }
