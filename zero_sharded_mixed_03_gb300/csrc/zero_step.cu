@@ -627,6 +627,7 @@ __device__ __forceinline__ bool step_quad_staged(const PT& P, const KSeg& S, con
 template <int DT, int MODE, typename PT>
 __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_constant__ PT P)
 {
+    static_assert(MODE != kNormAcc, "norm-report steps run fused_step_kernel");
     extern __shared__ __align__(128) unsigned char bulk_raw[];
     __shared__ float sk4[4];
     __shared__ int scur;
@@ -719,7 +720,6 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_co
 
     // Global non-finite flag: one OR across the block, one atomic per block that saw one.
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(P.flag, 1u);
-    if constexpr (MODE == kNormAcc) block_norm_commit<kBulkThreads>(P, norm2.value());
 }
 
 // Gradient-norm pre-pass: the reduction of the fused kernel without the update; reads only
