@@ -785,6 +785,45 @@ def test_bulk_staging_is_bit_identical_to_register_loads():
         b.close()
 
 
+def test_bulk_staging_first_launch_inside_a_graph_capture():
+    """A plan that stepped with register loads switches to the staged kernel, whose first launch
+    (kernel attributes, occupancy query) then happens inside a CUDA graph capture; the replays
+    must follow the oracle."""
+    w = dataclasses.replace(SMALL_CASES["z2_nd7_ragged_tensors"], wid=175, steps=3)
+    run = H.Run(w, options=LDG)
+    o = H.OracleFull(w, run.bound)
+    try:
+        res = run.step(1)
+        o.step(1)
+        assert res.t == 1
+        run.g.set_option(Z.ZERO_OPT_STAGING, 1)
+        run.g.set_option(Z.ZERO_OPT_BULK_TILE, 72)      # a geometry no other test launches
+        ranges = run.ranges()
+        bufs = [[torch.empty(max(8, hi - lo), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+                for (_, lo, hi) in ranges]
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for (which, lo, hi), unit in zip(ranges, bufs):
+                    run.g.step([b.data_ptr() for b in unit], which, run.hyper)
+                run.g.finish(wait=False)
+        for k in (2, 3):
+            for (which, lo, hi), unit in zip(ranges, bufs):
+                for r in range(w.n_d):
+                    H.fill_device(unit[r], synth.grad_stream(w, k, r), run.units, lo, hi)
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            o.step(k)
+            assert run.g.step_state().t == k
+            _compare_full(run, o, f"staged kernel first captured, step {k}")
+    finally:
+        run.close()
+
+
 def test_bulk_staging_wait_limit_runs_out_and_the_step_is_discarded():
     """A wait limit of 0 makes the first barrier wait that is not already satisfied give up:
     the kernel records it, drains its copies and returns; zero_step_finish reports
