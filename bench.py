@@ -457,7 +457,7 @@ def gpu_arm(args, world, rank, local):
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype":
            "fp16" if w.dtype == W.FP16 else "bf16", "data": "synthetic",
-           "config": {"workload": w.name, "config_index": args.config, "n_d": w.n_d,
+           "config": {"workload": w.name, "workload_index": args.config, "n_d": w.n_d,
                       "stage": w.stage, "phi": w.phi, "bucket_elems": w.bucket_elems,
                       "units": len(b.units), "bound_ranks": len(b.bound),
                       "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
@@ -579,7 +579,7 @@ def reference_arm(args, world, rank):
            "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic",
-           "config": {"workload": w.name, "config_index": args.config, "n_d": w.n_d,
+           "config": {"workload": w.name, "workload_index": args.config, "n_d": w.n_d,
                       "stage": w.stage, "phi": w.phi, "sample_elems": n},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                             "sample": f"first {n} flat elements per step, single-threaded"},

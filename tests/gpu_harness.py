@@ -1,4 +1,4 @@
-"""GPU-side driver for parity tests: seeded inputs on the device, oracle replay on the host.
+"""GPU-side harness for parity tests: seeded inputs on the device, oracle replay on the host.
 
 The device inputs come from the shared generator (synth); the expected values come only
 from the oracle, run on host copies of the same seeded streams.

@@ -122,7 +122,7 @@ def test_max_ranks_full_parity(name, staging):
 def test_config0_full_parity():
     w = W.workload(0)
     mism = _run_full(w)
-    print(f"configs[0]: {mism} bit mismatches (within tolerance)")
+    print(f"{w.name}: {mism} bit mismatches (within tolerance)")
 
 
 def _run_sampled(w: W.Workload, bound=None, n_random=20000, options=None):
@@ -164,13 +164,13 @@ def _run_sampled(w: W.Workload, bound=None, n_random=20000, options=None):
 @pytest.mark.parametrize("i", [1, 2, 3])
 def test_config_sampled_parity(i):
     n, mism = _run_sampled(W.workload(i))
-    print(f"configs[{i}]: {n} sampled elements, {mism} bit mismatches (within tolerance)")
+    print(f"{W.workload(i).name}: {n} sampled elements, {mism} bit mismatches (within tolerance)")
 
 
 def test_config4_rank0_and_last_rank_sampled():
     w = W.workload(4)
     n, mism = _run_sampled(w, bound=(0, w.n_d - 1))
-    print(f"configs[4] ranks 0 and {w.n_d - 1}: {n} sampled elements, {mism} bit mismatches")
+    print(f"{w.name}, ranks 0 and {w.n_d - 1}: {n} sampled elements, {mism} bit mismatches")
 
 
 # ---------------------------------------------------------------------- guards and errors
@@ -547,7 +547,7 @@ def test_per_param_full_parity(name):
 def test_per_param_config_sampled(i):
     w = W.per_param_variant(W.workload(i))
     n, mism = _run_sampled(w, bound=(0, w.n_d - 1) if i == 4 else None)
-    print(f"per-parameter configs[{i}]: {n} sampled elements, {mism} bit mismatches")
+    print(f"per-parameter {w.name}: {n} sampled elements, {mism} bit mismatches")
 
 
 def test_per_param_overlapped_schedule():
@@ -583,7 +583,7 @@ def test_offload_full_parity(name):
 def test_offload_sampled_config1():
     w = dataclasses.replace(W.workload(1), offload=True)
     n, mism = _run_sampled(w)
-    print(f"offloaded configs[1]: {n} sampled elements, {mism} bit mismatches")
+    print(f"offloaded {w.name}: {n} sampled elements, {mism} bit mismatches")
     assert mism == 0
 
 
@@ -730,15 +730,16 @@ def test_register_loads_small_case_full_parity(name):
 
 
 def test_register_loads_config0_full_parity():
-    mism = _run_full(W.workload(0), options=LDG)
-    print(f"configs[0], register loads: {mism} bit mismatches (within tolerance)")
+    w = W.workload(0)
+    mism = _run_full(w, options=LDG)
+    print(f"{w.name}, register loads: {mism} bit mismatches (within tolerance)")
 
 
 @pytest.mark.parametrize("i", [1, 2, 3, 4])
 def test_register_loads_config_sampled(i):
     w = W.workload(i)
     n, mism = _run_sampled(w, bound=(0, w.n_d - 1) if i == 4 else None, options=LDG)
-    print(f"configs[{i}], register loads: {n} sampled elements, {mism} bit mismatches")
+    print(f"{w.name}, register loads: {n} sampled elements, {mism} bit mismatches")
 
 
 @pytest.mark.parametrize("name", list(CLIP_CASES))

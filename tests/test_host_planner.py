@@ -95,7 +95,7 @@ def test_tables_match_oracle_workloads(i):
 
 
 def test_workload_shapes_in_planner():
-    # configs 2-4: all shards a multiple of 8 elements (vector phase 0 everywhere)
+    # GPT-2, 1.3B and Llama shapes: all shards a multiple of 8 elements (vector phase 0 everywhere)
     for i in (2, 3, 4):
         w = W.workload(i)
         plan = _plan_for(w.sizes, w.n_d, w.stage, w.bucket_elems, w.unit_first or None)
