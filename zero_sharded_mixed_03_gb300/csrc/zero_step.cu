@@ -1221,31 +1221,38 @@ int optin_smem(int dev)
     return cache[dev];
 }
 
-// Launch the bulk-staged kernel.  The dynamic shared-memory attribute and the occupancy are
-// set / queried when the ring size changes (host calls only; none inside a graph capture
-// once a step of the same geometry has run).
+// Launch the bulk-staged kernel.  The kernel's dynamic shared-memory limit only ever grows
+// (so a launch of another plan on another thread never finds it below its own ring), and
+// the blocks per SM are queried once per ring size; both are host calls.
 template <int DT, int MODE, typename PT>
 cudaError_t launch_bulk_mode(int dev, PT& P, const BulkCfg& B, cudaStream_t st)
 {
     static std::mutex mu;
-    static int64_t set_bytes[64] = {0};
-    static int per_sm_at[64] = {0};
+    static int64_t limit_set[64] = {0};
+    static std::unordered_map<int64_t, int> per_sm_of[64];
     auto kernel = bulk_step_kernel<DT, MODE, PT>;
     const int64_t smem = bulk_smem_bytes(B.tile, B.stages, P.n_d);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int per_sm = 1;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (set_bytes[dev] != smem) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (limit_set[dev] < smem) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, (size_t)smem);
-            if (e != cudaSuccess) return e;
-            per_sm_at[dev] = std::max(n, 1);
-            set_bytes[dev] = smem;
+            limit_set[dev] = smem;
         }
-        per_sm = per_sm_at[dev];
+        const auto it = per_sm_of[dev].find(smem);
+        if (it != per_sm_of[dev].end()) {
+            per_sm = it->second;
+        } else {
+            int n = 0;
+            const cudaError_t e =
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, (size_t)smem);
+            if (e != cudaSuccess) return e;
+            per_sm = std::max(n, 1);
+            per_sm_of[dev].emplace(smem, per_sm);
+        }
     }
     P.tile = B.tile;
     P.stages = B.stages;
