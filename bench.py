@@ -247,7 +247,7 @@ class Bench:
 
     def _count_launches(self):
         """Kernel launches per step, from the plan's work items: one launch per 32 items (256
-        when a call has more than 32), per call; gathers copy 32 shards per launch."""
+        when a call has more than 32), per call; gathers likewise per copied shard or chunk."""
         def launches(items):
             return 0 if items == 0 else (1 if items <= 32 else -(-items // 256))
         bound = set(self.bound)
@@ -267,7 +267,7 @@ class Bench:
                 copies = 0
             all_items += items if w.stage == 3 else 0
             fused.append(launches(items))
-            gathers.append(-(-copies // 32))
+            gathers.append(launches(copies))
         if w.stage != 3:
             all_items = len(bound)
         self.fused_launches, self.gather_launches = fused, gathers

@@ -130,11 +130,15 @@ struct CopySeg {
     int32_t head, tail;
 };
 
-struct CopyParams {
-    CopySeg seg[kMaxSegs];
+template <int MS>
+struct CopyParamsT {
+    CopySeg seg[MS];
     int n_seg;
     int64_t total_vec;
 };
+// 32 copies (1.5 KB), or 256 (12 KB) for gathers of many chunks (per-parameter plans)
+using CopyParams = CopyParamsT<kMaxSegs>;
+using CopyParamsWide = CopyParamsT<kWideSegs>;
 
 // ------------------------------------------------------------------ element helpers
 
@@ -1008,8 +1012,8 @@ __global__ void commit_kernel(const CommitParams C)
 
 // ------------------------------------------------------------------ gather kernel (stage 3)
 
-template <int VEC>
-__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ CopyParams P)
+template <int VEC, typename CP>
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ CP P)
 {
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -1023,8 +1027,22 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
             if (e >= 0) S.dst[e] = S.src[e];
         }
     }
-    int s = 0;
-    for (int64_t vi = tid; vi < P.total_vec; vi += stride) {
+    // Body: block b copies one contiguous range of vectors, its threads striding by the block
+    // size, so that a thread's walk over the copy list (up to 256 items) starts with a binary
+    // search and then advances at most a few items.
+    const int64_t per = ((P.total_vec + gridDim.x - 1) / gridDim.x + blockDim.x - 1) / blockDim.x *
+                        blockDim.x;
+    const int64_t v0 = (int64_t)blockIdx.x * per + threadIdx.x;
+    const int64_t v_end = min(P.total_vec, ((int64_t)blockIdx.x + 1) * per);
+    if (v0 >= v_end) return;
+    int lo = 0, hi = P.n_seg - 1;   // last item whose first vector is at or before v0
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (P.seg[mid].vbeg <= v0) lo = mid;
+        else hi = mid - 1;
+    }
+    int s = lo;
+    for (int64_t vi = v0; vi < v_end; vi += blockDim.x) {
         while (vi >= P.seg[s].vbeg + P.seg[s].nvec) ++s;
         const CopySeg& S = P.seg[s];
         if constexpr (VEC == 8) {
@@ -1321,6 +1339,54 @@ cudaError_t launch_recast(int dev, PT& P, bool vec, cudaStream_t st)
     if (vec) recast_kernel<DT, 8, PT><<<grid, kThreads, 0, st>>>(P);
     else recast_kernel<DT, 1, PT><<<grid, kThreads, 0, st>>>(P);
     return cudaGetLastError();
+}
+
+// One copy of a gather: a rank's 16-bit shard (or chunk) into the unit's full buffer.
+struct Copy {
+    const uint16_t* src;
+    uint16_t* dst;
+    int64_t n;
+};
+
+// Launch gather_kernel over `copies`, CP::seg's capacity at a time.
+template <typename CP>
+cudaError_t launch_gathers(int dev, const std::vector<Copy>& copies, CP& P, cudaStream_t s)
+{
+    const size_t cap = sizeof(P.seg) / sizeof(P.seg[0]);
+    for (size_t c0 = 0; c0 < copies.size(); c0 += cap) {
+        std::memset(&P, 0, sizeof(P));
+        bool vec = true;
+        const size_t c1 = std::min(copies.size(), c0 + cap);
+        P.n_seg = (int)(c1 - c0);
+        for (size_t i = c0; i < c1; ++i) {
+            CopySeg& K = P.seg[i - c0];
+            K.src = copies[i].src;
+            K.dst = copies[i].dst;
+            K.n = copies[i].n;
+            const int h = head16(K.dst);
+            vec &= head16(K.src) == h;
+            K.head = (int32_t)std::min<int64_t>(h, K.n);
+            K.nvec = (K.n - K.head) / 8;
+            K.tail = (int32_t)(K.n - K.head - 8 * K.nvec);
+        }
+        int64_t acc = 0;
+        for (int i = 0; i < P.n_seg; ++i) {
+            CopySeg& K = P.seg[i];
+            if (!vec) {
+                K.head = K.tail = 0;
+                K.nvec = K.n;
+            }
+            K.vbeg = acc;
+            acc += K.nvec;
+        }
+        P.total_vec = acc;
+        const int64_t work = std::max<int64_t>(acc, (int64_t)P.n_seg * kScalarSlots);
+        if (vec) gather_kernel<8, CP><<<grid_for(gather_kernel<8, CP>, dev, work), kThreads, 0, s>>>(P);
+        else gather_kernel<1, CP><<<grid_for(gather_kernel<1, CP>, dev, work), kThreads, 0, s>>>(P);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 zero_status_t set_device(const zero_plan* p)
@@ -1835,7 +1901,6 @@ zero_status_t zero_gather_layer(zero_plan_t* p, int64_t unit, void* full_unit16,
     if (st != ZERO_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     // copy list: (source in a rank's 16-bit shard, destination in the unit, length)
-    struct Copy { const uint16_t* src; uint16_t* dst; int64_t n; };
     std::vector<Copy> copies;
     if (p->per_param) {
         for (const Chunk& c : p->chunks)
@@ -1847,40 +1912,16 @@ zero_status_t zero_gather_layer(zero_plan_t* p, int64_t unit, void* full_unit16,
             copies.push_back({p->ranks[(size_t)r].shard16 + p->phys_off[(size_t)r][(size_t)unit],
                               (uint16_t*)full_unit16 + r * U.shard, U.shard});
     }
-    for (size_t c0 = 0; c0 < copies.size(); c0 += kMaxSegs) {
+    // one launch per 32 copies, or per 256 with the wide parameter block
+    cudaError_t gerr;
+    if (copies.size() > (size_t)kMaxSegs) {
+        CopyParamsWide P;
+        gerr = launch_gathers(p->device, copies, P, s);
+    } else {
         CopyParams P;
-        std::memset(&P, 0, sizeof(P));
-        bool vec = true;
-        const size_t c1 = std::min(copies.size(), c0 + kMaxSegs);
-        P.n_seg = (int)(c1 - c0);
-        for (size_t i = c0; i < c1; ++i) {
-            CopySeg& K = P.seg[i - c0];
-            K.src = copies[i].src;
-            K.dst = copies[i].dst;
-            K.n = copies[i].n;
-            const int h = head16(K.dst);
-            vec &= head16(K.src) == h;
-            K.head = (int32_t)std::min<int64_t>(h, K.n);
-            K.nvec = (K.n - K.head) / 8;
-            K.tail = (int32_t)(K.n - K.head - 8 * K.nvec);
-        }
-        int64_t acc = 0;
-        for (int i = 0; i < P.n_seg; ++i) {
-            CopySeg& K = P.seg[i];
-            if (!vec) {
-                K.head = K.tail = 0;
-                K.nvec = K.n;
-            }
-            K.vbeg = acc;
-            acc += K.nvec;
-        }
-        P.total_vec = acc;
-        const int64_t work = std::max<int64_t>(acc, (int64_t)P.n_seg * kScalarSlots);
-        if (vec) gather_kernel<8><<<grid_for(gather_kernel<8>, p->device, work), kThreads, 0, s>>>(P);
-        else gather_kernel<1><<<grid_for(gather_kernel<1>, p->device, work), kThreads, 0, s>>>(P);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+        gerr = launch_gathers(p->device, copies, P, s);
     }
+    if (gerr != cudaSuccess) return cuda_fail(gerr, "gather launch");
     p->gathered[(size_t)unit] = 1;
     return ZERO_OK;
 }
