@@ -38,8 +38,8 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_step.cu); reported as null once that source
 # changes.  Captures: profiles/*_ncu_full.md.
-MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("eedf4bf9956eab41", 2_288_748_800),
-                    (1, "fused_step_kernel"): ("eedf4bf9956eab41", 2_301_400_576)}
+MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("f8c082fe2d297b5b", 2_288_816_640),
+                    (1, "fused_step_kernel"): ("f8c082fe2d297b5b", 2_303_844_864)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_step.cu")
 
 
