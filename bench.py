@@ -26,7 +26,7 @@ sys.path.insert(0, ROOT)
 METRIC = "ZeRO step params updated/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "params/s"
 DEFAULT_CONFIG = 1
-DEFAULT_STAGING = "bulk"
+DEFAULT_STAGING = "auto"
 FALLBACK_HBM_GBS = 6800.0
 # Gradient sets rotated through the timed steps.  A backward pass rewrites the same gradient
 # buffers every step, so a few persistent sets model training; each step still reads inputs
@@ -75,9 +75,10 @@ def parse_args():
     ap.add_argument("--overlap", action="store_true",
                     help="stage 3: gather unit u+1 on a second stream while unit u steps "
                          "(zero_step_units_overlapped); no per-launch events in this mode")
-    ap.add_argument("--staging", choices=["ldg", "bulk"], default=DEFAULT_STAGING,
-                    help="bulk (default): cp.async.bulk (TMA) staging of the contribution and "
-                         "state tiles into shared memory; ldg: 128-bit register loads")
+    ap.add_argument("--staging", choices=["auto", "ldg", "bulk"], default=DEFAULT_STAGING,
+                    help="bulk: cp.async.bulk (TMA) staging of the contribution and state tiles "
+                         "into shared memory; ldg: 128-bit register loads; auto (default): the "
+                         "library's choice (staged where its residency pays off)")
     ap.add_argument("--bulk-tile", type=int, default=0, help="bulk staging: elements per tile")
     ap.add_argument("--bulk-stages", type=int, default=0, help="bulk staging: ring depth")
     ap.add_argument("--grad-norm", choices=["off", "report", "clip"], default="off",
@@ -346,10 +347,10 @@ def gpu_arm(args, world, rank, local):
         import dataclasses
         w = dataclasses.replace(w, offload=True)
     Z = importlib.import_module("zero_sharded_mixed_03_gb300")
-    options = {Z.ZERO_OPT_STAGING: 0}
-    if args.staging == "bulk":
-        options = {Z.ZERO_OPT_STAGING: 1, Z.ZERO_OPT_BULK_TILE: args.bulk_tile,
-                   Z.ZERO_OPT_BULK_STAGES: args.bulk_stages}
+    staging = {"ldg": Z.ZERO_STAGING_REGISTER_LOADS, "bulk": Z.ZERO_STAGING_BULK,
+               "auto": Z.ZERO_STAGING_AUTO}[args.staging]
+    options = {Z.ZERO_OPT_STAGING: staging, Z.ZERO_OPT_BULK_TILE: args.bulk_tile,
+               Z.ZERO_OPT_BULK_STAGES: args.bulk_stages}
     b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm,
               options)
     peak, peak_kind = peaks()
@@ -439,9 +440,10 @@ def gpu_arm(args, world, rank, local):
     launch_bytes = per_launch_elems * b.bytes_per_elem
     avg_fused_s = statistics.mean(fused_ms) / 1e3 if fused_ms else float("nan")
     achieved = launch_bytes / avg_fused_s / 1e9
-    # norm-report steps run the register-load kernel whatever the staging option
-    bulk = args.staging == "bulk" and args.grad_norm != "report"
-    kernel = "bulk_step_kernel" if bulk else "fused_step_kernel"
+    # the step kernel the library launched (the staging option, the residency rule of the
+    # automatic choice, norm-report steps)
+    last = Z.zero_get_option(b.g.plan, Z.ZERO_OPT_LAST_STEP_KERNEL)
+    kernel = "bulk_step_kernel" if last == 1 else "fused_step_kernel"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config, kernel),
                 "peak_source": peak_kind, "kernel": kernel,

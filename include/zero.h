@@ -37,9 +37,8 @@
  *    for the state layout below when bucket_elems is a multiple of 8); other
  *    launches use the scalar path of the same kernel.
  *  - Kernels never trap or assert.  The only waits are those of the bulk-staged step kernel
- *    (the default; zero_set_option, ZERO_OPT_STAGING) on its shared-memory barriers; each is
- *    bounded in time (ZERO_OPT_WAIT_LIMIT_NS) and one that runs out is reported as
- *    ZERO_ETIMEOUT.
+ *    (zero_set_option, ZERO_OPT_STAGING) on its shared-memory barriers; each is bounded in
+ *    time (ZERO_OPT_WAIT_LIMIT_NS) and one that runs out is reported as ZERO_ETIMEOUT.
  */
 #ifndef ZERO_H
 #define ZERO_H
@@ -267,15 +266,20 @@ zero_status_t zero_step_finish(zero_plan_t* plan, void* stream, zero_step_result
 zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_t* out);
 
 /* Execution options of a plan (not inside an open step; values are checked here):
- *   ZERO_OPT_STAGING        1 (default): per block a producer warp stages the contribution
- *                           slices and the fp32 state tile by tile into a ring of shared-memory
- *                           buffers with 1-D cp.async.bulk copies (the TMA engine) completing on
- *                           mbarriers, and four consumer warps reduce and update from shared
- *                           memory.  0: every thread loads them with 128-bit register loads.
- *                           Both give identical results, bit for bit.  Launches whose streams
- *                           do not share one 16-byte phase use the scalar register-load path
- *                           either way, and so do steps that report the gradient norm from the
- *                           fused pass (ZERO_REPORT_GRAD_NORM without clipping).
+ *   ZERO_OPT_STAGING        which step kernel zero_step launches.  ZERO_STAGING_BULK: per block
+ *                           a producer warp stages the contribution slices and the fp32 state
+ *                           tile by tile into a ring of shared-memory buffers with 1-D
+ *                           cp.async.bulk copies (the TMA engine) completing on mbarriers, and
+ *                           four consumer warps reduce and update from shared memory.
+ *                           ZERO_STAGING_REGISTER_LOADS: every thread loads them with 128-bit
+ *                           register loads.  ZERO_STAGING_AUTO (default): the staged kernel where
+ *                           its ring gives two resident blocks per SM, or three with 512-element
+ *                           tiles (measured faster there on GB300: N_d = 4-5, 7-9, 13-16, 22-47
+ *                           with the default geometry), register loads elsewhere.  All give
+ *                           identical results, bit for bit.  Launches whose streams do not
+ *                           share one 16-byte phase use the scalar register-load path either
+ *                           way, and so do steps that report the gradient norm from the fused
+ *                           pass (ZERO_REPORT_GRAD_NORM without clipping).
  *   ZERO_OPT_WAIT_LIMIT_NS  bound on each barrier wait of the bulk-staged kernel, in ns of
  *                           %globaltimer (default 1e9; 0 gives up at the first wait that does
  *                           not succeed at once).  A wait that runs out sets the plan's error
@@ -289,9 +293,15 @@ enum {
     ZERO_OPT_STAGING = 0,
     ZERO_OPT_WAIT_LIMIT_NS = 1,
     ZERO_OPT_BULK_TILE = 2,
-    ZERO_OPT_BULK_STAGES = 3
+    ZERO_OPT_BULK_STAGES = 3,
+    ZERO_OPT_LAST_STEP_KERNEL = 4   /* read only: the step kernel of the last zero_step launch
+                                       (1 staged, 0 register loads, -1 none yet) */
 };
+enum { ZERO_STAGING_REGISTER_LOADS = 0, ZERO_STAGING_BULK = 1, ZERO_STAGING_AUTO = 2 };
 zero_status_t zero_set_option(zero_plan_t* plan, int option, int64_t value);
+
+/* Read an option (the tile and stages in effect when left at 0), or ZERO_OPT_LAST_STEP_KERNEL. */
+zero_status_t zero_get_option(const zero_plan_t* plan, int option, int64_t* value);
 
 /* Overwrite the device-resident step state, e.g. when resuming from a checkpoint whose fp32
  * master/m/v were saved from the half `in->current` after `in->t` applied steps.  Clears the

@@ -716,12 +716,30 @@ def test_step_captured_in_a_cuda_graph(name, staging):
 
 
 # ---------------------------------------------------------------------- the two step kernels
-# The cases above run the default, bulk-staged kernel (cp.async.bulk into shared memory); the
-# register-load kernel re-runs them here, and the bulk kernel's own geometry, bit identity and
-# timeout tests follow.
+# The cases above run the default choice (the staged kernel where its residency pays off); the
+# register-load kernel re-runs them here, and the staged kernel's own tests (forced on) follow.
 
-BULK = {Z.ZERO_OPT_STAGING: 1}
-LDG = {Z.ZERO_OPT_STAGING: 0}
+BULK = {Z.ZERO_OPT_STAGING: Z.ZERO_STAGING_BULK}
+LDG = {Z.ZERO_OPT_STAGING: Z.ZERO_STAGING_REGISTER_LOADS}
+
+
+@pytest.mark.parametrize("n_d,staged", [(7, 1), (8, 1), (12, 0), (16, 1), (24, 1), (64, 0)])
+def test_automatic_kernel_choice(n_d, staged):
+    """The default (ZERO_STAGING_AUTO) launches the staged kernel where its ring gives two blocks
+    per SM (or three of 512-element tiles) on GB300's 228 KB of shared memory per SM, register
+    loads elsewhere; either way the step matches the oracle."""
+    w = _mk(180 + n_d, _ragged(40 + n_d, 20, 30000), n_d, 2, steps=1)
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    try:
+        assert Z.zero_get_option(run.g.plan, Z.ZERO_OPT_STAGING) == Z.ZERO_STAGING_AUTO
+        assert Z.zero_get_option(run.g.plan, Z.ZERO_OPT_LAST_STEP_KERNEL) == -1
+        run.step(1)
+        o.step(1)
+        assert Z.zero_get_option(run.g.plan, Z.ZERO_OPT_LAST_STEP_KERNEL) == staged
+        _compare_full(run, o, f"automatic choice, N_d = {n_d}")
+    finally:
+        run.close()
 
 
 @pytest.mark.parametrize("name", list(SMALL_CASES))
@@ -755,6 +773,21 @@ def test_register_loads_per_param_full_parity(name):
 
 def test_register_loads_overlapped_schedule():
     _run_overlap(OVERLAP_CASES["z3_nd16_units"], "register loads z3_nd16_units", options=LDG)
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_bulk_staging_small_case_full_parity(name):
+    _run_full(SMALL_CASES[name], options=BULK)
+
+
+@pytest.mark.parametrize("name", list(CLIP_CASES))
+def test_bulk_staging_norm_and_clipping(name):
+    _run_clip(name, options=BULK)
+
+
+@pytest.mark.parametrize("name", list(PP_CASES))
+def test_bulk_staging_per_param_full_parity(name):
+    _run_full(PP_CASES[name], options=BULK)
 
 
 @pytest.mark.parametrize("name,tile,stages", [

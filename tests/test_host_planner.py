@@ -168,19 +168,27 @@ def test_calls_out_of_order_fail_without_touching_the_gpu():
 
 
 def test_execution_options_are_checked_on_the_host():
-    """zero_set_option: values outside their ranges give EINVAL; a staging ring (stages x tile x
-    (2 N_d + 12) bytes + 256 bytes of barriers) beyond one block's 227 KB of shared memory gives
-    ERANGE and leaves the earlier geometry in place."""
+    """zero_set_option / zero_get_option: defaults, values outside their ranges give EINVAL; a
+    staging ring (stages x tile x (2 N_d + 12) bytes + 384 bytes) beyond one block's 227 KB of
+    shared memory gives ERANGE and leaves the earlier geometry in place."""
     plan = _plan_for([10, 20], 7, 2, 8)
     try:
-        for opt, val in ((Z.ZERO_OPT_STAGING, 2), (Z.ZERO_OPT_STAGING, -1),
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_STAGING) == Z.ZERO_STAGING_AUTO
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_WAIT_LIMIT_NS) == 1_000_000_000
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_BULK_TILE) == 1536      # 1536 x 26 B <= 45 KB
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_BULK_STAGES) == 2
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_LAST_STEP_KERNEL) == -1
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_get_option(plan, 9)
+        assert e.value.status == Z.ZERO_EINVAL
+        for opt, val in ((Z.ZERO_OPT_STAGING, 3), (Z.ZERO_OPT_STAGING, -1),
                          (Z.ZERO_OPT_WAIT_LIMIT_NS, -1), (Z.ZERO_OPT_BULK_TILE, 12),
                          (Z.ZERO_OPT_BULK_TILE, 16384), (Z.ZERO_OPT_BULK_TILE, 4),
                          (Z.ZERO_OPT_BULK_STAGES, 1), (Z.ZERO_OPT_BULK_STAGES, 17), (9, 0)):
             with pytest.raises(Z.ZeroError) as e:
                 Z.zero_set_option(plan, opt, val)
             assert e.value.status == Z.ZERO_EINVAL, (opt, val)
-        for opt, val in ((Z.ZERO_OPT_STAGING, 1), (Z.ZERO_OPT_STAGING, 0),
+        for opt, val in ((Z.ZERO_OPT_STAGING, 1), (Z.ZERO_OPT_STAGING, 2), (Z.ZERO_OPT_STAGING, 0),
                          (Z.ZERO_OPT_WAIT_LIMIT_NS, 0), (Z.ZERO_OPT_BULK_TILE, 4096),
                          (Z.ZERO_OPT_BULK_TILE, 1024), (Z.ZERO_OPT_BULK_STAGES, 8)):
             Z.zero_set_option(plan, opt, val)

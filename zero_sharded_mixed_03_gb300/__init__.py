@@ -19,7 +19,9 @@ ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ESTATE, ZERO_ERANGE, ZERO_ET
 ZERO_BF16, ZERO_FP16 = 0, 1
 ZERO_MAX_RANKS = 128
 ZERO_REPORT_GRAD_NORM = 1
-ZERO_OPT_STAGING, ZERO_OPT_WAIT_LIMIT_NS, ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES = range(4)
+(ZERO_OPT_STAGING, ZERO_OPT_WAIT_LIMIT_NS, ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES,
+ ZERO_OPT_LAST_STEP_KERNEL) = range(5)
+ZERO_STAGING_REGISTER_LOADS, ZERO_STAGING_BULK, ZERO_STAGING_AUTO = range(3)
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)
 TABLE_COLS = {0: 1, 1: 7, 2: 6, 3: 5, 4: 4, 5: 10}
@@ -31,7 +33,7 @@ EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", 
             "zero_release_layer", "zero_memory_report", "zero_comm_report", "zero_set_scaler",
             "zero_read_state", "zero_restore_state", "zero_grad_norm",
             "zero_step_units_overlapped", "zero_bind_offload", "zero_offload_step",
-            "zero_offload_finish", "zero_set_option",
+            "zero_offload_finish", "zero_set_option", "zero_get_option",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
@@ -139,6 +141,8 @@ def lib() -> ctypes.CDLL:
         L.zero_grad_norm.argtypes = [_vp, _vp, _i64, _i64, _vp]
         L.zero_set_option.restype = st
         L.zero_set_option.argtypes = [_vp, _int, _i64]
+        L.zero_get_option.restype = st
+        L.zero_get_option.argtypes = [_vp, _int, ctypes.POINTER(_i64)]
         L.zero_restore_state.restype = st
         L.zero_restore_state.argtypes = [_vp, ctypes.POINTER(zero_step_result_t), _vp]
         L.zero_gather_layer.restype = st
@@ -307,9 +311,16 @@ def zero_read_state(plan: int, stream: int = 0) -> zero_step_result_t:
 
 
 def zero_set_option(plan: int, option: int, value: int) -> None:
-    """ZERO_OPT_STAGING (0 register loads, 1 cp.async.bulk staging), ZERO_OPT_WAIT_LIMIT_NS,
+    """ZERO_OPT_STAGING (ZERO_STAGING_REGISTER_LOADS / _BULK / _AUTO), ZERO_OPT_WAIT_LIMIT_NS,
     ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES (0 = chosen from N_d)."""
     _check(lib().zero_set_option(plan, option, int(value)))
+
+
+def zero_get_option(plan: int, option: int) -> int:
+    """An option's value in effect, or ZERO_OPT_LAST_STEP_KERNEL (1 staged, 0 register loads)."""
+    v = _i64()
+    _check(lib().zero_get_option(plan, option, ctypes.byref(v)))
+    return v.value
 
 
 def zero_gather_layer(plan: int, unit: int, full_unit16: int, stream: int = 0) -> None:

@@ -130,10 +130,11 @@ struct zero_plan {
     double bias_beta1 = -1.0, bias_beta2 = -1.0;
     std::vector<char> gathered;         // stage 3: per unit
     // Execution options (zero_set_option).
-    int staging = 1;                    // 1: cp.async.bulk staging of the fused step; 0: register loads
+    int staging = ZERO_STAGING_AUTO;    // ZERO_STAGING_*: which step kernel zero_step launches
     int64_t wait_limit_ns = 1000000000; // bound on each barrier wait of the staged kernel
     int64_t bulk_tile = 0;              // elements per staged tile (0: chosen from N_d)
     int bulk_stages = 0;                // ring depth (0: chosen from the tile)
+    int last_step_kernel = -1;          // last zero_step launch: 1 staged, 0 register loads
     // Overlapped stage-3 schedule: CUDA events (created on first use, released by
     // zero_plan_destroy through the hook the device side installs).
     void* ov_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};

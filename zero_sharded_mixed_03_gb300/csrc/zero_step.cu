@@ -1185,12 +1185,25 @@ void launch_fused_mode(int dev, const PT& P, bool vec, int64_t work, cudaStream_
     else launch_grid(fused_step_kernel<DT, kRankBatch, 8, MODE, PT>, dev, work, P, st);
 }
 
-// Geometry of the bulk-staged kernel (tile == 0: register-load kernel).
+// Geometry of the bulk-staged kernel (tile == 0: register-load kernel).  automatic: launch
+// it only where its residency pays off (bulk_pays_off), else the register-load kernel.
 struct BulkCfg {
     int tile = 0;
     int stages = 0;
     uint64_t wait_ns = 0;
+    bool automatic = false;
 };
+
+// Where the staged kernel beats register loads, from a sweep of N_d = 1 .. 64 on GB300 (ragged
+// ZeRO-2 step, default geometry): with exactly two blocks per SM (8 consumer warps, 75-110 KB
+// rings) it won at every N_d but 9 and 33 (by 1-5 %); with three blocks of 512-element tiles
+// (N_d 22-30) it won by 2-6 %; three blocks of 1,024-2,048-element tiles (N_d 1-3, 6, 10-12)
+// lost 7-14 %, four blocks (N_d 17-21, 48) lost up to 4 % or won up to 4 %, and tiles below
+// 512 elements (N_d >= 49) lost 20 % and more.
+bool bulk_pays_off(int blocks_per_sm, int tile)
+{
+    return blocks_per_sm == 2 || (blocks_per_sm == 3 && tile == 512);
+}
 
 // Dynamic shared memory of one block: alignment slack, barriers, the ring.
 int64_t bulk_smem_bytes(int64_t tile, int64_t stages, int64_t n_d)
@@ -1218,10 +1231,11 @@ int auto_bulk_stages(int /*tile*/, int /*n_d*/) { return 2; }
 BulkCfg bulk_config(const zero_plan* p)
 {
     BulkCfg b;
-    if (!p->staging) return b;
+    if (p->staging == ZERO_STAGING_REGISTER_LOADS) return b;
     b.tile = p->bulk_tile > 0 ? (int)p->bulk_tile : auto_bulk_tile(p->n_d);
     b.stages = p->bulk_stages > 0 ? p->bulk_stages : auto_bulk_stages(b.tile, p->n_d);
     b.wait_ns = (uint64_t)p->wait_limit_ns;
+    b.automatic = p->staging == ZERO_STAGING_AUTO;
     return b;
 }
 
@@ -1239,39 +1253,44 @@ int optin_smem(int dev)
     return cache[dev];
 }
 
-// Launch the bulk-staged kernel.  The kernel's dynamic shared-memory limit only ever grows
-// (so a launch of another plan on another thread never finds it below its own ring), and
-// the blocks per SM are queried once per ring size; both are host calls.
+// Blocks per SM of the bulk-staged kernel with `smem` bytes of ring.  The kernel's dynamic
+// shared-memory limit only ever grows (so a launch of another plan on another thread never
+// finds it below its own ring), and the residency is queried once per ring size; both are
+// host calls.
 template <int DT, int MODE, typename PT>
-cudaError_t launch_bulk_mode(int dev, PT& P, const BulkCfg& B, cudaStream_t st)
+cudaError_t bulk_residency(int dev, int64_t smem, int* per_sm)
 {
     static std::mutex mu;
     static int64_t limit_set[64] = {0};
     static std::unordered_map<int64_t, int> per_sm_of[64];
     auto kernel = bulk_step_kernel<DT, MODE, PT>;
-    const int64_t smem = bulk_smem_bytes(B.tile, B.stages, P.n_d);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int per_sm = 1;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (limit_set[dev] < smem) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            limit_set[dev] = smem;
-        }
-        const auto it = per_sm_of[dev].find(smem);
-        if (it != per_sm_of[dev].end()) {
-            per_sm = it->second;
-        } else {
-            int n = 0;
-            const cudaError_t e =
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, (size_t)smem);
-            if (e != cudaSuccess) return e;
-            per_sm = std::max(n, 1);
-            per_sm_of[dev].emplace(smem, per_sm);
-        }
+    std::lock_guard<std::mutex> lock(mu);
+    if (limit_set[dev] < smem) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        limit_set[dev] = smem;
     }
+    const auto it = per_sm_of[dev].find(smem);
+    if (it != per_sm_of[dev].end()) {
+        *per_sm = it->second;
+        return cudaSuccess;
+    }
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, (size_t)smem);
+    if (e != cudaSuccess) return e;
+    *per_sm = std::max(n, 1);
+    per_sm_of[dev].emplace(smem, *per_sm);
+    return cudaSuccess;
+}
+
+// Launch the bulk-staged kernel with `per_sm` resident blocks per SM.
+template <int DT, int MODE, typename PT>
+cudaError_t launch_bulk_mode(int dev, PT& P, const BulkCfg& B, int per_sm, cudaStream_t st)
+{
+    auto kernel = bulk_step_kernel<DT, MODE, PT>;
+    const int64_t smem = bulk_smem_bytes(B.tile, B.stages, P.n_d);
     P.tile = B.tile;
     P.stages = B.stages;
     P.wait_ns = B.wait_ns;
@@ -1287,17 +1306,27 @@ cudaError_t launch_bulk_mode(int dev, PT& P, const BulkCfg& B, cudaStream_t st)
     return cudaGetLastError();
 }
 
+// *used (when given): 1 if the bulk-staged kernel was launched, 0 for register loads.
 template <int DT, typename PT>
 cudaError_t launch_fused(int dev, PT& P, bool vec, cudaStream_t st, int mode = kPlain,
-                         const BulkCfg* bulk = nullptr)
+                         const BulkCfg* bulk = nullptr, int* used = nullptr)
 {
+    if (used) *used = 0;
     finalize_vectors(P, vec);
     // Norm-report steps keep the register-load kernel: the per-element norm accumulation is a
     // serial chain per thread, which the bulk kernel's few consumer warps do not hide
     // (ragged N_d = 7 workload on GB300: 367 us against 353 us).
     if (bulk && bulk->tile > 0 && vec && P.st && mode != kNormAcc) {
-        if (mode == kClip) return launch_bulk_mode<DT, kClip>(dev, P, *bulk, st);
-        return launch_bulk_mode<DT, kPlain>(dev, P, *bulk, st);
+        const int64_t smem = bulk_smem_bytes(bulk->tile, bulk->stages, P.n_d);
+        int per_sm = 0;
+        const cudaError_t e = mode == kClip ? bulk_residency<DT, kClip, PT>(dev, smem, &per_sm)
+                                            : bulk_residency<DT, kPlain, PT>(dev, smem, &per_sm);
+        if (e != cudaSuccess) return e;
+        if (!bulk->automatic || bulk_pays_off(per_sm, bulk->tile)) {
+            if (used) *used = 1;
+            if (mode == kClip) return launch_bulk_mode<DT, kClip>(dev, P, *bulk, per_sm, st);
+            return launch_bulk_mode<DT, kPlain>(dev, P, *bulk, per_sm, st);
+        }
     }
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     if (mode == kNormAcc) launch_fused_mode<DT, kNormAcc>(dev, P, vec, work, st);
@@ -1646,7 +1675,9 @@ zero_status_t zero_set_option(zero_plan_t* p, int option, int64_t value)
     int64_t tile = p->bulk_tile, stages = p->bulk_stages;
     switch (option) {
     case ZERO_OPT_STAGING:
-        if (value != 0 && value != 1) return fail(ZERO_EINVAL, "zero_set_option: staging must be 0 or 1");
+        if (value != ZERO_STAGING_REGISTER_LOADS && value != ZERO_STAGING_BULK &&
+            value != ZERO_STAGING_AUTO)
+            return fail(ZERO_EINVAL, "zero_set_option: staging must be 0, 1 or 2");
         p->staging = (int)value;
         return ZERO_OK;
     case ZERO_OPT_WAIT_LIMIT_NS:
@@ -1677,6 +1708,22 @@ zero_status_t zero_set_option(zero_plan_t* p, int option, int64_t value)
     p->bulk_tile = tile;
     p->bulk_stages = (int)stages;
     return ZERO_OK;
+}
+
+zero_status_t zero_get_option(const zero_plan_t* p, int option, int64_t* value)
+{
+    if (!p || !value) return fail(ZERO_EINVAL, "zero_get_option: NULL argument");
+    switch (option) {
+    case ZERO_OPT_STAGING: *value = p->staging; return ZERO_OK;
+    case ZERO_OPT_WAIT_LIMIT_NS: *value = p->wait_limit_ns; return ZERO_OK;
+    case ZERO_OPT_BULK_TILE: *value = p->bulk_tile > 0 ? p->bulk_tile : auto_bulk_tile(p->n_d); return ZERO_OK;
+    case ZERO_OPT_BULK_STAGES:
+        *value = p->bulk_stages > 0 ? p->bulk_stages
+                                    : auto_bulk_stages((int)(p->bulk_tile > 0 ? p->bulk_tile : auto_bulk_tile(p->n_d)), p->n_d);
+        return ZERO_OK;
+    case ZERO_OPT_LAST_STEP_KERNEL: *value = p->last_step_kernel; return ZERO_OK;
+    default: return fail(ZERO_EINVAL, "zero_get_option: unknown option");
+    }
 }
 
 zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
@@ -1769,9 +1816,11 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
             fill_call_params(p, grad_contribs, P);
             P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
             const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
+            int used = 0;
             const cudaError_t err = p->dtype16 == ZERO_BF16
-                                        ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode, &bulk)
-                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode, &bulk);
+                                        ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode, &bulk, &used)
+                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode, &bulk, &used);
+            p->last_step_kernel = used;
             if (err != cudaSuccess) return err;
         }
         return cudaSuccess;
