@@ -9,8 +9,9 @@
 // memory over NVLink-C2C; this file updates the state and produces the 16-bit parameters.
 //
 // Built with -O3 -ffp-contract=off: every fp32 operation is separately rounded in the order
-// the GPU kernel uses, so offloaded and on-GPU updates agree bit for bit.  The loops
-// vectorise (IEEE division and square root have vector forms on Arm and x86).
+// the GPU kernel uses, so offloaded and on-GPU updates agree bit for bit.  With
+// -fno-math-errno the loops vectorise (IEEE division and square root have exact vector forms
+// on Arm and x86; errno would only be set for a negative square-root argument, and v >= 0).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -73,6 +74,8 @@ void adamw_span(const CpuSpan& s, const float* k)
     float* __restrict v = s.v;
     const float* __restrict g = s.grad;
     uint16_t* __restrict out = s.out16;
+    // bf16: the cast joins the loop (it still vectorises); the fp16 cast's branches would stop
+    // the whole loop from vectorising, so fp16 takes a second pass
     for (int64_t i = 0; i < s.n; ++i) {
         const float gi = g[i];
         const float mi = b1 * m[i] + omb1 * gi;
@@ -83,8 +86,10 @@ void adamw_span(const CpuSpan& s, const float* k)
         m[i] = mi;
         v[i] = vi;
         p[i] = pi;
+        if constexpr (!FP16) out[i] = to_bf16(pi);
     }
-    for (int64_t i = 0; i < s.n; ++i) out[i] = FP16 ? to_fp16(p[i]) : to_bf16(p[i]);
+    if constexpr (FP16)
+        for (int64_t i = 0; i < s.n; ++i) out[i] = to_fp16(p[i]);
 }
 
 template <bool FP16>
