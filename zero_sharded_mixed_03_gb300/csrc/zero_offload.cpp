@@ -39,28 +39,31 @@ inline uint16_t to_bf16(float f)
     return (uint16_t)(u >> 16);
 }
 
-// fp32 -> IEEE binary16, round to nearest even, subnormals and overflow to infinity included.
+inline float float_of(uint32_t u)
+{
+    float f;
+    std::memcpy(&f, &u, sizeof(f));
+    return f;
+}
+
+// fp32 -> IEEE binary16, round to nearest even, subnormals and overflow to infinity included,
+// without branches (so that loops over it vectorise):
+//  - normal halves: rebias the exponent (subtract 112 << 23) and round the 13 dropped
+//    mantissa bits to nearest even -- a carry into the exponent is the correct result;
+//  - subnormal halves (|f| < 2^-14): |f| + 0.5 puts the half's ulp, 2^-24, at the last place
+//    of the float, so the fp32 addition itself rounds to nearest even; what it added to 0.5
+//    is the half's bit pattern (1024 = the smallest normal);
+//  - |f| rounding past 65504 -> infinity; NaN -> quiet NaN with the sign kept.
 inline uint16_t to_fp16(float f)
 {
     const uint32_t u = bits_of(f);
     const uint32_t sign = (u >> 16) & 0x8000u;
     const uint32_t a = u & 0x7FFFFFFFu;
-    if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);
-    if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);          // rounds past 65504
-    if (a >= 0x38800000u) {                                            // normal binary16
-        const uint32_t mant = a & 0x7FFFFFu;
-        uint32_t h = ((a >> 23) - 112u) << 10 | (mant >> 13);
-        const uint32_t rest = mant & 0x1FFFu;
-        if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;  // may carry into exponent
-        return (uint16_t)(sign | h);
-    }
-    if (a < 0x33000001u) return (uint16_t)sign;                        // below half the least subnormal
-    const uint32_t e = a >> 23;                                         // 102 .. 112
-    const uint32_t m = (a & 0x7FFFFFu) | 0x800000u;
-    const uint32_t shift = 126u - e;                                    // 14 .. 24
-    uint32_t h = m >> shift;
-    const uint32_t rest = m & ((1u << shift) - 1u), halfway = 1u << (shift - 1u);
-    if (rest > halfway || (rest == halfway && (h & 1u))) h += 1u;
+    const uint32_t nrm = (a - 0x38000000u + 0x0FFFu + ((a >> 13) & 1u)) >> 13;
+    const uint32_t sub = bits_of(float_of(a) + 0.5f) - 0x3F000000u;
+    uint32_t h = a >= 0x38800000u ? nrm : sub;
+    h = a >= 0x477FF000u ? 0x7C00u : h;
+    h = a > 0x7F800000u ? 0x7E00u : h;
     return (uint16_t)(sign | h);
 }
 
@@ -74,8 +77,6 @@ void adamw_span(const CpuSpan& s, const float* k)
     float* __restrict v = s.v;
     const float* __restrict g = s.grad;
     uint16_t* __restrict out = s.out16;
-    // bf16: the cast joins the loop (it still vectorises); the fp16 cast's branches would stop
-    // the whole loop from vectorising, so fp16 takes a second pass
     for (int64_t i = 0; i < s.n; ++i) {
         const float gi = g[i];
         const float mi = b1 * m[i] + omb1 * gi;
@@ -86,10 +87,8 @@ void adamw_span(const CpuSpan& s, const float* k)
         m[i] = mi;
         v[i] = vi;
         p[i] = pi;
-        if constexpr (!FP16) out[i] = to_bf16(pi);
+        out[i] = FP16 ? to_fp16(pi) : to_bf16(pi);
     }
-    if constexpr (FP16)
-        for (int64_t i = 0; i < s.n; ++i) out[i] = to_fp16(p[i]);
 }
 
 template <bool FP16>
