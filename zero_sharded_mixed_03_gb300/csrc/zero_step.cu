@@ -1349,6 +1349,7 @@ cudaError_t launch_norm(int dev, PT& P, bool vec, cudaStream_t st)
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     if (!vec) launch_grid(grad_norm_kernel<DT, 1, 1, PT>, dev, work, P, st);
+    else if (P.n_d >= kWideRankBatchFrom) launch_grid(grad_norm_kernel<DT, kWideRankBatch, 8, PT>, dev, work, P, st);
     else launch_grid(grad_norm_kernel<DT, kNormRankBatch, 8, PT>, dev, work, P, st);
     return cudaGetLastError();
 }
@@ -1359,6 +1360,7 @@ cudaError_t launch_reduce_to_host(int dev, PT& P, bool vec, cudaStream_t st)
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     if (!vec) launch_grid(reduce_to_host_kernel<DT, 1, 1, PT>, dev, work, P, st);
+    else if (P.n_d >= kWideRankBatchFrom) launch_grid(reduce_to_host_kernel<DT, kWideRankBatch, 8, PT>, dev, work, P, st);
     else launch_grid(reduce_to_host_kernel<DT, kRankBatch, 8, PT>, dev, work, P, st);
     return cudaGetLastError();
 }
