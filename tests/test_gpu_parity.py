@@ -858,6 +858,45 @@ def test_bulk_staging_first_launch_inside_a_graph_capture():
         run.close()
 
 
+def test_two_plans_step_concurrently_from_two_threads():
+    """Two plans (N_d 7 staged, N_d 12 register loads under the automatic choice) stepped at
+    the same time from two host threads on two streams: the library's per-kernel caches and
+    per-thread error text are shared, the results must still match the oracle."""
+    import threading
+    cases = [_mk(195, _ragged(50, 25, 20000), 7, 2, steps=3, bucket=30_000),
+             _mk(196, _ragged(51, 25, 20000), 12, 2, steps=3)]
+    runs = [H.Run(w) for w in cases]
+    oracles = [H.OracleFull(w, r.bound) for w, r in zip(cases, runs)]
+    errors = []
+
+    def worker(i):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for k in range(1, cases[i].steps + 1):
+                    runs[i].step(k)
+            stream.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    try:
+        threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        assert not errors, errors
+        torch.cuda.synchronize()
+        for w, run, o in zip(cases, runs, oracles):
+            for k in range(1, w.steps + 1):
+                o.step(k)
+            assert run.g.step_state().t == w.steps
+            _compare_full(run, o, f"concurrent plan N_d = {w.n_d}")
+    finally:
+        for run in runs:
+            run.close()
+
+
 def test_bulk_staging_wait_limit_runs_out_and_the_step_is_discarded():
     """A wait limit of 0 makes the first barrier wait that is not already satisfied give up:
     the kernel records it, drains its copies and returns; zero_step_finish reports
