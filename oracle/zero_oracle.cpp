@@ -38,8 +38,9 @@
 // equivalence ([ZF] "Mathematical Formulation of ZeRO Partitioning Stages":
 // sharding keeps the exact semantics of data parallelism); torch.optim.AdamW
 // and numpy/torch 16-bit conversions as library cross-checks; closed forms of
-// the first AdamW step.  Parity unpinned: the exact fp32 operation order of
-// the update (R1/R7), the reduction precision and order (R2/R3).
+// the first AdamW step.  What the pins fix up to rounding rather than bit for
+// bit is the choice among equally valid fp32 operation orders of the update
+// (R1/R7) and of the reduction (R2/R3): a reading, shared with the GPU path.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
