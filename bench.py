@@ -171,6 +171,68 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML every ~0.5 ms while the timed region
+    runs (a short run's timed region lasts milliseconds, under nvidia-smi's sampling period).
+    Reads only; the device is found by its UUID, so CUDA_VISIBLE_DEVICES does not matter."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        import threading
+        self.ctypes, self.threading = ctypes, threading
+        self.ok, self.samples, self.thread, self.running = False, [], None, False
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            uuid = str(getattr(torch.cuda.get_device_properties(cuda_index), "uuid", "") or "")
+            if uuid:
+                key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                rc = nv.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(self.handle))
+            else:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.handle))
+            if rc != 0:
+                return
+            self.reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.ok = nv, True
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0 else None
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        ctypes = self.ctypes
+        mhz, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        while self.running:
+            if (self.nv.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0 and
+                    self.reasons(self.handle, ctypes.byref(bits)) == 0):
+                self.samples.append((float(mhz.value), int(bits.value)))
+            time.sleep(0.0005)
+
+    def start(self):
+        if self.ok:
+            self.running = True
+            self.thread = self.threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        if not self.ok or self.thread is None:
+            return None
+        self.running = False
+        self.thread.join()
+        if not self.samples:
+            return None
+        reasons = sorted({name for _, b in self.samples for bit, name in self.REASONS.items() if b & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml, timed region"}
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 class Bench:
@@ -410,6 +472,8 @@ def gpu_arm(args, world, rank, local):
         dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    region = NvmlSampler(local)
+    region.start()
     t0.record()
     if graph is not None:
         graph.replay()
@@ -417,9 +481,14 @@ def gpu_arm(args, world, rank, local):
         timed_steps()
     t1.record()
     torch.cuda.synchronize()
+    region_clk = region.stop()
     if dist:
         dist.barrier()
     clk = clocks.stop()
+    if region_clk is not None:               # samples taken inside the timed region
+        if clk is not None:
+            region_clk["nvidia_smi"] = clk
+        clk = region_clk
     ms = t0.elapsed_time(t1)
     if dist:
         ms = max_over_ranks(ms, dist)
