@@ -939,9 +939,18 @@ __global__ void __launch_bounds__(kThreads) recast_kernel(const __grid_constant_
             S.out16[e] = narrow1<DT>(S.p[cur][e]);
         }
     }
-    // The last launch of the re-cast also closes the step: the last block to finish (atomic
-    // ticket; every block read the flag and the current half before taking its ticket)
-    // applies the commit.
+    // The last launch of the re-cast also closes the step.  Clean step (the usual case):
+    // nothing was re-cast and the commit leaves the flag clear, so block 0 commits at once; a
+    // block that reads the state after that still sees a clear flag and does nothing.
+    // Flagged or discarded step: the last block to finish (atomic ticket; every block read
+    // the flag and the current half before taking its ticket) commits.
+    if (P.do_commit && !go) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            commit_state(P.commit);
+            __threadfence();
+        }
+        return;
+    }
     if (P.do_commit) {
         __shared__ bool last;
         __syncthreads();
