@@ -287,7 +287,7 @@ zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_
  *                           word, its block drains its own copies in flight and returns.
  *   ZERO_OPT_BULK_TILE      elements per staged tile, a multiple of 8 in [8, 8192]; 0 (default):
  *                           the largest multiple of 512 up to 2048 with tile * (2 N_d + 12)
- *                           bytes within 45 KB (a power of two below 512 for N_d >= 40).
+ *                           bytes within 53.5 KB (a power of two below 512 for N_d >= 48).
  *   ZERO_OPT_BULK_STAGES    ring depth in [2, 16]; 0 (default): 2 (two blocks per SM).
  * A tile/stage pair whose ring does not fit one block's shared memory gives ZERO_ERANGE. */
 enum {

@@ -723,11 +723,12 @@ BULK = {Z.ZERO_OPT_STAGING: Z.ZERO_STAGING_BULK}
 LDG = {Z.ZERO_OPT_STAGING: Z.ZERO_STAGING_REGISTER_LOADS}
 
 
-@pytest.mark.parametrize("n_d,staged", [(7, 1), (8, 1), (12, 0), (16, 1), (24, 1), (64, 0)])
+@pytest.mark.parametrize("n_d,staged", [(2, 0), (6, 1), (7, 1), (8, 1), (12, 0), (16, 1), (20, 1),
+                                          (24, 1), (64, 0), (96, 0)])
 def test_automatic_kernel_choice(n_d, staged):
     """The default (ZERO_STAGING_AUTO) launches the staged kernel where its ring gives two blocks
-    per SM (or three of 512-element tiles) on GB300's 228 KB of shared memory per SM, register
-    loads elsewhere; either way the step matches the oracle."""
+    per SM with tiles of 512 elements or more (or three of 512-element tiles) on GB300's 228 KB
+    of shared memory per SM, register loads elsewhere; either way the step matches the oracle."""
     w = _mk(180 + n_d, _ragged(40 + n_d, 20, 30000), n_d, 2, steps=1)
     run = H.Run(w)
     o = H.OracleFull(w, run.bound)

@@ -175,7 +175,7 @@ def test_execution_options_are_checked_on_the_host():
     try:
         assert Z.zero_get_option(plan, Z.ZERO_OPT_STAGING) == Z.ZERO_STAGING_AUTO
         assert Z.zero_get_option(plan, Z.ZERO_OPT_WAIT_LIMIT_NS) == 1_000_000_000
-        assert Z.zero_get_option(plan, Z.ZERO_OPT_BULK_TILE) == 1536      # 1536 x 26 B <= 45 KB
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_BULK_TILE) == 2048      # 2048 x 26 B <= 53.5 KB
         assert Z.zero_get_option(plan, Z.ZERO_OPT_BULK_STAGES) == 2
         assert Z.zero_get_option(plan, Z.ZERO_OPT_LAST_STEP_KERNEL) == -1
         with pytest.raises(Z.ZeroError) as e:

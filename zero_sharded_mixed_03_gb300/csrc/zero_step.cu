@@ -38,10 +38,12 @@ constexpr int kMaxSegs = 32;      // work items per launch (more are split acros
 constexpr int kWideSegs = 256;    // capacity of the wide parameter block (calls with many items)
 constexpr int kScalarSlots = 16;  // per segment: up to 7 head + 7 tail elements
 // Contribution slices loaded (128-bit each) per batch before they are summed; from
-// kWideRankBatchFrom ranks on, kWideRankBatch.
+// kWideRankBatchFrom ranks on (kWideNormBatchFrom for the reductions without an update),
+// kWideRankBatch.
 constexpr int kRankBatch = 4;
 constexpr int kWideRankBatch = 16;
-constexpr int kWideRankBatchFrom = 32;
+constexpr int kWideRankBatchFrom = 41;
+constexpr int kWideNormBatchFrom = 32;
 // The gradient-norm pre-pass reads nothing else, so it keeps more slices in flight.
 constexpr int kNormRankBatch = 8;
 
@@ -1190,10 +1192,11 @@ void launch_grid(K kernel, int dev, int64_t work, const PT& P, cudaStream_t st)
     kernel<<<grid, kThreads, 0, st>>>(P);
 }
 
-// Register loads keep NB contribution slices in flight per batch: 4, or 16 from N_d = 32 on,
+// Register loads keep NB contribution slices in flight per batch: 4, or 16 from N_d = 41 on,
 // where the rank loop otherwise serialises on load latency (GB300, ragged ZeRO-2 step: N_d =
-// 64 / 96 / 128 at 0.958 / 0.947 / 0.931 of the copy bandwidth against 0.913 / 0.909 / 0.893
-// with 4; below 32, batches of 16 cost occupancy and lost up to 25 %).
+// 48 / 64 / 96 / 128 at 0.96 / 0.96 / 0.95 / 0.93 of the copy bandwidth against 0.93 / 0.91 /
+// 0.91 / 0.89 with 4; at N_d = 33-40 batches of 16 cost occupancy and lost 2-12 %, below 32
+// up to 25 %).
 template <int DT, int MODE, typename PT>
 void launch_fused_mode(int dev, const PT& P, bool vec, int64_t work, cudaStream_t st)
 {
@@ -1211,15 +1214,15 @@ struct BulkCfg {
     bool automatic = false;
 };
 
-// Where the staged kernel beats register loads, from a sweep of N_d = 1 .. 64 on GB300 (ragged
-// ZeRO-2 step, default geometry): with exactly two blocks per SM (8 consumer warps, 75-110 KB
-// rings) it won at every N_d but 9 and 33 (by 1-5 %); with three blocks of 512-element tiles
-// (N_d 22-30) it won by 2-6 %; three blocks of 1,024-2,048-element tiles (N_d 1-3, 6, 10-12)
-// lost 7-14 %, four blocks (N_d 17-21, 48) lost up to 4 % or won up to 4 %, and tiles below
-// 512 elements (N_d >= 49) lost 20 % and more.
+// Where the staged kernel beats register loads, from sweeps of N_d = 1 .. 128 on GB300 (ragged
+// ZeRO-2 step): with exactly two blocks per SM (8 consumer warps, 75-110 KB rings) and tiles of
+// 512 elements or more it won almost everywhere (by up to 7 %; lost 1-2 % at N_d = 10-11);
+// with three blocks of 512-element tiles (N_d 22-31) it won by 2-6 %; three blocks of
+// 1,024-2,048-element tiles (N_d 1-3, 12) lost 7-14 %, four blocks were a wash, and tiles below
+// 512 elements (N_d >= 48: bulk copies of <= 512 B per rank) lost 20-50 % whatever the blocks.
 bool bulk_pays_off(int blocks_per_sm, int tile)
 {
-    return blocks_per_sm == 2 || (blocks_per_sm == 3 && tile == 512);
+    return (blocks_per_sm == 2 && tile >= 512) || (blocks_per_sm == 3 && tile == 512);
 }
 
 // Dynamic shared memory of one block: alignment slack, barriers, the ring.
@@ -1229,13 +1232,14 @@ int64_t bulk_smem_bytes(int64_t tile, int64_t stages, int64_t n_d)
 }
 
 // Default geometry: two buffers of the largest tile, a multiple of 512 elements (whole passes
-// of the consumer threads over 4-element quads) up to 2048, within 45 KB per buffer; for
-// N_d >= 40 the largest power of two within 45 KB.  Two blocks then share an SM with a
-// 80-90 KB ring each.  Measured on GB300 with N_d = 7, 8 and 16: two blocks of ~4
-// consumer warps with 40-50 KB tiles beat both deeper rings and more, smaller blocks.
+// of the consumer threads over 4-element quads) up to 2048, within 53.5 KB per buffer; for
+// N_d >= 48 the largest power of two within that.  Two blocks then share an SM with rings of
+// up to 107 KB.  Measured on GB300: two blocks of four consumer warps with 40-53 KB tiles
+// beat deeper rings and more, smaller blocks (a 45 KB cap left N_d = 6, 10, 11, 17-20 with
+// three or four blocks per SM, 3-7 % slower than this geometry).
 int auto_bulk_tile(int n_d)
 {
-    const int64_t per_elem = 2 * n_d + 12, cap = 45 * 1024;
+    const int64_t per_elem = 2 * n_d + 12, cap = 54784;
     int64_t tile = std::min<int64_t>(2048, cap / per_elem / 512 * 512);
     if (tile >= 512) return (int)tile;
     tile = 256;
@@ -1358,7 +1362,7 @@ cudaError_t launch_norm(int dev, PT& P, bool vec, cudaStream_t st)
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     if (!vec) launch_grid(grad_norm_kernel<DT, 1, 1, PT>, dev, work, P, st);
-    else if (P.n_d >= kWideRankBatchFrom) launch_grid(grad_norm_kernel<DT, kWideRankBatch, 8, PT>, dev, work, P, st);
+    else if (P.n_d >= kWideNormBatchFrom) launch_grid(grad_norm_kernel<DT, kWideRankBatch, 8, PT>, dev, work, P, st);
     else launch_grid(grad_norm_kernel<DT, kNormRankBatch, 8, PT>, dev, work, P, st);
     return cudaGetLastError();
 }
@@ -1369,7 +1373,7 @@ cudaError_t launch_reduce_to_host(int dev, PT& P, bool vec, cudaStream_t st)
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(P.total_vec, (int64_t)P.n_seg * kScalarSlots);
     if (!vec) launch_grid(reduce_to_host_kernel<DT, 1, 1, PT>, dev, work, P, st);
-    else if (P.n_d >= kWideRankBatchFrom) launch_grid(reduce_to_host_kernel<DT, kWideRankBatch, 8, PT>, dev, work, P, st);
+    else if (P.n_d >= kWideNormBatchFrom) launch_grid(reduce_to_host_kernel<DT, kWideRankBatch, 8, PT>, dev, work, P, st);
     else launch_grid(reduce_to_host_kernel<DT, kRankBatch, 8, PT>, dev, work, P, st);
     return cudaGetLastError();
 }
