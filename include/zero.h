@@ -273,10 +273,10 @@ zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_
  *                           four consumer warps reduce and update from shared memory.
  *                           ZERO_STAGING_REGISTER_LOADS: every thread loads them with 128-bit
  *                           register loads.  ZERO_STAGING_AUTO (default): the staged kernel where
- *                           its ring gives two resident blocks per SM, or three with 512-element
- *                           tiles (on GB300 with the default geometry: N_d = 4-5, 7-9, 13-16 and
- *                           22-47, where it measured faster at all but N_d = 9 and 33), register
- *                           loads elsewhere.  All give
+ *                           its ring gives two resident blocks per SM with tiles of at least 512
+ *                           elements, or three with 512-element tiles (on GB300 with the default
+ *                           geometry: N_d = 4-11, 13-20 and 22-47, where it measured faster at all
+ *                           but N_d = 10, 11 and 33), register loads elsewhere.  All give
  *                           identical results, bit for bit.  Launches whose streams do not
  *                           share one 16-byte phase use the scalar register-load path either
  *                           way, and so do steps that report the gradient norm from the fused
