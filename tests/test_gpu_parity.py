@@ -324,6 +324,33 @@ def test_steps_enqueued_without_host_waits():
         run.close()
 
 
+@pytest.mark.parametrize("staging", [0, 1])
+def test_long_run_with_loss_scale_cycles(staging):
+    """400 steps enqueued back to back (fp16, 3 buckets, dynamic loss scale growing every 25
+    clean steps, one planted inf): t, scale, skip count and every state bit must follow the
+    oracle at the end; no drift over hundreds of ping-pong flips and commits."""
+    w = _mk(197, _ragged(60, 12, 4000), 5, 2, steps=400, bucket=7_000, dtype=W.FP16,
+            scaler=W.Scaler(init_scale=256.0, growth_interval=25), inject=(123, 2, 4_321))
+    run = H.Run(w, options={Z.ZERO_OPT_STAGING: staging})
+    o = H.OracleFull(w, run.bound)
+    try:
+        skips = 0
+        for k in range(1, w.steps + 1):
+            for which, lo, hi in run.ranges():
+                for r in range(w.n_d):
+                    H.fill_device(run.contribs[r], synth.grad_stream(w, k, r), run.units, lo, hi)
+                run.g.step([c.data_ptr() for c in run.contribs], which, run.hyper)
+            run.g.finish(wait=False)
+            skips += o.step(k)
+        st = run.g.step_state()
+        assert skips == 1
+        assert (st.t, st.scale, st.skipped_total, st.finished, st.good_steps) == \
+            (o.sc.t, o.sc.scale, 1, w.steps, o.sc.good)
+        _compare_full(run, o, f"after {w.steps} steps")
+    finally:
+        run.close()
+
+
 def test_bias_table_saturates():
     """beta1 = 0.5, beta2 = 0.6: 1 - beta^t rounds to 1 after ~72 steps; 90 steps cross the
     end of the table and keep matching the oracle."""
