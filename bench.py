@@ -81,6 +81,13 @@ def parse_args():
                          "library's choice (staged where its residency pays off)")
     ap.add_argument("--bulk-tile", type=int, default=0, help="bulk staging: elements per tile")
     ap.add_argument("--bulk-stages", type=int, default=0, help="bulk staging: ring depth")
+    ap.add_argument("--gather-staging", choices=["default", "ldg", "bulk"], default="default",
+                    help="stage-3 gather kernel: register loads or bulk-staged (default: the plan's)")
+    ap.add_argument("--gather-chunk", type=int, default=0, help="bulk gather: elements per copy")
+    ap.add_argument("--gather-stages", type=int, default=0, help="bulk gather: ring entries")
+    ap.add_argument("--profile-unit", type=int, default=None,
+                    help="stage 3: restrict the workload to this one unit (for ncu captures of a "
+                         "few GB; not the benchmark workload)")
     ap.add_argument("--grad-norm", choices=["off", "report", "clip"], default="off",
                     help="report: global gradient norm inside the fused pass; clip: norm pre-pass "
                          "over every bucket/unit, then the update clipped at max norm 1.0")
@@ -405,6 +412,8 @@ def gpu_arm(args, world, rank, local):
     w = W.workload(args.config)
     if args.per_param:
         w = W.per_param_variant(w)
+    if args.profile_unit is not None:
+        w = W.unit_slice(w, args.profile_unit)
     if args.offload:
         import dataclasses
         w = dataclasses.replace(w, offload=True)
@@ -413,6 +422,12 @@ def gpu_arm(args, world, rank, local):
                "auto": Z.ZERO_STAGING_AUTO}[args.staging]
     options = {Z.ZERO_OPT_STAGING: staging, Z.ZERO_OPT_BULK_TILE: args.bulk_tile,
                Z.ZERO_OPT_BULK_STAGES: args.bulk_stages}
+    # gather ring: entries first when the chunk grows, so that no intermediate ring overflows
+    gather = [(Z.ZERO_OPT_GATHER_CHUNK, args.gather_chunk), (Z.ZERO_OPT_GATHER_STAGES, args.gather_stages)]
+    options.update(dict(gather[::-1] if args.gather_chunk > 16384 else gather))
+    if args.gather_staging != "default":
+        options[Z.ZERO_OPT_GATHER_STAGING] = {"ldg": Z.ZERO_STAGING_REGISTER_LOADS,
+                                             "bulk": Z.ZERO_STAGING_BULK}[args.gather_staging]
     b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm,
               options)
     peak, peak_kind = peaks()
@@ -523,6 +538,9 @@ def gpu_arm(args, world, rank, local):
     if gather_ms:
         g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
         roofline["gather_achieved_gbs"] = round(g_bytes / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
+        gstaging = Z.zero_get_option(b.g.plan, Z.ZERO_OPT_GATHER_STAGING)
+        roofline["gather_kernel"] = ("gather_kernel" if gstaging == Z.ZERO_STAGING_REGISTER_LOADS
+                                     else "bulk_gather_kernel")
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
@@ -536,6 +554,7 @@ def gpu_arm(args, world, rank, local):
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
                       "overlap": overlap, "graph": graph is not None, "per_param": w.per_param,
                       "offload": w.offload, "staging": args.staging,
+                      "profile_unit": args.profile_unit,
                       "offload_threads": b.g.offload_threads if w.offload else None},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,

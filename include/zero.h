@@ -36,9 +36,10 @@
  *    every stream of a launch has the same element phase modulo 8 (always true
  *    for the state layout below when bucket_elems is a multiple of 8); other
  *    launches use the scalar path of the same kernel.
- *  - Kernels never trap or assert.  The only waits are those of the bulk-staged step kernel
- *    (zero_set_option, ZERO_OPT_STAGING) on its shared-memory barriers; each is bounded in
- *    time (ZERO_OPT_WAIT_LIMIT_NS) and one that runs out is reported as ZERO_ETIMEOUT.
+ *  - Kernels never trap or assert.  The only waits are those of the bulk-staged step and
+ *    gather kernels (zero_set_option, ZERO_OPT_STAGING / ZERO_OPT_GATHER_STAGING) on their
+ *    shared-memory barriers; each is bounded in time (ZERO_OPT_WAIT_LIMIT_NS) and one that
+ *    runs out is reported as ZERO_ETIMEOUT.
  */
 #ifndef ZERO_H
 #define ZERO_H
@@ -259,10 +260,10 @@ zero_status_t zero_grad_norm(zero_plan_t* plan, const void* const* grad_contribs
 zero_status_t zero_step_finish(zero_plan_t* plan, void* stream, zero_step_result_t* out);
 
 /* Read the device-resident step state (synchronises `stream`).  zero_read_state and
- * zero_step_finish (out != NULL) return ZERO_ETIMEOUT, with *out filled, when a wait of the
- * bulk-staged kernel ran out since the state was last read: every step finished since then
- * was discarded (state, t, loss scale and counters unchanged; 16-bit parameters rewritten
- * from the current master).  Reading the state clears the condition. */
+ * zero_step_finish (out != NULL) return ZERO_ETIMEOUT, with *out filled, when a wait of a
+ * bulk-staged kernel (step or gather) ran out since the state was last read: every step
+ * finished since then was discarded (state, t, loss scale and counters unchanged; 16-bit
+ * parameters rewritten from the current master).  Reading the state clears the condition. */
 zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_t* out);
 
 /* Execution options of a plan (not inside an open step; values are checked here):
@@ -281,7 +282,7 @@ zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_
  *                           share one 16-byte phase use the scalar register-load path either
  *                           way, and so do steps that report the gradient norm from the fused
  *                           pass (ZERO_REPORT_GRAD_NORM without clipping).
- *   ZERO_OPT_WAIT_LIMIT_NS  bound on each barrier wait of the bulk-staged kernel, in ns of
+ *   ZERO_OPT_WAIT_LIMIT_NS  bound on each barrier wait of the bulk-staged kernels, in ns of
  *                           %globaltimer (default 1e9; 0 gives up at the first wait that does
  *                           not succeed at once).  A wait that runs out sets the plan's error
  *                           word, its block drains its own copies in flight and returns.
@@ -289,19 +290,35 @@ zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_
  *                           the largest multiple of 512 up to 2048 with tile * (2 N_d + 12)
  *                           bytes within 53.5 KB (a power of two below 512 for N_d >= 48).
  *   ZERO_OPT_BULK_STAGES    ring depth in [2, 16]; 0 (default): 2 (two blocks per SM).
- * A tile/stage pair whose ring does not fit one block's shared memory gives ZERO_ERANGE. */
+ *   ZERO_OPT_GATHER_STAGING which kernel zero_gather_layer launches.  ZERO_STAGING_AUTO
+ *                           (default) and ZERO_STAGING_BULK: one lane per block copies chunks
+ *                           of the shards through a ring of shared-memory entries with 1-D
+ *                           cp.async.bulk loads (completing on mbarriers) and bulk stores,
+ *                           the loads two chunks ahead of the stores; ZERO_STAGING_REGISTER_LOADS:
+ *                           128-bit register copies.  Gathers whose copies do not share one
+ *                           16-byte phase, and plans without a bound workspace (which holds the
+ *                           error word), use register loads either way.  Identical results.
+ *   ZERO_OPT_GATHER_CHUNK   elements per bulk copy of the staged gather, a multiple of 8 in
+ *                           [8, 32768]; 0 (default): 16384 (32 KB).
+ *   ZERO_OPT_GATHER_STAGES  its ring entries in [3, 32]; 0 (default): 4 (a 128 KB ring).
+ * A geometry whose ring does not fit one block's shared memory gives ZERO_ERANGE and leaves
+ * the earlier one in place. */
 enum {
     ZERO_OPT_STAGING = 0,
     ZERO_OPT_WAIT_LIMIT_NS = 1,
     ZERO_OPT_BULK_TILE = 2,
     ZERO_OPT_BULK_STAGES = 3,
-    ZERO_OPT_LAST_STEP_KERNEL = 4   /* read only: the step kernel of the last zero_step launch
+    ZERO_OPT_LAST_STEP_KERNEL = 4,  /* read only: the step kernel of the last zero_step launch
                                        (1 staged, 0 register loads, -1 none yet) */
+    ZERO_OPT_GATHER_STAGING = 5,
+    ZERO_OPT_GATHER_CHUNK = 6,
+    ZERO_OPT_GATHER_STAGES = 7
 };
 enum { ZERO_STAGING_REGISTER_LOADS = 0, ZERO_STAGING_BULK = 1, ZERO_STAGING_AUTO = 2 };
 zero_status_t zero_set_option(zero_plan_t* plan, int option, int64_t value);
 
-/* Read an option (the tile and stages in effect when left at 0), or ZERO_OPT_LAST_STEP_KERNEL. */
+/* Read an option (the tile, stages, chunk and entries in effect when left at 0), or
+ * ZERO_OPT_LAST_STEP_KERNEL. */
 zero_status_t zero_get_option(const zero_plan_t* plan, int option, int64_t* value);
 
 /* Overwrite the device-resident step state, e.g. when resuming from a checkpoint whose fp32
@@ -311,7 +328,9 @@ zero_status_t zero_restore_state(zero_plan_t* plan, const zero_step_result_t* in
 
 /* Stage 3 all-gather of unit `unit` ("ZeRO-3 / FSDP Layer Execution Lifecycle"): copies the
  * N_d 16-bit shards (bound or peer ranks) into full_unit16 (phi_pad_u elements, padding
- * included).  The unit stays "gathered" until zero_release_layer. */
+ * included), asynchronously on `stream` with the kernel ZERO_OPT_GATHER_STAGING selects.  The
+ * unit stays "gathered" until zero_release_layer.  A barrier wait of the staged gather that
+ * runs out leaves the unit incomplete and sets the plan's error word (see zero_read_state). */
 zero_status_t zero_gather_layer(zero_plan_t* plan, int64_t unit, void* full_unit16, void* stream);
 
 /* A whole stage-3 step with the all-gather overlapped ("Overlapping Computation and

@@ -122,6 +122,17 @@ def llama_dim0(vocab: int, d: int, ffn: int, layers: int) -> List[int]:
     return dims + [d, vocab]
 
 
+def unit_slice(w: "Workload", u: int) -> "Workload":
+    """Stage 3: the same workload restricted to the tensors of unit u (one unit), e.g. to
+    profile one unit's kernels with a few GB on the device."""
+    if w.stage != 3:
+        raise ValueError("unit_slice: stage-3 workloads only")
+    first, count = w.units()[u]
+    return dataclasses.replace(
+        w, name=f"{w.name}, unit {u} only", sizes=w.sizes[first:first + count], unit_first=(0,),
+        dim0=w.dim0[first:first + count] if w.dim0 else None, inject=None)
+
+
 def per_param_variant(w: "Workload") -> "Workload":
     """The same workload under FSDP-2 per-parameter sharding (stage-3 semantics)."""
     assert w.dim0 is not None

@@ -830,6 +830,80 @@ def test_bulk_staging_geometries(name, tile, stages):
                                           Z.ZERO_OPT_BULK_STAGES: stages})
 
 
+GATHER_BULK = {Z.ZERO_OPT_GATHER_STAGING: Z.ZERO_STAGING_BULK}
+GATHER_LDG = {Z.ZERO_OPT_GATHER_STAGING: Z.ZERO_STAGING_REGISTER_LOADS}
+STAGE3_SMALL = [n for n, w in SMALL_CASES.items() if w.stage == 3]
+
+
+@pytest.mark.parametrize("gather", ["ldg", "bulk"])
+@pytest.mark.parametrize("name", STAGE3_SMALL)
+def test_gather_kernels_small_stage3_full_parity(name, gather):
+    """Both gather kernels (register loads, bulk-staged) on every stage-3 case: each gathered
+    unit equals the oracle's concatenation of the rank shards, bit for bit, at every step."""
+    _run_full(SMALL_CASES[name], options=GATHER_BULK if gather == "bulk" else GATHER_LDG)
+
+
+@pytest.mark.parametrize("gather", ["ldg", "bulk"])
+@pytest.mark.parametrize("name", list(PP_CASES))
+def test_gather_kernels_per_param_full_parity(name, gather):
+    """Per-parameter gathers: up to 256 row-block chunks per launch, ragged and tiny."""
+    _run_full(PP_CASES[name], options=GATHER_BULK if gather == "bulk" else GATHER_LDG)
+
+
+@pytest.mark.parametrize("chunk,stages", [(8, 3), (64, 32), (1000, 5), (32768, 3), (4096, 12)])
+def test_bulk_gather_geometries(chunk, stages):
+    """Bulk-staged gather rings from one 8-element vector per copy to 64 KB copies, 3 to 32
+    entries (loads 1 to 30 chunks ahead), on units with shards shorter than a chunk, ragged
+    tails and empty tensors."""
+    # set in an order whose intermediate ring fits (the default is 4 entries of 16384)
+    order = ([Z.ZERO_OPT_GATHER_CHUNK, Z.ZERO_OPT_GATHER_STAGES] if chunk <= 16384
+             else [Z.ZERO_OPT_GATHER_STAGES, Z.ZERO_OPT_GATHER_CHUNK])
+    value = {Z.ZERO_OPT_GATHER_CHUNK: chunk, Z.ZERO_OPT_GATHER_STAGES: stages}
+    options = {Z.ZERO_OPT_GATHER_STAGING: 1, **{k: value[k] for k in order}}
+    for name in ("z3_nd16_units", "z3_nd3_fp16_peers_skip_first", "z3_nd16_empty_unit_tensors"):
+        _run_full(SMALL_CASES[name], options=options)
+
+
+@pytest.mark.parametrize("gather", ["ldg", "bulk"])
+@pytest.mark.parametrize("i", [3, 4])
+def test_gather_kernels_config_sampled(i, gather):
+    w = W.workload(i)
+    n, mism = _run_sampled(w, bound=(0, w.n_d - 1) if i == 4 else None,
+                           options=GATHER_BULK if gather == "bulk" else GATHER_LDG)
+    print(f"{w.name}, {gather} gather: {n} sampled elements, {mism} bit mismatches")
+
+
+def test_bulk_gather_wait_limit_runs_out_and_the_step_is_discarded():
+    """A gather whose barrier wait runs out (limit 0) records it in the plan's error word,
+    drains its copies and returns; the step then finishing reports ZERO_ETIMEOUT and is
+    discarded, and the next step (a full wait limit again) follows the oracle."""
+    w = _mk(171, [3_000_000 + 5, 2_500_000, 17], 4, 3, steps=2, units=(0, 1))
+    run = H.Run(w, options={**GATHER_BULK, **LDG})
+    o = H.OracleFull(w, run.bound)
+    try:
+        res = run.step(1)
+        o.step(1)
+        assert res.t == 1
+        before = {r: run.read_logical(r) for r in run.bound}
+        run.g.set_option(Z.ZERO_OPT_WAIT_LIMIT_NS, 0)
+        with pytest.raises(Z.ZeroError) as e:
+            run.step(2)
+        assert e.value.status == Z.ZERO_ETIMEOUT
+        st = e.value.result
+        assert (st.t, st.finished, st.skipped) == (1, 1, 1)
+        for r in run.bound:
+            now = run.read_logical(r)
+            for key in now:
+                assert np.array_equal(now[key].view(np.uint32), before[r][key].view(np.uint32)), key
+        run.g.set_option(Z.ZERO_OPT_WAIT_LIMIT_NS, 1_000_000_000)
+        res = run.step(2)
+        o.step(2)
+        assert (res.t, res.finished, res.skipped) == (2, 2, 0)
+        _compare_full(run, o, "after the gather timeout")
+    finally:
+        run.close()
+
+
 def test_bulk_staging_is_bit_identical_to_register_loads():
     w = dataclasses.replace(SMALL_CASES["z2_nd8_fp16_buckets_inf"], steps=4)
     a, b = H.Run(w, options=LDG), H.Run(w, options=BULK)

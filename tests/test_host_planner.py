@@ -215,6 +215,42 @@ def test_execution_options_are_checked_on_the_host():
         Z.zero_plan_destroy(plan)
 
 
+def test_gather_options_are_checked_on_the_host():
+    """The gather's kernel, bulk-copy chunk (a multiple of 8 elements up to 32768) and ring
+    entries (3 to 32); a ring of entries x chunk x 2 B + 384 B beyond 227 KB gives ERANGE
+    and leaves the earlier geometry in place."""
+    plan = _plan_for([10, 20], 4, 3, 0)
+    try:
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_GATHER_STAGING) == Z.ZERO_STAGING_AUTO
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_GATHER_CHUNK) == 16384
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_GATHER_STAGES) == 4
+        for opt, val in ((Z.ZERO_OPT_GATHER_STAGING, 3), (Z.ZERO_OPT_GATHER_STAGING, -1),
+                         (Z.ZERO_OPT_GATHER_CHUNK, 4), (Z.ZERO_OPT_GATHER_CHUNK, 12),
+                         (Z.ZERO_OPT_GATHER_CHUNK, 32776), (Z.ZERO_OPT_GATHER_STAGES, 2),
+                         (Z.ZERO_OPT_GATHER_STAGES, 33), (Z.ZERO_OPT_GATHER_STAGES, -1)):
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_set_option(plan, opt, val)
+            assert e.value.status == Z.ZERO_EINVAL, (opt, val)
+        for val in (0, 1, 2):
+            Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_STAGING, val)
+            assert Z.zero_get_option(plan, Z.ZERO_OPT_GATHER_STAGING) == val
+        Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_CHUNK, 8)
+        Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_STAGES, 32)
+        Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_STAGES, 0)
+        Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_CHUNK, 8192)            # 4 x 16 KB
+        with pytest.raises(Z.ZeroError) as e:                              # 4 x 64 KB
+            Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_CHUNK, 32768)
+        assert e.value.status == Z.ZERO_ERANGE
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_GATHER_CHUNK) == 8192
+        Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_STAGES, 13)             # 13 x 16 KB = 208 KB
+        with pytest.raises(Z.ZeroError) as e:                              # 15 x 16 KB = 240 KB
+            Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_STAGES, 15)
+        assert e.value.status == Z.ZERO_ERANGE
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_GATHER_STAGES) == 13
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
 def test_empty_model_plan():
     plan = _plan_for([], 4, 2, 0)
     info = Z.zero_plan_info(plan)

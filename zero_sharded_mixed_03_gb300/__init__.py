@@ -20,7 +20,8 @@ ZERO_BF16, ZERO_FP16 = 0, 1
 ZERO_MAX_RANKS = 128
 ZERO_REPORT_GRAD_NORM = 1
 (ZERO_OPT_STAGING, ZERO_OPT_WAIT_LIMIT_NS, ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES,
- ZERO_OPT_LAST_STEP_KERNEL) = range(5)
+ ZERO_OPT_LAST_STEP_KERNEL, ZERO_OPT_GATHER_STAGING, ZERO_OPT_GATHER_CHUNK,
+ ZERO_OPT_GATHER_STAGES) = range(8)
 ZERO_STAGING_REGISTER_LOADS, ZERO_STAGING_BULK, ZERO_STAGING_AUTO = range(3)
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)
@@ -312,7 +313,8 @@ def zero_read_state(plan: int, stream: int = 0) -> zero_step_result_t:
 
 def zero_set_option(plan: int, option: int, value: int) -> None:
     """ZERO_OPT_STAGING (ZERO_STAGING_REGISTER_LOADS / _BULK / _AUTO), ZERO_OPT_WAIT_LIMIT_NS,
-    ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES (0 = chosen from N_d)."""
+    ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES (0 = chosen from N_d); the gather's
+    ZERO_OPT_GATHER_STAGING, ZERO_OPT_GATHER_CHUNK, ZERO_OPT_GATHER_STAGES (0 = default)."""
     _check(lib().zero_set_option(plan, option, int(value)))
 
 

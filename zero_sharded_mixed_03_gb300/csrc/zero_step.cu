@@ -66,8 +66,9 @@ struct DevState {
     double last_norm2;      // last finished step's sum
     uint32_t norm_valid;    // open step computed a norm
     uint32_t last_norm_valid;
-    uint32_t error;         // bit 0: a barrier wait ran out; bit 1: a drain ran out (sticky
-                            // until read; every step finished meanwhile is discarded)
+    uint32_t error;         // bit 0: a barrier wait of the staged step ran out; bit 1: a drain
+                            // ran out; bit 2: a barrier wait of the staged gather ran out
+                            // (sticky until read; every step finished meanwhile is discarded)
     uint32_t pad32;
     int64_t pad;
 };
@@ -132,6 +133,7 @@ struct CopySeg {
     const uint16_t* src;
     uint16_t* dst;
     int64_t n, nvec, vbeg;
+    int64_t cbeg;           // bulk-staged gather: first chunk of this copy
     int32_t head, tail;
 };
 
@@ -140,8 +142,14 @@ struct CopyParamsT {
     CopySeg seg[MS];
     int n_seg;
     int64_t total_vec;
+    // bulk-staged gather only
+    uint32_t* err;          // the plan's error word
+    uint64_t wait_ns;       // bound on each barrier wait
+    int32_t chunk;          // elements per bulk copy (a multiple of 8)
+    int32_t stages;         // ring entries
+    int64_t n_chunks;       // chunks of all copies of the launch
 };
-// 32 copies (1.5 KB), or 256 (12 KB) for gathers of many chunks (per-parameter plans)
+// 32 copies (1.8 KB), or 256 (14 KB) for gathers of many chunks (per-parameter plans)
 using CopyParams = CopyParamsT<kMaxSegs>;
 using CopyParamsWide = CopyParamsT<kWideSegs>;
 
@@ -1069,6 +1077,154 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
     }
 }
 
+// ------------------------------------------------------------------ bulk-staged gather (stage 3)
+
+// The register-load gather above keeps one 16-byte load per thread in flight (~30 KB per SM),
+// which leaves copies of a ~100 MB unit latency-bound.  Here one lane per block moves the
+// bytes with 1-D bulk copies through a ring of `stages` shared-memory chunks: global ->
+// shared loads complete on the chunk's mbarrier (bounded waits), shared -> global bulk stores
+// are tracked as bulk groups, and the loads run stages - kGatherStoresPending chunks ahead of
+// the stores, so each block keeps ~(stages - 2) chunks of loads in flight.  The other lanes
+// copy the unaligned heads and tails with plain loads.  Block b takes chunks b, b + grid, ...
+// (a chunk never crosses the end of a copy).  A wait that runs out sets bit 2 of the error
+// word; the lane then waits (bounded) for the loads it issued and for its stores, and returns.
+constexpr int kGatherThreads = 32;
+constexpr int kGatherStoresPending = 2;      // bulk stores left in flight when a chunk is reused
+constexpr int kGatherMaxStages = 32;
+constexpr int kGatherBarrierBytes = 8 * kGatherMaxStages;
+constexpr int kGatherMaxChunk = 32768;
+// Default geometry, measured on GB300: 32 KB copies, four entries (two loads ahead), a 128 KB
+// ring and so one block per SM.  Against register loads: 1.3B units (100 MB) 5.55 -> 5.74
+// TB/s, Llama rank-view units (405 MB) 6.17 -> 6.54 TB/s, per-parameter gathers even (1.3B)
+// and +6 % (Llama).  Smaller copies with more blocks per SM gathered the 1.3B units faster
+// (6.1 TB/s with 24 KB x 4) but slowed the Llama step kernel that follows each gather from
+// 0.95 to 0.92 of the copy bandwidth.
+constexpr int kGatherDefaultChunk = 16384;
+constexpr int kGatherDefaultStages = 4;
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 ::"l"(dst), "r"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until every bulk group of this thread has completed (its writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Walk over the chunks of a launch in increasing order (chunk ids b, b + grid, ...): the
+// copy holding the current chunk and its chunk range (from the host's first-chunk table) are
+// carried along, so a step costs compares and adds, also across runs of one-chunk copies.
+template <typename CP>
+struct ChunkWalk {
+    int s = -1;
+    int64_t first = 0, end = 0;   // chunk ids of copy s: [first, end)
+
+    __device__ __forceinline__ TileRef at(const CP& P, int64_t c)
+    {
+        while (c >= end) {
+            ++s;
+            first = end;
+            end = s + 1 < P.n_seg ? P.seg[s + 1].cbeg : P.n_chunks;
+        }
+        const CopySeg& S = P.seg[s];
+        const int64_t off = (c - first) * P.chunk;
+        TileRef r;
+        r.e0 = S.head + off;
+        r.len = (int32_t)min((int64_t)P.chunk, 8 * S.nvec - off);
+        return r;
+    }
+};
+
+template <typename CP>
+__global__ void __launch_bounds__(kGatherThreads) bulk_gather_kernel(const __grid_constant__ CP P)
+{
+    extern __shared__ __align__(128) unsigned char gather_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(gather_raw);
+    const uint32_t full0 = (raw + 127u) & ~127u;
+    const uint32_t ring0 = full0 + kGatherBarrierBytes;
+    const uint32_t ns = (uint32_t)P.stages, cbytes = (uint32_t)P.chunk * 2u;
+    const int lane = threadIdx.x;
+    if (lane == 0) {
+        for (uint32_t i = 0; i < ns; ++i) mbar_init(full0 + 8u * i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+    // unaligned heads and tails: plain copies by every lane
+    for (int64_t q = (int64_t)blockIdx.x * kGatherThreads + lane; q < (int64_t)P.n_seg * kScalarSlots;
+         q += (int64_t)gridDim.x * kGatherThreads) {
+        const CopySeg& S = P.seg[q / kScalarSlots];
+        const int k = (int)(q % kScalarSlots);
+        int64_t e = -1;
+        if (k < S.head) e = k;
+        else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+        if (e >= 0) S.dst[e] = S.src[e];
+    }
+    if (lane != 0) return;
+    const uint64_t policy = evict_first_policy();
+    const int64_t grid = gridDim.x;
+    const int64_t mine = P.n_chunks > blockIdx.x ? (P.n_chunks - 1 - blockIdx.x) / grid + 1 : 0;
+    const int64_t ahead = (int64_t)ns - kGatherStoresPending;
+    ChunkWalk<CP> lw, sw;             // load / store walkers
+    uint32_t err = 0;
+    // loads: chunk id, ring entry and count issued; stores: the same, with the entry's phase
+    int64_t lc = blockIdx.x, issued = 0;
+    uint32_t lst = 0;
+    auto issue_load = [&]() {
+        const TileRef T = lw.at(P, lc);
+        const uint32_t full = full0 + 8u * lst;
+        mbar_arrive_expect_tx(full, 2u * (uint32_t)T.len);
+        bulk_load(ring0 + lst * cbytes, P.seg[lw.s].src + T.e0, 2u * (uint32_t)T.len, full, policy);
+        lc += grid;
+        ++issued;
+        if (++lst == ns) lst = 0;
+    };
+    while (issued < mine && issued < ahead) issue_load();
+    int64_t sc = blockIdx.x, j = 0;
+    uint32_t sst = 0, phase = 0;
+    for (; j < mine; ++j) {
+        if (!mbar_wait(full0 + 8u * sst, phase, P.wait_ns)) {
+            err |= 4u;
+            break;
+        }
+        const TileRef T = sw.at(P, sc);
+        bulk_store(P.seg[sw.s].dst + T.e0, ring0 + sst * cbytes, 2u * (uint32_t)T.len, policy);
+        bulk_commit();
+        sc += grid;
+        if (++sst == ns) {
+            sst = 0;
+            phase ^= 1u;
+        }
+        if (issued < mine) {
+            // the next load reuses the entry of the chunk stored kGatherStoresPending groups
+            // before the newest
+            bulk_wait_read<kGatherStoresPending>();
+            issue_load();
+        }
+    }
+    // Drain: every load issued and not yet waited for lands, and every store completes,
+    // before the block's shared memory goes away.
+    for (; j < issued; ++j) {
+        if (!mbar_wait(full0 + 8u * sst, phase, kDrainNs)) err |= 2u;
+        if (++sst == ns) {
+            sst = 0;
+            phase ^= 1u;
+        }
+    }
+    bulk_wait_all();
+    if (err && P.err) atomicOr(P.err, err);
+}
+
 // ------------------------------------------------------------------ host helpers
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
@@ -1274,22 +1430,22 @@ int optin_smem(int dev)
     return cache[dev];
 }
 
-// Blocks per SM of the bulk-staged kernel with `smem` bytes of ring.  The kernel's dynamic
-// shared-memory limit only ever grows (so a launch of another plan on another thread never
-// finds it below its own ring), and the residency is queried once per ring size; both are
-// host calls.
-template <int DT, int MODE, typename PT>
-cudaError_t bulk_residency(int dev, int64_t smem, int* per_sm)
+// Resident blocks per SM of `Kernel` launched with `Threads` threads and `smem` bytes of
+// dynamic shared memory (a ring of staged buffers).  The kernel's dynamic shared-memory limit
+// only ever grows (so a launch of another plan on another thread never finds it below its own
+// ring), and the residency is queried once per device and ring size; both are host calls,
+// cached per instantiation.
+template <auto Kernel, int Threads>
+cudaError_t residency(int dev, int64_t smem, int* per_sm)
 {
     static std::mutex mu;
     static int64_t limit_set[64] = {0};
     static std::unordered_map<int64_t, int> per_sm_of[64];
-    auto kernel = bulk_step_kernel<DT, MODE, PT>;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (limit_set[dev] < smem) {
         const cudaError_t e =
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         limit_set[dev] = smem;
     }
@@ -1299,11 +1455,17 @@ cudaError_t bulk_residency(int dev, int64_t smem, int* per_sm)
         return cudaSuccess;
     }
     int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, (size_t)smem);
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Kernel, Threads, (size_t)smem);
     if (e != cudaSuccess) return e;
     *per_sm = std::max(n, 1);
     per_sm_of[dev].emplace(smem, *per_sm);
     return cudaSuccess;
+}
+
+template <int DT, int MODE, typename PT>
+cudaError_t bulk_residency(int dev, int64_t smem, int* per_sm)
+{
+    return residency<bulk_step_kernel<DT, MODE, PT>, kBulkThreads>(dev, smem, per_sm);
 }
 
 // Launch the bulk-staged kernel with `per_sm` resident blocks per SM.
@@ -1400,9 +1562,45 @@ struct Copy {
     int64_t n;
 };
 
-// Launch gather_kernel over `copies`, CP::seg's capacity at a time.
+// The gather kernel of a launch: bulk-staged (with its ring) or register loads.
+struct GatherCfg {
+    bool bulk = false;
+    int chunk = 0;
+    int stages = 0;
+    uint32_t* err = nullptr;
+    uint64_t wait_ns = 0;
+};
+
+int64_t gather_smem_bytes(int64_t chunk, int64_t stages) { return 128 + kGatherBarrierBytes + stages * chunk * 2; }
+
 template <typename CP>
-cudaError_t launch_gathers(int dev, const std::vector<Copy>& copies, CP& P, cudaStream_t s)
+cudaError_t launch_bulk_gather(int dev, CP& P, const GatherCfg& g, cudaStream_t s)
+{
+    P.err = g.err;
+    P.wait_ns = g.wait_ns;
+    P.chunk = g.chunk;
+    P.stages = g.stages;
+    int64_t chunks = 0;
+    for (int i = 0; i < P.n_seg; ++i) {
+        P.seg[i].cbeg = chunks;
+        chunks += (8 * P.seg[i].nvec + g.chunk - 1) / g.chunk;
+    }
+    P.n_chunks = chunks;
+    const int64_t smem = gather_smem_bytes(g.chunk, g.stages);
+    int per_sm = 0;
+    const cudaError_t e = residency<bulk_gather_kernel<CP>, kGatherThreads>(dev, smem, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t scalar_blocks = ((int64_t)P.n_seg * kScalarSlots + kGatherThreads - 1) / kGatherThreads;
+    int64_t grid = std::min<int64_t>((int64_t)device_sms(dev) * per_sm, std::max(chunks, scalar_blocks));
+    grid = std::max<int64_t>(1, grid);
+    bulk_gather_kernel<CP><<<(int)grid, kGatherThreads, (size_t)smem, s>>>(P);
+    return cudaGetLastError();
+}
+
+// Launch the gather over `copies`, CP::seg's capacity at a time.
+template <typename CP>
+cudaError_t launch_gathers(int dev, const std::vector<Copy>& copies, CP& P, const GatherCfg& g,
+                           cudaStream_t s)
 {
     const size_t cap = sizeof(P.seg) / sizeof(P.seg[0]);
     for (size_t c0 = 0; c0 < copies.size(); c0 += cap) {
@@ -1433,9 +1631,14 @@ cudaError_t launch_gathers(int dev, const std::vector<Copy>& copies, CP& P, cuda
         }
         P.total_vec = acc;
         const int64_t work = std::max<int64_t>(acc, (int64_t)P.n_seg * kScalarSlots);
-        if (vec) gather_kernel<8, CP><<<grid_for(gather_kernel<8, CP>, dev, work), kThreads, 0, s>>>(P);
-        else gather_kernel<1, CP><<<grid_for(gather_kernel<1, CP>, dev, work), kThreads, 0, s>>>(P);
-        const cudaError_t e = cudaGetLastError();
+        cudaError_t e;
+        if (vec && g.bulk && g.err) {
+            e = launch_bulk_gather(dev, P, g, s);
+        } else {
+            if (vec) gather_kernel<8, CP><<<grid_for(gather_kernel<8, CP>, dev, work), kThreads, 0, s>>>(P);
+            else gather_kernel<1, CP><<<grid_for(gather_kernel<1, CP>, dev, work), kThreads, 0, s>>>(P);
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -1717,6 +1920,28 @@ zero_status_t zero_set_option(zero_plan_t* p, int option, int64_t value)
             return fail(ZERO_EINVAL, "zero_set_option: stages must be 0 or in [2, 16]");
         stages = value;
         break;
+    case ZERO_OPT_GATHER_STAGING:
+        if (value != ZERO_STAGING_REGISTER_LOADS && value != ZERO_STAGING_BULK &&
+            value != ZERO_STAGING_AUTO)
+            return fail(ZERO_EINVAL, "zero_set_option: gather staging must be 0, 1 or 2");
+        p->gather_staging = (int)value;
+        return ZERO_OK;
+    case ZERO_OPT_GATHER_CHUNK:
+    case ZERO_OPT_GATHER_STAGES: {
+        const bool is_chunk = option == ZERO_OPT_GATHER_CHUNK;
+        if (is_chunk && value != 0 && (value < 8 || value > kGatherMaxChunk || value % 8 != 0))
+            return fail(ZERO_EINVAL, "zero_set_option: gather chunk must be 0 or a multiple of 8 in [8, 32768]");
+        if (!is_chunk && value != 0 && (value < kGatherStoresPending + 1 || value > kGatherMaxStages))
+            return fail(ZERO_EINVAL, "zero_set_option: gather stages must be 0 or in [3, 32]");
+        const int64_t c = is_chunk ? value : p->gather_chunk;
+        const int64_t n = is_chunk ? p->gather_stages : value;
+        int64_t gcap = 227 * 1024;
+        if (p->device >= 0 && optin_smem(p->device) > 0) gcap = std::min<int64_t>(gcap, optin_smem(p->device));
+        if (gather_smem_bytes(c > 0 ? c : kGatherDefaultChunk, n > 0 ? n : kGatherDefaultStages) > gcap)
+            return fail(ZERO_ERANGE, "zero_set_option: the gather ring does not fit one block's shared memory");
+        (is_chunk ? p->gather_chunk : p->gather_stages) = (int)value;
+        return ZERO_OK;
+    }
     default:
         return fail(ZERO_EINVAL, "zero_set_option: unknown option");
     }
@@ -1745,6 +1970,9 @@ zero_status_t zero_get_option(const zero_plan_t* p, int option, int64_t* value)
                                     : auto_bulk_stages((int)(p->bulk_tile > 0 ? p->bulk_tile : auto_bulk_tile(p->n_d)), p->n_d);
         return ZERO_OK;
     case ZERO_OPT_LAST_STEP_KERNEL: *value = p->last_step_kernel; return ZERO_OK;
+    case ZERO_OPT_GATHER_STAGING: *value = p->gather_staging; return ZERO_OK;
+    case ZERO_OPT_GATHER_CHUNK: *value = p->gather_chunk > 0 ? p->gather_chunk : kGatherDefaultChunk; return ZERO_OK;
+    case ZERO_OPT_GATHER_STAGES: *value = p->gather_stages > 0 ? p->gather_stages : kGatherDefaultStages; return ZERO_OK;
     default: return fail(ZERO_EINVAL, "zero_get_option: unknown option");
     }
 }
@@ -1984,14 +2212,20 @@ zero_status_t zero_gather_layer(zero_plan_t* p, int64_t unit, void* full_unit16,
             copies.push_back({p->ranks[(size_t)r].shard16 + p->phys_off[(size_t)r][(size_t)unit],
                               (uint16_t*)full_unit16 + r * U.shard, U.shard});
     }
+    GatherCfg g;
+    g.bulk = p->gather_staging != ZERO_STAGING_REGISTER_LOADS;
+    g.chunk = p->gather_chunk > 0 ? p->gather_chunk : kGatherDefaultChunk;
+    g.stages = p->gather_stages > 0 ? p->gather_stages : kGatherDefaultStages;
+    g.err = p->workspace ? &dev_state(p)->error : nullptr;   // no workspace: register loads
+    g.wait_ns = (uint64_t)p->wait_limit_ns;
     // one launch per 32 copies, or per 256 with the wide parameter block
     cudaError_t gerr;
     if (copies.size() > (size_t)kMaxSegs) {
         CopyParamsWide P;
-        gerr = launch_gathers(p->device, copies, P, s);
+        gerr = launch_gathers(p->device, copies, P, g, s);
     } else {
         CopyParams P;
-        gerr = launch_gathers(p->device, copies, P, s);
+        gerr = launch_gathers(p->device, copies, P, g, s);
     }
     if (gerr != cudaSuccess) return cuda_fail(gerr, "gather launch");
     p->gathered[(size_t)unit] = 1;
