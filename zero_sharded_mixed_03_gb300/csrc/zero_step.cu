@@ -673,16 +673,6 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_co
     if (warp < kBulkConsumers) {
         const int ct = threadIdx.x;
         constexpr int kCT = 32 * kBulkConsumers;
-        // unaligned heads and tails: plain loads
-        for (int64_t q = (int64_t)blockIdx.x * kCT + ct; q < (int64_t)P.n_seg * kScalarSlots;
-             q += (int64_t)gridDim.x * kCT) {
-            const KSeg& S = P.seg[q / kScalarSlots];
-            const int k = (int)(q % kScalarSlots);
-            int64_t e = -1;
-            if (k < S.head) e = k;
-            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
-            if (e >= 0) bad |= step_scalar<DT, MODE>(P, S, e, sk, cur, norm2);
-        }
         int s = 0;
         int64_t base = 0;
         uint32_t k = 0;
@@ -700,6 +690,17 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_co
                 bad |= step_quad_staged<DT, MODE>(P, S, buf, T.e0 + 4 * q, q, sk, cur, norm2);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8u * st);
+        }
+        // Unaligned heads and tails (plain loads) after the tiles, from the last blocks first:
+        // round-robin gives the first blocks the extra tile of a partial last round.
+        const int64_t rb = (int64_t)gridDim.x - 1 - blockIdx.x;
+        for (int64_t q = rb * kCT + ct; q < (int64_t)P.n_seg * kScalarSlots; q += (int64_t)gridDim.x * kCT) {
+            const KSeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) bad |= step_scalar<DT, MODE>(P, S, e, sk, cur, norm2);
         }
     } else if (lane == 0) {
         const uint64_t policy = evict_first_policy();
@@ -1160,17 +1161,20 @@ __global__ void __launch_bounds__(kGatherThreads) bulk_gather_kernel(const __gri
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncwarp();
-    // unaligned heads and tails: plain copies by every lane
-    for (int64_t q = (int64_t)blockIdx.x * kGatherThreads + lane; q < (int64_t)P.n_seg * kScalarSlots;
-         q += (int64_t)gridDim.x * kGatherThreads) {
-        const CopySeg& S = P.seg[q / kScalarSlots];
-        const int k = (int)(q % kScalarSlots);
-        int64_t e = -1;
-        if (k < S.head) e = k;
-        else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
-        if (e >= 0) S.dst[e] = S.src[e];
+    if (lane != 0) {
+        // unaligned heads and tails: plain copies by the other lanes, while lane 0 streams
+        constexpr int kLanes = kGatherThreads - 1;
+        for (int64_t q = (int64_t)blockIdx.x * kLanes + (lane - 1); q < (int64_t)P.n_seg * kScalarSlots;
+             q += (int64_t)gridDim.x * kLanes) {
+            const CopySeg& S = P.seg[q / kScalarSlots];
+            const int k = (int)(q % kScalarSlots);
+            int64_t e = -1;
+            if (k < S.head) e = k;
+            else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
+            if (e >= 0) S.dst[e] = S.src[e];
+        }
+        return;
     }
-    if (lane != 0) return;
     const uint64_t policy = evict_first_policy();
     const int64_t grid = gridDim.x;
     const int64_t mine = P.n_chunks > blockIdx.x ? (P.n_chunks - 1 - blockIdx.x) / grid + 1 : 0;
@@ -1370,6 +1374,15 @@ struct BulkCfg {
     bool automatic = false;
 };
 
+// Units of `unit` elements over the vector bodies of a launch's segments.
+template <typename SegT>
+int64_t units_over(const SegT* seg, int n_seg, int64_t unit)
+{
+    int64_t n = 0;
+    for (int i = 0; i < n_seg; ++i) n += (8 * seg[i].nvec + unit - 1) / unit;
+    return n;
+}
+
 // Where the staged kernel beats register loads, from sweeps of N_d = 1 .. 128 on GB300 (ragged
 // ZeRO-2 step): with exactly two blocks per SM (8 consumer warps, 75-110 KB rings) and tiles of
 // 512 elements or more it won almost everywhere (by up to 7 %; lost 1-2 % at N_d = 10-11);
@@ -1474,17 +1487,17 @@ cudaError_t launch_bulk_mode(int dev, PT& P, const BulkCfg& B, int per_sm, cudaS
 {
     auto kernel = bulk_step_kernel<DT, MODE, PT>;
     const int64_t smem = bulk_smem_bytes(B.tile, B.stages, P.n_d);
+    int64_t slots = (int64_t)device_sms(dev) * per_sm;
+    if (P.partials) slots = std::min<int64_t>(slots, kNormSlots);
     P.tile = B.tile;
     P.stages = B.stages;
     P.wait_ns = B.wait_ns;
-    int64_t tiles = 0;
-    for (int i = 0; i < P.n_seg; ++i) tiles += (8 * P.seg[i].nvec + B.tile - 1) / B.tile;
+    const int64_t tiles = units_over(P.seg, P.n_seg, P.tile);
     P.n_tiles = tiles;
     const int64_t scalar_blocks = ((int64_t)P.n_seg * kScalarSlots + 32 * kBulkConsumers - 1) /
                                   (32 * kBulkConsumers);
-    int64_t grid = std::min<int64_t>((int64_t)device_sms(dev) * per_sm, std::max(tiles, scalar_blocks));
+    int64_t grid = std::min<int64_t>(slots, std::max(tiles, scalar_blocks));
     grid = std::max<int64_t>(1, grid);
-    if (P.partials) grid = std::min<int64_t>(grid, kNormSlots);
     kernel<<<(int)grid, kBulkThreads, (size_t)smem, st>>>(P);
     return cudaGetLastError();
 }
@@ -1576,6 +1589,11 @@ int64_t gather_smem_bytes(int64_t chunk, int64_t stages) { return 128 + kGatherB
 template <typename CP>
 cudaError_t launch_bulk_gather(int dev, CP& P, const GatherCfg& g, cudaStream_t s)
 {
+    const int64_t smem = gather_smem_bytes(g.chunk, g.stages);
+    int per_sm = 0;
+    const cudaError_t e = residency<bulk_gather_kernel<CP>, kGatherThreads>(dev, smem, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = (int64_t)device_sms(dev) * per_sm;
     P.err = g.err;
     P.wait_ns = g.wait_ns;
     P.chunk = g.chunk;
@@ -1583,15 +1601,11 @@ cudaError_t launch_bulk_gather(int dev, CP& P, const GatherCfg& g, cudaStream_t 
     int64_t chunks = 0;
     for (int i = 0; i < P.n_seg; ++i) {
         P.seg[i].cbeg = chunks;
-        chunks += (8 * P.seg[i].nvec + g.chunk - 1) / g.chunk;
+        chunks += (8 * P.seg[i].nvec + P.chunk - 1) / P.chunk;
     }
     P.n_chunks = chunks;
-    const int64_t smem = gather_smem_bytes(g.chunk, g.stages);
-    int per_sm = 0;
-    const cudaError_t e = residency<bulk_gather_kernel<CP>, kGatherThreads>(dev, smem, &per_sm);
-    if (e != cudaSuccess) return e;
-    const int64_t scalar_blocks = ((int64_t)P.n_seg * kScalarSlots + kGatherThreads - 1) / kGatherThreads;
-    int64_t grid = std::min<int64_t>((int64_t)device_sms(dev) * per_sm, std::max(chunks, scalar_blocks));
+    const int64_t scalar_blocks = ((int64_t)P.n_seg * kScalarSlots + kGatherThreads - 2) / (kGatherThreads - 1);
+    int64_t grid = std::min<int64_t>(slots, std::max(chunks, scalar_blocks));
     grid = std::max<int64_t>(1, grid);
     bulk_gather_kernel<CP><<<(int)grid, kGatherThreads, (size_t)smem, s>>>(P);
     return cudaGetLastError();
