@@ -38,8 +38,8 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_step.cu); reported as null once that source
 # changes.  Captures: profiles/*_ncu_full.md.
-MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("812e4f0cefa222d3", 2_287_424_768),
-                    (1, "fused_step_kernel"): ("812e4f0cefa222d3", 2_304_896_768)}
+MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("f8477ab68368ac75", 2_287_153_408),
+                    (1, "fused_step_kernel"): ("f8477ab68368ac75", 2_303_013_632)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_step.cu")
 
 
