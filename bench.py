@@ -38,8 +38,8 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_step.cu); reported as null once that source
 # changes.  Captures: profiles/*_ncu_full.md.
-MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("f8477ab68368ac75", 2_287_153_408),
-                    (1, "fused_step_kernel"): ("f8477ab68368ac75", 2_303_013_632)}
+MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("98d53f89377b08cd", 2_287_540_736),
+                    (1, "fused_step_kernel"): ("98d53f89377b08cd", 2_304_309_504)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_step.cu")
 
 
@@ -325,18 +325,37 @@ class Bench:
         fused, gathers = [], []
         all_items = 0
         for which, lo, hi in self.calls:
+            # element counts of the call's work items, in the library's launch order
             if w.per_param:
-                items = sum(1 for c in self.g.chunks if c[1] == which and c[4] > 0 and c[0] in bound)
+                sizes = [c[4] * c[5] for c in self.g.chunks if c[1] == which and c[4] > 0 and c[0] in bound]
                 copies = sum(1 for c in self.g.chunks if c[1] == which and c[4] > 0)
             elif w.stage == 3:
-                items = len(bound) if self.units[which][4] > 0 else 0
-                copies = w.n_d if self.units[which][4] > 0 else 0
+                shard = self.units[which][4]
+                sizes = [shard for r in sorted(bound)] if shard > 0 else []
+                copies = w.n_d if shard > 0 else 0
             else:
                 S = self.units[0][4]
-                items = sum(1 for r in bound if max(lo, r * S) < min(hi, (r + 1) * S))
+                sizes = [min(hi, (r + 1) * S) - max(lo, r * S) for r in sorted(bound)
+                         if max(lo, r * S) < min(hi, (r + 1) * S)]
                 copies = 0
+            items = len(sizes)
             all_items += items if w.stage == 3 else 0
-            fused.append(launches(items))
+            if w.offload:
+                # a flag-only pass over the call, then the writing reduction in groups of
+                # items of >= 4M elements, each group launched in pieces of the call's capacity
+                cap = 32 if items <= 32 else 256
+                n = launches(items)
+                k = 0
+                while k < items:
+                    e, acc = k, 0
+                    while e < items and acc < (1 << 22):
+                        acc += sizes[e]
+                        e += 1
+                    n += -(-(e - k) // cap)
+                    k = e
+                fused.append(n)
+            else:
+                fused.append(launches(items))
             gathers.append(launches(copies))
         if w.stage != 3:
             all_items = len(bound)
@@ -535,7 +554,7 @@ def gpu_arm(args, world, rank, local):
                 "launches_timed": len(fused_ms)}
     if not fused_ms or w.offload:                   # overlapped / offloaded: no fused kernel
         roofline = None
-    if gather_ms:
+    if gather_ms and roofline is not None:
         g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
         roofline["gather_achieved_gbs"] = round(g_bytes / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
         gstaging = Z.zero_get_option(b.g.plan, Z.ZERO_OPT_GATHER_STAGING)

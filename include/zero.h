@@ -361,16 +361,21 @@ zero_status_t zero_bind_offload(zero_plan_t* plan, int rank, float* master, floa
 
 /* Offloaded counterpart of zero_step: reduces bucket / unit `which` on the GPU (same
  * contributions, scaling and non-finite flag) and writes the averaged gradient into the bound
- * ranks' grad_host.  No gradient-norm options. */
+ * ranks' grad_host.  It first runs the reduction for the non-finite flag alone (no writes),
+ * then the writing reduction in groups of segments of at least 4M elements, an event after
+ * each group.  No gradient-norm options. */
 zero_status_t zero_offload_step(zero_plan_t* plan, const void* const* grad_contribs,
                                 int64_t n_contribs, int64_t which, const zero_hyper_t* hyper,
                                 void* stream);
 
-/* End an offloaded step: synchronises `stream`, then `threads` CPU threads apply AdamW to the
- * host state (or, if the flag is set, re-cast the unchanged master) with the same fp32
- * operation order as the GPU kernel, the 16-bit parameters are copied to the all-gather
- * destination on `stream`, and the commit kernel updates t / the loss scale.  out as for
- * zero_step_finish. */
+/* End an offloaded step.  Once the step's last flag pass is done, the step state is read on
+ * a side stream.  Then `threads` CPU threads apply AdamW to the host state with the same fp32
+ * operation order as the GPU kernel, each group of segments as soon as its gradient has
+ * landed.  Finished ranges of 16-bit parameters are copied to the all-gather destination on
+ * `stream` while the rest is still being updated.  If the flag is set, the call waits for
+ * every gradient and re-casts the unchanged master instead.  Then the commit kernel updates
+ * t / the loss scale.  Returns when the host update is complete (the copies and the commit
+ * are enqueued on `stream`); out as for zero_step_finish. */
 zero_status_t zero_offload_finish(zero_plan_t* plan, int threads, void* stream,
                                   zero_step_result_t* out);
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <functional>
 #include <string>
 #include <vector>
 
@@ -51,6 +52,17 @@ struct CpuSpan {
 // `threads` threads; k = the nine fp32 step constants.
 void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16, bool skipped,
                int threads);
+
+// The same update while the gradient is still arriving, in groups of spans (group_of_span,
+// non-decreasing): on the calling thread, wait_group(g) is called for g = 0, 1, ... and
+// returns once group g's gradient is in host memory (false: give up); the threads update the
+// spans of every group released so far, and copied(span, offset, n) is called on the calling
+// thread, in span order, for finished ranges of 16-bit parameters (false: give up).  Returns
+// false if a callback gave up; every thread has stopped by then.
+bool cpu_adamw_overlapped(const std::vector<CpuSpan>& spans, const std::vector<int>& group_of_span,
+                          const float k[9], int dtype16, int threads,
+                          const std::function<bool(int)>& wait_group,
+                          const std::function<bool(size_t, int64_t, int64_t)>& copied);
 
 // Elementwise work item of one launch: n elements of one rank's shard.
 //   contributions: element c_off of every contribution buffer
@@ -141,6 +153,14 @@ struct zero_plan {
     // Overlapped stage-3 schedule: CUDA events (created on first use, released by
     // zero_plan_destroy through the hook the device side installs).
     void* ov_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    // ZeRO-Offload step in flight: its segments in launch order, the end (index into
+    // off_segs) of each reduction group, one CUDA event per group (a pool), the event after
+    // the last flag pass, and a side stream that reads the step state once that event is done.
+    std::vector<zero::Segment> off_segs;
+    std::vector<size_t> off_group_end;
+    std::vector<void*> off_events;
+    void* off_flag_event = nullptr;
+    void* off_side = nullptr;
     void (*release_hook)(zero_plan*) = nullptr;
 };
 

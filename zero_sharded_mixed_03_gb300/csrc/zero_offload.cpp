@@ -13,8 +13,12 @@
 // -fno-math-errno the loops vectorise (IEEE division and square root have exact vector forms
 // on Arm and x86; errno would only be set for a negative square-root argument, and v >= 0).
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
+#include <condition_variable>
 #include <cstring>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -99,11 +103,16 @@ void recast_span(const CpuSpan& s)
 
 }  // namespace
 
+namespace {
+
+constexpr int64_t kPiece = 1 << 16;          // elements per unit of work of one thread
+
+}  // namespace
+
 void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16, bool skipped,
                int threads)
 {
     // Cut the spans into pieces of ~64K elements and deal them to the threads in turn.
-    constexpr int64_t kPiece = 1 << 16;
     std::vector<CpuSpan> pieces;
     for (const CpuSpan& s : spans)
         for (int64_t o = 0; o < s.n; o += kPiece) {
@@ -138,6 +147,109 @@ void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
     for (int t = 1; t < nt; ++t) pool.emplace_back(work, t);
     work(0);
     for (auto& th : pool) th.join();
+}
+
+bool cpu_adamw_overlapped(const std::vector<CpuSpan>& spans, const std::vector<int>& group_of_span,
+                          const float k[9], int dtype16, int threads,
+                          const std::function<bool(int)>& wait_group,
+                          const std::function<bool(size_t, int64_t, int64_t)>& copied)
+{
+    // Pieces of ~64K elements in span order; the threads take them in that order (one shared
+    // counter), each once its group has been released.
+    struct Piece {
+        size_t span;
+        int64_t off, n;
+        int group;
+    };
+    std::vector<Piece> pieces;
+    for (size_t i = 0; i < spans.size(); ++i)
+        for (int64_t o = 0; o < spans[i].n; o += kPiece)
+            pieces.push_back(Piece{i, o, std::min(kPiece, spans[i].n - o), group_of_span[i]});
+    const int64_t np = (int64_t)pieces.size();
+    const int n_groups = spans.empty() ? 0 : group_of_span.back() + 1;
+    std::vector<std::atomic<unsigned char>> done((size_t)np);
+    for (auto& d : done) d.store(0, std::memory_order_relaxed);
+    std::atomic<int64_t> next{0}, n_done{0};
+    std::mutex mu;
+    std::condition_variable released_cv, progress_cv;
+    int released = -1;              // groups [0, released] may be updated (guarded by mu)
+    bool stop = false;              // give up (guarded by mu)
+
+    auto worker = [&]() {
+        for (;;) {
+            const int64_t i = next.fetch_add(1);
+            if (i >= np) return;
+            const Piece& pc = pieces[(size_t)i];
+            {
+                std::unique_lock<std::mutex> lock(mu);
+                released_cv.wait(lock, [&] { return stop || released >= pc.group; });
+                if (stop) return;
+            }
+            CpuSpan q = spans[pc.span];
+            q.master += pc.off;
+            q.m += pc.off;
+            q.v += pc.off;
+            q.grad += pc.off;
+            q.out16 += pc.off;
+            q.n = pc.n;
+            if (dtype16 == ZERO_FP16) adamw_span<true>(q, k);
+            else adamw_span<false>(q, k);
+            done[(size_t)i].store(1, std::memory_order_release);
+            n_done.fetch_add(1, std::memory_order_release);
+            progress_cv.notify_one();
+        }
+    };
+    const int nt = std::max(1, std::min<int>(threads, (int)std::max<int64_t>(1, np)));
+    std::vector<std::thread> pool;
+    for (int t = 0; t < nt; ++t) pool.emplace_back(worker);
+
+    // Hand back the finished prefix of pieces, merged into runs of >= 1M elements per span
+    // (or the span's end, or everything once `final`).
+    int64_t handed = 0;             // pieces handed back
+    bool ok = true;
+    auto flush = [&](bool final) {
+        while (ok && handed < np && done[(size_t)handed].load(std::memory_order_acquire)) {
+            const size_t sp = pieces[(size_t)handed].span;
+            int64_t end = handed;
+            while (end < np && pieces[(size_t)end].span == sp && done[(size_t)end].load(std::memory_order_acquire))
+                ++end;
+            const int64_t off = pieces[(size_t)handed].off;
+            const int64_t n = pieces[(size_t)end - 1].off + pieces[(size_t)end - 1].n - off;
+            const bool span_done = end == np || pieces[(size_t)end].span != sp;
+            if (!final && !span_done && n < (int64_t)1 << 20) return;
+            ok = copied(sp, off, n);
+            handed = end;
+        }
+    };
+    auto give_up = [&]() {
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            stop = true;
+        }
+        released_cv.notify_all();
+    };
+    for (int g = 0; g < n_groups && ok; ++g) {
+        if (!wait_group(g)) {
+            ok = false;
+            break;
+        }
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            released = g;
+        }
+        released_cv.notify_all();
+        flush(false);
+    }
+    while (ok && handed < np) {
+        {
+            std::unique_lock<std::mutex> lock(mu);
+            progress_cv.wait_for(lock, std::chrono::milliseconds(1));
+        }
+        flush(n_done.load(std::memory_order_acquire) == np);
+    }
+    if (!ok) give_up();
+    for (auto& th : pool) th.join();
+    return ok;
 }
 
 }  // namespace zero

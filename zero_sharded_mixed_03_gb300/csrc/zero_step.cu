@@ -815,7 +815,9 @@ __global__ void __launch_bounds__(kThreads) grad_norm_kernel(const __grid_consta
 
 // ZeRO-Offload: the reduction of the fused kernel, its averaged gradient written into the
 // rank's pinned host buffer (S.p[0]) over NVLink-C2C instead of feeding an on-GPU update.
-template <int DT, int NB, int VEC, typename PT>
+// STORE = false: the same reduction writing nothing, for the step's non-finite flag alone (a
+// pass over HBM that lets the host know the skip decision before the gradients have landed).
+template <int DT, int NB, int VEC, typename PT, bool STORE>
 __global__ void __launch_bounds__(kThreads) reduce_to_host_kernel(const __grid_constant__ PT P)
 {
     __shared__ float sk4[4];
@@ -830,7 +832,7 @@ __global__ void __launch_bounds__(kThreads) reduce_to_host_kernel(const __grid_c
         for (int r = 0; r < P.n_d; ++r) sum = __fadd_rn(sum, widen1<DT>(P.c[r][S.c_off + e]));
         const float g = __fmul_rn(sum, inv);
         bad |= nonfinite(g);
-        S.p[0][e] = g;
+        if constexpr (STORE) S.p[0][e] = g;
     };
     if constexpr (VEC == 8) {
         for (int64_t q = tid; q < (int64_t)P.n_seg * kScalarSlots; q += stride) {
@@ -880,7 +882,7 @@ __global__ void __launch_bounds__(kThreads) reduce_to_host_kernel(const __grid_c
                 g[j] = __fmul_rn(acc[j], inv);
                 bad |= nonfinite(g[j]);
             }
-            *reinterpret_cast<float4*>(S.p[0] + e) = make_float4(g[0], g[1], g[2], g[3]);
+            if constexpr (STORE) *reinterpret_cast<float4*>(S.p[0] + e) = make_float4(g[0], g[1], g[2], g[3]);
         } else {
             one(S, vi - S.vbeg);
         }
@@ -1549,14 +1551,14 @@ cudaError_t launch_norm(int dev, PT& P, bool vec, cudaStream_t st)
     return cudaGetLastError();
 }
 
-template <int DT, typename PT>
+template <int DT, bool STORE, typename PT>
 cudaError_t launch_reduce_to_host(int dev, PT& P, bool vec, cudaStream_t st)
 {
     finalize_vectors(P, vec);
     const int64_t work = std::max<int64_t>(2 * P.total_vec, (int64_t)P.n_seg * kScalarSlots);
-    if (!vec) launch_grid(reduce_to_host_kernel<DT, 1, 1, PT>, dev, work, P, st);
-    else if (P.n_d >= kWideNormBatchFrom) launch_grid(reduce_to_host_kernel<DT, kWideRankBatch, 8, PT>, dev, work, P, st);
-    else launch_grid(reduce_to_host_kernel<DT, kRankBatch, 8, PT>, dev, work, P, st);
+    if (!vec) launch_grid(reduce_to_host_kernel<DT, 1, 1, PT, STORE>, dev, work, P, st);
+    else if (P.n_d >= kWideNormBatchFrom) launch_grid(reduce_to_host_kernel<DT, kWideRankBatch, 8, PT, STORE>, dev, work, P, st);
+    else launch_grid(reduce_to_host_kernel<DT, kRankBatch, 8, PT, STORE>, dev, work, P, st);
     return cudaGetLastError();
 }
 
@@ -1806,6 +1808,46 @@ void fill_call_params(const zero_plan* p, const void* const* grad_contribs, PT& 
     P.flag = &dev_state(p)->flag;
     P.partials = norm_slots(p);
     P.max_norm = 0.0;
+}
+
+// ZeRO-Offload: elements per reduction group (an event after each; the host starts updating
+// a group once its gradient has landed): 4M elements, 16 MB of fp32 gradient.
+constexpr int64_t kOffloadGroupElems = 1 << 22;
+
+// The CUDA objects a plan creates on first use, released by zero_plan_destroy.
+void release_plan_cuda(zero_plan* q)
+{
+    for (void*& ev : q->ov_events)
+        if (ev) {
+            cudaEventDestroy((cudaEvent_t)ev);
+            ev = nullptr;
+        }
+    for (void*& ev : q->off_events)
+        if (ev) {
+            cudaEventDestroy((cudaEvent_t)ev);
+            ev = nullptr;
+        }
+    if (q->off_flag_event) {
+        cudaEventDestroy((cudaEvent_t)q->off_flag_event);
+        q->off_flag_event = nullptr;
+    }
+    if (q->off_side) {
+        cudaStreamDestroy((cudaStream_t)q->off_side);
+        q->off_side = nullptr;
+    }
+}
+
+// Create the event in *slot unless it exists: no timing, and a host thread that waits for it
+// sleeps instead of spinning (the offload update's threads need the cores).
+cudaError_t offload_event(zero_plan* p, void** slot)
+{
+    if (*slot) return cudaSuccess;
+    cudaEvent_t ev;
+    const cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming | cudaEventBlockingSync);
+    if (e != cudaSuccess) return e;
+    *slot = ev;
+    p->release_hook = release_plan_cuda;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -2361,27 +2403,60 @@ zero_status_t zero_offload_step(zero_plan_t* p, const void* const* grad_contribs
         p->step_hyper = *hyper;
     }
     const std::vector<Segment> segs = step_segments(p, which, 0);
-    auto run = [&](auto& P, size_t cap) -> cudaError_t {
-        for (size_t b = 0; b < segs.size(); b += cap) {
-            const size_t e = std::min(segs.size(), b + cap);
+    if (!p->in_step) {
+        p->off_segs.clear();
+        p->off_group_end.clear();
+    }
+    // Reduce segs[b0, e0) (store: into host memory; else: the flag alone), cap items a launch.
+    auto run = [&](auto& P, size_t cap, size_t b0, size_t e0, bool store) -> cudaError_t {
+        for (size_t b = b0; b < e0; b += cap) {
+            const size_t e = std::min(e0, b + cap);
             fill_call_params(p, grad_contribs, P);
             const bool vec = build_offload_params(p, segs, b, e, grad_contribs, P);
-            const cudaError_t err = p->dtype16 == ZERO_BF16
-                                        ? launch_reduce_to_host<ZERO_BF16>(p->device, P, vec, s)
-                                        : launch_reduce_to_host<ZERO_FP16>(p->device, P, vec, s);
+            cudaError_t err;
+            if (p->dtype16 == ZERO_BF16)
+                err = store ? launch_reduce_to_host<ZERO_BF16, true>(p->device, P, vec, s)
+                            : launch_reduce_to_host<ZERO_BF16, false>(p->device, P, vec, s);
+            else
+                err = store ? launch_reduce_to_host<ZERO_FP16, true>(p->device, P, vec, s)
+                            : launch_reduce_to_host<ZERO_FP16, false>(p->device, P, vec, s);
             if (err != cudaSuccess) return err;
         }
         return cudaSuccess;
     };
+    // First the flag over the whole call (so that, after the step's last call, the host knows
+    // the skip decision early), then the reduction in groups of segments of at least
+    // kOffloadGroupElems elements, an event after each: the host updates a group as soon as
+    // its gradient has landed.
+    auto reduce_all = [&](auto& P, size_t cap) -> cudaError_t {
+        cudaError_t err = run(P, cap, 0, segs.size(), false);
+        if (err == cudaSuccess) err = offload_event(p, &p->off_flag_event);
+        if (err == cudaSuccess) err = cudaEventRecord((cudaEvent_t)p->off_flag_event, s);
+        size_t b = 0;
+        while (err == cudaSuccess && b < segs.size()) {
+            size_t e = b;
+            int64_t n = 0;
+            while (e < segs.size() && n < kOffloadGroupElems) n += segs[e++].n;
+            err = run(P, cap, b, e, true);
+            const size_t g = p->off_group_end.size();
+            if (g >= p->off_events.size()) p->off_events.push_back(nullptr);
+            if (err == cudaSuccess) err = offload_event(p, &p->off_events[g]);
+            if (err == cudaSuccess) err = cudaEventRecord((cudaEvent_t)p->off_events[g], s);
+            p->off_group_end.push_back(p->off_segs.size() + e);
+            b = e;
+        }
+        return err;
+    };
     cudaError_t err;
     if (segs.size() > (size_t)kMaxSegs) {
         StepParamsWide P;
-        err = run(P, kWideSegs);
+        err = reduce_all(P, kWideSegs);
     } else {
         StepParams P;
-        err = run(P, kMaxSegs);
+        err = reduce_all(P, kMaxSegs);
     }
     if (err != cudaSuccess) return cuda_fail(err, "reduce-to-host launch");
+    p->off_segs.insert(p->off_segs.end(), segs.begin(), segs.end());
     p->in_step = true;
     if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
     else p->covered[(size_t)which] = 1;
@@ -2399,29 +2474,67 @@ zero_status_t zero_offload_finish(zero_plan_t* p, int threads, void* stream, zer
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    // the gradients are in host memory once the stream is drained; t and the scale decide
-    // the constants, the flag decides between the update and the re-cast
+    // t and the scale decide the constants, the flag decides between the update and the
+    // re-cast: read them on a side stream as soon as the step's last flag pass is done, while
+    // the reductions are still streaming the gradients into host memory.
+    cudaError_t e = cudaSuccess;
+    if (!p->off_side) {
+        cudaStream_t side;
+        e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: side stream");
+        p->off_side = side;
+        p->release_hook = release_plan_cuda;
+    }
+    cudaStream_t side = (cudaStream_t)p->off_side;
     DevState host;
-    cudaError_t e = cudaMemcpyAsync(&host, p->workspace, sizeof(host), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    e = cudaStreamWaitEvent(side, (cudaEvent_t)p->off_flag_event, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&host, p->workspace, sizeof(host), cudaMemcpyDeviceToHost, side);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(side);
     if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: reading the step state");
     float k9[9];
     step_constants(p->step_hyper, host.t + 1, host.scale, p->n_d, k9);
-    const std::vector<Segment> segs = shard_segments_all(p);
+    const std::vector<Segment>& segs = p->off_segs;
     std::vector<CpuSpan> spans;
-    for (const Segment& sg : segs) {
+    std::vector<int> group_of_span;
+    int g = 0;
+    for (size_t i = 0; i < segs.size(); ++i) {
+        while (i >= p->off_group_end[(size_t)g]) ++g;
+        const Segment& sg = segs[i];
         const Rank& R = p->ranks[(size_t)sg.rank];
         spans.push_back(CpuSpan{R.master[0] + sg.s_off, R.m[0] + sg.s_off, R.v[0] + sg.s_off,
                                 R.grad_host + sg.s_off, R.param16_host + sg.s_off, sg.n});
+        group_of_span.push_back(g);
     }
-    cpu_adamw(spans, k9, p->dtype16, host.flag != 0, threads > 0 ? threads : 1);
-    // 16-bit parameters back to the all-gather destination
-    for (const Segment& sg : segs) {
+    // 16-bit parameters [off, off + n) of segment i back to the all-gather destination
+    auto copy_back = [&](size_t i, int64_t off, int64_t n) -> cudaError_t {
+        const Segment& sg = segs[i];
         const Rank& R = p->ranks[(size_t)sg.rank];
-        e = cudaMemcpyAsync(sg.out16 + sg.o_off, R.param16_host + sg.s_off, 2 * (size_t)sg.n,
-                            cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: copying the parameters");
+        return cudaMemcpyAsync(sg.out16 + sg.o_off + off, R.param16_host + sg.s_off + off, 2 * (size_t)n,
+                               cudaMemcpyHostToDevice, s);
+    };
+    const int nt = threads > 0 ? threads : 1;
+    if (host.flag != 0) {
+        // skipped step: every gradient lands first, then the re-cast of the unchanged master
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: waiting for the reductions");
+        cpu_adamw(spans, k9, p->dtype16, true, nt);
+        for (size_t i = 0; i < segs.size() && e == cudaSuccess; ++i) e = copy_back(i, 0, segs[i].n);
+    } else {
+        // the update of each group starts once its gradient has landed; finished ranges of
+        // 16-bit parameters are copied back while the rest is still being updated
+        const bool ok = cpu_adamw_overlapped(
+            spans, group_of_span, k9, p->dtype16, nt,
+            [&](int grp) {
+                e = cudaEventSynchronize((cudaEvent_t)p->off_events[(size_t)grp]);
+                return e == cudaSuccess;
+            },
+            [&](size_t i, int64_t off, int64_t n) {
+                e = copy_back(i, off, n);
+                return e == cudaSuccess;
+            });
+        if (!ok && e == cudaSuccess) e = cudaErrorUnknown;
     }
+    if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: the host update or the copy back");
     CommitParams C;
     C.st = dev_state(p);
     C.growth = p->scaler.growth_factor;
@@ -2462,13 +2575,7 @@ zero_status_t zero_step_units_overlapped(zero_plan_t* p, const void* const* unit
             if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: event");
             p->ov_events[i] = ev;
         }
-        p->release_hook = [](zero_plan* q) {
-            for (void*& ev : q->ov_events)
-                if (ev) {
-                    cudaEventDestroy((cudaEvent_t)ev);
-                    ev = nullptr;
-                }
-        };
+        p->release_hook = release_plan_cuda;
     }
     cudaStream_t cs = (cudaStream_t)compute_stream, ms = (cudaStream_t)comm_stream;
     cudaEvent_t start = (cudaEvent_t)p->ov_events[0];
