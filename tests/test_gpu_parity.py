@@ -596,6 +596,12 @@ OFFLOAD_CASES = {
     "z3_nd3_fp16_peers_skip_first": dataclasses.replace(
         SMALL_CASES["z3_nd3_fp16_peers_skip_first"], wid=163, offload=True),
     "pp_nd4_units": dataclasses.replace(PP_CASES["pp_nd4_units"], wid=164, offload=True),
+    # several reduction groups (>= 4M elements each) spread over two buckets, fp16 with a
+    # skipped second step: the host update of a group starts while later groups and the
+    # second bucket are still being reduced, and the flagged step takes the re-cast path
+    "z2_nd2_fp16_groups_buckets_skip": dataclasses.replace(
+        _mk(165, [9_000_003, 1_700_001], 2, 2, steps=3, bucket=6_000_000, dtype=W.FP16,
+            scaler=W.Scaler(), inject=(2, 1, 8_765_431)), offload=True),
 }
 
 
