@@ -554,6 +554,19 @@ def gpu_arm(args, world, rank, local):
                 "launches_timed": len(fused_ms)}
     if not fused_ms or w.offload:                   # overlapped / offloaded: no fused kernel
         roofline = None
+    if w.offload:
+        # host memory bounds an offloaded step: per parameter the GPU writes the fp32 gradient
+        # (4 B), the host update reads master, m, v and the gradient (16 B) and writes master,
+        # m, v and the 16-bit parameter (14 B), and the copy engines read that parameter back
+        # (2 B): 36 B, against the host's own copy bandwidth measured here with the update's
+        # threads
+        host_peak = host_copy_gbs(b.g.offload_threads)
+        achieved_host = elems * 36 * applied / (ms / 1e3) / 1e9
+        roofline = {"bound": "host memory", "achieved": round(achieved_host, 1),
+                    "peak": round(host_peak, 1), "unit": "GB/s",
+                    "frac": round(achieved_host / host_peak, 4), "traffic": None,
+                    "peak_source": f"measured here: torch CPU copy on {b.g.offload_threads} threads",
+                    "kernel": "host AdamW (zero_offload_finish)"}
     if gather_ms and roofline is not None:
         g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
         roofline["gather_achieved_gbs"] = round(g_bytes / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
@@ -666,6 +679,26 @@ def oracle_sample_run(w, sample_elems: int, steps: int, warmup: int = 0):
         if k > warmup:
             times.append(time.perf_counter() - t)
     return n, times
+
+
+def host_copy_gbs(threads: int, n_bytes: int = 1 << 30, reps: int = 3) -> float:
+    """Host memory copy bandwidth (read + write bytes / s, best of `reps`) of a 1 GB fp32 copy
+    by torch's CPU kernels on `threads` threads."""
+    import time
+    import torch
+    old = torch.get_num_threads()
+    torch.set_num_threads(threads)
+    try:
+        src = torch.ones(n_bytes // 4, dtype=torch.float32)
+        dst = torch.empty_like(src)
+        best = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            dst.copy_(src)
+            best = min(best, time.perf_counter() - t0)
+        return 2 * n_bytes / best / 1e9
+    finally:
+        torch.set_num_threads(old)
 
 
 def cpu_baseline(w, sample_elems: int):
