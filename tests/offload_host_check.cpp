@@ -52,14 +52,14 @@ std::vector<CpuSpan> spans_of(Buffers& b, const std::vector<int64_t>& sizes)
     return s;
 }
 
-int check(const std::vector<int64_t>& sizes, const std::vector<int>& groups, int dtype16, int threads,
-          int fail_at, uint32_t seed)
+int check(zero::WorkerPool* pool, const std::vector<int64_t>& sizes, const std::vector<int>& groups,
+          int dtype16, int threads, int fail_at, uint32_t seed)
 {
     int64_t n = 0;
     for (int64_t x : sizes) n += x;
     Buffers a = make(n, seed), b = make(n, seed);
     const float k[9] = {0.9f, 0.1f, 0.999f, 0.001f, 1e-8f, 1e-5f, 1e-3f, 0.0316f, 0.0f};
-    zero::cpu_adamw(spans_of(a, sizes), k, dtype16, false, threads);
+    zero::cpu_adamw(pool, spans_of(a, sizes), k, dtype16, false, threads);
     std::vector<CpuSpan> sb = spans_of(b, sizes);
     std::mt19937 rng(seed + 1);
     int next_group = 0;
@@ -71,7 +71,7 @@ int check(const std::vector<int64_t>& sizes, const std::vector<int>& groups, int
     std::vector<int64_t> base(sizes.size(), 0);
     for (size_t i = 1; i < sizes.size(); ++i) base[i] = base[i - 1] + sizes[i - 1];
     const bool ok = zero::cpu_adamw_overlapped(
-        sb, groups, k, dtype16, threads,
+        pool, sb, groups, k, dtype16, threads,
         [&](int g) {
             order_ok &= g == next_group++;
             std::this_thread::sleep_for(std::chrono::microseconds(rng() % 3000));
@@ -123,13 +123,20 @@ int check(const std::vector<int64_t>& sizes, const std::vector<int>& groups, int
 int main()
 {
     int bad = 0;
+    // One pool of 12 workers for every call, as a plan keeps its pool from step to step: calls
+    // with fewer threads leave workers idle, and a call that gave up is followed by others.
+    zero::WorkerPool* pool = zero::worker_pool_create(12);
     // (sizes of the spans, group of each span, dtype, threads, wait that gives up)
-    bad += check({5, 70000, 1, 200000, 65536, 3}, {0, 0, 0, 1, 2, 2}, ZERO_BF16, 4, -1, 1);
-    bad += check({1 << 20, 1 << 20, 777777}, {0, 1, 2}, ZERO_FP16, 8, -1, 2);
-    bad += check({300000, 0, 123457}, {0, 1, 1}, ZERO_BF16, 1, -1, 3);
-    bad += check({3000000}, {0}, ZERO_BF16, 16, -1, 4);
-    bad += check({100000, 100000, 100000, 100000}, {0, 1, 2, 3}, ZERO_FP16, 3, 2, 5);
-    bad += check({100000, 100000}, {0, 1}, ZERO_BF16, 2, 0, 6);
+    bad += check(pool, {5, 70000, 1, 200000, 65536, 3}, {0, 0, 0, 1, 2, 2}, ZERO_BF16, 4, -1, 1);
+    bad += check(pool, {1 << 20, 1 << 20, 777777}, {0, 1, 2}, ZERO_FP16, 8, -1, 2);
+    bad += check(pool, {300000, 0, 123457}, {0, 1, 1}, ZERO_BF16, 1, -1, 3);
+    bad += check(pool, {3000000}, {0}, ZERO_BF16, 16, -1, 4);
+    bad += check(pool, {100000, 100000, 100000, 100000}, {0, 1, 2, 3}, ZERO_FP16, 3, 2, 5);
+    bad += check(pool, {100000, 100000}, {0, 1}, ZERO_BF16, 2, 0, 6);
+    for (uint32_t r = 0; r < 20; ++r)
+        bad += check(pool, {70000 + 1000 * r, 65536, 9}, {0, 1, 1}, r % 2 ? ZERO_FP16 : ZERO_BF16,
+                     1 + (int)r % 12, r % 5 == 4 ? 1 : -1, 100 + r);
+    zero::worker_pool_destroy(pool);
     std::printf(bad ? "FAILED %d\n" : "ok\n", bad);
     return bad != 0;
 }

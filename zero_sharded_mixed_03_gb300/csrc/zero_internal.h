@@ -48,10 +48,17 @@ struct CpuSpan {
     int64_t n;
 };
 
+// Host worker threads kept between offloaded steps (creating and joining 16 threads took
+// ~0.3 ms a step on the Grace host).  Idle workers sleep on a condition variable.
+class WorkerPool;
+WorkerPool* worker_pool_create(int threads);
+void worker_pool_destroy(WorkerPool* pool);
+int worker_pool_size(const WorkerPool* pool);
+
 // CPU AdamW (or, for a skipped step, the re-cast of the unchanged master) over the spans, on
-// `threads` threads; k = the nine fp32 step constants.
-void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16, bool skipped,
-               int threads);
+// `threads` workers of `pool` (at most its size); k = the nine fp32 step constants.
+void cpu_adamw(WorkerPool* pool, const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
+               bool skipped, int threads);
 
 // The same update while the gradient is still arriving, in groups of spans (group_of_span,
 // non-decreasing): on the calling thread, wait_group(g) is called for g = 0, 1, ... and
@@ -59,8 +66,8 @@ void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
 // spans of every group released so far, and copied(span, offset, n) is called on the calling
 // thread, in span order, for finished ranges of 16-bit parameters (false: give up).  Returns
 // false if a callback gave up; every thread has stopped by then.
-bool cpu_adamw_overlapped(const std::vector<CpuSpan>& spans, const std::vector<int>& group_of_span,
-                          const float k[9], int dtype16, int threads,
+bool cpu_adamw_overlapped(WorkerPool* pool, const std::vector<CpuSpan>& spans,
+                          const std::vector<int>& group_of_span, const float k[9], int dtype16, int threads,
                           const std::function<bool(int)>& wait_group,
                           const std::function<bool(size_t, int64_t, int64_t)>& copied);
 
@@ -161,6 +168,7 @@ struct zero_plan {
     std::vector<void*> off_events;
     void* off_flag_event = nullptr;
     void* off_side = nullptr;
+    zero::WorkerPool* host_pool = nullptr;   // the host update's threads (created on first use)
     void (*release_hook)(zero_plan*) = nullptr;
 };
 

@@ -18,6 +18,7 @@
 #include <cmath>
 #include <condition_variable>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <thread>
 #include <vector>
@@ -109,8 +110,77 @@ constexpr int64_t kPiece = 1 << 16;          // elements per unit of work of one
 
 }  // namespace
 
-void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16, bool skipped,
-               int threads)
+// Persistent workers: start(n, fn) runs fn(0) .. fn(n - 1) on n workers and returns at once;
+// wait() returns when all of them have returned.  One job at a time.
+class WorkerPool {
+public:
+    explicit WorkerPool(int n)
+    {
+        for (int i = 0; i < n; ++i) threads_.emplace_back([this, i] { loop(i); });
+    }
+    ~WorkerPool()
+    {
+        {
+            std::lock_guard<std::mutex> lock(mu_);
+            quit_ = true;
+        }
+        job_cv_.notify_all();
+        for (auto& t : threads_) t.join();
+    }
+    int size() const { return (int)threads_.size(); }
+    void start(int n, std::function<void(int)> fn)
+    {
+        {
+            std::lock_guard<std::mutex> lock(mu_);
+            fn_ = std::move(fn);
+            active_ = std::min(n, size());
+            running_ = active_;
+            ++generation_;
+        }
+        job_cv_.notify_all();
+    }
+    void wait()
+    {
+        std::unique_lock<std::mutex> lock(mu_);
+        done_cv_.wait(lock, [this] { return running_ == 0; });
+    }
+
+private:
+    void loop(int i)
+    {
+        uint64_t seen = 0;
+        for (;;) {
+            std::function<void(int)> fn;
+            {
+                std::unique_lock<std::mutex> lock(mu_);
+                job_cv_.wait(lock, [&] { return quit_ || generation_ != seen; });
+                if (quit_) return;
+                seen = generation_;
+                if (i >= active_) continue;
+                fn = fn_;
+            }
+            fn(i);
+            {
+                std::lock_guard<std::mutex> lock(mu_);
+                if (--running_ == 0) done_cv_.notify_all();
+            }
+        }
+    }
+    std::vector<std::thread> threads_;
+    std::mutex mu_;
+    std::condition_variable job_cv_, done_cv_;
+    std::function<void(int)> fn_;
+    uint64_t generation_ = 0;
+    int active_ = 0, running_ = 0;
+    bool quit_ = false;
+};
+
+WorkerPool* worker_pool_create(int threads) { return new WorkerPool(std::max(1, threads)); }
+void worker_pool_destroy(WorkerPool* pool) { delete pool; }
+int worker_pool_size(const WorkerPool* pool) { return pool ? pool->size() : 0; }
+
+void cpu_adamw(WorkerPool* pool, const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
+               bool skipped, int threads)
 {
     // Cut the spans into pieces of ~64K elements and deal them to the threads in turn.
     std::vector<CpuSpan> pieces;
@@ -125,7 +195,7 @@ void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
             q.out16 += o;
             pieces.push_back(q);
         }
-    const int nt = std::max(1, std::min<int>(threads, (int)pieces.size()));
+    const int nt = std::max(1, std::min({threads, (int)pieces.size(), pool->size()}));
     auto work = [&](int tid) {
         for (size_t i = (size_t)tid; i < pieces.size(); i += (size_t)nt) {
             const CpuSpan& q = pieces[i];
@@ -139,18 +209,12 @@ void cpu_adamw(const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
             }
         }
     };
-    if (nt == 1) {
-        work(0);
-        return;
-    }
-    std::vector<std::thread> pool;
-    for (int t = 1; t < nt; ++t) pool.emplace_back(work, t);
-    work(0);
-    for (auto& th : pool) th.join();
+    pool->start(nt, work);
+    pool->wait();
 }
 
-bool cpu_adamw_overlapped(const std::vector<CpuSpan>& spans, const std::vector<int>& group_of_span,
-                          const float k[9], int dtype16, int threads,
+bool cpu_adamw_overlapped(WorkerPool* pool, const std::vector<CpuSpan>& spans,
+                          const std::vector<int>& group_of_span, const float k[9], int dtype16, int threads,
                           const std::function<bool(int)>& wait_group,
                           const std::function<bool(size_t, int64_t, int64_t)>& copied)
 {
@@ -175,7 +239,7 @@ bool cpu_adamw_overlapped(const std::vector<CpuSpan>& spans, const std::vector<i
     int released = -1;              // groups [0, released] may be updated (guarded by mu)
     bool stop = false;              // give up (guarded by mu)
 
-    auto worker = [&]() {
+    auto worker = [&](int) {
         for (;;) {
             const int64_t i = next.fetch_add(1);
             if (i >= np) return;
@@ -199,9 +263,8 @@ bool cpu_adamw_overlapped(const std::vector<CpuSpan>& spans, const std::vector<i
             progress_cv.notify_one();
         }
     };
-    const int nt = std::max(1, std::min<int>(threads, (int)std::max<int64_t>(1, np)));
-    std::vector<std::thread> pool;
-    for (int t = 0; t < nt; ++t) pool.emplace_back(worker);
+    const int nt = std::max(1, std::min({threads, (int)std::max<int64_t>(1, np), pool->size()}));
+    pool->start(nt, worker);
 
     // Hand back the finished prefix of pieces, merged into runs of >= 1M elements per span
     // (or the span's end, or everything once `final`).
@@ -248,7 +311,7 @@ bool cpu_adamw_overlapped(const std::vector<CpuSpan>& spans, const std::vector<i
         flush(n_done.load(std::memory_order_acquire) == np);
     }
     if (!ok) give_up();
-    for (auto& th : pool) th.join();
+    pool->wait();
     return ok;
 }
 

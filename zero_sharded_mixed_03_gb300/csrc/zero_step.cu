@@ -1814,9 +1814,14 @@ void fill_call_params(const zero_plan* p, const void* const* grad_contribs, PT& 
 // a group once its gradient has landed): 4M elements, 16 MB of fp32 gradient.
 constexpr int64_t kOffloadGroupElems = 1 << 22;
 
-// The CUDA objects a plan creates on first use, released by zero_plan_destroy.
-void release_plan_cuda(zero_plan* q)
+// The CUDA objects and host threads a plan creates on first use, released by
+// zero_plan_destroy.
+void release_plan_resources(zero_plan* q)
 {
+    if (q->host_pool) {
+        worker_pool_destroy(q->host_pool);
+        q->host_pool = nullptr;
+    }
     for (void*& ev : q->ov_events)
         if (ev) {
             cudaEventDestroy((cudaEvent_t)ev);
@@ -1846,7 +1851,7 @@ cudaError_t offload_event(zero_plan* p, void** slot)
     const cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming | cudaEventBlockingSync);
     if (e != cudaSuccess) return e;
     *slot = ev;
-    p->release_hook = release_plan_cuda;
+    p->release_hook = release_plan_resources;
     return cudaSuccess;
 }
 
@@ -2483,7 +2488,7 @@ zero_status_t zero_offload_finish(zero_plan_t* p, int threads, void* stream, zer
         e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
         if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: side stream");
         p->off_side = side;
-        p->release_hook = release_plan_cuda;
+        p->release_hook = release_plan_resources;
     }
     cudaStream_t side = (cudaStream_t)p->off_side;
     DevState host;
@@ -2513,17 +2518,22 @@ zero_status_t zero_offload_finish(zero_plan_t* p, int threads, void* stream, zer
                                cudaMemcpyHostToDevice, s);
     };
     const int nt = threads > 0 ? threads : 1;
+    if (worker_pool_size(p->host_pool) < nt) {
+        worker_pool_destroy(p->host_pool);
+        p->host_pool = worker_pool_create(nt);
+        p->release_hook = release_plan_resources;
+    }
     if (host.flag != 0) {
         // skipped step: every gradient lands first, then the re-cast of the unchanged master
         e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: waiting for the reductions");
-        cpu_adamw(spans, k9, p->dtype16, true, nt);
+        cpu_adamw(p->host_pool, spans, k9, p->dtype16, true, nt);
         for (size_t i = 0; i < segs.size() && e == cudaSuccess; ++i) e = copy_back(i, 0, segs[i].n);
     } else {
         // the update of each group starts once its gradient has landed; finished ranges of
         // 16-bit parameters are copied back while the rest is still being updated
         const bool ok = cpu_adamw_overlapped(
-            spans, group_of_span, k9, p->dtype16, nt,
+            p->host_pool, spans, group_of_span, k9, p->dtype16, nt,
             [&](int grp) {
                 e = cudaEventSynchronize((cudaEvent_t)p->off_events[(size_t)grp]);
                 return e == cudaSuccess;
@@ -2575,7 +2585,7 @@ zero_status_t zero_step_units_overlapped(zero_plan_t* p, const void* const* unit
             if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: event");
             p->ov_events[i] = ev;
         }
-        p->release_hook = release_plan_cuda;
+        p->release_hook = release_plan_resources;
     }
     cudaStream_t cs = (cudaStream_t)compute_stream, ms = (cudaStream_t)comm_stream;
     cudaEvent_t start = (cudaEvent_t)p->ov_events[0];
