@@ -38,8 +38,8 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_step.cu); reported as null once that source
 # changes.  Captures: profiles/*_ncu_full.md.
-MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("98d53f89377b08cd", 2_287_540_736),
-                    (1, "fused_step_kernel"): ("98d53f89377b08cd", 2_304_309_504)}
+MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("73e3e738775efc3e", 2_287_791_616),
+                    (1, "fused_step_kernel"): ("73e3e738775efc3e", 2_304_549_888)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_step.cu")
 
 
