@@ -38,8 +38,8 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_kernels.cuh, the device code); reported as null
 # once that source changes.  Captures: profiles/*_ncu_full.md.
-MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("73e3e738775efc3e", 2_287_791_616),
-                    (1, "fused_step_kernel"): ("73e3e738775efc3e", 2_304_549_888)}
+MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("ae6390b593db8a38", 2_287_339_520),
+                    (1, "fused_step_kernel"): ("ae6390b593db8a38", 2_303_291_136)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_kernels.cuh")
 
 
