@@ -39,7 +39,12 @@ ROTATE_SETS = 4
 # (first 16 hex digits of the SHA-256 of zero_kernels.cuh, the device code); reported as null
 # once that source changes.  Captures: profiles/*_ncu_full.md.
 MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("ae6390b593db8a38", 2_287_339_520),
-                    (1, "fused_step_kernel"): ("ae6390b593db8a38", 2_303_291_136)}
+                    (1, "fused_step_kernel"): ("ae6390b593db8a38", 2_303_291_136),
+                    # one launch captured (configs 3 and 4: one unit of the model), scaled by
+                    # elements to the average launch the bench times
+                    (2, "bulk_step_kernel"): ("ae6390b593db8a38", 1_003_436_229),
+                    (3, "bulk_step_kernel"): ("ae6390b593db8a38", 2_901_763_547),
+                    (4, "bulk_step_kernel"): ("ae6390b593db8a38", 999_794_979)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_kernels.cuh")
 
 
