@@ -369,7 +369,8 @@ zero_status_t zero_offload_step(zero_plan_t* plan, const void* const* grad_contr
                                 void* stream);
 
 /* End an offloaded step.  Once the step's last flag pass is done, the step state is read on
- * a side stream.  Then `threads` CPU threads apply AdamW to the host state with the same fp32
+ * a side stream.  Then `threads` CPU threads (kept by the plan from step to step, asleep in
+ * between, ended by zero_plan_destroy) apply AdamW to the host state with the same fp32
  * operation order as the GPU kernel, each group of segments as soon as its gradient has
  * landed.  Finished ranges of 16-bit parameters are copied to the all-gather destination on
  * `stream` while the rest is still being updated.  If the flag is set, the call waits for
