@@ -879,6 +879,37 @@ def test_gather_kernels_config_sampled(i, gather):
     print(f"{w.name}, {gather} gather: {n} sampled elements, {mism} bit mismatches")
 
 
+@pytest.mark.parametrize("gather", [Z.ZERO_STAGING_AUTO, Z.ZERO_STAGING_BULK])
+def test_gather_of_peer_shards_without_a_bound_rank(gather):
+    """A stage-3 plan whose ranks are all peers (16-bit shards only, no workspace): the staged
+    gather needs the workspace's error word, so the call falls back to register copies; every
+    gathered unit is the concatenation of the rank shards' slices, padding included."""
+    sizes, n_d, units = [70_001, 5, 123_457, 33, 4_000_003], 4, [0, 2, 4]
+    plan = Z.zero_plan_create(sizes, n_d, 3, 0, units)
+    try:
+        Z.zero_set_option(plan, Z.ZERO_OPT_GATHER_STAGING, gather)
+        gen = torch.Generator(device="cpu").manual_seed(7)
+        shards = []
+        for r in range(n_d):
+            n = Z.zero_rank_state_elems(plan, r)
+            sh = torch.randint(-32768, 32767, (n,), dtype=torch.int16, generator=gen).cuda()
+            Z.zero_bind_peer(plan, r, sh.data_ptr())
+            shards.append(sh)
+        layout = Z.zero_plan_tables(plan, Z.ZERO_TABLE_STATE_LAYOUT)   # rank, unit, offset, n
+        info = Z.zero_plan_info(plan)
+        for u in range(int(info.n_units)):
+            parts = [(r, off, n) for (r, uu, off, n) in layout if uu == u]
+            total = sum(n for _, _, n in parts)
+            dst = torch.full((max(8, total),), -1, dtype=torch.int16, device="cuda")
+            Z.zero_gather_layer(plan, u, dst.data_ptr())
+            Z.zero_release_layer(plan, u)
+            want = torch.cat([shards[r][off:off + n] for r, off, n in sorted(parts)])
+            torch.cuda.synchronize()
+            assert torch.equal(dst[:total], want), f"unit {u}"
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
 def test_bulk_gather_wait_limit_runs_out_and_the_step_is_discarded():
     """A gather whose barrier wait runs out (limit 0) records it in the plan's error word,
     drains its copies and returns; the step then finishing reports ZERO_ETIMEOUT and is
