@@ -24,6 +24,33 @@ def test_library_exports_every_declared_symbol():
     assert declared <= set(Z.EXPORTED)
 
 
+def test_binding_constants_match_the_header():
+    """Every ZERO_* constant of include/zero.h (enums and #defines) has the same value in the
+    Python binding."""
+    with open(os.path.join(ROOT, "include", "zero.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    values = {}
+    for body in re.findall(r"enum\s*(?:\w+\s*)?\{(.*?)\}", text, re.S):
+        nxt = 0
+        for item in body.split(","):
+            item = item.strip()
+            if not item:
+                continue
+            name, _, val = item.partition("=")
+            name = name.strip()
+            nxt = int(val.strip(), 0) if val.strip() else nxt
+            values[name] = nxt
+            nxt += 1
+    for name, val in re.findall(r"#define\s+(ZERO_\w+)\s+(\d+)", text):
+        values[name] = int(val)
+    assert len(values) >= 25
+    for name, val in sorted(values.items()):
+        if hasattr(Z, name):
+            assert getattr(Z, name) == val, name
+    missing = [n for n in values if n.startswith("ZERO_OPT_") and not hasattr(Z, n)]
+    assert not missing, missing
+
+
 def _plan_for(sizes, n_d, stage, bucket=0, units=None, dtype=Z.ZERO_BF16):
     return Z.zero_plan_create(list(sizes), n_d, stage, bucket, list(units) if units else None, dtype)
 
