@@ -57,7 +57,9 @@ typedef enum {
     ZERO_ECUDA = 3,   /* a CUDA runtime call failed */
     ZERO_ESTATE = 4,  /* call out of order (e.g. finish before every bucket was stepped) */
     ZERO_ERANGE = 5,  /* a size beyond a documented limit */
-    ZERO_ETIMEOUT = 6 /* a bounded wait inside a kernel ran out; the step was discarded */
+    ZERO_ETIMEOUT = 6, /* a bounded wait inside a kernel ran out; the step was discarded */
+    ZERO_ENOMEM = 7   /* a host resource (memory, a worker thread) could not be obtained; the
+                         call changed nothing it had not finished */
 } zero_status_t;
 
 enum { ZERO_BF16 = 0, ZERO_FP16 = 1 };

@@ -339,3 +339,39 @@ def test_per_param_argument_errors():
     with pytest.raises(Z.ZeroError) as e:
         Z.zero_plan_create_per_param([0, 7], [0, 7], 0)
     assert e.value.status == Z.ZERO_EINVAL
+
+
+_EXHAUSTION_CHILD = """
+import ctypes, resource, sys
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import zero_sharded_mixed_03_gb300 as Z
+L = Z.lib()
+n = 20_000_000
+sizes = np.ones(n, dtype=np.int64)
+out = ctypes.c_void_p()
+vm = int(open('/proc/self/statm').read().split()[0]) * resource.getpagesize()
+soft, hard = resource.getrlimit(resource.RLIMIT_AS)
+resource.setrlimit(resource.RLIMIT_AS, (vm + (256 << 20), hard))
+st = L.zero_plan_create(sizes.ctypes.data, n, 8, 2, 0, None, 0, 0, ctypes.byref(out))
+resource.setrlimit(resource.RLIMIT_AS, (soft, hard))
+print(st, out.value is None, L.zero_last_error().decode())
+"""
+
+
+def test_host_exhaustion_is_reported_not_thrown():
+    """A plan whose host tables do not fit (20M tensors under an address-space limit just above
+    the process's current use, in a child process): zero_plan_create returns ZERO_ENOMEM with a
+    message and no plan, instead of letting std::bad_alloc cross the C ABI (which would abort
+    the process)."""
+    import subprocess
+    import sys
+    if not os.path.exists("/proc/self/statm"):
+        pytest.skip("needs /proc")
+    run = subprocess.run([sys.executable, "-c", _EXHAUSTION_CHILD, ROOT], capture_output=True,
+                         text=True, timeout=300)
+    assert run.returncode == 0, run.stderr[-2000:]
+    status, no_plan, msg = run.stdout.strip().split(" ", 2)
+    assert int(status) == Z.ZERO_ENOMEM and no_plan == "True", run.stdout
+    assert "host resource exhausted" in msg
+

@@ -15,7 +15,7 @@ from typing import Optional, Sequence
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libzero.so")
 
-ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ESTATE, ZERO_ERANGE, ZERO_ETIMEOUT = range(7)
+ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ESTATE, ZERO_ERANGE, ZERO_ETIMEOUT, ZERO_ENOMEM = range(8)
 ZERO_BF16, ZERO_FP16 = 0, 1
 ZERO_MAX_RANKS = 128
 ZERO_REPORT_GRAD_NORM = 1
@@ -27,7 +27,7 @@ ZERO_STAGING_REGISTER_LOADS, ZERO_STAGING_BULK, ZERO_STAGING_AUTO = range(3)
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)
 TABLE_COLS = {0: 1, 1: 7, 2: 6, 3: 5, 4: 4, 5: 10}
 STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_EALIGN", 3: "ZERO_ECUDA",
-                4: "ZERO_ESTATE", 5: "ZERO_ERANGE", 6: "ZERO_ETIMEOUT"}
+                4: "ZERO_ESTATE", 5: "ZERO_ERANGE", 6: "ZERO_ETIMEOUT", 7: "ZERO_ENOMEM"}
 
 EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", "zero_rank_state_elems", "zero_plan_tables",
             "zero_bind", "zero_bind_peer", "zero_step", "zero_step_finish", "zero_gather_layer",

@@ -177,6 +177,10 @@ namespace zero {
 // Thread-local last-error text (zero_last_error).
 zero_status_t fail(zero_status_t code, const std::string& msg);
 
+// The status of an exception caught at the ABI (every exported function catches all, so none
+// crosses it): host memory or thread exhaustion is ZERO_ENOMEM.  Never throws.
+zero_status_t exception_status(const char* where) noexcept;
+
 // Bucket b's global flat range [lo, hi) (stages 1/2); b = -1: the whole buffer.
 void bucket_range(const zero_plan* p, int64_t b, int64_t* lo, int64_t* hi);
 

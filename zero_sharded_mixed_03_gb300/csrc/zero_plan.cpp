@@ -8,6 +8,8 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <exception>
+#include <memory>
 #include <new>
 
 #include "zero_internal.h"
@@ -24,6 +26,23 @@ zero_status_t fail(zero_status_t code, const std::string& msg)
 {
     g_last_error = msg;
     return code;
+}
+
+zero_status_t exception_status(const char* where) noexcept
+{
+    const char* what = "unknown exception";
+    try {
+        throw;
+    } catch (const std::exception& e) {
+        what = e.what();
+    } catch (...) {
+    }
+    try {
+        g_last_error = std::string(where) + ": host resource exhausted (" + what + ")";
+    } catch (...) {
+        // the message itself could not be stored: the status still reports the failure
+    }
+    return ZERO_ENOMEM;
 }
 
 void bucket_range(const zero_plan* p, int64_t b, int64_t* lo, int64_t* hi)
@@ -125,7 +144,7 @@ const char* zero_last_error(void) { return g_last_error.c_str(); }
 zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, int n_d, int stage,
                                int64_t bucket_elems, const int64_t* unit_first, int64_t n_units,
                                int dtype16, zero_plan_t** out)
-{
+try {
     if (out == nullptr) return fail(ZERO_EINVAL, "zero_plan_create: out is NULL");
     *out = nullptr;
     if (n_tensors < 0 || (n_tensors > 0 && tensor_sizes == nullptr))
@@ -144,8 +163,10 @@ zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, i
     for (int64_t i = 0; i < n_tensors; ++i)
         if (tensor_sizes[i] < 0) return fail(ZERO_EINVAL, "zero_plan_create: negative tensor size");
 
-    zero_plan* p = new (std::nothrow) zero_plan;
-    if (!p) return fail(ZERO_EINVAL, "zero_plan_create: out of host memory");
+    // owned here until it is handed out, so that a failure (or an exception) part way frees it
+    std::unique_ptr<zero_plan> owner(new (std::nothrow) zero_plan);
+    if (!owner) return fail(ZERO_ENOMEM, "zero_plan_create: out of host memory");
+    zero_plan* p = owner.get();
     p->n_d = n_d;
     p->stage = stage;
     p->dtype16 = dtype16;
@@ -159,10 +180,8 @@ zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, i
         bool ok = starts[0] == 0;
         for (size_t u = 1; ok && u < starts.size(); ++u)
             ok = starts[u] > starts[u - 1] && starts[u] <= n_tensors;
-        if (!ok || (n_tensors == 0 && starts.size() > 1)) {
-            delete p;
+        if (!ok || (n_tensors == 0 && starts.size() > 1))
             return fail(ZERO_EINVAL, "zero_plan_create: unit_first must start at 0 and increase");
-        }
     } else {
         starts.push_back(0);
     }
@@ -214,14 +233,17 @@ zero_status_t zero_plan_create(const int64_t* tensor_sizes, int64_t n_tensors, i
     p->covered.assign((size_t)std::max<int64_t>(p->n_buckets, 1), 0);
     p->norm_covered.assign((size_t)std::max<int64_t>(p->n_buckets, 1), 0);
     p->gathered.assign(p->units.size(), 0);
-    *out = p;
+    *out = owner.release();
     return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_plan_create");
 }
 
 zero_status_t zero_plan_create_per_param(const int64_t* tensor_sizes, const int64_t* dim0,
                                          int64_t n_tensors, int n_d, const int64_t* unit_first,
                                          int64_t n_units, int dtype16, zero_plan_t** out)
-{
+try {
     if (out == nullptr) return fail(ZERO_EINVAL, "zero_plan_create_per_param: out is NULL");
     *out = nullptr;
     if (n_tensors > 0 && dim0 == nullptr)
@@ -231,10 +253,13 @@ zero_status_t zero_plan_create_per_param(const int64_t* tensor_sizes, const int6
                              (dim0[t] > 0 && tensor_sizes[t] % dim0[t] != 0)))
             return fail(ZERO_EINVAL, "zero_plan_create_per_param: size is not a multiple of dim0");
     }
-    zero_plan_t* p = nullptr;
+    zero_plan_t* made = nullptr;
     zero_status_t st = zero_plan_create(tensor_sizes, n_tensors, n_d, 3, 0, unit_first, n_units,
-                                        dtype16, &p);
+                                        dtype16, &made);
     if (st != ZERO_OK) return st;
+    // destroyed here if anything below fails (or throws) before it is handed out
+    std::unique_ptr<zero_plan, void (*)(zero_plan*)> owner(made, zero_plan_destroy);
+    zero_plan* p = owner.get();
     p->per_param = true;
     p->dim0.assign(dim0, dim0 + n_tensors);
     // units: unpadded gradient buffers; a rank's unit shard = its padded local chunks
@@ -286,18 +311,24 @@ zero_status_t zero_plan_create_per_param(const int64_t* tensor_sizes, const int6
         }
         p->state_elems[(size_t)r] = ceil_div(cursor, 8) * 8;
     }
-    *out = p;
+    *out = owner.release();
     return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_plan_create_per_param");
 }
 
 void zero_plan_destroy(zero_plan_t* plan)
-{
+try {
     if (plan && plan->release_hook) plan->release_hook(plan);
     delete plan;
 }
+catch (...) {
+    (void)exception_status("zero_plan_destroy");
+}
 
 zero_status_t zero_plan_info(const zero_plan_t* p, zero_plan_info_t* out)
-{
+try {
     if (!p || !out) return fail(ZERO_EINVAL, "zero_plan_info: NULL argument");
     std::memset(out, 0, sizeof(*out));
     out->n_tensors = (int64_t)p->sizes.size();
@@ -321,18 +352,24 @@ zero_status_t zero_plan_info(const zero_plan_t* p, zero_plan_info_t* out)
     out->dtype16 = p->dtype16;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_plan_info");
+}
 
 zero_status_t zero_rank_state_elems(const zero_plan_t* p, int rank, int64_t* elems)
-{
+try {
     if (!p || !elems) return fail(ZERO_EINVAL, "zero_rank_state_elems: NULL argument");
     if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_rank_state_elems: bad rank");
     *elems = p->state_elems[(size_t)rank];
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_rank_state_elems");
+}
 
 zero_status_t zero_plan_tables(const zero_plan_t* p, int which, int64_t* dst, int64_t cap,
                                int64_t* n_rows)
-{
+try {
     if (!p || !n_rows) return fail(ZERO_EINVAL, "zero_plan_tables: NULL argument");
     std::vector<int64_t> rows;
     int cols = 0;
@@ -420,9 +457,12 @@ zero_status_t zero_plan_tables(const zero_plan_t* p, int which, int64_t* dst, in
     }
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_plan_tables");
+}
 
 zero_status_t zero_memory_report(const zero_plan_t* p, zero_mem_report_t* out)
-{
+try {
     if (!p || !out) return fail(ZERO_EINVAL, "zero_memory_report: NULL argument");
     std::memset(out, 0, sizeof(*out));
     const int64_t F = p->phi_pad, S = p->shard_total;
@@ -453,9 +493,12 @@ zero_status_t zero_memory_report(const zero_plan_t* p, zero_mem_report_t* out)
     out->workspace_bytes = info.workspace_bytes;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_memory_report");
+}
 
 zero_status_t zero_comm_report(const zero_plan_t* p, zero_comm_report_t* out)
-{
+try {
     if (!p || !out) return fail(ZERO_EINVAL, "zero_comm_report: NULL argument");
     std::memset(out, 0, sizeof(*out));
     const int64_t one = (int64_t)(p->n_d - 1) * p->shard_total;  // (N-1)/N * phi_pad
@@ -469,6 +512,9 @@ zero_status_t zero_comm_report(const zero_plan_t* p, zero_comm_report_t* out)
     out->collectives_per_step =
         p->stage == 3 ? 3 * (int64_t)p->units.size() : 2 * p->n_buckets;
     return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_comm_report");
 }
 
 }  // extern "C"

@@ -639,7 +639,7 @@ extern "C" {
 
 zero_status_t zero_bind(zero_plan_t* p, int rank, float* const master[2], float* const m[2],
                         float* const v[2], void* shard16, void* full16, void* workspace)
-{
+try {
     if (!p || !master || !m || !v) return fail(ZERO_EINVAL, "zero_bind: NULL argument");
     if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind: bad rank");
     if (p->in_step || p->stepped) return fail(ZERO_ESTATE, "zero_bind: bind every rank before the first step");
@@ -694,9 +694,12 @@ zero_status_t zero_bind(zero_plan_t* p, int rank, float* const master[2], float*
     R.shard16 = (uint16_t*)shard16;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_bind");
+}
 
 zero_status_t zero_bind_peer(zero_plan_t* p, int rank, const void* shard16)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_bind_peer: NULL plan");
     if (p->stage != 3) return fail(ZERO_EINVAL, "zero_bind_peer: stage 3 only");
     if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind_peer: bad rank");
@@ -709,9 +712,12 @@ zero_status_t zero_bind_peer(zero_plan_t* p, int rank, const void* shard16)
     R.shard16 = (uint16_t*)shard16;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_bind_peer");
+}
 
 zero_status_t zero_set_scaler(zero_plan_t* p, const zero_scaler_t* cfg, void* stream)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_set_scaler: NULL plan");
     if (!p->workspace) return fail(ZERO_ESTATE, "zero_set_scaler: bind a rank first");
     if (p->in_step) return fail(ZERO_ESTATE, "zero_set_scaler: a step is open");
@@ -736,9 +742,12 @@ zero_status_t zero_set_scaler(zero_plan_t* p, const zero_scaler_t* cfg, void* st
     if (e != cudaSuccess) return cuda_fail(e, "zero_set_scaler: writing the loss scale");
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_set_scaler");
+}
 
 zero_status_t zero_set_option(zero_plan_t* p, int option, int64_t value)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_set_option: NULL plan");
     if (p->in_step) return fail(ZERO_ESTATE, "zero_set_option: a step is open");
     int64_t tile = p->bulk_tile, stages = p->bulk_stages;
@@ -800,9 +809,12 @@ zero_status_t zero_set_option(zero_plan_t* p, int option, int64_t value)
     p->bulk_stages = (int)stages;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_set_option");
+}
 
 zero_status_t zero_get_option(const zero_plan_t* p, int option, int64_t* value)
-{
+try {
     if (!p || !value) return fail(ZERO_EINVAL, "zero_get_option: NULL argument");
     switch (option) {
     case ZERO_OPT_STAGING: *value = p->staging; return ZERO_OK;
@@ -819,10 +831,13 @@ zero_status_t zero_get_option(const zero_plan_t* p, int option, int64_t* value)
     default: return fail(ZERO_EINVAL, "zero_get_option: unknown option");
     }
 }
+catch (...) {
+    return exception_status("zero_get_option");
+}
 
 zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
                              int64_t which, void* stream)
-{
+try {
     zero_status_t st = check_call(p, grad_contribs, n_contribs, which, "zero_grad_norm");
     if (st != ZERO_OK) return st;
     if (p->in_step)
@@ -861,10 +876,13 @@ zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, i
     else p->norm_covered[(size_t)which] = 1;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_grad_norm");
+}
 
 zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
                         int64_t which, const zero_hyper_t* hyper, void* stream)
-{
+try {
     if (!hyper) return fail(ZERO_EINVAL, "zero_step: NULL argument");
     if (p && p->offload) return fail(ZERO_ESTATE, "zero_step: offloaded plan (zero_offload_step)");
     zero_status_t cst = check_call(p, grad_contribs, n_contribs, which, "zero_step");
@@ -933,9 +951,12 @@ zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_
     else p->covered[(size_t)which] = 1;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_step");
+}
 
 zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t* out)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_step_finish: NULL plan");
     if (!p->in_step) return fail(ZERO_ESTATE, "zero_step_finish: no open step");
     for (int64_t b = 0; b < p->n_buckets; ++b)
@@ -991,18 +1012,24 @@ zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t*
     if (out) return read_state(p, s, out);
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_step_finish");
+}
 
 zero_status_t zero_read_state(zero_plan_t* p, void* stream, zero_step_result_t* out)
-{
+try {
     if (!p || !out) return fail(ZERO_EINVAL, "zero_read_state: NULL argument");
     if (!p->workspace) return fail(ZERO_ESTATE, "zero_read_state: no rank bound");
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
     return read_state(p, (cudaStream_t)stream, out);
 }
+catch (...) {
+    return exception_status("zero_read_state");
+}
 
 zero_status_t zero_restore_state(zero_plan_t* p, const zero_step_result_t* in, void* stream)
-{
+try {
     if (!p || !in) return fail(ZERO_EINVAL, "zero_restore_state: NULL argument");
     if (!p->workspace) return fail(ZERO_ESTATE, "zero_restore_state: no rank bound");
     if (p->in_step) return fail(ZERO_ESTATE, "zero_restore_state: a step is open");
@@ -1026,9 +1053,12 @@ zero_status_t zero_restore_state(zero_plan_t* p, const zero_step_result_t* in, v
     if (e != cudaSuccess) return cuda_fail(e, "zero_restore_state: writing the state");
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_restore_state");
+}
 
 zero_status_t zero_gather_layer(zero_plan_t* p, int64_t unit, void* full_unit16, void* stream)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_gather_layer: NULL plan");
     if (p->stage != 3) return fail(ZERO_EINVAL, "zero_gather_layer: stage 3 only");
     if (unit < 0 || unit >= (int64_t)p->units.size())
@@ -1074,9 +1104,12 @@ zero_status_t zero_gather_layer(zero_plan_t* p, int64_t unit, void* full_unit16,
     p->gathered[(size_t)unit] = 1;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_gather_layer");
+}
 
 zero_status_t zero_release_layer(zero_plan_t* p, int64_t unit)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_release_layer: NULL plan");
     if (p->stage != 3) return fail(ZERO_EINVAL, "zero_release_layer: stage 3 only");
     if (unit < 0 || unit >= (int64_t)p->units.size())
@@ -1085,11 +1118,14 @@ zero_status_t zero_release_layer(zero_plan_t* p, int64_t unit)
     p->gathered[(size_t)unit] = 0;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_release_layer");
+}
 
 zero_status_t zero_bind_offload(zero_plan_t* p, int rank, float* master, float* m, float* v,
                                 float* grad_host, void* param16_host, void* shard16, void* full16,
                                 void* workspace)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_bind_offload: NULL plan");
     if (rank < 0 || rank >= p->n_d) return fail(ZERO_EINVAL, "zero_bind_offload: bad rank");
     if (p->in_step || p->stepped)
@@ -1151,10 +1187,13 @@ zero_status_t zero_bind_offload(zero_plan_t* p, int rank, float* master, float* 
     p->offload = true;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_bind_offload");
+}
 
 zero_status_t zero_offload_step(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
                                 int64_t which, const zero_hyper_t* hyper, void* stream)
-{
+try {
     if (!hyper) return fail(ZERO_EINVAL, "zero_offload_step: NULL argument");
     zero_status_t st = check_call(p, grad_contribs, n_contribs, which, "zero_offload_step");
     if (st != ZERO_OK) return st;
@@ -1242,9 +1281,12 @@ zero_status_t zero_offload_step(zero_plan_t* p, const void* const* grad_contribs
     else p->covered[(size_t)which] = 1;
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_offload_step");
+}
 
 zero_status_t zero_offload_finish(zero_plan_t* p, int threads, void* stream, zero_step_result_t* out)
-{
+try {
     if (!p) return fail(ZERO_EINVAL, "zero_offload_finish: NULL plan");
     if (!p->offload) return fail(ZERO_ESTATE, "zero_offload_finish: no offloaded rank bound");
     if (!p->in_step) return fail(ZERO_ESTATE, "zero_offload_finish: no open step");
@@ -1336,12 +1378,15 @@ zero_status_t zero_offload_finish(zero_plan_t* p, int threads, void* stream, zer
     if (out) return read_state(p, s, out);
     return ZERO_OK;
 }
+catch (...) {
+    return exception_status("zero_offload_finish");
+}
 
 zero_status_t zero_step_units_overlapped(zero_plan_t* p, const void* const* unit_contribs,
                                          int64_t n_ptrs, void* const* gather_bufs,
                                          const zero_hyper_t* hyper, void* compute_stream,
                                          void* comm_stream, zero_step_result_t* out)
-{
+try {
     if (!p || !unit_contribs || !gather_bufs || !hyper)
         return fail(ZERO_EINVAL, "zero_step_units_overlapped: NULL argument");
     if (p->stage != 3) return fail(ZERO_EINVAL, "zero_step_units_overlapped: stage 3 only");
@@ -1396,6 +1441,9 @@ zero_status_t zero_step_units_overlapped(zero_plan_t* p, const void* const* unit
     }
     return zero_step_finish(p, compute_stream, out);
 }
+catch (...) {
+    return exception_status("zero_step_units_overlapped");
+}
 
 // ---------------------------------------------------------------------------------------
 // No-allocation variant: the fused step over one flat range with its scratch (the non-finite
@@ -1445,7 +1493,7 @@ zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d,
                                       float* v_out, void* out16, const zero_hyper_t* hyper,
                                       int64_t t, double loss_scale, void* stream,
                                       int32_t* nonfinite)
-{
+try {
     static_assert(sizeof(uint32_t) <= ZERO_NOALLOC_SCRATCH_BYTES, "flag must fit the scratch");
     if (!grad_contribs || !hyper || !nonfinite)
         return fail(ZERO_EINVAL, "zero_step_range_noalloc: NULL argument");
@@ -1526,6 +1574,9 @@ zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d,
     if (e != cudaSuccess) return cuda_fail(e, "zero_step_range_noalloc: reading the flag");
     *nonfinite = flag ? 1 : 0;
     return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_step_range_noalloc");
 }
 
 }  // extern "C"
