@@ -375,3 +375,24 @@ def test_host_exhaustion_is_reported_not_thrown():
     assert int(status) == Z.ZERO_ENOMEM and no_plan == "True", run.stdout
     assert "host resource exhausted" in msg
 
+
+
+def test_unit_slice_keeps_one_unit_of_a_stage3_workload():
+    """The profiling slice of a stage-3 workload: the tensors (and dim-0 sizes) of one unit, as
+    a one-unit workload; the library's plan of the slice has that unit's padded size."""
+    w = W.workload(3)
+    first, count = w.units()[1]
+    s = W.unit_slice(w, 1)
+    assert s.sizes == w.sizes[first:first + count] and s.unit_first == (0,) and s.inject is None
+    assert s.phi == 50_358_272                         # one 2048-wide GPT block
+    plan = _plan_for(s.sizes, s.n_d, 3, 0, [0])
+    try:
+        info = Z.zero_plan_info(plan)
+        assert info.n_units == 1 and info.phi_pad == s.phi   # divisible by N_d = 16: no padding
+    finally:
+        Z.zero_plan_destroy(plan)
+    pp = W.unit_slice(W.per_param_variant(W.workload(4)), 1)
+    f4, c4 = W.workload(4).units()[1]
+    assert pp.dim0 == W.per_param_variant(W.workload(4)).dim0[f4:f4 + c4] and pp.per_param
+    with pytest.raises(ValueError):
+        W.unit_slice(W.workload(1), 0)                 # stage 2: no units
