@@ -48,6 +48,13 @@ MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("ae6390b593db8a38", 2_287_339_520)
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_kernels.cuh")
 
 
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the kernel source (the traffic records' key)."""
+    import hashlib
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
 def measured_traffic(config: int, kernel: str):
     import hashlib
     rec = MEASURED_TRAFFIC.get((config, kernel))
@@ -554,6 +561,7 @@ def gpu_arm(args, world, rank, local):
     kernel = "bulk_step_kernel" if last == 1 else "fused_step_kernel"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config, kernel),
+                "kernel_source_sha256": kernel_source_hash(),
                 "peak_source": peak_kind, "kernel": kernel,
                 "launch_bytes": int(launch_bytes), "avg_launch_us": round(avg_fused_s * 1e6, 2),
                 "launches_timed": len(fused_ms)}
