@@ -196,6 +196,9 @@ zero_status_t zero_plan_create_per_param(const int64_t* tensor_sizes, const int6
                                          int64_t n_tensors, int n_d, const int64_t* unit_first,
                                          int64_t n_units, int dtype16, zero_plan_t** out);
 
+/* Fill *out with the partition's sizes ("FSDP-1: FlatParameter": phi, phi_pad, the shard,
+ * buckets and units) and the buffer sizes the caller allocates (contributions, gather
+ * destination, workspace; see zero_plan_info_t).  Host-only; ZERO_EINVAL on NULL. */
 zero_status_t zero_plan_info(const zero_plan_t* plan, zero_plan_info_t* out);
 
 /* Element count of rank `rank`'s state buffers (master, m, v; and stage 3's 16-bit shard).
@@ -204,12 +207,16 @@ zero_status_t zero_plan_info(const zero_plan_t* plan, zero_plan_info_t* out);
  * share one 128-bit vector phase.  Unused gap elements are never read or written. */
 zero_status_t zero_rank_state_elems(const zero_plan_t* plan, int rank, int64_t* elems);
 
-/* Copy table `which` into dst (capacity `cap` int64 values).  *n_rows receives the row
- * count; if the table does not fit, nothing is written and ZERO_ERANGE is returned. */
+/* Copy table `which` of the partition ("FSDP-1: FlatParameter": tensor offsets, units,
+ * shard and bucket segments, state layout, per-parameter chunks) into dst (capacity `cap`
+ * int64 values).  *n_rows receives the row count; if the table does not fit, nothing is
+ * written and ZERO_ERANGE is returned. */
 zero_status_t zero_plan_tables(const zero_plan_t* plan, int which, int64_t* dst, int64_t cap,
                                int64_t* n_rows);
 
-/* Bind rank `rank`'s device buffers (caller-owned, each of zero_rank_state_elems elements):
+/* Bind rank `rank`'s device buffers ("Static Memory Allocation": the 12 bytes of fp32
+ * master/m/v per parameter a rank keeps for its shard; caller-owned, each of
+ * zero_rank_state_elems elements):
  *   master[2], m[2], v[2]  fp32 ping-pong pairs; index 0 holds the current state at bind time
  *   shard16                stage 3: the rank's 16-bit parameter shard; else NULL
  *   full16                 stages 1/2: the flat 16-bit parameter buffer (phi_pad elements),
@@ -222,16 +229,22 @@ zero_status_t zero_plan_tables(const zero_plan_t* plan, int which, int64_t* dst,
 zero_status_t zero_bind(zero_plan_t* plan, int rank, float* const master[2], float* const m[2],
                         float* const v[2], void* shard16, void* full16, void* workspace);
 
-/* Stage 3: register the 16-bit shard of a rank whose optimizer runs elsewhere, so that
- * zero_gather_layer can reconstruct full units.  The buffer follows that rank's layout. */
+/* Stage 3 ("ZeRO-3 / FSDP Layer Execution Lifecycle": every rank holds only its shard of the
+ * 16-bit parameters): register the 16-bit shard of a rank whose optimizer runs elsewhere, so
+ * that zero_gather_layer can reconstruct full units.  The buffer follows that rank's layout. */
 zero_status_t zero_bind_peer(zero_plan_t* plan, int rank, const void* shard16);
 
-/* Set (cfg != NULL) or disable (cfg == NULL: scale fixed at 1) the dynamic loss scale: writes
+/* Dynamic loss scaling (not on the pages, which name fp16/bf16 mixed precision only; the
+ * skip-and-back-off scheme of mixed-precision training).  Set (cfg != NULL) or disable
+ * (cfg == NULL: scale fixed at 1) the dynamic loss scale: writes
  * cfg->scale and cfg->good_steps into the device state and keeps the growth/back-off settings.
  * Not inside an open step.  Synchronises `stream`. */
 zero_status_t zero_set_scaler(zero_plan_t* plan, const zero_scaler_t* cfg, void* stream);
 
-/* One fused reduce + AdamW + cast over every bound rank's part of bucket / unit `which`.
+/* One fused reduce + AdamW + cast over every bound rank's part of bucket / unit `which`
+ * ("Execution Flow for ZeRO-1" steps 2-4: reduce-scatter of the averaged gradient, update of
+ * the owned shard, 16-bit write into the all-gather destination; "ZeRO-Stage 2": one call per
+ * bucket as gradients are produced; "ZeRO-3 / FSDP Layer Execution Lifecycle": one per unit).
  *   grad_contribs[n_contribs]  n_contribs == N_d device pointers; contribution r holds rank r's
  *                              16-bit gradient for the whole range of the bucket (stages 1/2:
  *                              [b*B, min((b+1)*B, phi_pad)); which = -1: all of [0, phi_pad))
@@ -361,7 +374,8 @@ zero_status_t zero_bind_offload(zero_plan_t* plan, int rank, float* master, floa
                                 float* grad_host, void* param16_host, void* shard16, void* full16,
                                 void* workspace);
 
-/* Offloaded counterpart of zero_step: reduces bucket / unit `which` on the GPU (same
+/* Offloaded counterpart of zero_step ("ZeRO-Offload Mechanics": gradients to the host, the
+ * optimizer step on the CPU): reduces bucket / unit `which` on the GPU (same
  * contributions, scaling and non-finite flag) and writes the averaged gradient into the bound
  * ranks' grad_host.  It first runs the reduction for the non-finite flag alone (no writes),
  * then the writing reduction in groups of segments of at least 4M elements, an event after
@@ -382,10 +396,19 @@ zero_status_t zero_offload_step(zero_plan_t* plan, const void* const* grad_contr
 zero_status_t zero_offload_finish(zero_plan_t* plan, int threads, void* stream,
                                   zero_step_result_t* out);
 
-/* Mark unit `unit`'s gathered buffer free; the caller may reuse its memory. */
+/* Release after use ("ZeRO-3 / FSDP Layer Execution Lifecycle": the full parameters of a unit
+ * are freed once its forward or backward is done): mark unit `unit`'s gathered buffer free;
+ * the caller may reuse its memory.  ZERO_ESTATE if the unit is not gathered. */
 zero_status_t zero_release_layer(zero_plan_t* plan, int64_t unit);
 
+/* Fill *out with the per-rank memory accounting of the plan (the closed forms of "Static
+ * Memory Allocation" and the stage equations, at phi_pad, plus this emulation's physical
+ * bytes; see zero_mem_report_t).  Host-only; ZERO_EINVAL on NULL arguments. */
 zero_status_t zero_memory_report(const zero_plan_t* plan, zero_mem_report_t* out);
+
+/* Fill *out with the elements each rank sends per step under DDP and ZeRO-1/2/3 ("Standard
+ * Ring-AllReduce Communication Analysis", "ZeRO-1 and ZeRO-2 Communication Volume", "ZeRO-3
+ * and FSDP Communication Volume"; see zero_comm_report_t).  Host-only; ZERO_EINVAL on NULL. */
 zero_status_t zero_comm_report(const zero_plan_t* plan, zero_comm_report_t* out);
 
 /* ---------------------------------------------------------------------------------------
@@ -426,7 +449,12 @@ zero_status_t zero_step_range_noalloc(const void* const* grad_contribs, int n_d,
                                       int64_t t, double loss_scale, void* stream,
                                       int32_t* nonfinite);
 
+/* Text of the last error of the calling thread (empty if none); valid until its next call. */
 const char* zero_last_error(void);
+
+/* Release a plan: its host tables, and the CUDA events, side stream and host worker threads
+ * it created on first use (the caller's device memory is not touched).  Not while work the
+ * plan enqueued may still use them: synchronise its streams first.  NULL is ignored. */
 void zero_plan_destroy(zero_plan_t* plan);
 
 #ifdef __cplusplus
