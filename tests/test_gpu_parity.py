@@ -613,6 +613,28 @@ def test_offload_full_parity(name):
     assert mism == 0
 
 
+def test_offload_worker_threads_end_with_the_plan():
+    """An offloaded plan keeps its host worker threads between steps and ends them in
+    zero_plan_destroy: the process's thread count returns to where it was."""
+    import os
+    if not os.path.isdir("/proc/self/task"):
+        pytest.skip("needs /proc")
+    threads = lambda: len(os.listdir("/proc/self/task"))
+    w = OFFLOAD_CASES["z1_nd4"]
+    torch.cuda.synchronize()
+    before = threads()
+    run = H.Run(w)
+    try:
+        run.g.offload_threads = 6
+        for k in (1, 2):
+            run.step(k)
+        during = threads()
+    finally:
+        run.close()
+    assert during >= before + 6, (before, during)
+    assert threads() <= before + 1, (before, threads())   # the pool's six are gone
+
+
 def test_offload_sampled_config1():
     w = dataclasses.replace(W.workload(1), offload=True)
     n, mism = _run_sampled(w)
