@@ -621,6 +621,14 @@ def test_offload_worker_threads_end_with_the_plan():
         pytest.skip("needs /proc")
     threads = lambda: len(os.listdir("/proc/self/task"))
     w = OFFLOAD_CASES["z1_nd4"]
+    # a first offloaded plan, so that threads the CUDA runtime starts lazily (pinned memory,
+    # blocking-sync events, side streams) exist before the count is taken
+    warm = H.Run(w)
+    try:
+        warm.g.offload_threads = 2
+        warm.step(1)
+    finally:
+        warm.close()
     torch.cuda.synchronize()
     before = threads()
     run = H.Run(w)
