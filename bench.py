@@ -4,7 +4,8 @@
 One step = one pass of the whole hot path over one step's synthetic gradients: for every
 reduce-scatter bucket (stages 1/2) or FSDP unit (stage 3: all-gather of the unit first) the
 fused reduce + unscale + inf/nan flag + AdamW + 16-bit cast kernel, then the commit/skip
-decision.  Default workload: ZeRO-2 over a ragged 10,000-tensor model, N_d = 7 emulated ranks.
+decision.  Default workload: ZeRO-3 per layer over a 1.3B-parameter GPT (24 blocks, d = 2048, ffn 8192,
+vocab 50257; 26 units), N_d = 16 emulated ranks.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the same workload.
 """
@@ -25,9 +26,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ZeRO step params updated/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "params/s"
-DEFAULT_CONFIG = 1
+DEFAULT_CONFIG = 3
 DEFAULT_STAGING = "auto"
 FALLBACK_HBM_GBS = 6800.0
+# GB300's rated HBM3e bandwidth per GPU (nominal, ~7.9 TB/s), reported beside the measured
+# copy bandwidth that the roofline fractions use as their peak
+NOMINAL_HBM_GBS = 7900.0
 # Gradient sets rotated through the timed steps.  A backward pass rewrites the same gradient
 # buffers every step, so a few persistent sets model training; each step still reads inputs
 # it did not read the step before, and every set is far larger than the 129 MB L2.  (Cycling
@@ -37,7 +41,7 @@ ROTATE_SETS = 4
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the step kernel from
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_kernels.cuh, the device code); reported as null
-# once that source changes.  Captures: profiles/*_ncu_full.md.
+# once that source changes.
 MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("ae6390b593db8a38", 2_287_339_520),
                     (1, "fused_step_kernel"): ("ae6390b593db8a38", 2_303_291_136),
                     # one launch captured (configs 3 and 4: one unit of the model), scaled by
@@ -261,15 +265,14 @@ class Bench:
                  options=None):
         import torch
         import synth
-        from zero_sharded_mixed_03_gb300.emulate import EmulatedGroup
         import zero_sharded_mixed_03_gb300 as Z
-        sys.path.insert(0, os.path.join(ROOT, "tests"))
-        import gpu_harness as H
+        from synth.fill import fill_device
+        from synth.run import Run
 
-        self.torch, self.Z, self.H, self.synth = torch, Z, H, synth
+        self.torch, self.Z, self.synth = torch, Z, synth
         self.w = w
         # plan, state, 16-bit buffers, initial params
-        self.run = H.Run(w, alloc_contribs=False, options=options)
+        self.run = Run(w, alloc_contribs=False, options=options)
         self.g = self.run.g
         self.units = self.run.units
         self.info = self.run.info
@@ -314,7 +317,7 @@ class Bench:
                 st = synth.grad_stream(w, s + 1, r, planted=False)   # no skip in the rotation
                 for spans in self.read_spans:
                     for (a, e, o, _rel) in spans:
-                        H.fill_device(bufs[r][o:o + (e - a)], st, self.units, a, e)
+                        fill_device(bufs[r][o:o + (e - a)], st, self.units, a, e)
             self.sets.append(bufs)
         torch.cuda.synchronize()
         self.elems_per_step = int(self.info.shard) * len(self.bound)
@@ -432,6 +435,60 @@ class Bench:
         return res, launches
 
 
+def measure(b, args, torch, overlap, comm, use_graph, dist, pairs, sample_clocks=False):
+    """Time args.steps steps between barrier/synchronise brackets: captured once as a CUDA
+    graph (timing events captured as graph nodes around every fused / gather launch) and
+    replayed, or enqueued one by one.  Returns the region's ms, the per-launch ms of the step
+    and gather kernels, the launch count and (sample_clocks) the NVML clock samples."""
+    w = b.w
+    n_calls = args.steps * len(b.calls)
+    fused_pairs = pairs(n_calls, use_graph) if not overlap else []
+    gather_pairs = pairs(n_calls, use_graph) if (w.stage == 3 and not overlap) else []
+    ev_fused, ev_gather = iter(fused_pairs), iter(gather_pairs)
+    launches = 0
+
+    def timed_steps():
+        nonlocal launches
+        for k in range(args.steps):
+            bufs = b.sets[(args.warmup + k) % b.n_sets]
+            if overlap:
+                _, n = b.step_overlapped(bufs, comm)
+            else:
+                _, n = b.step(bufs, ev_fused, ev_gather if w.stage == 3 else None)
+            launches += n
+
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                timed_steps()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    region = NvmlSampler(torch.cuda.current_device()) if sample_clocks else None
+    if region:
+        region.start()
+    t0.record()
+    if graph is not None:
+        graph.replay()
+    else:
+        timed_steps()
+    t1.record()
+    torch.cuda.synchronize()
+    region_clk = region.stop() if region else None
+    ms = t0.elapsed_time(t1)
+    if dist:
+        ms = max_over_ranks(ms, dist)
+    return {"ms": ms, "fused_ms": [x.elapsed_time(y) for x, y in fused_pairs],
+            "gather_ms": [x.elapsed_time(y) for x, y in gather_pairs], "launches": launches,
+            "region_clk": region_clk, "graph": graph is not None}
+
+
 def gpu_arm(args, world, rank, local):
     import torch
     from synth import workloads as W
@@ -488,46 +545,9 @@ def gpu_arm(args, world, rank, local):
             torch.cuda.Event(enable_timing=True, external=True)
         except TypeError:
             use_graph = False
-    n_calls = args.steps * len(b.calls)
-    fused_pairs = pairs(n_calls, use_graph) if not overlap else []
-    gather_pairs = pairs(n_calls, use_graph) if (w.stage == 3 and not overlap) else []
-    ev_fused, ev_gather = iter(fused_pairs), iter(gather_pairs)
-    launches = 0
     skipped_before = b.g.step_state().skipped_total
-
-    def timed_steps():
-        nonlocal launches
-        for k in range(args.steps):
-            bufs = b.sets[(args.warmup + k) % b.n_sets]
-            if overlap:
-                _, n = b.step_overlapped(bufs, comm)
-            else:
-                _, n = b.step(bufs, ev_fused, ev_gather if w.stage == 3 else None)
-            launches += n
-
-    graph = None
-    if use_graph:
-        graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(graph, stream=side):
-                timed_steps()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    region = NvmlSampler(local)
-    region.start()
-    t0.record()
-    if graph is not None:
-        graph.replay()
-    else:
-        timed_steps()
-    t1.record()
-    torch.cuda.synchronize()
-    region_clk = region.stop()
+    m = measure(b, args, torch, overlap, comm, use_graph, dist, pairs, sample_clocks=True)
+    region_clk = m["region_clk"]
     if dist:
         dist.barrier()
     clk = clocks.stop()
@@ -535,12 +555,23 @@ def gpu_arm(args, world, rank, local):
         if clk is not None:
             region_clk["nvidia_smi"] = clk
         clk = region_clk
-    ms = t0.elapsed_time(t1)
-    if dist:
-        ms = max_over_ranks(ms, dist)
+    ms, fused_ms, gather_ms, launches = m["ms"], m["fused_ms"], m["gather_ms"], m["launches"]
     skipped = b.g.step_state().skipped_total - skipped_before
-    fused_ms = [a.elapsed_time(c) for a, c in fused_pairs]
-    gather_ms = [a.elapsed_time(c) for a, c in gather_pairs]
+    overlap_report = None
+    if overlap:
+        # the same steps with every unit's gather followed by its step on one stream: what the
+        # second stream hides is the difference
+        ser = measure(b, args, torch, False, None, use_graph, dist, pairs)
+        g_ms = sum(ser["gather_ms"]) / args.steps
+        hidden = ser["ms"] / args.steps - ms / args.steps
+        frac = max(0.0, min(1.0, hidden / g_ms)) if g_ms > 0 else 0.0
+        overlap_report = {"overlapped_ms_per_step": round(ms / args.steps, 3),
+                          "serial_ms_per_step": round(ser["ms"] / args.steps, 3),
+                          "serial_gather_ms_per_step": round(g_ms, 3),
+                          "hidden_ms_per_step": round(hidden, 3),
+                          "gather_hidden_fraction": round(frac, 4),
+                          "gather_bytes_per_step": 4 * int(b.info.phi_pad),
+                          "gather_bytes_hidden_per_step": int(frac * 4 * int(b.info.phi_pad))}
 
     applied = args.steps - skipped
     elems = b.elems_per_step
@@ -563,6 +594,8 @@ def gpu_arm(args, world, rank, local):
                 "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config, kernel),
                 "kernel_source_sha256": kernel_source_hash(),
                 "peak_source": peak_kind, "kernel": kernel,
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                "nominal_peak": NOMINAL_HBM_GBS,
                 "launch_bytes": int(launch_bytes), "avg_launch_us": round(avg_fused_s * 1e6, 2),
                 "launches_timed": len(fused_ms)}
     if not fused_ms or w.offload:                   # overlapped / offloaded: no fused kernel
@@ -597,16 +630,19 @@ def gpu_arm(args, world, rank, local):
                       "elems_updated_per_step": elems, "bytes_per_param": b.bytes_per_elem,
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
-                      "overlap": overlap, "graph": graph is not None, "per_param": w.per_param,
+                      "overlap": overlap, "graph": m["graph"], "per_param": w.per_param,
                       "offload": w.offload, "staging": args.staging,
                       "profile_unit": args.profile_unit,
                       "offload_threads": b.g.offload_threads if w.offload else None},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
+           "hbm_frac_of_nominal": round(hbm_gbs / NOMINAL_HBM_GBS, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,
            "clocks": clk}
+    if overlap_report is not None:
+        out["overlap"] = overlap_report
 
-    if not args.no_e2e:
-        out["e2e"] = e2e_leg(b, min(args.steps, 10), world, dist)
+    if not args.no_e2e and not w.offload:
+        out["e2e"] = e2e_leg(b, min(args.steps, 10), world, dist, ms / args.steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_elems)
     if rank == 0:
@@ -615,50 +651,84 @@ def gpu_arm(args, world, rank, local):
         dist.destroy_process_group()
 
 
-def e2e_leg(b: Bench, steps: int, world: int, dist):
-    """Same metric through the public API with the gradients in pinned host memory: every step
-    copies its contributions host->device, runs the step, and reads the step result back.
-    With two device buffer sets the copy of step k+1 (on a copy stream) runs while step k
-    computes, as a training loop would double-buffer its inputs; the host->device link
-    (about 209 GB/s from pinned Grace memory, copy engines and SM loads alike) bounds it."""
-    torch = b.torch
-    host = [torch.empty(b.set_elems, dtype=torch.int16, pin_memory=True) for _ in range(b.w.n_d)]
-    for r in range(b.w.n_d):
-        host[r].copy_(b.sets[0][r][:b.set_elems])
-    bufs = b.sets[:2]
-    compute = torch.cuda.current_stream()
-    copy = torch.cuda.Stream()
-    copied = [torch.cuda.Event() for _ in bufs]
-
-    def fetch(k):
-        dev = bufs[k % len(bufs)]
-        copy.wait_stream(compute)          # the set's previous step has finished with it
-        with torch.cuda.stream(copy):
-            for r in range(b.w.n_d):
-                dev[r][:b.set_elems].copy_(host[r], non_blocking=True)
-            copied[k % len(bufs)].record(copy)
-
+def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
+    """Same metric through the C ABI with host buffers: every step, for every bucket / unit,
+    zero_step_host copies that call's contributions from pinned host memory into a device
+    staging area (the next call's copies run while this call's step does), runs the step and
+    copies the updated 16-bit parameters back into pinned host memory; (stage 3: the unit's
+    all-gather first;) zero_step_host_finish ends the step, waits for the copies and reads the
+    step state.  Host gradients: two pinned sets of N_d buffers of the largest call's range,
+    used by alternate calls (every byte crosses the host->device link every step; a set is
+    far larger than the host CPU's caches).  The same steps with the library's serial schedule
+    (ZERO_OPT_HOST_PIPELINE = 0: each call's copies, step and copy back one after another)
+    show what the pipelining hides."""
+    torch, Z, w = b.torch, b.Z, b.w
+    g = b.g
+    g.bind_host_staging()
+    n_max = int(b.info.max_contrib_elems)
+    host_sets = [[torch.empty(max(8, n_max), dtype=torch.int16, pin_memory=True)
+                  for _ in range(w.n_d)] for _ in range(2)]
+    # contents: the device gradients of the first call (the values do not change the speed)
+    first = b.read_spans[0][0] if b.read_spans[0] else (0, 0, 0, 0)
+    for hs in host_sets:
+        for r in range(w.n_d):
+            lo, hi, o, rel = first
+            n = min(hi - lo, n_max - rel)
+            if n > 0:
+                hs[r][rel:rel + n].copy_(b.sets[0][r][o:o + n])
+    host_out = torch.empty(max(8, b.set_elems), dtype=torch.int16, pin_memory=True)
+    outs = []
+    for ci in range(len(b.calls)):
+        spans = b.read_spans[ci]
+        a, e_, o, rel = spans[0] if spans else (0, 0, 0, 0)
+        assert o - rel >= 0, "host results are laid out like the compact device sets"
+        outs.append(host_out.data_ptr() + 2 * (o - rel))
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    t = time.perf_counter()
-    applied = 0
-    fetch(0)
-    for k in range(steps):
-        compute.wait_event(copied[k % len(bufs)])
-        if len(bufs) > 1 and k + 1 < steps:
-            fetch(k + 1)
-        res, _ = b.step(bufs[k % len(bufs)], wait=True)   # reads the step result back
-        applied += 1 - res.skipped
-        if len(bufs) == 1 and k + 1 < steps:
-            fetch(k + 1)
-    torch.cuda.synchronize()
-    el = time.perf_counter() - t
-    if dist:
-        el = max_over_ranks(el, dist)
+
+    def one_step():
+        for ci, (which, lo, hi) in enumerate(b.calls):
+            if w.stage == 3:
+                g.gather(which, b.run.gather_buf)
+                g.release(which)
+            g.step_host([t.data_ptr() for t in host_sets[ci % 2]], which, b.hyper, outs[ci])
+        return g.finish_host()             # waits for every copy; reads the step state back
+
+    def timed(n):
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t = time.perf_counter()
+        applied = 0
+        for _ in range(n):
+            applied += 1 - one_step().skipped
+        el = time.perf_counter() - t
+        if dist:
+            el = max_over_ranks(el, dist)
+        return el, applied
+
+    one_step()                                            # warm-up (creates the copy streams)
+    el, applied = timed(steps)
+    h2d = Z.zero_get_option(g.plan, Z.ZERO_OPT_HOST_H2D_BYTES)
+    d2h = Z.zero_get_option(g.plan, Z.ZERO_OPT_HOST_D2H_BYTES)
+    g.set_option(Z.ZERO_OPT_HOST_PIPELINE, 0)
+    n_serial = max(1, min(3, steps))
+    el_serial, _ = timed(n_serial)
+    g.set_option(Z.ZERO_OPT_HOST_PIPELINE, 1)
+    ms = 1e3 * el / steps
+    ms_serial = 1e3 * el_serial / n_serial
+    hidden_ms = ms_serial - ms
+    step_bytes = b.elems_per_step * b.bytes_per_elem
+    hidden_frac = max(0.0, min(1.0, hidden_ms / device_ms_per_step)) if device_ms_per_step > 0 else 0.0
     return {"value": job_value(b.elems_per_step, applied, world, el), "unit": UNIT,
-            "h2d_bytes_per_step": 2 * b.set_elems * b.w.n_d, "d2h_bytes_per_step": 64,
-            "steps": steps, "double_buffered": len(bufs) > 1}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h) + 96,
+            "steps": steps, "api": "zero_step_host / zero_step_host_finish",
+            "host_link_gbs": round((h2d + d2h) / (ms / 1e3) / 1e9, 1),
+            "overlap": {"pipelined_ms_per_step": round(ms, 3),
+                        "serial_ms_per_step": round(ms_serial, 3),
+                        "hidden_ms_per_step": round(hidden_ms, 3),
+                        "device_step_ms": round(device_ms_per_step, 3),
+                        "device_step_hidden_fraction": round(hidden_frac, 4),
+                        "device_step_bytes_hidden": int(hidden_frac * step_bytes)}}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -666,21 +736,20 @@ def e2e_leg(b: Bench, steps: int, world: int, dist):
 def oracle_sample_run(w, sample_elems: int, steps: int, warmup: int = 0):
     """Time the CPU oracle (single thread) on the first `sample_elems` flat elements."""
     import numpy as np
-    import oracle
+    import oracle                      # the CPU baseline legs alone load the oracle
     import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import gpu_harness as H
+    from synth.fill import fill_host
     L = oracle.Layout(w.sizes, w.n_d, w.unit_first or None)
     units = [tuple(int(x) for x in u) for u in L.units]
     n = min(sample_elems, L.total_pad)
-    p = oracle.widen16(H.fill_host(synth.param_stream(w), units, 0, n), w.dtype).astype(np.float32)
+    p = oracle.widen16(fill_host(synth.param_stream(w), units, 0, n), w.dtype).astype(np.float32)
     m = np.zeros(n, np.float32)
     v = np.zeros(n, np.float32)
     out16 = np.zeros(n, np.uint16)
     sc = oracle.ScalerState(w.scaler)
     times = []
     for k in range(1, warmup + steps + 1):
-        c = [H.fill_host(synth.grad_stream(w, k, r), units, 0, n) for r in range(w.n_d)]
+        c = [fill_host(synth.grad_stream(w, k, r), units, 0, n) for r in range(w.n_d)]
         t = time.perf_counter()
         k9 = oracle.consts(w.hyper, sc.t + 1, sc.scale, w.n_d)
         g, flag = oracle.reduce(c, w.dtype, float(k9[8]))

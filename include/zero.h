@@ -24,8 +24,9 @@
  *    (state, contributions, 16-bit buffers, workspace) is owned by the caller
  *    and is never freed by the library.  The library allocates no device memory.
  *  - Calls that take a `stream` (a cudaStream_t passed as void*) are
- *    asynchronous on it, except zero_set_scaler, zero_read_state and
- *    zero_step_finish with a result pointer, which synchronise it.  The skip
+ *    asynchronous on it, except zero_set_scaler, zero_read_state,
+ *    zero_step_host_finish and zero_step_finish with a result pointer, which
+ *    synchronise it.  The skip
  *    decision, the applied-step count t, the current ping-pong half and the
  *    loss scale live on the device (in the workspace), so a training loop
  *    enqueues step after step without waiting for the host.  Issue every call
@@ -110,6 +111,9 @@ typedef struct {
     int32_t stage;
     int32_t dtype16;
     int32_t reserved;
+    int64_t host_staging_bytes; /* each of the two device staging areas zero_bind_host_staging
+                                   takes: N_d areas of max_contrib_elems 16-bit elements, each
+                                   rounded up to a multiple of 8 elements */
 } zero_plan_info_t;
 
 /* Table selectors for zero_plan_tables (all entries int64, row-major). */
@@ -327,7 +331,17 @@ enum {
                                        (1 staged, 0 register loads, -1 none yet) */
     ZERO_OPT_GATHER_STAGING = 5,
     ZERO_OPT_GATHER_CHUNK = 6,
-    ZERO_OPT_GATHER_STAGES = 7
+    ZERO_OPT_GATHER_STAGES = 7,
+    ZERO_OPT_HOST_PIPELINE = 8,     /* zero_step_host: 1 (default) copies the next call's
+                                       gradients while this call's step runs; 0 runs each call's
+                                       host->device copies, step and device->host copies one
+                                       after another, after the previous call's (for measuring
+                                       what the overlap hides) */
+    ZERO_OPT_HOST_H2D_BYTES = 9,    /* read only: bytes zero_step_host copied host->device in
+                                       the last step finished by zero_step_host_finish */
+    ZERO_OPT_HOST_D2H_BYTES = 10    /* read only: bytes copied device->host in that step (the
+                                       updated 16-bit parameters, re-copies after a skip
+                                       included) */
 };
 enum { ZERO_STAGING_REGISTER_LOADS = 0, ZERO_STAGING_BULK = 1, ZERO_STAGING_AUTO = 2 };
 zero_status_t zero_set_option(zero_plan_t* plan, int option, int64_t value);
@@ -396,6 +410,44 @@ zero_status_t zero_offload_step(zero_plan_t* plan, const void* const* grad_contr
 zero_status_t zero_offload_finish(zero_plan_t* plan, int threads, void* stream,
                                   zero_step_result_t* out);
 
+/* ---- Steps fed from host memory ("Execution Flow for ZeRO-1" steps 2-4 with the gradients
+ * and the all-gather's result in host memory; "Overlapping Computation and Communication
+ * Streams": the transfer of the next bucket runs while the current one is reduced and
+ * updated). ----
+ * Bind two device staging areas (caller-owned device memory, each at least
+ * info.host_staging_bytes, 16-byte aligned, distinct) for zero_step_host.  Area k of a call
+ * holds rank r's contribution at byte offset r * (info.host_staging_bytes / N_d).  Not inside
+ * an open step; bind every rank first. */
+zero_status_t zero_bind_host_staging(zero_plan_t* plan, void* const staging[2], int64_t bytes_each);
+
+/* zero_step for bucket / unit `which` with host buffers:
+ *   host_contribs[n_contribs]  n_contribs == N_d pointers to pinned host memory (cudaHostAlloc
+ *                              or cudaHostRegister), laid out like zero_step's contributions
+ *                              (the bucket's or unit's range); only the slices the bound ranks
+ *                              read are copied
+ *   host_out16                 pinned host memory of the same range length: receives the
+ *                              updated 16-bit parameters of every element the bound ranks own
+ *                              in the range (all ranks bound: the whole range, i.e. what the
+ *                              all-gather delivers), at the element's offset in the range
+ * The library copies the slices into staging area (call count mod 2) on its own copy stream
+ * once the step that last read that area is done, runs zero_step on `stream` after the copies,
+ * and copies the 16-bit results to host_out16 on a second stream of its own after the step.
+ * With ZERO_OPT_HOST_PIPELINE = 1 (default) the copies of the next call therefore run while
+ * this call's step does.  Asynchronous: host_contribs must stay unchanged and host_out16 is
+ * not final until zero_step_host_finish returns.  No clipping on this path (max_grad_norm
+ * must be 0); ZERO_REPORT_GRAD_NORM is allowed.  ZERO_ESTATE without bound staging;
+ * ZERO_EINVAL for NULL or unpinned host pointers and the argument errors of zero_step. */
+zero_status_t zero_step_host(zero_plan_t* plan, const void* const* host_contribs,
+                             int64_t n_contribs, int64_t which, const zero_hyper_t* hyper,
+                             void* host_out16, void* stream);
+
+/* End a step that had zero_step_host calls: zero_step_finish on `stream`, then wait for every
+ * device->host copy; if the step was skipped (or discarded, ZERO_ETIMEOUT) the re-cast 16-bit
+ * parameters are copied to each call's host_out16 again.  Always synchronises; out (may be
+ * NULL) and the return value as for zero_step_finish with a result pointer.  A step with host
+ * calls must end here (zero_step_finish returns ZERO_ESTATE for it). */
+zero_status_t zero_step_host_finish(zero_plan_t* plan, void* stream, zero_step_result_t* out);
+
 /* Release after use ("ZeRO-3 / FSDP Layer Execution Lifecycle": the full parameters of a unit
  * are freed once its forward or backward is done): mark unit `unit`'s gathered buffer free;
  * the caller may reuse its memory.  ZERO_ESTATE if the unit is not gathered. */
@@ -431,12 +483,13 @@ zero_status_t zero_comm_report(const zero_plan_t* plan, zero_comm_report_t* out)
  *   t                    1-based index of the step being applied (bias correction)
  *   loss_scale           gradients are multiplied by 1 / (n_d * loss_scale)
  *   *nonfinite           receives 1 if any reduced gradient element is inf/nan, else 0
- * The call is enqueued on `stream` and then synchronises it to read the flag.
+ * The call enqueues its work on `stream` and then synchronises `stream` to read the flag.
  *
- * Set-up: the first call on each device looks up the array's device address (with that device
- * current) and caches it; make that first call before any stream capture.  All calls share
- * the one array: the flag is cleared at the start of every call, and calls that overlap on
- * the GPU (different streams, threads or processes sharing the library) race on it.
+ * Set-up: the first call on each device (in each CUDA context: a device reset makes a new
+ * one) looks up the array's device address, with that device current, and caches it; make
+ * that first call before any stream capture begins.  All calls share the one array: the flag
+ * is cleared at the start of every call, and calls that overlap on the GPU (different
+ * streams, threads or processes sharing the library) race on it.
  * Limits: n_d <= ZERO_MAX_RANKS (else ZERO_ERANGE); the call uses 4 of the
  * ZERO_NOALLOC_SCRATCH_BYTES bytes whatever n and n_d are.
  * --------------------------------------------------------------------------------------- */

@@ -1,0 +1,254 @@
+"""GPU parity of the host-buffer step (zero_step_host / zero_step_host_finish).
+
+Each rank's 16-bit gradient contribution sits in pinned host memory; the library copies the
+slices the bound ranks read into a device staging area (the next call's copies running while
+this call's step does), runs the fused step, and copies the updated 16-bit parameters back
+to host memory.  Compared with the oracle on the same seeded inputs: the device state
+element by element, and the host-side 16-bit results against the oracle's parameters;
+skipped steps included (their re-cast parameters must reach the host too).
+
+Tolerances as everywhere: fp32 |gpu - oracle| <= 1e-6 |oracle| + 1e-8, 16-bit <= 1 ulp,
+skip decisions, t and the loss scale exact, byte counts exact.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+import synth
+import zero_sharded_mixed_03_gb300 as Z
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    Z.lib()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _mk(wid, sizes, n_d, stage, steps=3, bucket=0, units=(), dtype=W.BF16, scaler=None,
+        outliers=False, inject=None, bound=None):
+    return W.Workload(wid=wid, name=f"host{wid}", sizes=tuple(sizes), n_d=n_d, stage=stage,
+                      bucket_elems=bucket, unit_first=tuple(units), dtype=dtype, steps=steps,
+                      hyper=W.Hyper(), scaler=scaler, outliers=outliers, inject=inject,
+                      bound_ranks=bound)
+
+
+def _ragged(seed, n, hi):
+    rng = np.random.default_rng(seed)
+    return [int(x) for x in rng.integers(1, hi, size=n)]
+
+
+CASES = {
+    # ZeRO-2 buckets, fp16, loss scale, a planted inf at step 2 (skip + back-off)
+    "z2_nd8_fp16_buckets_skip": _mk(401, _ragged(2, 40, 9000), 8, 2, steps=4, bucket=10_000,
+                                    dtype=W.FP16, scaler=W.Scaler(), outliers=True,
+                                    inject=(2, 3, 77_777)),
+    # one call over the whole buffer, ragged tiles
+    "z1_nd4_one_call": _mk(402, [3 * 65536 + 13], 4, 1),
+    # a subset of the ranks bound: only their shard slices are copied
+    "z2_nd8_subset_bound": _mk(403, _ragged(9, 25, 8000), 8, 2, bucket=8000, bound=(1, 6)),
+    # ZeRO-3 units with peers and a skipped first step
+    "z3_nd3_fp16_peers_skip_first": _mk(404, _ragged(5, 12, 3000), 3, 3, units=(0, 4, 9),
+                                        dtype=W.FP16, scaler=W.Scaler(init_scale=1024.0),
+                                        inject=(1, 2, 1234), bound=(0, 2)),
+    "z3_nd16_units": _mk(405, _ragged(4, 24, 6000), 16, 3, units=(0, 5, 11, 17, 23)),
+    # odd bucket size: the scalar path of the kernel on the staged contributions
+    "z2_nd5_odd_bucket": _mk(406, _ragged(3, 30, 7000), 5, 2, bucket=12_345),
+}
+
+
+def _expected_host16(run, o, which, lo, hi):
+    """(mask, values) of the host result of call `which` (range [lo, hi)): the oracle's 16-bit
+    parameters of the elements the bound ranks own."""
+    w = run.w
+    n = hi - lo
+    mask = np.zeros(n, dtype=bool)
+    want = np.zeros(n, dtype=np.uint16)
+    if w.per_param:
+        for (r, u, _t, _row0, rows, cols, _cr, coff, soff) in o.pp.chunks:
+            if u == which and rows and r in run.bound:
+                mask[coff:coff + rows * cols] = True
+                want[coff:coff + rows * cols] = o.sh16[r][soff:soff + rows * cols]
+        return mask, want
+    if w.stage == 3:
+        (_f, _c, _numel, _pad, S, _base, sb) = o.units[which]
+        for r in run.bound:
+            mask[r * S:(r + 1) * S] = True
+            want[r * S:(r + 1) * S] = o.sh16[r][sb:sb + S]
+        return mask, want
+    S = o.units[0][4]
+    idx = np.arange(lo, hi)
+    mask = np.isin(idx // S, run.bound)
+    want = o.full16[lo:hi].copy()
+    return mask, want
+
+
+def _run_host(w, pipeline, one_call=False, options=None):
+    run = H.Run(w, alloc_contribs=False, options=options)
+    o = H.OracleFull(w, run.bound)
+    try:
+        run.g.bind_host_staging()
+        run.g.set_option(Z.ZERO_OPT_HOST_PIPELINE, pipeline)
+        calls = run.ranges()
+        # one pinned set per call: the copies of one call may still run while the next is filled
+        host = [[torch.zeros(max(8, hi - lo), dtype=torch.int16, pin_memory=True)
+                 for _ in range(w.n_d)] for (_w, lo, hi) in calls]
+        out = [torch.zeros(max(8, hi - lo), dtype=torch.int16, pin_memory=True)
+               for (_w, lo, hi) in calls]
+        gbuf = run.gather_buf
+        for k in range(1, w.steps + 1):
+            expect_h2d = expect_d2h = 0
+            for ci, (which, lo, hi) in enumerate(calls):
+                for r in range(w.n_d):
+                    vals = H.fill_host(synth.grad_stream(w, k, r), run.units, lo, hi)
+                    host[ci][r][:hi - lo].copy_(torch.from_numpy(vals.view(np.int16)))
+                if w.stage == 3:
+                    run.g.gather(which, gbuf)
+                    run.g.release(which)
+                call = -1 if one_call else which
+                run.g.step_host([t.data_ptr() for t in host[ci]], call, run.hyper,
+                                out[ci].data_ptr())
+                mask, _ = _expected_host16(run, o, which, lo, hi)
+                owned = int(mask.sum())
+                expect_h2d += 2 * w.n_d * owned   # every contribution's slices of owned elements
+                expect_d2h += 2 * owned
+            res = run.g.finish_host()
+            flag = o.step(k)
+            assert res.skipped == flag, f"step {k}"
+            assert res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
+            H.compare_full(run, o, f"{w.name} host step {k}")
+            for ci, (which, lo, hi) in enumerate(calls):
+                mask, want = _expected_host16(run, o, which, lo, hi)
+                got = out[ci][:hi - lo].numpy().view(np.uint16)
+                H.assert_16_close(got[mask], want[mask], f"{w.name} step {k} call {which} host16")
+            h2d = Z.zero_get_option(run.g.plan, Z.ZERO_OPT_HOST_H2D_BYTES)
+            d2h = Z.zero_get_option(run.g.plan, Z.ZERO_OPT_HOST_D2H_BYTES)
+            # a skipped step copies its re-cast parameters once more
+            assert d2h == expect_d2h * (2 if flag else 1), (k, d2h, expect_d2h)
+            assert h2d == expect_h2d, (k, h2d, expect_h2d)
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("pipeline", [1, 0])
+@pytest.mark.parametrize("name", list(CASES))
+def test_host_path_full_parity(name, pipeline):
+    _run_host(CASES[name], pipeline)
+
+
+def test_host_path_one_call_over_the_whole_buffer():
+    _run_host(CASES["z1_nd4_one_call"], 1, one_call=True)
+
+
+@pytest.mark.parametrize("staging", [0, 1])
+def test_host_path_both_step_kernels(staging):
+    _run_host(CASES["z3_nd16_units"], 1, options={Z.ZERO_OPT_STAGING: staging})
+
+
+def test_host_path_per_parameter_plan():
+    w = W.Workload(wid=407, name="host_pp", sizes=(12 * 7, 5 * 3, 40 * 9, 2 * 11, 64), n_d=4,
+                   stage=3, bucket_elems=0, unit_first=(0, 2, 4), dtype=W.BF16, steps=3,
+                   hyper=W.Hyper(), scaler=None, dim0=(12, 5, 40, 2, 8), per_param=True,
+                   bound_ranks=(0, 3))
+    _run_host(w, 1)
+
+
+def test_host_path_config2_pipelined_sampled():
+    """The bucketed ZeRO-2 GPT-2-small workload at full size (fp16, 5 buckets of 25M, 8 ranks,
+    loss scale 2^16) fed from host memory with the bucket copies pipelined, over its first four
+    steps (the planted inf at step 3 is skipped); sampled elements against the oracle."""
+    w = dataclasses.replace(W.workload(2), steps=4)
+    run = H.Run(w, alloc_contribs=False)
+    try:
+        run.g.bind_host_staging()
+        assert Z.zero_get_option(run.g.plan, Z.ZERO_OPT_HOST_PIPELINE) == 1
+        idx = H.sample_indices(run, 20000)
+        o = H.OracleSampled(w, idx)
+        calls = run.ranges()
+        assert len(calls) == 5
+        host = [[torch.empty(hi - lo, dtype=torch.int16, pin_memory=True) for _ in range(w.n_d)]
+                for (_w, lo, hi) in calls]
+        out = [torch.zeros(hi - lo, dtype=torch.int16, pin_memory=True) for (_w, lo, hi) in calls]
+        for k in range(1, w.steps + 1):
+            for ci, (which, lo, hi) in enumerate(calls):
+                for r in range(w.n_d):
+                    synth.grad_stream(w, k, r).host_into(host[ci][r].numpy().view(np.uint16), lo)
+                run.g.step_host([t.data_ptr() for t in host[ci]], which, run.hyper,
+                                out[ci].data_ptr())
+            res = run.g.finish_host()
+            flag = o.step(k)
+            assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
+            st, g16 = run.read_sampled(idx)
+            for key, want in (("master", o.p), ("m", o.m), ("v", o.v)):
+                H.assert_state_close(st[key], want, f"config2 host step {k} {key}")
+            H.assert_16_close(g16, o.out16, f"config2 host step {k} device 16-bit")
+            host16 = np.concatenate([t.numpy().view(np.uint16) for t in out])
+            H.assert_16_close(host16[idx], o.out16, f"config2 host step {k} host 16-bit")
+            assert Z.zero_get_option(run.g.plan, Z.ZERO_OPT_HOST_H2D_BYTES) == 2 * w.n_d * w.phi
+    finally:
+        run.close()
+
+
+def test_host_path_errors():
+    w = CASES["z2_nd5_odd_bucket"]
+    run = H.Run(w, alloc_contribs=False)
+    try:
+        plan = run.g.plan
+        info = run.info
+        calls = run.ranges()
+        which, lo, hi = calls[0]
+        host = [torch.zeros(hi - lo, dtype=torch.int16, pin_memory=True) for _ in range(w.n_d)]
+        out = torch.zeros(hi - lo, dtype=torch.int16, pin_memory=True)
+        ptrs = [t.data_ptr() for t in host]
+        with pytest.raises(Z.ZeroError) as e:                    # no staging bound
+            Z.zero_step_host(plan, ptrs, which, run.hyper, out.data_ptr())
+        assert e.value.status == Z.ZERO_ESTATE
+        a = torch.empty(int(info.host_staging_bytes) + 64, dtype=torch.uint8, device="cuda")
+        with pytest.raises(Z.ZeroError) as e:                    # too small
+            Z.zero_bind_host_staging(plan, [a.data_ptr(), a.data_ptr() + 16], int(info.host_staging_bytes) - 2)
+        assert e.value.status == Z.ZERO_ERANGE
+        with pytest.raises(Z.ZeroError) as e:                    # the two areas overlap
+            Z.zero_bind_host_staging(plan, [a.data_ptr(), a.data_ptr() + 16], int(info.host_staging_bytes))
+        assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:                    # host memory is not device memory
+            Z.zero_bind_host_staging(plan, [host[0].data_ptr(), host[1].data_ptr()], int(info.host_staging_bytes))
+        assert e.value.status == Z.ZERO_EINVAL
+        run.g.bind_host_staging()
+        pageable = np.zeros(hi - lo, dtype=np.uint16)
+        with pytest.raises(Z.ZeroError) as e:                    # contributions must be pinned
+            Z.zero_step_host(plan, [pageable.ctypes.data] + ptrs[1:], which, run.hyper, out.data_ptr())
+        assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:                    # so must the result buffer
+            Z.zero_step_host(plan, ptrs, which, run.hyper, pageable.ctypes.data)
+        assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:                    # no clipping on this path
+            Z.zero_step_host(plan, ptrs, which, Z.hyper(max_grad_norm=1.0), out.data_ptr())
+        assert e.value.status in (Z.ZERO_EINVAL, Z.ZERO_ESTATE)
+        # a step with host calls must end with zero_step_host_finish (the host buffers stay
+        # alive until it returns)
+        keep = []
+        for (wh, lo2, hi2) in calls:
+            hb = [torch.zeros(hi2 - lo2, dtype=torch.int16, pin_memory=True) for _ in range(w.n_d)]
+            ob = torch.zeros(hi2 - lo2, dtype=torch.int16, pin_memory=True)
+            keep.append((hb, ob))
+            Z.zero_step_host(plan, [t.data_ptr() for t in hb], wh, run.hyper, ob.data_ptr())
+            with pytest.raises(Z.ZeroError) as e:                # the same bucket twice
+                Z.zero_step_host(plan, [t.data_ptr() for t in hb], wh, run.hyper, ob.data_ptr())
+            assert e.value.status == Z.ZERO_ESTATE
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_step_finish(plan, torch.cuda.current_stream().cuda_stream)
+        assert e.value.status == Z.ZERO_ESTATE
+        res = run.g.finish_host()
+        assert res.t == 1 and res.skipped == 0
+    finally:
+        torch.cuda.synchronize()
+        run.close()

@@ -62,18 +62,7 @@ SMALL_CASES = {
 
 
 def _compare_full(run: H.Run, o: H.OracleFull, label: str):
-    mism = 0
-    for r in run.bound:
-        got = run.read_logical(r)
-        for k, want in (("master", o.p[r]), ("m", o.m[r]), ("v", o.v[r])):
-            mism += H.assert_state_close(got[k], want, f"{label} rank {r} {k}")
-        if run.w.stage == 3:
-            g16 = run.g.logical(r, run.g.shard16[r]).cpu().numpy().view(np.uint16)
-            mism += H.assert_16_close(g16, o.sh16[r], f"{label} rank {r} shard16")
-    if run.w.stage != 3:
-        g16 = run.g.full16.cpu().numpy().view(np.uint16)
-        mism += H.assert_16_close(g16, o.full16, f"{label} full16")
-    return mism
+    return H.compare_full(run, o, label)
 
 
 def _run_full(w: W.Workload, options=None):

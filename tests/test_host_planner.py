@@ -205,17 +205,23 @@ def test_execution_options_are_checked_on_the_host():
         assert Z.zero_get_option(plan, Z.ZERO_OPT_BULK_TILE) == 2048      # 2048 x 26 B <= 53.5 KB
         assert Z.zero_get_option(plan, Z.ZERO_OPT_BULK_STAGES) == 2
         assert Z.zero_get_option(plan, Z.ZERO_OPT_LAST_STEP_KERNEL) == -1
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_HOST_PIPELINE) == 1
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_HOST_H2D_BYTES) == 0
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_HOST_D2H_BYTES) == 0
         with pytest.raises(Z.ZeroError) as e:
-            Z.zero_get_option(plan, 9)
+            Z.zero_get_option(plan, 99)
         assert e.value.status == Z.ZERO_EINVAL
         for opt, val in ((Z.ZERO_OPT_STAGING, 3), (Z.ZERO_OPT_STAGING, -1),
                          (Z.ZERO_OPT_WAIT_LIMIT_NS, -1), (Z.ZERO_OPT_BULK_TILE, 12),
                          (Z.ZERO_OPT_BULK_TILE, 16384), (Z.ZERO_OPT_BULK_TILE, 4),
-                         (Z.ZERO_OPT_BULK_STAGES, 1), (Z.ZERO_OPT_BULK_STAGES, 17), (9, 0)):
+                         (Z.ZERO_OPT_BULK_STAGES, 1), (Z.ZERO_OPT_BULK_STAGES, 17), (99, 0),
+                         (Z.ZERO_OPT_HOST_PIPELINE, 2), (Z.ZERO_OPT_HOST_H2D_BYTES, 0),
+                         (Z.ZERO_OPT_HOST_D2H_BYTES, 0), (Z.ZERO_OPT_LAST_STEP_KERNEL, 0)):
             with pytest.raises(Z.ZeroError) as e:
                 Z.zero_set_option(plan, opt, val)
             assert e.value.status == Z.ZERO_EINVAL, (opt, val)
         for opt, val in ((Z.ZERO_OPT_STAGING, 1), (Z.ZERO_OPT_STAGING, 2), (Z.ZERO_OPT_STAGING, 0),
+                         (Z.ZERO_OPT_HOST_PIPELINE, 0), (Z.ZERO_OPT_HOST_PIPELINE, 1),
                          (Z.ZERO_OPT_WAIT_LIMIT_NS, 0), (Z.ZERO_OPT_BULK_TILE, 4096),
                          (Z.ZERO_OPT_BULK_TILE, 1024), (Z.ZERO_OPT_BULK_STAGES, 8)):
             Z.zero_set_option(plan, opt, val)
@@ -396,3 +402,28 @@ def test_unit_slice_keeps_one_unit_of_a_stage3_workload():
     assert pp.dim0 == W.per_param_variant(W.workload(4)).dim0[f4:f4 + c4] and pp.per_param
     with pytest.raises(ValueError):
         W.unit_slice(W.workload(1), 0)                 # stage 2: no units
+
+
+def test_host_staging_size_and_host_path_state_errors():
+    """info.host_staging_bytes = N_d areas of the largest call's range rounded up to a multiple
+    of 8 elements, 2 bytes each; the host-buffer calls refuse an unbound plan (no GPU needed)."""
+    for sizes, n_d, stage, bucket, units in (([10, 20, 7], 3, 2, 9, None), ([1000], 4, 1, 0, None),
+                                             ([5, 6, 7, 8], 2, 3, 0, [0, 2])):
+        plan = _plan_for(sizes, n_d, stage, bucket, units)
+        try:
+            info = Z.zero_plan_info(plan)
+            assert info.host_staging_bytes == n_d * (-(-info.max_contrib_elems // 8) * 8) * 2
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_bind_host_staging(plan, [16, 4096], info.host_staging_bytes)
+            assert e.value.status == Z.ZERO_ESTATE               # no rank bound yet
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_step_host(plan, [16] * n_d, 0, Z.hyper(), 16)
+            assert e.value.status == Z.ZERO_ESTATE
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_step_host_finish(plan)
+            assert e.value.status == Z.ZERO_ESTATE               # no host call in the step
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_step_host(plan, [16] * (n_d + 1), 0, Z.hyper(), 16)
+            assert e.value.status == Z.ZERO_EINVAL
+        finally:
+            Z.zero_plan_destroy(plan)

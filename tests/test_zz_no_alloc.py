@@ -1,12 +1,13 @@
-"""The no-allocation entry point, checked against the plan-based step on the GPU.
+"""The no-allocation entry point, checked against the plan-based step and the oracle on the GPU.
 
 Some callers cannot allocate device memory: their host framework has reserved the GPU's
 memory for its own pool, or their loop cannot afford cudaMalloc/cudaFree, which may
 synchronise the whole device.  Those callers cannot hand zero_bind a workspace, so they use
 zero_step_range_noalloc, whose only scratch (the non-finite flag) lives in a static device
-array inside the library.  These tests run it through the C ABI and compare it with the
-plan-based zero_step / zero_step_finish on the same inputs, two steps in a row, within the
-tolerances the other parity tests use.  This file is collected last on purpose.
+array inside the library.  These tests run it through the C ABI and compare it, two steps in
+a row, with the plan-based zero_step / zero_step_finish on the same inputs and with the CPU
+oracle's step on the same seeded values, within the tolerances the other parity tests use.
+This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -38,6 +39,7 @@ def _workload(dtype, scaler=None, inject=None):
 def test_noalloc_matches_plan_step_two_calls(dtype):
     w = _workload(dtype, scaler=W.Scaler(init_scale=512.0) if dtype == W.FP16 else None)
     run = H.Run(w)
+    o = H.OracleFull(w, run.bound)          # the oracle on the same seeded inputs
     try:
         S = run.units[0][4]
         scale = run.scaler.scale if run.scaler is not None else 1.0
@@ -49,6 +51,7 @@ def test_noalloc_matches_plan_step_two_calls(dtype):
         for k in (1, 2):
             res = run.step(k)                       # the existing entry point (plan-based)
             assert res.skipped == 0
+            assert o.step(k) == 0
             # this step's contributions (regenerated into the buffers run.step used)
             for rr in range(w.n_d):
                 H.fill_device(run.contribs[rr], synth.grad_stream(w, k, rr), run.units, 0,
@@ -67,6 +70,11 @@ def test_noalloc_matches_plan_step_two_calls(dtype):
                     H.assert_state_close(outs[key].cpu().numpy(), want[key], f"step {k} rank {r} {key}")
                 full16 = run.g.full16[r * S:(r + 1) * S].cpu().numpy().view(np.uint16)
                 H.assert_16_close(out16.cpu().numpy().view(np.uint16), full16, f"step {k} rank {r} 16-bit")
+                # and directly against the oracle
+                for key, want in (("master", o.p[r]), ("m", o.m[r]), ("v", o.v[r])):
+                    H.assert_state_close(outs[key].cpu().numpy(), want, f"oracle step {k} rank {r} {key}")
+                H.assert_16_close(out16.cpu().numpy().view(np.uint16), o.full16[r * S:(r + 1) * S],
+                                  f"oracle step {k} rank {r} 16-bit")
                 mine[r] = outs                      # the next call reads this call's outputs
     finally:
         run.close()

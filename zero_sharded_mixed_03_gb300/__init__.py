@@ -21,7 +21,8 @@ ZERO_MAX_RANKS = 128
 ZERO_REPORT_GRAD_NORM = 1
 (ZERO_OPT_STAGING, ZERO_OPT_WAIT_LIMIT_NS, ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES,
  ZERO_OPT_LAST_STEP_KERNEL, ZERO_OPT_GATHER_STAGING, ZERO_OPT_GATHER_CHUNK,
- ZERO_OPT_GATHER_STAGES) = range(8)
+ ZERO_OPT_GATHER_STAGES, ZERO_OPT_HOST_PIPELINE, ZERO_OPT_HOST_H2D_BYTES,
+ ZERO_OPT_HOST_D2H_BYTES) = range(11)
 ZERO_STAGING_REGISTER_LOADS, ZERO_STAGING_BULK, ZERO_STAGING_AUTO = range(3)
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)
@@ -35,6 +36,7 @@ EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", 
             "zero_read_state", "zero_restore_state", "zero_grad_norm",
             "zero_step_units_overlapped", "zero_bind_offload", "zero_offload_step",
             "zero_offload_finish", "zero_set_option", "zero_get_option",
+            "zero_bind_host_staging", "zero_step_host", "zero_step_host_finish",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
@@ -65,7 +67,7 @@ class zero_plan_info_t(ctypes.Structure):
                 ("max_contrib_elems", ctypes.c_int64), ("max_unit_pad", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("n_d", ctypes.c_int32),
                 ("stage", ctypes.c_int32), ("dtype16", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32), ("host_staging_bytes", ctypes.c_int64)]
 
 
 class zero_step_result_t(ctypes.Structure):
@@ -138,6 +140,12 @@ def lib() -> ctypes.CDLL:
         L.zero_offload_step.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t), _vp]
         L.zero_offload_finish.restype = st
         L.zero_offload_finish.argtypes = [_vp, _int, _vp, ctypes.POINTER(zero_step_result_t)]
+        L.zero_bind_host_staging.restype = st
+        L.zero_bind_host_staging.argtypes = [_vp, _vp, _i64]
+        L.zero_step_host.restype = st
+        L.zero_step_host.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t), _vp, _vp]
+        L.zero_step_host_finish.restype = st
+        L.zero_step_host_finish.argtypes = [_vp, _vp, ctypes.POINTER(zero_step_result_t)]
         L.zero_grad_norm.restype = st
         L.zero_grad_norm.argtypes = [_vp, _vp, _i64, _i64, _vp]
         L.zero_set_option.restype = st
@@ -293,6 +301,23 @@ def zero_offload_finish(plan: int, threads: int, stream: int = 0,
     return res
 
 
+def zero_bind_host_staging(plan: int, staging: Sequence[int], bytes_each: int) -> None:
+    _check(lib().zero_bind_host_staging(plan, _ptr_array(staging), bytes_each))
+
+
+def zero_step_host(plan: int, host_contribs: Sequence[int], which: int, hyper: zero_hyper_t,
+                   host_out16: int, stream: int = 0) -> None:
+    _check(lib().zero_step_host(plan, _ptr_array(host_contribs), len(host_contribs), which,
+                                ctypes.byref(hyper), host_out16 or None, stream or None))
+
+
+def zero_step_host_finish(plan: int, stream: int = 0) -> zero_step_result_t:
+    """End a step that had zero_step_host calls (synchronises); returns the step state."""
+    res = zero_step_result_t()
+    _check(lib().zero_step_host_finish(plan, stream or None, ctypes.byref(res)), res)
+    return res
+
+
 def zero_step_finish(plan: int, stream: int = 0, wait: bool = True) -> Optional[zero_step_result_t]:
     """Enqueue the commit; with wait=True also read back the step state (synchronises)."""
     res = zero_step_result_t() if wait else None
@@ -314,7 +339,8 @@ def zero_read_state(plan: int, stream: int = 0) -> zero_step_result_t:
 def zero_set_option(plan: int, option: int, value: int) -> None:
     """ZERO_OPT_STAGING (ZERO_STAGING_REGISTER_LOADS / _BULK / _AUTO), ZERO_OPT_WAIT_LIMIT_NS,
     ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES (0 = chosen from N_d); the gather's
-    ZERO_OPT_GATHER_STAGING, ZERO_OPT_GATHER_CHUNK, ZERO_OPT_GATHER_STAGES (0 = default)."""
+    ZERO_OPT_GATHER_STAGING, ZERO_OPT_GATHER_CHUNK, ZERO_OPT_GATHER_STAGES (0 = default);
+    ZERO_OPT_HOST_PIPELINE (host-buffer steps: 1 pipelined, 0 serial)."""
     _check(lib().zero_set_option(plan, option, int(value)))
 
 

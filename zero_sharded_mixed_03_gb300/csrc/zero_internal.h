@@ -169,6 +169,27 @@ struct zero_plan {
     void* off_flag_event = nullptr;
     void* off_side = nullptr;
     zero::WorkerPool* host_pool = nullptr;   // the host update's threads (created on first use)
+    // Steps fed from host memory (zero_step_host): two caller-owned device staging areas, the
+    // elements between consecutive ranks' parts of an area, the plan's two copy streams and
+    // its events (created on first use: copied[2], used[2], recast done), the calls issued so
+    // far (call k uses area k % 2), and the open step's device->host copies (repeated after a
+    // skipped step's re-cast) with its byte counts.
+    struct HostCopy {
+        uint16_t* host;
+        const uint16_t* dev;
+        int64_t n;
+    };
+    void* host_staging[2] = {nullptr, nullptr};
+    int64_t host_rank_stride = 0;
+    void* host_h2d = nullptr;
+    void* host_d2h = nullptr;
+    void* host_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    int64_t host_calls = 0;
+    bool host_step = false;
+    int host_pipeline = 1;
+    std::vector<HostCopy> host_outs;
+    int64_t host_h2d_bytes = 0, host_d2h_bytes = 0;             // the open step
+    int64_t host_h2d_last = 0, host_d2h_last = 0;               // the last finished host step
     void (*release_hook)(zero_plan*) = nullptr;
 };
 

@@ -346,6 +346,7 @@ try {
     }
     out->max_contrib_elems = maxc;
     out->max_unit_pad = maxu;
+    out->host_staging_bytes = (int64_t)p->n_d * ((maxc + 7) / 8 * 8) * 2;
     out->workspace_bytes = kWorkspaceBytes;
     out->n_d = p->n_d;
     out->stage = p->stage;

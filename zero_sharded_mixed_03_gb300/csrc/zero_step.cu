@@ -8,6 +8,8 @@
 #include <mutex>
 #include <unordered_map>
 
+#include <cuda.h>
+
 #include "zero_kernels.cuh"
 
 namespace zero {
@@ -615,6 +617,16 @@ void release_plan_resources(zero_plan* q)
         cudaStreamDestroy((cudaStream_t)q->off_side);
         q->off_side = nullptr;
     }
+    for (void*& ev : q->host_events)
+        if (ev) {
+            cudaEventDestroy((cudaEvent_t)ev);
+            ev = nullptr;
+        }
+    for (void** st : {&q->host_h2d, &q->host_d2h})
+        if (*st) {
+            cudaStreamDestroy((cudaStream_t)*st);
+            *st = nullptr;
+        }
 }
 
 // Create the event in *slot unless it exists: no timing, and a host thread that waits for it
@@ -629,6 +641,138 @@ cudaError_t offload_event(zero_plan* p, void** slot)
     p->release_hook = release_plan_resources;
     return cudaSuccess;
 }
+
+// Everything zero_step checks before it enqueues anything (shared with zero_step_host).
+zero_status_t check_step(const zero_plan* p, const void* const* grad_contribs, int64_t n_contribs,
+                         int64_t which, const zero_hyper_t* hyper, const char* fn)
+{
+    const std::string f(fn);
+    if (!hyper) return fail(ZERO_EINVAL, f + ": NULL argument");
+    if (p && p->offload) return fail(ZERO_ESTATE, f + ": offloaded plan (zero_offload_step)");
+    zero_status_t cst = check_call(p, grad_contribs, n_contribs, which, fn);
+    if (cst != ZERO_OK) return cst;
+    if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
+        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay) ||
+        !(hyper->max_grad_norm >= 0.0) || !std::isfinite(hyper->max_grad_norm))
+        return fail(ZERO_EINVAL, f + ": betas must lie in [0, 1); lr, eps, wd, max_grad_norm finite");
+    if (hyper->max_grad_norm > 0.0)
+        for (int64_t b = 0; b < p->n_buckets; ++b)
+            if (!p->norm_covered[(size_t)b])
+                return fail(ZERO_ESTATE, f + ": clipping needs zero_grad_norm over every bucket/unit first");
+    if (p->in_step && std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0)
+        return fail(ZERO_EINVAL, f + ": hyperparameters changed inside a step");
+    if (which == -1) {
+        if (p->in_step) return fail(ZERO_ESTATE, f + ": bucket -1 must be the only call of a step");
+    } else if (p->covered[(size_t)which]) {
+        return fail(ZERO_ESTATE, f + ": bucket/unit already stepped in this step");
+    }
+    return ZERO_OK;
+}
+
+// The launches of one checked zero_step call (device contribution pointers).
+zero_status_t enqueue_step(zero_plan* p, const void* const* grad_contribs, int64_t which,
+                           const zero_hyper_t* hyper, cudaStream_t s)
+{
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    if (!p->in_step) {
+        if (p->bias_len == 0 || p->bias_beta1 != hyper->beta1 || p->bias_beta2 != hyper->beta2) {
+            st = upload_bias_table(p, hyper->beta1, hyper->beta2, s);
+            if (st != ZERO_OK) return st;
+        }
+        // t, the loss scale and the current half are read on the device; the constants that
+        // do not depend on them are rounded here once.
+        step_constants(*hyper, 1, 1.0, p->n_d, p->consts);
+        p->step_hyper = *hyper;
+    }
+    // clip: the norm is complete on the device; report: accumulate it in this pass
+    int mode = kPlain;
+    if (hyper->max_grad_norm > 0.0) mode = kClip;
+    else if ((hyper->flags & ZERO_REPORT_GRAD_NORM) && !p->norm_open) mode = kNormAcc;
+    const std::vector<Segment> segs = step_segments(p, which, 0);
+    const BulkCfg bulk = bulk_config(p);
+    auto run = [&](auto& P, size_t cap) -> cudaError_t {
+        for (size_t b = 0; b < segs.size(); b += cap) {
+            const size_t e = std::min(segs.size(), b + cap);
+            fill_call_params(p, grad_contribs, P);
+            P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
+            const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
+            int used = 0;
+            const cudaError_t err = p->dtype16 == ZERO_BF16
+                                        ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode, &bulk, &used)
+                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode, &bulk, &used);
+            p->last_step_kernel = used;
+            if (err != cudaSuccess) return err;
+        }
+        return cudaSuccess;
+    };
+    cudaError_t lerr;
+    if (segs.size() > (size_t)kMaxSegs) {
+        StepParamsWide P;
+        lerr = run(P, kWideSegs);
+    } else {
+        StepParams P;
+        lerr = run(P, kMaxSegs);
+    }
+    if (lerr != cudaSuccess) return cuda_fail(lerr, "fused step launch");
+    p->in_step = true;
+    if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
+    else p->covered[(size_t)which] = 1;
+    return ZERO_OK;
+}
+
+// Steps fed from host memory: the plan's two copy streams and five events (copied[2],
+// used[2], the last device->host copy), created on first use and released with the plan.
+cudaError_t host_resources(zero_plan* p)
+{
+    if (p->host_h2d) return cudaSuccess;
+    cudaStream_t st[2] = {nullptr, nullptr};
+    cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        for (cudaEvent_t x : ev)
+            if (x) cudaEventDestroy(x);
+        for (cudaStream_t x : st)
+            if (x) cudaStreamDestroy(x);
+        return e;
+    }
+    p->host_h2d = st[0];
+    p->host_d2h = st[1];
+    for (int i = 0; i < 5; ++i) p->host_events[i] = ev[i];
+    p->release_hook = release_plan_resources;
+    return cudaSuccess;
+}
+
+bool pinned_host(const void* q)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+
+// [lo, hi) element ranges of a call's range that its work items read from every contribution,
+// merged where they touch or overlap.
+std::vector<std::pair<int64_t, int64_t>> read_runs(const std::vector<Segment>& segs)
+{
+    std::vector<std::pair<int64_t, int64_t>> r;
+    for (const Segment& sg : segs)
+        if (sg.n > 0) r.emplace_back(sg.c_off, sg.c_off + sg.n);
+    std::sort(r.begin(), r.end());
+    std::vector<std::pair<int64_t, int64_t>> out;
+    for (const auto& x : r) {
+        if (!out.empty() && x.first <= out.back().second) out.back().second = std::max(out.back().second, x.second);
+        else out.push_back(x);
+    }
+    return out;
+}
+
+// Re-cast + commit of the open step (zero_step_finish without its checks on host calls).
+zero_status_t finish_step(zero_plan_t* p, void* stream, zero_step_result_t* out);
 
 }  // namespace
 }  // namespace zero
@@ -772,6 +916,13 @@ try {
             return fail(ZERO_EINVAL, "zero_set_option: stages must be 0 or in [2, 16]");
         stages = value;
         break;
+    case ZERO_OPT_HOST_PIPELINE:
+        if (value != 0 && value != 1) return fail(ZERO_EINVAL, "zero_set_option: host pipeline must be 0 or 1");
+        p->host_pipeline = (int)value;
+        return ZERO_OK;
+    case ZERO_OPT_HOST_H2D_BYTES:
+    case ZERO_OPT_HOST_D2H_BYTES:
+        return fail(ZERO_EINVAL, "zero_set_option: read-only option");
     case ZERO_OPT_GATHER_STAGING:
         if (value != ZERO_STAGING_REGISTER_LOADS && value != ZERO_STAGING_BULK &&
             value != ZERO_STAGING_AUTO)
@@ -828,6 +979,9 @@ try {
     case ZERO_OPT_GATHER_STAGING: *value = p->gather_staging; return ZERO_OK;
     case ZERO_OPT_GATHER_CHUNK: *value = p->gather_chunk > 0 ? p->gather_chunk : kGatherDefaultChunk; return ZERO_OK;
     case ZERO_OPT_GATHER_STAGES: *value = p->gather_stages > 0 ? p->gather_stages : kGatherDefaultStages; return ZERO_OK;
+    case ZERO_OPT_HOST_PIPELINE: *value = p->host_pipeline; return ZERO_OK;
+    case ZERO_OPT_HOST_H2D_BYTES: *value = p->host_h2d_last; return ZERO_OK;
+    case ZERO_OPT_HOST_D2H_BYTES: *value = p->host_d2h_last; return ZERO_OK;
     default: return fail(ZERO_EINVAL, "zero_get_option: unknown option");
     }
 }
@@ -883,73 +1037,9 @@ catch (...) {
 zero_status_t zero_step(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
                         int64_t which, const zero_hyper_t* hyper, void* stream)
 try {
-    if (!hyper) return fail(ZERO_EINVAL, "zero_step: NULL argument");
-    if (p && p->offload) return fail(ZERO_ESTATE, "zero_step: offloaded plan (zero_offload_step)");
-    zero_status_t cst = check_call(p, grad_contribs, n_contribs, which, "zero_step");
-    if (cst != ZERO_OK) return cst;
-    if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
-        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay) ||
-        !(hyper->max_grad_norm >= 0.0) || !std::isfinite(hyper->max_grad_norm))
-        return fail(ZERO_EINVAL, "zero_step: betas must lie in [0, 1); lr, eps, wd, max_grad_norm finite");
-    if (hyper->max_grad_norm > 0.0)
-        for (int64_t b = 0; b < p->n_buckets; ++b)
-            if (!p->norm_covered[(size_t)b])
-                return fail(ZERO_ESTATE, "zero_step: clipping needs zero_grad_norm over every bucket/unit first");
-    if (p->in_step && std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0)
-        return fail(ZERO_EINVAL, "zero_step: hyperparameters changed inside a step");
-    if (which == -1) {
-        if (p->in_step) return fail(ZERO_ESTATE, "zero_step: bucket -1 must be the only call of a step");
-    } else if (p->covered[(size_t)which]) {
-        return fail(ZERO_ESTATE, "zero_step: bucket/unit already stepped in this step");
-    }
-
-    zero_status_t st = set_device(p);
+    const zero_status_t st = check_step(p, grad_contribs, n_contribs, which, hyper, "zero_step");
     if (st != ZERO_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
-    if (!p->in_step) {
-        if (p->bias_len == 0 || p->bias_beta1 != hyper->beta1 || p->bias_beta2 != hyper->beta2) {
-            st = upload_bias_table(p, hyper->beta1, hyper->beta2, s);
-            if (st != ZERO_OK) return st;
-        }
-        // t, the loss scale and the current half are read on the device; the constants that
-        // do not depend on them are rounded here once.
-        step_constants(*hyper, 1, 1.0, p->n_d, p->consts);
-        p->step_hyper = *hyper;
-    }
-    // clip: the norm is complete on the device; report: accumulate it in this pass
-    int mode = kPlain;
-    if (hyper->max_grad_norm > 0.0) mode = kClip;
-    else if ((hyper->flags & ZERO_REPORT_GRAD_NORM) && !p->norm_open) mode = kNormAcc;
-    const std::vector<Segment> segs = step_segments(p, which, 0);
-    const BulkCfg bulk = bulk_config(p);
-    auto run = [&](auto& P, size_t cap) -> cudaError_t {
-        for (size_t b = 0; b < segs.size(); b += cap) {
-            const size_t e = std::min(segs.size(), b + cap);
-            fill_call_params(p, grad_contribs, P);
-            P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
-            const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
-            int used = 0;
-            const cudaError_t err = p->dtype16 == ZERO_BF16
-                                        ? launch_fused<ZERO_BF16>(p->device, P, vec, s, mode, &bulk, &used)
-                                        : launch_fused<ZERO_FP16>(p->device, P, vec, s, mode, &bulk, &used);
-            p->last_step_kernel = used;
-            if (err != cudaSuccess) return err;
-        }
-        return cudaSuccess;
-    };
-    cudaError_t lerr;
-    if (segs.size() > (size_t)kMaxSegs) {
-        StepParamsWide P;
-        lerr = run(P, kWideSegs);
-    } else {
-        StepParams P;
-        lerr = run(P, kMaxSegs);
-    }
-    if (lerr != cudaSuccess) return cuda_fail(lerr, "fused step launch");
-    p->in_step = true;
-    if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
-    else p->covered[(size_t)which] = 1;
-    return ZERO_OK;
+    return enqueue_step(p, grad_contribs, which, hyper, (cudaStream_t)stream);
 }
 catch (...) {
     return exception_status("zero_step");
@@ -958,6 +1048,21 @@ catch (...) {
 zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t* out)
 try {
     if (!p) return fail(ZERO_EINVAL, "zero_step_finish: NULL plan");
+    if (p->host_step)
+        return fail(ZERO_ESTATE, "zero_step_finish: the step has zero_step_host calls (zero_step_host_finish)");
+    return finish_step(p, stream, out);
+}
+catch (...) {
+    return exception_status("zero_step_finish");
+}
+
+}  // extern "C"
+
+namespace zero {
+namespace {
+
+zero_status_t finish_step(zero_plan_t* p, void* stream, zero_step_result_t* out)
+{
     if (!p->in_step) return fail(ZERO_ESTATE, "zero_step_finish: no open step");
     for (int64_t b = 0; b < p->n_buckets; ++b)
         if (!p->covered[(size_t)b])
@@ -1012,9 +1117,11 @@ try {
     if (out) return read_state(p, s, out);
     return ZERO_OK;
 }
-catch (...) {
-    return exception_status("zero_step_finish");
-}
+
+}  // namespace
+}  // namespace zero
+
+extern "C" {
 
 zero_status_t zero_read_state(zero_plan_t* p, void* stream, zero_step_result_t* out)
 try {
@@ -1382,6 +1489,155 @@ catch (...) {
     return exception_status("zero_offload_finish");
 }
 
+zero_status_t zero_bind_host_staging(zero_plan_t* p, void* const staging[2], int64_t bytes_each)
+try {
+    if (!p || !staging || !staging[0] || !staging[1])
+        return fail(ZERO_EINVAL, "zero_bind_host_staging: NULL argument");
+    if (p->in_step) return fail(ZERO_ESTATE, "zero_bind_host_staging: a step is open");
+    if (p->offload) return fail(ZERO_ESTATE, "zero_bind_host_staging: offloaded plan");
+    if (p->device < 0 || !p->workspace)
+        return fail(ZERO_ESTATE, "zero_bind_host_staging: bind the ranks first");
+    zero_plan_info_t info;
+    zero_status_t st = zero_plan_info(p, &info);
+    if (st != ZERO_OK) return st;
+    if (bytes_each < info.host_staging_bytes)
+        return fail(ZERO_ERANGE, "zero_bind_host_staging: an area is smaller than info.host_staging_bytes");
+    if (!aligned(staging[0], 16) || !aligned(staging[1], 16))
+        return fail(ZERO_EALIGN, "zero_bind_host_staging: areas must be 16-byte aligned");
+    const uintptr_t a = (uintptr_t)staging[0], b = (uintptr_t)staging[1];
+    const uintptr_t need = (uintptr_t)info.host_staging_bytes;
+    if (need > 0 && (a < b ? b - a : a - b) < need)
+        return fail(ZERO_EINVAL, "zero_bind_host_staging: the two areas overlap");
+    for (int i = 0; i < 2; ++i) {
+        cudaPointerAttributes at;
+        const cudaError_t e = cudaPointerGetAttributes(&at, staging[i]);
+        if (e != cudaSuccess || (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) ||
+            at.device != p->device) {
+            (void)cudaGetLastError();
+            return fail(ZERO_EINVAL, "zero_bind_host_staging: areas must be device memory of the plan's device");
+        }
+    }
+    p->host_staging[0] = staging[0];
+    p->host_staging[1] = staging[1];
+    p->host_rank_stride = (info.max_contrib_elems + 7) / 8 * 8;
+    return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_bind_host_staging");
+}
+
+zero_status_t zero_step_host(zero_plan_t* p, const void* const* host_contribs, int64_t n_contribs,
+                             int64_t which, const zero_hyper_t* hyper, void* host_out16, void* stream)
+try {
+    zero_status_t st = check_step(p, host_contribs, n_contribs, which, hyper, "zero_step_host");
+    if (st != ZERO_OK) return st;
+    if (!p->host_staging[0]) return fail(ZERO_ESTATE, "zero_step_host: no staging bound (zero_bind_host_staging)");
+    if (hyper->max_grad_norm != 0.0) return fail(ZERO_EINVAL, "zero_step_host: no clipping on this path");
+    if (!host_out16) return fail(ZERO_EINVAL, "zero_step_host: NULL host_out16");
+    if (!aligned(host_out16, 2)) return fail(ZERO_EALIGN, "zero_step_host: host_out16 not 2-byte aligned");
+    const std::vector<Segment> segs = step_segments(p, which, 0);
+    const auto runs = read_runs(segs);
+    if (!segs.empty()) {
+        if (!pinned_host(host_out16)) return fail(ZERO_EINVAL, "zero_step_host: host_out16 is not pinned host memory");
+        for (int r = 0; r < p->n_d; ++r)
+            if (!pinned_host(host_contribs[r]))
+                return fail(ZERO_EINVAL, "zero_step_host: a contribution is not pinned host memory");
+    }
+    st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaError_t e = host_resources(p);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: copy streams");
+    cudaStream_t s = (cudaStream_t)stream, h2d = (cudaStream_t)p->host_h2d, d2h = (cudaStream_t)p->host_d2h;
+    const int b = (int)(p->host_calls % 2);
+    cudaEvent_t copied = (cudaEvent_t)p->host_events[b], used = (cudaEvent_t)p->host_events[2 + b];
+    cudaEvent_t out_done = (cudaEvent_t)p->host_events[4];
+    // host -> device: after the step that last read this area (pipelined), or after everything
+    // the previous call did, its device -> host copies included (serial)
+    e = cudaStreamWaitEvent(h2d, p->host_pipeline ? used : out_done, 0);
+    std::vector<const void*> dev(p->n_d);
+    int64_t h2d_bytes = 0;
+    for (int r = 0; r < p->n_d && e == cudaSuccess; ++r) {
+        uint16_t* area = (uint16_t*)p->host_staging[b] + (int64_t)r * p->host_rank_stride;
+        dev[(size_t)r] = area;
+        for (const auto& run : runs) {
+            const size_t bytes = 2 * (size_t)(run.second - run.first);
+            e = cudaMemcpyAsync(area + run.first, (const uint16_t*)host_contribs[r] + run.first, bytes,
+                                cudaMemcpyHostToDevice, h2d);
+            if (e != cudaSuccess) break;
+            h2d_bytes += (int64_t)bytes;
+        }
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(copied, h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: host-to-device copies");
+    st = enqueue_step(p, dev.data(), which, hyper, s);
+    if (st != ZERO_OK) return st;
+    // device -> host: the 16-bit results of the call, merged where both sides are contiguous
+    e = cudaEventRecord(used, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d2h, used, 0);
+    std::vector<zero_plan::HostCopy> outs;
+    for (const Segment& sg : segs) {
+        if (sg.n <= 0) continue;
+        uint16_t* h = (uint16_t*)host_out16 + sg.c_off;
+        const uint16_t* d = sg.out16 + sg.o_off;
+        if (!outs.empty() && outs.back().host + outs.back().n == h && outs.back().dev + outs.back().n == d)
+            outs.back().n += sg.n;
+        else
+            outs.push_back({h, d, sg.n});
+    }
+    int64_t d2h_bytes = 0;
+    for (size_t i = 0; i < outs.size() && e == cudaSuccess; ++i) {
+        e = cudaMemcpyAsync(outs[i].host, outs[i].dev, 2 * (size_t)outs[i].n, cudaMemcpyDeviceToHost, d2h);
+        d2h_bytes += 2 * outs[i].n;
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(out_done, d2h);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: device-to-host copies");
+    p->host_outs.insert(p->host_outs.end(), outs.begin(), outs.end());
+    p->host_h2d_bytes += h2d_bytes;
+    p->host_d2h_bytes += d2h_bytes;
+    p->host_step = true;
+    ++p->host_calls;
+    return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_step_host");
+}
+
+zero_status_t zero_step_host_finish(zero_plan_t* p, void* stream, zero_step_result_t* out)
+try {
+    if (!p) return fail(ZERO_EINVAL, "zero_step_host_finish: NULL plan");
+    if (!p->host_step) return fail(ZERO_ESTATE, "zero_step_host_finish: no zero_step_host call in the open step");
+    zero_status_t st = set_device(p);
+    if (st != ZERO_OK) return st;
+    zero_step_result_t res;
+    st = finish_step(p, stream, &res);                 // synchronises `stream`
+    if (st == ZERO_ESTATE || st == ZERO_EINVAL) return st;   // nothing was enqueued
+    const std::string finish_msg = st != ZERO_OK ? zero_last_error() : "";
+    cudaStream_t d2h = (cudaStream_t)p->host_d2h;
+    cudaError_t e = cudaStreamSynchronize(d2h);
+    // a skipped or discarded step re-cast its 16-bit parameters after they were copied
+    if (e == cudaSuccess && (st == ZERO_ETIMEOUT || (st == ZERO_OK && res.skipped))) {
+        for (const zero_plan::HostCopy& c : p->host_outs) {
+            e = cudaMemcpyAsync(c.host, c.dev, 2 * (size_t)c.n, cudaMemcpyDeviceToHost, d2h);
+            if (e != cudaSuccess) break;
+            p->host_d2h_bytes += 2 * c.n;
+        }
+        if (e == cudaSuccess) e = cudaStreamSynchronize(d2h);
+    }
+    p->host_h2d_last = p->host_h2d_bytes;
+    p->host_d2h_last = p->host_d2h_bytes;
+    p->host_h2d_bytes = p->host_d2h_bytes = 0;
+    p->host_outs.clear();
+    p->host_step = false;
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_host_finish: device-to-host copies");
+    if (out) *out = res;
+    if (st != ZERO_OK) return fail(st, finish_msg);
+    return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_step_host_finish");
+}
+
 zero_status_t zero_step_units_overlapped(zero_plan_t* p, const void* const* unit_contribs,
                                          int64_t n_ptrs, void* const* gather_bufs,
                                          const zero_hyper_t* hyper, void* compute_stream,
@@ -1459,10 +1715,44 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
+struct NoallocAddr {
+    unsigned long long ctx = 0;   // unique ID of the CUDA context the address belongs to
+    void* addr = nullptr;
+};
+NoallocAddr g_noalloc_addr[kMaxDevices];
 
-// Device address of g_noalloc_scratch on the current device (looked up once per device).
-// In host code the array's name is only a host-side handle, never a device address.
+// Unique ID of the calling thread's current CUDA context (0 when none is current or the
+// driver cannot say).  Context IDs are never reused within a process, so a device reset,
+// which replaces the primary context and reloads the module, changes the ID.
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static bool resolved = false;
+    if (!resolved) {            // under g_noalloc_mu
+        cudaDriverEntryPointQueryResult q1, q2;
+        void *f1 = nullptr, *f2 = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+            get_current = (GetCurrent)f1;
+            get_id = (GetId)f2;
+        }
+        (void)cudaGetLastError();
+        resolved = true;
+    }
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch for the current device.  In host code the array's name
+// is only a host-side handle, never a device address.  The address is looked up with the
+// device current the first time a device (in a given CUDA context) is used, and cached.
 zero_status_t noalloc_scratch(void** out)
 {
     int dev = -1;
@@ -1471,14 +1761,17 @@ zero_status_t noalloc_scratch(void** out)
     if (dev < 0 || dev >= kMaxDevices)
         return fail(ZERO_ERANGE, "zero_step_range_noalloc: device index beyond the supported range");
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    NoallocAddr& c = g_noalloc_addr[dev];
+    const unsigned long long ctx = current_context_id();
+    if (!c.addr || ctx == 0 || c.ctx != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // makes the context current
         if (e != cudaSuccess || !p)
             return cuda_fail(e, "zero_step_range_noalloc: cudaGetSymbolAddress of the scratch");
-        g_noalloc_addr[dev] = p;
+        c.addr = p;
+        c.ctx = current_context_id();
     }
-    *out = g_noalloc_addr[dev];
+    *out = c.addr;
     return ZERO_OK;
 }
 

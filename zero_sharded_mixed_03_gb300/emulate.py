@@ -18,7 +18,8 @@ from . import (ZERO_BF16, zero_set_option, ZERO_TABLE_PARAM_CHUNKS, ZERO_TABLE_S
                zero_gather_layer, zero_plan_create, zero_plan_destroy, zero_plan_info,
                zero_grad_norm, zero_plan_tables, zero_rank_state_elems, zero_read_state,
                zero_release_layer,
-               zero_set_scaler, zero_step, zero_step_finish)
+               zero_set_scaler, zero_step, zero_step_finish,
+               zero_bind_host_staging, zero_step_host, zero_step_host_finish)
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
@@ -159,6 +160,23 @@ class EmulatedGroup:
             zero_offload_step(self.plan, list(contribs), which, hyper, _stream_handle(stream))
             return
         zero_step(self.plan, list(contribs), which, hyper, _stream_handle(stream))
+
+    def bind_host_staging(self) -> None:
+        """Allocate and bind the two device staging areas of the host-buffer path."""
+        n = int(self.info.host_staging_bytes)
+        self.host_staging = [torch.empty(max(16, n), dtype=torch.uint8, device=self.device)
+                             for _ in range(2)]
+        zero_bind_host_staging(self.plan, [t.data_ptr() for t in self.host_staging], max(16, n))
+
+    def step_host(self, host_contribs: Sequence[int], which: int, hyper, host_out16: int,
+                  stream=None) -> None:
+        """zero_step with the contributions and the 16-bit result in pinned host memory."""
+        zero_step_host(self.plan, list(host_contribs), which, hyper, host_out16,
+                       _stream_handle(stream))
+
+    def finish_host(self, stream=None):
+        """End a step with host-buffer calls (synchronises); returns the step state."""
+        return zero_step_host_finish(self.plan, _stream_handle(stream))
 
     def grad_norm(self, contribs: Sequence[int], which: int, stream=None) -> None:
         """Gradient-norm pre-pass of one bucket/unit (needed before a clipping step)."""
