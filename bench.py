@@ -685,12 +685,16 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
         outs.append(host_out.data_ptr() + 2 * (o - rel))
     torch.cuda.synchronize()
 
+    enqueue_s = [0.0]
+
     def one_step():
+        t = time.perf_counter()
         for ci, (which, lo, hi) in enumerate(b.calls):
             if w.stage == 3:
                 g.gather(which, b.run.gather_buf)
                 g.release(which)
             g.step_host([t.data_ptr() for t in host_sets[ci % 2]], which, b.hyper, outs[ci])
+        enqueue_s[0] += time.perf_counter() - t
         return g.finish_host()             # waits for every copy; reads the step state back
 
     def timed(n):
@@ -707,7 +711,9 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
         return el, applied
 
     one_step()                                            # warm-up (creates the copy streams)
+    enqueue_s[0] = 0.0
     el, applied = timed(steps)
+    enqueue_ms = 1e3 * enqueue_s[0] / steps
     h2d = Z.zero_get_option(g.plan, Z.ZERO_OPT_HOST_H2D_BYTES)
     d2h = Z.zero_get_option(g.plan, Z.ZERO_OPT_HOST_D2H_BYTES)
     g.set_option(Z.ZERO_OPT_HOST_PIPELINE, 0)
@@ -723,6 +729,7 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h) + 96,
             "steps": steps, "api": "zero_step_host / zero_step_host_finish",
             "host_link_gbs": round((h2d + d2h) / (ms / 1e3) / 1e9, 1),
+            "host_enqueue_ms_per_step": round(enqueue_ms, 3),
             "overlap": {"pipelined_ms_per_step": round(ms, 3),
                         "serial_ms_per_step": round(ms_serial, 3),
                         "hidden_ms_per_step": round(hidden_ms, 3),

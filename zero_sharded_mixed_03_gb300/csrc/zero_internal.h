@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <functional>
 #include <string>
+#include <unordered_set>
 #include <vector>
 
 #include "../../include/zero.h"
@@ -188,6 +189,9 @@ struct zero_plan {
     bool host_step = false;
     int host_pipeline = 1;
     std::vector<HostCopy> host_outs;
+    // host pointers already found to be pinned (cudaPointerGetAttributes costs a driver call;
+    // training loops pass the same buffers every step)
+    std::unordered_set<const void*> host_pinned;
     int64_t host_h2d_bytes = 0, host_d2h_bytes = 0;             // the open step
     int64_t host_h2d_last = 0, host_d2h_last = 0;               // the last finished host step
     void (*release_hook)(zero_plan*) = nullptr;

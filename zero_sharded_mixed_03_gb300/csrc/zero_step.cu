@@ -755,6 +755,18 @@ bool pinned_host(const void* q)
     return at.type == cudaMemoryTypeHost;
 }
 
+// pinned_host with the plan's cache of pointers already checked (bounded: cleared when full).
+// A stale entry (a pinned buffer freed and the address reused by pageable memory) would only
+// make that call's copies synchronous with the host; the data copied is the same.
+bool pinned_host_cached(zero_plan* p, const void* q)
+{
+    if (p->host_pinned.count(q)) return true;
+    if (!pinned_host(q)) return false;
+    if (p->host_pinned.size() >= 4096) p->host_pinned.clear();
+    p->host_pinned.insert(q);
+    return true;
+}
+
 // [lo, hi) element ranges of a call's range that its work items read from every contribution,
 // merged where they touch or overlap.
 std::vector<std::pair<int64_t, int64_t>> read_runs(const std::vector<Segment>& segs)
@@ -1538,9 +1550,10 @@ try {
     const std::vector<Segment> segs = step_segments(p, which, 0);
     const auto runs = read_runs(segs);
     if (!segs.empty()) {
-        if (!pinned_host(host_out16)) return fail(ZERO_EINVAL, "zero_step_host: host_out16 is not pinned host memory");
+        if (!pinned_host_cached(p, host_out16))
+            return fail(ZERO_EINVAL, "zero_step_host: host_out16 is not pinned host memory");
         for (int r = 0; r < p->n_d; ++r)
-            if (!pinned_host(host_contribs[r]))
+            if (!pinned_host_cached(p, host_contribs[r]))
                 return fail(ZERO_EINVAL, "zero_step_host: a contribution is not pinned host memory");
     }
     st = set_device(p);
