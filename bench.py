@@ -91,6 +91,10 @@ def parse_args():
     ap.add_argument("--overlap", action="store_true",
                     help="stage 3: gather unit u+1 on a second stream while unit u steps "
                          "(zero_step_units_overlapped); no per-launch events in this mode")
+    ap.add_argument("--schedule", choices=["fused", "serial"], default="fused",
+                    help="stage 3: fused (default): unit u's step launch also gathers unit u+1 "
+                         "(zero_step_gather_next; unit 0 is gathered on its own); serial: every "
+                         "unit's gather as a launch of its own before its step")
     ap.add_argument("--staging", choices=["auto", "ldg", "bulk"], default=DEFAULT_STAGING,
                     help="bulk: cp.async.bulk (TMA) staging of the contribution and state tiles "
                          "into shared memory; ldg: 128-bit register loads; auto (default): the "
@@ -262,7 +266,7 @@ class Bench:
     """A workload bound to the product API with pre-generated contribution sets."""
 
     def __init__(self, w, mem_budget_gb: float, n_sets_wanted: int, grad_norm: str = "off",
-                 options=None):
+                 options=None, fused_gather: bool = False):
         import torch
         import synth
         import zero_sharded_mixed_03_gb300 as Z
@@ -271,6 +275,8 @@ class Bench:
 
         self.torch, self.Z, self.synth = torch, Z, synth
         self.w = w
+        self.fused_gather = fused_gather and w.stage == 3
+        self.gather_in_step = None            # learnt from the library on the first step
         # plan, state, 16-bit buffers, initial params
         self.run = Run(w, alloc_contribs=False, options=options)
         self.g = self.run.g
@@ -389,15 +395,55 @@ class Bench:
 
     def step_overlapped(self, bufs, comm, wait=False):
         """Whole stage-3 step through zero_step_units_overlapped; returns (result, launches)."""
-        if not hasattr(self, "_gbufs"):
-            n = max(8, int(self.info.max_unit_pad))
-            self._gbufs = [self.torch.empty(n, dtype=self.torch.int16, device="cuda") for _ in range(2)]
+        gb = self.gather_bufs()
         ptrs = [p for ci in range(len(self.calls)) for p in self.call_ptrs(bufs, ci)]
         res = self.Z.zero_step_units_overlapped(
-            self.g.plan, ptrs, [b.data_ptr() for b in self._gbufs], self.hyper,
+            self.g.plan, ptrs, [b.data_ptr() for b in gb], self.hyper,
             self.torch.cuda.current_stream().cuda_stream, comm.cuda_stream, wait)
         launches = ((1 + self.clip) * sum(self.fused_launches) + sum(self.gather_launches)
                     + self.recast_launches + (0 if self.recast_launches else 1))
+        return res, launches
+
+    def gather_bufs(self):
+        if not hasattr(self, "_gbufs"):
+            n = max(8, int(self.info.max_unit_pad))
+            self._gbufs = [self.torch.empty(n, dtype=self.torch.int16, device="cuda") for _ in range(2)]
+        return self._gbufs
+
+    def step_fused(self, bufs, events=None, gather_events=None, wait=False):
+        """One stage-3 step in which unit u's step launch also gathers unit u+1
+        (zero_step_gather_next); unit 0 is gathered by a launch of its own.  Events as in step();
+        the gather pairs then time only unit 0's gather.  Returns (result, launches)."""
+        gb = self.gather_bufs()
+        launches = 0
+        n = len(self.calls)
+        if gather_events is not None:
+            a, c = next(gather_events)
+            a.record()
+        self.g.gather(self.calls[0][0], gb[0])
+        if gather_events is not None:
+            c.record()
+        launches += self.gather_launches[0]
+        for ci, (which, lo, hi) in enumerate(self.calls):
+            self.g.release(which)
+            if events is not None:
+                a, c = next(events)
+                a.record()
+            if ci + 1 < n:
+                self.g.step_gather_next(self.call_ptrs(bufs, ci), which, self.hyper,
+                                        self.calls[ci + 1][0], gb[(ci + 1) % 2])
+                if self.gather_in_step is None:
+                    self.gather_in_step = self.Z.zero_get_option(
+                        self.g.plan, self.Z.ZERO_OPT_LAST_GATHER_IN_STEP) == 1
+                if not self.gather_in_step:
+                    launches += self.gather_launches[ci + 1]
+            else:
+                self.g.step(self.call_ptrs(bufs, ci), which, self.hyper)
+            if events is not None:
+                c.record()
+            launches += self.fused_launches[ci]
+        res = self.g.finish(wait=wait)
+        launches += self.recast_launches + (0 if self.recast_launches else 1)
         return res, launches
 
     def step(self, bufs, events=None, gather_events=None, wait=False):
@@ -406,6 +452,8 @@ class Bench:
         events / gather_events: iterators of pre-created (start, end) CUDA event pairs recorded
         around each fused launch / gather launch.  Returns (result or None, kernel launches).
         """
+        if self.fused_gather and not self.clip:
+            return self.step_fused(bufs, events, gather_events, wait)
         launches = 0
         if self.clip:
             for ci, (which, lo, hi) in enumerate(self.calls):
@@ -443,7 +491,8 @@ def measure(b, args, torch, overlap, comm, use_graph, dist, pairs, sample_clocks
     w = b.w
     n_calls = args.steps * len(b.calls)
     fused_pairs = pairs(n_calls, use_graph) if not overlap else []
-    gather_pairs = pairs(n_calls, use_graph) if (w.stage == 3 and not overlap) else []
+    n_gathers = args.steps if b.fused_gather and not b.clip else n_calls
+    gather_pairs = pairs(n_gathers, use_graph) if (w.stage == 3 and not overlap) else []
     ev_fused, ev_gather = iter(fused_pairs), iter(gather_pairs)
     launches = 0
 
@@ -517,7 +566,7 @@ def gpu_arm(args, world, rank, local):
         options[Z.ZERO_OPT_GATHER_STAGING] = {"ldg": Z.ZERO_STAGING_REGISTER_LOADS,
                                              "bulk": Z.ZERO_STAGING_BULK}[args.gather_staging]
     b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm,
-              options)
+              options, fused_gather=args.schedule == "fused" and not args.overlap)
     peak, peak_kind = peaks()
 
     for k in range(args.warmup):
@@ -561,7 +610,9 @@ def gpu_arm(args, world, rank, local):
     if overlap:
         # the same steps with every unit's gather followed by its step on one stream: what the
         # second stream hides is the difference
+        fg, b.fused_gather = b.fused_gather, False
         ser = measure(b, args, torch, False, None, use_graph, dist, pairs)
+        b.fused_gather = fg
         g_ms = sum(ser["gather_ms"]) / args.steps
         hidden = ser["ms"] / args.steps - ms / args.steps
         frac = max(0.0, min(1.0, hidden / g_ms)) if g_ms > 0 else 0.0
@@ -582,8 +633,14 @@ def gpu_arm(args, world, rank, local):
     gather_bytes = 4 * int(b.info.phi_pad) if w.stage == 3 else 0
     hbm_gbs = (step_bytes + gather_bytes) * args.steps / (ms / 1e3) / 1e9
     # dominant kernel: the fused step; algorithmic bytes per launch = elements x (2 N_d + 26)
+    # (+ 4 bytes per element of the unit a launch also gathers, in the fused schedule)
     per_launch_elems = elems / max(1, len(b.calls))
     launch_bytes = per_launch_elems * b.bytes_per_elem
+    fused_sched = b.fused_gather and not b.clip and not overlap
+    in_step_gather_bytes = 0
+    if fused_sched and b.gather_in_step:
+        in_step_gather_bytes = 4 * sum(b.units[c[0]][3] for c in b.calls[1:])
+        launch_bytes = (elems * b.bytes_per_elem + in_step_gather_bytes) / max(1, len(b.calls))
     avg_fused_s = statistics.mean(fused_ms) / 1e3 if fused_ms else float("nan")
     achieved = launch_bytes / avg_fused_s / 1e9
     # the step kernel the library launched (the staging option, the residency rule of the
@@ -591,7 +648,8 @@ def gpu_arm(args, world, rank, local):
     last = Z.zero_get_option(b.g.plan, Z.ZERO_OPT_LAST_STEP_KERNEL)
     kernel = "bulk_step_kernel" if last == 1 else "fused_step_kernel"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config, kernel),
+                "frac": round(achieved / peak, 4),
+                "traffic": measured_traffic(args.config, kernel + (" + gather" if fused_sched and b.gather_in_step else "")),
                 "kernel_source_sha256": kernel_source_hash(),
                 "peak_source": peak_kind, "kernel": kernel,
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
@@ -614,11 +672,23 @@ def gpu_arm(args, world, rank, local):
                     "peak_source": f"measured here: torch CPU copy on {b.g.offload_threads} threads",
                     "kernel": "host AdamW (zero_offload_finish)"}
     if gather_ms and roofline is not None:
-        g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
-        roofline["gather_achieved_gbs"] = round(g_bytes / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
         gstaging = Z.zero_get_option(b.g.plan, Z.ZERO_OPT_GATHER_STAGING)
-        roofline["gather_kernel"] = ("gather_kernel" if gstaging == Z.ZERO_STAGING_REGISTER_LOADS
-                                     else "bulk_gather_kernel")
+        standalone = ("gather_kernel" if gstaging == Z.ZERO_STAGING_REGISTER_LOADS
+                      else "bulk_gather_kernel")
+        if fused_sched and b.gather_in_step:
+            # the gathers of units 1.. stream inside the step launches: their bytes move at the
+            # launch's combined rate; unit 0's gather is a launch of its own
+            roofline["kernel"] = "bulk_step_kernel + next unit's gather (zero_step_gather_next)"
+            roofline["gather_in_step_launch"] = True
+            roofline["gather_achieved_gbs"] = roofline["achieved"]
+            roofline["in_step_gather_bytes_per_step"] = in_step_gather_bytes
+            g0 = 4 * b.units[b.calls[0][0]][3]
+            roofline["unit0_gather_gbs"] = round(g0 / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
+            roofline["unit0_gather_kernel"] = standalone
+        else:
+            g_bytes = 4 * int(b.info.phi_pad) / len(b.calls)
+            roofline["gather_achieved_gbs"] = round(g_bytes / (statistics.mean(gather_ms) / 1e3) / 1e9, 1)
+            roofline["gather_kernel"] = standalone
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
@@ -631,6 +701,7 @@ def gpu_arm(args, world, rank, local):
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
                       "overlap": overlap, "graph": m["graph"], "per_param": w.per_param,
+                      "schedule": ("overlap" if overlap else args.schedule) if w.stage == 3 else None,
                       "offload": w.offload, "staging": args.staging,
                       "profile_unit": args.profile_unit,
                       "offload_threads": b.g.offload_threads if w.offload else None},

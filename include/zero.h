@@ -339,9 +339,12 @@ enum {
                                        what the overlap hides) */
     ZERO_OPT_HOST_H2D_BYTES = 9,    /* read only: bytes zero_step_host copied host->device in
                                        the last step finished by zero_step_host_finish */
-    ZERO_OPT_HOST_D2H_BYTES = 10    /* read only: bytes copied device->host in that step (the
+    ZERO_OPT_HOST_D2H_BYTES = 10,   /* read only: bytes copied device->host in that step (the
                                        updated 16-bit parameters, re-copies after a skip
                                        included) */
+    ZERO_OPT_LAST_GATHER_IN_STEP = 11 /* read only: 1 if the last zero_step_gather_next streamed
+                                       its gather inside the step launch, 0 if the gather ran
+                                       as a launch of its own, -1 none yet */
 };
 enum { ZERO_STAGING_REGISTER_LOADS = 0, ZERO_STAGING_BULK = 1, ZERO_STAGING_AUTO = 2 };
 zero_status_t zero_set_option(zero_plan_t* plan, int option, int64_t value);
@@ -362,15 +365,32 @@ zero_status_t zero_restore_state(zero_plan_t* plan, const zero_step_result_t* in
  * runs out leaves the unit incomplete and sets the plan's error word (see zero_read_state). */
 zero_status_t zero_gather_layer(zero_plan_t* plan, int64_t unit, void* full_unit16, void* stream);
 
+/* zero_step of stage-3 unit `unit` and zero_gather_layer of unit `next_unit` into next_full16
+ * (max_unit_pad elements suffice) in one launch where possible ("Overlapping Computation and
+ * Communication Streams": the next unit's all-gather runs while this unit is reduced and
+ * updated; "ZeRO-3 / FSDP Layer Execution Lifecycle").  When the bulk-staged step kernel runs
+ * the unit and the gather's copy list fits its parameter block (32 copies, or 256 when the
+ * call has more than 32 work items), each block's producer warp streams gather chunks through
+ * its shared-memory ring after its last tile; otherwise the gather follows as its own launch
+ * on `stream` (ZERO_OPT_LAST_GATHER_IN_STEP tells which).  Results are those of the two calls
+ * made one after the other.  next_unit must differ from unit (the step writes unit's shards)
+ * and next_full16 must not overlap any buffer of the plan.  The errors of zero_step and of
+ * zero_gather_layer; next_unit stays gathered until zero_release_layer. */
+zero_status_t zero_step_gather_next(zero_plan_t* plan, const void* const* grad_contribs,
+                                    int64_t n_contribs, int64_t unit, const zero_hyper_t* hyper,
+                                    int64_t next_unit, void* next_full16, void* stream);
+
 /* A whole stage-3 step with the all-gather overlapped ("Overlapping Computation and
  * Communication Streams"): for every unit u in order, `comm_stream` gathers u into
  * gather_bufs[u % 2] (each max_unit_pad elements) while `compute_stream` runs the fused step
  * of unit u-1; unit u's step waits only for its own gather (the point where a layer's
  * backward would consume W_u), and a buffer is re-filled only after the step that followed
- * its gather has been enqueued past it.  Ends with zero_step_finish on `compute_stream`
- * (out as there).  unit_contribs: n_units * N_d pointers, unit-major (unit u's N_d
- * contributions at [u * N_d]).  With max_grad_norm > 0 a norm pre-pass over every unit runs
- * first on compute_stream.  Stage 3 only; the two streams must differ. */
+ * its gather has been enqueued past it.  comm_stream == NULL: one stream; unit 0 is gathered
+ * on its own, then unit u's step and unit u+1's gather run as zero_step_gather_next (one
+ * launch each where possible).  Ends with zero_step_finish on `compute_stream` (out as
+ * there).  unit_contribs: n_units * N_d pointers, unit-major (unit u's N_d contributions at
+ * [u * N_d]).  With max_grad_norm > 0 a norm pre-pass over every unit runs first on
+ * compute_stream.  Stage 3 only; two given streams must differ. */
 zero_status_t zero_step_units_overlapped(zero_plan_t* plan, const void* const* unit_contribs,
                                          int64_t n_ptrs, void* const* gather_bufs,
                                          const zero_hyper_t* hyper, void* compute_stream,

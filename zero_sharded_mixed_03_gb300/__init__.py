@@ -22,7 +22,7 @@ ZERO_REPORT_GRAD_NORM = 1
 (ZERO_OPT_STAGING, ZERO_OPT_WAIT_LIMIT_NS, ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES,
  ZERO_OPT_LAST_STEP_KERNEL, ZERO_OPT_GATHER_STAGING, ZERO_OPT_GATHER_CHUNK,
  ZERO_OPT_GATHER_STAGES, ZERO_OPT_HOST_PIPELINE, ZERO_OPT_HOST_H2D_BYTES,
- ZERO_OPT_HOST_D2H_BYTES) = range(11)
+ ZERO_OPT_HOST_D2H_BYTES, ZERO_OPT_LAST_GATHER_IN_STEP) = range(12)
 ZERO_STAGING_REGISTER_LOADS, ZERO_STAGING_BULK, ZERO_STAGING_AUTO = range(3)
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)
@@ -37,6 +37,7 @@ EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", 
             "zero_step_units_overlapped", "zero_bind_offload", "zero_offload_step",
             "zero_offload_finish", "zero_set_option", "zero_get_option",
             "zero_bind_host_staging", "zero_step_host", "zero_step_host_finish",
+            "zero_step_gather_next",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
 
@@ -140,6 +141,9 @@ def lib() -> ctypes.CDLL:
         L.zero_offload_step.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t), _vp]
         L.zero_offload_finish.restype = st
         L.zero_offload_finish.argtypes = [_vp, _int, _vp, ctypes.POINTER(zero_step_result_t)]
+        L.zero_step_gather_next.restype = st
+        L.zero_step_gather_next.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t), _i64,
+                                            _vp, _vp]
         L.zero_bind_host_staging.restype = st
         L.zero_bind_host_staging.argtypes = [_vp, _vp, _i64]
         L.zero_step_host.restype = st
@@ -263,14 +267,22 @@ def zero_step(plan: int, grad_contribs: Sequence[int], which: int, hyper: zero_h
                            ctypes.byref(hyper), stream or None))
 
 
+def zero_step_gather_next(plan: int, grad_contribs: Sequence[int], unit: int, hyper: zero_hyper_t,
+                          next_unit: int, next_full16: int, stream: int = 0) -> None:
+    _check(lib().zero_step_gather_next(plan, _ptr_array(grad_contribs), len(grad_contribs), unit,
+                                       ctypes.byref(hyper), next_unit, next_full16 or None,
+                                       stream or None))
+
+
 def zero_grad_norm(plan: int, grad_contribs: Sequence[int], which: int, stream: int = 0) -> None:
     _check(lib().zero_grad_norm(plan, _ptr_array(grad_contribs), len(grad_contribs), which,
                                 stream or None))
 
 
 def zero_step_units_overlapped(plan: int, unit_contribs: Sequence[int], gather_bufs: Sequence[int],
-                               hyper: zero_hyper_t, compute_stream: int, comm_stream: int,
+                               hyper: zero_hyper_t, compute_stream: int, comm_stream: Optional[int],
                                wait: bool = True) -> Optional[zero_step_result_t]:
+    """comm_stream None / 0: the one-stream schedule (unit u+1's gather inside unit u's step)."""
     res = zero_step_result_t() if wait else None
     _check(lib().zero_step_units_overlapped(plan, _ptr_array(unit_contribs), len(unit_contribs),
                                             _ptr_array(gather_bufs), ctypes.byref(hyper),

@@ -155,6 +155,8 @@ struct zero_plan {
     int64_t bulk_tile = 0;              // elements per staged tile (0: chosen from N_d)
     int bulk_stages = 0;                // ring depth (0: chosen from the tile)
     int last_step_kernel = -1;          // last zero_step launch: 1 staged, 0 register loads
+    int last_gather_in_step = -1;       // last zero_step_gather_next: 1 gather inside the step
+                                        // launch, 0 launched on its own
     int gather_staging = ZERO_STAGING_AUTO;   // zero_gather_layer's kernel
     int gather_chunk = 0;               // elements per bulk copy of the staged gather (0: default)
     int gather_stages = 0;              // its ring entries (0: default)

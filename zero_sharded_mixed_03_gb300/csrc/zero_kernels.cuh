@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "zero_internal.h"
 
@@ -127,6 +128,43 @@ struct StepParamsT {
 // limit) for calls with many work items, e.g. per-parameter plans (one item per tensor chunk).
 using StepParams = StepParamsT<kMaxSegs>;
 using StepParamsWide = StepParamsT<kWideSegs>;
+
+// One copy of a stage-3 all-gather streamed inside a step launch ("Overlapping Computation
+// and Communication Streams": the next unit's all-gather runs while this unit is reduced and
+// updated).  Compact, so that the wide block stays under the 32 KB kernel-parameter limit:
+// the destination is g_dst + dst_off; source and destination share one 16-byte phase, and
+// the unaligned head and tail are derived from the destination's address.
+struct GCopy {
+    const uint16_t* src;
+    uint32_t dst_off;   // element offset of the copy in the gather destination
+    uint32_t n;         // elements
+    uint32_t cbeg;      // first chunk of this copy among the launch's gather chunks
+    uint32_t pad;
+};
+
+template <int MS, int MG>
+struct StepGatherParamsT : StepParamsT<MS> {
+    GCopy gc[MG];
+    uint16_t* g_dst;    // the gathered unit's full buffer
+    int32_t g_n;        // copies
+    int32_t g_chunk;    // elements per chunk (a multiple of 8, at most one ring buffer)
+    int64_t g_chunks;   // chunks over the vector bodies of all copies
+};
+using StepGatherParams = StepGatherParamsT<kMaxSegs, kMaxSegs>;
+using StepGatherParamsWide = StepGatherParamsT<kWideSegs, kWideSegs>;
+static_assert(sizeof(StepGatherParamsWide) <= 32764, "kernel parameter limit");
+
+template <typename PT>
+struct HasGather : std::false_type {};
+template <int MS, int MG>
+struct HasGather<StepGatherParamsT<MS, MG>> : std::true_type {};
+
+// Elements before the first 16-byte boundary of a 16-bit stream starting at p (at most n).
+__device__ __forceinline__ int64_t head_elems(const void* p, int64_t n)
+{
+    const int64_t h = (int64_t)(((16u - ((uint32_t)(uintptr_t)p & 15u)) & 15u) >> 1);
+    return h < n ? h : n;
+}
 
 struct CopySeg {
     const uint16_t* src;
@@ -574,6 +612,27 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// 1-D bulk copy shared -> global of `bytes` (16-byte aligned addresses, a multiple of 16
+// bytes), tracked as part of this thread's current bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 ::"l"(dst), "r"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until every bulk group of this thread has completed (its writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Launch tile `tile` (tiles increase along a thread's loop): segment s, first body element
 // e0 and length (a multiple of 8).  s and base (first tile of segment s) carry the walk.
 struct TileRef {
@@ -597,6 +656,36 @@ __device__ __forceinline__ TileRef locate_tile(const PT& P, int64_t tile, int& s
     r.len = (int32_t)min((int64_t)P.tile, 8 * S.nvec - off);
     return r;
 }
+
+// Walk over the gather chunks of a step launch in increasing order (chunk ids c, c + grid,
+// ...): the copy holding the current chunk and its chunk range (from the host's first-chunk
+// table) are carried along.  Returns the chunk's first body element and length; *src / *dst
+// are the copy's streams.
+template <typename PT>
+struct GChunkWalk {
+    int s = -1;
+    int64_t first = 0, end = 0;
+
+    __device__ __forceinline__ TileRef at(const PT& P, int64_t c, const uint16_t** src, uint16_t** dst)
+    {
+        while (c >= end) {
+            ++s;
+            first = end;
+            end = s + 1 < P.g_n ? (int64_t)P.gc[s + 1].cbeg : P.g_chunks;
+        }
+        const GCopy& C = P.gc[s];
+        uint16_t* d = P.g_dst + C.dst_off;
+        const int64_t head = head_elems(d, C.n);
+        const int64_t body = ((int64_t)C.n - head) / 8 * 8;
+        const int64_t off = (c - first) * P.g_chunk;
+        TileRef r;
+        r.e0 = head + off;
+        r.len = (int32_t)min((int64_t)P.g_chunk, body - off);
+        *src = C.src;
+        *dst = d;
+        return r;
+    }
+};
 
 // Four consecutive elements e .. e+3 (quad q of the tile in buffer `buf`).
 template <int DT, int MODE, typename PT>
@@ -645,6 +734,13 @@ __device__ __forceinline__ bool step_quad_staged(const PT& P, const KSeg& S, con
 // Dynamic shared memory (from a 128-byte boundary): kBulkBarrierBytes of mbarriers, then
 // `stages` buffers of tile * (2 N_d + 12) bytes: N_d contribution slices (tile * 2 bytes
 // each), master, m, v.
+// With a gather in the parameters (StepGatherParamsT: the next unit's all-gather), the
+// producer lane continues after its last tile: block b takes gather chunks grid-1-b,
+// 2 grid-1-b, ... (the blocks with one tile fewer start first), loads each through the next
+// ring buffer once the consumers have released it (or, for a buffer that held a gather chunk,
+// once that chunk's bulk store has read it), one load ahead of the stores, and writes it
+// back with a bulk store; the consumer warps copy the copies' unaligned heads and tails.  A
+// wait that runs out sets bit 2 of the error word (as the standalone gather does).
 template <int DT, int MODE, typename PT>
 __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_constant__ PT P)
 {
@@ -706,6 +802,22 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_co
             else if (k - S.head < S.tail) e = S.head + 8 * S.nvec + (k - S.head);
             if (e >= 0) bad |= step_scalar<DT, MODE>(P, S, e, sk, cur, norm2);
         }
+        if constexpr (HasGather<PT>::value) {
+            // the gather copies' unaligned heads and tails (plain copies)
+            for (int64_t q = (int64_t)blockIdx.x * kCT + ct; q < (int64_t)P.g_n * kScalarSlots;
+                 q += (int64_t)gridDim.x * kCT) {
+                const GCopy& C = P.gc[q / kScalarSlots];
+                const int j = (int)(q % kScalarSlots);
+                uint16_t* d = P.g_dst + C.dst_off;
+                const int64_t head = head_elems(d, C.n);
+                const int64_t body = ((int64_t)C.n - head) / 8 * 8;
+                const int64_t tail = (int64_t)C.n - head - body;
+                int64_t e = -1;
+                if (j < head) e = j;
+                else if (j - head < tail) e = head + body + (j - head);
+                if (e >= 0) d[e] = C.src[e];
+            }
+        }
     } else if (lane == 0) {
         const uint64_t policy = evict_first_policy();
         const uint32_t ring0 = full0 + kBulkBarrierBytes;
@@ -733,10 +845,59 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_co
             bulk_load(sdst + sbytes, S.m[cur] + T.e0, 4u * len, full, policy);
             bulk_load(sdst + 2u * sbytes, S.v[cur] + T.e0, 4u * len, full, policy);
         }
-        // Drain: the last phase issued on each buffer completes before the block returns.
         const uint32_t ns = (uint32_t)P.stages;
-        for (uint32_t j = k > ns ? k - ns : 0u; j < k; ++j)
+        uint32_t used = k;   // ring buffers filled so far (tiles, then gather chunks)
+        if constexpr (HasGather<PT>::value) {
+            const int64_t grid = gridDim.x;
+            const int64_t rb = grid - 1 - blockIdx.x;
+            const int64_t mine = (!err && P.g_chunks > rb) ? (P.g_chunks - 1 - rb) / grid + 1 : 0;
+            GChunkWalk<PT> lw, sw;
+            int64_t lc = rb, sc = rb, issued = 0;
+            // load of gather chunk `issued` into ring use k + issued: its buffer held a tile
+            // (wait until the consumers release it) or the gather chunk ns uses before (whose
+            // store has read it: the caller waited for all but the newest store group)
+            auto issue = [&]() -> bool {
+                const uint32_t u = k + (uint32_t)issued, st = u % ns;
+                if (u >= ns && u - ns < k && !mbar_wait(empty0 + 8u * st, ((u / ns) - 1u) & 1u, P.wait_ns))
+                    return false;
+                const uint16_t* src;
+                uint16_t* dst;
+                const TileRef T = lw.at(P, lc, &src, &dst);
+                const uint32_t full = full0 + 8u * st;
+                mbar_arrive_expect_tx(full, 2u * (uint32_t)T.len);
+                bulk_load(ring0 + st * stage_bytes, src + T.e0, 2u * (uint32_t)T.len, full, policy);
+                lc += grid;
+                ++issued;
+                return true;
+            };
+            if (mine > 0 && !issue()) err |= 4u;
+            for (int64_t j = 0; j < mine && !err; ++j) {
+                const uint32_t u = k + (uint32_t)j, st = u % ns;
+                if (!mbar_wait(full0 + 8u * st, (u / ns) & 1u, P.wait_ns)) {
+                    err |= 4u;
+                    break;
+                }
+                const uint16_t* src;
+                uint16_t* dst;
+                const TileRef T = sw.at(P, sc, &src, &dst);
+                bulk_store(dst + T.e0, ring0 + st * stage_bytes, 2u * (uint32_t)T.len, policy);
+                bulk_commit();
+                sc += grid;
+                if (issued < mine) {
+                    bulk_wait_read<1>();   // the store of chunk j - 1 has read its buffer
+                    if (!issue()) {
+                        err |= 4u;
+                        break;
+                    }
+                }
+            }
+            used = k + (uint32_t)issued;
+        }
+        // Drain: the last phase issued on each buffer completes before the block returns, and
+        // so does every bulk store.
+        for (uint32_t j = used > ns ? used - ns : 0u; j < used; ++j)
             if (!mbar_wait(full0 + 8u * (j % ns), (j / ns) & 1u, kDrainNs)) err |= 2u;
+        if constexpr (HasGather<PT>::value) bulk_wait_all();
     }
     if (err) atomicOr(&P.st->error, err);
 
@@ -1110,25 +1271,6 @@ constexpr int kGatherMaxChunk = 32768;
 // 0.95 to 0.92 of the copy bandwidth.
 constexpr int kGatherDefaultChunk = 16384;
 constexpr int kGatherDefaultStages = 4;
-
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
-                 ::"l"(dst), "r"(src), "r"(bytes), "l"(policy)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until at most N bulk groups of this thread still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Wait until every bulk group of this thread has completed (its writes performed).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Walk over the chunks of a launch in increasing order (chunk ids b, b + grid, ...): the
 // copy holding the current chunk and its chunk range (from the host's first-chunk table) are

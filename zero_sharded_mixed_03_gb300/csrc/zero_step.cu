@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <unordered_map>
 
@@ -100,12 +101,15 @@ bool build_step_params(const zero_plan* p, const std::vector<Segment>& segs, siz
         K.c_off = sg.c_off;
         K.n = sg.n;
         const int hd = head16(K.out16);
-        if (contribs)
-            for (int r = 0; r < p->n_d; ++r)
-                vec_ok &= head16((const uint16_t*)contribs[r] + sg.c_off) == hd;
         const int64_t hh = std::min<int64_t>(hd, sg.n);
-        for (int h = 0; h < 2; ++h)
-            vec_ok &= aligned(K.p[h] + hh, 16) && aligned(K.m[h] + hh, 16) && aligned(K.v[h] + hh, 16);
+        // a segment without an 8-element body is all head and tail (scalar): no phase to match
+        if (sg.n - hh >= 8) {
+            if (contribs)
+                for (int r = 0; r < p->n_d; ++r)
+                    vec_ok &= head16((const uint16_t*)contribs[r] + sg.c_off) == hd;
+            for (int h = 0; h < 2; ++h)
+                vec_ok &= aligned(K.p[h] + hh, 16) && aligned(K.m[h] + hh, 16) && aligned(K.v[h] + hh, 16);
+        }
         K.head = (int32_t)hh;
         K.nvec = (sg.n - hh) / 8;
         K.tail = (int32_t)(sg.n - hh - 8 * K.nvec);
@@ -282,7 +286,13 @@ cudaError_t launch_bulk_mode(int dev, PT& P, const BulkCfg& B, int per_sm, cudaS
     P.n_tiles = tiles;
     const int64_t scalar_blocks = ((int64_t)P.n_seg * kScalarSlots + 32 * kBulkConsumers - 1) /
                                   (32 * kBulkConsumers);
-    int64_t grid = std::min<int64_t>(slots, std::max(tiles, scalar_blocks));
+    int64_t want = std::max(tiles, scalar_blocks);
+    if constexpr (HasGather<PT>::value) {
+        const int64_t gscalar = ((int64_t)P.g_n * kScalarSlots + 32 * kBulkConsumers - 1) /
+                                (32 * kBulkConsumers);
+        want = std::max(want, std::max<int64_t>(P.g_chunks, gscalar));
+    }
+    int64_t grid = std::min<int64_t>(slots, want);
     grid = std::max<int64_t>(1, grid);
     kernel<<<(int)grid, kBulkThreads, (size_t)smem, st>>>(P);
     return cudaGetLastError();
@@ -414,8 +424,8 @@ cudaError_t launch_gathers(int dev, const std::vector<Copy>& copies, CP& P, cons
             K.dst = copies[i].dst;
             K.n = copies[i].n;
             const int h = head16(K.dst);
-            vec &= head16(K.src) == h;
             K.head = (int32_t)std::min<int64_t>(h, K.n);
+            if (K.n - K.head >= 8) vec &= head16(K.src) == h;   // a copy with a vector body
             K.nvec = (K.n - K.head) / 8;
             K.tail = (int32_t)(K.n - K.head - 8 * K.nvec);
         }
@@ -442,6 +452,84 @@ cudaError_t launch_gathers(int dev, const std::vector<Copy>& copies, CP& P, cons
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// Copy list of unit `unit`'s all-gather into full_unit16: (source in a rank's 16-bit shard,
+// destination in the unit, length).
+std::vector<Copy> gather_copies(const zero_plan* p, int64_t unit, void* full_unit16)
+{
+    std::vector<Copy> copies;
+    const Unit& U = p->units[(size_t)unit];
+    if (p->per_param) {
+        for (const Chunk& c : p->chunks)
+            if (c.unit == unit && c.rows > 0)
+                copies.push_back({p->ranks[(size_t)c.rank].shard16 + c.phys_off,
+                                  (uint16_t*)full_unit16 + c.contrib_off, c.rows * c.cols});
+    } else if (U.shard > 0) {
+        for (int r = 0; r < p->n_d; ++r)
+            copies.push_back({p->ranks[(size_t)r].shard16 + p->phys_off[(size_t)r][(size_t)unit],
+                              (uint16_t*)full_unit16 + r * U.shard, U.shard});
+    }
+    return copies;
+}
+
+// Fill the gather part of a step launch's parameters from `copies` into `dst`.  False when the
+// copies do not fit the parameter block or the compact record (32-bit offsets and lengths), or
+// when a copy's source and destination are not in one 16-byte phase.
+template <typename GPT>
+bool build_gather_params(const std::vector<Copy>& copies, uint16_t* dst, GPT& P)
+{
+    const size_t cap = sizeof(P.gc) / sizeof(P.gc[0]);
+    if (copies.empty() || copies.size() > cap) return false;
+    P.g_dst = dst;
+    P.g_n = (int32_t)copies.size();
+    for (size_t i = 0; i < copies.size(); ++i) {
+        const Copy& c = copies[i];
+        const int64_t off = c.dst - dst;
+        if (off < 0 || off > (int64_t)UINT32_MAX || c.n < 0 || c.n > (int64_t)UINT32_MAX) return false;
+        const int64_t hd = std::min<int64_t>(head16(c.dst), c.n);
+        if (c.n - hd >= 8 && head16(c.src) != head16(c.dst)) return false;
+        P.gc[i].src = c.src;
+        P.gc[i].dst_off = (uint32_t)off;
+        P.gc[i].n = (uint32_t)c.n;
+        P.gc[i].cbeg = 0;
+        P.gc[i].pad = 0;
+    }
+    return true;
+}
+
+// One step launch (the bulk-staged kernel) that also streams the gather in P's copy list,
+// chunked to one ring buffer (at most 32K elements).  *fused = false and nothing launched when
+// the staged kernel is not the one this launch would use (automatic choice, norm-report step,
+// streams of different phases): the caller then launches the step and the gather separately.
+template <int DT, typename GPT>
+cudaError_t launch_step_gather(int dev, GPT& P, bool vec, cudaStream_t st, int mode,
+                               const BulkCfg& bulk, bool* fused)
+{
+    *fused = false;
+    if (!(bulk.tile > 0 && vec && P.st && mode != kNormAcc)) return cudaSuccess;
+    finalize_vectors(P, vec);
+    const int64_t smem = bulk_smem_bytes(bulk.tile, bulk.stages, P.n_d);
+    int per_sm = 0;
+    const cudaError_t e = mode == kClip ? bulk_residency<DT, kClip, GPT>(dev, smem, &per_sm)
+                                        : bulk_residency<DT, kPlain, GPT>(dev, smem, &per_sm);
+    if (e != cudaSuccess) return e;
+    if (bulk.automatic && !bulk_pays_off(per_sm, bulk.tile)) return cudaSuccess;
+    const int64_t stage_bytes = (int64_t)bulk.tile * (2 * P.n_d + 12);
+    P.g_chunk = (int32_t)std::min<int64_t>(32768, stage_bytes / 16 * 8);
+    int64_t chunks = 0;
+    for (int i = 0; i < P.g_n; ++i) {
+        const uint16_t* d = P.g_dst + P.gc[i].dst_off;
+        const int64_t n = P.gc[i].n;
+        const int64_t body = (n - std::min<int64_t>(head16(d), n)) / 8 * 8;
+        if (chunks > (int64_t)UINT32_MAX) return cudaSuccess;
+        P.gc[i].cbeg = (uint32_t)chunks;
+        chunks += (body + P.g_chunk - 1) / P.g_chunk;
+    }
+    P.g_chunks = chunks;
+    *fused = true;
+    return mode == kClip ? launch_bulk_mode<DT, kClip>(dev, P, bulk, per_sm, st)
+                         : launch_bulk_mode<DT, kPlain>(dev, P, bulk, per_sm, st);
 }
 
 zero_status_t set_device(const zero_plan* p)
@@ -669,9 +757,39 @@ zero_status_t check_step(const zero_plan* p, const void* const* grad_contribs, i
     return ZERO_OK;
 }
 
-// The launches of one checked zero_step call (device contribution pointers).
+// The gather kernel zero_gather_layer launches for the plan (bulk-staged unless disabled or
+// without a workspace, whose error word it needs).
+GatherCfg gather_cfg(const zero_plan* p)
+{
+    GatherCfg g;
+    g.bulk = p->gather_staging != ZERO_STAGING_REGISTER_LOADS;
+    g.chunk = p->gather_chunk > 0 ? p->gather_chunk : kGatherDefaultChunk;
+    g.stages = p->gather_stages > 0 ? p->gather_stages : kGatherDefaultStages;
+    g.err = p->workspace ? &dev_state(p)->error : nullptr;   // no workspace: register loads
+    g.wait_ns = (uint64_t)p->wait_limit_ns;
+    return g;
+}
+
+// The gather launches of a copy list (32 copies a launch, or 256 with the wide block).
+cudaError_t launch_gather_list(const zero_plan* p, const std::vector<Copy>& copies, cudaStream_t s)
+{
+    const GatherCfg g = gather_cfg(p);
+    if (copies.size() > (size_t)kMaxSegs) {
+        CopyParamsWide P;
+        return launch_gathers(p->device, copies, P, g, s);
+    }
+    CopyParams P;
+    return launch_gathers(p->device, copies, P, g, s);
+}
+
+// The launches of one checked zero_step call (device contribution pointers).  With `gather`
+// (a copy list into gather_dst) the call's last launch also streams that all-gather when the
+// staged kernel runs it and the list fits the parameter block; otherwise the gather follows
+// as its own launch.  *gather_fused (when given) tells which.
 zero_status_t enqueue_step(zero_plan* p, const void* const* grad_contribs, int64_t which,
-                           const zero_hyper_t* hyper, cudaStream_t s)
+                           const zero_hyper_t* hyper, cudaStream_t s,
+                           const std::vector<Copy>* gather = nullptr, uint16_t* gather_dst = nullptr,
+                           bool* gather_fused = nullptr)
 {
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
@@ -691,9 +809,41 @@ zero_status_t enqueue_step(zero_plan* p, const void* const* grad_contribs, int64
     else if ((hyper->flags & ZERO_REPORT_GRAD_NORM) && !p->norm_open) mode = kNormAcc;
     const std::vector<Segment> segs = step_segments(p, which, 0);
     const BulkCfg bulk = bulk_config(p);
+    bool pending = gather && !gather->empty();
+    if (gather_fused) *gather_fused = false;
+    // the last launch of the call with the gather in its parameters, if that form applies
+    auto try_fused = [&](auto& GP, size_t b, size_t e) -> cudaError_t {
+        fill_call_params(p, grad_contribs, GP);
+        GP.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
+        const bool vec = build_step_params(p, segs, b, e, grad_contribs, GP);
+        if (!build_gather_params(*gather, gather_dst, GP)) return cudaSuccess;
+        bool fused = false;
+        const cudaError_t err = p->dtype16 == ZERO_BF16
+                                    ? launch_step_gather<ZERO_BF16>(p->device, GP, vec, s, mode, bulk, &fused)
+                                    : launch_step_gather<ZERO_FP16>(p->device, GP, vec, s, mode, bulk, &fused);
+        if (fused) {
+            pending = false;
+            p->last_step_kernel = 1;
+            if (gather_fused) *gather_fused = true;
+        }
+        return err;
+    };
     auto run = [&](auto& P, size_t cap) -> cudaError_t {
         for (size_t b = 0; b < segs.size(); b += cap) {
             const size_t e = std::min(segs.size(), b + cap);
+            if (pending && e == segs.size()) {
+                const size_t n = std::max(e - b, gather->size());
+                cudaError_t err = cudaSuccess;
+                if (n <= (size_t)kMaxSegs) {
+                    StepGatherParams GP;
+                    err = try_fused(GP, b, e);
+                } else if (n <= (size_t)kWideSegs) {
+                    std::unique_ptr<StepGatherParamsWide> GP(new StepGatherParamsWide);
+                    err = try_fused(*GP, b, e);
+                }
+                if (err != cudaSuccess) return err;
+                if (!pending) continue;          // launched with the gather inside
+            }
             fill_call_params(p, grad_contribs, P);
             P.max_norm = mode == kClip ? hyper->max_grad_norm : 0.0;
             const bool vec = build_step_params(p, segs, b, e, grad_contribs, P);
@@ -708,12 +858,13 @@ zero_status_t enqueue_step(zero_plan* p, const void* const* grad_contribs, int64
     };
     cudaError_t lerr;
     if (segs.size() > (size_t)kMaxSegs) {
-        StepParamsWide P;
-        lerr = run(P, kWideSegs);
+        std::unique_ptr<StepParamsWide> P(new StepParamsWide);
+        lerr = run(*P, kWideSegs);
     } else {
         StepParams P;
         lerr = run(P, kMaxSegs);
     }
+    if (lerr == cudaSuccess && pending) lerr = launch_gather_list(p, *gather, s);
     if (lerr != cudaSuccess) return cuda_fail(lerr, "fused step launch");
     p->in_step = true;
     if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
@@ -934,6 +1085,7 @@ try {
         return ZERO_OK;
     case ZERO_OPT_HOST_H2D_BYTES:
     case ZERO_OPT_HOST_D2H_BYTES:
+    case ZERO_OPT_LAST_GATHER_IN_STEP:
         return fail(ZERO_EINVAL, "zero_set_option: read-only option");
     case ZERO_OPT_GATHER_STAGING:
         if (value != ZERO_STAGING_REGISTER_LOADS && value != ZERO_STAGING_BULK &&
@@ -994,6 +1146,7 @@ try {
     case ZERO_OPT_HOST_PIPELINE: *value = p->host_pipeline; return ZERO_OK;
     case ZERO_OPT_HOST_H2D_BYTES: *value = p->host_h2d_last; return ZERO_OK;
     case ZERO_OPT_HOST_D2H_BYTES: *value = p->host_d2h_last; return ZERO_OK;
+    case ZERO_OPT_LAST_GATHER_IN_STEP: *value = p->last_gather_in_step; return ZERO_OK;
     default: return fail(ZERO_EINVAL, "zero_get_option: unknown option");
     }
 }
@@ -1055,6 +1208,35 @@ try {
 }
 catch (...) {
     return exception_status("zero_step");
+}
+
+zero_status_t zero_step_gather_next(zero_plan_t* p, const void* const* grad_contribs,
+                                    int64_t n_contribs, int64_t unit, const zero_hyper_t* hyper,
+                                    int64_t next_unit, void* next_full16, void* stream)
+try {
+    zero_status_t st = check_step(p, grad_contribs, n_contribs, unit, hyper, "zero_step_gather_next");
+    if (st != ZERO_OK) return st;
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_step_gather_next: stage 3 only");
+    if (next_unit < 0 || next_unit >= (int64_t)p->units.size() || next_unit == unit)
+        return fail(ZERO_EINVAL, "zero_step_gather_next: next_unit out of range or equal to unit");
+    if (p->gathered[(size_t)next_unit]) return fail(ZERO_ESTATE, "zero_step_gather_next: next unit not released");
+    const Unit& U = p->units[(size_t)next_unit];
+    if (U.numel_pad > 0 && !next_full16) return fail(ZERO_EINVAL, "zero_step_gather_next: NULL destination");
+    if (!aligned(next_full16, 2)) return fail(ZERO_EALIGN, "zero_step_gather_next: destination not 2-byte aligned");
+    for (const Rank& R : p->ranks)
+        if (!R.shard16 && U.shard > 0)
+            return fail(ZERO_ESTATE, "zero_step_gather_next: a rank has no 16-bit shard bound");
+    const std::vector<Copy> copies = gather_copies(p, next_unit, next_full16);
+    bool fused = false;
+    st = enqueue_step(p, grad_contribs, unit, hyper, (cudaStream_t)stream, &copies,
+                      (uint16_t*)next_full16, &fused);
+    if (st != ZERO_OK) return st;
+    p->gathered[(size_t)next_unit] = 1;
+    p->last_gather_in_step = fused ? 1 : 0;
+    return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_step_gather_next");
 }
 
 zero_status_t zero_step_finish(zero_plan_t* p, void* stream, zero_step_result_t* out)
@@ -1192,33 +1374,8 @@ try {
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    // copy list: (source in a rank's 16-bit shard, destination in the unit, length)
-    std::vector<Copy> copies;
-    if (p->per_param) {
-        for (const Chunk& c : p->chunks)
-            if (c.unit == unit && c.rows > 0)
-                copies.push_back({p->ranks[(size_t)c.rank].shard16 + c.phys_off,
-                                  (uint16_t*)full_unit16 + c.contrib_off, c.rows * c.cols});
-    } else if (U.shard > 0) {
-        for (int r = 0; r < p->n_d; ++r)
-            copies.push_back({p->ranks[(size_t)r].shard16 + p->phys_off[(size_t)r][(size_t)unit],
-                              (uint16_t*)full_unit16 + r * U.shard, U.shard});
-    }
-    GatherCfg g;
-    g.bulk = p->gather_staging != ZERO_STAGING_REGISTER_LOADS;
-    g.chunk = p->gather_chunk > 0 ? p->gather_chunk : kGatherDefaultChunk;
-    g.stages = p->gather_stages > 0 ? p->gather_stages : kGatherDefaultStages;
-    g.err = p->workspace ? &dev_state(p)->error : nullptr;   // no workspace: register loads
-    g.wait_ns = (uint64_t)p->wait_limit_ns;
-    // one launch per 32 copies, or per 256 with the wide parameter block
-    cudaError_t gerr;
-    if (copies.size() > (size_t)kMaxSegs) {
-        CopyParamsWide P;
-        gerr = launch_gathers(p->device, copies, P, g, s);
-    } else {
-        CopyParams P;
-        gerr = launch_gathers(p->device, copies, P, g, s);
-    }
+    const std::vector<Copy> copies = gather_copies(p, unit, full_unit16);
+    const cudaError_t gerr = launch_gather_list(p, copies, s);
     if (gerr != cudaSuccess) return cuda_fail(gerr, "gather launch");
     p->gathered[(size_t)unit] = 1;
     return ZERO_OK;
@@ -1662,11 +1819,34 @@ try {
     const int64_t nu = (int64_t)p->units.size();
     if (n_ptrs != nu * p->n_d)
         return fail(ZERO_EINVAL, "zero_step_units_overlapped: need n_units * N_d contributions");
-    if (compute_stream == comm_stream)
+    if (comm_stream && compute_stream == comm_stream)
         return fail(ZERO_EINVAL, "zero_step_units_overlapped: the two streams must differ");
     if (p->in_step) return fail(ZERO_ESTATE, "zero_step_units_overlapped: a step is open");
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
+    const int64_t nd = p->n_d;
+    if (!comm_stream) {
+        // one stream: unit u+1's all-gather streams inside unit u's step launch
+        if (hyper->max_grad_norm > 0.0)
+            for (int64_t u = 0; u < nu; ++u) {
+                st = zero_grad_norm(p, unit_contribs + u * nd, nd, u, compute_stream);
+                if (st != ZERO_OK) return st;
+            }
+        if (nu > 0) {
+            st = zero_gather_layer(p, 0, gather_bufs[0], compute_stream);
+            if (st != ZERO_OK) return st;
+        }
+        for (int64_t u = 0; u < nu; ++u) {
+            // (a layer's forward/backward would consume gather_bufs[u % 2] here)
+            st = zero_release_layer(p, u);
+            if (st != ZERO_OK) return st;
+            st = u + 1 < nu ? zero_step_gather_next(p, unit_contribs + u * nd, nd, u, hyper, u + 1,
+                                                    gather_bufs[(u + 1) % 2], compute_stream)
+                            : zero_step(p, unit_contribs + u * nd, nd, u, hyper, compute_stream);
+            if (st != ZERO_OK) return st;
+        }
+        return zero_step_finish(p, compute_stream, out);
+    }
     if (!p->ov_events[0]) {
         for (int i = 0; i < 5; ++i) {
             cudaEvent_t ev;
@@ -1680,7 +1860,6 @@ try {
     cudaEvent_t start = (cudaEvent_t)p->ov_events[0];
     cudaEvent_t gathered[2] = {(cudaEvent_t)p->ov_events[1], (cudaEvent_t)p->ov_events[2]};
     cudaEvent_t released[2] = {(cudaEvent_t)p->ov_events[3], (cudaEvent_t)p->ov_events[4]};
-    const int64_t nd = p->n_d;
     if (hyper->max_grad_norm > 0.0)
         for (int64_t u = 0; u < nu; ++u) {
             st = zero_grad_norm(p, unit_contribs + u * nd, nd, u, compute_stream);

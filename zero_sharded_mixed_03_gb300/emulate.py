@@ -19,7 +19,8 @@ from . import (ZERO_BF16, zero_set_option, ZERO_TABLE_PARAM_CHUNKS, ZERO_TABLE_S
                zero_grad_norm, zero_plan_tables, zero_rank_state_elems, zero_read_state,
                zero_release_layer,
                zero_set_scaler, zero_step, zero_step_finish,
-               zero_bind_host_staging, zero_step_host, zero_step_host_finish)
+               zero_bind_host_staging, zero_step_host, zero_step_host_finish,
+               zero_step_gather_next)
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
@@ -187,6 +188,12 @@ class EmulatedGroup:
         if self.offload:
             return zero_offload_finish(self.plan, self.offload_threads, _stream_handle(stream), wait)
         return zero_step_finish(self.plan, _stream_handle(stream), wait)
+
+    def step_gather_next(self, contribs: Sequence[int], unit: int, hyper, next_unit: int,
+                         dst: torch.Tensor, stream=None) -> None:
+        """Step of `unit` with the all-gather of `next_unit` into dst in the same launch."""
+        zero_step_gather_next(self.plan, list(contribs), unit, hyper, next_unit, dst.data_ptr(),
+                              _stream_handle(stream))
 
     def gather(self, unit: int, dst: torch.Tensor, stream=None) -> None:
         zero_gather_layer(self.plan, unit, dst.data_ptr(), _stream_handle(stream))
