@@ -48,7 +48,12 @@ MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("ae6390b593db8a38", 2_287_339_520)
                     # elements to the average launch the bench times
                     (2, "bulk_step_kernel"): ("ae6390b593db8a38", 1_003_436_229),
                     (3, "bulk_step_kernel"): ("ae6390b593db8a38", 2_901_763_547),
-                    (4, "bulk_step_kernel"): ("ae6390b593db8a38", 999_794_979)}
+                    (4, "bulk_step_kernel"): ("ae6390b593db8a38", 999_794_979),
+                    # the step launch that also gathers the next unit (one launch captured on
+                    # a two-unit slice of the model, scaled by algorithmic bytes to the average
+                    # launch of the full step)
+                    (3, "bulk_step_kernel + gather"): ("2f4a92a011191c99", 3_068_451_376),
+                    (4, "bulk_step_kernel + gather"): ("2f4a92a011191c99", 1_764_906_338)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_kernels.cuh")
 
 
@@ -108,6 +113,9 @@ def parse_args():
     ap.add_argument("--profile-unit", type=int, default=None,
                     help="stage 3: restrict the workload to this one unit (for ncu captures of a "
                          "few GB; not the benchmark workload)")
+    ap.add_argument("--profile-units", type=int, default=1,
+                    help="with --profile-unit: this many units from it (2: one step launch that "
+                         "also gathers the next unit)")
     ap.add_argument("--grad-norm", choices=["off", "report", "clip"], default="off",
                     help="report: global gradient norm inside the fused pass; clip: norm pre-pass "
                          "over every bucket/unit, then the update clipped at max norm 1.0")
@@ -550,7 +558,7 @@ def gpu_arm(args, world, rank, local):
     if args.per_param:
         w = W.per_param_variant(w)
     if args.profile_unit is not None:
-        w = W.unit_slice(w, args.profile_unit)
+        w = W.unit_slice(w, args.profile_unit, args.profile_units)
     if args.offload:
         import dataclasses
         w = dataclasses.replace(w, offload=True)
@@ -704,6 +712,7 @@ def gpu_arm(args, world, rank, local):
                       "schedule": ("overlap" if overlap else args.schedule) if w.stage == 3 else None,
                       "offload": w.offload, "staging": args.staging,
                       "profile_unit": args.profile_unit,
+                      "profile_units": args.profile_units if args.profile_unit is not None else None,
                       "offload_threads": b.g.offload_threads if w.offload else None},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "hbm_frac_of_nominal": round(hbm_gbs / NOMINAL_HBM_GBS, 4),

@@ -122,15 +122,21 @@ def llama_dim0(vocab: int, d: int, ffn: int, layers: int) -> List[int]:
     return dims + [d, vocab]
 
 
-def unit_slice(w: "Workload", u: int) -> "Workload":
-    """Stage 3: the same workload restricted to the tensors of unit u (one unit), e.g. to
-    profile one unit's kernels with a few GB on the device."""
+def unit_slice(w: "Workload", u: int, n_units: int = 1) -> "Workload":
+    """Stage 3: the same workload restricted to the tensors of units u .. u + n_units - 1, e.g.
+    to profile one or two units' kernels with a few GB on the device."""
     if w.stage != 3:
         raise ValueError("unit_slice: stage-3 workloads only")
-    first, count = w.units()[u]
+    units = w.units()[u:u + n_units]
+    if not units or n_units < 1:
+        raise ValueError("unit_slice: no such units")
+    first = units[0][0]
+    last = units[-1][0] + units[-1][1]
+    firsts = tuple(f - first for f, _ in units)
+    label = f"unit {u} only" if n_units == 1 else f"units {u}..{u + n_units - 1} only"
     return dataclasses.replace(
-        w, name=f"{w.name}, unit {u} only", sizes=w.sizes[first:first + count], unit_first=(0,),
-        dim0=w.dim0[first:first + count] if w.dim0 else None, inject=None)
+        w, name=f"{w.name}, {label}", sizes=w.sizes[first:last], unit_first=firsts,
+        dim0=w.dim0[first:last] if w.dim0 else None, inject=None)
 
 
 def per_param_variant(w: "Workload") -> "Workload":
