@@ -42,13 +42,10 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_kernels.cuh, the device code); reported as null
 # once that source changes.
-MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("ae6390b593db8a38", 2_287_339_520),
-                    (1, "fused_step_kernel"): ("ae6390b593db8a38", 2_303_291_136),
-                    # one launch captured (configs 3 and 4: one unit of the model), scaled by
-                    # elements to the average launch the bench times
-                    (2, "bulk_step_kernel"): ("ae6390b593db8a38", 1_003_436_229),
-                    (3, "bulk_step_kernel"): ("ae6390b593db8a38", 2_901_763_547),
-                    (4, "bulk_step_kernel"): ("ae6390b593db8a38", 999_794_979),
+MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("2f4a92a011191c99", 2_286_647_808),
+                    # one launch captured (bucket 0 of 5), scaled by elements to the average
+                    # launch the bench times
+                    (2, "bulk_step_kernel"): ("2f4a92a011191c99", 1_003_566_203),
                     # the step launch that also gathers the next unit (one launch captured on
                     # a two-unit slice of the model, scaled by algorithmic bytes to the average
                     # launch of the full step)
@@ -91,6 +88,10 @@ def parse_args():
     ap.add_argument("--offload", action="store_true",
                     help="ZeRO-Offload: gradients reduced on the GPU into pinned host memory, AdamW "
                          "on the host CPU threads, 16-bit parameters copied back")
+    ap.add_argument("--offload-defer", action="store_true",
+                    help="with --offload: ZERO_OPT_OFFLOAD_DEFER (the contribution buffers stay "
+                         "unchanged until the finish, so every bucket's flag pass runs first and "
+                         "the reductions stream to the host while it updates)")
     ap.add_argument("--per-param", action="store_true",
                     help="FSDP-2 per-parameter (dim-0) sharding of the same model")
     ap.add_argument("--overlap", action="store_true",
@@ -283,7 +284,7 @@ class Bench:
 
         self.torch, self.Z, self.synth = torch, Z, synth
         self.w = w
-        self.fused_gather = fused_gather and w.stage == 3
+        self.fused_gather = fused_gather and w.stage == 3 and not w.offload
         self.gather_in_step = None            # learnt from the library on the first step
         # plan, state, 16-bit buffers, initial params
         self.run = Run(w, alloc_contribs=False, options=options)
@@ -567,6 +568,8 @@ def gpu_arm(args, world, rank, local):
                "auto": Z.ZERO_STAGING_AUTO}[args.staging]
     options = {Z.ZERO_OPT_STAGING: staging, Z.ZERO_OPT_BULK_TILE: args.bulk_tile,
                Z.ZERO_OPT_BULK_STAGES: args.bulk_stages}
+    if args.offload and args.offload_defer:
+        options[Z.ZERO_OPT_OFFLOAD_DEFER] = 1
     # gather ring: entries first when the chunk grows, so that no intermediate ring overflows
     gather = [(Z.ZERO_OPT_GATHER_CHUNK, args.gather_chunk), (Z.ZERO_OPT_GATHER_STAGES, args.gather_stages)]
     options.update(dict(gather[::-1] if args.gather_chunk > 16384 else gather))
@@ -713,7 +716,8 @@ def gpu_arm(args, world, rank, local):
                       "offload": w.offload, "staging": args.staging,
                       "profile_unit": args.profile_unit,
                       "profile_units": args.profile_units if args.profile_unit is not None else None,
-                      "offload_threads": b.g.offload_threads if w.offload else None},
+                      "offload_threads": b.g.offload_threads if w.offload else None,
+                      "offload_defer": bool(w.offload and args.offload_defer)},
            "hbm_gbs": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / peak, 4),
            "hbm_frac_of_nominal": round(hbm_gbs / NOMINAL_HBM_GBS, 4),
            "skipped_steps": skipped, "roofline": roofline, "gpu_launches": launches,

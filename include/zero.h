@@ -342,9 +342,17 @@ enum {
     ZERO_OPT_HOST_D2H_BYTES = 10,   /* read only: bytes copied device->host in that step (the
                                        updated 16-bit parameters, re-copies after a skip
                                        included) */
-    ZERO_OPT_LAST_GATHER_IN_STEP = 11 /* read only: 1 if the last zero_step_gather_next streamed
-                                       its gather inside the step launch, 0 if the gather ran
-                                       as a launch of its own, -1 none yet */
+    ZERO_OPT_LAST_GATHER_IN_STEP = 11, /* read only: 1 if the last zero_step_gather_next
+                                       streamed its gather inside the step launch, 0 if the
+                                       gather ran as a launch of its own, -1 none yet */
+    ZERO_OPT_OFFLOAD_DEFER = 12     /* offloaded plans: 0 (default) zero_offload_step reduces its
+                                       contributions into host memory in stream order; 1 it only
+                                       runs the non-finite flag pass, and zero_offload_finish,
+                                       once every call's flag is known, streams the reductions
+                                       (a skipped step skips them) while the host threads update
+                                       each group as it lands.  With 1 the contributions of every
+                                       call must stay unchanged until zero_offload_finish
+                                       returns. */
 };
 enum { ZERO_STAGING_REGISTER_LOADS = 0, ZERO_STAGING_BULK = 1, ZERO_STAGING_AUTO = 2 };
 zero_status_t zero_set_option(zero_plan_t* plan, int option, int64_t value);

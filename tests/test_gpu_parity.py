@@ -602,6 +602,36 @@ def test_offload_full_parity(name):
     assert mism == 0
 
 
+@pytest.mark.parametrize("name", ["z2_nd2_fp16_groups_buckets_skip", "z2_nd8_fp16_buckets_inf",
+                                  "z3_nd3_fp16_peers_skip_first", "pp_nd4_units", "z1_nd4"])
+def test_offload_deferred_reductions_full_parity(name):
+    """ZERO_OPT_OFFLOAD_DEFER: every call runs only its flag pass; the finish, knowing the skip
+    decision, streams the reductions (none on a skipped step) while the host threads update.
+    Each bucket / unit keeps its own contribution buffers until the finish, as the option
+    requires.  Same results as the stream-ordered path: the oracle's, bit for bit."""
+    w = OFFLOAD_CASES[name]
+    run = H.Run(w, alloc_contribs=False, options={Z.ZERO_OPT_OFFLOAD_DEFER: 1})
+    o = H.OracleFull(w, run.bound)
+    calls = run.ranges()
+    bufs = [[torch.empty(max(8, hi - lo), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+            for (_w, lo, hi) in calls]
+    try:
+        for k in range(1, w.steps + 1):
+            for ci, (which, lo, hi) in enumerate(calls):
+                for r in range(w.n_d):
+                    H.fill_device(bufs[ci][r], synth.grad_stream(w, k, r), run.units, lo, hi)
+                if w.stage == 3:
+                    run.g.gather(which, run.gather_buf)
+                    run.g.release(which)
+                run.g.step([t.data_ptr() for t in bufs[ci]], which, run.hyper)
+            res = run.g.finish()
+            flag = o.step(k)
+            assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
+            _compare_full(run, o, f"offload deferred {name} step {k}")
+    finally:
+        run.close()
+
+
 def test_offload_worker_threads_end_with_the_plan():
     """An offloaded plan keeps its host worker threads between steps and ends them in
     zero_plan_destroy: the process's thread count returns to where it was."""

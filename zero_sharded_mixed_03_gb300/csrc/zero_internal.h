@@ -168,6 +168,13 @@ struct zero_plan {
     // the last flag pass, and a side stream that reads the step state once that event is done.
     std::vector<zero::Segment> off_segs;
     std::vector<size_t> off_group_end;
+    // ZERO_OPT_OFFLOAD_DEFER: the calls whose writing reduction waits for zero_offload_finish
+    struct OffloadCall {
+        std::vector<const void*> contribs;
+        std::vector<zero::Segment> segs;
+    };
+    std::vector<OffloadCall> off_deferred;
+    int offload_defer = 0;
     std::vector<void*> off_events;
     void* off_flag_event = nullptr;
     void* off_side = nullptr;

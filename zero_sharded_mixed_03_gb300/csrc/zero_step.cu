@@ -934,6 +934,77 @@ std::vector<std::pair<int64_t, int64_t>> read_runs(const std::vector<Segment>& s
     return out;
 }
 
+// ZeRO-Offload: reduce segs[b0, e0) of one call (store: the averaged gradient into the
+// bound ranks' pinned host buffers; else: the non-finite flag alone), `cap` items a launch.
+template <typename PT>
+cudaError_t offload_launches(zero_plan* p, const void* const* contribs, const std::vector<Segment>& segs,
+                             PT& P, size_t cap, size_t b0, size_t e0, bool store, cudaStream_t s)
+{
+    for (size_t b = b0; b < e0; b += cap) {
+        const size_t e = std::min(e0, b + cap);
+        fill_call_params(p, contribs, P);
+        const bool vec = build_offload_params(p, segs, b, e, contribs, P);
+        cudaError_t err;
+        if (p->dtype16 == ZERO_BF16)
+            err = store ? launch_reduce_to_host<ZERO_BF16, true>(p->device, P, vec, s)
+                        : launch_reduce_to_host<ZERO_BF16, false>(p->device, P, vec, s);
+        else
+            err = store ? launch_reduce_to_host<ZERO_FP16, true>(p->device, P, vec, s)
+                        : launch_reduce_to_host<ZERO_FP16, false>(p->device, P, vec, s);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+template <typename F>
+cudaError_t with_offload_params(const std::vector<Segment>& segs, F&& f)
+{
+    if (segs.size() > (size_t)kMaxSegs) {
+        std::unique_ptr<StepParamsWide> P(new StepParamsWide);
+        return f(*P, (size_t)kWideSegs);
+    }
+    StepParams P;
+    return f(P, (size_t)kMaxSegs);
+}
+
+// The flag-only pass over a call (so that, after the step's last call, the host knows the skip
+// decision early), then an event the finish waits for.
+cudaError_t offload_flag_pass(zero_plan* p, const void* const* contribs, const std::vector<Segment>& segs,
+                              cudaStream_t s)
+{
+    cudaError_t err = with_offload_params(segs, [&](auto& P, size_t cap) {
+        return offload_launches(p, contribs, segs, P, cap, 0, segs.size(), false, s);
+    });
+    if (err == cudaSuccess) err = offload_event(p, &p->off_flag_event);
+    if (err == cudaSuccess) err = cudaEventRecord((cudaEvent_t)p->off_flag_event, s);
+    return err;
+}
+
+// The writing reduction of a call in groups of segments of at least kOffloadGroupElems
+// elements, an event after each (the host updates a group as soon as its gradient has
+// landed).  first: index in off_segs of the call's first segment.
+cudaError_t offload_reduce_groups(zero_plan* p, const void* const* contribs, const std::vector<Segment>& segs,
+                                  size_t first, cudaStream_t s)
+{
+    return with_offload_params(segs, [&](auto& P, size_t cap) {
+        cudaError_t err = cudaSuccess;
+        size_t b = 0;
+        while (err == cudaSuccess && b < segs.size()) {
+            size_t e = b;
+            int64_t n = 0;
+            while (e < segs.size() && n < kOffloadGroupElems) n += segs[e++].n;
+            err = offload_launches(p, contribs, segs, P, cap, b, e, true, s);
+            const size_t g = p->off_group_end.size();
+            if (g >= p->off_events.size()) p->off_events.push_back(nullptr);
+            if (err == cudaSuccess) err = offload_event(p, &p->off_events[g]);
+            if (err == cudaSuccess) err = cudaEventRecord((cudaEvent_t)p->off_events[g], s);
+            p->off_group_end.push_back(first + e);
+            b = e;
+        }
+        return err;
+    });
+}
+
 // Re-cast + commit of the open step (zero_step_finish without its checks on host calls).
 zero_status_t finish_step(zero_plan_t* p, void* stream, zero_step_result_t* out);
 
@@ -1083,6 +1154,10 @@ try {
         if (value != 0 && value != 1) return fail(ZERO_EINVAL, "zero_set_option: host pipeline must be 0 or 1");
         p->host_pipeline = (int)value;
         return ZERO_OK;
+    case ZERO_OPT_OFFLOAD_DEFER:
+        if (value != 0 && value != 1) return fail(ZERO_EINVAL, "zero_set_option: offload defer must be 0 or 1");
+        p->offload_defer = (int)value;
+        return ZERO_OK;
     case ZERO_OPT_HOST_H2D_BYTES:
     case ZERO_OPT_HOST_D2H_BYTES:
     case ZERO_OPT_LAST_GATHER_IN_STEP:
@@ -1144,6 +1219,7 @@ try {
     case ZERO_OPT_GATHER_CHUNK: *value = p->gather_chunk > 0 ? p->gather_chunk : kGatherDefaultChunk; return ZERO_OK;
     case ZERO_OPT_GATHER_STAGES: *value = p->gather_stages > 0 ? p->gather_stages : kGatherDefaultStages; return ZERO_OK;
     case ZERO_OPT_HOST_PIPELINE: *value = p->host_pipeline; return ZERO_OK;
+    case ZERO_OPT_OFFLOAD_DEFER: *value = p->offload_defer; return ZERO_OK;
     case ZERO_OPT_HOST_H2D_BYTES: *value = p->host_h2d_last; return ZERO_OK;
     case ZERO_OPT_HOST_D2H_BYTES: *value = p->host_d2h_last; return ZERO_OK;
     case ZERO_OPT_LAST_GATHER_IN_STEP: *value = p->last_gather_in_step; return ZERO_OK;
@@ -1501,57 +1577,20 @@ try {
     if (!p->in_step) {
         p->off_segs.clear();
         p->off_group_end.clear();
+        p->off_deferred.clear();
     }
-    // Reduce segs[b0, e0) (store: into host memory; else: the flag alone), cap items a launch.
-    auto run = [&](auto& P, size_t cap, size_t b0, size_t e0, bool store) -> cudaError_t {
-        for (size_t b = b0; b < e0; b += cap) {
-            const size_t e = std::min(e0, b + cap);
-            fill_call_params(p, grad_contribs, P);
-            const bool vec = build_offload_params(p, segs, b, e, grad_contribs, P);
-            cudaError_t err;
-            if (p->dtype16 == ZERO_BF16)
-                err = store ? launch_reduce_to_host<ZERO_BF16, true>(p->device, P, vec, s)
-                            : launch_reduce_to_host<ZERO_BF16, false>(p->device, P, vec, s);
-            else
-                err = store ? launch_reduce_to_host<ZERO_FP16, true>(p->device, P, vec, s)
-                            : launch_reduce_to_host<ZERO_FP16, false>(p->device, P, vec, s);
-            if (err != cudaSuccess) return err;
-        }
-        return cudaSuccess;
-    };
-    // First the flag over the whole call (so that, after the step's last call, the host knows
-    // the skip decision early), then the reduction in groups of segments of at least
-    // kOffloadGroupElems elements, an event after each: the host updates a group as soon as
-    // its gradient has landed.
-    auto reduce_all = [&](auto& P, size_t cap) -> cudaError_t {
-        cudaError_t err = run(P, cap, 0, segs.size(), false);
-        if (err == cudaSuccess) err = offload_event(p, &p->off_flag_event);
-        if (err == cudaSuccess) err = cudaEventRecord((cudaEvent_t)p->off_flag_event, s);
-        size_t b = 0;
-        while (err == cudaSuccess && b < segs.size()) {
-            size_t e = b;
-            int64_t n = 0;
-            while (e < segs.size() && n < kOffloadGroupElems) n += segs[e++].n;
-            err = run(P, cap, b, e, true);
-            const size_t g = p->off_group_end.size();
-            if (g >= p->off_events.size()) p->off_events.push_back(nullptr);
-            if (err == cudaSuccess) err = offload_event(p, &p->off_events[g]);
-            if (err == cudaSuccess) err = cudaEventRecord((cudaEvent_t)p->off_events[g], s);
-            p->off_group_end.push_back(p->off_segs.size() + e);
-            b = e;
-        }
-        return err;
-    };
     cudaError_t err;
-    if (segs.size() > (size_t)kMaxSegs) {
-        StepParamsWide P;
-        err = reduce_all(P, kWideSegs);
+    if (p->offload_defer) {
+        // the flag pass now; the writing reduction when zero_offload_finish knows the decision
+        err = offload_flag_pass(p, grad_contribs, segs, s);
+        if (err == cudaSuccess)
+            p->off_deferred.push_back({std::vector<const void*>(grad_contribs, grad_contribs + p->n_d), segs});
     } else {
-        StepParams P;
-        err = reduce_all(P, kMaxSegs);
+        err = offload_flag_pass(p, grad_contribs, segs, s);
+        if (err == cudaSuccess) err = offload_reduce_groups(p, grad_contribs, segs, p->off_segs.size(), s);
     }
     if (err != cudaSuccess) return cuda_fail(err, "reduce-to-host launch");
-    p->off_segs.insert(p->off_segs.end(), segs.begin(), segs.end());
+    if (!p->offload_defer) p->off_segs.insert(p->off_segs.end(), segs.begin(), segs.end());
     p->in_step = true;
     if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
     else p->covered[(size_t)which] = 1;
@@ -1591,12 +1630,26 @@ try {
     if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: reading the step state");
     float k9[9];
     step_constants(p->step_hyper, host.t + 1, host.scale, p->n_d, k9);
+    // deferred reductions (ZERO_OPT_OFFLOAD_DEFER): the decision is known; a clean step streams
+    // every call's gradient to the host now, a skipped one needs none of it
+    if (!p->off_deferred.empty()) {
+        if (host.flag == 0)
+            for (const zero_plan::OffloadCall& c : p->off_deferred) {
+                e = offload_reduce_groups(p, c.contribs.data(), c.segs, p->off_segs.size(), s);
+                if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: reduce-to-host launch");
+                p->off_segs.insert(p->off_segs.end(), c.segs.begin(), c.segs.end());
+            }
+        else
+            for (const zero_plan::OffloadCall& c : p->off_deferred)
+                p->off_segs.insert(p->off_segs.end(), c.segs.begin(), c.segs.end());
+        p->off_deferred.clear();
+    }
     const std::vector<Segment>& segs = p->off_segs;
     std::vector<CpuSpan> spans;
     std::vector<int> group_of_span;
     int g = 0;
     for (size_t i = 0; i < segs.size(); ++i) {
-        while (i >= p->off_group_end[(size_t)g]) ++g;
+        while ((size_t)g < p->off_group_end.size() && i >= p->off_group_end[(size_t)g]) ++g;
         const Segment& sg = segs[i];
         const Rank& R = p->ranks[(size_t)sg.rank];
         spans.push_back(CpuSpan{R.master[0] + sg.s_off, R.m[0] + sg.s_off, R.v[0] + sg.s_off,
