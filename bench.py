@@ -585,6 +585,12 @@ def gpu_arm(args, world, rank, local):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
+    schedule_note = None
+    if b.fused_gather and b.gather_in_step is False:
+        # the library ran the gathers as launches of their own (e.g. register-load step
+        # kernel): time them as such, every gather between its own events
+        b.fused_gather = False
+        schedule_note = "serial: the library launched the gathers separately"
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -712,7 +718,8 @@ def gpu_arm(args, world, rank, local):
                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)",
                       "contribution_sets": b.n_sets, "grad_norm": args.grad_norm,
                       "overlap": overlap, "graph": m["graph"], "per_param": w.per_param,
-                      "schedule": ("overlap" if overlap else args.schedule) if w.stage == 3 else None,
+                      "schedule": (("overlap" if overlap else (schedule_note or args.schedule))
+                                   if w.stage == 3 else None),
                       "offload": w.offload, "staging": args.staging,
                       "profile_unit": args.profile_unit,
                       "profile_units": args.profile_units if args.profile_unit is not None else None,
