@@ -7,8 +7,9 @@ against the oracle on the same seeded inputs: every gathered unit bit for bit (t
 reads the shards the previous step wrote), the fp32 state within 1e-6 |x| + 1e-8, the 16-bit
 shards within 1 ulp, skips, t and the loss scale exactly.  Also: the register-load fallback
 (gather as a launch of its own), per-parameter plans (the wide parameter block), a tiny step
-carrying a large gather, the one-stream schedule, the 1.3B workload sampled at full size, and
-a wait that runs out inside the gather part.
+carrying a large gather, clipping, norm-report steps (which fall back), the one-stream
+schedule (also captured in a CUDA graph and replayed), the 1.3B and Llama workloads sampled at
+full size, flat and per-parameter, and a wait that runs out inside the gather part.
 """
 import dataclasses
 
@@ -79,7 +80,7 @@ def _fill_units(run, w, k, contribs):
             H.fill_device(contribs[u][r], synth.grad_stream(w, k, r), run.units, lo, hi)
 
 
-def _run_fused(w, options=None, expect_fused=True):
+def _run_fused(w, options=None, expect_fused=True, check_norm=False):
     run = H.Run(w, options=options, alloc_contribs=False)
     o = H.OracleFull(w, run.bound)
     nu = len(run.units)
@@ -92,6 +93,9 @@ def _run_fused(w, options=None, expect_fused=True):
         for k in range(1, w.steps + 1):
             expect_g = [o.gathered(u) for u in range(nu)]
             _fill_units(run, w, k, contribs)
+            if w.hyper.max_grad_norm > 0:              # clipping: the norm over every unit first
+                for u in range(nu):
+                    run.g.grad_norm([c.data_ptr() for c in contribs[u]], u)
             run.g.gather(0, bufs[0])
             for u in range(nu):
                 torch.cuda.synchronize()
@@ -109,6 +113,9 @@ def _run_fused(w, options=None, expect_fused=True):
             flag = o.step(k)
             assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
             H.compare_full(run, o, f"{w.name} fused step {k}")
+            if check_norm:
+                want = float(np.sqrt(o.norm2))
+                assert abs(res.grad_norm - want) <= 1e-12 * want, (res.grad_norm, want)
         if expect_fused is not None:
             assert all(x == (1 if expect_fused else 0) for x in in_step), in_step
     finally:
@@ -162,26 +169,38 @@ def test_one_stream_overlapped_schedule(name):
         run.close()
 
 
-def test_step_with_next_gather_config3_sampled():
-    """The ZeRO-3 1.3B workload at full size (N_d = 16, 26 units) in the one-stream schedule:
-    sampled state elements and every gathered unit at sampled positions against the oracle."""
-    w = dataclasses.replace(W.workload(3), steps=2)
-    run = H.Run(w, options=BULK)
+@pytest.mark.parametrize("cfg,per_param,bound", [(3, False, None), (4, False, (0, 7)),
+                                                  (3, True, None), (4, True, (0, 7))])
+def test_step_with_next_gather_config_sampled(cfg, per_param, bound):
+    """The ZeRO-3 1.3B and Llama rank-view workloads at full size (flat and per-parameter
+    plans) in the one-stream schedule the bench times: sampled state elements and every
+    gathered unit at sampled positions against the oracle."""
+    w = W.workload(cfg)
+    if per_param:
+        w = W.per_param_variant(w)
+    w = dataclasses.replace(w, steps=2)
+    run = H.Run(w, bound=bound, options=BULK)
     try:
         idx = H.sample_indices(run, 20000)
         o = H.OracleSampled(w, idx)
+        # elements of ranks without local state: their gathered values stay the initial ones
+        allr = H.sample_indices(run, 4000, seed=1, bound_only=False)
+        rank, _ = run.locate(allr)
+        peer_idx = allr[rank < 0]
+        peer16 = H.values_at(synth.param_stream(w), o.units, peer_idx)
         nu = len(run.units)
         maxu = int(run.info.max_unit_pad)
         bufs = [torch.empty(maxu, dtype=torch.int16, device="cuda") for _ in range(2)]
         calls = run.ranges()
         for k in range(1, w.steps + 1):
-            exp16 = o.out16.copy()               # the shards as the previous step left them
+            exp_idx = np.concatenate([idx, peer_idx])
+            exp16 = np.concatenate([o.out16, peer16])    # the shards the previous step left
             run.g.gather(0, bufs[0])
             for u, (which, lo, hi) in enumerate(calls):
                 torch.cuda.synchronize()
-                sel = (idx >= lo) & (idx < hi)
+                sel = (exp_idx >= lo) & (exp_idx < hi)
                 if sel.any():
-                    got = bufs[u % 2][torch.from_numpy(idx[sel] - lo).cuda()].cpu().numpy().view(np.uint16)
+                    got = bufs[u % 2][torch.from_numpy(exp_idx[sel] - lo).cuda()].cpu().numpy().view(np.uint16)
                     assert np.array_equal(got, exp16[sel]), f"gathered unit {u} at step {k}"
                 run.g.release(u)
                 for r in range(w.n_d):
@@ -197,8 +216,8 @@ def test_step_with_next_gather_config3_sampled():
             assert res.skipped == flag and res.t == o.sc.t, f"step {k}"
             st, g16 = run.read_sampled(idx)
             for key, want in (("master", o.p), ("m", o.m), ("v", o.v)):
-                H.assert_state_close(st[key], want, f"config3 fused step {k} {key}")
-            H.assert_16_close(g16, o.out16, f"config3 fused step {k} 16-bit")
+                H.assert_state_close(st[key], want, f"{w.name} fused step {k} {key}")
+            H.assert_16_close(g16, o.out16, f"{w.name} fused step {k} 16-bit")
     finally:
         run.close()
 
@@ -267,5 +286,66 @@ def test_wait_limit_runs_out_in_the_gather_part():
         o.step(2)
         assert (res.t, res.finished, res.skipped) == (2, 2, 0)
         H.compare_full(run, o, "after the timeout")
+    finally:
+        run.close()
+
+
+def test_step_with_next_gather_and_clipping():
+    """Clipping (norm pre-pass over every unit, then the clip-mode step): the step launches
+    still carry the next unit's gather; states and the norm match the oracle."""
+    w = dataclasses.replace(CASES["nd16_units"], wid=508, hyper=W.Hyper(max_grad_norm=0.02))
+    _run_fused(w, options=BULK, check_norm=True)
+
+
+def test_step_with_next_gather_norm_report_falls_back():
+    """Norm-report steps run the register-load kernel, so the gather is a launch of its own;
+    the update is unchanged and the reported norm matches the oracle."""
+    w = dataclasses.replace(CASES["nd16_units"], wid=509, hyper=W.Hyper(report_norm=True))
+    _run_fused(w, options=BULK, expect_fused=False, check_norm=True)
+
+
+def test_one_stream_schedule_captured_in_a_cuda_graph():
+    """A whole one-stream step (unit 0's gather, the step launches that gather the next unit,
+    the re-cast and the commit) captured once and replayed with new gradients written in place:
+    every replay follows the oracle, through a skipped step."""
+    w = dataclasses.replace(CASES["nd3_fp16_peers_skip_first"], wid=510, steps=4, inject=(3, 1, 4321))
+    run = H.Run(w, options=BULK, alloc_contribs=False)
+    o = H.OracleFull(w, run.bound)
+    nu = len(run.units)
+    bufs = [torch.empty(int(run.info.max_unit_pad), dtype=torch.int16, device="cuda") for _ in range(2)]
+    contribs = [[torch.empty(max(8, U[3]), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+                for U in run.units]
+    ptrs = [c.data_ptr() for unit in contribs for c in unit]
+    gptrs = [b.data_ptr() for b in bufs]
+
+    def enqueue(stream):
+        Z.zero_step_units_overlapped(run.g.plan, ptrs, gptrs, run.hyper, stream.cuda_stream, None,
+                                     wait=False)
+
+    try:
+        _fill_units(run, w, 1, contribs)
+        enqueue(torch.cuda.current_stream())      # step 1 uncaptured: bias table, kernel set-up
+        o.step(1)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                enqueue(side)                     # captured, not run
+        skips = 0
+        for k in range(2, w.steps + 1):
+            expect_last = o.gathered(nu - 1)
+            _fill_units(run, w, k, contribs)
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            skips += o.step(k)
+            st = run.g.step_state()
+            assert (st.t, st.scale, st.skipped_total) == (o.sc.t, o.sc.scale, skips), k
+            got = bufs[(nu - 1) % 2][:run.units[nu - 1][3]].cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, expect_last), f"gathered unit {nu - 1} at replay {k}"
+            H.compare_full(run, o, f"one-stream graph replay step {k}")
+        assert skips == 1
     finally:
         run.close()
