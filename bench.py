@@ -105,6 +105,8 @@ def parse_args():
                     help="bulk: cp.async.bulk (TMA) staging of the contribution and state tiles "
                          "into shared memory; ldg: 128-bit register loads; auto (default): the "
                          "library's choice (staged where its residency pays off)")
+    ap.add_argument("--n-d", type=int, default=0,
+                    help="override the workload's N_d (kernel sweeps; 0: the workload's own)")
     ap.add_argument("--bulk-tile", type=int, default=0, help="bulk staging: elements per tile")
     ap.add_argument("--bulk-stages", type=int, default=0, help="bulk staging: ring depth")
     ap.add_argument("--gather-staging", choices=["default", "ldg", "bulk"], default="default",
@@ -556,6 +558,10 @@ def gpu_arm(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     w = W.workload(args.config)
+    if args.n_d:
+        import dataclasses
+        w = dataclasses.replace(w, n_d=args.n_d, name=f"{w.name} at N_d = {args.n_d}",
+                                bound_ranks=None, inject=None)
     if args.per_param:
         w = W.per_param_variant(w)
     if args.profile_unit is not None:

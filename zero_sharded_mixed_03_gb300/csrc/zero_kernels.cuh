@@ -527,6 +527,13 @@ constexpr int kBulkBarrierBytes = 256;                   // full[16] + empty[16]
 constexpr int kBulkMaxStages = 16;
 constexpr int kBulkMaxTile = 8192;
 constexpr uint64_t kDrainNs = 2000000000ull;             // bound on the final drain
+// Tiles of at most this many bulk copies (N_d + 3) are issued by lane 0 alone, in order; larger
+// ones by all 32 lanes of the producer warp.  Measured on GB300 (ragged ZeRO-2 step, fraction
+// of the copy bandwidth, one lane / 32 lanes): N_d = 7: 1.012 / 1.004, 8: 0.974 / 0.968,
+// 16: 1.036 / 1.030, 24: 1.024 / 1.017; 32: 0.939 / 0.965, 40: 0.944 / 0.983, 47: 0.942 /
+// 1.003, 48 (512-element tiles): 0.956 / 1.006.  From N_d = 32 on, one lane's sequential issue
+// of the tile's copies no longer keeps up.
+constexpr int kOneIssuerMaxCopies = 30;
 constexpr uint32_t kWaitIterCap = 1u << 26;              // polls per wait, whatever the clock
 
 __device__ __forceinline__ uint64_t global_ns()
@@ -818,86 +825,122 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_step_kernel(const __grid_co
                 if (e >= 0) d[e] = C.src[e];
             }
         }
-    } else if (lane == 0) {
+    } else if (P.n_d + 3 > kOneIssuerMaxCopies || lane == 0) {
+        // The producer: lane 0 waits for a free buffer and arms its barrier with the tile's byte
+        // count; the tile's N_d + 3 bulk copies are issued by lane 0 alone or, for tiles of
+        // many copies, by the 32 lanes of the warp between them.  Lane 0 alone then streams a
+        // gather (if any) and drains.
         const uint64_t policy = evict_first_policy();
         const uint32_t ring0 = full0 + kBulkBarrierBytes;
         const uint32_t cbytes = (uint32_t)P.tile * 2u, sbytes = (uint32_t)P.tile * 4u;
         int s = 0;
         int64_t base = 0;
         uint32_t k = 0;   // tiles issued
-        for (int64_t tile = blockIdx.x; tile < P.n_tiles; tile += gridDim.x, ++k) {
-            const TileRef T = locate_tile(P, tile, s, base);
-            const uint32_t st = k % (uint32_t)P.stages;
-            if (k >= (uint32_t)P.stages &&
-                !mbar_wait(empty0 + 8u * st, ((k / (uint32_t)P.stages) - 1u) & 1u, P.wait_ns)) {
-                err |= 1u;
-                break;
-            }
-            const KSeg& S = P.seg[s];
-            const uint32_t full = full0 + 8u * st;
-            const uint32_t dst = ring0 + st * stage_bytes;
-            const uint32_t len = (uint32_t)T.len;
-            mbar_arrive_expect_tx(full, len * (2u * (uint32_t)P.n_d + 12u));
-            for (int r = 0; r < P.n_d; ++r)
-                bulk_load(dst + (uint32_t)r * cbytes, P.c[r] + S.c_off + T.e0, 2u * len, full, policy);
-            const uint32_t sdst = dst + (uint32_t)P.n_d * cbytes;
-            bulk_load(sdst, S.p[cur] + T.e0, 4u * len, full, policy);
-            bulk_load(sdst + sbytes, S.m[cur] + T.e0, 4u * len, full, policy);
-            bulk_load(sdst + 2u * sbytes, S.v[cur] + T.e0, 4u * len, full, policy);
-        }
-        const uint32_t ns = (uint32_t)P.stages;
-        uint32_t used = k;   // ring buffers filled so far (tiles, then gather chunks)
-        if constexpr (HasGather<PT>::value) {
-            const int64_t grid = gridDim.x;
-            const int64_t rb = grid - 1 - blockIdx.x;
-            const int64_t mine = (!err && P.g_chunks > rb) ? (P.g_chunks - 1 - rb) / grid + 1 : 0;
-            GChunkWalk<PT> lw, sw;
-            int64_t lc = rb, sc = rb, issued = 0;
-            // load of gather chunk `issued` into ring use k + issued: its buffer held a tile
-            // (wait until the consumers release it) or the gather chunk ns uses before (whose
-            // store has read it: the caller waited for all but the newest store group)
-            auto issue = [&]() -> bool {
-                const uint32_t u = k + (uint32_t)issued, st = u % ns;
-                if (u >= ns && u - ns < k && !mbar_wait(empty0 + 8u * st, ((u / ns) - 1u) & 1u, P.wait_ns))
-                    return false;
-                const uint16_t* src;
-                uint16_t* dst;
-                const TileRef T = lw.at(P, lc, &src, &dst);
-                const uint32_t full = full0 + 8u * st;
-                mbar_arrive_expect_tx(full, 2u * (uint32_t)T.len);
-                bulk_load(ring0 + st * stage_bytes, src + T.e0, 2u * (uint32_t)T.len, full, policy);
-                lc += grid;
-                ++issued;
-                return true;
-            };
-            if (mine > 0 && !issue()) err |= 4u;
-            for (int64_t j = 0; j < mine && !err; ++j) {
-                const uint32_t u = k + (uint32_t)j, st = u % ns;
-                if (!mbar_wait(full0 + 8u * st, (u / ns) & 1u, P.wait_ns)) {
-                    err |= 4u;
+        if (P.n_d + 3 <= kOneIssuerMaxCopies) {
+            for (int64_t tile = blockIdx.x; tile < P.n_tiles; tile += gridDim.x, ++k) {
+                const TileRef T = locate_tile(P, tile, s, base);
+                const uint32_t st = k % (uint32_t)P.stages;
+                if (k >= (uint32_t)P.stages &&
+                    !mbar_wait(empty0 + 8u * st, ((k / (uint32_t)P.stages) - 1u) & 1u, P.wait_ns)) {
+                    err |= 1u;
                     break;
                 }
-                const uint16_t* src;
-                uint16_t* dst;
-                const TileRef T = sw.at(P, sc, &src, &dst);
-                bulk_store(dst + T.e0, ring0 + st * stage_bytes, 2u * (uint32_t)T.len, policy);
-                bulk_commit();
-                sc += grid;
-                if (issued < mine) {
-                    bulk_wait_read<1>();   // the store of chunk j - 1 has read its buffer
-                    if (!issue()) {
-                        err |= 4u;
-                        break;
+                const KSeg& S = P.seg[s];
+                const uint32_t full = full0 + 8u * st;
+                const uint32_t dst = ring0 + st * stage_bytes;
+                const uint32_t len = (uint32_t)T.len;
+                mbar_arrive_expect_tx(full, len * (2u * (uint32_t)P.n_d + 12u));
+                for (int r = 0; r < P.n_d; ++r)
+                    bulk_load(dst + (uint32_t)r * cbytes, P.c[r] + S.c_off + T.e0, 2u * len, full, policy);
+                const uint32_t sdst = dst + (uint32_t)P.n_d * cbytes;
+                bulk_load(sdst, S.p[cur] + T.e0, 4u * len, full, policy);
+                bulk_load(sdst + sbytes, S.m[cur] + T.e0, 4u * len, full, policy);
+                bulk_load(sdst + 2u * sbytes, S.v[cur] + T.e0, 4u * len, full, policy);
+            }
+        } else {
+            for (int64_t tile = blockIdx.x; tile < P.n_tiles; tile += gridDim.x, ++k) {
+                const TileRef T = locate_tile(P, tile, s, base);
+                const uint32_t st = k % (uint32_t)P.stages;
+                bool ok = true;
+                if (lane == 0 && k >= (uint32_t)P.stages)
+                    ok = mbar_wait(empty0 + 8u * st, ((k / (uint32_t)P.stages) - 1u) & 1u, P.wait_ns);
+                if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) {
+                    if (lane == 0) err |= 1u;
+                    break;
+                }
+                const KSeg& S = P.seg[s];
+                const uint32_t full = full0 + 8u * st;
+                const uint32_t dst = ring0 + st * stage_bytes;
+                const uint32_t len = (uint32_t)T.len;
+                if (lane == 0) mbar_arrive_expect_tx(full, len * (2u * (uint32_t)P.n_d + 12u));
+                __syncwarp();
+                const uint32_t sdst = dst + (uint32_t)P.n_d * cbytes;
+                for (int c = lane; c < P.n_d + 3; c += 32) {
+                    if (c < P.n_d) {
+                        bulk_load(dst + (uint32_t)c * cbytes, P.c[c] + S.c_off + T.e0, 2u * len, full, policy);
+                    } else {
+                        const int j = c - P.n_d;
+                        const float* src = j == 0 ? S.p[cur] : (j == 1 ? S.m[cur] : S.v[cur]);
+                        bulk_load(sdst + (uint32_t)j * sbytes, src + T.e0, 4u * len, full, policy);
                     }
                 }
             }
-            used = k + (uint32_t)issued;
         }
-        // Drain: the last phase issued on each buffer completes before the block returns, and
-        // so does every bulk store.
-        for (uint32_t j = used > ns ? used - ns : 0u; j < used; ++j)
-            if (!mbar_wait(full0 + 8u * (j % ns), (j / ns) & 1u, kDrainNs)) err |= 2u;
-        if constexpr (HasGather<PT>::value) bulk_wait_all();
+        if (lane == 0) {
+            const uint32_t ns = (uint32_t)P.stages;
+            uint32_t used = k;   // ring buffers filled so far (tiles, then gather chunks)
+            if constexpr (HasGather<PT>::value) {
+                const int64_t grid = gridDim.x;
+                const int64_t rb = grid - 1 - blockIdx.x;
+                const int64_t mine = (!err && P.g_chunks > rb) ? (P.g_chunks - 1 - rb) / grid + 1 : 0;
+                GChunkWalk<PT> lw, sw;
+                int64_t lc = rb, sc = rb, issued = 0;
+                // load of gather chunk `issued` into ring use k + issued: its buffer held a tile
+                // (wait until the consumers release it) or the gather chunk ns uses before (whose
+                // store has read it: the caller waited for all but the newest store group)
+                auto issue = [&]() -> bool {
+                    const uint32_t u = k + (uint32_t)issued, st = u % ns;
+                    if (u >= ns && u - ns < k && !mbar_wait(empty0 + 8u * st, ((u / ns) - 1u) & 1u, P.wait_ns))
+                        return false;
+                    const uint16_t* src;
+                    uint16_t* dst;
+                    const TileRef T = lw.at(P, lc, &src, &dst);
+                    const uint32_t full = full0 + 8u * st;
+                    mbar_arrive_expect_tx(full, 2u * (uint32_t)T.len);
+                    bulk_load(ring0 + st * stage_bytes, src + T.e0, 2u * (uint32_t)T.len, full, policy);
+                    lc += grid;
+                    ++issued;
+                    return true;
+                };
+                if (mine > 0 && !issue()) err |= 4u;
+                for (int64_t j = 0; j < mine && !err; ++j) {
+                    const uint32_t u = k + (uint32_t)j, st = u % ns;
+                    if (!mbar_wait(full0 + 8u * st, (u / ns) & 1u, P.wait_ns)) {
+                        err |= 4u;
+                        break;
+                    }
+                    const uint16_t* src;
+                    uint16_t* dst;
+                    const TileRef T = sw.at(P, sc, &src, &dst);
+                    bulk_store(dst + T.e0, ring0 + st * stage_bytes, 2u * (uint32_t)T.len, policy);
+                    bulk_commit();
+                    sc += grid;
+                    if (issued < mine) {
+                        bulk_wait_read<1>();   // the store of chunk j - 1 has read its buffer
+                        if (!issue()) {
+                            err |= 4u;
+                            break;
+                        }
+                    }
+                }
+                used = k + (uint32_t)issued;
+            }
+            // Drain: the last phase issued on each buffer completes before the block returns, and
+            // so does every bulk store.
+            for (uint32_t j = used > ns ? used - ns : 0u; j < used; ++j)
+                if (!mbar_wait(full0 + 8u * (j % ns), (j / ns) & 1u, kDrainNs)) err |= 2u;
+            if constexpr (HasGather<PT>::value) bulk_wait_all();
+        }
     }
     if (err) atomicOr(&P.st->error, err);
 
