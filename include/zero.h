@@ -295,7 +295,7 @@ zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_
  *                           register loads.  ZERO_STAGING_AUTO (default): the staged kernel where
  *                           its ring gives two resident blocks per SM with tiles of at least 512
  *                           elements, or three with 512-element tiles (on GB300 with the default
- *                           geometry: N_d = 4-11, 13-20 and 22-47, where it measured faster at all
+ *                           geometry: N_d = 4-11, 13-20 and 22-50, where it measured faster at all
  *                           but N_d = 10, 11 and 33), register loads elsewhere.  All give
  *                           identical results, bit for bit.  Launches whose streams do not
  *                           share one 16-byte phase use the scalar register-load path either
@@ -307,7 +307,8 @@ zero_status_t zero_read_state(zero_plan_t* plan, void* stream, zero_step_result_
  *                           word, its block drains its own copies in flight and returns.
  *   ZERO_OPT_BULK_TILE      elements per staged tile, a multiple of 8 in [8, 8192]; 0 (default):
  *                           the largest multiple of 512 up to 2048 with tile * (2 N_d + 12)
- *                           bytes within 53.5 KB (a power of two below 512 for N_d >= 48).
+ *                           bytes within 53.5 KB; 512 while that is within 56 KB (N_d <= 50);
+ *                           a power of two below 512 beyond.
  *   ZERO_OPT_BULK_STAGES    ring depth in [2, 16]; 0 (default): 2 (two blocks per SM).
  *   ZERO_OPT_GATHER_STAGING which kernel zero_gather_layer launches.  ZERO_STAGING_AUTO
  *                           (default) and ZERO_STAGING_BULK: one lane per block copies chunks
