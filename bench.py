@@ -42,15 +42,15 @@ ROTATE_SETS = 4
 # one ncu capture, per (workload, kernel), valid only for the kernel source it was taken on
 # (first 16 hex digits of the SHA-256 of zero_kernels.cuh, the device code); reported as null
 # once that source changes.
-MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("2f4a92a011191c99", 2_286_647_808),
+MEASURED_TRAFFIC = {(1, "bulk_step_kernel"): ("1087b358f163289b", 2_286_208_768),
                     # one launch captured (bucket 0 of 5), scaled by elements to the average
                     # launch the bench times
-                    (2, "bulk_step_kernel"): ("2f4a92a011191c99", 1_003_566_203),
+                    (2, "bulk_step_kernel"): ("1087b358f163289b", 1_003_294_020),
                     # the step launch that also gathers the next unit (one launch captured on
                     # a two-unit slice of the model, scaled by algorithmic bytes to the average
                     # launch of the full step)
-                    (3, "bulk_step_kernel + gather"): ("2f4a92a011191c99", 3_068_451_376),
-                    (4, "bulk_step_kernel + gather"): ("2f4a92a011191c99", 1_764_906_338)}
+                    (3, "bulk_step_kernel + gather"): ("1087b358f163289b", 3_068_613_361),
+                    (4, "bulk_step_kernel + gather"): ("1087b358f163289b", 1_765_648_613)}
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_03_gb300", "csrc", "zero_kernels.cuh")
 
 
