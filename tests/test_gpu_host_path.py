@@ -252,3 +252,53 @@ def test_host_path_errors():
     finally:
         torch.cuda.synchronize()
         run.close()
+
+
+def test_host_path_discarded_step_copies_the_recast_parameters():
+    """A barrier wait of the staged kernel that runs out (limit 0) discards the step: the
+    finish reports ZERO_ETIMEOUT, the state is unchanged, and the 16-bit parameters re-cast from
+    the unchanged master are copied to the host buffers again (the rejected update's values,
+    copied after the step, are overwritten).  The next step follows the oracle."""
+    w = dataclasses.replace(CASES["z2_nd8_fp16_buckets_skip"], wid=408, inject=None, steps=2)
+    run = H.Run(w, alloc_contribs=False, options={Z.ZERO_OPT_STAGING: Z.ZERO_STAGING_BULK})
+    o = H.OracleFull(w, run.bound)
+    try:
+        run.g.bind_host_staging()
+        calls = run.ranges()
+        host = [[torch.zeros(hi - lo, dtype=torch.int16, pin_memory=True) for _ in range(w.n_d)]
+                for (_w, lo, hi) in calls]
+        out = [torch.zeros(hi - lo, dtype=torch.int16, pin_memory=True) for (_w, lo, hi) in calls]
+
+        def step(k):
+            for ci, (which, lo, hi) in enumerate(calls):
+                for r in range(w.n_d):
+                    vals = H.fill_host(synth.grad_stream(w, k, r), run.units, lo, hi)
+                    host[ci][r].copy_(torch.from_numpy(vals.view(np.int16)))
+                run.g.step_host([t.data_ptr() for t in host[ci]], which, run.hyper, out[ci].data_ptr())
+            return run.g.finish_host()
+
+        res = step(1)
+        o.step(1)
+        assert res.t == 1
+        before = {r: run.read_logical(r) for r in run.bound}
+        run.g.set_option(Z.ZERO_OPT_WAIT_LIMIT_NS, 0)
+        with pytest.raises(Z.ZeroError) as e:
+            step(2)
+        assert e.value.status == Z.ZERO_ETIMEOUT
+        assert e.value.result.t == 1
+        for r in run.bound:
+            now = run.read_logical(r)
+            for key in now:
+                assert np.array_equal(now[key].view(np.uint32), before[r][key].view(np.uint32)), key
+        # the host holds the parameters of the state after step 1 (the oracle's)
+        for ci, (which, lo, hi) in enumerate(calls):
+            H.assert_16_close(out[ci].numpy().view(np.uint16), o.full16[lo:hi], f"after the discard, call {which}")
+        run.g.set_option(Z.ZERO_OPT_WAIT_LIMIT_NS, 1_000_000_000)
+        res = step(2)
+        o.step(2)
+        assert (res.t, res.skipped) == (2, 0)
+        H.compare_full(run, o, "host path after the discarded step")
+        for ci, (which, lo, hi) in enumerate(calls):
+            H.assert_16_close(out[ci].numpy().view(np.uint16), o.full16[lo:hi], f"step 2, call {which}")
+    finally:
+        run.close()
