@@ -428,6 +428,10 @@ class Bench:
         gb = self.gather_bufs()
         launches = 0
         n = len(self.calls)
+        if self.clip:                    # the norm over every unit before any step
+            for ci, (which, lo, hi) in enumerate(self.calls):
+                self.g.grad_norm(self.call_ptrs(bufs, ci), which)
+                launches += self.fused_launches[ci]
         if gather_events is not None:
             a, c = next(gather_events)
             a.record()
@@ -463,7 +467,7 @@ class Bench:
         events / gather_events: iterators of pre-created (start, end) CUDA event pairs recorded
         around each fused launch / gather launch.  Returns (result or None, kernel launches).
         """
-        if self.fused_gather and not self.clip:
+        if self.fused_gather:
             return self.step_fused(bufs, events, gather_events, wait)
         launches = 0
         if self.clip:
@@ -505,7 +509,7 @@ def measure(b, args, torch, overlap, comm, use_graph, dist, pairs, sample_clocks
     w = b.w
     n_calls = args.steps * len(b.calls)
     fused_pairs = pairs(n_calls, use_graph) if (not overlap and launch_events) else []
-    n_gathers = args.steps if b.fused_gather and not b.clip else n_calls
+    n_gathers = args.steps if b.fused_gather else n_calls
     gather_pairs = (pairs(n_gathers, use_graph)
                     if (w.stage == 3 and not overlap and launch_events) else [])
     ev_fused, ev_gather = iter(fused_pairs), iter(gather_pairs)
@@ -644,10 +648,13 @@ def gpu_arm(args, world, rank, local):
     if overlap:
         # the same steps with every unit's gather followed by its step on one stream: what the
         # second stream hides is the difference
+        # (timed without per-launch events, like the overlapped steps; the gathers' own time
+        # from the same serial steps with events around each launch)
         fg, b.fused_gather = b.fused_gather, False
-        ser = measure(b, args, torch, False, None, use_graph, dist, pairs)
+        ser = measure(b, args, torch, False, None, use_graph, dist, pairs, launch_events=False)
+        ser_i = measure(b, args, torch, False, None, use_graph, dist, pairs)
         b.fused_gather = fg
-        g_ms = sum(ser["gather_ms"]) / args.steps
+        g_ms = sum(ser_i["gather_ms"]) / args.steps
         hidden = ser["ms"] / args.steps - ms / args.steps
         frac = max(0.0, min(1.0, hidden / g_ms)) if g_ms > 0 else 0.0
         overlap_report = {"overlapped_ms_per_step": round(ms / args.steps, 3),
@@ -670,7 +677,7 @@ def gpu_arm(args, world, rank, local):
     # (+ 4 bytes per element of the unit a launch also gathers, in the fused schedule)
     per_launch_elems = elems / max(1, len(b.calls))
     launch_bytes = per_launch_elems * b.bytes_per_elem
-    fused_sched = b.fused_gather and not b.clip and not overlap
+    fused_sched = b.fused_gather and not overlap
     in_step_gather_bytes = 0
     if fused_sched and b.gather_in_step:
         in_step_gather_bytes = 4 * sum(b.units[c[0]][3] for c in b.calls[1:])
