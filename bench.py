@@ -757,10 +757,18 @@ def gpu_arm(args, world, rank, local):
     if overlap_report is not None:
         out["overlap"] = overlap_report
 
+    # the end-to-end and CPU legs report a failure in the line instead of losing it
     if not args.no_e2e and not w.offload:
-        out["e2e"] = e2e_leg(b, min(args.steps, 10), world, dist, ms / args.steps)
+        try:
+            out["e2e"] = e2e_leg(b, min(args.steps, 10), world, dist, ms / args.steps)
+        except Exception as exc:                      # e.g. pinned host memory not available
+            out["e2e"] = {"value": None, "unit": UNIT, "error": f"{type(exc).__name__}: {exc}"[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_elems)
+        try:
+            out["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_elems)
+        except Exception as exc:
+            out["cpu_baseline"] = {"value": None, "unit": UNIT, "kind": "oracle",
+                                   "error": f"{type(exc).__name__}: {exc}"[:300]}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
