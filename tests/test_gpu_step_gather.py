@@ -290,6 +290,16 @@ def test_wait_limit_runs_out_in_the_gather_part():
         run.close()
 
 
+def test_step_with_next_gather_edge_units():
+    """An empty unit as the next one (nothing to gather), and a per-parameter unit whose gather
+    has more copies (20 tensors x 16 ranks) than the wide parameter block holds: that launch
+    runs its gather separately, the others inside; results match the oracle either way."""
+    empty_next = _mk(511, [0, 40, 0, 0, 33, 1, 0], 16, units=(0, 2, 4))
+    _run_fused(empty_next, options=BULK, expect_fused=None)
+    many = _pp(512, 24, 16, 9, units=(0, 2, 22), max_rows=600)
+    _run_fused(many, options=BULK, expect_fused=None)
+
+
 def test_step_with_next_gather_and_clipping():
     """Clipping (norm pre-pass over every unit, then the clip-mode step): the step launches
     still carry the next unit's gather; states and the norm match the oracle."""
