@@ -162,6 +162,27 @@ def test_host_path_per_parameter_plan():
     _run_host(w, 1)
 
 
+SPLIT_CASES = {
+    # one call of 17.4M elements: cut into 2 pieces (a piece is at least 2^23 elements)
+    "z1_nd4_two_pieces": _mk(409, [9_000_001, 8_388_613, 777], 4, 1),
+    # one fp16 bucket of 25.2M elements over 3 ranks, 2 of them bound: 3 pieces, the cuts
+    # inside a rank's shard and across the unbound rank's; an inf at step 2 is skipped
+    "z2_nd3_fp16_three_pieces_skip": _mk(410, [12_582_917, 12_582_911, 100_003], 3, 2,
+                                         dtype=W.FP16, scaler=W.Scaler(), inject=(2, 1, 4_000_001),
+                                         bound=(0, 2)),
+    # one ZeRO-3 unit of 16.8M elements over 5 ranks: the call's range is the 5 shards
+    "z3_nd5_one_unit_two_pieces": _mk(411, [16_777_259], 5, 3, units=(0,)),
+}
+
+
+@pytest.mark.parametrize("name", list(SPLIT_CASES))
+def test_host_path_one_large_call_split_into_pieces(name):
+    """A host-buffer call that is the step's only call is cut into pieces of its range, each
+    piece's step launch and copy back running while the next piece is copied in; the results
+    and the byte counts are those of one call."""
+    _run_host(SPLIT_CASES[name], 1)
+
+
 def test_host_path_config2_pipelined_sampled():
     """The bucketed ZeRO-2 GPT-2-small workload at full size (fp16, 5 buckets of 25M, 8 ranks,
     loss scale 2^16) fed from host memory with the bucket copies pipelined, over its first four

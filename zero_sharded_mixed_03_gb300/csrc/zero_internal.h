@@ -181,7 +181,7 @@ struct zero_plan {
     zero::WorkerPool* host_pool = nullptr;   // the host update's threads (created on first use)
     // Steps fed from host memory (zero_step_host): two caller-owned device staging areas, the
     // elements between consecutive ranks' parts of an area, the plan's two copy streams and
-    // its events (created on first use: copied[2], used[2], recast done), the calls issued so
+    // its events (created on first use: copied[2], used[2], the last copy back), the calls issued so
     // far (call k uses area k % 2), and the open step's device->host copies (repeated after a
     // skipped step's re-cast) with its byte counts.
     struct HostCopy {
@@ -194,6 +194,7 @@ struct zero_plan {
     void* host_h2d = nullptr;
     void* host_d2h = nullptr;
     void* host_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    std::vector<void*> host_piece_events;   // copied / used of each piece of a split call
     int64_t host_calls = 0;
     bool host_step = false;
     int host_pipeline = 1;

@@ -714,6 +714,8 @@ void release_plan_resources(zero_plan* q)
             cudaEventDestroy((cudaEvent_t)ev);
             ev = nullptr;
         }
+    for (void* ev : q->host_piece_events) cudaEventDestroy((cudaEvent_t)ev);
+    q->host_piece_events.clear();
     for (void** st : {&q->host_h2d, &q->host_d2h})
         if (*st) {
             cudaStreamDestroy((cudaStream_t)*st);
@@ -793,7 +795,8 @@ cudaError_t launch_gather_list(const zero_plan* p, const std::vector<Copy>& copi
 zero_status_t enqueue_step(zero_plan* p, const void* const* grad_contribs, int64_t which,
                            const zero_hyper_t* hyper, cudaStream_t s,
                            const std::vector<Copy>* gather = nullptr, uint16_t* gather_dst = nullptr,
-                           bool* gather_fused = nullptr)
+                           bool* gather_fused = nullptr, const std::vector<Segment>* only = nullptr,
+                           bool mark = true)
 {
     zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
@@ -811,7 +814,9 @@ zero_status_t enqueue_step(zero_plan* p, const void* const* grad_contribs, int64
     int mode = kPlain;
     if (hyper->max_grad_norm > 0.0) mode = kClip;
     else if ((hyper->flags & ZERO_REPORT_GRAD_NORM) && !p->norm_open) mode = kNormAcc;
-    const std::vector<Segment> segs = step_segments(p, which, 0);
+    // only: a part of the call's work items (a host-buffer call split into pieces); mark = false
+    // leaves the call open for its remaining pieces
+    const std::vector<Segment> segs = only ? *only : step_segments(p, which, 0);
     const BulkCfg bulk = bulk_config(p);
     bool pending = gather && !gather->empty();
     if (gather_fused) *gather_fused = false;
@@ -870,6 +875,7 @@ zero_status_t enqueue_step(zero_plan* p, const void* const* grad_contribs, int64
     }
     if (lerr == cudaSuccess && pending) lerr = launch_gather_list(p, *gather, s);
     if (lerr != cudaSuccess) return cuda_fail(lerr, "fused step launch");
+    if (!mark) return ZERO_OK;
     p->in_step = true;
     if (which == -1) std::fill(p->covered.begin(), p->covered.end(), 1);
     else p->covered[(size_t)which] = 1;
@@ -920,6 +926,30 @@ bool pinned_host_cached(zero_plan* p, const void* q)
     if (p->host_pinned.size() >= 4096) p->host_pinned.clear();
     p->host_pinned.insert(q);
     return true;
+}
+
+// A host-buffer call that is the step's only call has no neighbour to overlap with; it is cut
+// into pieces of its range instead (at least kHostPieceElems elements each, at most
+// kHostMaxPieces), so that a piece's step and copy back run while the next piece is copied in.
+constexpr int64_t kHostPieceElems = 1 << 23;
+constexpr int kHostMaxPieces = 8;
+
+// The work items of `segs` that fall in [lo, hi) of the call's range, cut at its ends.
+std::vector<Segment> segments_in(const std::vector<Segment>& segs, int64_t lo, int64_t hi)
+{
+    std::vector<Segment> out;
+    for (const Segment& sg : segs) {
+        const int64_t a = std::max(lo, sg.c_off), e = std::min(hi, sg.c_off + sg.n);
+        if (a >= e) continue;
+        Segment t = sg;
+        const int64_t d = a - sg.c_off;
+        t.n = e - a;
+        t.c_off = a;
+        t.s_off = sg.s_off + d;
+        t.o_off = sg.o_off + d;
+        out.push_back(t);
+    }
+    return out;
 }
 
 // [lo, hi) element ranges of a call's range that its work items read from every contribution,
@@ -1778,46 +1808,74 @@ try {
     const int b = (int)(p->host_calls % 2);
     cudaEvent_t copied = (cudaEvent_t)p->host_events[b], used = (cudaEvent_t)p->host_events[2 + b];
     cudaEvent_t out_done = (cudaEvent_t)p->host_events[4];
+    // pieces: the call alone makes the step (nothing before or after it to overlap with)
+    // (runs are sorted and disjoint: the call reads [front.first, back.second))
+    const int64_t lo = runs.empty() ? 0 : runs.front().first;
+    const int64_t hi = runs.empty() ? 0 : runs.back().second;
+    int pieces = 1;
+    if (p->host_pipeline && !p->in_step && (which == -1 || p->n_buckets == 1))
+        pieces = (int)std::max<int64_t>(1, std::min<int64_t>(kHostMaxPieces, (hi - lo) / kHostPieceElems));
+    while (pieces > 1 && p->host_piece_events.size() < (size_t)(2 * pieces)) {
+        cudaEvent_t ev;
+        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: events");
+        p->host_piece_events.push_back(ev);
+        p->release_hook = release_plan_resources;
+    }
     // host -> device: after the step that last read this area (pipelined), or after everything
     // the previous call did, its device -> host copies included (serial)
     e = cudaStreamWaitEvent(h2d, p->host_pipeline ? used : out_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: ordering the copies");
     std::vector<const void*> dev(p->n_d);
-    int64_t h2d_bytes = 0;
-    for (int r = 0; r < p->n_d && e == cudaSuccess; ++r) {
-        uint16_t* area = (uint16_t*)p->host_staging[b] + (int64_t)r * p->host_rank_stride;
-        dev[(size_t)r] = area;
-        for (const auto& run : runs) {
-            const size_t bytes = 2 * (size_t)(run.second - run.first);
-            e = cudaMemcpyAsync(area + run.first, (const uint16_t*)host_contribs[r] + run.first, bytes,
-                                cudaMemcpyHostToDevice, h2d);
-            if (e != cudaSuccess) break;
-            h2d_bytes += (int64_t)bytes;
-        }
-    }
-    if (e == cudaSuccess) e = cudaEventRecord(copied, h2d);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: host-to-device copies");
-    st = enqueue_step(p, dev.data(), which, hyper, s);
-    if (st != ZERO_OK) return st;
-    // device -> host: the 16-bit results of the call, merged where both sides are contiguous
-    e = cudaEventRecord(used, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(d2h, used, 0);
+    for (int r = 0; r < p->n_d; ++r)
+        dev[(size_t)r] = (uint16_t*)p->host_staging[b] + (int64_t)r * p->host_rank_stride;
+    int64_t h2d_bytes = 0, d2h_bytes = 0;
     std::vector<zero_plan::HostCopy> outs;
-    for (const Segment& sg : segs) {
-        if (sg.n <= 0) continue;
-        uint16_t* h = (uint16_t*)host_out16 + sg.c_off;
-        const uint16_t* d = sg.out16 + sg.o_off;
-        if (!outs.empty() && outs.back().host + outs.back().n == h && outs.back().dev + outs.back().n == d)
-            outs.back().n += sg.n;
-        else
-            outs.push_back({h, d, sg.n});
+    for (int i = 0; i < pieces; ++i) {
+        // piece i: [plo, phi) of the call's range, cut at a multiple of 8 elements
+        const int64_t plo = i == 0 ? lo : (lo + (hi - lo) * i / pieces) / 8 * 8;
+        const int64_t phi = i + 1 == pieces ? hi : (lo + (hi - lo) * (i + 1) / pieces) / 8 * 8;
+        const std::vector<Segment> part = pieces == 1 ? segs : segments_in(segs, plo, phi);
+        const auto part_runs = pieces == 1 ? runs : read_runs(part);
+        cudaEvent_t pc = pieces == 1 ? copied : (cudaEvent_t)p->host_piece_events[(size_t)(2 * i)];
+        cudaEvent_t pu = pieces == 1 ? used : (cudaEvent_t)p->host_piece_events[(size_t)(2 * i + 1)];
+        for (int r = 0; r < p->n_d && e == cudaSuccess; ++r) {
+            uint16_t* area = (uint16_t*)dev[(size_t)r];
+            for (const auto& run : part_runs) {
+                const size_t bytes = 2 * (size_t)(run.second - run.first);
+                e = cudaMemcpyAsync(area + run.first, (const uint16_t*)host_contribs[r] + run.first, bytes,
+                                    cudaMemcpyHostToDevice, h2d);
+                if (e != cudaSuccess) break;
+                h2d_bytes += (int64_t)bytes;
+            }
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(pc, h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, pc, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: host-to-device copies");
+        st = enqueue_step(p, dev.data(), which, hyper, s, nullptr, nullptr, nullptr,
+                          pieces == 1 ? nullptr : &part, i + 1 == pieces);
+        if (st != ZERO_OK) return st;
+        // device -> host: the piece's 16-bit results, merged where both sides are contiguous
+        e = cudaEventRecord(pu, s);
+        if (e == cudaSuccess && pieces > 1 && i + 1 == pieces) e = cudaEventRecord(used, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(d2h, pu, 0);
+        const size_t first_out = outs.size();
+        for (const Segment& sg : part) {
+            if (sg.n <= 0) continue;
+            uint16_t* h = (uint16_t*)host_out16 + sg.c_off;
+            const uint16_t* d = sg.out16 + sg.o_off;
+            if (outs.size() > first_out && outs.back().host + outs.back().n == h && outs.back().dev + outs.back().n == d)
+                outs.back().n += sg.n;
+            else
+                outs.push_back({h, d, sg.n});
+        }
+        for (size_t j = first_out; j < outs.size() && e == cudaSuccess; ++j) {
+            e = cudaMemcpyAsync(outs[j].host, outs[j].dev, 2 * (size_t)outs[j].n, cudaMemcpyDeviceToHost, d2h);
+            d2h_bytes += 2 * outs[j].n;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: device-to-host copies");
     }
-    int64_t d2h_bytes = 0;
-    for (size_t i = 0; i < outs.size() && e == cudaSuccess; ++i) {
-        e = cudaMemcpyAsync(outs[i].host, outs[i].dev, 2 * (size_t)outs[i].n, cudaMemcpyDeviceToHost, d2h);
-        d2h_bytes += 2 * outs[i].n;
-    }
-    if (e == cudaSuccess) e = cudaEventRecord(out_done, d2h);
+    e = cudaEventRecord(out_done, d2h);
     if (e != cudaSuccess) return cuda_fail(e, "zero_step_host: device-to-host copies");
     p->host_outs.insert(p->host_outs.end(), outs.begin(), outs.end());
     p->host_h2d_bytes += h2d_bytes;
