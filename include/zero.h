@@ -518,10 +518,9 @@ zero_status_t zero_comm_report(const zero_plan_t* plan, zero_comm_report_t* out)
  * The call enqueues its work on `stream` and then synchronises `stream` to read the flag.
  *
  * Set-up: the first call on each device (in each CUDA context: a device reset makes a new
- * one) looks up the array's device address, with that device current, and caches it; make
- * that first call before any stream capture begins.  All calls share the one array: the flag
- * is cleared at the start of every call, and calls that overlap on the GPU (different
- * streams, threads or processes sharing the library) race on it.
+ * one) looks up the array's device address, with that device current, and caches it.  All
+ * calls share the one array: the flag is cleared at the start of every call, and calls that
+ * overlap on the GPU (different streams, threads or processes sharing the library) race on it.
  * Limits: n_d <= ZERO_MAX_RANKS (else ZERO_ERANGE); the call uses 4 of the
  * ZERO_NOALLOC_SCRATCH_BYTES bytes whatever n and n_d are.
  * --------------------------------------------------------------------------------------- */
