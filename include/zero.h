@@ -443,10 +443,14 @@ zero_status_t zero_offload_finish(zero_plan_t* plan, int threads, void* stream,
  * and the all-gather's result in host memory; "Overlapping Computation and Communication
  * Streams": the transfer of the next bucket runs while the current one is reduced and
  * updated). ----
- * Bind two device staging areas (caller-owned device memory, each at least
- * info.host_staging_bytes, 16-byte aligned, distinct) for zero_step_host.  Area k of a call
- * holds rank r's contribution at byte offset r * (info.host_staging_bytes / N_d).  Not inside
- * an open step; bind every rank first. */
+ * Bind two device staging areas of bytes_each bytes (caller-owned device memory, each at
+ * least info.host_staging_bytes, 16-byte aligned, not overlapping) for zero_step_host.  Area
+ * k of a call holds rank r's contribution at byte offset r * P, P = bytes_each / N_d rounded
+ * down to a multiple of 16.  info.host_staging_bytes gives P room for the largest bucket or
+ * unit; bucket -1 on a plan of several buckets or units needs P >= 2 * (its range), i.e.
+ * areas of N_d * 2 * R bytes, R = phi_pad rounded up to a multiple of 8 (stages 1/2).  Not inside an open step; bind every rank
+ * first.  ZERO_ERANGE if bytes_each < info.host_staging_bytes; ZERO_EINVAL if the areas
+ * overlap or are not device memory of the plan's device. */
 zero_status_t zero_bind_host_staging(zero_plan_t* plan, void* const staging[2], int64_t bytes_each);
 
 /* zero_step for bucket / unit `which` with host buffers:
@@ -468,6 +472,7 @@ zero_status_t zero_bind_host_staging(zero_plan_t* plan, void* const staging[2], 
  * Asynchronous: host_contribs must stay unchanged and host_out16 is
  * not final until zero_step_host_finish returns.  No clipping on this path (max_grad_norm
  * must be 0); ZERO_REPORT_GRAD_NORM is allowed.  ZERO_ESTATE without bound staging;
+ * ZERO_ERANGE (nothing enqueued) if the call's range does not fit a rank's part of the areas;
  * ZERO_EINVAL for NULL or unpinned host pointers and the argument errors of zero_step. */
 zero_status_t zero_step_host(zero_plan_t* plan, const void* const* host_contribs,
                              int64_t n_contribs, int64_t which, const zero_hyper_t* hyper,

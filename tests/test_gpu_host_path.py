@@ -183,6 +183,46 @@ def test_host_path_one_large_call_split_into_pieces(name):
     _run_host(SPLIT_CASES[name], 1)
 
 
+def test_host_path_bucket_minus_one_split_into_pieces():
+    """Bucket -1 on a plan of four buckets: the one call covers every bucket, and its pieces cut
+    across bucket, shard and tensor boundaries alike.  Staging areas of the minimum size hold
+    one bucket per rank: the call is refused with ZERO_ERANGE and nothing runs; areas of
+    N_d * 2 * phi_pad bytes (phi_pad rounded up to 8) take it."""
+    w = _mk(412, [6_000_011, 5_999_993, 4_194_304, 1_234_567], 4, 2, steps=2, bucket=4_500_000)
+    run = H.Run(w, alloc_contribs=False)
+    o = H.OracleFull(w, run.bound)
+    try:
+        assert len(run.ranges()) == 4
+        n = int(run.info.phi_pad)
+        host = [torch.zeros(n, dtype=torch.int16, pin_memory=True) for _ in range(w.n_d)]
+        out = torch.zeros(n, dtype=torch.int16, pin_memory=True)
+        run.g.bind_host_staging()
+        with pytest.raises(Z.ZeroError) as e:
+            run.g.step_host([t.data_ptr() for t in host], -1, run.hyper, out.data_ptr())
+        assert e.value.status == Z.ZERO_ERANGE
+        part = 2 * ((n + 7) // 8 * 8)                 # a rank's part: the range, whole 16 bytes
+        big = [torch.empty(w.n_d * part, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        with pytest.raises(Z.ZeroError) as e:         # 16 bytes short of the rank parts
+            Z.zero_bind_host_staging(run.g.plan, [t.data_ptr() for t in big], w.n_d * part - 16)
+            run.g.step_host([t.data_ptr() for t in host], -1, run.hyper, out.data_ptr())
+        assert e.value.status == Z.ZERO_ERANGE
+        Z.zero_bind_host_staging(run.g.plan, [t.data_ptr() for t in big], w.n_d * part)
+        for k in range(1, w.steps + 1):
+            for r in range(w.n_d):
+                vals = H.fill_host(synth.grad_stream(w, k, r), run.units, 0, n)
+                host[r].copy_(torch.from_numpy(vals.view(np.int16)))
+            run.g.step_host([t.data_ptr() for t in host], -1, run.hyper, out.data_ptr())
+            res = run.g.finish_host()
+            flag = o.step(k)
+            assert (res.skipped, res.t) == (flag, o.sc.t), f"step {k}"
+            H.compare_full(run, o, f"bucket -1 host step {k}")
+            H.assert_16_close(out.numpy().view(np.uint16), o.full16, f"bucket -1 host step {k} host16")
+            assert Z.zero_get_option(run.g.plan, Z.ZERO_OPT_HOST_H2D_BYTES) == 2 * w.n_d * n
+            assert Z.zero_get_option(run.g.plan, Z.ZERO_OPT_HOST_D2H_BYTES) == 2 * n
+    finally:
+        run.close()
+
+
 def test_host_path_config2_pipelined_sampled():
     """The bucketed ZeRO-2 GPT-2-small workload at full size (fp16, 5 buckets of 25M, 8 ranks,
     loss scale 2^16) fed from host memory with the bucket copies pipelined, over its first four

@@ -1761,8 +1761,7 @@ try {
     if (!aligned(staging[0], 16) || !aligned(staging[1], 16))
         return fail(ZERO_EALIGN, "zero_bind_host_staging: areas must be 16-byte aligned");
     const uintptr_t a = (uintptr_t)staging[0], b = (uintptr_t)staging[1];
-    const uintptr_t need = (uintptr_t)info.host_staging_bytes;
-    if (need > 0 && (a < b ? b - a : a - b) < need)
+    if (bytes_each > 0 && (a < b ? b - a : a - b) < (uintptr_t)bytes_each)
         return fail(ZERO_EINVAL, "zero_bind_host_staging: the two areas overlap");
     for (int i = 0; i < 2; ++i) {
         cudaPointerAttributes at;
@@ -1775,7 +1774,9 @@ try {
     }
     p->host_staging[0] = staging[0];
     p->host_staging[1] = staging[1];
-    p->host_rank_stride = (info.max_contrib_elems + 7) / 8 * 8;
+    // rank r's part starts r * (bytes_each / N_d, rounded down to 16 bytes) into an area: at
+    // least one bucket's or unit's range, whole-buffer calls (bucket -1) given larger areas
+    p->host_rank_stride = bytes_each / p->n_d / 16 * 8;
     return ZERO_OK;
 }
 catch (...) {
@@ -1793,6 +1794,9 @@ try {
     if (!aligned(host_out16, 2)) return fail(ZERO_EALIGN, "zero_step_host: host_out16 not 2-byte aligned");
     const std::vector<Segment> segs = step_segments(p, which, 0);
     const auto runs = read_runs(segs);
+    if (!runs.empty() && runs.back().second > p->host_rank_stride)
+        return fail(ZERO_ERANGE, "zero_step_host: the call's range exceeds a rank's part of the staging areas "
+                                 "(bucket -1 needs areas of N_d * 2 * phi_pad bytes, phi_pad rounded up to 8)");
     if (!segs.empty()) {
         if (!pinned_host_cached(p, host_out16))
             return fail(ZERO_EINVAL, "zero_step_host: host_out16 is not pinned host memory");
