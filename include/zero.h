@@ -382,9 +382,10 @@ zero_status_t zero_gather_layer(zero_plan_t* plan, int64_t unit, void* full_unit
  * call has more than 32 work items), each block's producer warp streams gather chunks through
  * its shared-memory ring after its last tile; otherwise the gather follows as its own launch
  * on `stream` (ZERO_OPT_LAST_GATHER_IN_STEP tells which).  Results are those of the two calls
- * made one after the other.  next_unit must differ from unit (the step writes unit's shards)
- * and next_full16 must not overlap any buffer of the plan.  The errors of zero_step and of
- * zero_gather_layer; next_unit stays gathered until zero_release_layer. */
+ * made one after the other.  unit must name one unit (not -1) and next_unit must differ from
+ * it (the step writes unit's shards), else ZERO_EINVAL; next_full16 must not overlap any buffer
+ * of the plan.  The errors of zero_step and of zero_gather_layer; next_unit stays gathered
+ * until zero_release_layer. */
 zero_status_t zero_step_gather_next(zero_plan_t* plan, const void* const* grad_contribs,
                                     int64_t n_contribs, int64_t unit, const zero_hyper_t* hyper,
                                     int64_t next_unit, void* next_full16, void* stream);

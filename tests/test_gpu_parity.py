@@ -532,6 +532,54 @@ def test_overlapped_schedule_argument_errors():
         run.close()
 
 
+@pytest.mark.parametrize("two_streams", [True, False])
+def test_overlapped_schedule_refuses_before_enqueuing(two_streams):
+    """A bad argument of any unit (a NULL contribution of the last unit, a unit left gathered, a
+    NULL gather buffer, betas out of range) is refused before anything is enqueued: no step is
+    left open and no unit gathered, and the next call runs the step the oracle expects."""
+    w = dataclasses.replace(SMALL_CASES["z3_nd16_units"], wid=196, steps=1)
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    comm = torch.cuda.Stream() if two_streams else None
+    nu = len(run.units)
+    bufs = [torch.empty(max(8, int(run.info.max_unit_pad)), dtype=torch.int16, device="cuda")
+            for _ in range(2)]
+    contribs = [[torch.empty(max(8, U[3]), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+                for U in run.units]
+    s = torch.cuda.current_stream().cuda_stream
+    cs = comm.cuda_stream if comm is not None else None
+    try:
+        for u, (which, lo, hi) in enumerate(run.ranges()):
+            for r in range(w.n_d):
+                H.fill_device(contribs[u][r], synth.grad_stream(w, 1, r), run.units, lo, hi)
+        ptrs = [c.data_ptr() for unit in contribs for c in unit]
+        gptrs = [b.data_ptr() for b in bufs]
+
+        def refused(status, ptrs=ptrs, gptrs=gptrs, hyper=run.hyper):
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_step_units_overlapped(run.g.plan, ptrs, gptrs, hyper, s, cs)
+            assert e.value.status == status
+            assert not run.g.step_state().t                        # nothing committed
+            with pytest.raises(Z.ZeroError) as e:                  # and no step open
+                Z.zero_step_finish(run.g.plan, s)
+            assert e.value.status == Z.ZERO_ESTATE
+
+        refused(Z.ZERO_EINVAL, ptrs=ptrs[:-1] + [0])               # last unit, last rank
+        refused(Z.ZERO_EINVAL, gptrs=[gptrs[0], 0])                # unit 1's buffer
+        refused(Z.ZERO_EALIGN, gptrs=[gptrs[0], gptrs[1] + 1])
+        refused(Z.ZERO_EINVAL, hyper=Z.hyper(beta1=1.0))
+        run.g.gather(nu - 1, bufs[0])
+        refused(Z.ZERO_ESTATE)                                     # a unit left gathered
+        run.g.release(nu - 1)
+        res = Z.zero_step_units_overlapped(run.g.plan, ptrs, gptrs, run.hyper, s, cs)
+        flag = o.step(1)
+        assert (res.skipped, res.t) == (flag, 1)
+        _compare_full(run, o, "overlapped schedule after refused calls")
+    finally:
+        torch.cuda.synchronize()
+        run.close()
+
+
 # ---------------------------------------------------------------------- FSDP-2 per-parameter plans
 
 def _pp(wid, n_t, n_d, seed, dtype=W.BF16, units=(0,), steps=3, scaler=None, inject=None,

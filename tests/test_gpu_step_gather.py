@@ -232,6 +232,9 @@ def test_step_with_next_gather_argument_errors():
             with pytest.raises(Z.ZeroError) as e:
                 run.g.step_gather_next(ptrs, 0, run.hyper, bad_next, buf)
             assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:                      # the whole step: it would
+            run.g.step_gather_next(ptrs, -1, run.hyper, 1, buf)    # update unit 1 as it gathers
+        assert e.value.status == Z.ZERO_EINVAL
         run.g.gather(1, buf)
         with pytest.raises(Z.ZeroError) as e:                      # still gathered
             run.g.step_gather_next(ptrs, 0, run.hyper, 1, buf)

@@ -737,6 +737,16 @@ cudaError_t offload_event(zero_plan* p, void** slot)
 }
 
 // Everything zero_step checks before it enqueues anything (shared with zero_step_host).
+// The hyperparameters every step call accepts.
+zero_status_t check_hyper(const zero_hyper_t* hyper, const char* fn)
+{
+    if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
+        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay) ||
+        !(hyper->max_grad_norm >= 0.0) || !std::isfinite(hyper->max_grad_norm))
+        return fail(ZERO_EINVAL, std::string(fn) + ": betas must lie in [0, 1); lr, eps, wd, max_grad_norm finite");
+    return ZERO_OK;
+}
+
 zero_status_t check_step(const zero_plan* p, const void* const* grad_contribs, int64_t n_contribs,
                          int64_t which, const zero_hyper_t* hyper, const char* fn)
 {
@@ -745,10 +755,8 @@ zero_status_t check_step(const zero_plan* p, const void* const* grad_contribs, i
     if (p && p->offload) return fail(ZERO_ESTATE, f + ": offloaded plan (zero_offload_step)");
     zero_status_t cst = check_call(p, grad_contribs, n_contribs, which, fn);
     if (cst != ZERO_OK) return cst;
-    if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
-        !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay) ||
-        !(hyper->max_grad_norm >= 0.0) || !std::isfinite(hyper->max_grad_norm))
-        return fail(ZERO_EINVAL, f + ": betas must lie in [0, 1); lr, eps, wd, max_grad_norm finite");
+    cst = check_hyper(hyper, fn);
+    if (cst != ZERO_OK) return cst;
     if (hyper->max_grad_norm > 0.0)
         for (int64_t b = 0; b < p->n_buckets; ++b)
             if (!p->norm_covered[(size_t)b])
@@ -1327,6 +1335,8 @@ try {
     zero_status_t st = check_step(p, grad_contribs, n_contribs, unit, hyper, "zero_step_gather_next");
     if (st != ZERO_OK) return st;
     if (p->stage != 3) return fail(ZERO_EINVAL, "zero_step_gather_next: stage 3 only");
+    // bucket -1 would update next_unit's shards in the launch that gathers them
+    if (unit < 0) return fail(ZERO_EINVAL, "zero_step_gather_next: unit must name one unit (not -1)");
     if (next_unit < 0 || next_unit >= (int64_t)p->units.size() || next_unit == unit)
         return fail(ZERO_EINVAL, "zero_step_gather_next: next_unit out of range or equal to unit");
     if (p->gathered[(size_t)next_unit]) return fail(ZERO_ESTATE, "zero_step_gather_next: next unit not released");
@@ -1941,9 +1951,28 @@ try {
     if (comm_stream && compute_stream == comm_stream)
         return fail(ZERO_EINVAL, "zero_step_units_overlapped: the two streams must differ");
     if (p->in_step) return fail(ZERO_ESTATE, "zero_step_units_overlapped: a step is open");
-    zero_status_t st = set_device(p);
-    if (st != ZERO_OK) return st;
     const int64_t nd = p->n_d;
+    // every argument the calls below check, checked before the first is enqueued, so a refused
+    // call leaves no step open and no unit gathered
+    zero_status_t st = check_hyper(hyper, "zero_step_units_overlapped");
+    if (st != ZERO_OK) return st;
+    for (int64_t u = 0; u < nu; ++u) {
+        st = check_call(p, unit_contribs + u * nd, nd, u, "zero_step_units_overlapped");
+        if (st != ZERO_OK) return st;
+        if (p->gathered[(size_t)u]) return fail(ZERO_ESTATE, "zero_step_units_overlapped: a unit is gathered");
+    }
+    for (int64_t u = 0; u < nu; ++u) {
+        const Unit& U = p->units[(size_t)u];
+        void* buf = gather_bufs[u % 2];
+        if (U.numel_pad > 0 && !buf) return fail(ZERO_EINVAL, "zero_step_units_overlapped: NULL gather buffer");
+        if (!aligned(buf, 2))
+            return fail(ZERO_EALIGN, "zero_step_units_overlapped: gather buffer not 2-byte aligned");
+        for (const Rank& R : p->ranks)
+            if (!R.shard16 && U.shard > 0)
+                return fail(ZERO_ESTATE, "zero_step_units_overlapped: a rank has no 16-bit shard bound");
+    }
+    st = set_device(p);
+    if (st != ZERO_OK) return st;
     if (!comm_stream) {
         // one stream: unit u+1's all-gather streams inside unit u's step launch
         if (hyper->max_grad_norm > 0.0)
