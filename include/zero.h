@@ -26,11 +26,11 @@
  *  - Calls that take a `stream` (a cudaStream_t passed as void*) are
  *    asynchronous on it, except zero_set_scaler, zero_read_state,
  *    zero_step_host_finish and zero_step_finish with a result pointer, which
- *    synchronise it.  The skip
- *    decision, the applied-step count t, the current ping-pong half and the
- *    loss scale live on the device (in the workspace), so a training loop
- *    enqueues step after step without waiting for the host.  Issue every call
- *    of one plan on one stream (or order the streams yourself).
+ *    synchronise it.  The skip decision, the applied-step count t, the current
+ *    ping-pong half and the loss scale live on the device (in the workspace),
+ *    so a training loop enqueues step after step without waiting for the host.
+ *    Issue every call of one plan on one stream (or order the streams
+ *    yourself).
  *  - Device pointers must be aligned to their element size (2 B for 16-bit
  *    data, 4 B for fp32, 16 B for the workspace); otherwise ZERO_EALIGN.  The
  *    128-bit vector path is used when every base pointer is 16-byte aligned and
