@@ -35,10 +35,10 @@ def _cuda():
 
 
 def _mk(wid, sizes, n_d, stage, steps=3, bucket=0, units=(), dtype=W.BF16, scaler=None,
-        outliers=False, inject=None, bound=None):
+        outliers=False, inject=None, bound=None, hyper=None):
     return W.Workload(wid=wid, name=f"host{wid}", sizes=tuple(sizes), n_d=n_d, stage=stage,
                       bucket_elems=bucket, unit_first=tuple(units), dtype=dtype, steps=steps,
-                      hyper=W.Hyper(), scaler=scaler, outliers=outliers, inject=inject,
+                      hyper=hyper or W.Hyper(), scaler=scaler, outliers=outliers, inject=inject,
                       bound_ranks=bound)
 
 
@@ -63,6 +63,9 @@ CASES = {
     "z3_nd16_units": _mk(405, _ragged(4, 24, 6000), 16, 3, units=(0, 5, 11, 17, 23)),
     # odd bucket size: the scalar path of the kernel on the staged contributions
     "z2_nd5_odd_bucket": _mk(406, _ragged(3, 30, 7000), 5, 2, bucket=12_345),
+    # the gradient norm reported over the buckets' calls
+    "z2_nd4_buckets_norm": _mk(414, _ragged(6, 30, 9000), 4, 2, bucket=30_000,
+                               hyper=W.Hyper(report_norm=True)),
 }
 
 
@@ -125,6 +128,9 @@ def _run_host(w, pipeline, one_call=False, options=None):
             flag = o.step(k)
             assert res.skipped == flag, f"step {k}"
             assert res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
+            if w.hyper.report_norm:                      # summed over every launch of the step
+                want = np.sqrt(o.norm2)
+                assert abs(res.grad_norm - want) <= 1e-12 * want, (k, res.grad_norm, want)
             H.compare_full(run, o, f"{w.name} host step {k}")
             for ci, (which, lo, hi) in enumerate(calls):
                 mask, want = _expected_host16(run, o, which, lo, hi)
@@ -172,6 +178,9 @@ SPLIT_CASES = {
                                          bound=(0, 2)),
     # one ZeRO-3 unit of 16.8M elements over 5 ranks: the call's range is the 5 shards
     "z3_nd5_one_unit_two_pieces": _mk(411, [16_777_259], 5, 3, units=(0,)),
+    # the gradient norm reported over the two pieces' launches
+    "z1_nd6_two_pieces_norm": _mk(413, [8_400_001, 8_388_611], 6, 1, steps=2,
+                                  hyper=W.Hyper(report_norm=True)),
 }
 
 
@@ -315,12 +324,14 @@ def test_host_path_errors():
         run.close()
 
 
-def test_host_path_discarded_step_copies_the_recast_parameters():
+@pytest.mark.parametrize("base", ["z2_nd8_fp16_buckets_skip", "z1_nd4_two_pieces"])
+def test_host_path_discarded_step_copies_the_recast_parameters(base):
     """A barrier wait of the staged kernel that runs out (limit 0) discards the step: the
     finish reports ZERO_ETIMEOUT, the state is unchanged, and the 16-bit parameters re-cast from
     the unchanged master are copied to the host buffers again (the rejected update's values,
-    copied after the step, are overwritten).  The next step follows the oracle."""
-    w = dataclasses.replace(CASES["z2_nd8_fp16_buckets_skip"], wid=408, inject=None, steps=2)
+    copied after the step, are overwritten).  The next step follows the oracle.  Four buckets
+    (four calls), and one call cut into two pieces."""
+    w = dataclasses.replace({**CASES, **SPLIT_CASES}[base], wid=408, inject=None, steps=2)
     run = H.Run(w, alloc_contribs=False, options={Z.ZERO_OPT_STAGING: Z.ZERO_STAGING_BULK})
     o = H.OracleFull(w, run.bound)
     try:
