@@ -151,6 +151,31 @@ def test_host_path_full_parity(name, pipeline):
     _run_host(CASES[name], pipeline)
 
 
+def test_host_path_tiny_case_sweep():
+    """Bounds of the copy lists: 80 random plans with phi <= 120, N_d 1..16, stages 1/2/3, bf16
+    and fp16, odd buckets, zero-size tensors and random subsets of the ranks bound, fed from
+    host memory pipelined and serial in turn; two steps each against the oracle (device state,
+    host results and byte counts)."""
+    rng = np.random.default_rng(61)
+    for trial in range(80):
+        nt = int(rng.integers(1, 7))
+        sizes = [int(x) for x in rng.integers(0, 21, size=nt)]
+        if sum(sizes) == 0:
+            sizes[0] = 1
+        n_d = int(rng.integers(1, 17))
+        stage = int(rng.integers(1, 4))
+        units = ()
+        if stage == 3 and nt > 1:
+            units = tuple([0] + sorted(set(int(x) for x in rng.integers(1, nt, size=2))))
+        bucket = int(rng.integers(0, 40)) if stage == 2 else 0
+        bound = None
+        if n_d > 1 and rng.integers(0, 2):
+            bound = tuple(sorted(set(int(x) for x in rng.integers(0, n_d, size=int(rng.integers(1, n_d))))))
+        w = _mk(600 + trial, sizes, n_d, stage, steps=2, bucket=bucket, units=units,
+                dtype=int(rng.integers(0, 2)), bound=bound)
+        _run_host(w, trial % 2)
+
+
 def test_host_path_one_call_over_the_whole_buffer():
     _run_host(CASES["z1_nd4_one_call"], 1, one_call=True)
 
