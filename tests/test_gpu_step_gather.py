@@ -118,6 +118,7 @@ def _run_fused(w, options=None, expect_fused=True, check_norm=False):
                 assert abs(res.grad_norm - want) <= 1e-12 * want, (res.grad_norm, want)
         if expect_fused is not None:
             assert all(x == (1 if expect_fused else 0) for x in in_step), in_step
+        return in_step
     finally:
         run.close()
 
@@ -130,6 +131,38 @@ def test_step_with_next_gather_full_parity(name):
 @pytest.mark.parametrize("name", ["nd16_units", "nd7_odd_shards"])
 def test_step_with_next_gather_automatic_choice(name):
     _run_fused(CASES[name])
+
+
+def test_step_with_next_gather_tiny_case_sweep():
+    """Bounds of the gather part: 60 random stage-3 plans, flat (phi <= 120) and per-parameter
+    (dim-0 rows <= 20), N_d 1..16, bf16 and fp16, zero-size tensors, random subsets of the
+    ranks bound; every unit gathered inside the previous unit's step launch where the kernel
+    takes it; two steps each against the oracle."""
+    rng = np.random.default_rng(62)
+    fused = 0
+    for trial in range(60):
+        nt = int(rng.integers(1, 8))
+        n_d = int(rng.integers(1, 17))
+        units = tuple([0] + sorted(set(int(x) for x in rng.integers(1, nt, size=3)))) if nt > 1 else (0,)
+        bound = None
+        if n_d > 1 and rng.integers(0, 2):
+            bound = tuple(sorted(set(int(x) for x in rng.integers(0, n_d, size=int(rng.integers(1, n_d))))))
+        dtype = int(rng.integers(0, 2))
+        if trial % 2:
+            dim0 = [int(x) for x in rng.integers(0, 21, size=nt)]
+            sizes = [d * int(c) for d, c in zip(dim0, rng.integers(1, 9, size=nt))]
+            w = W.Workload(wid=700 + trial, name=f"sgtiny{trial}", sizes=tuple(sizes), n_d=n_d,
+                           stage=3, bucket_elems=0, unit_first=units, dtype=dtype, steps=2,
+                           hyper=W.Hyper(), scaler=None, bound_ranks=bound, dim0=tuple(dim0),
+                           per_param=True)
+        else:
+            sizes = [int(x) for x in rng.integers(0, 21, size=nt)]
+            if sum(sizes) == 0:
+                sizes[0] = 1
+            w = dataclasses.replace(_mk(700 + trial, sizes, n_d, steps=2, units=units, bound=bound),
+                                    dtype=dtype)
+        fused += any(_run_fused(w, options=BULK, expect_fused=None))
+    assert fused >= 20, fused                  # most plans take the gather into the launch
 
 
 @pytest.mark.parametrize("name", ["nd16_units", "nd3_fp16_peers_skip_first", "pp_nd8_peers"])
