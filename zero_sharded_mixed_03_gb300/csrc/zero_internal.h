@@ -141,7 +141,7 @@ struct zero_plan {
     std::vector<char> norm_covered;     // per bucket / unit: gradient-norm pre-pass done
     bool norm_open = false;             // a norm pre-pass of the next step has been issued
     float consts[9] = {0};              // fp32 constants that do not depend on t or the scale
-    zero_hyper_t step_hyper = {0, 0, 0, 0, 0};
+    zero_hyper_t step_hyper = {};
     zero_scaler_t scaler = {1.0, 1.0, 1.0, 1.0, 0, 0};
     int scaler_dynamic = 0;
     std::vector<double> bias_host;      // the table last copied into the workspace
