@@ -471,13 +471,24 @@ zero_status_t zero_bind_host_staging(zero_plan_t* plan, void* const staging[2], 
  * bucket) is cut into pieces of its range instead (at least 2^23 elements each, at most 8),
  * each piece's step launch and copy back running while the next piece is copied in.
  * Asynchronous: host_contribs must stay unchanged and host_out16 is
- * not final until zero_step_host_finish returns.  No clipping on this path (max_grad_norm
- * must be 0); ZERO_REPORT_GRAD_NORM is allowed.  ZERO_ESTATE without bound staging;
+ * not final until zero_step_host_finish returns.  ZERO_REPORT_GRAD_NORM is allowed; clipping
+ * (max_grad_norm > 0) needs the norm pre-pass of every bucket/unit first (zero_grad_norm_host,
+ * or zero_grad_norm on device copies), as zero_step does.  ZERO_ESTATE without bound staging;
  * ZERO_ERANGE (nothing enqueued) if the call's range does not fit a rank's part of the areas;
  * ZERO_EINVAL for NULL or unpinned host pointers and the argument errors of zero_step. */
 zero_status_t zero_step_host(zero_plan_t* plan, const void* const* host_contribs,
                              int64_t n_contribs, int64_t which, const zero_hyper_t* hyper,
                              void* host_out16, void* stream);
+
+/* zero_grad_norm with host buffers: copies the slices of bucket / unit `which` the bound ranks
+ * read from pinned host memory (host_contribs as for zero_step_host) into the next staging
+ * area, in the same rotation and order as zero_step_host, and runs the norm pre-pass on
+ * `stream` over them.  For clipped steps fed from host memory: every bucket's norm call first,
+ * then the zero_step_host calls, which copy the gradients again (twice the host-to-device
+ * bytes of an unclipped step; the counters of ZERO_OPT_HOST_H2D_BYTES include both).  The
+ * errors of zero_grad_norm, and those of zero_step_host for the staging and host pointers. */
+zero_status_t zero_grad_norm_host(zero_plan_t* plan, const void* const* host_contribs,
+                                  int64_t n_contribs, int64_t which, void* stream);
 
 /* End a step that had zero_step_host calls: zero_step_finish on `stream`, then wait for every
  * device->host copy; if the step was skipped (or discarded, ZERO_ETIMEOUT) the re-cast 16-bit

@@ -108,12 +108,22 @@ def _run_host(w, pipeline, one_call=False, options=None):
         out = [torch.zeros(max(8, hi - lo), dtype=torch.int16, pin_memory=True)
                for (_w, lo, hi) in calls]
         gbuf = run.gather_buf
+        clip = w.hyper.max_grad_norm > 0
         for k in range(1, w.steps + 1):
             expect_h2d = expect_d2h = 0
+            if clip:                             # every call's norm pre-pass from host memory first
+                for ci, (which, lo, hi) in enumerate(calls):
+                    for r in range(w.n_d):
+                        vals = H.fill_host(synth.grad_stream(w, k, r), run.units, lo, hi)
+                        host[ci][r][:hi - lo].copy_(torch.from_numpy(vals.view(np.int16)))
+                    run.g.grad_norm_host([t.data_ptr() for t in host[ci]], -1 if one_call else which)
+                    mask, _ = _expected_host16(run, o, which, lo, hi)
+                    expect_h2d += 2 * w.n_d * int(mask.sum())
             for ci, (which, lo, hi) in enumerate(calls):
-                for r in range(w.n_d):
-                    vals = H.fill_host(synth.grad_stream(w, k, r), run.units, lo, hi)
-                    host[ci][r][:hi - lo].copy_(torch.from_numpy(vals.view(np.int16)))
+                if not clip:
+                    for r in range(w.n_d):
+                        vals = H.fill_host(synth.grad_stream(w, k, r), run.units, lo, hi)
+                        host[ci][r][:hi - lo].copy_(torch.from_numpy(vals.view(np.int16)))
                 if w.stage == 3:
                     run.g.gather(which, gbuf)
                     run.g.release(which)
@@ -128,9 +138,12 @@ def _run_host(w, pipeline, one_call=False, options=None):
             flag = o.step(k)
             assert res.skipped == flag, f"step {k}"
             assert res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
-            if w.hyper.report_norm:                      # summed over every launch of the step
+            if w.hyper.report_norm or clip:             # summed over every launch of the step
                 want = np.sqrt(o.norm2)
-                assert abs(res.grad_norm - want) <= 1e-12 * want, (k, res.grad_norm, want)
+                if np.isfinite(want):
+                    assert abs(res.grad_norm - want) <= 1e-12 * want, (k, res.grad_norm, want)
+                else:                                    # a non-finite gradient: no norm
+                    assert not np.isfinite(res.grad_norm), (k, res.grad_norm)
             H.compare_full(run, o, f"{w.name} host step {k}")
             for ci, (which, lo, hi) in enumerate(calls):
                 mask, want = _expected_host16(run, o, which, lo, hi)
@@ -191,6 +204,26 @@ def test_host_path_per_parameter_plan():
                    hyper=W.Hyper(), scaler=None, dim0=(12, 5, 40, 2, 8), per_param=True,
                    bound_ranks=(0, 3))
     _run_host(w, 1)
+
+
+CLIP_CASES = {
+    # clipped steps fed from host memory: the norm pre-pass of every call, then the steps
+    "z2_nd8_fp16_buckets_clip_skip": _mk(415, _ragged(16, 40, 9000), 8, 2, steps=4, bucket=10_000,
+                                         dtype=W.FP16, scaler=W.Scaler(), outliers=True,
+                                         inject=(2, 5, 33_333), hyper=W.Hyper(max_grad_norm=1e-6)),
+    "z3_nd16_units_clip": _mk(416, _ragged(17, 24, 6000), 16, 3, units=(0, 5, 11, 17, 23),
+                              hyper=W.Hyper(max_grad_norm=0.02)),
+    "z1_nd4_two_pieces_clip": _mk(417, [9_000_001, 8_388_613], 4, 1, steps=2,
+                                  hyper=W.Hyper(max_grad_norm=0.05)),
+}
+
+
+@pytest.mark.parametrize("pipeline", [1, 0])
+@pytest.mark.parametrize("name", list(CLIP_CASES))
+def test_host_path_clipping_full_parity(name, pipeline):
+    """zero_grad_norm_host over every call, then the clipped zero_step_host calls: states,
+    host results, the reported norm and the byte counts (the gradients cross the link twice)."""
+    _run_host(CLIP_CASES[name], pipeline)
 
 
 SPLIT_CASES = {
@@ -344,6 +377,43 @@ def test_host_path_errors():
         assert e.value.status == Z.ZERO_ESTATE
         res = run.g.finish_host()
         assert res.t == 1 and res.skipped == 0
+    finally:
+        torch.cuda.synchronize()
+        run.close()
+
+
+def test_host_norm_pass_errors():
+    w = CASES["z2_nd5_odd_bucket"]
+    run = H.Run(w, alloc_contribs=False)
+    try:
+        plan = run.g.plan
+        which, lo, hi = run.ranges()[0]
+        host = [torch.zeros(hi - lo, dtype=torch.int16, pin_memory=True) for _ in range(w.n_d)]
+        out = torch.zeros(hi - lo, dtype=torch.int16, pin_memory=True)
+        ptrs = [t.data_ptr() for t in host]
+        with pytest.raises(Z.ZeroError) as e:                    # no staging bound
+            Z.zero_grad_norm_host(plan, ptrs, which)
+        assert e.value.status == Z.ZERO_ESTATE
+        run.g.bind_host_staging()
+        pageable = np.zeros(hi - lo, dtype=np.uint16)
+        with pytest.raises(Z.ZeroError) as e:                    # contributions must be pinned
+            Z.zero_grad_norm_host(plan, [pageable.ctypes.data] + ptrs[1:], which)
+        assert e.value.status == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:                    # one pointer per rank
+            Z.zero_grad_norm_host(plan, ptrs[1:], which)
+        assert e.value.status == Z.ZERO_EINVAL
+        Z.zero_grad_norm_host(plan, ptrs, which)
+        with pytest.raises(Z.ZeroError) as e:                    # the same bucket twice
+            Z.zero_grad_norm_host(plan, ptrs, which)
+        assert e.value.status == Z.ZERO_ESTATE
+        clip = Z.hyper(max_grad_norm=1.0)
+        with pytest.raises(Z.ZeroError) as e:                    # clipping needs every bucket's norm
+            Z.zero_step_host(plan, ptrs, which, clip, out.data_ptr())
+        assert e.value.status == Z.ZERO_ESTATE
+        Z.zero_step_host(plan, ptrs, which, Z.hyper(), out.data_ptr())
+        with pytest.raises(Z.ZeroError) as e:                    # the norm must precede the steps
+            Z.zero_grad_norm_host(plan, ptrs, run.ranges()[1][0])
+        assert e.value.status == Z.ZERO_ESTATE
     finally:
         torch.cuda.synchronize()
         run.close()

@@ -36,7 +36,7 @@ EXPORTED = ["zero_plan_create", "zero_plan_create_per_param", "zero_plan_info", 
             "zero_read_state", "zero_restore_state", "zero_grad_norm",
             "zero_step_units_overlapped", "zero_bind_offload", "zero_offload_step",
             "zero_offload_finish", "zero_set_option", "zero_get_option",
-            "zero_bind_host_staging", "zero_step_host", "zero_step_host_finish",
+            "zero_bind_host_staging", "zero_step_host", "zero_step_host_finish", "zero_grad_norm_host",
             "zero_step_gather_next",
             "zero_last_error", "zero_plan_destroy", "zero_step_range_noalloc"]
 ZERO_NOALLOC_SCRATCH_BYTES = 256
@@ -148,6 +148,8 @@ def lib() -> ctypes.CDLL:
         L.zero_bind_host_staging.argtypes = [_vp, _vp, _i64]
         L.zero_step_host.restype = st
         L.zero_step_host.argtypes = [_vp, _vp, _i64, _i64, ctypes.POINTER(zero_hyper_t), _vp, _vp]
+        L.zero_grad_norm_host.restype = st
+        L.zero_grad_norm_host.argtypes = [_vp, _vp, _i64, _i64, _vp]
         L.zero_step_host_finish.restype = st
         L.zero_step_host_finish.argtypes = [_vp, _vp, ctypes.POINTER(zero_step_result_t)]
         L.zero_grad_norm.restype = st
@@ -321,6 +323,11 @@ def zero_step_host(plan: int, host_contribs: Sequence[int], which: int, hyper: z
                    host_out16: int, stream: int = 0) -> None:
     _check(lib().zero_step_host(plan, _ptr_array(host_contribs), len(host_contribs), which,
                                 ctypes.byref(hyper), host_out16 or None, stream or None))
+
+
+def zero_grad_norm_host(plan: int, host_contribs: Sequence[int], which: int, stream: int = 0) -> None:
+    _check(lib().zero_grad_norm_host(plan, _ptr_array(host_contribs), len(host_contribs), which,
+                                     stream or None))
 
 
 def zero_step_host_finish(plan: int, stream: int = 0) -> zero_step_result_t:

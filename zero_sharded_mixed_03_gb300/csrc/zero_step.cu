@@ -1272,21 +1272,32 @@ catch (...) {
     return exception_status("zero_get_option");
 }
 
-zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
-                             int64_t which, void* stream)
-try {
-    zero_status_t st = check_call(p, grad_contribs, n_contribs, which, "zero_grad_norm");
+}  // extern "C"
+
+namespace zero {
+namespace {
+
+// The checks of a gradient-norm pre-pass call (fn: the entry point's name).
+zero_status_t check_norm_call(const zero_plan* p, const void* const* grad_contribs, int64_t n_contribs,
+                              int64_t which, const char* fn)
+{
+    const std::string f(fn);
+    zero_status_t st = check_call(p, grad_contribs, n_contribs, which, fn);
     if (st != ZERO_OK) return st;
-    if (p->in_step)
-        return fail(ZERO_ESTATE, "zero_grad_norm: the norm must precede every zero_step of a step");
+    if (p->in_step) return fail(ZERO_ESTATE, f + ": the norm must precede every zero_step of a step");
     if (which == -1) {
-        if (p->norm_open) return fail(ZERO_ESTATE, "zero_grad_norm: bucket -1 must be the only call");
+        if (p->norm_open) return fail(ZERO_ESTATE, f + ": bucket -1 must be the only call");
     } else if (p->norm_covered[(size_t)which]) {
-        return fail(ZERO_ESTATE, "zero_grad_norm: bucket/unit already included");
+        return fail(ZERO_ESTATE, f + ": bucket/unit already included");
     }
-    st = set_device(p);
+    return ZERO_OK;
+}
+
+// Launch the norm pre-pass of bucket/unit `which` over device contributions on `s`.
+zero_status_t enqueue_norm(zero_plan* p, const void* const* grad_contribs, int64_t which, cudaStream_t s)
+{
+    zero_status_t st = set_device(p);
     if (st != ZERO_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
     const std::vector<Segment> segs = step_segments(p, which, 0);
     auto run = [&](auto& P, size_t cap) -> cudaError_t {
         for (size_t b = 0; b < segs.size(); b += cap) {
@@ -1312,6 +1323,19 @@ try {
     if (which == -1) std::fill(p->norm_covered.begin(), p->norm_covered.end(), 1);
     else p->norm_covered[(size_t)which] = 1;
     return ZERO_OK;
+}
+
+}  // namespace
+}  // namespace zero
+
+extern "C" {
+
+zero_status_t zero_grad_norm(zero_plan_t* p, const void* const* grad_contribs, int64_t n_contribs,
+                             int64_t which, void* stream)
+try {
+    const zero_status_t st = check_norm_call(p, grad_contribs, n_contribs, which, "zero_grad_norm");
+    if (st != ZERO_OK) return st;
+    return enqueue_norm(p, grad_contribs, which, (cudaStream_t)stream);
 }
 catch (...) {
     return exception_status("zero_grad_norm");
@@ -1793,13 +1817,66 @@ catch (...) {
     return exception_status("zero_bind_host_staging");
 }
 
+zero_status_t zero_grad_norm_host(zero_plan_t* p, const void* const* host_contribs, int64_t n_contribs,
+                                  int64_t which, void* stream)
+try {
+    zero_status_t st = check_norm_call(p, host_contribs, n_contribs, which, "zero_grad_norm_host");
+    if (st != ZERO_OK) return st;
+    if (!p->host_staging[0])
+        return fail(ZERO_ESTATE, "zero_grad_norm_host: no staging bound (zero_bind_host_staging)");
+    const std::vector<Segment> segs = step_segments(p, which, 0);
+    const auto runs = read_runs(segs);
+    if (!runs.empty() && runs.back().second > p->host_rank_stride)
+        return fail(ZERO_ERANGE, "zero_grad_norm_host: the call's range exceeds a rank's part of the staging areas");
+    if (!segs.empty())
+        for (int r = 0; r < p->n_d; ++r)
+            if (!pinned_host_cached(p, host_contribs[r]))
+                return fail(ZERO_EINVAL, "zero_grad_norm_host: a contribution is not pinned host memory");
+    st = set_device(p);
+    if (st != ZERO_OK) return st;
+    cudaError_t e = host_resources(p);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_grad_norm_host: copy streams");
+    cudaStream_t s = (cudaStream_t)stream, h2d = (cudaStream_t)p->host_h2d;
+    const int b = (int)(p->host_calls % 2);
+    cudaEvent_t copied = (cudaEvent_t)p->host_events[b], used = (cudaEvent_t)p->host_events[2 + b];
+    cudaEvent_t out_done = (cudaEvent_t)p->host_events[4];
+    // the same staging rotation and ordering as zero_step_host
+    e = cudaStreamWaitEvent(h2d, p->host_pipeline ? used : out_done, 0);
+    std::vector<const void*> dev(p->n_d);
+    int64_t h2d_bytes = 0;
+    for (int r = 0; r < p->n_d && e == cudaSuccess; ++r) {
+        dev[(size_t)r] = (uint16_t*)p->host_staging[b] + (int64_t)r * p->host_rank_stride;
+        for (const auto& run : runs) {
+            const size_t bytes = 2 * (size_t)(run.second - run.first);
+            e = cudaMemcpyAsync((uint16_t*)dev[(size_t)r] + run.first, (const uint16_t*)host_contribs[r] + run.first,
+                                bytes, cudaMemcpyHostToDevice, h2d);
+            if (e != cudaSuccess) break;
+            h2d_bytes += (int64_t)bytes;
+        }
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(copied, h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_grad_norm_host: host-to-device copies");
+    st = enqueue_norm(p, dev.data(), which, s);
+    if (st != ZERO_OK) return st;
+    // the area is free again once the pass has read it (serial: the next call waits for it)
+    e = cudaEventRecord(used, s);
+    if (e == cudaSuccess) e = cudaEventRecord(out_done, s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero_grad_norm_host: ordering the copies");
+    p->host_h2d_bytes += h2d_bytes;
+    ++p->host_calls;
+    return ZERO_OK;
+}
+catch (...) {
+    return exception_status("zero_grad_norm_host");
+}
+
 zero_status_t zero_step_host(zero_plan_t* p, const void* const* host_contribs, int64_t n_contribs,
                              int64_t which, const zero_hyper_t* hyper, void* host_out16, void* stream)
 try {
     zero_status_t st = check_step(p, host_contribs, n_contribs, which, hyper, "zero_step_host");
     if (st != ZERO_OK) return st;
     if (!p->host_staging[0]) return fail(ZERO_ESTATE, "zero_step_host: no staging bound (zero_bind_host_staging)");
-    if (hyper->max_grad_norm != 0.0) return fail(ZERO_EINVAL, "zero_step_host: no clipping on this path");
     if (!host_out16) return fail(ZERO_EINVAL, "zero_step_host: NULL host_out16");
     if (!aligned(host_out16, 2)) return fail(ZERO_EALIGN, "zero_step_host: host_out16 not 2-byte aligned");
     const std::vector<Segment> segs = step_segments(p, which, 0);

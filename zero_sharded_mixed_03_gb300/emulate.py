@@ -19,7 +19,7 @@ from . import (ZERO_BF16, zero_set_option, ZERO_TABLE_PARAM_CHUNKS, ZERO_TABLE_S
                zero_grad_norm, zero_plan_tables, zero_rank_state_elems, zero_read_state,
                zero_release_layer,
                zero_set_scaler, zero_step, zero_step_finish,
-               zero_bind_host_staging, zero_step_host, zero_step_host_finish,
+               zero_bind_host_staging, zero_step_host, zero_step_host_finish, zero_grad_norm_host,
                zero_step_gather_next)
 
 
@@ -174,6 +174,10 @@ class EmulatedGroup:
         """zero_step with the contributions and the 16-bit result in pinned host memory."""
         zero_step_host(self.plan, list(host_contribs), which, hyper, host_out16,
                        _stream_handle(stream))
+
+    def grad_norm_host(self, host_contribs: Sequence[int], which: int, stream=None) -> None:
+        """Gradient-norm pre-pass of one bucket/unit fed from pinned host memory."""
+        zero_grad_norm_host(self.plan, list(host_contribs), which, _stream_handle(stream))
 
     def finish_host(self, stream=None):
         """End a step with host-buffer calls (synchronises); returns the step state."""
