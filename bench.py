@@ -780,8 +780,8 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
     zero_step_host copies that call's contributions from pinned host memory into a device
     staging area (the next call's copies run while this call's step does), runs the step and
     copies the updated 16-bit parameters back into pinned host memory; (stage 3: the unit's
-    all-gather first;) zero_step_host_finish ends the step, waits for the copies and reads the
-    step state.  Host gradients: two pinned sets of N_d buffers of the largest call's range,
+    all-gather first; with clipping, zero_grad_norm_host over every call before the steps;)
+    zero_step_host_finish ends the step, waits for the copies and reads the step state.  Host gradients: two pinned sets of N_d buffers of the largest call's range,
     used by alternate calls (every byte crosses the host->device link every step; a set is
     far larger than the host CPU's caches).  The same steps with the library's serial schedule
     (ZERO_OPT_HOST_PIPELINE = 0: each call's copies, step and copy back one after another)
@@ -813,6 +813,9 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
 
     def one_step():
         t = time.perf_counter()
+        if b.clip:                       # clipping: every call's norm pre-pass from host memory first
+            for ci, (which, lo, hi) in enumerate(b.calls):
+                g.grad_norm_host([t.data_ptr() for t in host_sets[ci % 2]], which)
         for ci, (which, lo, hi) in enumerate(b.calls):
             if w.stage == 3:
                 g.gather(which, b.run.gather_buf)
@@ -851,7 +854,8 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
     hidden_frac = max(0.0, min(1.0, hidden_ms / device_ms_per_step)) if device_ms_per_step > 0 else 0.0
     return {"value": job_value(b.elems_per_step, applied, world, el), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h) + 96,
-            "steps": steps, "api": "zero_step_host / zero_step_host_finish",
+            "steps": steps,
+            "api": ("zero_grad_norm_host / " if b.clip else "") + "zero_step_host / zero_step_host_finish",
             "host_link_gbs": round((h2d + d2h) / (ms / 1e3) / 1e9, 1),
             "host_enqueue_ms_per_step": round(enqueue_ms, 3),
             "overlap": {"pipelined_ms_per_step": round(ms, 3),
