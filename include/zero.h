@@ -423,7 +423,11 @@ zero_status_t zero_bind_offload(zero_plan_t* plan, int rank, float* master, floa
  * contributions, scaling and non-finite flag) and writes the averaged gradient into the bound
  * ranks' grad_host.  It first runs the reduction for the non-finite flag alone (no writes),
  * then the writing reduction in groups of segments of at least 4M elements, an event after
- * each group.  No gradient-norm options. */
+ * each group.  Clipping (max_grad_norm > 0) needs zero_grad_norm over every bucket/unit
+ * first (ZERO_ESTATE otherwise); the finish then scales each gradient by the coefficient
+ * min(1, max_grad_norm / (norm + 1e-6)), formed in double as the GPU step forms it and
+ * rounded once to fp32.  ZERO_REPORT_GRAD_NORM is refused (ZERO_EINVAL): with clipping the
+ * norm is reported anyway. */
 zero_status_t zero_offload_step(zero_plan_t* plan, const void* const* grad_contribs,
                                 int64_t n_contribs, int64_t which, const zero_hyper_t* hyper,
                                 void* stream);

@@ -1,7 +1,9 @@
 // Host-side check of the offloaded update's pipeline (zero_offload.cpp), no GPU involved:
 // cpu_adamw_overlapped with groups released one by one (with random delays) must give the
 // bits of cpu_adamw, hand back every 16-bit element exactly once in span order, and stop
-// cleanly when a wait gives up.  Built and run by tests/test_offload_host.py.
+// cleanly when a wait gives up; with a clipping coefficient, the update must equal the plain
+// update of gradients scaled by that coefficient beforehand (one fp32 multiply each).  Built
+// and run by tests/test_offload_host.py.
 #include <chrono>
 #include <cmath>
 #include <cstdio>
@@ -53,13 +55,30 @@ std::vector<CpuSpan> spans_of(Buffers& b, const std::vector<int64_t>& sizes)
 }
 
 int check(zero::WorkerPool* pool, const std::vector<int64_t>& sizes, const std::vector<int>& groups,
-          int dtype16, int threads, int fail_at, uint32_t seed)
+          int dtype16, int threads, int fail_at, uint32_t seed, float coef = 1.0f)
 {
     int64_t n = 0;
     for (int64_t x : sizes) n += x;
     Buffers a = make(n, seed), b = make(n, seed);
     const float k[9] = {0.9f, 0.1f, 0.999f, 0.001f, 1e-8f, 1e-5f, 1e-3f, 0.0316f, 0.0f};
-    zero::cpu_adamw(pool, spans_of(a, sizes), k, dtype16, false, threads);
+    zero::cpu_adamw(pool, spans_of(a, sizes), k, dtype16, false, threads, coef);
+    if (coef != 1.0f) {
+        // the clipped update is the plain update of the pre-scaled gradient
+        Buffers c = make(n, seed);
+        for (int64_t i = 0; i < n; ++i) c.g[i] = c.g[i] * coef;
+        zero::cpu_adamw(pool, spans_of(c, sizes), k, dtype16, false, threads, 1.0f);
+        if (std::memcmp(a.p.data(), c.p.data(), 4 * n) != 0 || std::memcmp(a.v.data(), c.v.data(), 4 * n) != 0 ||
+            std::memcmp(a.out.data(), c.out.data(), 2 * n) != 0) {
+            std::printf("FAIL: the clipped update differs from the update of scaled gradients\n");
+            return 1;
+        }
+        Buffers u = make(n, seed);                     // and it does change the result
+        zero::cpu_adamw(pool, spans_of(u, sizes), k, dtype16, false, threads, 1.0f);
+        if (std::memcmp(a.p.data(), u.p.data(), 4 * n) == 0) {
+            std::printf("FAIL: the clipping coefficient had no effect\n");
+            return 1;
+        }
+    }
     std::vector<CpuSpan> sb = spans_of(b, sizes);
     std::mt19937 rng(seed + 1);
     int next_group = 0;
@@ -71,7 +90,7 @@ int check(zero::WorkerPool* pool, const std::vector<int64_t>& sizes, const std::
     std::vector<int64_t> base(sizes.size(), 0);
     for (size_t i = 1; i < sizes.size(); ++i) base[i] = base[i - 1] + sizes[i - 1];
     const bool ok = zero::cpu_adamw_overlapped(
-        pool, sb, groups, k, dtype16, threads,
+        pool, sb, groups, k, dtype16, threads, coef,
         [&](int g) {
             order_ok &= g == next_group++;
             std::this_thread::sleep_for(std::chrono::microseconds(rng() % 3000));
@@ -133,6 +152,9 @@ int main()
     bad += check(pool, {3000000}, {0}, ZERO_BF16, 16, -1, 4);
     bad += check(pool, {100000, 100000, 100000, 100000}, {0, 1, 2, 3}, ZERO_FP16, 3, 2, 5);
     bad += check(pool, {100000, 100000}, {0, 1}, ZERO_BF16, 2, 0, 6);
+    // a clipping coefficient, in the plain and the overlapped update alike
+    bad += check(pool, {5, 70000, 1, 200000, 65536, 3}, {0, 0, 0, 1, 2, 2}, ZERO_BF16, 4, -1, 7, 0.37f);
+    bad += check(pool, {1 << 20, 777777}, {0, 1}, ZERO_FP16, 8, -1, 8, 1e-3f);
     for (uint32_t r = 0; r < 20; ++r)
         bad += check(pool, {70000 + 1000 * r, 65536, 9}, {0, 1, 1}, r % 2 ? ZERO_FP16 : ZERO_BF16,
                      1 + (int)r % 12, r % 5 == 4 ? 1 : -1, 100 + r);

@@ -680,6 +680,44 @@ def test_offload_deferred_reductions_full_parity(name):
         run.close()
 
 
+@pytest.mark.parametrize("defer", [0, 1])
+@pytest.mark.parametrize("name", ["z1_nd4_clip", "z2_nd8_fp16_buckets_clip_skip", "z3_nd16_units_clip"])
+def test_offload_clipping_full_parity(name, defer):
+    """ZeRO-Offload with clipping: the GPU norm pre-pass over every bucket/unit, then the
+    reductions to host memory; the host threads scale each gradient by the coefficient formed
+    from the step's norm with the GPU's double operations before the update.  Against the
+    oracle bit for bit, with the reported norm; stream-ordered and deferred reductions."""
+    w = dataclasses.replace(CLIP_CASES[name], wid=CLIP_CASES[name].wid + 50, offload=True)
+    run = H.Run(w, alloc_contribs=False, options={Z.ZERO_OPT_OFFLOAD_DEFER: defer})
+    o = H.OracleFull(w, run.bound)
+    calls = run.ranges()
+    # every call keeps its own contribution buffers until the finish (deferred reductions)
+    bufs = [[torch.empty(max(8, hi - lo), dtype=torch.int16, device="cuda") for _ in range(w.n_d)]
+            for (_w, lo, hi) in calls]
+    try:
+        for k in range(1, w.steps + 1):
+            for ci, (which, lo, hi) in enumerate(calls):
+                for r in range(w.n_d):
+                    H.fill_device(bufs[ci][r], synth.grad_stream(w, k, r), run.units, lo, hi)
+                run.g.grad_norm([t.data_ptr() for t in bufs[ci]], which)
+            for ci, (which, lo, hi) in enumerate(calls):
+                if w.stage == 3:
+                    run.g.gather(which, run.gather_buf)
+                    run.g.release(which)
+                run.g.step([t.data_ptr() for t in bufs[ci]], which, run.hyper)
+            res = run.g.finish()
+            flag = o.step(k)
+            assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale, k
+            want = np.sqrt(o.norm2)
+            if np.isfinite(want):
+                assert abs(res.grad_norm - want) <= 1e-12 * want, (res.grad_norm, want)
+            else:
+                assert not np.isfinite(res.grad_norm)
+            assert _compare_full(run, o, f"offload {name} step {k}") == 0
+    finally:
+        run.close()
+
+
 def test_offload_worker_threads_end_with_the_plan():
     """An offloaded plan keeps its host worker threads between steps and ends them in
     zero_plan_destroy: the process's thread count returns to where it was."""

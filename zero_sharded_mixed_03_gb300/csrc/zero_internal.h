@@ -57,9 +57,10 @@ void worker_pool_destroy(WorkerPool* pool);
 int worker_pool_size(const WorkerPool* pool);
 
 // CPU AdamW (or, for a skipped step, the re-cast of the unchanged master) over the spans, on
-// `threads` workers of `pool` (at most its size); k = the nine fp32 step constants.
+// `threads` workers of `pool` (at most its size); k = the nine fp32 step constants, coef = the
+// gradient-clipping coefficient (1: none).
 void cpu_adamw(WorkerPool* pool, const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
-               bool skipped, int threads);
+               bool skipped, int threads, float coef = 1.0f);
 
 // The same update while the gradient is still arriving, in groups of spans (group_of_span,
 // non-decreasing): on the calling thread, wait_group(g) is called for g = 0, 1, ... and
@@ -69,7 +70,7 @@ void cpu_adamw(WorkerPool* pool, const std::vector<CpuSpan>& spans, const float 
 // false if a callback gave up; every thread has stopped by then.
 bool cpu_adamw_overlapped(WorkerPool* pool, const std::vector<CpuSpan>& spans,
                           const std::vector<int>& group_of_span, const float k[9], int dtype16, int threads,
-                          const std::function<bool(int)>& wait_group,
+                          float coef, const std::function<bool(int)>& wait_group,
                           const std::function<bool(size_t, int64_t, int64_t)>& copied);
 
 // Elementwise work item of one launch: n elements of one rank's shard.

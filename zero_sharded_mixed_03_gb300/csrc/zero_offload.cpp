@@ -72,8 +72,10 @@ inline uint16_t to_fp16(float f)
     return (uint16_t)(sign | h);
 }
 
-template <bool FP16>
-void adamw_span(const CpuSpan& s, const float* k)
+// CLIP: the gradient is scaled by the clipping coefficient first (one fp32 multiply, as the
+// GPU step does in clip mode).
+template <bool FP16, bool CLIP>
+void adamw_span(const CpuSpan& s, const float* k, float coef)
 {
     const float b1 = k[0], omb1 = k[1], b2 = k[2], omb2 = k[3], eps = k[4], lrwd = k[5];
     const float step = k[6], bc2s = k[7];
@@ -83,7 +85,7 @@ void adamw_span(const CpuSpan& s, const float* k)
     const float* __restrict g = s.grad;
     uint16_t* __restrict out = s.out16;
     for (int64_t i = 0; i < s.n; ++i) {
-        const float gi = g[i];
+        const float gi = CLIP ? g[i] * coef : g[i];
         const float mi = b1 * m[i] + omb1 * gi;
         const float vi = b2 * v[i] + omb2 * (gi * gi);
         const float d = std::sqrt(vi) / bc2s + eps;
@@ -179,8 +181,22 @@ WorkerPool* worker_pool_create(int threads) { return new WorkerPool(std::max(1, 
 void worker_pool_destroy(WorkerPool* pool) { delete pool; }
 int worker_pool_size(const WorkerPool* pool) { return pool ? pool->size() : 0; }
 
+// The update of one piece: clip coefficient 1 (no clipping, or a norm within the bound) leaves
+// the gradient as it is, exactly as a multiply by 1 would.
+void adamw_piece(const CpuSpan& q, const float* k, int dtype16, float coef)
+{
+    if (coef != 1.0f) {
+        if (dtype16 == ZERO_FP16) adamw_span<true, true>(q, k, coef);
+        else adamw_span<false, true>(q, k, coef);
+    } else if (dtype16 == ZERO_FP16) {
+        adamw_span<true, false>(q, k, 1.0f);
+    } else {
+        adamw_span<false, false>(q, k, 1.0f);
+    }
+}
+
 void cpu_adamw(WorkerPool* pool, const std::vector<CpuSpan>& spans, const float k[9], int dtype16,
-               bool skipped, int threads)
+               bool skipped, int threads, float coef)
 {
     // Cut the spans into pieces of ~64K elements and deal them to the threads in turn.
     std::vector<CpuSpan> pieces;
@@ -202,10 +218,8 @@ void cpu_adamw(WorkerPool* pool, const std::vector<CpuSpan>& spans, const float 
             if (skipped) {
                 if (dtype16 == ZERO_FP16) recast_span<true>(q);
                 else recast_span<false>(q);
-            } else if (dtype16 == ZERO_FP16) {
-                adamw_span<true>(q, k);
             } else {
-                adamw_span<false>(q, k);
+                adamw_piece(q, k, dtype16, coef);
             }
         }
     };
@@ -215,7 +229,7 @@ void cpu_adamw(WorkerPool* pool, const std::vector<CpuSpan>& spans, const float 
 
 bool cpu_adamw_overlapped(WorkerPool* pool, const std::vector<CpuSpan>& spans,
                           const std::vector<int>& group_of_span, const float k[9], int dtype16, int threads,
-                          const std::function<bool(int)>& wait_group,
+                          float coef, const std::function<bool(int)>& wait_group,
                           const std::function<bool(size_t, int64_t, int64_t)>& copied)
 {
     // Pieces of ~64K elements in span order; the threads take them in that order (one shared
@@ -256,8 +270,7 @@ bool cpu_adamw_overlapped(WorkerPool* pool, const std::vector<CpuSpan>& spans,
             q.grad += pc.off;
             q.out16 += pc.off;
             q.n = pc.n;
-            if (dtype16 == ZERO_FP16) adamw_span<true>(q, k);
-            else adamw_span<false>(q, k);
+            adamw_piece(q, k, dtype16, coef);
             done[(size_t)i].store(1, std::memory_order_release);
             n_done.fetch_add(1, std::memory_order_release);
             progress_cv.notify_one();

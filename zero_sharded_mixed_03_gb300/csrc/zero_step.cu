@@ -1621,8 +1621,13 @@ try {
     if (!(hyper->beta1 >= 0.0 && hyper->beta1 < 1.0) || !(hyper->beta2 >= 0.0 && hyper->beta2 < 1.0) ||
         !std::isfinite(hyper->lr) || !std::isfinite(hyper->eps) || !std::isfinite(hyper->weight_decay))
         return fail(ZERO_EINVAL, "zero_offload_step: betas must lie in [0, 1); lr, eps, wd finite");
-    if (hyper->max_grad_norm != 0.0 || hyper->flags != 0)
-        return fail(ZERO_EINVAL, "zero_offload_step: no gradient-norm options on the offload path");
+    if (hyper->flags != 0) return fail(ZERO_EINVAL, "zero_offload_step: no norm report on the offload path");
+    if (!(hyper->max_grad_norm >= 0.0) || !std::isfinite(hyper->max_grad_norm))
+        return fail(ZERO_EINVAL, "zero_offload_step: max_grad_norm must be finite and >= 0");
+    if (hyper->max_grad_norm > 0.0)
+        for (int64_t b = 0; b < p->n_buckets; ++b)
+            if (!p->norm_covered[(size_t)b])
+                return fail(ZERO_ESTATE, "zero_offload_step: clipping needs zero_grad_norm over every bucket/unit first");
     if (p->in_step && std::memcmp(&p->step_hyper, hyper, sizeof(*hyper)) != 0)
         return fail(ZERO_EINVAL, "zero_offload_step: hyperparameters changed inside a step");
     if (which == -1) {
@@ -1698,6 +1703,14 @@ try {
     if (e != cudaSuccess) return cuda_fail(e, "zero_offload_finish: reading the step state");
     float k9[9];
     step_constants(p->step_hyper, host.t + 1, host.scale, p->n_d, k9);
+    // clipping: the coefficient from the step's norm, with the double operations of the GPU
+    // step's clip mode (correctly rounded sqrt, add, divide; rounded once to fp32)
+    float coef = 1.0f;
+    if (p->step_hyper.max_grad_norm > 0.0) {
+        double c = p->step_hyper.max_grad_norm / (std::sqrt(host.norm2) + 1e-6);
+        if (c > 1.0) c = 1.0;
+        coef = (float)c;
+    }
     // deferred reductions (ZERO_OPT_OFFLOAD_DEFER): the decision is known; a clean step streams
     // every call's gradient to the host now, a skipped one needs none of it
     if (!p->off_deferred.empty()) {
@@ -1747,7 +1760,7 @@ try {
         // the update of each group starts once its gradient has landed; finished ranges of
         // 16-bit parameters are copied back while the rest is still being updated
         const bool ok = cpu_adamw_overlapped(
-            p->host_pool, spans, group_of_span, k9, p->dtype16, nt,
+            p->host_pool, spans, group_of_span, k9, p->dtype16, nt, coef,
             [&](int grp) {
                 e = cudaEventSynchronize((cudaEvent_t)p->off_events[(size_t)grp]);
                 return e == cudaSuccess;
@@ -1771,7 +1784,9 @@ try {
     if (e != cudaSuccess) return cuda_fail(e, "commit launch");
     p->in_step = false;
     p->stepped = true;
+    p->norm_open = false;
     std::fill(p->covered.begin(), p->covered.end(), 0);
+    std::fill(p->norm_covered.begin(), p->norm_covered.end(), 0);
     if (out) return read_state(p, s, out);
     return ZERO_OK;
 }
