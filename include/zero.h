@@ -74,8 +74,8 @@ typedef struct zero_plan zero_plan_t;
  * global gradient norm: max_grad_norm > 0 clips the averaged, unscaled gradient g by
  * fp32(min(1, max_grad_norm / (norm + 1e-6))), norm = sqrt(sum of fp32(g*g) in double), which
  * needs zero_grad_norm (or zero_grad_norm_host) over every bucket/unit of the step first;
- * flags & ZERO_REPORT_GRAD_NORM
- * computes the norm inside the fused pass for reporting (no clipping, no extra pass). */
+ * flags & ZERO_REPORT_GRAD_NORM computes the norm inside the fused pass for reporting (no
+ * clipping, no extra pass). */
 typedef struct {
     double lr, beta1, beta2, eps, weight_decay;
     double max_grad_norm;    /* 0: no clipping */
