@@ -156,6 +156,16 @@ def test_config_sampled_parity(i):
     print(f"{W.workload(i).name}: {n} sampled elements, {mism} bit mismatches (within tolerance)")
 
 
+@pytest.mark.parametrize("i,steps", [(1, 64), (2, 40)])
+def test_config_sampled_long_run(i, steps):
+    """Many steps at full size (the ragged ZeRO-2 workload; the fp16 GPT-2 workload with its
+    loss scale and the skipped step 3): sampled state, parameters, t, skips and the scale
+    after every step, so that nothing drifts as the bias correction and the moments evolve."""
+    w = dataclasses.replace(W.workload(i), steps=steps)
+    n, mism = _run_sampled(w)
+    print(f"{w.name}, {steps} steps: {n} sampled elements, {mism} bit mismatches (within tolerance)")
+
+
 def test_config4_rank0_and_last_rank_sampled():
     w = W.workload(4)
     n, mism = _run_sampled(w, bound=(0, w.n_d - 1))
