@@ -473,7 +473,7 @@ zero_status_t zero_bind_host_staging(zero_plan_t* plan, void* const staging[2], 
  * and copies the 16-bit results to host_out16 on a second stream of its own after the step.
  * With ZERO_OPT_HOST_PIPELINE = 1 (default) the copies of the next call therefore run while
  * this call's step does; a call that is the step's only call (bucket -1, or the plan's one
- * bucket) is cut into pieces of its range instead (at least 2^23 elements each, at most 8),
+ * bucket) is cut into pieces of its range instead (at least 2^24 elements each, at most 8),
  * each piece's step launch and copy back running while the next piece is copied in.
  * Asynchronous: host_contribs must stay unchanged and host_out16 is
  * not final until zero_step_host_finish returns.  ZERO_REPORT_GRAD_NORM is allowed; clipping

@@ -139,9 +139,13 @@ def _run_host(w, pipeline, one_call=False, options=None):
             assert res.skipped == flag, f"step {k}"
             assert res.t == o.sc.t and res.scale == o.sc.scale, f"step {k}"
             if w.hyper.report_norm or clip:             # summed over every launch of the step
+                # The GPU sums fp32(g*g) per thread as an error-free pair of floats and the
+                # block partials in double; the oracle sums them in double in flat order.  Both
+                # stay within about n * 2^-53 of the exact sum; over these sizes (<= 34M
+                # elements) 1e-10 of the norm bounds the difference.
                 want = np.sqrt(o.norm2)
                 if np.isfinite(want):
-                    assert abs(res.grad_norm - want) <= 1e-12 * want, (k, res.grad_norm, want)
+                    assert abs(res.grad_norm - want) <= 1e-10 * want, (k, res.grad_norm, want)
                 else:                                    # a non-finite gradient: no norm
                     assert not np.isfinite(res.grad_norm), (k, res.grad_norm)
             H.compare_full(run, o, f"{w.name} host step {k}")
@@ -213,7 +217,7 @@ CLIP_CASES = {
                                          inject=(2, 5, 33_333), hyper=W.Hyper(max_grad_norm=1e-6)),
     "z3_nd16_units_clip": _mk(416, _ragged(17, 24, 6000), 16, 3, units=(0, 5, 11, 17, 23),
                               hyper=W.Hyper(max_grad_norm=0.02)),
-    "z1_nd4_two_pieces_clip": _mk(417, [9_000_001, 8_388_613], 4, 1, steps=2,
+    "z1_nd4_two_pieces_clip": _mk(417, [17_000_001, 16_777_259], 4, 1, steps=2,
                                   hyper=W.Hyper(max_grad_norm=0.05)),
 }
 
@@ -227,17 +231,17 @@ def test_host_path_clipping_full_parity(name, pipeline):
 
 
 SPLIT_CASES = {
-    # one call of 17.4M elements: cut into 2 pieces (a piece is at least 2^23 elements)
-    "z1_nd4_two_pieces": _mk(409, [9_000_001, 8_388_613, 777], 4, 1),
-    # one fp16 bucket of 25.2M elements over 3 ranks, 2 of them bound: 3 pieces, the cuts
+    # one call of 33.8M elements: cut into 2 pieces (a piece is at least 2^24 elements)
+    "z1_nd4_two_pieces": _mk(409, [17_000_001, 16_777_259, 777], 4, 1),
+    # one fp16 bucket of 50.4M elements over 3 ranks, 2 of them bound: 3 pieces, the cuts
     # inside a rank's shard and across the unbound rank's; an inf at step 2 is skipped
-    "z2_nd3_fp16_three_pieces_skip": _mk(410, [12_582_917, 12_582_911, 100_003], 3, 2,
-                                         dtype=W.FP16, scaler=W.Scaler(), inject=(2, 1, 4_000_001),
+    "z2_nd3_fp16_three_pieces_skip": _mk(410, [25_165_837, 25_165_831, 100_003], 3, 2,
+                                         dtype=W.FP16, scaler=W.Scaler(), inject=(2, 1, 8_000_001),
                                          bound=(0, 2)),
-    # one ZeRO-3 unit of 16.8M elements over 5 ranks: the call's range is the 5 shards
-    "z3_nd5_one_unit_two_pieces": _mk(411, [16_777_259], 5, 3, units=(0,)),
+    # one ZeRO-3 unit of 33.6M elements over 5 ranks: the call's range is the 5 shards
+    "z3_nd5_one_unit_two_pieces": _mk(411, [33_554_467], 5, 3, units=(0,)),
     # the gradient norm reported over the two pieces' launches
-    "z1_nd6_two_pieces_norm": _mk(413, [8_400_001, 8_388_611], 6, 1, steps=2,
+    "z1_nd6_two_pieces_norm": _mk(413, [16_800_001, 16_777_259], 6, 1, steps=2,
                                   hyper=W.Hyper(report_norm=True)),
 }
 
@@ -255,7 +259,7 @@ def test_host_path_bucket_minus_one_split_into_pieces():
     across bucket, shard and tensor boundaries alike.  Staging areas of the minimum size hold
     one bucket per rank: the call is refused with ZERO_ERANGE and nothing runs; areas of
     N_d * 2 * phi_pad bytes (phi_pad rounded up to 8) take it."""
-    w = _mk(412, [6_000_011, 5_999_993, 4_194_304, 1_234_567], 4, 2, steps=2, bucket=4_500_000)
+    w = _mk(412, [12_000_011, 11_999_993, 8_388_608, 1_234_567], 4, 2, steps=2, bucket=9_000_000)
     run = H.Run(w, alloc_contribs=False)
     o = H.OracleFull(w, run.bound)
     try:

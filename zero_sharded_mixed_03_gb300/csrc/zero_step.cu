@@ -939,7 +939,9 @@ bool pinned_host_cached(zero_plan* p, const void* q)
 // A host-buffer call that is the step's only call has no neighbour to overlap with; it is cut
 // into pieces of its range instead (at least kHostPieceElems elements each, at most
 // kHostMaxPieces), so that a piece's step and copy back run while the next piece is copied in.
-constexpr int64_t kHostPieceElems = 1 << 23;
+// (GB300, the 58M-element ragged ZeRO-2 step over 7 ranks: 4.39 ms a step with pieces of at
+// least 2^24 elements (3), 4.48 ms with 2^23 (6), 5.0-5.2 ms with 2^22-2^21, 4.8 ms with two.)
+constexpr int64_t kHostPieceElems = 1 << 24;
 constexpr int kHostMaxPieces = 8;
 
 // The work items of `segs` that fall in [lo, hi) of the call's range, cut at its ends.
