@@ -101,6 +101,9 @@ def parse_args():
                     help="stage 3: fused (default): unit u's step launch also gathers unit u+1 "
                          "(zero_step_gather_next; unit 0 is gathered on its own); serial: every "
                          "unit's gather as a launch of its own before its step")
+    ap.add_argument("--unit-order", choices=["asc", "desc"], default="asc",
+                    help="stage 3: step the units first to last (default), or last to first as "
+                         "a backward pass produces their gradients (ZERO_OPT_UNIT_ORDER)")
     ap.add_argument("--staging", choices=["auto", "ldg", "bulk"], default=DEFAULT_STAGING,
                     help="bulk: cp.async.bulk (TMA) staging of the contribution and state tiles "
                          "into shared memory; ldg: 128-bit register loads; auto (default): the "
@@ -277,7 +280,7 @@ class Bench:
     """A workload bound to the product API with pre-generated contribution sets."""
 
     def __init__(self, w, mem_budget_gb: float, n_sets_wanted: int, grad_norm: str = "off",
-                 options=None, fused_gather: bool = False):
+                 options=None, fused_gather: bool = False, unit_order: str = "asc"):
         import torch
         import synth
         import zero_sharded_mixed_03_gb300 as Z
@@ -296,6 +299,11 @@ class Bench:
         self.bound = self.run.bound
         self.all_bound = len(self.bound) == w.n_d
         self.calls = self.run.ranges()
+        if unit_order == "desc" and w.stage == 3:
+            # last unit first: the order of every per-call loop below, the compact contribution
+            # layout included; the whole-step call takes the same order as an option
+            self.calls = self.calls[::-1]
+            self.g.set_option(Z.ZERO_OPT_UNIT_ORDER, 1)
         # Contribution layout of one step: for each call the slices the bound ranks read.
         # All ranks bound: the call's whole range.  Otherwise: each bound rank's shard slice.
         self.read_spans = []          # per call: list of (flat lo, flat hi, compact offset)
@@ -407,7 +415,9 @@ class Bench:
     def step_overlapped(self, bufs, comm, wait=False):
         """Whole stage-3 step through zero_step_units_overlapped; returns (result, launches)."""
         gb = self.gather_bufs()
-        ptrs = [p for ci in range(len(self.calls)) for p in self.call_ptrs(bufs, ci)]
+        # unit-major pointers (unit u's contributions at [u * N_d]), whatever the call order
+        by_unit = sorted(range(len(self.calls)), key=lambda ci: self.calls[ci][0])
+        ptrs = [p for ci in by_unit for p in self.call_ptrs(bufs, ci)]
         res = self.Z.zero_step_units_overlapped(
             self.g.plan, ptrs, [b.data_ptr() for b in gb], self.hyper,
             self.torch.cuda.current_stream().cuda_stream, comm.cuda_stream, wait)
@@ -593,7 +603,8 @@ def gpu_arm(args, world, rank, local):
         options[Z.ZERO_OPT_GATHER_STAGING] = {"ldg": Z.ZERO_STAGING_REGISTER_LOADS,
                                              "bulk": Z.ZERO_STAGING_BULK}[args.gather_staging]
     b = Bench(w, args.mem_budget_gb, min(ROTATE_SETS, args.warmup + args.steps), args.grad_norm,
-              options, fused_gather=args.schedule == "fused" and not args.overlap)
+              options, fused_gather=args.schedule == "fused" and not args.overlap,
+              unit_order=args.unit_order)
     peak, peak_kind = peaks()
 
     for k in range(args.warmup):
@@ -745,6 +756,7 @@ def gpu_arm(args, world, rank, local):
                       "overlap": overlap, "graph": m["graph"], "per_param": w.per_param,
                       "schedule": (("overlap" if overlap else (schedule_note or args.schedule))
                                    if w.stage == 3 else None),
+                      "unit_order": args.unit_order if w.stage == 3 else None,
                       "offload": w.offload, "staging": args.staging,
                       "profile_unit": args.profile_unit,
                       "profile_units": args.profile_units if args.profile_unit is not None else None,

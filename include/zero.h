@@ -347,7 +347,7 @@ enum {
     ZERO_OPT_LAST_GATHER_IN_STEP = 11, /* read only: 1 if the last zero_step_gather_next
                                        streamed its gather inside the step launch, 0 if the
                                        gather ran as a launch of its own, -1 none yet */
-    ZERO_OPT_OFFLOAD_DEFER = 12     /* offloaded plans: 0 (default) zero_offload_step reduces its
+    ZERO_OPT_OFFLOAD_DEFER = 12,    /* offloaded plans: 0 (default) zero_offload_step reduces its
                                        contributions into host memory in stream order; 1 it only
                                        runs the non-finite flag pass, and zero_offload_finish,
                                        once every call's flag is known, streams the reductions
@@ -355,6 +355,11 @@ enum {
                                        each group as it lands.  With 1 the contributions of every
                                        call must stay unchanged until zero_offload_finish
                                        returns. */
+    ZERO_OPT_UNIT_ORDER = 13        /* stage 3, zero_step_units_overlapped: 0 (default) steps the
+                                       units first to last, each unit's gather prefetching the
+                                       next one (a forward pass's order); 1 last to first, each
+                                       prefetching the one before it (a backward pass's order,
+                                       in which the gradients arrive).  Same results. */
 };
 enum { ZERO_STAGING_REGISTER_LOADS = 0, ZERO_STAGING_BULK = 1, ZERO_STAGING_AUTO = 2 };
 zero_status_t zero_set_option(zero_plan_t* plan, int option, int64_t value);
@@ -392,13 +397,14 @@ zero_status_t zero_step_gather_next(zero_plan_t* plan, const void* const* grad_c
                                     int64_t next_unit, void* next_full16, void* stream);
 
 /* A whole stage-3 step with the all-gather overlapped ("Overlapping Computation and
- * Communication Streams"): for every unit u in order, `comm_stream` gathers u into
- * gather_bufs[u % 2] (each max_unit_pad elements) while `compute_stream` runs the fused step
- * of unit u-1; unit u's step waits only for its own gather (the point where a layer's
+ * Communication Streams"): for every unit u in order (ZERO_OPT_UNIT_ORDER: first to last,
+ * or last to first), `comm_stream` gathers u into gather_bufs[i % 2] (i = its position in that
+ * order; each buffer max_unit_pad elements) while `compute_stream` runs the fused step of the
+ * unit before it; unit u's step waits only for its own gather (the point where a layer's
  * backward would consume W_u), and a buffer is re-filled only after the step that followed
- * its gather has been enqueued past it.  comm_stream == NULL: one stream; unit 0 is gathered
- * on its own, then unit u's step and unit u+1's gather run as zero_step_gather_next (one
- * launch each where possible).  Ends with zero_step_finish on `compute_stream` (out as
+ * its gather has been enqueued past it.  comm_stream == NULL: one stream; the first unit in
+ * the order is gathered on its own, then each unit's step and the next unit's gather run as
+ * zero_step_gather_next (one launch each where possible).  Ends with zero_step_finish on `compute_stream` (out as
  * there).  unit_contribs: n_units * N_d pointers, unit-major (unit u's N_d contributions at
  * [u * N_d]).  With max_grad_norm > 0 a norm pre-pass over every unit runs first on
  * compute_stream.  Stage 3 only; two given streams must differ. */

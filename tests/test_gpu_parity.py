@@ -492,14 +492,17 @@ OVERLAP_CASES = {
 }
 
 
+@pytest.mark.parametrize("order", [0, 1])
 @pytest.mark.parametrize("name", list(OVERLAP_CASES))
-def test_overlapped_stage3_schedule_full_parity(name):
+def test_overlapped_stage3_schedule_full_parity(name, order):
     """Gathers on a second stream, double-buffered, against the oracle: states, shards and the
-    last two gathered units (left in the two buffers) must match."""
-    _run_overlap(OVERLAP_CASES[name], name)
+    last two gathered units (left in the two buffers) must match.  Units first to last, and
+    last to first (ZERO_OPT_UNIT_ORDER = 1)."""
+    _run_overlap(OVERLAP_CASES[name], name, options={Z.ZERO_OPT_UNIT_ORDER: order})
 
 
 def _run_overlap(w, name, options=None):
+    order = (options or {}).get(Z.ZERO_OPT_UNIT_ORDER, 0)
     run = H.Run(w, options=options)
     o = H.OracleFull(w, run.bound)
     comm = torch.cuda.Stream()
@@ -521,10 +524,12 @@ def _run_overlap(w, name, options=None):
             flag = o.step(k)
             assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale
             torch.cuda.synchronize()
-            for u in range(max(0, nu - 2), nu):
-                got = bufs[u % 2][:run.units[u][3]].cpu().numpy().view(np.uint16)
+            seq = list(range(nu))[::-1] if order else list(range(nu))
+            for i in range(max(0, nu - 2), nu):            # the last two positions of the order
+                u = seq[i]
+                got = bufs[i % 2][:run.units[u][3]].cpu().numpy().view(np.uint16)
                 assert np.array_equal(got, expect_g[u]), f"gathered unit {u} at step {k}"
-            _compare_full(run, o, f"overlapped {name} step {k}")
+            _compare_full(run, o, f"overlapped {name} order {order} step {k}")
     finally:
         run.close()
 
@@ -624,12 +629,9 @@ def test_per_param_config_sampled(i):
     print(f"per-parameter {w.name}: {n} sampled elements, {mism} bit mismatches")
 
 
-def test_per_param_overlapped_schedule():
-    OVERLAP_CASES["pp"] = PP_CASES["pp_nd4_units"]
-    try:
-        test_overlapped_stage3_schedule_full_parity("pp")
-    finally:
-        del OVERLAP_CASES["pp"]
+@pytest.mark.parametrize("order", [0, 1])
+def test_per_param_overlapped_schedule(order):
+    _run_overlap(PP_CASES["pp_nd4_units"], "pp", options={Z.ZERO_OPT_UNIT_ORDER: order})
 
 
 # ---------------------------------------------------------------------- ZeRO-Offload

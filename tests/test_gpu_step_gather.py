@@ -171,12 +171,14 @@ def test_step_with_next_gather_register_loads_fallback(name):
     _run_fused(CASES[name], options=LDG, expect_fused=False)
 
 
+@pytest.mark.parametrize("order", [0, 1])
 @pytest.mark.parametrize("name", ["nd16_units", "nd3_fp16_peers_skip_first", "pp_nd16_wide"])
-def test_one_stream_overlapped_schedule(name):
+def test_one_stream_overlapped_schedule(name, order):
     """zero_step_units_overlapped without a second stream: the gathers run inside the steps;
-    states, shards and the last two gathered units (left in the buffers) match the oracle."""
+    states, shards and the last two gathered units (left in the buffers) match the oracle.
+    Units first to last, and last to first (ZERO_OPT_UNIT_ORDER = 1: a backward pass's order)."""
     w = CASES[name]
-    run = H.Run(w, options=BULK, alloc_contribs=False)
+    run = H.Run(w, options={**BULK, Z.ZERO_OPT_UNIT_ORDER: order}, alloc_contribs=False)
     o = H.OracleFull(w, run.bound)
     nu = len(run.units)
     maxu = int(run.info.max_unit_pad)
@@ -194,10 +196,12 @@ def test_one_stream_overlapped_schedule(name):
             flag = o.step(k)
             assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale
             torch.cuda.synchronize()
-            for u in range(max(0, nu - 2), nu):
-                got = bufs[u % 2][:run.units[u][3]].cpu().numpy().view(np.uint16)
+            seq = list(range(nu))[::-1] if order else list(range(nu))
+            for i in range(max(0, nu - 2), nu):            # the last two positions of the order
+                u = seq[i]
+                got = bufs[i % 2][:run.units[u][3]].cpu().numpy().view(np.uint16)
                 assert np.array_equal(got, expect_g[u]), f"gathered unit {u} at step {k}"
-            H.compare_full(run, o, f"one-stream {name} step {k}")
+            H.compare_full(run, o, f"one-stream {name} order {order} step {k}")
     finally:
         run.close()
 

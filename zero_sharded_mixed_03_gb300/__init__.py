@@ -22,7 +22,8 @@ ZERO_REPORT_GRAD_NORM = 1
 (ZERO_OPT_STAGING, ZERO_OPT_WAIT_LIMIT_NS, ZERO_OPT_BULK_TILE, ZERO_OPT_BULK_STAGES,
  ZERO_OPT_LAST_STEP_KERNEL, ZERO_OPT_GATHER_STAGING, ZERO_OPT_GATHER_CHUNK,
  ZERO_OPT_GATHER_STAGES, ZERO_OPT_HOST_PIPELINE, ZERO_OPT_HOST_H2D_BYTES,
- ZERO_OPT_HOST_D2H_BYTES, ZERO_OPT_LAST_GATHER_IN_STEP, ZERO_OPT_OFFLOAD_DEFER) = range(13)
+ ZERO_OPT_HOST_D2H_BYTES, ZERO_OPT_LAST_GATHER_IN_STEP, ZERO_OPT_OFFLOAD_DEFER,
+ ZERO_OPT_UNIT_ORDER) = range(14)
 ZERO_STAGING_REGISTER_LOADS, ZERO_STAGING_BULK, ZERO_STAGING_AUTO = range(3)
 (ZERO_TABLE_TENSOR_OFFSET, ZERO_TABLE_UNITS, ZERO_TABLE_SHARD_SEGMENTS,
  ZERO_TABLE_BUCKET_SEGMENTS, ZERO_TABLE_STATE_LAYOUT, ZERO_TABLE_PARAM_CHUNKS) = range(6)

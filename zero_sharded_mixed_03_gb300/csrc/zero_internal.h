@@ -176,6 +176,7 @@ struct zero_plan {
     };
     std::vector<OffloadCall> off_deferred;
     int offload_defer = 0;
+    int unit_order = 0;                 // zero_step_units_overlapped: 0 first to last, 1 reversed
     std::vector<void*> off_events;
     void* off_flag_event = nullptr;
     void* off_side = nullptr;

@@ -1202,6 +1202,10 @@ try {
         if (value != 0 && value != 1) return fail(ZERO_EINVAL, "zero_set_option: offload defer must be 0 or 1");
         p->offload_defer = (int)value;
         return ZERO_OK;
+    case ZERO_OPT_UNIT_ORDER:
+        if (value != 0 && value != 1) return fail(ZERO_EINVAL, "zero_set_option: unit order must be 0 or 1");
+        p->unit_order = (int)value;
+        return ZERO_OK;
     case ZERO_OPT_HOST_H2D_BYTES:
     case ZERO_OPT_HOST_D2H_BYTES:
     case ZERO_OPT_LAST_GATHER_IN_STEP:
@@ -1266,6 +1270,7 @@ try {
     case ZERO_OPT_OFFLOAD_DEFER: *value = p->offload_defer; return ZERO_OK;
     case ZERO_OPT_HOST_H2D_BYTES: *value = p->host_h2d_last; return ZERO_OK;
     case ZERO_OPT_HOST_D2H_BYTES: *value = p->host_d2h_last; return ZERO_OK;
+    case ZERO_OPT_UNIT_ORDER: *value = p->unit_order; return ZERO_OK;
     case ZERO_OPT_LAST_GATHER_IN_STEP: *value = p->last_gather_in_step; return ZERO_OK;
     default: return fail(ZERO_EINVAL, "zero_get_option: unknown option");
     }
@@ -2046,6 +2051,9 @@ try {
         return fail(ZERO_EINVAL, "zero_step_units_overlapped: the two streams must differ");
     if (p->in_step) return fail(ZERO_ESTATE, "zero_step_units_overlapped: a step is open");
     const int64_t nd = p->n_d;
+    // the units in the order of the schedule: first to last, or last to first
+    std::vector<int64_t> seq((size_t)nu);
+    for (int64_t i = 0; i < nu; ++i) seq[(size_t)i] = p->unit_order ? nu - 1 - i : i;
     // every argument the calls below check, checked before the first is enqueued, so a refused
     // call leaves no step open and no unit gathered
     zero_status_t st = check_hyper(hyper, "zero_step_units_overlapped");
@@ -2055,9 +2063,9 @@ try {
         if (st != ZERO_OK) return st;
         if (p->gathered[(size_t)u]) return fail(ZERO_ESTATE, "zero_step_units_overlapped: a unit is gathered");
     }
-    for (int64_t u = 0; u < nu; ++u) {
-        const Unit& U = p->units[(size_t)u];
-        void* buf = gather_bufs[u % 2];
+    for (int64_t i = 0; i < nu; ++i) {
+        const Unit& U = p->units[(size_t)seq[(size_t)i]];
+        void* buf = gather_bufs[i % 2];
         if (U.numel_pad > 0 && !buf) return fail(ZERO_EINVAL, "zero_step_units_overlapped: NULL gather buffer");
         if (!aligned(buf, 2))
             return fail(ZERO_EALIGN, "zero_step_units_overlapped: gather buffer not 2-byte aligned");
@@ -2068,22 +2076,23 @@ try {
     st = set_device(p);
     if (st != ZERO_OK) return st;
     if (!comm_stream) {
-        // one stream: unit u+1's all-gather streams inside unit u's step launch
+        // one stream: the next unit's all-gather streams inside each unit's step launch
         if (hyper->max_grad_norm > 0.0)
             for (int64_t u = 0; u < nu; ++u) {
                 st = zero_grad_norm(p, unit_contribs + u * nd, nd, u, compute_stream);
                 if (st != ZERO_OK) return st;
             }
         if (nu > 0) {
-            st = zero_gather_layer(p, 0, gather_bufs[0], compute_stream);
+            st = zero_gather_layer(p, seq[0], gather_bufs[0], compute_stream);
             if (st != ZERO_OK) return st;
         }
-        for (int64_t u = 0; u < nu; ++u) {
-            // (a layer's forward/backward would consume gather_bufs[u % 2] here)
+        for (int64_t i = 0; i < nu; ++i) {
+            const int64_t u = seq[(size_t)i];
+            // (a layer's forward/backward would consume gather_bufs[i % 2] here)
             st = zero_release_layer(p, u);
             if (st != ZERO_OK) return st;
-            st = u + 1 < nu ? zero_step_gather_next(p, unit_contribs + u * nd, nd, u, hyper, u + 1,
-                                                    gather_bufs[(u + 1) % 2], compute_stream)
+            st = i + 1 < nu ? zero_step_gather_next(p, unit_contribs + u * nd, nd, u, hyper, seq[(size_t)i + 1],
+                                                    gather_bufs[(i + 1) % 2], compute_stream)
                             : zero_step(p, unit_contribs + u * nd, nd, u, hyper, compute_stream);
             if (st != ZERO_OK) return st;
         }
@@ -2110,9 +2119,10 @@ try {
     cudaError_t e = cudaEventRecord(start, cs);           // the previous step's shards are final
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ms, start, 0);
     if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: ordering the streams");
-    for (int64_t u = 0; u < nu; ++u) {
-        const int b = (int)(u % 2);
-        if (u >= 2) {
+    for (int64_t i = 0; i < nu; ++i) {
+        const int64_t u = seq[(size_t)i];
+        const int b = (int)(i % 2);
+        if (i >= 2) {
             e = cudaStreamWaitEvent(ms, released[b], 0);
             if (e != cudaSuccess) return cuda_fail(e, "zero_step_units_overlapped: wait release");
         }
