@@ -207,6 +207,7 @@ def test_execution_options_are_checked_on_the_host():
         assert Z.zero_get_option(plan, Z.ZERO_OPT_LAST_STEP_KERNEL) == -1
         assert Z.zero_get_option(plan, Z.ZERO_OPT_HOST_PIPELINE) == 1
         assert Z.zero_get_option(plan, Z.ZERO_OPT_OFFLOAD_DEFER) == 0
+        assert Z.zero_get_option(plan, Z.ZERO_OPT_UNIT_ORDER) == 0
         assert Z.zero_get_option(plan, Z.ZERO_OPT_LAST_GATHER_IN_STEP) == -1
         assert Z.zero_get_option(plan, Z.ZERO_OPT_HOST_H2D_BYTES) == 0
         assert Z.zero_get_option(plan, Z.ZERO_OPT_HOST_D2H_BYTES) == 0
@@ -219,13 +220,15 @@ def test_execution_options_are_checked_on_the_host():
                          (Z.ZERO_OPT_BULK_STAGES, 1), (Z.ZERO_OPT_BULK_STAGES, 17), (99, 0),
                          (Z.ZERO_OPT_HOST_PIPELINE, 2), (Z.ZERO_OPT_HOST_H2D_BYTES, 0),
                          (Z.ZERO_OPT_HOST_D2H_BYTES, 0), (Z.ZERO_OPT_LAST_STEP_KERNEL, 0),
-                         (Z.ZERO_OPT_LAST_GATHER_IN_STEP, 1), (Z.ZERO_OPT_OFFLOAD_DEFER, 2)):
+                         (Z.ZERO_OPT_LAST_GATHER_IN_STEP, 1), (Z.ZERO_OPT_OFFLOAD_DEFER, 2),
+                         (Z.ZERO_OPT_UNIT_ORDER, 2), (Z.ZERO_OPT_UNIT_ORDER, -1)):
             with pytest.raises(Z.ZeroError) as e:
                 Z.zero_set_option(plan, opt, val)
             assert e.value.status == Z.ZERO_EINVAL, (opt, val)
         for opt, val in ((Z.ZERO_OPT_STAGING, 1), (Z.ZERO_OPT_STAGING, 2), (Z.ZERO_OPT_STAGING, 0),
                          (Z.ZERO_OPT_HOST_PIPELINE, 0), (Z.ZERO_OPT_HOST_PIPELINE, 1),
                          (Z.ZERO_OPT_OFFLOAD_DEFER, 1), (Z.ZERO_OPT_OFFLOAD_DEFER, 0),
+                         (Z.ZERO_OPT_UNIT_ORDER, 1), (Z.ZERO_OPT_UNIT_ORDER, 0),
                          (Z.ZERO_OPT_WAIT_LIMIT_NS, 0), (Z.ZERO_OPT_BULK_TILE, 4096),
                          (Z.ZERO_OPT_BULK_TILE, 1024), (Z.ZERO_OPT_BULK_STAGES, 8)):
             Z.zero_set_option(plan, opt, val)
