@@ -210,6 +210,15 @@ def test_host_path_per_parameter_plan():
     _run_host(w, 1)
 
 
+def test_host_path_per_parameter_one_unit_split_into_pieces():
+    """A per-parameter plan of one unit (two 4096-row tensors, 33.6M elements, 4 ranks): the
+    step's only call is cut into pieces whose cuts fall inside the ranks' row chunks."""
+    w = W.Workload(wid=418, name="host_pp_pieces", sizes=(4096 * 4096, 4096 * 4100), n_d=4,
+                   stage=3, bucket_elems=0, unit_first=(0,), dtype=W.BF16, steps=2,
+                   hyper=W.Hyper(), scaler=None, dim0=(4096, 4096), per_param=True)
+    _run_host(w, 1)
+
+
 CLIP_CASES = {
     # clipped steps fed from host memory: the norm pre-pass of every call, then the steps
     "z2_nd8_fp16_buckets_clip_skip": _mk(415, _ragged(16, 40, 9000), 8, 2, steps=4, bucket=10_000,
