@@ -75,6 +75,9 @@ def lib():
         L.orc_pp_step.restype = ctypes.c_int
         L.orc_pp_step.argtypes = [vp, vp, i64, vp, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp,
                                   vp, vp, vp, vp]
+        L.orc_pp_step_ex.restype = ctypes.c_int
+        L.orc_pp_step_ex.argtypes = [vp, vp, i64, vp, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                     vp, vp, vp, vp, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
         L.orc_pp_gather.restype = ctypes.c_int
         L.orc_pp_gather.argtypes = [vp, vp, i64, vp, i64, ctypes.c_int, i64, vp, vp]
         L.orc_scaler_update.restype = i64
@@ -212,6 +215,16 @@ class PerParam:
         return lib().orc_pp_step(_p(self.sizes), _p(self.dim0), self.sizes.size, _p(self.unit_first),
                                  self.n_units_arg, self.n_d, is_fp16, _ptrs(contribs), _p(bound),
                                  _ptrs(p), _ptrs(m), _ptrs(v), _ptrs(shard16), _p(k9))
+
+    def step_ex(self, is_fp16, contribs, bound, p, m, v, shard16, k9, max_norm: float):
+        """step with the global gradient norm (R8): returns (flag, norm^2); max_norm > 0 clips."""
+        bound = np.ascontiguousarray(np.asarray(bound, dtype=np.int32))
+        norm2 = ctypes.c_double(0.0)
+        flag = lib().orc_pp_step_ex(_p(self.sizes), _p(self.dim0), self.sizes.size, _p(self.unit_first),
+                                    self.n_units_arg, self.n_d, is_fp16, _ptrs(contribs), _p(bound),
+                                    _ptrs(p), _ptrs(m), _ptrs(v), _ptrs(shard16), _p(k9),
+                                    float(max_norm), ctypes.byref(norm2))
+        return flag, norm2.value
 
     def gather(self, unit: int, shard16) -> np.ndarray:
         out = np.zeros(self.unit_numel[unit], dtype=np.uint16)

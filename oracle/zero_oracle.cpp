@@ -604,10 +604,15 @@ int64_t orc_pp_chunks(const int64_t* sizes, const int64_t* dim0, int64_t n_tenso
 // Whole per-parameter-sharded step.  contrib[r]: rank r's gradient over every unit's buffer
 // (units concatenated, unpadded); p/m/v/shard16[r]: rank r's local shards (padded layout).
 // Returns the global non-finite flag.
-int orc_pp_step(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
-                const int64_t* unit_first, int64_t n_units, int n_d, int is_fp16,
-                const uint16_t* const* contrib, const int32_t* bound, float* const* p,
-                float* const* m, float* const* v, uint16_t* const* shard16, const float* k9)
+// The per-parameter step with the optional global gradient norm and clipping (R8, as in
+// orc_sharded_step_ex): norm^2 sums fp32(g*g) in double over the bound ranks' chunks in chunk
+// order; max_norm > 0 multiplies each g by clip_coef before AdamW; *norm2_out (if not NULL)
+// receives norm^2.
+int orc_pp_step_ex(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
+                   const int64_t* unit_first, int64_t n_units, int n_d, int is_fp16,
+                   const uint16_t* const* contrib, const int32_t* bound, float* const* p,
+                   float* const* m, float* const* v, uint16_t* const* shard16, const float* k9,
+                   double max_norm, double* norm2_out)
 {
     std::vector<PChunk> ch;
     std::vector<int64_t> ub;
@@ -618,6 +623,7 @@ int orc_pp_step(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
     for (int r = 0; r < n_d; ++r)
         if (bound[r]) g[(size_t)r].assign((size_t)per_rank, 0.0f);
     int flag = 0;
+    double norm2 = 0.0;
     for (const PChunk& c : ch) {
         if (!bound[c.rank]) continue;
         for (int64_t i = 0; i < c.rows * c.cols; ++i) {
@@ -625,18 +631,31 @@ int orc_pp_step(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
                                         k.inv);
             g[(size_t)c.rank][(size_t)(c.state_off + i)] = gi;
             flag |= nonfinite(gi);
+            norm2 += (double)(gi * gi);
         }
     }
+    if (norm2_out) *norm2_out = norm2;
+    const float coef = max_norm > 0.0 ? clip_coef(norm2, max_norm) : 1.0f;
     for (const PChunk& c : ch) {
         if (!bound[c.rank]) continue;
         const int r = (int)c.rank;
         for (int64_t i = 0; i < c.rows * c.cols; ++i) {
             const size_t j = (size_t)(c.state_off + i);
-            if (!flag) adamw_one(g[(size_t)r][j], p[r][j], m[r][j], v[r][j], k);
+            const float gj = max_norm > 0.0 ? g[(size_t)r][j] * coef : g[(size_t)r][j];
+            if (!flag) adamw_one(gj, p[r][j], m[r][j], v[r][j], k);
             shard16[r][j] = round16(p[r][j], is_fp16);
         }
     }
     return flag;
+}
+
+int orc_pp_step(const int64_t* sizes, const int64_t* dim0, int64_t n_tensors,
+                const int64_t* unit_first, int64_t n_units, int n_d, int is_fp16,
+                const uint16_t* const* contrib, const int32_t* bound, float* const* p,
+                float* const* m, float* const* v, uint16_t* const* shard16, const float* k9)
+{
+    return orc_pp_step_ex(sizes, dim0, n_tensors, unit_first, n_units, n_d, is_fp16, contrib, bound, p, m,
+                          v, shard16, k9, 0.0, nullptr);
 }
 
 // All-gather of unit `unit` into its unpadded buffer: every rank's owned rows of every tensor.

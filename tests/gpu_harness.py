@@ -72,7 +72,6 @@ class OracleFull:
         self.p, self.m, self.v, self.sh16 = [], [], [], []
         self.sc = oracle.ScalerState(w.scaler)
         if w.per_param:
-            assert w.hyper.max_grad_norm == 0
             self.pp = oracle.PerParam(w.sizes, w.dim0, w.n_d, w.unit_first or None)
             self.total = int(self.pp.unit_base[-1])
             self.params16 = fill_host(synth.param_stream(w), self.units, 0, self.total)
@@ -107,8 +106,8 @@ class OracleFull:
         if w.per_param:
             c = [fill_host(synth.grad_stream(w, k, r), self.units, 0, self.total) for r in range(w.n_d)]
             k9 = oracle.consts(w.hyper, self.sc.t + 1, self.sc.scale, w.n_d)
-            flag = self.pp.step(w.dtype, c, self.bound, self.p, self.m, self.v, self.sh16, k9)
-            self.norm2 = float("nan")
+            flag, self.norm2 = self.pp.step_ex(w.dtype, c, self.bound, self.p, self.m, self.v, self.sh16,
+                                               k9, w.hyper.max_grad_norm)
             self.sc.update(flag)
             return flag
         n = self.L.total_pad

@@ -673,6 +673,72 @@ def test_per_param_chunks_brute_force():
         assert all(state[r] == pp.per_rank for r in range(n_d))
 
 
+def test_per_param_clipping_equals_the_flat_clipped_step():
+    """R8 on per-parameter plans: the global norm and the clipping of the flat step (whose
+    clipping is pinned to torch.nn.utils.clip_grad_norm_ above), over the same gradients.
+    With every rank bound, norm^2 equals the flat step's up to the order of its double sum
+    (1e-12 relative), and the owned rows of every rank's update, placed back, equal the flat
+    step's update bit for bit whenever the two fp32 coefficients agree."""
+    rng = np.random.default_rng(43)
+    hyper = W.Hyper()
+    clipped = 0
+    for trial in range(120):
+        sizes, dim0, units = _random_pp_case(rng)
+        n = int(sum(sizes))
+        if n == 0:
+            continue
+        n_d = int(rng.integers(1, 7))
+        is_fp16 = int(rng.integers(0, 2))
+        max_norm = float(rng.choice([1e-4, 1e-2, 1e3]))
+        pp = oracle.PerParam(sizes, dim0, n_d, units)
+        params16 = _rand16(rng, n, is_fp16, 0.02)
+        contribs = [_rand16(rng, n, is_fp16) for _ in range(n_d)]
+        k9 = oracle.consts(hyper, int(rng.integers(1, 5)), 1.0, n_d)
+        p, m, v, sh = [], [], [], []
+        for r in range(n_d):
+            P = np.zeros(max(1, pp.per_rank), np.float32)
+            S16 = np.zeros(max(1, pp.per_rank), np.uint16)
+            for (rr, u, t, row0, rows, cols, c_rows, coff, soff) in pp.chunks:
+                if rr == r and rows:
+                    g0 = pp.unit_base[u] + coff
+                    S16[soff:soff + rows * cols] = params16[g0:g0 + rows * cols]
+                    P[soff:soff + rows * cols] = oracle.widen16(params16[g0:g0 + rows * cols], is_fp16)
+            p.append(P)
+            m.append(np.zeros_like(P))
+            v.append(np.zeros_like(P))
+            sh.append(S16)
+        flag, n2pp = pp.step_ex(is_fp16, contribs, [1] * n_d, p, m, v, sh, k9, max_norm)
+        assert flag == 0
+        # the flat stage-1 step over the same tensors (padded to a multiple of N_d with zeros)
+        L = oracle.Layout(sizes, n_d)
+        pad = L.total_pad - n
+        cf = [np.concatenate([c, np.zeros(pad, np.uint16)]) for c in contribs]
+        pf16 = np.concatenate([params16, np.zeros(pad, np.uint16)])
+        fp, fm, fv, fsh, full = [], [], [], [], pf16.copy()
+        for r in range(n_d):
+            U = L.units[0]
+            seg = pf16[U[5] + r * U[4]:U[5] + (r + 1) * U[4]]
+            fp.append(oracle.widen16(seg, is_fp16).astype(np.float32))
+            fm.append(np.zeros(seg.size, np.float32))
+            fv.append(np.zeros(seg.size, np.float32))
+        f_flag, n2flat = oracle.sharded_step_ex(L, 1, 0, is_fp16, cf, [1] * n_d, fp, fm, fv, None, full,
+                                                k9, max_norm)
+        assert f_flag == 0
+        assert abs(n2pp - n2flat) <= 1e-12 * n2flat, (trial, n2pp, n2flat)
+        same_coef = oracle.clip_coef(n2pp, max_norm) == oracle.clip_coef(n2flat, max_norm)
+        clipped += oracle.clip_coef(n2pp, max_norm) < 1.0
+        Pf, Mf, Vf = _union(L, fp), _union(L, fm), _union(L, fv)
+        for (r, u, t, row0, rows, cols, c_rows, coff, soff) in pp.chunks:
+            g0 = pp.unit_base[u] + coff
+            for mine, ref in ((p[r], Pf), (m[r], Mf), (v[r], Vf)):
+                a, b = mine[soff:soff + rows * cols], ref[g0:g0 + rows * cols]
+                if same_coef:
+                    assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), trial
+                else:
+                    assert np.all(np.abs(a - b) <= 1e-6 * np.abs(b) + 1e-8), trial
+    assert clipped >= 30, clipped
+
+
 def test_per_param_union_equals_ddp():
     """[ZF] 'Mathematical Formulation of ZeRO Partitioning Stages': per-parameter sharding also
     keeps data-parallel semantics -- the owned rows of every rank's update, placed back, equal
