@@ -228,6 +228,11 @@ CLIP_CASES = {
                               hyper=W.Hyper(max_grad_norm=0.02)),
     "z1_nd4_two_pieces_clip": _mk(417, [17_000_001, 16_777_259], 4, 1, steps=2,
                                   hyper=W.Hyper(max_grad_norm=0.05)),
+    # a per-parameter plan (dim-0 row chunks), two ranks bound
+    "pp_nd4_clip": W.Workload(wid=419, name="host_pp_clip", sizes=(12 * 7, 5 * 3, 40 * 9, 2 * 11, 64),
+                              n_d=4, stage=3, bucket_elems=0, unit_first=(0, 2, 4), dtype=W.BF16,
+                              steps=3, hyper=W.Hyper(max_grad_norm=1e-3), scaler=None,
+                              dim0=(12, 5, 40, 2, 8), per_param=True, bound_ranks=(0, 3)),
 }
 
 

@@ -622,6 +622,33 @@ def test_per_param_full_parity(name):
     _run_full(PP_CASES[name])
 
 
+@pytest.mark.parametrize("offload", [False, True])
+@pytest.mark.parametrize("name", ["pp_nd4_units", "pp_nd8_fp16_peers_skip"])
+def test_per_param_clipping_full_parity(name, offload):
+    """FSDP-2 per-parameter plans with clipping: the norm pre-pass over every unit's row chunks,
+    then the clipped updates, on the GPU and offloaded to host threads; states, shards, skips
+    and the reported norm against the oracle."""
+    w = dataclasses.replace(PP_CASES[name], wid=PP_CASES[name].wid + 60, hyper=_hyper(1e-3),
+                            offload=offload)
+    run = H.Run(w)
+    o = H.OracleFull(w, run.bound)
+    try:
+        for k in range(1, w.steps + 1):
+            res = run.step(k)
+            flag = o.step(k)
+            assert res.skipped == flag and res.t == o.sc.t and res.scale == o.sc.scale, k
+            want = np.sqrt(o.norm2)
+            if np.isfinite(want):
+                assert abs(res.grad_norm - want) <= 1e-12 * want, (res.grad_norm, want)
+            else:
+                assert not np.isfinite(res.grad_norm)
+            mism = _compare_full(run, o, f"per-parameter clip {name} step {k}")
+            if offload:
+                assert mism == 0
+    finally:
+        run.close()
+
+
 @pytest.mark.parametrize("i", [3, 4])
 def test_per_param_config_sampled(i):
     w = W.per_param_variant(W.workload(i))
