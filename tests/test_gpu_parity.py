@@ -622,13 +622,16 @@ def test_per_param_full_parity(name):
     _run_full(PP_CASES[name])
 
 
-@pytest.mark.parametrize("offload", [False, True])
+@pytest.mark.parametrize("mode", ["clip", "clip_offload", "report"])
 @pytest.mark.parametrize("name", ["pp_nd4_units", "pp_nd8_fp16_peers_skip"])
-def test_per_param_clipping_full_parity(name, offload):
-    """FSDP-2 per-parameter plans with clipping: the norm pre-pass over every unit's row chunks,
-    then the clipped updates, on the GPU and offloaded to host threads; states, shards, skips
-    and the reported norm against the oracle."""
-    w = dataclasses.replace(PP_CASES[name], wid=PP_CASES[name].wid + 60, hyper=_hyper(1e-3),
+def test_per_param_clipping_full_parity(name, mode):
+    """FSDP-2 per-parameter plans with the global gradient norm: the norm pre-pass over every
+    unit's row chunks, then the clipped updates, on the GPU and offloaded to host threads; or
+    the norm reported from the fused pass.  States, shards, skips and the norm against the
+    oracle."""
+    offload = mode == "clip_offload"
+    hyper = _hyper(0.0, True) if mode == "report" else _hyper(1e-3)
+    w = dataclasses.replace(PP_CASES[name], wid=PP_CASES[name].wid + 60, hyper=hyper,
                             offload=offload)
     run = H.Run(w)
     o = H.OracleFull(w, run.bound)
