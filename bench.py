@@ -850,6 +850,7 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
         return el, applied
 
     one_step()                                            # warm-up (creates the copy streams)
+    link_peak = h2d_copy_gbs()
     enqueue_s[0] = 0.0
     el, applied = timed(steps)
     enqueue_ms = 1e3 * enqueue_s[0] / steps
@@ -869,6 +870,9 @@ def e2e_leg(b: Bench, steps: int, world: int, dist, device_ms_per_step: float):
             "steps": steps,
             "api": ("zero_grad_norm_host / " if b.clip else "") + "zero_step_host / zero_step_host_finish",
             "host_link_gbs": round((h2d + d2h) / (ms / 1e3) / 1e9, 1),
+            # host->device bytes per second against one plain pinned 1 GB copy in this run
+            "h2d_gbs": round(h2d / (ms / 1e3) / 1e9, 1), "h2d_copy_peak_gbs": round(link_peak, 1),
+            "h2d_frac": round(h2d / (ms / 1e3) / 1e9 / link_peak, 4),
             "host_enqueue_ms_per_step": round(enqueue_ms, 3),
             "overlap": {"pipelined_ms_per_step": round(ms, 3),
                         "serial_ms_per_step": round(ms_serial, 3),
@@ -908,6 +912,25 @@ def oracle_sample_run(w, sample_elems: int, steps: int, warmup: int = 0):
         if k > warmup:
             times.append(time.perf_counter() - t)
     return n, times
+
+
+def h2d_copy_gbs(n_bytes: int = 1 << 30, reps: int = 3) -> float:
+    """Host->device copy rate (best of `reps`) of one pinned 1 GB buffer by the copy engine:
+    the peak the end-to-end leg's host->device bytes are compared with."""
+    import torch
+    src = torch.ones(n_bytes // 2, dtype=torch.int16, pin_memory=True)
+    dst = torch.empty(n_bytes // 2, dtype=torch.int16, device="cuda")
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(reps + 1):                 # the first copy warms the path
+        torch.cuda.synchronize()
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del src, dst
+    return n_bytes / (best / 1e3) / 1e9
 
 
 def host_copy_gbs(threads: int, n_bytes: int = 1 << 30, reps: int = 3) -> float:
